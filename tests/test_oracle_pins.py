@@ -1,0 +1,444 @@
+"""Pins for the CPU oracle: every oracle function is checked against something
+other than itself -- closed forms, invariants the pages state, library
+routines (numpy / torch / scipy) on tiny inputs, and an independently written
+vector form of the Sinkhorn-Knopp iteration.  A plausible slip anywhere in the
+oracle (a dropped term, a wrong sign or index, a transposed operand, an extra
+or missing round, a misplaced eps) fails at least one test here.
+
+No GPU: these run with -m "not gpu".
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from hyper_connection_residual_mixes_gb300 import inputs
+
+RNG = np.random.default_rng(12345)
+
+
+# ---------------------------------------------------------------- bf16 cast
+def _torch_bf16_bits_from_f32(v32):
+    t = torch.from_numpy(np.asarray(v32, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def test_bf16_round_matches_torch_on_fp32_values():
+    # fp32-representable doubles: torch's fp32 -> bf16 (round to nearest even)
+    # is a library reference with no double rounding on these inputs.
+    v = np.concatenate([
+        RNG.standard_normal(20000).astype(np.float32),
+        (RNG.standard_normal(5000) * 1e-3).astype(np.float32),
+        (RNG.standard_normal(5000) * 1e30).astype(np.float32),
+        (RNG.standard_normal(2000) * 1e-39).astype(np.float32),   # fp32 subnormals
+        np.array([3.38e38, -3.38e38, 3.3961e38, 1.1754944e-38, 0.0, -0.0], np.float32),
+    ])
+    got = oracle.bf16_from_f64(v.astype(np.float64))
+    want = _torch_bf16_bits_from_f32(v)
+    assert np.array_equal(got, want)
+
+
+def test_bf16_round_ties_to_even_and_specials():
+    one = 1.0
+    cases = {
+        one: 0x3F80,
+        one + 2.0 ** -8: 0x3F80,             # tie -> even (1.0)
+        one + 3 * 2.0 ** -8: 0x3F82,         # tie -> even (1 + 2^-6)
+        one + 2.0 ** -8 + 2.0 ** -40: 0x3F81,  # just above the tie (not fp32-representable)
+        one + 2.0 ** -8 - 2.0 ** -40: 0x3F80,  # just below the tie
+        -2.5: 0xC020,
+        float("inf"): 0x7F80,
+        -float("inf"): 0xFF80,
+        1e39: 0x7F80,                         # overflows bf16
+        2.0 ** -133: 0x0001,                  # smallest bf16 subnormal
+        2.0 ** -134: 0x0000,                  # tie between 0 and the smallest subnormal -> 0 (even)
+        3 * 2.0 ** -134: 0x0002,              # tie between 1 and 2 subnormal units -> 2 (even)
+        -0.0: 0x8000,
+    }
+    for v, bits in cases.items():
+        assert int(oracle.bf16_from_f64(np.array([v]))[0]) == bits, (v, hex(bits))
+    assert (int(oracle.bf16_from_f64(np.array([float("nan")]))[0]) & 0x7FFF) > 0x7F80
+
+
+def test_bf16_to_f64_is_exact():
+    bits = RNG.integers(0, 1 << 16, size=50000, dtype=np.uint16)
+    bits = bits[(bits & 0x7F80) != 0x7F80]  # finite values only
+    got = oracle.bf16_to_f64(bits)
+    want = torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(got, want)
+
+
+# ------------------------------------------------------------- a1: mixes
+def _rand_x(n, hc, d, scale=1.0):
+    return inputs.bf16_bits_np((torch.from_numpy(RNG.standard_normal((n, hc, d))) * scale)
+                               .to(torch.bfloat16))
+
+
+def test_mixes_matches_numpy_gemv_tiny():
+    n, hc, d = 5, 4, 24
+    x = _rand_x(n, hc, d)
+    w = (RNG.standard_normal(((2 + hc) * hc, hc * d)) * 0.1).astype(np.float32)
+    got = oracle.mixes(x, w, norm_eps=1e-20)
+    xf = oracle.bf16_to_f64(x).reshape(n, hc * d)
+    r = 1.0 / np.sqrt(np.mean(xf * xf, axis=1, keepdims=True) + 1e-20)
+    want = (xf @ w.astype(np.float64).T) * r
+    np.testing.assert_allclose(got, want, rtol=1e-13, atol=1e-15)
+
+
+@pytest.mark.parametrize("hc", [1, 2, 3, 4])
+def test_mixes_generic_hc_matches_numpy(hc):
+    n, d = 3, 16
+    x = _rand_x(n, hc, d)
+    w = (RNG.standard_normal(((2 + hc) * hc, hc * d)) * 0.1).astype(np.float32)
+    got = oracle.mixes(x, w, norm_eps=1e-6)
+    xf = oracle.bf16_to_f64(x).reshape(n, hc * d)
+    want = (xf @ w.astype(np.float64).T) / np.sqrt(np.mean(xf * xf, axis=1, keepdims=True) + 1e-6)
+    np.testing.assert_allclose(got, want, rtol=1e-13, atol=1e-15)
+
+
+def test_mixes_power_of_two_scale_invariance_bitwise():
+    n, hc, d = 4, 4, 64
+    x = _rand_x(n, hc, d)
+    w = (RNG.standard_normal((24, hc * d)) * 0.01).astype(np.float32)
+    base = oracle.mixes(x, w)
+    for k in (-3, 1, 5):
+        xs = oracle.bf16_from_f64(oracle.bf16_to_f64(x) * 2.0 ** k).reshape(x.shape)
+        assert np.array_equal(oracle.mixes(xs, w), base)
+
+
+def test_mixes_zero_input_is_exactly_zero():
+    x = np.zeros((3, 4, 32), np.uint16)
+    w = (RNG.standard_normal((24, 128))).astype(np.float32)
+    assert np.array_equal(oracle.mixes(x, w, 1e-20), np.zeros((3, 24)))
+
+
+def test_mixes_statistic_uses_all_streams():
+    # one statistic per token over all hc*d values: a stream of zeros still
+    # counts in the mean (a per-stream norm would give a different value).
+    hc, d = 4, 8
+    x = np.zeros((1, hc, d), np.uint16)
+    x[0, 0, :] = 0x3F80  # stream 0 all ones, others zero
+    w = np.zeros((24, hc * d), np.float32)
+    w[0, 0] = 1.0
+    m = oracle.mixes(x, w, norm_eps=0.0)
+    # mean(x^2) over 32 values = 8/32 = 1/4 -> r = 2; m0 = 1 * r
+    assert m[0, 0] == 2.0
+
+
+# --------------------------------------------- a2 + a3: split + Sinkhorn
+def _vector_form_sinkhorn(logits, iters, eps):
+    """Independent restatement: the row softmax + eps gives K0; every later
+    step only rescales rows (u) or columns (v), so P = diag(u) K0 diag(v).
+    Rows use sums of P along axis 1, columns along axis 0, each divided by
+    (sum + eps).  Written as matrix-vector products on the fixed K0."""
+    z = logits - logits.max(axis=1, keepdims=True)
+    e = np.exp(z)
+    K0 = e / e.sum(axis=1, keepdims=True) + eps
+    hc = K0.shape[0]
+    u = np.ones(hc)
+    v = np.ones(hc)
+    steps = ["col"] + ["row", "col"] * (iters - 1)
+    for s in steps:
+        if s == "row":
+            rs = u * (K0 @ v)
+            u = u / (rs + eps)
+        else:
+            cs = v * (K0.T @ u)
+            v = v / (cs + eps)
+    return u[:, None] * K0 * v[None, :]
+
+
+@pytest.mark.parametrize("hc", [2, 3, 4])
+@pytest.mark.parametrize("iters", [1, 2, 3, 20, 57])
+@pytest.mark.parametrize("eps", [1e-6, 0.0, 0.05])
+def test_sinkhorn_matches_vector_form(hc, iters, eps):
+    mix = (2 + hc) * hc
+    n = 6
+    m = RNG.standard_normal((n, mix)) * 3.0
+    scale = np.array([0.7, 1.3, 1.9], np.float32)
+    base = RNG.standard_normal(mix).astype(np.float32)
+    pre, post, comb = oracle.split_sinkhorn(m, scale, base, hc=hc, iters=iters, eps=eps)
+    for t in range(n):
+        logits = (m[t, 2 * hc:] * float(scale[2]) + base[2 * hc:].astype(np.float64)).reshape(hc, hc)
+        want = _vector_form_sinkhorn(logits, iters, eps)
+        np.testing.assert_allclose(comb[t], want, rtol=1e-12, atol=1e-15)
+
+
+def test_split_pre_post_closed_forms():
+    from scipy.special import expit  # library logistic function
+    hc, n = 4, 50
+    m = RNG.standard_normal((n, 24)) * 3.0
+    scale = np.array([0.6, 1.7, 1.1], np.float32)
+    base = RNG.standard_normal(24).astype(np.float32)
+    pre, post, _ = oracle.split_sinkhorn(m, scale, base, hc=hc, iters=20, eps=1e-6)
+    sc = scale.astype(np.float64)
+    b = base.astype(np.float64)
+    np.testing.assert_allclose(pre, expit(m[:, :4] * sc[0] + b[:4]) + 1e-6, rtol=1e-14, atol=1e-16)
+    np.testing.assert_allclose(post, 2.0 * expit(m[:, 4:8] * sc[1] + b[4:8]), rtol=1e-14, atol=1e-16)
+
+
+def test_split_reads_comb_row_major_from_offset_2hc():
+    # comb[j][k] = m[2hc + j*hc + k]: put a single large logit at one index.
+    # iters=1, eps=0: after the softmax row j is (almost exactly) the unit
+    # vector e_k and the other rows are uniform 1/4, so column k sums to 7/4
+    # and the entry becomes 4/7; the other columns sum to 3/4 and their
+    # uniform-row entries become 1/3.
+    hc = 4
+    for j, k in [(0, 3), (2, 1), (3, 0)]:
+        m = np.zeros((1, 24))
+        m[0, 2 * hc + j * hc + k] = 50.0
+        _, _, comb = oracle.split_sinkhorn(m, np.ones(3, np.float32), np.zeros(24, np.float32),
+                                           hc=hc, iters=1, eps=0.0)
+        assert abs(comb[0, j, k] - 4.0 / 7.0) < 1e-12
+        other_row = (j + 1) % hc
+        assert abs(comb[0, other_row, k] - 1.0 / 7.0) < 1e-12
+        assert abs(comb[0, other_row, (k + 1) % hc] - 1.0 / 3.0) < 1e-12
+        assert comb[0, j, (k + 1) % hc] < 1e-20
+
+
+def test_sinkhorn_uniform_logits_scalar_recursion():
+    # all 16 logits equal: the softmax gives 1/4, + eps; every later
+    # normalisation maps a constant matrix c to c / (4c + eps).
+    eps = 1e-6
+    for iters in (1, 2, 20):
+        m = np.zeros((1, 24))
+        _, _, comb = oracle.split_sinkhorn(m, np.ones(3, np.float32), np.zeros(24, np.float32),
+                                           hc=4, iters=iters, eps=eps)
+        c = 0.25 + eps
+        for _ in range(1 + 2 * (iters - 1)):
+            c = c / (4.0 * c + eps)
+        assert np.all(comb[0] == comb[0, 0, 0])
+        assert abs(comb[0, 0, 0] - c) < 1e-15
+    # the fixed point of c -> c / (4c + eps) is (1 - eps) / 4
+    assert abs(comb[0, 0, 0] - (1 - eps) / 4) < 1e-15
+
+
+def test_sinkhorn_2x2_limit_closed_form():
+    # eps = 0: scaling preserves the cross ratio P00 P11 / (P01 P10) = exp(delta),
+    # delta = c00 + c11 - c01 - c10; the doubly stochastic 2x2 limit is
+    # [[p, 1-p], [1-p, p]] with p / (1 - p) = exp(delta / 2).
+    hc = 2
+    for _ in range(10):
+        m = RNG.standard_normal((1, 8)) * 2.0
+        _, _, comb = oracle.split_sinkhorn(m, np.ones(3, np.float32), np.zeros(8, np.float32),
+                                           hc=hc, iters=400, eps=0.0)
+        c = m[0, 4:].reshape(2, 2)
+        delta = c[0, 0] + c[1, 1] - c[0, 1] - c[1, 0]
+        p = 1.0 / (1.0 + math.exp(-delta / 2.0))
+        np.testing.assert_allclose(comb[0], [[p, 1 - p], [1 - p, p]], rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("iters", [1, 2, 7, 20])
+def test_sinkhorn_cross_ratios_preserved_eps0(iters):
+    # with eps = 0 every step is a diagonal scaling, so every cross ratio
+    # P[i,j] P[k,l] / (P[i,l] P[k,j]) equals exp(c[i,j] + c[k,l] - c[i,l] - c[k,j]).
+    m = RNG.standard_normal((1, 24)) * 2.0
+    _, _, comb = oracle.split_sinkhorn(m, np.ones(3, np.float32), np.zeros(24, np.float32),
+                                       hc=4, iters=iters, eps=0.0)
+    P = comb[0]
+    c = m[0, 8:].reshape(4, 4)
+    for (i, k) in [(0, 1), (1, 3), (2, 0)]:
+        for (j, l) in [(0, 2), (3, 1)]:
+            got = P[i, j] * P[k, l] / (P[i, l] * P[k, j])
+            want = math.exp(c[i, j] + c[k, l] - c[i, l] - c[k, j])
+            assert abs(got / want - 1) < 1e-11
+
+
+def test_page_invariants_on_tiny_like_data(golden_constants):
+    # columns sum to 1 within 1e-5 after the final column step; all entries
+    # positive; pre > eps; 0 < post < 2 (strict, fp64 oracle).
+    case = inputs.tiny(seed=0, n=16, d=256)
+    p = case.params[0]
+    m = oracle.mixes(inputs.bf16_bits_np(case.x), p.hc_fn.numpy())
+    eps = golden_constants["hc_eps"]
+    pre, post, comb = oracle.split_sinkhorn(m, p.hc_scale.numpy(), p.hc_base.numpy(),
+                                            hc=golden_constants["hc_mult"],
+                                            iters=golden_constants["hc_sinkhorn_iters"], eps=eps)
+    colsum = comb.sum(axis=1)
+    assert np.max(np.abs(colsum - 1)) <= golden_constants["comb_col_sum_tolerance_after_final_column_step"]
+    assert np.all(comb > 0)
+    assert np.all(pre > eps)
+    assert np.all((post > 0) & (post < 2))
+
+
+def test_rows_sum_to_one_on_convergent_fixture(golden_constants):
+    # logits of std <= 0.5: 20 rounds converge, rows sum to 1 within 1e-3.
+    n = 2000
+    m = RNG.standard_normal((n, 24)) * 0.5
+    pre, post, comb = oracle.split_sinkhorn(m, np.ones(3, np.float32), np.zeros(24, np.float32),
+                                            hc=4, iters=20, eps=1e-6)
+    rows = comb.sum(axis=2)
+    assert np.max(np.abs(rows - 1)) <= golden_constants["comb_row_sum_tolerance_convergent"]
+    assert np.max(np.abs(comb.sum(axis=1) - 1)) <= 1e-5
+
+
+def test_rows_need_not_converge_on_wide_logits():
+    # documents the reading: on N(0,3) logits, 20 rounds leave some rows off by
+    # more than 1e-3 even in fp64 (so that check is scoped to convergent data).
+    m = RNG.standard_normal((4000, 24)) * 3.0
+    _, _, comb = oracle.split_sinkhorn(m, np.array([1.5, 1.5, 1.5], np.float32),
+                                       np.zeros(24, np.float32), hc=4, iters=20, eps=1e-6)
+    rows = comb.sum(axis=2)
+    assert np.max(np.abs(rows - 1)) > 1e-3
+    assert np.max(np.abs(comb.sum(axis=1) - 1)) <= 1e-5
+
+
+# -------------------------------------------------------------- a4: pre
+def test_pre_matches_numpy_then_round():
+    n, hc, d = 7, 4, 40
+    x = _rand_x(n, hc, d)
+    pm = RNG.uniform(0.1, 1.0, (n, hc))
+    got = oracle.pre(x, pm)
+    xf = oracle.bf16_to_f64(x)
+    want = oracle.bf16_from_f64(np.einsum("ts,tsd->td", pm, xf))
+    # einsum may sum in another order: allow a 1-ulp tie flip, never more
+    diff = np.abs(got.astype(np.int32) - want.astype(np.int32))
+    assert diff.max() <= 1 and np.mean(diff) < 1e-3
+
+
+def test_pre_identical_streams_closed_form():
+    n, hc, d = 3, 4, 32
+    v = _rand_x(n, 1, d)
+    x = np.repeat(v, hc, axis=1)
+    pm = np.array([[0.5, 0.25, 0.125, 0.0625]] * n)  # dyadic: exact sums
+    got = oracle.pre(x, pm)
+    want = oracle.bf16_from_f64(oracle.bf16_to_f64(v[:, 0, :]) * 0.9375)
+    assert np.array_equal(got, want)
+
+
+# ---------------------------------------------------------- a5: RMSNorm
+def test_rmsnorm_matches_torch_rms_norm():
+    n, d = 6, 64
+    h = _rand_x(n, 1, d)[:, 0, :]
+    w = RNG.uniform(0.5, 1.5, d).astype(np.float32)
+    got = oracle.rmsnorm(h, w, eps=1e-20)
+    hf = torch.from_numpy(oracle.bf16_to_f64(h))
+    ref = torch.nn.functional.rms_norm(hf, (d,), weight=torch.from_numpy(w.astype(np.float64)),
+                                       eps=1e-20).numpy()
+    want = oracle.bf16_from_f64(ref)
+    diff = np.abs(got.astype(np.int32) - want.astype(np.int32))
+    assert diff.max() <= 1 and np.mean(diff) < 1e-2
+
+
+def test_rmsnorm_scale_invariance_and_constant_vector():
+    n, d = 4, 128
+    h = _rand_x(n, 1, d)[:, 0, :]
+    w = RNG.uniform(0.5, 1.5, d).astype(np.float32)
+    base = oracle.rmsnorm(h, w)
+    for k in (-4, 3):
+        hs = oracle.bf16_from_f64(oracle.bf16_to_f64(h) * 2.0 ** k)
+        assert np.array_equal(oracle.rmsnorm(hs, w), base)
+    # a constant vector normalises to +-1, so the output is the rounded gain
+    c = oracle.bf16_from_f64(np.full((1, d), -3.0))
+    assert np.array_equal(oracle.rmsnorm(c, w), oracle.bf16_from_f64(-w.astype(np.float64))[None])
+
+
+def test_rmsnorm_eps_matters_only_near_zero():
+    d = 16
+    z = np.zeros((1, d), np.uint16)
+    w = np.ones(d, np.float32)
+    assert np.array_equal(oracle.rmsnorm(z, w, 1e-20), np.zeros((1, d), np.uint16))
+
+
+# ------------------------------------------------------------- a6: post
+def test_post_matches_numpy_einsum():
+    n, hc, d = 5, 4, 48
+    r = _rand_x(n, hc, d)
+    f = _rand_x(n, 1, d)[:, 0, :]
+    post = RNG.uniform(0, 2, (n, hc))
+    comb = RNG.uniform(0, 1, (n, hc, hc))
+    got = oracle.post(f, r, post, comb)
+    rf = oracle.bf16_to_f64(r)
+    ff = oracle.bf16_to_f64(f)
+    ref = post[:, :, None] * ff[:, None, :] + np.einsum("tjk,tjd->tkd", comb, rf)
+    want = oracle.bf16_from_f64(ref)
+    diff = np.abs(got.astype(np.int32) - want.astype(np.int32))
+    assert diff.max() <= 1 and np.mean(diff) < 1e-3
+
+
+def test_post_column_k_feeds_output_k():
+    # comb = permutation matrix (j -> k) with post = 0 routes stream j to output k
+    n, hc, d = 1, 4, 16
+    r = _rand_x(n, hc, d)
+    f = _rand_x(n, 1, d)[:, 0, :]
+    perm = [2, 0, 3, 1]  # input j goes to output perm[j]
+    comb = np.zeros((1, 4, 4))
+    for j, k in enumerate(perm):
+        comb[0, j, k] = 1.0
+    y = oracle.post(f, r, np.zeros((1, 4)), comb)
+    for j, k in enumerate(perm):
+        assert np.array_equal(y[0, k], r[0, j])
+
+
+def test_post_identical_streams_and_stream_sum():
+    n, hc, d = 2, 4, 32
+    v = _rand_x(n, 1, d)
+    r = np.repeat(v, hc, axis=1)
+    f = _rand_x(n, 1, d)[:, 0, :]
+    post = np.array([[0.5, 1.0, 1.5, 0.25]] * n)
+    comb = np.full((n, hc, hc), 0.25)  # column sums exactly 1
+    y = oracle.post(f, r, post, comb)
+    want = oracle.bf16_from_f64(post[:, :, None] * oracle.bf16_to_f64(f)[:, None, :]
+                                + oracle.bf16_to_f64(v))
+    assert np.array_equal(y, want)
+
+
+# -------------------------------------------------- a7: the side step / block
+def test_block_step_stream_permutation_equivariance():
+    # relabel the streams by a permutation pi consistently (x streams,
+    # hc_fn column blocks, pre/post base entries, comb rows and columns,
+    # pre_mix): pre/post/comb/y are relabelled, h_norm is unchanged.
+    hc, d, n = 4, 32, 3
+    case = inputs.tiny(seed=5, n=n, d=d)
+    p = case.params[0]
+    x = inputs.bf16_bits_np(case.x)
+    f = inputs.bf16_bits_np(case.fs[0])
+    pm = case.pre_mix.numpy().astype(np.float64)
+    W = p.hc_fn.numpy()
+    base = p.hc_base.numpy()
+    out = oracle.block_step(x, pm, f, W, p.hc_scale.numpy(), base, p.norm_w.numpy())
+    pi = np.array([2, 0, 3, 1])
+    xp = x[:, pi, :]
+    pmp = pm[:, pi]
+    Wb = W.reshape(24, hc, d)[:, pi, :]
+    rows = np.concatenate([pi, 4 + pi, (8 + (pi[:, None] * 4 + pi[None, :])).reshape(-1)])
+    Wp = Wb[rows].reshape(24, hc * d)
+    bp = base[rows]
+    o2 = oracle.block_step(xp, pmp, f, Wp, p.hc_scale.numpy(), bp, p.norm_w.numpy())
+    np.testing.assert_allclose(o2["pre"], out["pre"][:, pi], rtol=1e-12, atol=1e-15)
+    np.testing.assert_allclose(o2["post"], out["post"][:, pi], rtol=1e-12, atol=1e-15)
+    np.testing.assert_allclose(o2["comb"], out["comb"][:, pi][:, :, pi], rtol=1e-10, atol=1e-14)
+    assert np.abs(o2["y"].astype(np.int32) - out["y"][:, pi].astype(np.int32)).max() <= 1
+    assert np.abs(o2["h_norm"].astype(np.int32) - out["h_norm"].astype(np.int32)).max() <= 1
+
+
+def test_block_layer_wiring():
+    # the FFN side reads with the attention side's pre and consumes its y
+    hc, d, n = 4, 16, 2
+    case = inputs.decode(seed=1, n=n, d=d)
+    pa, pf = (p.astuple() for p in case.params)
+    pa = tuple(t.numpy() for t in pa)
+    pf = tuple(t.numpy() for t in pf)
+    x = inputs.bf16_bits_np(case.x)
+    fa, ff = (inputs.bf16_bits_np(f) for f in case.fs)
+    pm = case.pre_mix.numpy().astype(np.float64)
+    a, b = oracle.block_layer(x, pm, fa, ff, pa, pf)
+    a2 = oracle.block_step(x, pm, fa, *pa)
+    b2 = oracle.block_step(a2["y"], a2["pre"], ff, *pf)
+    assert np.array_equal(b["y"], b2["y"]) and np.array_equal(b["h_norm"], b2["h_norm"])
+    # the FFN side's h_norm depends on the attention side's pre, not its own
+    h_expected = oracle.rmsnorm(oracle.pre(a["y"], a["pre"]), pf[3])
+    assert np.array_equal(b["h_norm"], h_expected)
+
+
+def test_param_counts_match_pages(golden_constants):
+    g = golden_constants
+    p = inputs.side_params(torch.Generator().manual_seed(0), hc=g["hc_mult"], d=g["dim"])
+    n_params = p.hc_fn.numel() + p.hc_base.numel() + p.hc_scale.numel()
+    assert n_params == g["stream_weights_params_per_sublayer"] == 491547
+    assert p.norm_w.numel() == g["rmsnorm_params"]
+    hc = g["hc_mult"]
+    assert hc * hc + 1 == g["comb_params_per_instance"]
+    assert (2 + hc) * hc == g["comb_in_out_shapes"]["in_mix_numbers"]
