@@ -1,0 +1,445 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused hyper-connection side step (hc_block_step).
+
+Workload (default): long prefill -- 4 x 16384 = 65,536 tokens, hc = 4,
+d = 5120, through 40 layers = 80 side steps, each side with its own seeded
+parameters and its own N(0, 2) sublayer stand-in output.  One benchmark
+"step" is one pass of all 80 side steps over the batch.  Metric: tokens/s
+through the full depth (plus achieved HBM GB/s of the side-step kernel
+against the measured HBM peak).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs its own replica on its own GPU with
+its own batch (weak scaling, no collective on the data path); the timing is
+the max over ranks.  --impl reference times the CPU oracle on the host cores
+on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np
+import torch
+
+import hyper_connection_residual_mixes_gb300 as hcg
+from hyper_connection_residual_mixes_gb300 import inputs
+
+HC, D = 4, 5120
+TOKENS = 65536
+LAYERS = 40
+SIDES = 2 * LAYERS
+MIX = (2 + HC) * HC
+# algorithmic bytes of one side step: each input once, each output once
+BYTES_PER_TOKEN = HC * D * 2 + D * 2 + HC * 4 + HC * D * 2 + D * 2 + HC * 4   # 102,432
+BYTES_WEIGHTS = MIX * HC * D * 4 + 3 * 4 + MIX * 4 + D * 4                      # 1,986,668
+FLOPS_PER_TOKEN = 2 * MIX * HC * D
+L2_BYTES = 135_528_448
+KERNEL_NAME = "hc_block_step"
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)),
+            int(os.environ.get("WORLD_SIZE", 1)))
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            pk = json.load(fh)
+        return float(pk["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def source_digest():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "hyper_connection_residual_mixes_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as fh:
+            h.update(name.encode())
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic_per_launch(n_tokens):
+    """DRAM bytes per launch from the committed ncu summary, scaled by tokens;
+    None when it was taken on other kernel sources."""
+    path = os.path.join(ROOT, "profiles", "hc_block_step_traffic.json")
+    try:
+        with open(path) as fh:
+            rec = json.load(fh)
+    except Exception:
+        return None
+    if rec.get("source_digest") != source_digest():
+        return None
+    return int(rec["dram_bytes_per_token"] * n_tokens + rec.get("dram_bytes_fixed", 0))
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled during the timed region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.proc = None
+        self.dev = device_index
+
+    def _gpu_id(self):
+        try:
+            p = torch.cuda.get_device_properties(self.dev)
+            return "%08X:%02X:%02X.0" % (p.pci_domain_id, p.pci_bus_id, p.pci_device_id)
+        except Exception:
+            return str(self.dev)
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self._gpu_id(), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+                power.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "power_w_max": max(power) if power else None, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------- our arm
+def build_workload(device, rank):
+    seed = 4 + 1000 * rank  # rank 0 runs exactly the long-prefill seed
+    case = inputs.long_prefill(device=device, seed=seed, materialize_f=False)
+    fs = [inputs.long_prefill_f(s, case.n, case.d, device, seed) for s in range(SIDES)]
+    return case, fs, seed
+
+
+def run_ours(args, rank, local_rank, world):
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    hcg._lib.load()
+    case, fs, seed = build_workload(dev, rank)
+    n, d = case.n, case.d
+    x0, pm0 = case.x, case.pre_mix
+    ys = [torch.empty_like(x0), torch.empty_like(x0)]
+    pres = [torch.empty((n, HC), device=dev), torch.empty((n, HC), device=dev)]
+    h_norm = torch.empty((n, d), dtype=torch.bfloat16, device=dev)
+    params = [p.astuple() for p in case.params]
+    stream = torch.cuda.current_stream(dev)
+    launches = {"n": 0}
+
+    def step(events=None):
+        x, pm = x0, pm0
+        for s in range(SIDES):
+            if events is not None:
+                events[s][0].record(stream)
+            hcg.hc_block_step(x, pm, fs[s], *params[s], h_norm=h_norm, y=ys[s % 2],
+                              pre_out=pres[s % 2])
+            if events is not None:
+                events[s][1].record(stream)
+            launches["n"] += 1
+            x, pm = ys[s % 2], pres[s % 2]
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    launches["n"] = 0
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(SIDES)] for _ in range(args.steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for k in range(args.steps):
+        step(ev[k])
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    if world > 1:
+        torch.distributed.barrier()
+    elapsed_ms = t0.elapsed_time(t1)
+    launch_ms = [a.elapsed_time(b) for e in ev for (a, b) in e]
+    gpu_launches = launches["n"]
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+
+    e2e = None if args.no_e2e else run_e2e(args, dev, case, seed, world)
+    out = None
+    if rank == 0:
+        ms_per_step = elapsed_ms / args.steps
+        tokens_per_s = world * n / (ms_per_step / 1e3)
+        avg_launch_s = statistics.mean(launch_ms) / 1e3
+        alg_bytes = n * BYTES_PER_TOKEN + BYTES_WEIGHTS
+        achieved = alg_bytes / avg_launch_s / 1e9
+        peak, peak_kind = measured_peaks()
+        step_bytes = SIDES * alg_bytes
+        out = {
+            "metric": "tokens/s (65,536-token long prefill through 40 layers = 80 fused "
+                      "hc_block_step side steps) and achieved HBM GB/s",
+            "value": tokens_per_s,
+            "unit": "tokens/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": ms_per_step,
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "bf16 streams, fp32 arithmetic",
+            "data": "synthetic, seeded (x N(0,1); hc_fn N(0,0.01); f N(0,2); per-side params)",
+            "config": {"workload": "long_prefill", "batch": 4, "seq_len": 16384,
+                       "tokens": n, "hc": HC, "d": d, "layers": LAYERS, "side_steps": SIDES,
+                       "sinkhorn_iters": 20, "seed": seed, "parallelism": "replicas" if world > 1 else "single",
+                       "l2": "inputs larger than L2 (x is %.1f GB per side, L2 %.0f MB); no flush"
+                             % (n * HC * d * 2 / 1e9, L2_BYTES / 1e6)},
+            "hbm_gbs_step": step_bytes / (ms_per_step / 1e3) / 1e9,
+            "hbm_frac_step": step_bytes / (ms_per_step / 1e3) / 1e9 / peak,
+            "roofline": {"kernel": KERNEL_NAME, "bound": "hbm", "achieved": achieved,
+                         "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                         "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs)"
+                         if peak_kind == "measured" else peak_kind,
+                         "traffic": ncu_traffic_per_launch(n),
+                         "algorithmic_bytes_per_launch": alg_bytes,
+                         "avg_launch_us": avg_launch_s * 1e6, "launches_timed": len(launch_ms)},
+            "clocks": clk,
+            "gpu_launches": gpu_launches,
+            "e2e": e2e,
+        }
+        if world == 1 and not args.no_cpu_baseline:
+            out["cpu_baseline"] = cpu_baseline_sample(case, fs, target_s=args.cpu_seconds)
+    return out
+
+
+def run_e2e(args, dev, case, seed, world):
+    """Same metric end to end through the public API: every step copies the
+    step's inputs (x and the 80 sublayer outputs) from pinned host memory and
+    reads the result (final y and pre) back.  f is double-buffered on the
+    device so copies of side s+1 overlap the side-s kernel."""
+    n, d = case.n, case.d
+    f_bytes = n * d * 2
+    need = SIDES * f_bytes + 2 * n * HC * d * 2
+    try:
+        host_ram = os.sysconf("SC_PHYS_PAGES") * os.sysconf("SC_PAGE_SIZE")
+    except Exception:
+        host_ram = 0
+    n_host_f = SIDES if need < 0.45 * host_ram / max(1, world) else max(2, int(
+        0.3 * host_ram / max(1, world) // f_bytes))
+    n_host_f = min(SIDES, n_host_f)
+    x_h = torch.empty((n, HC, d), dtype=torch.bfloat16, pin_memory=True)
+    x_h.copy_(case.x)
+    f_h = []
+    for s in range(n_host_f):
+        t = torch.empty((n, d), dtype=torch.bfloat16, pin_memory=True)
+        t.copy_(inputs.long_prefill_f(s, n, d, dev, seed))
+        f_h.append(t)
+    pm_h = case.pre_mix.cpu().pin_memory()
+    y_h = torch.empty((n, HC, d), dtype=torch.bfloat16, pin_memory=True)
+    pre_h = torch.empty((n, HC), dtype=torch.float32, pin_memory=True)
+    x_d = torch.empty((n, HC, d), dtype=torch.bfloat16, device=dev)
+    pm_d = torch.empty((n, HC), device=dev)
+    f_d = [torch.empty((n, d), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    ys = [torch.empty_like(x_d), torch.empty_like(x_d)]
+    pres = [torch.empty((n, HC), device=dev), torch.empty((n, HC), device=dev)]
+    h_norm = torch.empty((n, d), dtype=torch.bfloat16, device=dev)
+    params = [p.astuple() for p in case.params]
+    comp = torch.cuda.current_stream(dev)
+    copy = torch.cuda.Stream(dev)
+    f_ready = [torch.cuda.Event() for _ in range(2)]
+    f_free = [torch.cuda.Event() for _ in range(2)]
+
+    def step():
+        with torch.cuda.stream(copy):
+            copy.wait_event(f_free[0])
+            x_d.copy_(x_h, non_blocking=True)
+            pm_d.copy_(pm_h, non_blocking=True)
+            f_d[0].copy_(f_h[0], non_blocking=True)
+            f_ready[0].record(copy)
+        x, pm = x_d, pm_d
+        for s in range(SIDES):
+            b = s % 2
+            if s + 1 < SIDES:
+                nb = (s + 1) % 2
+                with torch.cuda.stream(copy):
+                    copy.wait_event(f_free[nb])
+                    f_d[nb].copy_(f_h[(s + 1) % n_host_f], non_blocking=True)
+                    f_ready[nb].record(copy)
+            comp.wait_event(f_ready[b])
+            hcg.hc_block_step(x, pm, f_d[b], *params[s], h_norm=h_norm, y=ys[b], pre_out=pres[b],
+                              stream=comp)
+            f_free[b].record(comp)
+            x, pm = ys[b], pres[b]
+        y_h.copy_(x, non_blocking=True)
+        pre_h.copy_(pm, non_blocking=True)
+
+    for e in f_free:
+        e.record(comp)
+    step()
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    steps = max(1, min(args.steps, 5))
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    torch.cuda.synchronize(dev)
+    dt = time.perf_counter() - t0
+    if world > 1:
+        t = torch.tensor([dt], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        dt = float(t.item())
+    h2d = n * HC * d * 2 + n * HC * 4 + SIDES * f_bytes
+    d2h = n * HC * d * 2 + n * HC * 4
+    return {"value": world * n * steps / dt, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": steps,
+            "host_f_buffers": n_host_f,
+            "note": "pinned host buffers; H2D of x and all 80 f per step, D2H of final y and pre; "
+                    "f copies double-buffered against the kernels"
+                    + ("" if n_host_f == SIDES else "; host f pool of %d reused cyclically" % n_host_f)}
+
+
+# ---------------------------------------------------------------- oracle arm
+def _oracle_chain(oracle, x_bits, pm, fs_bits, params_np):
+    for s in range(SIDES):
+        o = oracle.block_step(x_bits, pm, fs_bits[s], *params_np[s])
+        x_bits, pm = o["y"], o["pre"]
+    return x_bits, pm
+
+
+def cpu_baseline_sample(case, fs, target_s=15.0, sample_tokens=None):
+    """The oracle (single-threaded C, fp64) on a sample of tokens through all
+    80 side steps; tokens/s extrapolated from the sample."""
+    import oracle
+    n = case.n
+    params_np = [tuple(t.detach().cpu().numpy() for t in p.astuple()) for p in case.params]
+    rows = torch.arange(0, n, max(1, n // 4096), device=case.x.device)
+    probe = rows[:2]
+    fs_np = lambda r: [inputs.bf16_bits_np(f.index_select(0, r)) for f in fs]
+    t0 = time.perf_counter()
+    _oracle_chain(oracle, inputs.bf16_bits_np(case.x.index_select(0, probe)),
+                  case.pre_mix.index_select(0, probe).cpu().numpy().astype(np.float64),
+                  fs_np(probe), params_np)
+    per_tok = (time.perf_counter() - t0) / 2
+    k = sample_tokens or max(2, min(len(rows), int(target_s / max(per_tok, 1e-6))))
+    sel = rows[:k]
+    t0 = time.perf_counter()
+    _oracle_chain(oracle, inputs.bf16_bits_np(case.x.index_select(0, sel)),
+                  case.pre_mix.index_select(0, sel).cpu().numpy().astype(np.float64),
+                  fs_np(sel), params_np)
+    dt = time.perf_counter() - t0
+    return {"value": k / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": "%d of %d tokens through all 80 side steps (%.1f s)" % (k, n, dt),
+            "host_cores_available": os.cpu_count()}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    import oracle
+    oracle.build()
+    dev = "cpu"
+    # a bounded sample of the same workload: the same generators and
+    # distributions, drawn for `tok` tokens
+    tok = max(1, args.reference_tokens)
+    case = inputs.long_prefill(device=dev, seed=4, n=tok, materialize_f=False)
+    fs = [inputs.long_prefill_f(s, tok, D, dev, 4) for s in range(SIDES)]
+    params_np = [tuple(t.numpy() for t in p.astuple()) for p in case.params]
+    xb = inputs.bf16_bits_np(case.x[:tok])
+    pm = case.pre_mix[:tok].numpy().astype(np.float64)
+    fb = [inputs.bf16_bits_np(f[:tok]) for f in fs]
+    for _ in range(args.warmup):
+        _oracle_chain(oracle, xb[:1], pm[:1], [f[:1] for f in fb], params_np)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        _oracle_chain(oracle, xb, pm, fb, params_np)
+    dt = time.perf_counter() - t0
+    value = tok * args.steps / dt
+    return {
+        "impl": "reference",
+        "metric": "tokens/s (65,536-token long prefill through 40 layers = 80 fused "
+                  "hc_block_step side steps) and achieved HBM GB/s",
+        "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic, seeded",
+        "config": {"workload": "long_prefill", "batch": 4, "seq_len": 16384, "tokens": TOKENS,
+                   "hc": HC, "d": D, "layers": LAYERS, "side_steps": SIDES},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": "%d tokens of the long prefill through all 80 side steps per step"
+                                   % tok},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling runs)")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--reference-tokens", type=int, default=4)
+    args = ap.parse_args()
+    rank, local_rank, world = dist_env()
+    if world > 1:
+        backend = "nccl" if (args.impl == "ours" and torch.cuda.is_available()) else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group(backend=backend)
+    if args.impl == "reference":
+        out = run_reference(args, rank, world)
+    else:
+        out = run_ours(args, rank, local_rank, world)
+    if out is not None and rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1 and args.impl == "ours":
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

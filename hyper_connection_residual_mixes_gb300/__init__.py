@@ -1,0 +1,177 @@
+"""GB300-native hyper-connection residual path (DeepSeek-V4.1-style blocks).
+
+A thin PyTorch binding over libhc.so (C ABI in include/hc.h).  Each function
+has the name of the C entry point it calls, checks and marshals tensors
+(device, dtype, contiguity, shapes), allocates outputs with PyTorch when they
+are not supplied, and enqueues the call on the current CUDA stream.  Every
+step of the path runs in the CUDA kernels; there is no CPU or PyTorch
+fallback, and calling with CPU tensors raises.
+
+Shapes (hc = 4 streams, d = 5120 in the released model, mix = (2+hc)*hc = 24):
+  x, residual, y  [..., hc, d] bf16;  f, h_norm [..., d] bf16
+  hc_fn [mix, hc*d] fp32;  hc_base [mix];  hc_scale [3];  norm_w [d] fp32
+  pre, post, pre_mix [..., hc] fp32;  comb [..., hc, hc] fp32;  mixes [..., mix] fp32
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _lib
+from ._lib import HcError
+
+__all__ = ["hc_mixes", "hc_split_sinkhorn", "hc_pre_norm", "hc_post", "hc_block_step",
+           "HcError", "library_path", "version"]
+
+HC_EPS = 1e-6
+NORM_EPS = 1e-20
+SINKHORN_ITERS = 20
+
+
+def library_path() -> str:
+    return _lib.LIB_PATH
+
+
+def version() -> int:
+    return _lib.load().hc_version()
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _check(t, name, dtype, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor (libhc has no CPU path)" % name)
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if device is not None and t.device != device:
+        raise ValueError("%s is on %s, expected %s" % (name, t.device, device))
+    return t
+
+
+def _out(t, name, shape, dtype, device):
+    if t is None:
+        return torch.empty(shape, dtype=dtype, device=device)
+    _check(t, name, dtype, device)
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError("%s has shape %s, expected %s" % (name, tuple(t.shape), tuple(shape)))
+    return t
+
+
+def hc_split_sinkhorn(mixes, hc_scale, hc_base, hc_mult=4, sinkhorn_iters=SINKHORN_ITERS,
+                      eps=HC_EPS, pre=None, post=None, comb=None, stream=None):
+    """a2-a3: mixes [..., (2+hc)*hc] fp32 -> (pre [..., hc], post [..., hc], comb [..., hc, hc])."""
+    _check(mixes, "mixes", torch.float32)
+    dev = mixes.device
+    _check(hc_scale, "hc_scale", torch.float32, dev)
+    _check(hc_base, "hc_base", torch.float32, dev)
+    lead = tuple(mixes.shape[:-1])
+    n = mixes.numel() // mixes.shape[-1] if mixes.dim() else 0
+    pre = _out(pre, "pre", lead + (hc_mult,), torch.float32, dev)
+    post = _out(post, "post", lead + (hc_mult,), torch.float32, dev)
+    comb = _out(comb, "comb", lead + (hc_mult, hc_mult), torch.float32, dev)
+    with torch.cuda.device(dev):
+        _lib.call("hc_split_sinkhorn", _ptr(mixes), _ptr(hc_scale), _ptr(hc_base), n, hc_mult,
+                  sinkhorn_iters, eps, _ptr(pre), _ptr(post), _ptr(comb), _stream(stream))
+    return pre, post, comb
+
+
+def hc_mixes(x, hc_fn, hc_scale, hc_base, sinkhorn_iters=SINKHORN_ITERS, eps=HC_EPS,
+             norm_eps=NORM_EPS, pre=None, post=None, comb=None, mixes_out=None,
+             return_mixes=False, stream=None):
+    """a1-a3: x [..., hc, d] bf16 -> (pre, post, comb) [+ mixes when return_mixes]."""
+    _check(x, "x", torch.bfloat16)
+    dev = x.device
+    hc, d = x.shape[-2], x.shape[-1]
+    lead = tuple(x.shape[:-2])
+    n = x.numel() // (hc * d) if x.numel() else 0
+    mix = (2 + hc) * hc
+    _check(hc_fn, "hc_fn", torch.float32, dev)
+    _check(hc_scale, "hc_scale", torch.float32, dev)
+    _check(hc_base, "hc_base", torch.float32, dev)
+    pre = _out(pre, "pre", lead + (hc,), torch.float32, dev)
+    post = _out(post, "post", lead + (hc,), torch.float32, dev)
+    comb = _out(comb, "comb", lead + (hc, hc), torch.float32, dev)
+    if return_mixes:
+        mixes_out = _out(mixes_out, "mixes_out", lead + (mix,), torch.float32, dev)
+    elif mixes_out is not None:
+        _out(mixes_out, "mixes_out", lead + (mix,), torch.float32, dev)
+    with torch.cuda.device(dev):
+        _lib.call("hc_mixes", _ptr(x), _ptr(hc_fn), _ptr(hc_scale), _ptr(hc_base), n, hc, d,
+                  sinkhorn_iters, eps, norm_eps, _ptr(pre), _ptr(post), _ptr(comb),
+                  _ptr(mixes_out), _stream(stream))
+    if return_mixes:
+        return pre, post, comb, mixes_out
+    return pre, post, comb
+
+
+def hc_pre_norm(x, pre_mix, norm_w, norm_eps=NORM_EPS, out=None, stream=None):
+    """a4-a5: x [..., hc, d] bf16, pre_mix [..., hc] fp32 -> RMSNorm(hc_pre) [..., d] bf16."""
+    _check(x, "x", torch.bfloat16)
+    dev = x.device
+    hc, d = x.shape[-2], x.shape[-1]
+    lead = tuple(x.shape[:-2])
+    n = x.numel() // (hc * d) if x.numel() else 0
+    _check(pre_mix, "pre_mix", torch.float32, dev)
+    _check(norm_w, "norm_w", torch.float32, dev)
+    out = _out(out, "out", lead + (d,), torch.bfloat16, dev)
+    with torch.cuda.device(dev):
+        _lib.call("hc_pre_norm", _ptr(x), _ptr(pre_mix), _ptr(norm_w), n, hc, d, norm_eps,
+                  _ptr(out), _stream(stream))
+    return out
+
+
+def hc_post(f, residual, post, comb, y=None, stream=None):
+    """a6: f [..., d] bf16, residual [..., hc, d] bf16, post [..., hc], comb [..., hc, hc] -> y."""
+    _check(residual, "residual", torch.bfloat16)
+    dev = residual.device
+    hc, d = residual.shape[-2], residual.shape[-1]
+    n = residual.numel() // (hc * d) if residual.numel() else 0
+    _check(f, "f", torch.bfloat16, dev)
+    _check(post, "post", torch.float32, dev)
+    _check(comb, "comb", torch.float32, dev)
+    y = _out(y, "y", tuple(residual.shape), torch.bfloat16, dev)
+    with torch.cuda.device(dev):
+        _lib.call("hc_post", _ptr(f), _ptr(residual), _ptr(post), _ptr(comb), n, hc, d, _ptr(y),
+                  _stream(stream))
+    return y
+
+
+def hc_block_step(x, pre_mix, f, hc_fn, hc_scale, hc_base, norm_w,
+                  sinkhorn_iters=SINKHORN_ITERS, eps=HC_EPS, norm_eps=NORM_EPS,
+                  h_norm=None, y=None, pre_out=None, post_out=None, comb_out=None,
+                  return_post_comb=False, stream=None):
+    """Fused side step a1-a6.  Returns (h_norm, y, pre_out) or, with
+    return_post_comb, (h_norm, y, pre_out, post_out, comb_out)."""
+    _check(x, "x", torch.bfloat16)
+    dev = x.device
+    hc, d = x.shape[-2], x.shape[-1]
+    lead = tuple(x.shape[:-2])
+    n = x.numel() // (hc * d) if x.numel() else 0
+    for t, nm, dt in ((pre_mix, "pre_mix", torch.float32), (f, "f", torch.bfloat16),
+                      (hc_fn, "hc_fn", torch.float32), (hc_scale, "hc_scale", torch.float32),
+                      (hc_base, "hc_base", torch.float32), (norm_w, "norm_w", torch.float32)):
+        _check(t, nm, dt, dev)
+    h_norm = _out(h_norm, "h_norm", lead + (d,), torch.bfloat16, dev)
+    y = _out(y, "y", tuple(x.shape), torch.bfloat16, dev)
+    pre_out = _out(pre_out, "pre_out", lead + (hc,), torch.float32, dev)
+    if return_post_comb:
+        post_out = _out(post_out, "post_out", lead + (hc,), torch.float32, dev)
+        comb_out = _out(comb_out, "comb_out", lead + (hc, hc), torch.float32, dev)
+    with torch.cuda.device(dev):
+        _lib.call("hc_block_step", _ptr(x), _ptr(pre_mix), _ptr(f), _ptr(hc_fn), _ptr(hc_scale),
+                  _ptr(hc_base), _ptr(norm_w), n, hc, d, sinkhorn_iters, eps, norm_eps,
+                  _ptr(h_norm), _ptr(y), _ptr(pre_out), _ptr(post_out), _ptr(comb_out),
+                  _stream(stream))
+    if return_post_comb:
+        return h_norm, y, pre_out, post_out, comb_out
+    return h_norm, y, pre_out

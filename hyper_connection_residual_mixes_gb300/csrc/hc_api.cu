@@ -1,0 +1,198 @@
+// hc_api.cu -- the C ABI of libhc: host-side validation, then dispatch to the
+// kernels.  Nothing here allocates device memory; every launch goes on the
+// caller's stream.  See include/hc.h for the contract of each entry point.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "../../include/hc.h"
+#include "hc_launch.h"
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+constexpr int kMaxD = 16384;
+
+struct Span {
+    uintptr_t lo, hi;  // [lo, hi); empty when lo == hi
+};
+
+Span span(const void *p, int64_t bytes) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    return Span{a, a + (uintptr_t)(bytes > 0 ? bytes : 0)};
+}
+
+bool overlaps(Span a, Span b) {
+    if (a.lo == a.hi || b.lo == b.hi) return false;
+    return a.lo < b.hi && b.lo < a.hi;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool finite_nonneg(float v) { return std::isfinite(v) && v >= 0.0f; }
+
+hc_status cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return HC_OK;
+    g_last_cuda_error = (int)e;
+    return HC_ERR_CUDA;
+}
+
+// Shape checks shared by the entry points.  n == 0 is valid (no work).
+hc_status check_shape(int64_t n, int hc, int d, bool uses_d) {
+    if (n < 0) return HC_ERR_INVALID_ARG;
+    if (hc <= 0) return HC_ERR_INVALID_ARG;
+    if (hc != 4) return HC_ERR_UNSUPPORTED;  // the compiled stream count
+    if (uses_d) {
+        if (d <= 0) return HC_ERR_INVALID_ARG;
+        if (d % 64 != 0 || d > kMaxD) return HC_ERR_UNSUPPORTED;
+        // n * hc * d elements must be addressable with 64-bit byte offsets
+        if (n > (INT64_MAX / 8) / ((int64_t)hc * d)) return HC_ERR_INVALID_ARG;
+    } else if (n > INT64_MAX / 1024) {
+        return HC_ERR_INVALID_ARG;
+    }
+    return HC_OK;
+}
+
+// Every output span must be disjoint from every input span and from the other outputs.
+hc_status check_alias(const Span *outs, int n_out, const Span *ins, int n_in) {
+    for (int i = 0; i < n_out; ++i) {
+        for (int j = 0; j < n_in; ++j)
+            if (overlaps(outs[i], ins[j])) return HC_ERR_ALIAS;
+        for (int j = i + 1; j < n_out; ++j)
+            if (overlaps(outs[i], outs[j])) return HC_ERR_ALIAS;
+    }
+    return HC_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *hc_status_string(hc_status status) {
+    switch (status) {
+        case HC_OK: return "HC_OK";
+        case HC_ERR_INVALID_ARG: return "HC_ERR_INVALID_ARG: null pointer, bad size or bad scalar";
+        case HC_ERR_UNSUPPORTED: return "HC_ERR_UNSUPPORTED: needs hc == 4 and d a multiple of 64 in [64, 16384]";
+        case HC_ERR_MISALIGNED: return "HC_ERR_MISALIGNED: every pointer must be 16-byte aligned";
+        case HC_ERR_ALIAS: return "HC_ERR_ALIAS: an output overlaps an input or another output";
+        case HC_ERR_CUDA: return "HC_ERR_CUDA: a CUDA call failed (see hc_last_cuda_error)";
+    }
+    return "unknown hc_status";
+}
+
+int hc_last_cuda_error(void) { return g_last_cuda_error; }
+
+int hc_version(void) { return 100; }
+
+hc_status hc_split_sinkhorn(const float *mixes, const float *hc_scale, const float *hc_base,
+                            int64_t n, int hc, int sinkhorn_iters, float eps, float *pre,
+                            float *post, float *comb, cudaStream_t stream) {
+    hc_status st = check_shape(n, hc, 0, false);
+    if (st != HC_OK) return st;
+    if (sinkhorn_iters < 1 || !finite_nonneg(eps)) return HC_ERR_INVALID_ARG;
+    if (n == 0) return HC_OK;
+    if (!mixes || !hc_scale || !hc_base || !pre || !post || !comb) return HC_ERR_INVALID_ARG;
+    const void *ptrs[] = {mixes, hc_scale, hc_base, pre, post, comb};
+    for (const void *p : ptrs)
+        if (!aligned16(p)) return HC_ERR_MISALIGNED;
+    const int64_t mix = (int64_t)(2 + hc) * hc;
+    const Span ins[] = {span(mixes, n * mix * 4), span(hc_scale, 12), span(hc_base, mix * 4)};
+    const Span outs[] = {span(pre, n * hc * 4), span(post, n * hc * 4), span(comb, n * hc * hc * 4)};
+    if ((st = check_alias(outs, 3, ins, 3)) != HC_OK) return st;
+    return cuda_status(hc::launch_split_sinkhorn(mixes, hc_scale, hc_base, n, sinkhorn_iters, eps,
+                                                 pre, post, comb, stream));
+}
+
+hc_status hc_mixes(const uint16_t *x, const float *hc_fn, const float *hc_scale,
+                   const float *hc_base, int64_t n, int hc, int d, int sinkhorn_iters,
+                   float eps, float norm_eps, float *pre, float *post, float *comb,
+                   float *mixes_out, cudaStream_t stream) {
+    hc_status st = check_shape(n, hc, d, true);
+    if (st != HC_OK) return st;
+    if (sinkhorn_iters < 1 || !finite_nonneg(eps) || !finite_nonneg(norm_eps))
+        return HC_ERR_INVALID_ARG;
+    if (n == 0) return HC_OK;
+    if (!x || !hc_fn || !hc_scale || !hc_base || !pre || !post || !comb) return HC_ERR_INVALID_ARG;
+    const void *ptrs[] = {x, hc_fn, hc_scale, hc_base, pre, post, comb};
+    for (const void *p : ptrs)
+        if (!aligned16(p)) return HC_ERR_MISALIGNED;
+    if (mixes_out && !aligned16(mixes_out)) return HC_ERR_MISALIGNED;
+    const int64_t mix = (int64_t)(2 + hc) * hc, K = (int64_t)hc * d;
+    const Span ins[] = {span(x, n * K * 2), span(hc_fn, mix * K * 4), span(hc_scale, 12),
+                        span(hc_base, mix * 4)};
+    const Span outs[] = {span(pre, n * hc * 4), span(post, n * hc * 4),
+                         span(comb, n * hc * hc * 4), span(mixes_out, mixes_out ? n * mix * 4 : 0)};
+    if ((st = check_alias(outs, 4, ins, 4)) != HC_OK) return st;
+    return cuda_status(hc::launch_tokens_simple(x, nullptr, nullptr, hc_fn, hc_scale, hc_base,
+                                                nullptr, n, d, sinkhorn_iters, eps, norm_eps,
+                                                nullptr, nullptr, pre, post, comb, mixes_out,
+                                                stream));
+}
+
+hc_status hc_pre_norm(const uint16_t *x, const float *pre_mix, const float *norm_w, int64_t n,
+                      int hc, int d, float norm_eps, uint16_t *out, cudaStream_t stream) {
+    hc_status st = check_shape(n, hc, d, true);
+    if (st != HC_OK) return st;
+    if (!finite_nonneg(norm_eps)) return HC_ERR_INVALID_ARG;
+    if (n == 0) return HC_OK;
+    if (!x || !pre_mix || !norm_w || !out) return HC_ERR_INVALID_ARG;
+    const void *ptrs[] = {x, pre_mix, norm_w, out};
+    for (const void *p : ptrs)
+        if (!aligned16(p)) return HC_ERR_MISALIGNED;
+    const Span ins[] = {span(x, n * hc * d * 2), span(pre_mix, n * hc * 4), span(norm_w, d * 4)};
+    const Span outs[] = {span(out, n * d * 2)};
+    if ((st = check_alias(outs, 1, ins, 3)) != HC_OK) return st;
+    return cuda_status(hc::launch_pre_norm(x, pre_mix, norm_w, n, d, norm_eps, out, stream));
+}
+
+hc_status hc_post(const uint16_t *f, const uint16_t *residual, const float *post,
+                  const float *comb, int64_t n, int hc, int d, uint16_t *y,
+                  cudaStream_t stream) {
+    hc_status st = check_shape(n, hc, d, true);
+    if (st != HC_OK) return st;
+    if (n == 0) return HC_OK;
+    if (!f || !residual || !post || !comb || !y) return HC_ERR_INVALID_ARG;
+    const void *ptrs[] = {f, residual, post, comb, y};
+    for (const void *p : ptrs)
+        if (!aligned16(p)) return HC_ERR_MISALIGNED;
+    const Span ins[] = {span(f, n * d * 2), span(residual, n * hc * d * 2), span(post, n * hc * 4),
+                        span(comb, n * hc * hc * 4)};
+    const Span outs[] = {span(y, n * hc * d * 2)};
+    if ((st = check_alias(outs, 1, ins, 4)) != HC_OK) return st;
+    return cuda_status(hc::launch_post(f, residual, post, comb, n, d, y, stream));
+}
+
+hc_status hc_block_step(const uint16_t *x, const float *pre_mix, const uint16_t *f,
+                        const float *hc_fn, const float *hc_scale, const float *hc_base,
+                        const float *norm_w, int64_t n, int hc, int d, int sinkhorn_iters,
+                        float eps, float norm_eps, uint16_t *h_norm, uint16_t *y,
+                        float *pre_out, float *post_out, float *comb_out,
+                        cudaStream_t stream) {
+    hc_status st = check_shape(n, hc, d, true);
+    if (st != HC_OK) return st;
+    if (sinkhorn_iters < 1 || !finite_nonneg(eps) || !finite_nonneg(norm_eps))
+        return HC_ERR_INVALID_ARG;
+    if (n == 0) return HC_OK;
+    if (!x || !pre_mix || !f || !hc_fn || !hc_scale || !hc_base || !norm_w || !h_norm || !y ||
+        !pre_out)
+        return HC_ERR_INVALID_ARG;
+    const void *ptrs[] = {x, pre_mix, f, hc_fn, hc_scale, hc_base, norm_w, h_norm, y, pre_out};
+    for (const void *p : ptrs)
+        if (!aligned16(p)) return HC_ERR_MISALIGNED;
+    if ((post_out && !aligned16(post_out)) || (comb_out && !aligned16(comb_out)))
+        return HC_ERR_MISALIGNED;
+    const int64_t mix = (int64_t)(2 + hc) * hc, K = (int64_t)hc * d;
+    const Span ins[] = {span(x, n * K * 2),        span(pre_mix, n * hc * 4), span(f, n * d * 2),
+                        span(hc_fn, mix * K * 4),  span(hc_scale, 12),        span(hc_base, mix * 4),
+                        span(norm_w, d * 4)};
+    const Span outs[] = {span(h_norm, n * d * 2), span(y, n * K * 2), span(pre_out, n * hc * 4),
+                         span(post_out, post_out ? n * hc * 4 : 0),
+                         span(comb_out, comb_out ? n * hc * hc * 4 : 0)};
+    if ((st = check_alias(outs, 5, ins, 7)) != HC_OK) return st;
+    return cuda_status(hc::launch_tokens_simple(x, pre_mix, f, hc_fn, hc_scale, hc_base, norm_w, n,
+                                                d, sinkhorn_iters, eps, norm_eps, h_norm, y,
+                                                pre_out, post_out, comb_out, nullptr, stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,120 @@
+// hc_device.cuh -- device helpers shared by the libhc kernels (sm_103a).
+//
+// bf16 packing, the per-token split + Sinkhorn of the 24 mix numbers in
+// registers, and block reductions.  The split follows the DeepSeek-V4.1
+// "Stream combination" page (hc_split_sinkhorn kernel); the sigmoid / 2 sigma /
+// + eps_hc placement follows the DeepSeek V4.1 Flash diagram blocks of the
+// same names.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+namespace hc {
+
+constexpr int kHC = 4;                      // streams (hc_mult)
+constexpr int kMix = (2 + kHC) * kHC;       // 24 mix numbers per token
+
+// ---------------------------------------------------------------- bf16 helpers
+__device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+
+// Two fp32 -> packed bf16x2 (round to nearest, ties to even); `a` lands in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// Unpack 8 bf16 held in a uint4 into 8 floats.
+__device__ __forceinline__ void unpack8(const uint4 &v, float (&o)[8]) {
+    o[0] = bf16lo(v.x); o[1] = bf16hi(v.x);
+    o[2] = bf16lo(v.y); o[3] = bf16hi(v.y);
+    o[4] = bf16lo(v.z); o[5] = bf16hi(v.z);
+    o[6] = bf16lo(v.w); o[7] = bf16hi(v.w);
+}
+
+__device__ __forceinline__ uint4 pack8(const float (&o)[8]) {
+    return make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]),
+                      pack_bf16x2(o[4], o[5]), pack_bf16x2(o[6], o[7]));
+}
+
+// ---------------------------------------------------------------- reductions
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// ---------------------------------------------------------------- split + Sinkhorn
+__device__ __forceinline__ float sigmoid(float z) {
+    // 1 / (1 + e^-z); e^-z -> inf gives exactly 0.
+    return __frcp_rn(1.0f + expf(-z));
+}
+
+// One token: 24 mix numbers -> pre[4], post[4], comb[16] (row j = input
+// stream, column k = output stream).  First round: row softmax (row maximum
+// subtracted) + eps, then each column divided by (its sum + eps).  Then
+// (iters - 1) rounds of: each row divided by (its sum + eps), each column
+// divided by (its sum + eps).  Division is a correctly rounded reciprocal
+// followed by a multiply.
+__device__ __forceinline__ void split_sinkhorn_token(const float (&m)[kMix], float s0, float s1,
+                                                     float s2, const float *__restrict__ base,
+                                                     int iters, float eps, float (&pre)[kHC],
+                                                     float (&post)[kHC], float (&c)[kHC * kHC]) {
+#pragma unroll
+    for (int j = 0; j < kHC; ++j) pre[j] = sigmoid(fmaf(m[j], s0, base[j])) + eps;
+#pragma unroll
+    for (int j = 0; j < kHC; ++j) post[j] = 2.0f * sigmoid(fmaf(m[kHC + j], s1, base[kHC + j]));
+#pragma unroll
+    for (int i = 0; i < kHC * kHC; ++i) c[i] = fmaf(m[2 * kHC + i], s2, base[2 * kHC + i]);
+
+    // first round: row softmax + eps
+#pragma unroll
+    for (int j = 0; j < kHC; ++j) {
+        float mx = c[j * kHC];
+#pragma unroll
+        for (int k = 1; k < kHC; ++k) mx = fmaxf(mx, c[j * kHC + k]);
+        float s = 0.0f;
+#pragma unroll
+        for (int k = 0; k < kHC; ++k) {
+            c[j * kHC + k] = expf(c[j * kHC + k] - mx);
+            s += c[j * kHC + k];
+        }
+        const float r = __frcp_rn(s);
+#pragma unroll
+        for (int k = 0; k < kHC; ++k) c[j * kHC + k] = fmaf(c[j * kHC + k], r, eps);
+    }
+    // first round: columns
+#pragma unroll
+    for (int k = 0; k < kHC; ++k) {
+        float s = 0.0f;
+#pragma unroll
+        for (int j = 0; j < kHC; ++j) s += c[j * kHC + k];
+        const float r = __frcp_rn(s + eps);
+#pragma unroll
+        for (int j = 0; j < kHC; ++j) c[j * kHC + k] *= r;
+    }
+    for (int it = 1; it < iters; ++it) {
+#pragma unroll
+        for (int j = 0; j < kHC; ++j) {
+            float s = 0.0f;
+#pragma unroll
+            for (int k = 0; k < kHC; ++k) s += c[j * kHC + k];
+            const float r = __frcp_rn(s + eps);
+#pragma unroll
+            for (int k = 0; k < kHC; ++k) c[j * kHC + k] *= r;
+        }
+#pragma unroll
+        for (int k = 0; k < kHC; ++k) {
+            float s = 0.0f;
+#pragma unroll
+            for (int j = 0; j < kHC; ++j) s += c[j * kHC + k];
+            const float r = __frcp_rn(s + eps);
+#pragma unroll
+            for (int j = 0; j < kHC; ++j) c[j * kHC + k] *= r;
+        }
+    }
+}
+
+}  // namespace hc

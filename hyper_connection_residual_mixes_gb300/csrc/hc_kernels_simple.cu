@@ -1,0 +1,375 @@
+// hc_kernels_simple.cu -- straightforward kernels for every step of the
+// hyper-connection side step (sm_103a).
+//
+//  k_split_sinkhorn  a2-a3, one thread per token row of 24 mix numbers
+//                    ("Stream combination" page, hc_split_sinkhorn).
+//  k_pre_norm        a4-a5, one CTA per token: collapse the streams under
+//                    pre_mix, round to bf16, RMSNorm with gain (Block page,
+//                    Block.hc_pre + attn_norm).
+//  k_post            a6, one CTA per token (Block page, Block.hc_post).
+//  k_tokens_simple   a1-a3 and optionally a4-a6 for TOK whole tokens per CTA
+//                    (Block page, Block.hc_mixes and Block.forward).
+//
+// These are the small-n and standalone paths; the fused large-n side step
+// lives in hc_block_cluster.cu.
+#include "hc_device.cuh"
+#include "hc_launch.h"
+
+namespace hc {
+
+// ------------------------------------------------------------------ a2-a3
+__global__ void __launch_bounds__(128)
+k_split_sinkhorn(const float *__restrict__ mixes, const float *__restrict__ hc_scale,
+                 const float *__restrict__ hc_base, int64_t n, int iters, float eps,
+                 float *__restrict__ pre, float *__restrict__ post, float *__restrict__ comb) {
+    const int64_t row = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (row >= n) return;
+    float m[kMix];
+    const float4 *src = reinterpret_cast<const float4 *>(mixes + row * kMix);
+#pragma unroll
+    for (int q = 0; q < kMix / 4; ++q) {
+        const float4 v = __ldg(src + q);
+        m[4 * q + 0] = v.x; m[4 * q + 1] = v.y; m[4 * q + 2] = v.z; m[4 * q + 3] = v.w;
+    }
+    float pr[kHC], po[kHC], c[kHC * kHC];
+    split_sinkhorn_token(m, __ldg(hc_scale), __ldg(hc_scale + 1), __ldg(hc_scale + 2), hc_base,
+                         iters, eps, pr, po, c);
+    reinterpret_cast<float4 *>(pre)[row] = make_float4(pr[0], pr[1], pr[2], pr[3]);
+    reinterpret_cast<float4 *>(post)[row] = make_float4(po[0], po[1], po[2], po[3]);
+    float4 *cd = reinterpret_cast<float4 *>(comb + row * kHC * kHC);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) cd[q] = make_float4(c[4 * q], c[4 * q + 1], c[4 * q + 2], c[4 * q + 3]);
+}
+
+cudaError_t launch_split_sinkhorn(const float *mixes, const float *hc_scale, const float *hc_base,
+                                  int64_t n, int iters, float eps, float *pre, float *post,
+                                  float *comb, cudaStream_t s) {
+    const int threads = 128;
+    const int64_t blocks = (n + threads - 1) / threads;
+    k_split_sinkhorn<<<(unsigned)blocks, threads, 0, s>>>(mixes, hc_scale, hc_base, n, iters, eps,
+                                                           pre, post, comb);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ block sum helper
+template <int NT>
+__device__ __forceinline__ float block_sum(float v, float *scratch /* NT/32 floats */) {
+    v = warp_sum(v);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    __syncthreads();
+    if (lane == 0) scratch[warp] = v;
+    __syncthreads();
+    float t = 0.0f;
+#pragma unroll
+    for (int w = 0; w < NT / 32; ++w) t += scratch[w];
+    return t;
+}
+
+// ------------------------------------------------------------------ a4-a5
+// h[c] = bf16(sum_s pre_mix[s] * x[s][c]) in fp32 in stream order; then
+// out[c] = bf16((h[c] * rsqrt(mean(h^2) + eps)) * w[c]).
+constexpr int kRowThreads = 256;
+
+__global__ void __launch_bounds__(kRowThreads)
+k_pre_norm(const uint16_t *__restrict__ x, const float *__restrict__ pre_mix,
+           const float *__restrict__ norm_w, int d, float norm_eps, uint16_t *__restrict__ out) {
+    extern __shared__ uint4 hbuf[];  // d/8 chunks of 8 bf16
+    __shared__ float red[kRowThreads / 32];
+    const int64_t t = blockIdx.x;
+    const int d8 = d >> 3;
+    const uint4 *xs = reinterpret_cast<const uint4 *>(x + t * kHC * d);
+    const float p0 = __ldg(pre_mix + t * kHC), p1 = __ldg(pre_mix + t * kHC + 1),
+                p2 = __ldg(pre_mix + t * kHC + 2), p3 = __ldg(pre_mix + t * kHC + 3);
+    float ss = 0.0f;
+    for (int c = threadIdx.x; c < d8; c += kRowThreads) {
+        float a[8], b[8], e[8], g[8], h[8];
+        unpack8(__ldg(xs + c), a);
+        unpack8(__ldg(xs + d8 + c), b);
+        unpack8(__ldg(xs + 2 * d8 + c), e);
+        unpack8(__ldg(xs + 3 * d8 + c), g);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) h[i] = fmaf(p3, g[i], fmaf(p2, e[i], fmaf(p1, b[i], p0 * a[i])));
+        const uint4 hb = pack8(h);
+        hbuf[c] = hb;
+        float r[8];
+        unpack8(hb, r);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) ss = fmaf(r[i], r[i], ss);
+    }
+    const float tot = block_sum<kRowThreads>(ss, red);
+    const float rs = rsqrtf(tot / (float)d + norm_eps);
+    uint4 *o = reinterpret_cast<uint4 *>(out + t * d);
+    const float4 *w4 = reinterpret_cast<const float4 *>(norm_w);
+    for (int c = threadIdx.x; c < d8; c += kRowThreads) {
+        float h[8];
+        unpack8(hbuf[c], h);
+        const float4 wa = __ldg(w4 + 2 * c), wb = __ldg(w4 + 2 * c + 1);
+        const float wv[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) h[i] = (h[i] * rs) * wv[i];
+        o[c] = pack8(h);
+    }
+}
+
+cudaError_t launch_pre_norm(const uint16_t *x, const float *pre_mix, const float *norm_w,
+                            int64_t n, int d, float norm_eps, uint16_t *out, cudaStream_t s) {
+    const size_t smem = (size_t)d * 2;
+    cudaError_t e = cudaFuncSetAttribute(k_pre_norm, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    k_pre_norm<<<(unsigned)n, kRowThreads, smem, s>>>(x, pre_mix, norm_w, d, norm_eps, out);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ a6
+// y[k][c] = bf16(post[k] * f[c] + sum_j comb[j][k] * x[j][c]), fp32, j in order.
+__global__ void __launch_bounds__(kRowThreads)
+k_post(const uint16_t *__restrict__ f, const uint16_t *__restrict__ residual,
+       const float *__restrict__ post, const float *__restrict__ comb, int d,
+       uint16_t *__restrict__ y) {
+    const int64_t t = blockIdx.x;
+    const int d8 = d >> 3;
+    float po[kHC], cm[kHC * kHC];
+#pragma unroll
+    for (int k = 0; k < kHC; ++k) po[k] = __ldg(post + t * kHC + k);
+#pragma unroll
+    for (int i = 0; i < kHC * kHC; ++i) cm[i] = __ldg(comb + t * kHC * kHC + i);
+    const uint4 *fs = reinterpret_cast<const uint4 *>(f + t * d);
+    const uint4 *xs = reinterpret_cast<const uint4 *>(residual + t * kHC * d);
+    uint4 *ys = reinterpret_cast<uint4 *>(y + t * kHC * d);
+    for (int c = threadIdx.x; c < d8; c += kRowThreads) {
+        float fv[8], xv[kHC][8];
+        unpack8(__ldg(fs + c), fv);
+#pragma unroll
+        for (int j = 0; j < kHC; ++j) unpack8(__ldg(xs + j * d8 + c), xv[j]);
+#pragma unroll
+        for (int k = 0; k < kHC; ++k) {
+            float o[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                float acc = po[k] * fv[i];
+#pragma unroll
+                for (int j = 0; j < kHC; ++j) acc = fmaf(cm[j * kHC + k], xv[j][i], acc);
+                o[i] = acc;
+            }
+            ys[k * d8 + c] = pack8(o);
+        }
+    }
+}
+
+cudaError_t launch_post(const uint16_t *f, const uint16_t *residual, const float *post,
+                        const float *comb, int64_t n, int d, uint16_t *y, cudaStream_t s) {
+    k_post<<<(unsigned)n, kRowThreads, 0, s>>>(f, residual, post, comb, d, y);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ a1-a6, TOK tokens per CTA
+// Phase 1: every thread walks 8-wide chunks of the flattened hc*d axis,
+// accumulating the 24 partial dot products and the sum of squares of each of
+// the CTA's tokens; block reduction; one thread per token computes
+// r = rsqrt(mean(x^2) + norm_eps), mixes = dot * r, and the split + Sinkhorn.
+// Phase 2 (side step only): y and h for every token (x re-read through L1/L2),
+// sum of squares of the rounded h, then h_norm.
+constexpr int kTok = 4;
+constexpr int kTokThreads = 256;
+
+template <bool kFull>
+__global__ void __launch_bounds__(kTokThreads)
+k_tokens_simple(const uint16_t *__restrict__ x, const float *__restrict__ pre_mix,
+                const uint16_t *__restrict__ f, const float *__restrict__ hc_fn,
+                const float *__restrict__ hc_scale, const float *__restrict__ hc_base,
+                const float *__restrict__ norm_w, int64_t n, int d, int iters, float eps,
+                float norm_eps, uint16_t *__restrict__ h_norm, uint16_t *__restrict__ y,
+                float *__restrict__ pre_out, float *__restrict__ post_out,
+                float *__restrict__ comb_out, float *__restrict__ mixes_out) {
+    constexpr int kVals = kMix * kTok + kTok;  // 24 dots per token + sum of squares per token
+    extern __shared__ uint4 hbuf[];            // kTok * d/8 chunks (side step only)
+    __shared__ float red[kTokThreads / 32][kVals];
+    __shared__ float tot[kVals];
+    __shared__ float coef[kTok][kHC + kHC * kHC];
+    __shared__ float ssh[kTokThreads / 32][kTok];
+
+    const int64_t t0 = (int64_t)blockIdx.x * kTok;
+    const int ntok = (n - t0 < kTok) ? (int)(n - t0) : kTok;
+    const int K = kHC * d, K8 = K >> 3;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    float acc[kMix][kTok];
+    float ss[kTok];
+#pragma unroll
+    for (int i = 0; i < kMix; ++i)
+#pragma unroll
+        for (int u = 0; u < kTok; ++u) acc[i][u] = 0.0f;
+#pragma unroll
+    for (int u = 0; u < kTok; ++u) ss[u] = 0.0f;
+
+    for (int ch = threadIdx.x; ch < K8; ch += kTokThreads) {
+        float xv[kTok][8];
+#pragma unroll
+        for (int u = 0; u < kTok; ++u) {
+            if (u < ntok) {
+                unpack8(__ldg(reinterpret_cast<const uint4 *>(x + (t0 + u) * K) + ch), xv[u]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) xv[u][e] = 0.0f;
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) ss[u] = fmaf(xv[u][e], xv[u][e], ss[u]);
+        }
+#pragma unroll
+        for (int i = 0; i < kMix; ++i) {
+            const float4 *wp = reinterpret_cast<const float4 *>(hc_fn + (int64_t)i * K) + 2 * ch;
+            const float4 wa = __ldg(wp), wb = __ldg(wp + 1);
+            const float w[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+            for (int u = 0; u < kTok; ++u)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[i][u] = fmaf(xv[u][e], w[e], acc[i][u]);
+        }
+    }
+    // block reduction of the 24*kTok dots and kTok sums of squares
+#pragma unroll
+    for (int i = 0; i < kMix; ++i)
+#pragma unroll
+        for (int u = 0; u < kTok; ++u) {
+            const float v = warp_sum(acc[i][u]);
+            if (lane == 0) red[warp][i * kTok + u] = v;
+        }
+#pragma unroll
+    for (int u = 0; u < kTok; ++u) {
+        const float v = warp_sum(ss[u]);
+        if (lane == 0) red[warp][kMix * kTok + u] = v;
+    }
+    __syncthreads();
+    for (int v = threadIdx.x; v < kVals; v += kTokThreads) {
+        float s = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kTokThreads / 32; ++w) s += red[w][v];
+        tot[v] = s;
+    }
+    __syncthreads();
+    if (threadIdx.x < ntok) {
+        const int u = threadIdx.x;
+        const int64_t t = t0 + u;
+        const float r = rsqrtf(tot[kMix * kTok + u] / (float)K + norm_eps);
+        float m[kMix];
+#pragma unroll
+        for (int i = 0; i < kMix; ++i) m[i] = tot[i * kTok + u] * r;
+        float pr[kHC], po[kHC], c[kHC * kHC];
+        split_sinkhorn_token(m, __ldg(hc_scale), __ldg(hc_scale + 1), __ldg(hc_scale + 2), hc_base,
+                             iters, eps, pr, po, c);
+        if (pre_out) reinterpret_cast<float4 *>(pre_out)[t] = make_float4(pr[0], pr[1], pr[2], pr[3]);
+        if (post_out) reinterpret_cast<float4 *>(post_out)[t] = make_float4(po[0], po[1], po[2], po[3]);
+        if (comb_out) {
+            float4 *cd = reinterpret_cast<float4 *>(comb_out + t * kHC * kHC);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                cd[q] = make_float4(c[4 * q], c[4 * q + 1], c[4 * q + 2], c[4 * q + 3]);
+        }
+        if (mixes_out) {
+            float4 *md = reinterpret_cast<float4 *>(mixes_out + t * kMix);
+#pragma unroll
+            for (int q = 0; q < kMix / 4; ++q)
+                md[q] = make_float4(m[4 * q], m[4 * q + 1], m[4 * q + 2], m[4 * q + 3]);
+        }
+#pragma unroll
+        for (int k = 0; k < kHC; ++k) coef[u][k] = po[k];
+#pragma unroll
+        for (int i = 0; i < kHC * kHC; ++i) coef[u][kHC + i] = c[i];
+    }
+    if constexpr (!kFull) return;
+    __syncthreads();
+
+    // phase 2: y, h (kept in shared memory as bf16), sum of squares of h
+    const int d8 = d >> 3;
+    float hs[kTok];
+#pragma unroll
+    for (int u = 0; u < kTok; ++u) hs[u] = 0.0f;
+#pragma unroll
+    for (int u = 0; u < kTok; ++u) {
+        if (u >= ntok) break;
+        const int64_t t = t0 + u;
+        const float p0 = __ldg(pre_mix + t * kHC), p1 = __ldg(pre_mix + t * kHC + 1),
+                    p2 = __ldg(pre_mix + t * kHC + 2), p3 = __ldg(pre_mix + t * kHC + 3);
+        const uint4 *xs = reinterpret_cast<const uint4 *>(x + t * K);
+        const uint4 *fs = reinterpret_cast<const uint4 *>(f + t * d);
+        uint4 *ys = reinterpret_cast<uint4 *>(y + t * K);
+        for (int c = threadIdx.x; c < d8; c += kTokThreads) {
+            float fv[8], xv[kHC][8];
+            unpack8(__ldg(fs + c), fv);
+#pragma unroll
+            for (int j = 0; j < kHC; ++j) unpack8(__ldg(xs + j * d8 + c), xv[j]);
+#pragma unroll
+            for (int k = 0; k < kHC; ++k) {
+                float o[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    float a = coef[u][k] * fv[i];
+#pragma unroll
+                    for (int j = 0; j < kHC; ++j) a = fmaf(coef[u][kHC + j * kHC + k], xv[j][i], a);
+                    o[i] = a;
+                }
+                ys[k * d8 + c] = pack8(o);
+            }
+            float h[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                h[i] = fmaf(p3, xv[3][i], fmaf(p2, xv[2][i], fmaf(p1, xv[1][i], p0 * xv[0][i])));
+            const uint4 hb = pack8(h);
+            hbuf[u * d8 + c] = hb;
+            float r8[8];
+            unpack8(hb, r8);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) hs[u] = fmaf(r8[i], r8[i], hs[u]);
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < kTok; ++u) {
+        const float v = warp_sum(hs[u]);
+        if (lane == 0) ssh[warp][u] = v;
+    }
+    __syncthreads();
+    const float4 *w4 = reinterpret_cast<const float4 *>(norm_w);
+    for (int u = 0; u < ntok; ++u) {
+        float s = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kTokThreads / 32; ++w) s += ssh[w][u];
+        const float rs = rsqrtf(s / (float)d + norm_eps);
+        uint4 *o = reinterpret_cast<uint4 *>(h_norm + (t0 + u) * d);
+        for (int c = threadIdx.x; c < d8; c += kTokThreads) {
+            float h[8];
+            unpack8(hbuf[u * d8 + c], h);
+            const float4 wa = __ldg(w4 + 2 * c), wb = __ldg(w4 + 2 * c + 1);
+            const float wv[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) h[i] = (h[i] * rs) * wv[i];
+            o[c] = pack8(h);
+        }
+    }
+}
+
+cudaError_t launch_tokens_simple(const uint16_t *x, const float *pre_mix, const uint16_t *f,
+                                 const float *hc_fn, const float *hc_scale, const float *hc_base,
+                                 const float *norm_w, int64_t n, int d, int iters, float eps,
+                                 float norm_eps, uint16_t *h_norm, uint16_t *y, float *pre_out,
+                                 float *post_out, float *comb_out, float *mixes_out,
+                                 cudaStream_t s) {
+    const int64_t blocks = (n + kTok - 1) / kTok;
+    cudaError_t e;
+    if (f) {
+        const size_t smem = (size_t)kTok * d * 2;
+        e = cudaFuncSetAttribute(k_tokens_simple<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem);
+        if (e != cudaSuccess) return e;
+        k_tokens_simple<true><<<(unsigned)blocks, kTokThreads, smem, s>>>(
+            x, pre_mix, f, hc_fn, hc_scale, hc_base, norm_w, n, d, iters, eps, norm_eps, h_norm, y,
+            pre_out, post_out, comb_out, mixes_out);
+    } else {
+        k_tokens_simple<false><<<(unsigned)blocks, kTokThreads, 0, s>>>(
+            x, pre_mix, f, hc_fn, hc_scale, hc_base, norm_w, n, d, iters, eps, norm_eps, h_norm, y,
+            pre_out, post_out, comb_out, mixes_out);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace hc

@@ -1,0 +1,148 @@
+/*
+ * hc.h -- C ABI of libhc, the GB300 (sm_103a) implementation of the
+ * hyper-connection residual path of a DeepSeek-V4.1-style block.
+ *
+ * The residual of a token is hc parallel streams of width d (hc = 4,
+ * d = 5120 in the released configuration).  Each sublayer side runs:
+ *   a1  mixes   = (x_flat . hc_fn^T) * rsqrt(mean(x_flat^2) + norm_eps)
+ *   a2  pre     = sigmoid(mixes[0:hc] * s0 + b) + eps,  post = 2 sigmoid(mixes[hc:2hc] * s1 + b)
+ *   a3  comb    = Sinkhorn(row softmax + eps of mixes[2hc:] * s2 + b), iters rounds
+ *   a4  h       = bf16(sum_s pre_mix[s] * x[s])
+ *   a5  h_norm  = bf16(RMSNorm(h) * w)
+ *   a6  y[k]    = bf16(post[k] * f + sum_j comb[j][k] * x[j])
+ * Sources: DeepSeek-V4.1 "Block(layer_id, args)" page, Code section
+ * (Block.hc_mixes, hc_pre, hc_post, forward); DeepSeek-V4.1 "Stream
+ * combination" page, Code section (hc_split_sinkhorn); DeepSeek V4.1 Flash
+ * diagram (Cast, sigma, 2 sigma, x + eps_hc, First Sinkhorn Round, Sinkhorn
+ * Round, Single-Pass mHC blocks); RMSNorm per the DeepSeek-R1 dossier's
+ * RMSNorm records (the V4.1 body is not on the pages).
+ *
+ * Conventions for every entry point
+ *  - All tensor pointers are DEVICE pointers owned by the caller.  The
+ *    library never allocates, frees or retains caller memory, keeps no
+ *    state between calls, and never reads or writes outside the extents
+ *    stated below.
+ *  - Layouts are dense row-major with the innermost index last:
+ *      x, residual, y   [n, hc, d]   bf16 (uint16_t bit patterns)
+ *      f, h_norm        [n, d]       bf16
+ *      hc_fn            [(2+hc)*hc, hc*d] fp32  (row i, column s*d + c)
+ *      hc_base          [(2+hc)*hc] fp32,  hc_scale [3] fp32,  norm_w [d] fp32
+ *      mixes            [n, (2+hc)*hc] fp32: [pre 0:hc | post hc:2hc | comb 2hc:, row-major j*hc+k]
+ *      pre, post, pre_mix  [n, hc] fp32;  comb [n, hc, hc] fp32 (row j = input stream, column k = output stream)
+ *  - Every pointer must be 16-byte aligned (HC_ERR_MISALIGNED otherwise).
+ *  - Work is enqueued on `stream` (0 = legacy default stream) and is
+ *    asynchronous; results are ready when the stream reaches that point.
+ *  - Arguments are validated on the host before any launch; an invalid call
+ *    launches nothing and returns a non-zero status.  n == 0 is valid and
+ *    does nothing.  A failed launch returns HC_ERR_CUDA and records the CUDA
+ *    error code for hc_last_cuda_error() (per host thread).
+ *  - Compiled fast paths: hc == 4 and d a positive multiple of 64 with
+ *    d <= 16384; anything else returns HC_ERR_UNSUPPORTED.
+ *  - Output ranges must not overlap input ranges or each other
+ *    (HC_ERR_ALIAS), except where an entry point says otherwise.
+ */
+#ifndef HC_H_
+#define HC_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    HC_OK = 0,
+    HC_ERR_INVALID_ARG = 1,  /* null pointer, negative size, iters < 1, non-finite or negative eps */
+    HC_ERR_UNSUPPORTED = 2,  /* hc != 4, or d not a multiple of 64 in [64, 16384] */
+    HC_ERR_MISALIGNED = 3,   /* a pointer that is not 16-byte aligned */
+    HC_ERR_ALIAS = 4,        /* an output range overlaps an input or another output */
+    HC_ERR_CUDA = 5          /* a CUDA runtime call failed; see hc_last_cuda_error() */
+} hc_status;
+
+/* Static, never-freed description of a status code. */
+const char *hc_status_string(hc_status status);
+
+/* The cudaError_t value behind the last HC_ERR_CUDA on this host thread (0 if none). */
+int hc_last_cuda_error(void);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int hc_version(void);
+
+/*
+ * a1-a3 (DeepSeek-V4.1 Block page, Block.hc_mixes, and the "Stream
+ * combination" page's hc_split_sinkhorn): from the streams x of n tokens,
+ * the 24 mix numbers (one rsqrt statistic over all hc*d values per token,
+ * applied after the projection), then pre, post and the Sinkhorn comb.
+ *   x          [n, hc, d] bf16            in
+ *   hc_fn      [(2+hc)*hc, hc*d] fp32     in
+ *   hc_scale   [3] fp32, hc_base [(2+hc)*hc] fp32  in
+ *   pre, post  [n, hc] fp32  out;  comb [n, hc, hc] fp32  out
+ *   mixes_out  [n, (2+hc)*hc] fp32 out, optional (NULL: not written)
+ *   sinkhorn_iters >= 1 (20 in the released model); eps = hc_eps (1e-6);
+ *   norm_eps (1e-20).
+ */
+hc_status hc_mixes(const uint16_t *x, const float *hc_fn, const float *hc_scale,
+                   const float *hc_base, int64_t n, int hc, int d, int sinkhorn_iters,
+                   float eps, float norm_eps, float *pre, float *post, float *comb,
+                   float *mixes_out, cudaStream_t stream);
+
+/*
+ * a2-a3 only ("Stream combination" page, hc_split_sinkhorn kernel and
+ * wrapper): mixes [n, (2+hc)*hc] fp32 -> pre [n, hc], post [n, hc],
+ * comb [n, hc, hc] (all fp32).  pre = sigmoid(m*s0 + b) + eps;
+ * post = 2 sigmoid(m*s1 + b); comb = row softmax + eps, one column
+ * normalisation, then (iters - 1) rounds of row and column normalisation,
+ * each dividing by (sum + eps).  d is not involved.
+ */
+hc_status hc_split_sinkhorn(const float *mixes, const float *hc_scale, const float *hc_base,
+                            int64_t n, int hc, int sinkhorn_iters, float eps, float *pre,
+                            float *post, float *comb, cudaStream_t stream);
+
+/*
+ * a4 + a5 (Block page, Block.hc_pre then attn_norm / ffn_norm): collapse the
+ * streams under pre_mix in fp32, round to bf16, then RMSNorm over d with
+ * eps = norm_eps and fp32 gain norm_w, rounding the result to bf16.
+ *   x [n, hc, d] bf16, pre_mix [n, hc] fp32, norm_w [d] fp32  in
+ *   out [n, d] bf16  out
+ */
+hc_status hc_pre_norm(const uint16_t *x, const float *pre_mix, const float *norm_w, int64_t n,
+                      int hc, int d, float norm_eps, uint16_t *out, cudaStream_t stream);
+
+/*
+ * a6 (Block page, Block.hc_post): y[t,k,:] = bf16(post[t,k] * f[t,:] +
+ * sum_j comb[t,j,k] * residual[t,j,:]), in fp32.
+ *   f [n, d] bf16, residual [n, hc, d] bf16, post [n, hc], comb [n, hc, hc] fp32  in
+ *   y [n, hc, d] bf16  out (must not overlap any input)
+ */
+hc_status hc_post(const uint16_t *f, const uint16_t *residual, const float *post,
+                  const float *comb, int64_t n, int hc, int d, uint16_t *y,
+                  cudaStream_t stream);
+
+/*
+ * One fused side step a1-a6 (Block page, Block.forward; the diagram's
+ * "Single-Pass mHC" block): coefficients from this side's x; the sublayer
+ * input read with pre_mix handed in from the previous side; the sublayer
+ * output f (given) expanded with this side's post and comb.
+ *   x [n, hc, d] bf16, pre_mix [n, hc] fp32, f [n, d] bf16, hc_fn, hc_scale,
+ *   hc_base, norm_w (as above)                                        in
+ *   h_norm [n, d] bf16     out: RMSNorm(hc_pre(x, pre_mix)) -- the sublayer input
+ *   y [n, hc, d] bf16      out: hc_post(f, x, post, comb) -- the next residual
+ *   pre_out [n, hc] fp32   out: this side's pre (the next side's pre_mix)
+ *   post_out [n, hc], comb_out [n, hc, hc] fp32  out, optional (NULL: not written)
+ * In a model f depends on h_norm; this fused form takes f as an input (the
+ * sublayer body is not part of this path).
+ */
+hc_status hc_block_step(const uint16_t *x, const float *pre_mix, const uint16_t *f,
+                        const float *hc_fn, const float *hc_scale, const float *hc_base,
+                        const float *norm_w, int64_t n, int hc, int d, int sinkhorn_iters,
+                        float eps, float norm_eps, uint16_t *h_norm, uint16_t *y,
+                        float *pre_out, float *post_out, float *comb_out,
+                        cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HC_H_ */

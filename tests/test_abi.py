@@ -1,0 +1,133 @@
+"""The C ABI without a GPU: the library loads, exports every symbol that
+include/hc.h declares, and its host-side validation rejects bad arguments
+before any launch (no CUDA call is made on these paths)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from hyper_connection_residual_mixes_gb300 import _lib
+from hyper_connection_residual_mixes_gb300 import build as hc_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "hc.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    hc_build.build()
+    return _lib.load()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(hc_\w+)\s*\(", src, flags=re.M)))
+
+
+def test_header_declares_the_five_entry_points():
+    names = declared_functions()
+    for n in ("hc_mixes", "hc_split_sinkhorn", "hc_pre_norm", "hc_post", "hc_block_step",
+              "hc_status_string", "hc_last_cuda_error", "hc_version"):
+        assert n in names, n
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", _lib.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\s[TW]\s+(\w+)$", out, flags=re.M))
+    for name in declared_functions():
+        assert name in exported, "%s declared in hc.h but not exported" % name
+        getattr(lib, name)  # resolvable through ctypes too
+    # the binding knows every declared entry point, with the same name
+    assert set(declared_functions()) == set(_lib.SIGNATURES)
+
+
+def test_status_strings(lib):
+    for code, name in _lib.STATUS.items():
+        s = lib.hc_status_string(code).decode()
+        assert s.startswith(name)
+    assert lib.hc_last_cuda_error() == 0
+    assert lib.hc_version() >= 100
+
+
+FAKE = 0x10000  # 16-byte aligned, never dereferenced: validation fails first
+FAKE2 = 0x20000
+
+
+def _block(**kw):
+    a = dict(x=FAKE, pre_mix=FAKE + 0x100000, f=FAKE + 0x200000, hc_fn=FAKE + 0x300000,
+             hc_scale=FAKE + 0x400000, hc_base=FAKE + 0x500000, norm_w=FAKE + 0x600000,
+             n=16, hc=4, d=5120, iters=20, eps=1e-6, norm_eps=1e-20, h_norm=FAKE2 * 0x100,
+             y=FAKE2 * 0x200, pre_out=FAKE2 * 0x300, post_out=None, comb_out=None, stream=None)
+    a.update(kw)
+    return _lib.raw("hc_block_step", a["x"], a["pre_mix"], a["f"], a["hc_fn"], a["hc_scale"],
+                    a["hc_base"], a["norm_w"], a["n"], a["hc"], a["d"], a["iters"], a["eps"],
+                    a["norm_eps"], a["h_norm"], a["y"], a["pre_out"], a["post_out"],
+                    a["comb_out"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(n=-1), 1),
+    (dict(hc=3), 2),
+    (dict(hc=0), 1),
+    (dict(d=5121), 2),
+    (dict(d=32), 2),
+    (dict(d=32768), 2),
+    (dict(d=0), 1),
+    (dict(iters=0), 1),
+    (dict(eps=-1.0), 1),
+    (dict(eps=float("nan")), 1),
+    (dict(norm_eps=float("inf")), 1),
+    (dict(x=None), 1),
+    (dict(pre_out=None), 1),
+    (dict(f=None), 1),
+    (dict(x=FAKE + 8), 3),
+    (dict(post_out=FAKE2 * 0x400 + 4), 3),
+    (dict(y=FAKE + 64), 4),                       # y overlaps x
+    (dict(pre_out=FAKE2 * 0x100 + 16), 4),        # pre_out overlaps h_norm
+])
+def test_block_step_validation(lib, kw, expect):
+    assert _block(**kw) == expect
+
+
+def test_block_step_empty_is_ok(lib):
+    assert _block(n=0, x=None, y=None) == 0
+
+
+def test_split_sinkhorn_validation(lib):
+    r = lambda **kw: _lib.raw("hc_split_sinkhorn", kw.get("mixes", FAKE), FAKE + 0x1000,
+                              FAKE + 0x2000, kw.get("n", 4), kw.get("hc", 4), kw.get("iters", 20),
+                              kw.get("eps", 1e-6), kw.get("pre", FAKE2), FAKE2 + 0x1000,
+                              FAKE2 + 0x2000, None)
+    assert r(n=0) == 0
+    assert r(n=-3) == 1
+    assert r(hc=2) == 2
+    assert r(iters=0) == 1
+    assert r(mixes=None) == 1
+    assert r(mixes=FAKE + 4) == 3
+    assert r(pre=FAKE + 16) == 4
+
+
+def test_pre_norm_and_post_validation(lib):
+    assert _lib.raw("hc_pre_norm", FAKE, FAKE + 0x100000, FAKE + 0x200000, 2, 4, 5120, 1e-20,
+                    FAKE + 0x100, None) == 4  # out overlaps x
+    assert _lib.raw("hc_pre_norm", FAKE, FAKE + 0x100000, FAKE + 0x200000, 2, 4, 100, 1e-20,
+                    FAKE2 * 0x100, None) == 2
+    assert _lib.raw("hc_post", FAKE, FAKE + 0x100000, FAKE + 0x200000, FAKE + 0x300000, 2, 4,
+                    5120, None, None) == 1
+    assert _lib.raw("hc_post", FAKE, FAKE + 0x100000, FAKE + 0x200000, FAKE + 0x300000, 2, 4,
+                    5120, FAKE + 0x100010, None) == 4
+    assert _lib.raw("hc_mixes", FAKE, FAKE + 0x100000, FAKE + 0x200000, FAKE + 0x300000, 2, 4,
+                    5120, 20, 1e-6, 1e-20, FAKE2 * 0x100, FAKE2 * 0x200, FAKE2 * 0x300,
+                    FAKE2 * 0x300 + 8, None) == 3
+
+
+def test_binding_rejects_cpu_tensors():
+    import torch
+    import hyper_connection_residual_mixes_gb300 as hcg
+    x = torch.zeros(2, 4, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA"):
+        hcg.hc_pre_norm(x, torch.zeros(2, 4), torch.ones(64))
