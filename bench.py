@@ -144,10 +144,23 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- our arm
-def build_workload(device, rank):
-    seed = 4 + 1000 * rank  # rank 0 runs exactly the long-prefill seed
-    case = inputs.long_prefill(device=device, seed=seed, materialize_f=False)
-    fs = [inputs.long_prefill_f(s, case.n, case.d, device, seed) for s in range(SIDES)]
+WORKLOADS = {
+    # name: (generator, base seed, description)
+    "long_prefill": (None, 4, "B=4, T=16384 (65,536 tokens), 40 layers = 80 side steps"),
+    "prefill": (inputs.prefill, 3, "B=1, T=8192, outliers, attention + FFN side"),
+    "decode": (inputs.decode, 1, "B=128, T=1, attention + FFN side"),
+}
+
+
+def build_workload(device, rank, name="long_prefill"):
+    gen, base_seed, _ = WORKLOADS[name]
+    seed = base_seed + 1000 * rank  # rank 0 runs exactly the workload's seed
+    if name == "long_prefill":
+        case = inputs.long_prefill(device=device, seed=seed, materialize_f=False)
+        fs = [inputs.long_prefill_f(s, case.n, case.d, device, seed) for s in range(SIDES)]
+    else:
+        case = gen(device=device, seed=seed)
+        fs = case.fs
     return case, fs, seed
 
 
@@ -155,8 +168,9 @@ def run_ours(args, rank, local_rank, world):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     hcg._lib.load()
-    case, fs, seed = build_workload(dev, rank)
+    case, fs, seed = build_workload(dev, rank, args.workload)
     n, d = case.n, case.d
+    sides = len(case.params)
     x0, pm0 = case.x, case.pre_mix
     ys = [torch.empty_like(x0), torch.empty_like(x0)]
     pres = [torch.empty((n, HC), device=dev), torch.empty((n, HC), device=dev)]
@@ -167,7 +181,7 @@ def run_ours(args, rank, local_rank, world):
 
     def step(events=None):
         x, pm = x0, pm0
-        for s in range(SIDES):
+        for s in range(sides):
             if events is not None:
                 events[s][0].record(stream)
             hcg.hc_block_step(x, pm, fs[s], *params[s], h_norm=h_norm, y=ys[s % 2],
@@ -188,7 +202,7 @@ def run_ours(args, rank, local_rank, world):
     clocks.start()
     time.sleep(0.3)
     ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(SIDES)] for _ in range(args.steps)]
+           for _ in range(sides)] for _ in range(args.steps)]
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
@@ -207,7 +221,8 @@ def run_ours(args, rank, local_rank, world):
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         elapsed_ms = float(t.item())
 
-    e2e = None if args.no_e2e else run_e2e(args, dev, case, seed, world)
+    e2e = None if (args.no_e2e or args.workload != "long_prefill") else \
+        run_e2e(args, dev, case, seed, world)
     out = None
     if rank == 0:
         ms_per_step = elapsed_ms / args.steps
@@ -216,10 +231,12 @@ def run_ours(args, rank, local_rank, world):
         alg_bytes = n * BYTES_PER_TOKEN + BYTES_WEIGHTS
         achieved = alg_bytes / avg_launch_s / 1e9
         peak, peak_kind = measured_peaks()
-        step_bytes = SIDES * alg_bytes
+        step_bytes = sides * alg_bytes
         out = {
             "metric": "tokens/s (65,536-token long prefill through 40 layers = 80 fused "
-                      "hc_block_step side steps) and achieved HBM GB/s",
+                      "hc_block_step side steps) and achieved HBM GB/s"
+                      if args.workload == "long_prefill" else
+                      "tokens/s through the %s workload's %d side steps" % (args.workload, sides),
             "value": tokens_per_s,
             "unit": "tokens/s",
             "n_gpus": world,
@@ -231,11 +248,14 @@ def run_ours(args, rank, local_rank, world):
             "vs_baseline": None,
             "dtype": "bf16 streams, fp32 arithmetic",
             "data": "synthetic, seeded (x N(0,1); hc_fn N(0,0.01); f N(0,2); per-side params)",
-            "config": {"workload": "long_prefill", "batch": 4, "seq_len": 16384,
-                       "tokens": n, "hc": HC, "d": d, "layers": LAYERS, "side_steps": SIDES,
+            "config": {"workload": args.workload, "description": WORKLOADS[args.workload][2],
+                       "tokens": n, "hc": HC, "d": d, "side_steps": sides,
                        "sinkhorn_iters": 20, "seed": seed, "parallelism": "replicas" if world > 1 else "single",
-                       "l2": "inputs larger than L2 (x is %.1f GB per side, L2 %.0f MB); no flush"
-                             % (n * HC * d * 2 / 1e9, L2_BYTES / 1e6)},
+                       "l2": ("inputs larger than L2 (x is %.2f GB per side, L2 %.0f MB); no flush"
+                              % (n * HC * d * 2 / 1e9, L2_BYTES / 1e6))
+                             if n * HC * d * 2 > L2_BYTES else
+                             "inputs smaller than L2 (%.1f MB per side); not flushed: latency case"
+                             % (n * HC * d * 2 / 1e6)},
             "hbm_gbs_step": step_bytes / (ms_per_step / 1e3) / 1e9,
             "hbm_frac_step": step_bytes / (ms_per_step / 1e3) / 1e9 / peak,
             "roofline": {"kernel": KERNEL_NAME, "bound": "hbm", "achieved": achieved,
@@ -249,7 +269,7 @@ def run_ours(args, rank, local_rank, world):
             "gpu_launches": gpu_launches,
             "e2e": e2e,
         }
-        if world == 1 and not args.no_cpu_baseline:
+        if world == 1 and not args.no_cpu_baseline and args.workload == "long_prefill":
             out["cpu_baseline"] = cpu_baseline_sample(case, fs, target_s=args.cpu_seconds)
     return out
 
@@ -419,6 +439,8 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="long_prefill",
+                    help="long_prefill is the benchmark; the others serve profiling")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling runs)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)

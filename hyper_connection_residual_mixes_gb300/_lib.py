@@ -27,6 +27,7 @@ SIGNATURES = {
     "hc_status_string": [I32],
     "hc_last_cuda_error": [],
     "hc_version": [],
+    "hc_consume_device_error": [P],
     "hc_mixes": [P, P, P, P, I64, I32, I32, I32, F32, F32, P, P, P, P, P],
     "hc_split_sinkhorn": [P, P, P, I64, I32, I32, F32, P, P, P, P],
     "hc_pre_norm": [P, P, P, I64, I32, I32, F32, P, P],
@@ -41,6 +42,7 @@ STATUS = {
     3: "HC_ERR_MISALIGNED",
     4: "HC_ERR_ALIAS",
     5: "HC_ERR_CUDA",
+    6: "HC_ERR_TIMEOUT",
 }
 
 

@@ -77,6 +77,7 @@ const char *hc_status_string(hc_status status) {
         case HC_ERR_MISALIGNED: return "HC_ERR_MISALIGNED: every pointer must be 16-byte aligned";
         case HC_ERR_ALIAS: return "HC_ERR_ALIAS: an output overlaps an input or another output";
         case HC_ERR_CUDA: return "HC_ERR_CUDA: a CUDA call failed (see hc_last_cuda_error)";
+        case HC_ERR_TIMEOUT: return "HC_ERR_TIMEOUT: a kernel gave up waiting on a barrier";
     }
     return "unknown hc_status";
 }
@@ -84,6 +85,13 @@ const char *hc_status_string(hc_status status) {
 int hc_last_cuda_error(void) { return g_last_cuda_error; }
 
 int hc_version(void) { return 100; }
+
+hc_status hc_consume_device_error(cudaStream_t stream) {
+    unsigned int flag = 0;
+    hc_status st = cuda_status(hc::consume_device_error(stream, &flag));
+    if (st != HC_OK) return st;
+    return flag ? HC_ERR_TIMEOUT : HC_OK;
+}
 
 hc_status hc_split_sinkhorn(const float *mixes, const float *hc_scale, const float *hc_base,
                             int64_t n, int hc, int sinkhorn_iters, float eps, float *pre,
@@ -124,6 +132,11 @@ hc_status hc_mixes(const uint16_t *x, const float *hc_fn, const float *hc_scale,
     const Span outs[] = {span(pre, n * hc * 4), span(post, n * hc * 4),
                          span(comb, n * hc * hc * 4), span(mixes_out, mixes_out ? n * mix * 4 : 0)};
     if ((st = check_alias(outs, 4, ins, 4)) != HC_OK) return st;
+    if (hc::cluster_path_supported(d))
+        return cuda_status(hc::launch_block_cluster(x, nullptr, nullptr, hc_fn, hc_scale, hc_base,
+                                                    nullptr, n, d, sinkhorn_iters, eps, norm_eps,
+                                                    nullptr, nullptr, pre, post, comb, mixes_out,
+                                                    stream));
     return cuda_status(hc::launch_tokens_simple(x, nullptr, nullptr, hc_fn, hc_scale, hc_base,
                                                 nullptr, n, d, sinkhorn_iters, eps, norm_eps,
                                                 nullptr, nullptr, pre, post, comb, mixes_out,
@@ -190,6 +203,10 @@ hc_status hc_block_step(const uint16_t *x, const float *pre_mix, const uint16_t 
                          span(post_out, post_out ? n * hc * 4 : 0),
                          span(comb_out, comb_out ? n * hc * hc * 4 : 0)};
     if ((st = check_alias(outs, 5, ins, 7)) != HC_OK) return st;
+    if (hc::cluster_path_supported(d))
+        return cuda_status(hc::launch_block_cluster(x, pre_mix, f, hc_fn, hc_scale, hc_base, norm_w,
+                                                    n, d, sinkhorn_iters, eps, norm_eps, h_norm, y,
+                                                    pre_out, post_out, comb_out, nullptr, stream));
     return cuda_status(hc::launch_tokens_simple(x, pre_mix, f, hc_fn, hc_scale, hc_base, norm_w, n,
                                                 d, sinkhorn_iters, eps, norm_eps, h_norm, y,
                                                 pre_out, post_out, comb_out, nullptr, stream));

@@ -1,0 +1,700 @@
+// hc_block_cluster.cu -- the fused hyper-connection side step for GB300.
+//
+// What it computes (DeepSeek-V4.1 Block page, Code section: Block.hc_mixes,
+// Block.hc_pre, Block.hc_post; "Stream combination" page: hc_split_sinkhorn):
+// per token, the 24 mix numbers from the flattened streams and one
+// rsqrt(mean(x^2) + norm_eps) statistic, split + Sinkhorn into pre/post/comb,
+// h = bf16(sum_s pre_mix[s] x[s]), h_norm = bf16(RMSNorm(h) * w) and
+// y[k] = bf16(post[k] f + sum_j comb[j][k] x[j]).
+//
+// How (one launch per side step, persistent thread-block clusters):
+//  * A cluster of kC = 16 CTAs (one per SM) splits the model dimension d into
+//    16 column slices; CTA `rank` owns columns [rank*d/16, (rank+1)*d/16) of
+//    each of the 4 streams.  Its slice of hc_fn (24 rows x 4*d/16 columns,
+//    fp32) stays resident in shared memory for the whole launch, so the
+//    projection weights are read from memory once per CTA, not once per token.
+//  * A cluster walks 64-token tiles.  Each tile's streams pass through a
+//    3-slot TMA ring (32 columns x 64 tokens x 4 streams per slot, 64-byte
+//    swizzle) twice: phase 1 (the projection, sum of squares, and the sum of
+//    squares of the bf16-rounded h) and phase 3 (y and h_norm).  The second
+//    read comes from L2 (the first read is tagged evict_last, the second
+//    evict_first); phase 1 of the next tile runs between them so the
+//    cross-CTA reduction of a tile is hidden behind useful streaming.
+//  * The 24 x (4*d/16) projection runs on the tensor cores with
+//    mma.sync m16n8k16 (bf16 in, fp32 accumulate).  hc_fn is fp32; each
+//    weight is split on the fly into three bf16 parts (hi + mid + lo) whose
+//    sum equals the fp32 weight to ~2^-24, and all three products accumulate
+//    into the same fp32 sums.  x is bf16 and enters the MMA exactly.
+//  * Partial sums (24 dots, sum x^2, sum h^2) of each token go to the token's
+//    owner CTA through distributed shared memory with cluster-scope mbarrier
+//    arrivals; the owner finishes the statistics, runs the split + 20-round
+//    Sinkhorn in registers, writes pre/post/comb, and broadcasts post, comb
+//    and the RMSNorm scale back to all 16 CTAs.
+//
+// Warp roles (256 threads): warp 0 TMA producer; warps 1-2 tensor-core MMA
+// (each a half of every slot's K range, all 64 tokens); warp 3 owner-side
+// reduction + Sinkhorn + broadcast; warps 4-7 CUDA-core streaming math.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "hc_device.cuh"
+#include "hc_launch.h"
+#include "hc_ptx.cuh"
+
+namespace hc {
+
+namespace cl {
+
+constexpr int kC = 16;          // CTAs per cluster = column slices of d
+constexpr int kT = 64;          // tokens per tile
+constexpr int kCB = 32;         // columns per slot (per stream)
+constexpr int kSlots = 3;       // TMA ring depth
+constexpr int kThreads = 256;
+constexpr int kBoxBytes = kT * kCB * 2;             // 4096: 64 tokens x 32 bf16
+constexpr int kStageXBytes = kHC * kBoxBytes;       // 16384
+constexpr int kSlotBytes = kStageXBytes + kBoxBytes;  // + f box = 20480
+constexpr int kTokPerOwner = kT / kC;               // 4
+constexpr int kPartF = 28;      // 24 partial dots, sum x^2, sum h^2, 2 pad
+constexpr int kCoefF = 24;      // post[4], comb[16], rs_h, 3 pad
+constexpr int kWarpProducer = 0;
+constexpr int kWarpMma = 1;     // warps 1, 2
+constexpr int kWarpReducer = 3;
+constexpr int kWarpCuda = 4;    // warps 4..7
+
+struct Params {
+    const float *pre_mix;
+    const float *hc_fn;
+    const float *hc_scale;
+    const float *hc_base;
+    const float *norm_w;
+    uint16_t *h_norm;
+    uint16_t *y;
+    float *pre_out;
+    float *post_out;
+    float *comb_out;
+    float *mixes_out;
+    int64_t n;
+    int d;
+    int iters;
+    float eps;
+    float norm_eps;
+    int num_tiles;
+};
+
+// Shared-memory layout (byte offsets from a 1024-aligned base).
+struct Layout {
+    int dc;        // columns per CTA per stream = d / 16
+    int ncb;       // slots per tile = dc / 32
+    int wstr;      // hc_fn row stride in floats (4*dc + 8: conflict-free 8-byte loads)
+    int off_w, off_coef, off_part, off_mma, off_normw, off_bar, total;
+};
+
+__host__ __device__ inline Layout make_layout(int d) {
+    Layout L;
+    L.dc = d / kC;
+    L.ncb = L.dc / kCB;
+    L.wstr = kHC * L.dc + 8;
+    int o = kSlots * kSlotBytes;
+    L.off_w = o;
+    o += kMix * L.wstr * 4;
+    L.off_coef = o;
+    o += 2 * kT * kCoefF * 4;
+    L.off_part = o;
+    o += 2 * kC * kTokPerOwner * kPartF * 4;
+    L.off_mma = o;
+    o += 2 * kT * kMix * 4;
+    L.off_normw = o;
+    o += L.dc * 4;
+    o = (o + 15) & ~15;
+    L.off_bar = o;
+    o += 16 * 8;
+    L.total = o + 1024;  // slack for aligning the base
+    return L;
+}
+
+// Split an fp32 pair into three bf16x2 parts with hi + mid + lo == w to ~2^-24.
+__device__ __forceinline__ void split3(float w0, float w1, uint32_t &hi, uint32_t &mid, uint32_t &lo) {
+    hi = pack_bf16x2(w0, w1);
+    const float r0 = w0 - bf16lo(hi), r1 = w1 - bf16hi(hi);
+    mid = pack_bf16x2(r0, r1);
+    const float s0 = r0 - bf16lo(mid), s1 = r1 - bf16hi(mid);
+    lo = pack_bf16x2(s0, s1);
+}
+
+// Byte offset of (row r, 16-byte unit u) inside a 64-byte-swizzled box of 64-byte rows.
+__device__ __forceinline__ uint32_t sw64(int r, int u) {
+    return (uint32_t)(r * 64 + ((u ^ ((r >> 1) & 3)) << 4));
+}
+
+// The ring walks, per cluster, the sequence P1(0), P1(1), P3(0), P1(2), P3(1), ...
+// with `ncb` slots per phase.  Use u -> (phase-3?, local tile j, column block cb).
+struct Use {
+    bool p3;
+    int j;
+    int cb;
+};
+__device__ __forceinline__ Use decode_use(int u, int ncb, int J, bool full) {
+    Use r;
+    if (!full) {
+        r.p3 = false;
+        r.j = u / ncb;
+        r.cb = u % ncb;
+        return r;
+    }
+    // group g: P1(g) (if g < J) followed by P3(g-1) (if g >= 1)
+    if (u < ncb) {
+        r.p3 = false; r.j = 0; r.cb = u;
+        return r;
+    }
+    const int v = u - ncb;
+    const int g = 1 + v / (2 * ncb);
+    const int w = v % (2 * ncb);
+    if (g < J) {
+        if (w < ncb) { r.p3 = false; r.j = g; r.cb = w; }
+        else         { r.p3 = true;  r.j = g - 1; r.cb = w - ncb; }
+    } else {
+        r.p3 = true; r.j = J - 1; r.cb = w;
+    }
+    return r;
+}
+__device__ __forceinline__ int total_uses(int ncb, int J, bool full) {
+    return full ? 2 * ncb * J : ncb * J;
+}
+
+template <bool kFull>
+__global__ void __launch_bounds__(kThreads, 1)
+k_block_cluster(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_f,
+                const Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~uintptr_t(1023));
+    __shared__ volatile int s_abort;
+    const Layout L = make_layout(p.d);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const int cid = (int)cluster_id_x(), ncl = (int)cluster_count_x();
+    const int J = (p.num_tiles > cid) ? (p.num_tiles - cid + ncl - 1) / ncl : 0;
+    const int ncb = L.ncb, dc = L.dc, d = p.d;
+    const int64_t K = (int64_t)kHC * d;
+    const int U = total_uses(ncb, J, kFull);
+
+    float *sW = reinterpret_cast<float *>(smem + L.off_w);
+    float *sCoef = reinterpret_cast<float *>(smem + L.off_coef);
+    float *sPart = reinterpret_cast<float *>(smem + L.off_part);
+    float *sMma = reinterpret_cast<float *>(smem + L.off_mma);
+    float *sNormW = reinterpret_cast<float *>(smem + L.off_normw);
+    const uint32_t bar0 = smem_u32(smem + L.off_bar);
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (kSlots + s); };
+    auto part_bar = [&](int b) { return bar0 + 8u * (2 * kSlots + b); };
+    auto coef_bar = [&](int b) { return bar0 + 8u * (2 * kSlots + 2 + b); };
+    // the two MMA warps meet twice per tile: before reading each other's sums, and
+    // after the send (so neither rewrites its half while the other still reads it)
+    const uint32_t mma_bar = bar0 + 8u * (2 * kSlots + 4);
+    const uint32_t mma_bar2 = bar0 + 8u * (2 * kSlots + 5);
+    const uint32_t slot0 = smem_u32(smem);
+
+    if (threadIdx.x == 0) {
+        s_abort = 0;
+        for (int s = 0; s < kSlots; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 2 + 4);  // MMA warps + CUDA-core warps
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(part_bar(b), kC * (kT / kC) * (kFull ? 2 : 2));  // see the senders below
+            mbar_init(coef_bar(b), kC * 2);
+        }
+        mbar_init(mma_bar, 64);
+        mbar_init(mma_bar2, 64);
+        fence_mbar_init_cluster();
+    }
+    if (warp == kWarpProducer && lane == 0) {
+        prefetch_tmap(&tm_x);
+        if (kFull) prefetch_tmap(&tm_f);
+    }
+    // resident hc_fn slice: row i, local column s*dc + c  <-  global column s*d + rank*dc + c
+    {
+        const int q4 = dc / 4;  // float4 per stream per row
+        for (int idx = threadIdx.x; idx < kMix * kHC * q4; idx += kThreads) {
+            const int i = idx / (kHC * q4);
+            const int rem = idx % (kHC * q4);
+            const int s = rem / q4, c4 = rem % q4;
+            const float4 v = __ldg(reinterpret_cast<const float4 *>(
+                p.hc_fn + (int64_t)i * K + (int64_t)s * d + (int64_t)rank * dc + 4 * c4));
+            *reinterpret_cast<float4 *>(sW + i * L.wstr + s * dc + 4 * c4) = v;
+        }
+        if (kFull)
+            for (int c = threadIdx.x; c < dc; c += kThreads) sNormW[c] = __ldg(p.norm_w + rank * dc + c);
+    }
+    cluster_sync_all();  // barriers initialised and visible cluster-wide; W resident
+
+    if (warp == kWarpProducer) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            const uint64_t pol_keep = policy_evict_last(), pol_stream = policy_evict_first();
+            int armed = 0;
+            for (int u = 0; u < U; ++u) {
+                const int slot = u % kSlots;
+                const uint32_t ph = (uint32_t)(u / kSlots) & 1u;
+                if (!mbar_wait<false>(empty_bar(slot), ph ^ 1u, &s_abort)) break;
+                const Use us = decode_use(u, ncb, J, kFull);
+                const int tile = cid + us.j * ncl;
+                const int row = tile * kT;
+                const int col = (int)rank * dc + us.cb * kCB;
+                const uint32_t dst = slot0 + slot * kSlotBytes;
+                mbar_arrive_expect_tx(full_bar(slot), us.p3 ? kSlotBytes : kStageXBytes);
+                for (int s = 0; s < kHC; ++s)
+                    tma_load_2d(dst + s * kBoxBytes, &tm_x, full_bar(slot), s * d + col, row,
+                                us.p3 ? pol_stream : pol_keep);
+                if (us.p3) tma_load_2d(dst + kStageXBytes, &tm_f, full_bar(slot), col, row, pol_stream);
+                armed = u + 1;
+            }
+            // no copy may still be landing when the CTA leaves: wait (bounded) for the
+            // last armed uses of every slot
+            for (int u = (armed > kSlots ? armed - kSlots : 0); u < armed; ++u)
+                mbar_wait<false>(full_bar(u % kSlots), (uint32_t)(u / kSlots) & 1u, &s_abort);
+        }
+    } else if (warp == kWarpMma || warp == kWarpMma + 1) {
+        // ------------------------------------------------------------ tensor-core projection
+        const int mw = warp - kWarpMma;  // streams 2*mw, 2*mw+1
+        const int g = lane >> 2, t = lane & 3;
+        float acc[4][3][4];
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+            for (int b = 0; b < 3; ++b)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) acc[a][b][c] = 0.0f;
+        int tiles_done = 0;
+        for (int u = 0; u < U; ++u) {
+            const int slot = u % kSlots;
+            const uint32_t ph = (uint32_t)(u / kSlots) & 1u;
+            if (!mbar_wait_warp<false>(full_bar(slot), ph, &s_abort)) break;
+            const Use us = decode_use(u, ncb, J, kFull);
+            if (!us.p3) {
+                const uint32_t sb = slot0 + slot * kSlotBytes;
+#pragma unroll
+                for (int si = 0; si < 2; ++si) {
+                    const int s = 2 * mw + si;
+                    const uint32_t box = sb + s * kBoxBytes;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int kb = s * dc + us.cb * kCB + h * 16;
+                        uint32_t bh[3][2], bm[3][2], bl[3][2];
+#pragma unroll
+                        for (int nt = 0; nt < 3; ++nt) {
+                            const float *wr = sW + (nt * 8 + g) * L.wstr + kb + 2 * t;
+                            const float2 p0 = *reinterpret_cast<const float2 *>(wr);
+                            const float2 p1 = *reinterpret_cast<const float2 *>(wr + 8);
+                            split3(p0.x, p0.y, bh[nt][0], bm[nt][0], bl[nt][0]);
+                            split3(p1.x, p1.y, bh[nt][1], bm[nt][1], bl[nt][1]);
+                        }
+#pragma unroll
+                        for (int mt = 0; mt < 4; ++mt) {
+                            const int r = mt * 16 + (lane & 15);
+                            uint32_t a0, a1, a2, a3;
+                            ldmatrix_x4(box + sw64(r, 2 * h + (lane >> 4)), a0, a1, a2, a3);
+#pragma unroll
+                            for (int nt = 0; nt < 3; ++nt) {
+                                mma_bf16_16816(acc[mt][nt], a0, a1, a2, a3, bl[nt][0], bl[nt][1]);
+                                mma_bf16_16816(acc[mt][nt], a0, a1, a2, a3, bm[nt][0], bm[nt][1]);
+                                mma_bf16_16816(acc[mt][nt], a0, a1, a2, a3, bh[nt][0], bh[nt][1]);
+                            }
+                        }
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty_bar(slot));
+            if (!us.p3 && us.cb == ncb - 1) {
+                // tile finished: combine the two K halves, send each token's 24 partial
+                // dots to its owner CTA
+                float *mine = sMma + mw * kT * kMix;
+#pragma unroll
+                for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+                    for (int nt = 0; nt < 3; ++nt) {
+                        const int r = mt * 16 + g, c = nt * 8 + 2 * t;
+                        *reinterpret_cast<float2 *>(mine + r * kMix + c) = make_float2(acc[mt][nt][0], acc[mt][nt][1]);
+                        *reinterpret_cast<float2 *>(mine + (r + 8) * kMix + c) = make_float2(acc[mt][nt][2], acc[mt][nt][3]);
+                        acc[mt][nt][0] = acc[mt][nt][1] = acc[mt][nt][2] = acc[mt][nt][3] = 0.0f;
+                    }
+                mbar_arrive(mma_bar);
+                if (!mbar_wait_warp<false>(mma_bar, (uint32_t)tiles_done & 1u, &s_abort)) break;
+                const int tk = mw * 32 + lane;          // token within the tile
+                const int owner = tk / kTokPerOwner, tl = tk % kTokPerOwner;
+                const int buf = us.j & 1;
+                const float *a = sMma + tk * kMix, *b = sMma + kT * kMix + tk * kMix;
+                const uint32_t dst = mapa(smem_u32(sPart + ((buf * kC + rank) * kTokPerOwner + tl) * kPartF), owner);
+#pragma unroll
+                for (int q = 0; q < kMix / 4; ++q)
+                    st_cluster_v4(dst + 16 * q, a[4 * q] + b[4 * q], a[4 * q + 1] + b[4 * q + 1],
+                                  a[4 * q + 2] + b[4 * q + 2], a[4 * q + 3] + b[4 * q + 3]);
+                mbar_arrive_remote(mapa(part_bar(buf), owner));
+                mbar_arrive(mma_bar2);
+                const bool met = mbar_wait_warp<false>(mma_bar2, (uint32_t)tiles_done & 1u, &s_abort);
+                ++tiles_done;
+                if (!met) break;
+            }
+        }
+    } else if (warp == kWarpReducer) {
+        // ------------------------------------------------------------ owner: statistics + Sinkhorn
+        const float s0 = __ldg(p.hc_scale), s1 = __ldg(p.hc_scale + 1), s2 = __ldg(p.hc_scale + 2);
+        for (int j = 0; j < J; ++j) {
+            const int buf = j & 1;
+            if (!mbar_wait_warp<true>(part_bar(buf), (uint32_t)(j >> 1) & 1u, &s_abort)) break;
+            const int tile = cid + j * ncl;
+            // lanes 0..3: one owned token each; the others mirror lane & 3
+            const int tl = lane & 3;
+            const int tk = (int)rank * kTokPerOwner + tl;
+            const int64_t tok = (int64_t)tile * kT + tk;
+            float m[kMix];
+#pragma unroll
+            for (int i = 0; i < kMix; ++i) m[i] = 0.0f;
+            float ssx = 0.0f, ssh = 0.0f;
+            for (int src = 0; src < kC; ++src) {
+                const float *e = sPart + ((buf * kC + src) * kTokPerOwner + tl) * kPartF;
+#pragma unroll
+                for (int i = 0; i < kMix; ++i) m[i] += e[i];
+                ssx += e[kMix];
+                ssh += e[kMix + 1];
+            }
+            const float r = rsqrtf(ssx / (float)K + p.norm_eps);
+#pragma unroll
+            for (int i = 0; i < kMix; ++i) m[i] *= r;
+            float pr[kHC], po[kHC], c[kHC * kHC];
+            split_sinkhorn_token(m, s0, s1, s2, p.hc_base, p.iters, p.eps, pr, po, c);
+            const float rs_h = rsqrtf(ssh / (float)d + p.norm_eps);
+            if (lane < kTokPerOwner && tok < p.n) {
+                if (p.pre_out) reinterpret_cast<float4 *>(p.pre_out)[tok] = make_float4(pr[0], pr[1], pr[2], pr[3]);
+                if (p.post_out) reinterpret_cast<float4 *>(p.post_out)[tok] = make_float4(po[0], po[1], po[2], po[3]);
+                if (p.comb_out) {
+                    float4 *cd = reinterpret_cast<float4 *>(p.comb_out + tok * kHC * kHC);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) cd[q] = make_float4(c[4 * q], c[4 * q + 1], c[4 * q + 2], c[4 * q + 3]);
+                }
+                if (p.mixes_out) {
+                    float4 *md = reinterpret_cast<float4 *>(p.mixes_out + tok * kMix);
+#pragma unroll
+                    for (int q = 0; q < kMix / 4; ++q) md[q] = make_float4(m[4 * q], m[4 * q + 1], m[4 * q + 2], m[4 * q + 3]);
+                }
+            }
+            if (kFull) {
+                // broadcast: lane l -> destination CTA l % 16, tokens 2*(l/16) + {0, 1}
+                const int dest = lane & 15;
+                const int ta = 2 * (lane >> 4);
+#pragma unroll
+                for (int k2 = 0; k2 < 2; ++k2) {
+                    const int tsel = ta + k2;  // owned token whose coefficients to send
+                    float v[kCoefF];
+#pragma unroll
+                    for (int i = 0; i < kCoefF; ++i) v[i] = 0.0f;
+                    // fetch token tsel's values from the lane that computed them (lane tsel)
+#pragma unroll
+                    for (int k = 0; k < kHC; ++k) v[k] = __shfl_sync(0xffffffffu, po[k], tsel);
+#pragma unroll
+                    for (int i = 0; i < kHC * kHC; ++i) v[kHC + i] = __shfl_sync(0xffffffffu, c[i], tsel);
+                    v[kHC + kHC * kHC] = __shfl_sync(0xffffffffu, rs_h, tsel);
+                    const int trow = (int)rank * kTokPerOwner + tsel;
+                    const uint32_t dst = mapa(smem_u32(sCoef + (buf * kT + trow) * kCoefF), dest);
+#pragma unroll
+                    for (int q = 0; q < kCoefF / 4; ++q)
+                        st_cluster_v4(dst + 16 * q, v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                }
+                mbar_arrive_remote(mapa(coef_bar(buf), dest));
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ CUDA-core streaming math
+        // 128 threads; per slot, thread tc handles the 8-column unit uu = tc % 4 of
+        // token rows tc / 4 and 32 + tc / 4, as four packed fp32 pairs per stream.
+        const int tc = threadIdx.x - kWarpCuda * 32;  // 0..127
+        const int uu = tc & 3;
+        const int r0 = tc >> 2, r1 = 32 + (tc >> 2);
+        f32x2 pm[2][kHC];   // pre_mix of the two tokens, duplicated into both lanes
+        f32x2 ssx2[2], ssh2[2];
+        float cf[2][kHC + kHC * kHC + 1];  // post, comb, RMSNorm scale of the two tokens
+        const f32x2 zero2 = f2_dup(0.0f);
+        ssx2[0] = ssx2[1] = ssh2[0] = ssh2[1] = zero2;
+        int cur_coef_tile = -1;
+        for (int u = 0; u < U; ++u) {
+            const int slot = u % kSlots;
+            const uint32_t ph = (uint32_t)(u / kSlots) & 1u;
+            if (!mbar_wait_warp<false>(full_bar(slot), ph, &s_abort)) break;
+            const Use us = decode_use(u, ncb, J, kFull);
+            const int tile = cid + us.j * ncl;
+            const uint8_t *sb = smem + slot * kSlotBytes;
+            if (us.cb == 0) {
+                // pre_mix of this thread's two tokens for the tile of this use
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const int64_t tok = (int64_t)tile * kT + (i ? r1 : r0);
+                    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (kFull && tok < p.n) v = __ldg(reinterpret_cast<const float4 *>(p.pre_mix) + tok);
+                    pm[i][0] = f2_dup(v.x); pm[i][1] = f2_dup(v.y);
+                    pm[i][2] = f2_dup(v.z); pm[i][3] = f2_dup(v.w);
+                }
+            }
+            if (!us.p3) {
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const int r = i ? r1 : r0;
+                    uint4 xr[kHC];
+#pragma unroll
+                    for (int s = 0; s < kHC; ++s)
+                        xr[s] = *reinterpret_cast<const uint4 *>(sb + s * kBoxBytes + sw64(r, uu));
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        f32x2 xs[kHC];
+#pragma unroll
+                        for (int s = 0; s < kHC; ++s) {
+                            const uint32_t w = q == 0 ? xr[s].x : q == 1 ? xr[s].y : q == 2 ? xr[s].z : xr[s].w;
+                            xs[s] = f2_from_bf16x2(w);
+                            ssx2[i] = f2_fma(xs[s], xs[s], ssx2[i]);
+                        }
+                        if (kFull) {
+                            f32x2 h = f2_mul(pm[i][0], xs[0]);
+                            h = f2_fma(pm[i][1], xs[1], h);
+                            h = f2_fma(pm[i][2], xs[2], h);
+                            h = f2_fma(pm[i][3], xs[3], h);
+                            const f32x2 hr = f2_from_bf16x2(f2_to_bf16x2(h));
+                            ssh2[i] = f2_fma(hr, hr, ssh2[i]);
+                        }
+                    }
+                }
+            } else {
+                const int buf = us.j & 1;
+                if (cur_coef_tile != us.j) {
+                    if (!mbar_wait_warp<true>(coef_bar(buf), (uint32_t)(us.j >> 1) & 1u, &s_abort)) break;
+                    cur_coef_tile = us.j;
+#pragma unroll
+                    for (int i = 0; i < 2; ++i) {
+                        const float *c = sCoef + (buf * kT + (i ? r1 : r0)) * kCoefF;
+#pragma unroll
+                        for (int q = 0; q < kHC + kHC * kHC + 1; ++q) cf[i][q] = c[q];
+                    }
+                }
+                const float4 *nw = reinterpret_cast<const float4 *>(sNormW + us.cb * kCB + uu * 8);
+                const float4 w0 = nw[0], w1 = nw[1];
+                const f32x2 wv[4] = {f2_make(w0.x, w0.y), f2_make(w0.z, w0.w), f2_make(w1.x, w1.y),
+                                     f2_make(w1.z, w1.w)};
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const int r = i ? r1 : r0;
+                    const int64_t tok = (int64_t)tile * kT + r;
+                    uint4 xr[kHC];
+#pragma unroll
+                    for (int s = 0; s < kHC; ++s)
+                        xr[s] = *reinterpret_cast<const uint4 *>(sb + s * kBoxBytes + sw64(r, uu));
+                    const uint4 fr = *reinterpret_cast<const uint4 *>(sb + kStageXBytes + sw64(r, uu));
+                    if (tok < p.n) {
+                        const int64_t cbase = (int64_t)rank * dc + us.cb * kCB + uu * 8;
+                        uint32_t yo[kHC][4], ho[4];
+                        const f32x2 rs2 = f2_dup(cf[i][kHC + kHC * kHC]);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            f32x2 xs[kHC];
+#pragma unroll
+                            for (int s = 0; s < kHC; ++s)
+                                xs[s] = f2_from_bf16x2(q == 0 ? xr[s].x : q == 1 ? xr[s].y : q == 2 ? xr[s].z : xr[s].w);
+                            const f32x2 fv = f2_from_bf16x2(q == 0 ? fr.x : q == 1 ? fr.y : q == 2 ? fr.z : fr.w);
+#pragma unroll
+                            for (int k = 0; k < kHC; ++k) {
+                                f32x2 a = f2_mul(f2_dup(cf[i][k]), fv);
+#pragma unroll
+                                for (int jj = 0; jj < kHC; ++jj)
+                                    a = f2_fma(f2_dup(cf[i][kHC + jj * kHC + k]), xs[jj], a);
+                                yo[k][q] = f2_to_bf16x2(a);
+                            }
+                            f32x2 h = f2_mul(pm[i][0], xs[0]);
+                            h = f2_fma(pm[i][1], xs[1], h);
+                            h = f2_fma(pm[i][2], xs[2], h);
+                            h = f2_fma(pm[i][3], xs[3], h);
+                            const f32x2 hr = f2_from_bf16x2(f2_to_bf16x2(h));
+                            ho[q] = f2_to_bf16x2(f2_mul(f2_mul(hr, rs2), wv[q]));
+                        }
+#pragma unroll
+                        for (int k = 0; k < kHC; ++k)
+                            *reinterpret_cast<uint4 *>(p.y + (tok * kHC + k) * d + cbase) =
+                                make_uint4(yo[k][0], yo[k][1], yo[k][2], yo[k][3]);
+                        *reinterpret_cast<uint4 *>(p.h_norm + tok * d + cbase) =
+                            make_uint4(ho[0], ho[1], ho[2], ho[3]);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty_bar(slot));
+            if (!us.p3 && us.cb == ncb - 1) {
+                // tile finished: this CTA's sums of squares of each token go to the owner
+                float ssx[2], ssh[2];
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    ssx[i] = f2_hsum(ssx2[i]);
+                    ssh[i] = f2_hsum(ssh2[i]);
+                    ssx[i] += __shfl_xor_sync(0xffffffffu, ssx[i], 1);
+                    ssx[i] += __shfl_xor_sync(0xffffffffu, ssx[i], 2);
+                    ssh[i] += __shfl_xor_sync(0xffffffffu, ssh[i], 1);
+                    ssh[i] += __shfl_xor_sync(0xffffffffu, ssh[i], 2);
+                }
+                if (uu < 2) {
+                    const int r = uu == 0 ? r0 : r1;
+                    const int owner = r / kTokPerOwner, tl = r % kTokPerOwner;
+                    const int buf = us.j & 1;
+                    const uint32_t dst = mapa(smem_u32(sPart + ((buf * kC + rank) * kTokPerOwner + tl) * kPartF + kMix), owner);
+                    st_cluster_v2(dst, uu == 0 ? ssx[0] : ssx[1], uu == 0 ? ssh[0] : ssh[1]);
+                    mbar_arrive_remote(mapa(part_bar(buf), owner));
+                }
+                ssx2[0] = ssx2[1] = ssh2[0] = ssh2[1] = zero2;
+            }
+        }
+    }
+    __syncwarp();
+    cluster_sync_all();  // no CTA leaves while a peer may still touch its shared memory
+}
+
+}  // namespace cl
+
+// ---------------------------------------------------------------- host side
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        cudaDriverEntryPointQueryResult q;
+        void *f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    }
+    return fn;
+}
+
+// rows x cols bf16 matrix (row stride `cols` elements), box of 64 rows x 32 columns, 64B swizzle
+bool make_tmap(CUtensorMap *m, const void *base, int64_t rows, int64_t cols) {
+    auto enc = get_encode();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    cuuint32_t box[2] = {(cuuint32_t)cl::kCB, (cuuint32_t)cl::kT};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+struct DevInfo {
+    int max_clusters = -1;
+};
+DevInfo g_dev[64];
+
+}  // namespace
+
+bool cluster_path_supported(int d) {
+    if (d % (cl::kC * cl::kCB) != 0 || d <= 0) return false;
+    return cl::make_layout(d).total <= 232448;
+}
+
+template <bool kFull>
+static cudaError_t launch_cluster_impl(const uint16_t *x, const float *pre_mix, const uint16_t *f,
+                                       const float *hc_fn, const float *hc_scale,
+                                       const float *hc_base, const float *norm_w, int64_t n, int d,
+                                       int iters, float eps, float norm_eps, uint16_t *h_norm,
+                                       uint16_t *y, float *pre_out, float *post_out,
+                                       float *comb_out, float *mixes_out, cudaStream_t s) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const cl::Layout L = cl::make_layout(d);
+    auto kern = cl::k_block_cluster<kFull>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cl::kC;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.blockDim = dim3(cl::kThreads);
+    cfg.dynamicSmemBytes = L.total;
+    cfg.stream = s;
+    DevInfo &di = g_dev[dev & 63];
+    if (di.max_clusters < 0) {
+        cfg.gridDim = dim3(cl::kC * 64);
+        int mc = 0;
+        e = cudaOccupancyMaxActiveClusters(&mc, kern, &cfg);
+        if (e != cudaSuccess) return e;
+        if (mc <= 0) return cudaErrorInvalidConfiguration;
+        di.max_clusters = mc;
+    }
+    const int64_t tiles = (n + cl::kT - 1) / cl::kT;
+    const int ncl = (int)(tiles < di.max_clusters ? tiles : di.max_clusters);
+    cfg.gridDim = dim3(cl::kC * ncl);
+
+    CUtensorMap tmx, tmf;
+    if (!make_tmap(&tmx, x, n, (int64_t)kHC * d)) return cudaErrorInvalidValue;
+    if (kFull) {
+        if (!make_tmap(&tmf, f, n, d)) return cudaErrorInvalidValue;
+    } else {
+        tmf = tmx;
+    }
+    cl::Params prm;
+    prm.pre_mix = pre_mix;
+    prm.hc_fn = hc_fn;
+    prm.hc_scale = hc_scale;
+    prm.hc_base = hc_base;
+    prm.norm_w = norm_w;
+    prm.h_norm = h_norm;
+    prm.y = y;
+    prm.pre_out = pre_out;
+    prm.post_out = post_out;
+    prm.comb_out = comb_out;
+    prm.mixes_out = mixes_out;
+    prm.n = n;
+    prm.d = d;
+    prm.iters = iters;
+    prm.eps = eps;
+    prm.norm_eps = norm_eps;
+    prm.num_tiles = (int)tiles;
+    e = cudaLaunchKernelEx(&cfg, kern, tmx, tmf, prm);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_block_cluster(const uint16_t *x, const float *pre_mix, const uint16_t *f,
+                                 const float *hc_fn, const float *hc_scale, const float *hc_base,
+                                 const float *norm_w, int64_t n, int d, int iters, float eps,
+                                 float norm_eps, uint16_t *h_norm, uint16_t *y, float *pre_out,
+                                 float *post_out, float *comb_out, float *mixes_out,
+                                 cudaStream_t s) {
+    if (f)
+        return launch_cluster_impl<true>(x, pre_mix, f, hc_fn, hc_scale, hc_base, norm_w, n, d,
+                                         iters, eps, norm_eps, h_norm, y, pre_out, post_out,
+                                         comb_out, mixes_out, s);
+    return launch_cluster_impl<false>(x, pre_mix, f, hc_fn, hc_scale, hc_base, norm_w, n, d, iters,
+                                      eps, norm_eps, h_norm, y, pre_out, post_out, comb_out,
+                                      mixes_out, s);
+}
+
+cudaError_t consume_device_error(cudaStream_t s, unsigned int *flag) {
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return e;
+    unsigned int v = 0;
+    e = cudaMemcpyFromSymbol(&v, g_device_error, sizeof v);
+    if (e != cudaSuccess) return e;
+    *flag = v;
+    if (v) {
+        const unsigned int zero = 0;
+        e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof zero);
+    }
+    return e;
+}
+
+}  // namespace hc

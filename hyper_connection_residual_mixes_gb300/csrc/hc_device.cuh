@@ -39,6 +39,52 @@ __device__ __forceinline__ uint4 pack8(const float (&o)[8]) {
                       pack_bf16x2(o[4], o[5]), pack_bf16x2(o[6], o[7]));
 }
 
+// ---------------------------------------------------------------- packed fp32 pairs
+// Two fp32 lanes in one 64-bit register pair, for the sm_100+ packed
+// instructions (add/mul/fma .rn.f32x2).  Each lane rounds exactly like the
+// scalar instruction, so results are bitwise those of the scalar code.
+typedef unsigned long long f32x2;
+
+__device__ __forceinline__ f32x2 f2_make(float lo, float hi) {
+    f32x2 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_split(f32x2 v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ f32x2 f2_dup(float a) { return f2_make(a, a); }
+__device__ __forceinline__ f32x2 f2_fma(f32x2 a, f32x2 b, f32x2 c) {
+    f32x2 d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ f32x2 f2_mul(f32x2 a, f32x2 b) {
+    f32x2 d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ f32x2 f2_add(f32x2 a, f32x2 b) {
+    f32x2 d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+// packed bf16 pair (element 0 in the low half) -> fp32 pair (exact)
+__device__ __forceinline__ f32x2 f2_from_bf16x2(uint32_t v) {
+    return f2_make(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
+}
+// fp32 pair -> packed bf16 pair, round to nearest even
+__device__ __forceinline__ uint32_t f2_to_bf16x2(f32x2 v) {
+    float a, b;
+    f2_split(v, a, b);
+    return pack_bf16x2(a, b);
+}
+__device__ __forceinline__ float f2_hsum(f32x2 v) {
+    float a, b;
+    f2_split(v, a, b);
+    return a + b;
+}
+
 // ---------------------------------------------------------------- reductions
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll

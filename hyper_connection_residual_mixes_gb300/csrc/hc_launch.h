@@ -27,4 +27,20 @@ cudaError_t launch_tokens_simple(const uint16_t *x, const float *pre_mix, const 
                                  float *post_out, float *comb_out, float *mixes_out,
                                  cudaStream_t s);
 
+// The fused persistent-cluster path (hc_block_cluster.cu).  Supported when d
+// is a multiple of 512 and the per-CTA weight slice fits in shared memory
+// (d <= 5120).  With f == nullptr it computes a1-a3 only.
+bool cluster_path_supported(int d);
+
+cudaError_t launch_block_cluster(const uint16_t *x, const float *pre_mix, const uint16_t *f,
+                                 const float *hc_fn, const float *hc_scale, const float *hc_base,
+                                 const float *norm_w, int64_t n, int d, int iters, float eps,
+                                 float norm_eps, uint16_t *h_norm, uint16_t *y, float *pre_out,
+                                 float *post_out, float *comb_out, float *mixes_out,
+                                 cudaStream_t s);
+
+// Synchronise `s`, then read and clear the device flag that bounded waits set
+// when they time out.
+cudaError_t consume_device_error(cudaStream_t s, unsigned int *flag);
+
 }  // namespace hc

@@ -58,7 +58,8 @@ typedef enum {
     HC_ERR_UNSUPPORTED = 2,  /* hc != 4, or d not a multiple of 64 in [64, 16384] */
     HC_ERR_MISALIGNED = 3,   /* a pointer that is not 16-byte aligned */
     HC_ERR_ALIAS = 4,        /* an output range overlaps an input or another output */
-    HC_ERR_CUDA = 5          /* a CUDA runtime call failed; see hc_last_cuda_error() */
+    HC_ERR_CUDA = 5,         /* a CUDA runtime call failed; see hc_last_cuda_error() */
+    HC_ERR_TIMEOUT = 6       /* a kernel's bounded barrier wait ran out (reported by hc_consume_device_error) */
 } hc_status;
 
 /* Static, never-freed description of a status code. */
@@ -69,6 +70,16 @@ int hc_last_cuda_error(void);
 
 /* Library version as major*10000 + minor*100 + patch. */
 int hc_version(void);
+
+/*
+ * Synchronise `stream`, then report and clear the library's device-side
+ * error flag.  Kernels never spin without bound: a barrier wait that runs out
+ * (a peer that never arrives) records a flag and the kernel returns early
+ * with its outputs incomplete.  Returns HC_ERR_TIMEOUT if any kernel on this
+ * device set the flag since the last call, HC_ERR_CUDA if synchronising
+ * failed, HC_OK otherwise.  Not part of the method: a health check.
+ */
+hc_status hc_consume_device_error(cudaStream_t stream);
 
 /*
  * a1-a3 (DeepSeek-V4.1 Block page, Block.hc_mixes, and the "Stream
