@@ -10,30 +10,33 @@
 // How (one launch per side step, persistent thread-block clusters):
 //  * A cluster of kC = 16 CTAs (one per SM) splits the model dimension d into
 //    16 column slices; CTA `rank` owns columns [rank*d/16, (rank+1)*d/16) of
-//    each of the 4 streams.  Its slice of hc_fn (24 rows x 4*d/16 columns,
-//    fp32) stays resident in shared memory for the whole launch, so the
-//    projection weights are read from memory once per CTA, not once per token.
-//  * A cluster walks 64-token tiles.  Each tile's streams pass through a
-//    3-slot TMA ring (32 columns x 64 tokens x 4 streams per slot, 64-byte
+//    each of the 4 streams.
+//  * The CTA's slice of hc_fn (24 rows x 4*d/16 columns) is split once, at
+//    launch, into three bf16 parts per fp32 weight (hi + mid + lo, exact to
+//    ~2^-24 relative) laid out as mma.sync B fragments, and kept in tensor
+//    memory for the whole launch: one 32-lane TMEM quadrant per MMA warp, one
+//    stream per MMA warp.  Weights are never re-read per token and take no
+//    shared memory.
+//  * A cluster walks 64-token tiles.  Each tile's streams pass through an
+//    8-slot TMA ring (32 columns x 64 tokens x 4 streams per slot, 64-byte
 //    swizzle) twice: phase 1 (the projection, sum of squares, and the sum of
 //    squares of the bf16-rounded h) and phase 3 (y and h_norm).  The second
 //    read comes from L2 (the first read is tagged evict_last, the second
 //    evict_first); phase 1 of the next tile runs between them so the
 //    cross-CTA reduction of a tile is hidden behind useful streaming.
-//  * The 24 x (4*d/16) projection runs on the tensor cores with
-//    mma.sync m16n8k16 (bf16 in, fp32 accumulate).  hc_fn is fp32; each
-//    weight is split on the fly into three bf16 parts (hi + mid + lo) whose
-//    sum equals the fp32 weight to ~2^-24, and all three products accumulate
-//    into the same fp32 sums.  x is bf16 and enters the MMA exactly.
+//  * The projection runs on the tensor cores (mma.sync m16n8k16, bf16 in,
+//    fp32 accumulate); x is bf16 and enters exactly; the three weight parts
+//    accumulate into the same fp32 sums.
 //  * Partial sums (24 dots, sum x^2, sum h^2) of each token go to the token's
 //    owner CTA through distributed shared memory with cluster-scope mbarrier
 //    arrivals; the owner finishes the statistics, runs the split + 20-round
 //    Sinkhorn in registers, writes pre/post/comb, and broadcasts post, comb
 //    and the RMSNorm scale back to all 16 CTAs.
 //
-// Warp roles (256 threads): warp 0 TMA producer; warps 1-2 tensor-core MMA
-// (each a half of every slot's K range, all 64 tokens); warp 3 owner-side
-// reduction + Sinkhorn + broadcast; warps 4-7 CUDA-core streaming math.
+// Warp roles (448 threads): warps 0-3 tensor-core MMA (warp w: stream w, TMEM
+// quadrant w); warp 4 TMA producer; warp 5 owner-side reduction + Sinkhorn +
+// broadcast; warps 6-13 CUDA-core streaming math (one 8-column unit of one
+// token per thread per slot, packed f32x2 arithmetic).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -48,18 +51,22 @@ namespace cl {
 constexpr int kC = 16;          // CTAs per cluster = column slices of d
 constexpr int kT = 64;          // tokens per tile
 constexpr int kCB = 32;         // columns per slot (per stream)
-constexpr int kSlots = 3;       // TMA ring depth
-constexpr int kThreads = 256;
+constexpr int kSlots = 8;       // TMA ring depth (160 KB in flight per SM)
+constexpr uint32_t kTmemCols = 512;  // the whole tensor memory of the SM (1 CTA per SM)
+constexpr int kThreads = 448;
 constexpr int kBoxBytes = kT * kCB * 2;             // 4096: 64 tokens x 32 bf16
 constexpr int kStageXBytes = kHC * kBoxBytes;       // 16384
 constexpr int kSlotBytes = kStageXBytes + kBoxBytes;  // + f box = 20480
 constexpr int kTokPerOwner = kT / kC;               // 4
 constexpr int kPartF = 28;      // 24 partial dots, sum x^2, sum h^2, 2 pad
 constexpr int kCoefF = 24;      // post[4], comb[16], rs_h, 3 pad
-constexpr int kWarpProducer = 0;
-constexpr int kWarpMma = 1;     // warps 1, 2
-constexpr int kWarpReducer = 3;
-constexpr int kWarpCuda = 4;    // warps 4..7
+constexpr int kWarpMma = 0;     // warps 0..3: MMA warp w owns stream w and TMEM quadrant w
+constexpr int kMmaWarps = 4;
+constexpr int kWarpProducer = 4;
+constexpr int kWarpReducer = 5;
+constexpr int kWarpCuda = 6;    // warps 6..13
+constexpr int kCudaWarps = 8;
+constexpr int kWCols = 18;      // TMEM columns per k16 step: 3 n-tiles x (hi, mid, lo) x (b0, b1)
 
 struct Params {
     const float *pre_mix;
@@ -85,29 +92,30 @@ struct Params {
 struct Layout {
     int dc;        // columns per CTA per stream = d / 16
     int ncb;       // slots per tile = dc / 32
-    int wstr;      // hc_fn row stride in floats (4*dc + 8: conflict-free 8-byte loads)
-    int off_w, off_coef, off_part, off_mma, off_normw, off_bar, total;
+    int wcols;     // tensor-memory columns per MMA warp: 18 per k16 step, 2*ncb steps
+    int off_coef, off_part, off_mma, off_normw, off_bar, off_tmem, total;
 };
 
 __host__ __device__ inline Layout make_layout(int d) {
     Layout L;
     L.dc = d / kC;
     L.ncb = L.dc / kCB;
-    L.wstr = kHC * L.dc + 8;
+    L.wcols = kWCols * 2 * L.ncb;
     int o = kSlots * kSlotBytes;
-    L.off_w = o;
-    o += kMix * L.wstr * 4;
     L.off_coef = o;
     o += 2 * kT * kCoefF * 4;
     L.off_part = o;
     o += 2 * kC * kTokPerOwner * kPartF * 4;
     L.off_mma = o;
-    o += 2 * kT * kMix * 4;
+    o += kMmaWarps * kT * kMix * 4;
     L.off_normw = o;
     o += L.dc * 4;
     o = (o + 15) & ~15;
     L.off_bar = o;
-    o += 16 * 8;
+    o += (2 * kSlots + 6) * 8;  // full[], empty[], part[2], coef[2], two MMA meeting points
+    o = (o + 15) & ~15;
+    L.off_tmem = o;
+    o += 16;
     L.total = o + 1024;  // slack for aligning the base
     return L;
 }
@@ -178,57 +186,157 @@ k_block_cluster(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     const int64_t K = (int64_t)kHC * d;
     const int U = total_uses(ncb, J, kFull);
 
-    float *sW = reinterpret_cast<float *>(smem + L.off_w);
     float *sCoef = reinterpret_cast<float *>(smem + L.off_coef);
     float *sPart = reinterpret_cast<float *>(smem + L.off_part);
     float *sMma = reinterpret_cast<float *>(smem + L.off_mma);
     float *sNormW = reinterpret_cast<float *>(smem + L.off_normw);
+    uint32_t *sTmem = reinterpret_cast<uint32_t *>(smem + L.off_tmem);
     const uint32_t bar0 = smem_u32(smem + L.off_bar);
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (kSlots + s); };
     auto part_bar = [&](int b) { return bar0 + 8u * (2 * kSlots + b); };
     auto coef_bar = [&](int b) { return bar0 + 8u * (2 * kSlots + 2 + b); };
-    // the two MMA warps meet twice per tile: before reading each other's sums, and
-    // after the send (so neither rewrites its half while the other still reads it)
+    // the MMA warps meet twice per tile: before reading each other's sums, and
+    // after the send (so none rewrites its part while another still reads it)
     const uint32_t mma_bar = bar0 + 8u * (2 * kSlots + 4);
     const uint32_t mma_bar2 = bar0 + 8u * (2 * kSlots + 5);
     const uint32_t slot0 = smem_u32(smem);
 
-    if (threadIdx.x == 0) {
+    if (threadIdx.x == kWarpProducer * 32) {
         s_abort = 0;
         for (int s = 0; s < kSlots; ++s) {
             mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), 2 + 4);  // MMA warps + CUDA-core warps
+            mbar_init(empty_bar(s), kMmaWarps + kCudaWarps);
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(part_bar(b), kC * (kT / kC) * (kFull ? 2 : 2));  // see the senders below
+            // per tile, from each of the 16 CTAs: 4 MMA lanes and 4 CUDA-core lanes
+            mbar_init(part_bar(b), kC * 2 * kTokPerOwner);
+            // per tile, from each of the 16 owners: 2 reducer lanes
             mbar_init(coef_bar(b), kC * 2);
         }
-        mbar_init(mma_bar, 64);
-        mbar_init(mma_bar2, 64);
+        mbar_init(mma_bar, kMmaWarps * 32);
+        mbar_init(mma_bar2, kMmaWarps * 32);
         fence_mbar_init_cluster();
-    }
-    if (warp == kWarpProducer && lane == 0) {
         prefetch_tmap(&tm_x);
         if (kFull) prefetch_tmap(&tm_f);
     }
-    // resident hc_fn slice: row i, local column s*dc + c  <-  global column s*d + rank*dc + c
-    {
-        const int q4 = dc / 4;  // float4 per stream per row
-        for (int idx = threadIdx.x; idx < kMix * kHC * q4; idx += kThreads) {
-            const int i = idx / (kHC * q4);
-            const int rem = idx % (kHC * q4);
-            const int s = rem / q4, c4 = rem % q4;
-            const float4 v = __ldg(reinterpret_cast<const float4 *>(
-                p.hc_fn + (int64_t)i * K + (int64_t)s * d + (int64_t)rank * dc + 4 * c4));
-            *reinterpret_cast<float4 *>(sW + i * L.wstr + s * dc + 4 * c4) = v;
-        }
-        if (kFull)
-            for (int c = threadIdx.x; c < dc; c += kThreads) sNormW[c] = __ldg(p.norm_w + rank * dc + c);
+    if (warp == kWarpMma) {  // one warp owns the tensor-memory allocation
+        tmem_alloc(smem_u32(sTmem), kTmemCols);
+        tmem_relinquish();
     }
-    cluster_sync_all();  // barriers initialised and visible cluster-wide; W resident
+    if (kFull)
+        for (int c = threadIdx.x; c < dc; c += kThreads) sNormW[c] = __ldg(p.norm_w + rank * dc + c);
+    tmem_fence_before_sync();
+    cluster_sync_all();  // barriers initialised and visible cluster-wide; TMEM allocated
+    tmem_fence_after_sync();
+    const uint32_t tmem_base = *sTmem;
 
-    if (warp == kWarpProducer) {
+    if (warp < kWarpMma + kMmaWarps) {
+        // ------------------------------------------------------------ tensor-core projection
+        const int s = warp - kWarpMma;  // this warp's stream
+        const int g = lane >> 2, t = lane & 3;
+        // B fragments of the resident weights in TMEM lane 32*s + lane: k16 step
+        // q (column block q / 2, half q % 2 of this CTA's columns of stream s)
+        // occupies columns 18q .. 18q + 17 as, per n-tile nt, the bf16x2 pairs
+        // hi(b0), hi(b1), mid(b0), mid(b1), lo(b0), lo(b1) of
+        // W[nt*8+g][k0+2t, k0+2t+1] (b0) and W[nt*8+g][k0+8+2t, k0+9+2t] (b1).
+        const uint32_t tw = tmem_base + ((uint32_t)(32 * (warp & 3)) << 16);
+        for (int q = 0; q < 2 * ncb; ++q) {
+            const int cb = q >> 1, h = q & 1;
+            const int64_t col = (int64_t)s * d + (int64_t)rank * dc + cb * kCB + h * 16 + 2 * t;
+#pragma unroll
+            for (int nt = 0; nt < 3; ++nt) {
+                const float *wr = p.hc_fn + (int64_t)(nt * 8 + g) * K + col;
+                const float2 p0 = __ldg(reinterpret_cast<const float2 *>(wr));
+                const float2 p1 = __ldg(reinterpret_cast<const float2 *>(wr + 8));
+                uint32_t h0, m0, l0, h1, m1, l1;
+                split3(p0.x, p0.y, h0, m0, l0);
+                split3(p1.x, p1.y, h1, m1, l1);
+                const uint32_t c0 = tw + kWCols * q + 6 * nt;
+                tmem_st2(c0 + 0, h0, h1);
+                tmem_st2(c0 + 2, m0, m1);
+                tmem_st2(c0 + 4, l0, l1);
+            }
+        }
+        tmem_wait_st();
+        float acc[4][3][4];
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+            for (int b = 0; b < 3; ++b)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) acc[a][b][c] = 0.0f;
+        int tiles_done = 0;
+        for (int u = 0; u < U; ++u) {
+            const int slot = u % kSlots;
+            const uint32_t ph = (uint32_t)(u / kSlots) & 1u;
+            if (!mbar_wait_warp<false>(full_bar(slot), ph, &s_abort)) break;
+            const Use us = decode_use(u, ncb, J, kFull);
+            if (!us.p3) {
+                uint32_t bw[36];
+                tmem_ld36(tw + 2 * kWCols * us.cb, bw);
+                tmem_wait_ld36(bw);
+                const uint32_t box = slot0 + slot * kSlotBytes + s * kBoxBytes;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+#pragma unroll
+                    for (int mt = 0; mt < 4; ++mt) {
+                        const int r = mt * 16 + (lane & 15);
+                        uint32_t a0, a1, a2, a3;
+                        ldmatrix_x4(box + sw64(r, 2 * h + (lane >> 4)), a0, a1, a2, a3);
+#pragma unroll
+                        for (int nt = 0; nt < 3; ++nt) {
+                            const uint32_t *b = bw + kWCols * h + 6 * nt;
+                            mma_bf16_16816(acc[mt][nt], a0, a1, a2, a3, b[4], b[5]);  // lo
+                            mma_bf16_16816(acc[mt][nt], a0, a1, a2, a3, b[2], b[3]);  // mid
+                            mma_bf16_16816(acc[mt][nt], a0, a1, a2, a3, b[0], b[1]);  // hi
+                        }
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty_bar(slot));
+            if (!us.p3 && us.cb == ncb - 1) {
+                // tile finished: combine the four streams' sums, send each token's 24
+                // partial dots to its owner CTA
+                float *mine = sMma + s * kT * kMix;
+#pragma unroll
+                for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+                    for (int nt = 0; nt < 3; ++nt) {
+                        const int r = mt * 16 + g, c = nt * 8 + 2 * t;
+                        *reinterpret_cast<float2 *>(mine + r * kMix + c) = make_float2(acc[mt][nt][0], acc[mt][nt][1]);
+                        *reinterpret_cast<float2 *>(mine + (r + 8) * kMix + c) = make_float2(acc[mt][nt][2], acc[mt][nt][3]);
+                        acc[mt][nt][0] = acc[mt][nt][1] = acc[mt][nt][2] = acc[mt][nt][3] = 0.0f;
+                    }
+                mbar_arrive(mma_bar);
+                if (!mbar_wait_warp<false>(mma_bar, (uint32_t)tiles_done & 1u, &s_abort)) break;
+                if (lane < 16) {
+                    const int tk = s * 16 + lane;  // token within the tile
+                    const int owner = tk / kTokPerOwner, tl = tk % kTokPerOwner;
+                    const int buf = us.j & 1;
+                    float v[kMix];
+#pragma unroll
+                    for (int i = 0; i < kMix; ++i) v[i] = 0.0f;
+#pragma unroll
+                    for (int w = 0; w < kMmaWarps; ++w) {
+                        const float *e = sMma + (w * kT + tk) * kMix;
+#pragma unroll
+                        for (int i = 0; i < kMix; ++i) v[i] += e[i];
+                    }
+                    const uint32_t dst = mapa(smem_u32(sPart + ((buf * kC + rank) * kTokPerOwner + tl) * kPartF), owner);
+#pragma unroll
+                    for (int q = 0; q < kMix / 4; ++q)
+                        st_cluster_v4(dst + 16 * q, v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                    mbar_arrive_remote(mapa(part_bar(buf), owner));
+                }
+                mbar_arrive(mma_bar2);
+                const bool met = mbar_wait_warp<false>(mma_bar2, (uint32_t)tiles_done & 1u, &s_abort);
+                ++tiles_done;
+                if (!met) break;
+            }
+        }
+    } else if (warp == kWarpProducer) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
             const uint64_t pol_keep = policy_evict_last(), pol_stream = policy_evict_first();
@@ -253,89 +361,6 @@ k_block_cluster(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             // last armed uses of every slot
             for (int u = (armed > kSlots ? armed - kSlots : 0); u < armed; ++u)
                 mbar_wait<false>(full_bar(u % kSlots), (uint32_t)(u / kSlots) & 1u, &s_abort);
-        }
-    } else if (warp == kWarpMma || warp == kWarpMma + 1) {
-        // ------------------------------------------------------------ tensor-core projection
-        const int mw = warp - kWarpMma;  // streams 2*mw, 2*mw+1
-        const int g = lane >> 2, t = lane & 3;
-        float acc[4][3][4];
-#pragma unroll
-        for (int a = 0; a < 4; ++a)
-#pragma unroll
-            for (int b = 0; b < 3; ++b)
-#pragma unroll
-                for (int c = 0; c < 4; ++c) acc[a][b][c] = 0.0f;
-        int tiles_done = 0;
-        for (int u = 0; u < U; ++u) {
-            const int slot = u % kSlots;
-            const uint32_t ph = (uint32_t)(u / kSlots) & 1u;
-            if (!mbar_wait_warp<false>(full_bar(slot), ph, &s_abort)) break;
-            const Use us = decode_use(u, ncb, J, kFull);
-            if (!us.p3) {
-                const uint32_t sb = slot0 + slot * kSlotBytes;
-#pragma unroll
-                for (int si = 0; si < 2; ++si) {
-                    const int s = 2 * mw + si;
-                    const uint32_t box = sb + s * kBoxBytes;
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int kb = s * dc + us.cb * kCB + h * 16;
-                        uint32_t bh[3][2], bm[3][2], bl[3][2];
-#pragma unroll
-                        for (int nt = 0; nt < 3; ++nt) {
-                            const float *wr = sW + (nt * 8 + g) * L.wstr + kb + 2 * t;
-                            const float2 p0 = *reinterpret_cast<const float2 *>(wr);
-                            const float2 p1 = *reinterpret_cast<const float2 *>(wr + 8);
-                            split3(p0.x, p0.y, bh[nt][0], bm[nt][0], bl[nt][0]);
-                            split3(p1.x, p1.y, bh[nt][1], bm[nt][1], bl[nt][1]);
-                        }
-#pragma unroll
-                        for (int mt = 0; mt < 4; ++mt) {
-                            const int r = mt * 16 + (lane & 15);
-                            uint32_t a0, a1, a2, a3;
-                            ldmatrix_x4(box + sw64(r, 2 * h + (lane >> 4)), a0, a1, a2, a3);
-#pragma unroll
-                            for (int nt = 0; nt < 3; ++nt) {
-                                mma_bf16_16816(acc[mt][nt], a0, a1, a2, a3, bl[nt][0], bl[nt][1]);
-                                mma_bf16_16816(acc[mt][nt], a0, a1, a2, a3, bm[nt][0], bm[nt][1]);
-                                mma_bf16_16816(acc[mt][nt], a0, a1, a2, a3, bh[nt][0], bh[nt][1]);
-                            }
-                        }
-                    }
-                }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(empty_bar(slot));
-            if (!us.p3 && us.cb == ncb - 1) {
-                // tile finished: combine the two K halves, send each token's 24 partial
-                // dots to its owner CTA
-                float *mine = sMma + mw * kT * kMix;
-#pragma unroll
-                for (int mt = 0; mt < 4; ++mt)
-#pragma unroll
-                    for (int nt = 0; nt < 3; ++nt) {
-                        const int r = mt * 16 + g, c = nt * 8 + 2 * t;
-                        *reinterpret_cast<float2 *>(mine + r * kMix + c) = make_float2(acc[mt][nt][0], acc[mt][nt][1]);
-                        *reinterpret_cast<float2 *>(mine + (r + 8) * kMix + c) = make_float2(acc[mt][nt][2], acc[mt][nt][3]);
-                        acc[mt][nt][0] = acc[mt][nt][1] = acc[mt][nt][2] = acc[mt][nt][3] = 0.0f;
-                    }
-                mbar_arrive(mma_bar);
-                if (!mbar_wait_warp<false>(mma_bar, (uint32_t)tiles_done & 1u, &s_abort)) break;
-                const int tk = mw * 32 + lane;          // token within the tile
-                const int owner = tk / kTokPerOwner, tl = tk % kTokPerOwner;
-                const int buf = us.j & 1;
-                const float *a = sMma + tk * kMix, *b = sMma + kT * kMix + tk * kMix;
-                const uint32_t dst = mapa(smem_u32(sPart + ((buf * kC + rank) * kTokPerOwner + tl) * kPartF), owner);
-#pragma unroll
-                for (int q = 0; q < kMix / 4; ++q)
-                    st_cluster_v4(dst + 16 * q, a[4 * q] + b[4 * q], a[4 * q + 1] + b[4 * q + 1],
-                                  a[4 * q + 2] + b[4 * q + 2], a[4 * q + 3] + b[4 * q + 3]);
-                mbar_arrive_remote(mapa(part_bar(buf), owner));
-                mbar_arrive(mma_bar2);
-                const bool met = mbar_wait_warp<false>(mma_bar2, (uint32_t)tiles_done & 1u, &s_abort);
-                ++tiles_done;
-                if (!met) break;
-            }
         }
     } else if (warp == kWarpReducer) {
         // ------------------------------------------------------------ owner: statistics + Sinkhorn
@@ -406,16 +431,14 @@ k_block_cluster(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
         }
     } else {
         // ------------------------------------------------------------ CUDA-core streaming math
-        // 128 threads; per slot, thread tc handles the 8-column unit uu = tc % 4 of
-        // token rows tc / 4 and 32 + tc / 4, as four packed fp32 pairs per stream.
-        const int tc = threadIdx.x - kWarpCuda * 32;  // 0..127
+        // 256 threads; per slot, thread tc handles the 8-column unit uu = tc % 4 of
+        // token row r = tc / 4, as four packed fp32 pairs per stream.
+        const int tc = threadIdx.x - kWarpCuda * 32;  // 0..255
         const int uu = tc & 3;
-        const int r0 = tc >> 2, r1 = 32 + (tc >> 2);
-        f32x2 pm[2][kHC];   // pre_mix of the two tokens, duplicated into both lanes
-        f32x2 ssx2[2], ssh2[2];
-        float cf[2][kHC + kHC * kHC + 1];  // post, comb, RMSNorm scale of the two tokens
-        const f32x2 zero2 = f2_dup(0.0f);
-        ssx2[0] = ssx2[1] = ssh2[0] = ssh2[1] = zero2;
+        const int r = tc >> 2;
+        f32x2 pm[kHC];  // pre_mix of the token, duplicated into both lanes
+        f32x2 ssx2 = f2_dup(0.0f), ssh2 = f2_dup(0.0f);
+        float cf[kHC + kHC * kHC + 1];  // post, comb, RMSNorm scale of the token
         int cur_coef_tile = -1;
         for (int u = 0; u < U; ++u) {
             const int slot = u % kSlots;
@@ -423,43 +446,33 @@ k_block_cluster(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             if (!mbar_wait_warp<false>(full_bar(slot), ph, &s_abort)) break;
             const Use us = decode_use(u, ncb, J, kFull);
             const int tile = cid + us.j * ncl;
+            const int64_t tok = (int64_t)tile * kT + r;
             const uint8_t *sb = smem + slot * kSlotBytes;
             if (us.cb == 0) {
-                // pre_mix of this thread's two tokens for the tile of this use
-#pragma unroll
-                for (int i = 0; i < 2; ++i) {
-                    const int64_t tok = (int64_t)tile * kT + (i ? r1 : r0);
-                    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (kFull && tok < p.n) v = __ldg(reinterpret_cast<const float4 *>(p.pre_mix) + tok);
-                    pm[i][0] = f2_dup(v.x); pm[i][1] = f2_dup(v.y);
-                    pm[i][2] = f2_dup(v.z); pm[i][3] = f2_dup(v.w);
-                }
+                // pre_mix of this thread's token for the tile of this use
+                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (kFull && tok < p.n) v = __ldg(reinterpret_cast<const float4 *>(p.pre_mix) + tok);
+                pm[0] = f2_dup(v.x); pm[1] = f2_dup(v.y); pm[2] = f2_dup(v.z); pm[3] = f2_dup(v.w);
             }
+            uint4 xr[kHC];
+#pragma unroll
+            for (int s = 0; s < kHC; ++s) xr[s] = *reinterpret_cast<const uint4 *>(sb + s * kBoxBytes + sw64(r, uu));
             if (!us.p3) {
 #pragma unroll
-                for (int i = 0; i < 2; ++i) {
-                    const int r = i ? r1 : r0;
-                    uint4 xr[kHC];
+                for (int q = 0; q < 4; ++q) {
+                    f32x2 xs[kHC];
 #pragma unroll
-                    for (int s = 0; s < kHC; ++s)
-                        xr[s] = *reinterpret_cast<const uint4 *>(sb + s * kBoxBytes + sw64(r, uu));
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        f32x2 xs[kHC];
-#pragma unroll
-                        for (int s = 0; s < kHC; ++s) {
-                            const uint32_t w = q == 0 ? xr[s].x : q == 1 ? xr[s].y : q == 2 ? xr[s].z : xr[s].w;
-                            xs[s] = f2_from_bf16x2(w);
-                            ssx2[i] = f2_fma(xs[s], xs[s], ssx2[i]);
-                        }
-                        if (kFull) {
-                            f32x2 h = f2_mul(pm[i][0], xs[0]);
-                            h = f2_fma(pm[i][1], xs[1], h);
-                            h = f2_fma(pm[i][2], xs[2], h);
-                            h = f2_fma(pm[i][3], xs[3], h);
-                            const f32x2 hr = f2_from_bf16x2(f2_to_bf16x2(h));
-                            ssh2[i] = f2_fma(hr, hr, ssh2[i]);
-                        }
+                    for (int s = 0; s < kHC; ++s) {
+                        xs[s] = f2_from_bf16x2(q == 0 ? xr[s].x : q == 1 ? xr[s].y : q == 2 ? xr[s].z : xr[s].w);
+                        ssx2 = f2_fma(xs[s], xs[s], ssx2);
+                    }
+                    if (kFull) {
+                        f32x2 h = f2_mul(pm[0], xs[0]);
+                        h = f2_fma(pm[1], xs[1], h);
+                        h = f2_fma(pm[2], xs[2], h);
+                        h = f2_fma(pm[3], xs[3], h);
+                        const f32x2 hr = f2_from_bf16x2(f2_to_bf16x2(h));
+                        ssh2 = f2_fma(hr, hr, ssh2);
                     }
                 }
             } else {
@@ -467,89 +480,72 @@ k_block_cluster(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 if (cur_coef_tile != us.j) {
                     if (!mbar_wait_warp<true>(coef_bar(buf), (uint32_t)(us.j >> 1) & 1u, &s_abort)) break;
                     cur_coef_tile = us.j;
+                    const float *c = sCoef + (buf * kT + r) * kCoefF;
 #pragma unroll
-                    for (int i = 0; i < 2; ++i) {
-                        const float *c = sCoef + (buf * kT + (i ? r1 : r0)) * kCoefF;
-#pragma unroll
-                        for (int q = 0; q < kHC + kHC * kHC + 1; ++q) cf[i][q] = c[q];
-                    }
+                    for (int q = 0; q < kHC + kHC * kHC + 1; ++q) cf[q] = c[q];
                 }
-                const float4 *nw = reinterpret_cast<const float4 *>(sNormW + us.cb * kCB + uu * 8);
-                const float4 w0 = nw[0], w1 = nw[1];
-                const f32x2 wv[4] = {f2_make(w0.x, w0.y), f2_make(w0.z, w0.w), f2_make(w1.x, w1.y),
-                                     f2_make(w1.z, w1.w)};
+                const uint4 fr = *reinterpret_cast<const uint4 *>(sb + kStageXBytes + sw64(r, uu));
+                if (tok < p.n) {
+                    const float4 *nw = reinterpret_cast<const float4 *>(sNormW + us.cb * kCB + uu * 8);
+                    const float4 w0 = nw[0], w1 = nw[1];
+                    const f32x2 wv[4] = {f2_make(w0.x, w0.y), f2_make(w0.z, w0.w), f2_make(w1.x, w1.y),
+                                         f2_make(w1.z, w1.w)};
+                    const int64_t cbase = (int64_t)rank * dc + us.cb * kCB + uu * 8;
+                    uint32_t yo[kHC][4], ho[4];
+                    const f32x2 rs2 = f2_dup(cf[kHC + kHC * kHC]);
 #pragma unroll
-                for (int i = 0; i < 2; ++i) {
-                    const int r = i ? r1 : r0;
-                    const int64_t tok = (int64_t)tile * kT + r;
-                    uint4 xr[kHC];
+                    for (int q = 0; q < 4; ++q) {
+                        f32x2 xs[kHC];
 #pragma unroll
-                    for (int s = 0; s < kHC; ++s)
-                        xr[s] = *reinterpret_cast<const uint4 *>(sb + s * kBoxBytes + sw64(r, uu));
-                    const uint4 fr = *reinterpret_cast<const uint4 *>(sb + kStageXBytes + sw64(r, uu));
-                    if (tok < p.n) {
-                        const int64_t cbase = (int64_t)rank * dc + us.cb * kCB + uu * 8;
-                        uint32_t yo[kHC][4], ho[4];
-                        const f32x2 rs2 = f2_dup(cf[i][kHC + kHC * kHC]);
+                        for (int s = 0; s < kHC; ++s)
+                            xs[s] = f2_from_bf16x2(q == 0 ? xr[s].x : q == 1 ? xr[s].y : q == 2 ? xr[s].z : xr[s].w);
+                        const f32x2 fv = f2_from_bf16x2(q == 0 ? fr.x : q == 1 ? fr.y : q == 2 ? fr.z : fr.w);
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            f32x2 xs[kHC];
+                        for (int k = 0; k < kHC; ++k) {
+                            f32x2 a = f2_mul(f2_dup(cf[k]), fv);
 #pragma unroll
-                            for (int s = 0; s < kHC; ++s)
-                                xs[s] = f2_from_bf16x2(q == 0 ? xr[s].x : q == 1 ? xr[s].y : q == 2 ? xr[s].z : xr[s].w);
-                            const f32x2 fv = f2_from_bf16x2(q == 0 ? fr.x : q == 1 ? fr.y : q == 2 ? fr.z : fr.w);
-#pragma unroll
-                            for (int k = 0; k < kHC; ++k) {
-                                f32x2 a = f2_mul(f2_dup(cf[i][k]), fv);
-#pragma unroll
-                                for (int jj = 0; jj < kHC; ++jj)
-                                    a = f2_fma(f2_dup(cf[i][kHC + jj * kHC + k]), xs[jj], a);
-                                yo[k][q] = f2_to_bf16x2(a);
-                            }
-                            f32x2 h = f2_mul(pm[i][0], xs[0]);
-                            h = f2_fma(pm[i][1], xs[1], h);
-                            h = f2_fma(pm[i][2], xs[2], h);
-                            h = f2_fma(pm[i][3], xs[3], h);
-                            const f32x2 hr = f2_from_bf16x2(f2_to_bf16x2(h));
-                            ho[q] = f2_to_bf16x2(f2_mul(f2_mul(hr, rs2), wv[q]));
+                            for (int jj = 0; jj < kHC; ++jj) a = f2_fma(f2_dup(cf[kHC + jj * kHC + k]), xs[jj], a);
+                            yo[k][q] = f2_to_bf16x2(a);
                         }
-#pragma unroll
-                        for (int k = 0; k < kHC; ++k)
-                            *reinterpret_cast<uint4 *>(p.y + (tok * kHC + k) * d + cbase) =
-                                make_uint4(yo[k][0], yo[k][1], yo[k][2], yo[k][3]);
-                        *reinterpret_cast<uint4 *>(p.h_norm + tok * d + cbase) =
-                            make_uint4(ho[0], ho[1], ho[2], ho[3]);
+                        f32x2 h = f2_mul(pm[0], xs[0]);
+                        h = f2_fma(pm[1], xs[1], h);
+                        h = f2_fma(pm[2], xs[2], h);
+                        h = f2_fma(pm[3], xs[3], h);
+                        const f32x2 hr = f2_from_bf16x2(f2_to_bf16x2(h));
+                        ho[q] = f2_to_bf16x2(f2_mul(f2_mul(hr, rs2), wv[q]));
                     }
+#pragma unroll
+                    for (int k = 0; k < kHC; ++k)
+                        *reinterpret_cast<uint4 *>(p.y + (tok * kHC + k) * d + cbase) =
+                            make_uint4(yo[k][0], yo[k][1], yo[k][2], yo[k][3]);
+                    *reinterpret_cast<uint4 *>(p.h_norm + tok * d + cbase) = make_uint4(ho[0], ho[1], ho[2], ho[3]);
                 }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(empty_bar(slot));
             if (!us.p3 && us.cb == ncb - 1) {
-                // tile finished: this CTA's sums of squares of each token go to the owner
-                float ssx[2], ssh[2];
-#pragma unroll
-                for (int i = 0; i < 2; ++i) {
-                    ssx[i] = f2_hsum(ssx2[i]);
-                    ssh[i] = f2_hsum(ssh2[i]);
-                    ssx[i] += __shfl_xor_sync(0xffffffffu, ssx[i], 1);
-                    ssx[i] += __shfl_xor_sync(0xffffffffu, ssx[i], 2);
-                    ssh[i] += __shfl_xor_sync(0xffffffffu, ssh[i], 1);
-                    ssh[i] += __shfl_xor_sync(0xffffffffu, ssh[i], 2);
-                }
-                if (uu < 2) {
-                    const int r = uu == 0 ? r0 : r1;
+                // tile finished: this CTA's sums of squares of the token go to its owner
+                float ssx = f2_hsum(ssx2), ssh = f2_hsum(ssh2);
+                ssx += __shfl_xor_sync(0xffffffffu, ssx, 1);
+                ssx += __shfl_xor_sync(0xffffffffu, ssx, 2);
+                ssh += __shfl_xor_sync(0xffffffffu, ssh, 1);
+                ssh += __shfl_xor_sync(0xffffffffu, ssh, 2);
+                if (uu == 0) {
                     const int owner = r / kTokPerOwner, tl = r % kTokPerOwner;
                     const int buf = us.j & 1;
                     const uint32_t dst = mapa(smem_u32(sPart + ((buf * kC + rank) * kTokPerOwner + tl) * kPartF + kMix), owner);
-                    st_cluster_v2(dst, uu == 0 ? ssx[0] : ssx[1], uu == 0 ? ssh[0] : ssh[1]);
+                    st_cluster_v2(dst, ssx, ssh);
                     mbar_arrive_remote(mapa(part_bar(buf), owner));
                 }
-                ssx2[0] = ssx2[1] = ssh2[0] = ssh2[1] = zero2;
+                ssx2 = ssh2 = f2_dup(0.0f);
             }
         }
     }
     __syncwarp();
+    tmem_fence_before_sync();
     cluster_sync_all();  // no CTA leaves while a peer may still touch its shared memory
+    tmem_fence_after_sync();
+    if (warp == kWarpMma) tmem_dealloc(tmem_base, kTmemCols);  // every path ends here
 }
 
 }  // namespace cl
@@ -595,7 +591,10 @@ DevInfo g_dev[64];
 
 bool cluster_path_supported(int d) {
     if (d % (cl::kC * cl::kCB) != 0 || d <= 0) return false;
-    return cl::make_layout(d).total <= 232448;
+    const cl::Layout L = cl::make_layout(d);
+    // the weight fragments of one MMA warp must fit its 512 tensor-memory columns,
+    // and the CTA must be alone on its SM (it takes the whole tensor memory)
+    return L.wcols <= (int)cl::kTmemCols && L.total <= 232448 && 2 * L.total > 233472;
 }
 
 template <bool kFull>
