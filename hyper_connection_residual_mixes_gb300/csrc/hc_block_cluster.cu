@@ -51,7 +51,9 @@ namespace cl {
 constexpr int kC = 16;          // CTAs per cluster = column slices of d
 constexpr int kT = 64;          // tokens per tile
 constexpr int kCB = 32;         // columns per slot (per stream)
-constexpr int kSlots = 8;       // TMA ring depth (160 KB in flight per SM)
+constexpr int kSlots = 7;       // TMA ring depth (140 KB in flight per SM)
+constexpr int kLag = 2;         // phase 3 of tile j runs after phase 1 of tile j + kLag
+constexpr int kBufs = kLag + 1; // partial / coefficient buffers in rotation
 constexpr uint32_t kTmemCols = 512;  // the whole tensor memory of the SM (1 CTA per SM)
 constexpr int kThreads = 448;
 constexpr int kBoxBytes = kT * kCB * 2;             // 4096: 64 tokens x 32 bf16
@@ -93,7 +95,7 @@ struct Layout {
     int dc;        // columns per CTA per stream = d / 16
     int ncb;       // slots per tile = dc / 32
     int wcols;     // tensor-memory columns per MMA warp: 18 per k16 step, 2*ncb steps
-    int off_coef, off_part, off_mma, off_normw, off_bar, off_tmem, total;
+    int off_coef, off_part, off_mma, off_ss, off_normw, off_bar, off_tmem, total;
 };
 
 __host__ __device__ inline Layout make_layout(int d) {
@@ -103,16 +105,18 @@ __host__ __device__ inline Layout make_layout(int d) {
     L.wcols = kWCols * 2 * L.ncb;
     int o = kSlots * kSlotBytes;
     L.off_coef = o;
-    o += 2 * kT * kCoefF * 4;
+    o += kBufs * kT * kCoefF * 4;
     L.off_part = o;
-    o += 2 * kC * kTokPerOwner * kPartF * 4;
+    o += kBufs * kC * kTokPerOwner * kPartF * 4;
     L.off_mma = o;
     o += kMmaWarps * kT * kMix * 4;
+    L.off_ss = o;  // CTA-local sums of squares, handed from the CUDA-core to the MMA warps
+    o += 2 * kT * 2 * 4;
     L.off_normw = o;
     o += L.dc * 4;
     o = (o + 15) & ~15;
     L.off_bar = o;
-    o += (2 * kSlots + 6) * 8;  // full[], empty[], part[2], coef[2], two MMA meeting points
+    o += (2 * kSlots + 2 * kBufs + 4) * 8;  // full[], empty[], part[], coef[], 2 MMA meetings, ss[2]
     o = (o + 15) & ~15;
     L.off_tmem = o;
     o += 16;
@@ -134,8 +138,11 @@ __device__ __forceinline__ uint32_t sw64(int r, int u) {
     return (uint32_t)(r * 64 + ((u ^ ((r >> 1) & 3)) << 4));
 }
 
-// The ring walks, per cluster, the sequence P1(0), P1(1), P3(0), P1(2), P3(1), ...
-// with `ncb` slots per phase.  Use u -> (phase-3?, local tile j, column block cb).
+// The ring walks, per cluster, blocks of `ncb` slot uses:
+//   P1(0) .. P1(kLag-1), then pairs P1(j + kLag), P3(j), then the last P3s.
+// Phase 3 of a tile thus starts kLag tiles of streaming after its phase 1,
+// which hides the cross-CTA reduction, Sinkhorn and broadcast of that tile.
+// Use u -> (phase 3?, local tile j, column block cb).
 struct Use {
     bool p3;
     int j;
@@ -143,26 +150,28 @@ struct Use {
 };
 __device__ __forceinline__ Use decode_use(int u, int ncb, int J, bool full) {
     Use r;
+    r.cb = u % ncb;
+    const int b = u / ncb;
     if (!full) {
         r.p3 = false;
-        r.j = u / ncb;
-        r.cb = u % ncb;
+        r.j = b;
         return r;
     }
-    // group g: P1(g) (if g < J) followed by P3(g-1) (if g >= 1)
-    if (u < ncb) {
-        r.p3 = false; r.j = 0; r.cb = u;
+    const int l0 = J < kLag ? J : kLag;
+    if (b < l0) {
+        r.p3 = false;
+        r.j = b;
         return r;
     }
-    const int v = u - ncb;
-    const int g = 1 + v / (2 * ncb);
-    const int w = v % (2 * ncb);
-    if (g < J) {
-        if (w < ncb) { r.p3 = false; r.j = g; r.cb = w; }
-        else         { r.p3 = true;  r.j = g - 1; r.cb = w - ncb; }
-    } else {
-        r.p3 = true; r.j = J - 1; r.cb = w;
+    const int c = b - l0;
+    const int pairs = J - l0;
+    if (c < 2 * pairs) {
+        r.p3 = (c & 1) != 0;
+        r.j = r.p3 ? (c >> 1) : l0 + (c >> 1);
+        return r;
     }
+    r.p3 = true;
+    r.j = pairs + (c - 2 * pairs);
     return r;
 }
 __device__ __forceinline__ int total_uses(int ncb, int J, bool full) {
@@ -195,11 +204,14 @@ k_block_cluster(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (kSlots + s); };
     auto part_bar = [&](int b) { return bar0 + 8u * (2 * kSlots + b); };
-    auto coef_bar = [&](int b) { return bar0 + 8u * (2 * kSlots + 2 + b); };
+    auto coef_bar = [&](int b) { return bar0 + 8u * (2 * kSlots + kBufs + b); };
     // the MMA warps meet twice per tile: before reading each other's sums, and
     // after the send (so none rewrites its part while another still reads it)
-    const uint32_t mma_bar = bar0 + 8u * (2 * kSlots + 4);
-    const uint32_t mma_bar2 = bar0 + 8u * (2 * kSlots + 5);
+    const uint32_t mma_bar = bar0 + 8u * (2 * kSlots + 2 * kBufs);
+    const uint32_t mma_bar2 = bar0 + 8u * (2 * kSlots + 2 * kBufs + 1);
+    // the CUDA-core warps hand each tile's sums of squares to the MMA warps
+    auto ss_bar = [&](int b) { return bar0 + 8u * (2 * kSlots + 2 * kBufs + 2 + b); };
+    float *sSS = reinterpret_cast<float *>(smem + L.off_ss);
     const uint32_t slot0 = smem_u32(smem);
 
     if (threadIdx.x == kWarpProducer * 32) {
@@ -208,12 +220,13 @@ k_block_cluster(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             mbar_init(full_bar(s), 1);
             mbar_init(empty_bar(s), kMmaWarps + kCudaWarps);
         }
-        for (int b = 0; b < 2; ++b) {
-            // per tile, from each of the 16 CTAs: 4 MMA lanes and 4 CUDA-core lanes
-            mbar_init(part_bar(b), kC * 2 * kTokPerOwner);
+        for (int b = 0; b < kBufs; ++b) {
+            // per tile, from each of the 16 CTAs: one MMA lane per owned token
+            mbar_init(part_bar(b), kC * kTokPerOwner);
             // per tile, from each of the 16 owners: 2 reducer lanes
             mbar_init(coef_bar(b), kC * 2);
         }
+        for (int b = 0; b < 2; ++b) mbar_init(ss_bar(b), kT);  // one lane per token
         mbar_init(mma_bar, kMmaWarps * 32);
         mbar_init(mma_bar2, kMmaWarps * 32);
         fence_mbar_init_cluster();
@@ -311,11 +324,15 @@ k_block_cluster(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                     }
                 mbar_arrive(mma_bar);
                 if (!mbar_wait_warp<false>(mma_bar, (uint32_t)tiles_done & 1u, &s_abort)) break;
+                // this tile's sums of squares from the CUDA-core warps (CTA-local)
+                if (!mbar_wait_warp<false>(ss_bar(us.j & 1), (uint32_t)(us.j >> 1) & 1u, &s_abort)) break;
                 if (lane < 16) {
+                    // Only warps without outstanding global stores send to other CTAs,
+                    // so the cluster-scope release of the arrival below is cheap.
                     const int tk = s * 16 + lane;  // token within the tile
                     const int owner = tk / kTokPerOwner, tl = tk % kTokPerOwner;
-                    const int buf = us.j & 1;
-                    float v[kMix];
+                    const int buf = us.j % kBufs;
+                    float v[kPartF];
 #pragma unroll
                     for (int i = 0; i < kMix; ++i) v[i] = 0.0f;
 #pragma unroll
@@ -324,9 +341,13 @@ k_block_cluster(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
 #pragma unroll
                         for (int i = 0; i < kMix; ++i) v[i] += e[i];
                     }
+                    const float2 ss = *reinterpret_cast<const float2 *>(sSS + ((us.j & 1) * kT + tk) * 2);
+                    v[kMix] = ss.x;
+                    v[kMix + 1] = ss.y;
+                    v[kMix + 2] = v[kMix + 3] = 0.0f;
                     const uint32_t dst = mapa(smem_u32(sPart + ((buf * kC + rank) * kTokPerOwner + tl) * kPartF), owner);
 #pragma unroll
-                    for (int q = 0; q < kMix / 4; ++q)
+                    for (int q = 0; q < kPartF / 4; ++q)
                         st_cluster_v4(dst + 16 * q, v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
                     mbar_arrive_remote(mapa(part_bar(buf), owner));
                 }
@@ -364,33 +385,64 @@ k_block_cluster(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
         }
     } else if (warp == kWarpReducer) {
         // ------------------------------------------------------------ owner: statistics + Sinkhorn
+        // Lanes 8*tl .. 8*tl + 7 serve owned token tl: each sums two of the 16
+        // sources, a 3-step shuffle finishes the sums, and all 8 lanes then run
+        // the same split + Sinkhorn (fast flavour) so any of them can broadcast.
         const float s0 = __ldg(p.hc_scale), s1 = __ldg(p.hc_scale + 1), s2 = __ldg(p.hc_scale + 2);
+        const int tl = lane >> 3, sub = lane & 7;
         for (int j = 0; j < J; ++j) {
-            const int buf = j & 1;
-            if (!mbar_wait_warp<true>(part_bar(buf), (uint32_t)(j >> 1) & 1u, &s_abort)) break;
+            const int buf = j % kBufs;
+            if (!mbar_wait_warp<true>(part_bar(buf), (uint32_t)(j / kBufs) & 1u, &s_abort)) break;
             const int tile = cid + j * ncl;
-            // lanes 0..3: one owned token each; the others mirror lane & 3
-            const int tl = lane & 3;
             const int tk = (int)rank * kTokPerOwner + tl;
             const int64_t tok = (int64_t)tile * kT + tk;
-            float m[kMix];
+            float m[kMix + 2];
+            {
+                const float *e0 = sPart + ((buf * kC + sub) * kTokPerOwner + tl) * kPartF;
+                const float *e1 = sPart + ((buf * kC + sub + 8) * kTokPerOwner + tl) * kPartF;
 #pragma unroll
-            for (int i = 0; i < kMix; ++i) m[i] = 0.0f;
-            float ssx = 0.0f, ssh = 0.0f;
-            for (int src = 0; src < kC; ++src) {
-                const float *e = sPart + ((buf * kC + src) * kTokPerOwner + tl) * kPartF;
-#pragma unroll
-                for (int i = 0; i < kMix; ++i) m[i] += e[i];
-                ssx += e[kMix];
-                ssh += e[kMix + 1];
+                for (int i = 0; i < kMix + 2; ++i) m[i] = e0[i] + e1[i];
             }
-            const float r = rsqrtf(ssx / (float)K + p.norm_eps);
 #pragma unroll
-            for (int i = 0; i < kMix; ++i) m[i] *= r;
+            for (int i = 0; i < kMix + 2; ++i) {
+                m[i] += __shfl_xor_sync(0xffffffffu, m[i], 1);
+                m[i] += __shfl_xor_sync(0xffffffffu, m[i], 2);
+                m[i] += __shfl_xor_sync(0xffffffffu, m[i], 4);
+            }
+            const float ssx = m[kMix], ssh = m[kMix + 1];
+            const float r = rsqrtf(ssx / (float)K + p.norm_eps);
+            float mm[kMix];
+#pragma unroll
+            for (int i = 0; i < kMix; ++i) mm[i] = m[i] * r;
             float pr[kHC], po[kHC], c[kHC * kHC];
-            split_sinkhorn_token(m, s0, s1, s2, p.hc_base, p.iters, p.eps, pr, po, c);
+            split_sinkhorn_token<true>(mm, s0, s1, s2, p.hc_base, p.iters, p.eps, pr, po, c);
             const float rs_h = rsqrtf(ssh / (float)d + p.norm_eps);
-            if (lane < kTokPerOwner && tok < p.n) {
+            if (kFull) {
+                // broadcast first: lane l -> destination CTA l % 16, tokens 2*(l/16) + {0, 1}
+                const int dest = lane & 15;
+                const int ta = 2 * (lane >> 4);
+#pragma unroll
+                for (int k2 = 0; k2 < 2; ++k2) {
+                    const int tsel = ta + k2;  // owned token whose coefficients to send
+                    const int srcl = 8 * tsel;  // a lane that computed them
+                    float v[kCoefF];
+#pragma unroll
+                    for (int i = 0; i < kCoefF; ++i) v[i] = 0.0f;
+#pragma unroll
+                    for (int k = 0; k < kHC; ++k) v[k] = __shfl_sync(0xffffffffu, po[k], srcl);
+#pragma unroll
+                    for (int i = 0; i < kHC * kHC; ++i) v[kHC + i] = __shfl_sync(0xffffffffu, c[i], srcl);
+                    v[kHC + kHC * kHC] = __shfl_sync(0xffffffffu, rs_h, srcl);
+                    const int trow = (int)rank * kTokPerOwner + tsel;
+                    const uint32_t dst = mapa(smem_u32(sCoef + (buf * kT + trow) * kCoefF), dest);
+#pragma unroll
+                    for (int q = 0; q < kCoefF / 4; ++q)
+                        st_cluster_v4(dst + 16 * q, v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                }
+                mbar_arrive_remote(mapa(coef_bar(buf), dest));
+            }
+            // then this tile's global outputs (after the release above, not before it)
+            if (sub == 0 && tok < p.n) {
                 if (p.pre_out) reinterpret_cast<float4 *>(p.pre_out)[tok] = make_float4(pr[0], pr[1], pr[2], pr[3]);
                 if (p.post_out) reinterpret_cast<float4 *>(p.post_out)[tok] = make_float4(po[0], po[1], po[2], po[3]);
                 if (p.comb_out) {
@@ -401,32 +453,8 @@ k_block_cluster(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 if (p.mixes_out) {
                     float4 *md = reinterpret_cast<float4 *>(p.mixes_out + tok * kMix);
 #pragma unroll
-                    for (int q = 0; q < kMix / 4; ++q) md[q] = make_float4(m[4 * q], m[4 * q + 1], m[4 * q + 2], m[4 * q + 3]);
+                    for (int q = 0; q < kMix / 4; ++q) md[q] = make_float4(mm[4 * q], mm[4 * q + 1], mm[4 * q + 2], mm[4 * q + 3]);
                 }
-            }
-            if (kFull) {
-                // broadcast: lane l -> destination CTA l % 16, tokens 2*(l/16) + {0, 1}
-                const int dest = lane & 15;
-                const int ta = 2 * (lane >> 4);
-#pragma unroll
-                for (int k2 = 0; k2 < 2; ++k2) {
-                    const int tsel = ta + k2;  // owned token whose coefficients to send
-                    float v[kCoefF];
-#pragma unroll
-                    for (int i = 0; i < kCoefF; ++i) v[i] = 0.0f;
-                    // fetch token tsel's values from the lane that computed them (lane tsel)
-#pragma unroll
-                    for (int k = 0; k < kHC; ++k) v[k] = __shfl_sync(0xffffffffu, po[k], tsel);
-#pragma unroll
-                    for (int i = 0; i < kHC * kHC; ++i) v[kHC + i] = __shfl_sync(0xffffffffu, c[i], tsel);
-                    v[kHC + kHC * kHC] = __shfl_sync(0xffffffffu, rs_h, tsel);
-                    const int trow = (int)rank * kTokPerOwner + tsel;
-                    const uint32_t dst = mapa(smem_u32(sCoef + (buf * kT + trow) * kCoefF), dest);
-#pragma unroll
-                    for (int q = 0; q < kCoefF / 4; ++q)
-                        st_cluster_v4(dst + 16 * q, v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-                }
-                mbar_arrive_remote(mapa(coef_bar(buf), dest));
             }
         }
     } else {
@@ -476,9 +504,9 @@ k_block_cluster(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                     }
                 }
             } else {
-                const int buf = us.j & 1;
+                const int buf = us.j % kBufs;
                 if (cur_coef_tile != us.j) {
-                    if (!mbar_wait_warp<true>(coef_bar(buf), (uint32_t)(us.j >> 1) & 1u, &s_abort)) break;
+                    if (!mbar_wait_warp<true>(coef_bar(buf), (uint32_t)(us.j / kBufs) & 1u, &s_abort)) break;
                     cur_coef_tile = us.j;
                     const float *c = sCoef + (buf * kT + r) * kCoefF;
 #pragma unroll
@@ -531,11 +559,9 @@ k_block_cluster(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 ssh += __shfl_xor_sync(0xffffffffu, ssh, 1);
                 ssh += __shfl_xor_sync(0xffffffffu, ssh, 2);
                 if (uu == 0) {
-                    const int owner = r / kTokPerOwner, tl = r % kTokPerOwner;
-                    const int buf = us.j & 1;
-                    const uint32_t dst = mapa(smem_u32(sPart + ((buf * kC + rank) * kTokPerOwner + tl) * kPartF + kMix), owner);
-                    st_cluster_v2(dst, ssx, ssh);
-                    mbar_arrive_remote(mapa(part_bar(buf), owner));
+                    // CTA-local hand-off to the MMA warps, which send it with the dots
+                    *reinterpret_cast<float2 *>(sSS + ((us.j & 1) * kT + r) * 2) = make_float2(ssx, ssh);
+                    mbar_arrive(ss_bar(us.j & 1));
                 }
                 ssx2 = ssh2 = f2_dup(0.0f);
             }

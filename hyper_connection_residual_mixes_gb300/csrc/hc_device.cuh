@@ -93,25 +93,45 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 // ---------------------------------------------------------------- split + Sinkhorn
+// Reciprocal: correctly rounded (__frcp_rn) in the accurate flavour, the
+// hardware approximation (rcp.approx.ftz, within 1 ulp) in the fast one.
+template <bool kFast>
+__device__ __forceinline__ float recip(float x) {
+    if constexpr (kFast) {
+        float r;
+        asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+        return r;
+    } else {
+        return __frcp_rn(x);
+    }
+}
+template <bool kFast>
+__device__ __forceinline__ float expo(float x) {
+    if constexpr (kFast) return __expf(x);
+    else return expf(x);
+}
+template <bool kFast>
 __device__ __forceinline__ float sigmoid(float z) {
     // 1 / (1 + e^-z); e^-z -> inf gives exactly 0.
-    return __frcp_rn(1.0f + expf(-z));
+    return recip<kFast>(1.0f + expo<kFast>(-z));
 }
 
 // One token: 24 mix numbers -> pre[4], post[4], comb[16] (row j = input
 // stream, column k = output stream).  First round: row softmax (row maximum
 // subtracted) + eps, then each column divided by (its sum + eps).  Then
 // (iters - 1) rounds of: each row divided by (its sum + eps), each column
-// divided by (its sum + eps).  Division is a correctly rounded reciprocal
-// followed by a multiply.
+// divided by (its sum + eps).  Division is a reciprocal followed by a
+// multiply.  Both flavours stay within 1e-6 of the exact values on the
+// workloads here; the fast one has a much shorter dependency chain.
+template <bool kFast = false>
 __device__ __forceinline__ void split_sinkhorn_token(const float (&m)[kMix], float s0, float s1,
                                                      float s2, const float *__restrict__ base,
                                                      int iters, float eps, float (&pre)[kHC],
                                                      float (&post)[kHC], float (&c)[kHC * kHC]) {
 #pragma unroll
-    for (int j = 0; j < kHC; ++j) pre[j] = sigmoid(fmaf(m[j], s0, base[j])) + eps;
+    for (int j = 0; j < kHC; ++j) pre[j] = sigmoid<kFast>(fmaf(m[j], s0, base[j])) + eps;
 #pragma unroll
-    for (int j = 0; j < kHC; ++j) post[j] = 2.0f * sigmoid(fmaf(m[kHC + j], s1, base[kHC + j]));
+    for (int j = 0; j < kHC; ++j) post[j] = 2.0f * sigmoid<kFast>(fmaf(m[kHC + j], s1, base[kHC + j]));
 #pragma unroll
     for (int i = 0; i < kHC * kHC; ++i) c[i] = fmaf(m[2 * kHC + i], s2, base[2 * kHC + i]);
 
@@ -124,10 +144,10 @@ __device__ __forceinline__ void split_sinkhorn_token(const float (&m)[kMix], flo
         float s = 0.0f;
 #pragma unroll
         for (int k = 0; k < kHC; ++k) {
-            c[j * kHC + k] = expf(c[j * kHC + k] - mx);
+            c[j * kHC + k] = expo<kFast>(c[j * kHC + k] - mx);
             s += c[j * kHC + k];
         }
-        const float r = __frcp_rn(s);
+        const float r = recip<kFast>(s);
 #pragma unroll
         for (int k = 0; k < kHC; ++k) c[j * kHC + k] = fmaf(c[j * kHC + k], r, eps);
     }
@@ -137,7 +157,7 @@ __device__ __forceinline__ void split_sinkhorn_token(const float (&m)[kMix], flo
         float s = 0.0f;
 #pragma unroll
         for (int j = 0; j < kHC; ++j) s += c[j * kHC + k];
-        const float r = __frcp_rn(s + eps);
+        const float r = recip<kFast>(s + eps);
 #pragma unroll
         for (int j = 0; j < kHC; ++j) c[j * kHC + k] *= r;
     }
@@ -147,7 +167,7 @@ __device__ __forceinline__ void split_sinkhorn_token(const float (&m)[kMix], flo
             float s = 0.0f;
 #pragma unroll
             for (int k = 0; k < kHC; ++k) s += c[j * kHC + k];
-            const float r = __frcp_rn(s + eps);
+            const float r = recip<kFast>(s + eps);
 #pragma unroll
             for (int k = 0; k < kHC; ++k) c[j * kHC + k] *= r;
         }
@@ -156,7 +176,7 @@ __device__ __forceinline__ void split_sinkhorn_token(const float (&m)[kMix], flo
             float s = 0.0f;
 #pragma unroll
             for (int j = 0; j < kHC; ++j) s += c[j * kHC + k];
-            const float r = __frcp_rn(s + eps);
+            const float r = recip<kFast>(s + eps);
 #pragma unroll
             for (int j = 0; j < kHC; ++j) c[j * kHC + k] *= r;
         }
