@@ -50,13 +50,30 @@ namespace cl {
 
 constexpr int kC = 16;          // CTAs per cluster = column slices of d
 constexpr int kT = 64;          // tokens per tile
-constexpr int kCB = 32;         // columns per slot (per stream)
-constexpr int kSlots = 7;       // TMA ring depth (140 KB in flight per SM)
-constexpr int kLag = 2;         // phase 3 of tile j runs after phase 1 of tile j + kLag
+#ifndef HC_CB
+#define HC_CB 64
+#endif
+constexpr int kCB = HC_CB;      // columns per slot (per stream): 32 (64-byte rows) or 64 (128-byte rows)
+constexpr int kUnits = kCB / 8;  // 16-byte units per box row
+constexpr int kItems = kUnits / 4;  // 8-column items per CUDA-core thread per slot
+constexpr int kStepsPerSlot = kCB / 16;  // k16 MMA steps per stream per slot
+static_assert(kCB == 32 || kCB == 64, "column block must be 32 or 64");
+// Tuning knobs (compile-time): ring depth and the phase-3 lag.
+#ifndef HC_SLOTS
+#define HC_SLOTS 4
+#endif
+#ifndef HC_LAG
+#define HC_LAG 1
+#endif
+#ifndef HC_STORE_EVICT_FIRST
+#define HC_STORE_EVICT_FIRST 1
+#endif
+constexpr int kSlots = HC_SLOTS;  // TMA ring depth (20 KB per slot)
+constexpr int kLag = HC_LAG;      // phase 3 of tile j runs after phase 1 of tile j + kLag
 constexpr int kBufs = kLag + 1; // partial / coefficient buffers in rotation
 constexpr uint32_t kTmemCols = 512;  // the whole tensor memory of the SM (1 CTA per SM)
 constexpr int kThreads = 448;
-constexpr int kBoxBytes = kT * kCB * 2;             // 4096: 64 tokens x 32 bf16
+constexpr int kBoxBytes = kT * kCB * 2;             // 64 tokens x kCB bf16
 constexpr int kStageXBytes = kHC * kBoxBytes;       // 16384
 constexpr int kSlotBytes = kStageXBytes + kBoxBytes;  // + f box = 20480
 constexpr int kTokPerOwner = kT / kC;               // 4
@@ -102,7 +119,7 @@ __host__ __device__ inline Layout make_layout(int d) {
     Layout L;
     L.dc = d / kC;
     L.ncb = L.dc / kCB;
-    L.wcols = kWCols * 2 * L.ncb;
+    L.wcols = kWCols * (L.dc / 16);
     int o = kSlots * kSlotBytes;
     L.off_coef = o;
     o += kBufs * kT * kCoefF * 4;
@@ -133,9 +150,12 @@ __device__ __forceinline__ void split3(float w0, float w1, uint32_t &hi, uint32_
     lo = pack_bf16x2(s0, s1);
 }
 
-// Byte offset of (row r, 16-byte unit u) inside a 64-byte-swizzled box of 64-byte rows.
-__device__ __forceinline__ uint32_t sw64(int r, int u) {
-    return (uint32_t)(r * 64 + ((u ^ ((r >> 1) & 3)) << 4));
+// Byte offset of (row r, 16-byte unit u) inside a TMA box of kCB-column rows,
+// written with the 64-byte (kCB = 32) or 128-byte (kCB = 64) swizzle: the
+// unit index is XORed with address bits 7-8 (resp. 7-9).
+__device__ __forceinline__ uint32_t swz(int r, int u) {
+    if constexpr (kCB == 32) return (uint32_t)(r * 64 + ((u ^ ((r >> 1) & 3)) << 4));
+    else return (uint32_t)(r * 128 + ((u ^ (r & 7)) << 4));
 }
 
 // The ring walks, per cluster, blocks of `ncb` slot uses:
@@ -249,14 +269,13 @@ k_block_cluster(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
         const int s = warp - kWarpMma;  // this warp's stream
         const int g = lane >> 2, t = lane & 3;
         // B fragments of the resident weights in TMEM lane 32*s + lane: k16 step
-        // q (column block q / 2, half q % 2 of this CTA's columns of stream s)
-        // occupies columns 18q .. 18q + 17 as, per n-tile nt, the bf16x2 pairs
+        // q (columns 16q .. 16q + 15 of this CTA's slice of stream s) occupies
+        // TMEM columns 18q .. 18q + 17 as, per n-tile nt, the bf16x2 pairs
         // hi(b0), hi(b1), mid(b0), mid(b1), lo(b0), lo(b1) of
         // W[nt*8+g][k0+2t, k0+2t+1] (b0) and W[nt*8+g][k0+8+2t, k0+9+2t] (b1).
         const uint32_t tw = tmem_base + ((uint32_t)(32 * (warp & 3)) << 16);
-        for (int q = 0; q < 2 * ncb; ++q) {
-            const int cb = q >> 1, h = q & 1;
-            const int64_t col = (int64_t)s * d + (int64_t)rank * dc + cb * kCB + h * 16 + 2 * t;
+        for (int q = 0; q < dc / 16; ++q) {  // k16 step q = columns 16q .. 16q + 15 of the slice
+            const int64_t col = (int64_t)s * d + (int64_t)rank * dc + 16 * q + 2 * t;
 #pragma unroll
             for (int nt = 0; nt < 3; ++nt) {
                 const float *wr = p.hc_fn + (int64_t)(nt * 8 + g) * K + col;
@@ -286,23 +305,27 @@ k_block_cluster(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             if (!mbar_wait_warp<false>(full_bar(slot), ph, &s_abort)) break;
             const Use us = decode_use(u, ncb, J, kFull);
             if (!us.p3) {
-                uint32_t bw[36];
-                tmem_ld36(tw + 2 * kWCols * us.cb, bw);
-                tmem_wait_ld36(bw);
                 const uint32_t box = slot0 + slot * kSlotBytes + s * kBoxBytes;
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
+                for (int hp = 0; hp < kStepsPerSlot / 2; ++hp) {  // pairs of k16 steps
+                    uint32_t bw[36];
+                    tmem_ld36(tw + kWCols * (us.cb * kStepsPerSlot + 2 * hp), bw);
+                    tmem_wait_ld36(bw);
 #pragma unroll
-                    for (int mt = 0; mt < 4; ++mt) {
-                        const int r = mt * 16 + (lane & 15);
-                        uint32_t a0, a1, a2, a3;
-                        ldmatrix_x4(box + sw64(r, 2 * h + (lane >> 4)), a0, a1, a2, a3);
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        const int h = 2 * hp + h2;
 #pragma unroll
-                        for (int nt = 0; nt < 3; ++nt) {
-                            const uint32_t *b = bw + kWCols * h + 6 * nt;
-                            mma_bf16_16816(acc[mt][nt], a0, a1, a2, a3, b[4], b[5]);  // lo
-                            mma_bf16_16816(acc[mt][nt], a0, a1, a2, a3, b[2], b[3]);  // mid
-                            mma_bf16_16816(acc[mt][nt], a0, a1, a2, a3, b[0], b[1]);  // hi
+                        for (int mt = 0; mt < 4; ++mt) {
+                            const int r = mt * 16 + (lane & 15);
+                            uint32_t a0, a1, a2, a3;
+                            ldmatrix_x4(box + swz(r, 2 * h + (lane >> 4)), a0, a1, a2, a3);
+#pragma unroll
+                            for (int nt = 0; nt < 3; ++nt) {
+                                const uint32_t *b = bw + kWCols * h2 + 6 * nt;
+                                mma_bf16_16816(acc[mt][nt], a0, a1, a2, a3, b[4], b[5]);  // lo
+                                mma_bf16_16816(acc[mt][nt], a0, a1, a2, a3, b[2], b[3]);  // mid
+                                mma_bf16_16816(acc[mt][nt], a0, a1, a2, a3, b[0], b[1]);  // hi
+                            }
                         }
                     }
                 }
@@ -459,15 +482,17 @@ k_block_cluster(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
         }
     } else {
         // ------------------------------------------------------------ CUDA-core streaming math
-        // 256 threads; per slot, thread tc handles the 8-column unit uu = tc % 4 of
-        // token row r = tc / 4, as four packed fp32 pairs per stream.
+        // 256 threads; per slot, thread tc handles token row r = tc / 4 and the
+        // 8-column units uu + 4i (i < kItems), as four packed fp32 pairs per stream.
         const int tc = threadIdx.x - kWarpCuda * 32;  // 0..255
         const int uu = tc & 3;
         const int r = tc >> 2;
         f32x2 pm[kHC];  // pre_mix of the token, duplicated into both lanes
         f32x2 ssx2 = f2_dup(0.0f), ssh2 = f2_dup(0.0f);
-        float cf[kHC + kHC * kHC + 1];  // post, comb, RMSNorm scale of the token
+        f32x2 cf2[kHC + kHC * kHC];  // post, comb of the token, duplicated into both lanes
+        f32x2 rs2 = f2_dup(0.0f);     // RMSNorm scale of the token
         int cur_coef_tile = -1;
+        const uint64_t pol_out = HC_STORE_EVICT_FIRST ? policy_evict_first() : policy_evict_normal();
         for (int u = 0; u < U; ++u) {
             const int slot = u % kSlots;
             const uint32_t ph = (uint32_t)(u / kSlots) & 1u;
@@ -482,25 +507,29 @@ k_block_cluster(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 if (kFull && tok < p.n) v = __ldg(reinterpret_cast<const float4 *>(p.pre_mix) + tok);
                 pm[0] = f2_dup(v.x); pm[1] = f2_dup(v.y); pm[2] = f2_dup(v.z); pm[3] = f2_dup(v.w);
             }
-            uint4 xr[kHC];
-#pragma unroll
-            for (int s = 0; s < kHC; ++s) xr[s] = *reinterpret_cast<const uint4 *>(sb + s * kBoxBytes + sw64(r, uu));
             if (!us.p3) {
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    f32x2 xs[kHC];
+                for (int it = 0; it < kItems; ++it) {
+                    const int un = uu + 4 * it;
+                    uint4 xr[kHC];
 #pragma unroll
-                    for (int s = 0; s < kHC; ++s) {
-                        xs[s] = f2_from_bf16x2(q == 0 ? xr[s].x : q == 1 ? xr[s].y : q == 2 ? xr[s].z : xr[s].w);
-                        ssx2 = f2_fma(xs[s], xs[s], ssx2);
-                    }
-                    if (kFull) {
-                        f32x2 h = f2_mul(pm[0], xs[0]);
-                        h = f2_fma(pm[1], xs[1], h);
-                        h = f2_fma(pm[2], xs[2], h);
-                        h = f2_fma(pm[3], xs[3], h);
-                        const f32x2 hr = f2_from_bf16x2(f2_to_bf16x2(h));
-                        ssh2 = f2_fma(hr, hr, ssh2);
+                    for (int s = 0; s < kHC; ++s) xr[s] = *reinterpret_cast<const uint4 *>(sb + s * kBoxBytes + swz(r, un));
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        f32x2 xs[kHC];
+#pragma unroll
+                        for (int s = 0; s < kHC; ++s) {
+                            xs[s] = f2_from_bf16x2(q == 0 ? xr[s].x : q == 1 ? xr[s].y : q == 2 ? xr[s].z : xr[s].w);
+                            ssx2 = f2_fma(xs[s], xs[s], ssx2);
+                        }
+                        if (kFull) {
+                            f32x2 h = f2_mul(pm[0], xs[0]);
+                            h = f2_fma(pm[1], xs[1], h);
+                            h = f2_fma(pm[2], xs[2], h);
+                            h = f2_fma(pm[3], xs[3], h);
+                            const f32x2 hr = f2_from_bf16x2(f2_to_bf16x2(h));
+                            ssh2 = f2_fma(hr, hr, ssh2);
+                        }
                     }
                 }
             } else {
@@ -510,49 +539,58 @@ k_block_cluster(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                     cur_coef_tile = us.j;
                     const float *c = sCoef + (buf * kT + r) * kCoefF;
 #pragma unroll
-                    for (int q = 0; q < kHC + kHC * kHC + 1; ++q) cf[q] = c[q];
+                    for (int q = 0; q < kHC + kHC * kHC; ++q) cf2[q] = f2_dup(c[q]);
+                    rs2 = f2_dup(c[kHC + kHC * kHC]);
                 }
-                const uint4 fr = *reinterpret_cast<const uint4 *>(sb + kStageXBytes + sw64(r, uu));
                 if (tok < p.n) {
-                    const float4 *nw = reinterpret_cast<const float4 *>(sNormW + us.cb * kCB + uu * 8);
-                    const float4 w0 = nw[0], w1 = nw[1];
-                    const f32x2 wv[4] = {f2_make(w0.x, w0.y), f2_make(w0.z, w0.w), f2_make(w1.x, w1.y),
-                                         f2_make(w1.z, w1.w)};
-                    const int64_t cbase = (int64_t)rank * dc + us.cb * kCB + uu * 8;
-                    uint32_t yo[kHC][4], ho[4];
-                    const f32x2 rs2 = f2_dup(cf[kHC + kHC * kHC]);
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        f32x2 xs[kHC];
+                    for (int it = 0; it < kItems; ++it) {
+                        const int un = uu + 4 * it;
+                        uint4 xr[kHC];
 #pragma unroll
-                        for (int s = 0; s < kHC; ++s)
-                            xs[s] = f2_from_bf16x2(q == 0 ? xr[s].x : q == 1 ? xr[s].y : q == 2 ? xr[s].z : xr[s].w);
-                        const f32x2 fv = f2_from_bf16x2(q == 0 ? fr.x : q == 1 ? fr.y : q == 2 ? fr.z : fr.w);
+                        for (int s = 0; s < kHC; ++s) xr[s] = *reinterpret_cast<const uint4 *>(sb + s * kBoxBytes + swz(r, un));
+                        const uint4 fr = *reinterpret_cast<const uint4 *>(sb + kStageXBytes + swz(r, un));
+                        const float4 *nw = reinterpret_cast<const float4 *>(sNormW + us.cb * kCB + un * 8);
+                        const float4 w0 = nw[0], w1 = nw[1];
+                        const f32x2 wv[4] = {f2_make(w0.x, w0.y), f2_make(w0.z, w0.w), f2_make(w1.x, w1.y),
+                                             f2_make(w1.z, w1.w)};
+                        const int64_t cbase = (int64_t)rank * dc + us.cb * kCB + un * 8;
+                        uint32_t yo[kHC][4], ho[4];
 #pragma unroll
-                        for (int k = 0; k < kHC; ++k) {
-                            f32x2 a = f2_mul(f2_dup(cf[k]), fv);
+                        for (int q = 0; q < 4; ++q) {
+                            f32x2 xs[kHC];
 #pragma unroll
-                            for (int jj = 0; jj < kHC; ++jj) a = f2_fma(f2_dup(cf[kHC + jj * kHC + k]), xs[jj], a);
-                            yo[k][q] = f2_to_bf16x2(a);
+                            for (int s = 0; s < kHC; ++s)
+                                xs[s] = f2_from_bf16x2(q == 0 ? xr[s].x : q == 1 ? xr[s].y : q == 2 ? xr[s].z : xr[s].w);
+                            const f32x2 fv = f2_from_bf16x2(q == 0 ? fr.x : q == 1 ? fr.y : q == 2 ? fr.z : fr.w);
+#pragma unroll
+                            for (int k = 0; k < kHC; ++k) {
+                                f32x2 a = f2_mul(cf2[k], fv);
+#pragma unroll
+                                for (int jj = 0; jj < kHC; ++jj) a = f2_fma(cf2[kHC + jj * kHC + k], xs[jj], a);
+                                yo[k][q] = f2_to_bf16x2(a);
+                            }
+                            f32x2 h = f2_mul(pm[0], xs[0]);
+                            h = f2_fma(pm[1], xs[1], h);
+                            h = f2_fma(pm[2], xs[2], h);
+                            h = f2_fma(pm[3], xs[3], h);
+                            const f32x2 hr = f2_from_bf16x2(f2_to_bf16x2(h));
+                            ho[q] = f2_to_bf16x2(f2_mul(f2_mul(hr, rs2), wv[q]));
                         }
-                        f32x2 h = f2_mul(pm[0], xs[0]);
-                        h = f2_fma(pm[1], xs[1], h);
-                        h = f2_fma(pm[2], xs[2], h);
-                        h = f2_fma(pm[3], xs[3], h);
-                        const f32x2 hr = f2_from_bf16x2(f2_to_bf16x2(h));
-                        ho[q] = f2_to_bf16x2(f2_mul(f2_mul(hr, rs2), wv[q]));
-                    }
+                        // outputs are written once and not read here again: keep them from
+                        // displacing the tiles of x that phase 3 still has to re-read from L2
 #pragma unroll
-                    for (int k = 0; k < kHC; ++k)
-                        *reinterpret_cast<uint4 *>(p.y + (tok * kHC + k) * d + cbase) =
-                            make_uint4(yo[k][0], yo[k][1], yo[k][2], yo[k][3]);
-                    *reinterpret_cast<uint4 *>(p.h_norm + tok * d + cbase) = make_uint4(ho[0], ho[1], ho[2], ho[3]);
+                        for (int k = 0; k < kHC; ++k)
+                            st_global_v4_hint(p.y + (tok * kHC + k) * d + cbase, yo[k][0], yo[k][1], yo[k][2],
+                                              yo[k][3], pol_out);
+                        st_global_v4_hint(p.h_norm + tok * d + cbase, ho[0], ho[1], ho[2], ho[3], pol_out);
+                    }
                 }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(empty_bar(slot));
             if (!us.p3 && us.cb == ncb - 1) {
-                // tile finished: this CTA's sums of squares of the token go to its owner
+                // tile finished: this CTA's sums of squares of the token go to the MMA warps
                 float ssx = f2_hsum(ssx2), ssh = f2_hsum(ssh2);
                 ssx += __shfl_xor_sync(0xffffffffu, ssx, 1);
                 ssx += __shfl_xor_sync(0xffffffffu, ssx, 2);
@@ -603,7 +641,8 @@ bool make_tmap(CUtensorMap *m, const void *base, int64_t rows, int64_t cols) {
     cuuint32_t box[2] = {(cuuint32_t)cl::kCB, (cuuint32_t)cl::kT};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
-                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     cl::kCB == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }

@@ -143,6 +143,19 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
     return p;
 }
 
+__device__ __forceinline__ uint64_t policy_evict_normal() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+// 16-byte global store with an L2 eviction-priority hint.
+__device__ __forceinline__ void st_global_v4_hint(void *ptr, uint32_t a, uint32_t b, uint32_t c,
+                                                  uint32_t d, uint64_t policy) {
+    asm volatile("st.global.L2::cache_hint.v4.b32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(ptr), "r"(a),
+                 "r"(b), "r"(c), "r"(d), "l"(policy)
+                 : "memory");
+}
+
 // 2D tiled tensor load into this CTA's shared memory, completing on `bar`.
 // c0 is the innermost coordinate (elements); it must be a multiple of 16 bytes.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, uint32_t bar, int c0,
