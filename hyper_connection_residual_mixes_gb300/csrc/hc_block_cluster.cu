@@ -86,6 +86,7 @@ constexpr int kWarpReducer = 5;
 constexpr int kWarpCuda = 6;    // warps 6..13
 constexpr int kCudaWarps = 8;
 constexpr int kWCols = 18;      // TMEM columns per k16 step: 3 n-tiles x (hi, mid, lo) x (b0, b1)
+constexpr int kPmBufs = 3;      // pre_mix tile buffers: tile j's stays until its phase 3 is under way
 
 struct Params {
     const float *pre_mix;
@@ -112,7 +113,7 @@ struct Layout {
     int dc;        // columns per CTA per stream = d / 16
     int ncb;       // slots per tile = dc / 32
     int wcols;     // tensor-memory columns per MMA warp: 18 per k16 step, 2*ncb steps
-    int off_coef, off_part, off_mma, off_ss, off_normw, off_bar, off_tmem, total;
+    int off_coef, off_part, off_mma, off_ss, off_pm, off_normw, off_bar, off_tmem, total;
 };
 
 __host__ __device__ inline Layout make_layout(int d) {
@@ -129,6 +130,8 @@ __host__ __device__ inline Layout make_layout(int d) {
     o += kMmaWarps * kT * kMix * 4;
     L.off_ss = o;  // CTA-local sums of squares, handed from the CUDA-core to the MMA warps
     o += 2 * kT * 2 * 4;
+    L.off_pm = o;  // pre_mix rows of a tile, copied in with its first slot; 3 tiles in rotation
+    o += kPmBufs * kT * 16;
     L.off_normw = o;
     o += L.dc * 4;
     o = (o + 15) & ~15;
@@ -203,6 +206,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 k_block_cluster(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_f,
                 const Params p) {
     extern __shared__ uint8_t smem_raw[];
+    // (measured: accesses through this generic base pointer are faster here than
+    // through one kept in the shared address space or through explicit ld.shared)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~uintptr_t(1023));
     __shared__ volatile int s_abort;
@@ -394,7 +399,14 @@ k_block_cluster(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 const int row = tile * kT;
                 const int col = (int)rank * dc + us.cb * kCB;
                 const uint32_t dst = slot0 + slot * kSlotBytes;
-                mbar_arrive_expect_tx(full_bar(slot), us.p3 ? kSlotBytes : kStageXBytes);
+                // the tile's pre_mix rows travel with its first phase-1 slot
+                const bool with_pm = kFull && !us.p3 && us.cb == 0;
+                const int64_t rows_left = p.n - (int64_t)row;
+                const uint32_t pm_bytes = with_pm ? 16u * (uint32_t)(rows_left < kT ? rows_left : kT) : 0u;
+                mbar_arrive_expect_tx(full_bar(slot), (us.p3 ? kSlotBytes : kStageXBytes) + pm_bytes);
+                if (with_pm)
+                    bulk_load(smem_u32(smem + L.off_pm) + (us.j % kPmBufs) * kT * 16,
+                              p.pre_mix + (int64_t)row * kHC, pm_bytes, full_bar(slot));
                 for (int s = 0; s < kHC; ++s)
                     tma_load_2d(dst + s * kBoxBytes, &tm_x, full_bar(slot), s * d + col, row,
                                 us.p3 ? pol_stream : pol_keep);
@@ -484,6 +496,9 @@ k_block_cluster(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
         // ------------------------------------------------------------ CUDA-core streaming math
         // 256 threads; per slot, thread tc handles token row r = tc / 4 and the
         // 8-column units uu + 4i (i < kItems), as four packed fp32 pairs per stream.
+        // The slot's data is copied to registers and the slot released at once, so
+        // the ring reloads while this warp computes; outputs go out with 16-byte
+        // global stores.
         const int tc = threadIdx.x - kWarpCuda * 32;  // 0..255
         const int uu = tc & 3;
         const int r = tc >> 2;
@@ -493,6 +508,7 @@ k_block_cluster(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
         f32x2 rs2 = f2_dup(0.0f);     // RMSNorm scale of the token
         int cur_coef_tile = -1;
         const uint64_t pol_out = HC_STORE_EVICT_FIRST ? policy_evict_first() : policy_evict_normal();
+        const float4 *sPm = reinterpret_cast<const float4 *>(smem + L.off_pm);
         for (int u = 0; u < U; ++u) {
             const int slot = u % kSlots;
             const uint32_t ph = (uint32_t)(u / kSlots) & 1u;
@@ -501,25 +517,32 @@ k_block_cluster(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             const int tile = cid + us.j * ncl;
             const int64_t tok = (int64_t)tile * kT + r;
             const uint8_t *sb = smem + slot * kSlotBytes;
+            uint4 xr[kItems][kHC], fr[kItems];
+#pragma unroll
+            for (int it = 0; it < kItems; ++it) {
+#pragma unroll
+                for (int s = 0; s < kHC; ++s)
+                    xr[it][s] = *reinterpret_cast<const uint4 *>(sb + s * kBoxBytes + swz(r, uu + 4 * it));
+                if (us.p3) fr[it] = *reinterpret_cast<const uint4 *>(sb + kStageXBytes + swz(r, uu + 4 * it));
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty_bar(slot));  // after this warp's loads of the slot
             if (us.cb == 0) {
-                // pre_mix of this thread's token for the tile of this use
+                // pre_mix of this thread's token (copied in with the tile's first slot)
                 float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (kFull && tok < p.n) v = __ldg(reinterpret_cast<const float4 *>(p.pre_mix) + tok);
+                if (kFull && tok < p.n) v = sPm[(us.j % kPmBufs) * kT + r];
                 pm[0] = f2_dup(v.x); pm[1] = f2_dup(v.y); pm[2] = f2_dup(v.z); pm[3] = f2_dup(v.w);
             }
             if (!us.p3) {
 #pragma unroll
                 for (int it = 0; it < kItems; ++it) {
-                    const int un = uu + 4 * it;
-                    uint4 xr[kHC];
-#pragma unroll
-                    for (int s = 0; s < kHC; ++s) xr[s] = *reinterpret_cast<const uint4 *>(sb + s * kBoxBytes + swz(r, un));
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         f32x2 xs[kHC];
 #pragma unroll
                         for (int s = 0; s < kHC; ++s) {
-                            xs[s] = f2_from_bf16x2(q == 0 ? xr[s].x : q == 1 ? xr[s].y : q == 2 ? xr[s].z : xr[s].w);
+                            const uint4 &w = xr[it][s];
+                            xs[s] = f2_from_bf16x2(q == 0 ? w.x : q == 1 ? w.y : q == 2 ? w.z : w.w);
                             ssx2 = f2_fma(xs[s], xs[s], ssx2);
                         }
                         if (kFull) {
@@ -546,10 +569,6 @@ k_block_cluster(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
 #pragma unroll
                     for (int it = 0; it < kItems; ++it) {
                         const int un = uu + 4 * it;
-                        uint4 xr[kHC];
-#pragma unroll
-                        for (int s = 0; s < kHC; ++s) xr[s] = *reinterpret_cast<const uint4 *>(sb + s * kBoxBytes + swz(r, un));
-                        const uint4 fr = *reinterpret_cast<const uint4 *>(sb + kStageXBytes + swz(r, un));
                         const float4 *nw = reinterpret_cast<const float4 *>(sNormW + us.cb * kCB + un * 8);
                         const float4 w0 = nw[0], w1 = nw[1];
                         const f32x2 wv[4] = {f2_make(w0.x, w0.y), f2_make(w0.z, w0.w), f2_make(w1.x, w1.y),
@@ -560,9 +579,12 @@ k_block_cluster(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                         for (int q = 0; q < 4; ++q) {
                             f32x2 xs[kHC];
 #pragma unroll
-                            for (int s = 0; s < kHC; ++s)
-                                xs[s] = f2_from_bf16x2(q == 0 ? xr[s].x : q == 1 ? xr[s].y : q == 2 ? xr[s].z : xr[s].w);
-                            const f32x2 fv = f2_from_bf16x2(q == 0 ? fr.x : q == 1 ? fr.y : q == 2 ? fr.z : fr.w);
+                            for (int s = 0; s < kHC; ++s) {
+                                const uint4 &w = xr[it][s];
+                                xs[s] = f2_from_bf16x2(q == 0 ? w.x : q == 1 ? w.y : q == 2 ? w.z : w.w);
+                            }
+                            const uint4 &fw = fr[it];
+                            const f32x2 fv = f2_from_bf16x2(q == 0 ? fw.x : q == 1 ? fw.y : q == 2 ? fw.z : fw.w);
 #pragma unroll
                             for (int k = 0; k < kHC; ++k) {
                                 f32x2 a = f2_mul(cf2[k], fv);
@@ -587,8 +609,6 @@ k_block_cluster(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                     }
                 }
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(empty_bar(slot));
             if (!us.p3 && us.cb == ncb - 1) {
                 // tile finished: this CTA's sums of squares of the token go to the MMA warps
                 float ssx = f2_hsum(ssx2), ssh = f2_hsum(ssh2);
