@@ -33,10 +33,11 @@
 //    Sinkhorn in registers, writes pre/post/comb, and broadcasts post, comb
 //    and the RMSNorm scale back to all 16 CTAs.
 //
-// Warp roles (448 threads): warps 0-3 tensor-core MMA (warp w: stream w, TMEM
+// Warp roles (480 threads): warps 0-3 tensor-core MMA (warp w: stream w, TMEM
 // quadrant w); warp 4 TMA producer; warp 5 owner-side reduction + Sinkhorn +
-// broadcast; warps 6-13 CUDA-core streaming math (one 8-column unit of one
-// token per thread per slot, packed f32x2 arithmetic).
+// broadcast; warps 6-13 CUDA-core streaming math (two 8-column units of one
+// token per thread per slot, packed f32x2 arithmetic); warp 14 sends each
+// tile's partial sums to the owners.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -72,7 +73,7 @@ constexpr int kSlots = HC_SLOTS;  // TMA ring depth (20 KB per slot)
 constexpr int kLag = HC_LAG;      // phase 3 of tile j runs after phase 1 of tile j + kLag
 constexpr int kBufs = kLag + 1; // partial / coefficient buffers in rotation
 constexpr uint32_t kTmemCols = 512;  // the whole tensor memory of the SM (1 CTA per SM)
-constexpr int kThreads = 448;
+constexpr int kThreads = 480;
 constexpr int kBoxBytes = kT * kCB * 2;             // 64 tokens x kCB bf16
 constexpr int kStageXBytes = kHC * kBoxBytes;       // 16384
 constexpr int kSlotBytes = kStageXBytes + kBoxBytes;  // + f box = 20480
@@ -85,6 +86,7 @@ constexpr int kWarpProducer = 4;
 constexpr int kWarpReducer = 5;
 constexpr int kWarpCuda = 6;    // warps 6..13
 constexpr int kCudaWarps = 8;
+constexpr int kWarpSender = 14; // adds up each tile's partial sums and sends them to the owners
 constexpr int kWCols = 18;      // TMEM columns per k16 step: 3 n-tiles x (hi, mid, lo) x (b0, b1)
 constexpr int kPmBufs = 3;      // pre_mix tile buffers: tile j's stays until its phase 3 is under way
 
@@ -230,11 +232,11 @@ k_block_cluster(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     auto empty_bar = [&](int s) { return bar0 + 8u * (kSlots + s); };
     auto part_bar = [&](int b) { return bar0 + 8u * (2 * kSlots + b); };
     auto coef_bar = [&](int b) { return bar0 + 8u * (2 * kSlots + kBufs + b); };
-    // the MMA warps meet twice per tile: before reading each other's sums, and
-    // after the send (so none rewrites its part while another still reads it)
-    const uint32_t mma_bar = bar0 + 8u * (2 * kSlots + 2 * kBufs);
-    const uint32_t mma_bar2 = bar0 + 8u * (2 * kSlots + 2 * kBufs + 1);
-    // the CUDA-core warps hand each tile's sums of squares to the MMA warps
+    // the MMA warps hand each tile's partial dots to the sender warp (full), which
+    // hands the buffer back once it has sent them (free)
+    const uint32_t mma_full = bar0 + 8u * (2 * kSlots + 2 * kBufs);
+    const uint32_t mma_free = bar0 + 8u * (2 * kSlots + 2 * kBufs + 1);
+    // the CUDA-core warps hand each tile's sums of squares to the sender warp
     auto ss_bar = [&](int b) { return bar0 + 8u * (2 * kSlots + 2 * kBufs + 2 + b); };
     float *sSS = reinterpret_cast<float *>(smem + L.off_ss);
     const uint32_t slot0 = smem_u32(smem);
@@ -246,14 +248,14 @@ k_block_cluster(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             mbar_init(empty_bar(s), kMmaWarps + kCudaWarps);
         }
         for (int b = 0; b < kBufs; ++b) {
-            // per tile, from each of the 16 CTAs: one MMA lane per owned token
-            mbar_init(part_bar(b), kC * kTokPerOwner);
+            // per tile, from each of the 16 CTAs: the 2 sender lanes serving this owner
+            mbar_init(part_bar(b), kC * 2);
             // per tile, from each of the 16 owners: 2 reducer lanes
             mbar_init(coef_bar(b), kC * 2);
         }
         for (int b = 0; b < 2; ++b) mbar_init(ss_bar(b), kT);  // one lane per token
-        mbar_init(mma_bar, kMmaWarps * 32);
-        mbar_init(mma_bar2, kMmaWarps * 32);
+        mbar_init(mma_full, kMmaWarps * 32);
+        mbar_init(mma_free, 32);
         fence_mbar_init_cluster();
         prefetch_tmap(&tm_x);
         if (kFull) prefetch_tmap(&tm_f);
@@ -338,8 +340,9 @@ k_block_cluster(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             __syncwarp();
             if (lane == 0) mbar_arrive(empty_bar(slot));
             if (!us.p3 && us.cb == ncb - 1) {
-                // tile finished: combine the four streams' sums, send each token's 24
-                // partial dots to its owner CTA
+                // tile finished: hand this warp's partial dots of the tile's 64 tokens
+                // to the sender warp, once it has drained the previous tile's
+                if (!mbar_wait_warp<false>(mma_free, ((uint32_t)tiles_done & 1u) ^ 1u, &s_abort)) break;
                 float *mine = sMma + s * kT * kMix;
 #pragma unroll
                 for (int mt = 0; mt < 4; ++mt)
@@ -350,39 +353,8 @@ k_block_cluster(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                         *reinterpret_cast<float2 *>(mine + (r + 8) * kMix + c) = make_float2(acc[mt][nt][2], acc[mt][nt][3]);
                         acc[mt][nt][0] = acc[mt][nt][1] = acc[mt][nt][2] = acc[mt][nt][3] = 0.0f;
                     }
-                mbar_arrive(mma_bar);
-                if (!mbar_wait_warp<false>(mma_bar, (uint32_t)tiles_done & 1u, &s_abort)) break;
-                // this tile's sums of squares from the CUDA-core warps (CTA-local)
-                if (!mbar_wait_warp<false>(ss_bar(us.j & 1), (uint32_t)(us.j >> 1) & 1u, &s_abort)) break;
-                if (lane < 16) {
-                    // Only warps without outstanding global stores send to other CTAs,
-                    // so the cluster-scope release of the arrival below is cheap.
-                    const int tk = s * 16 + lane;  // token within the tile
-                    const int owner = tk / kTokPerOwner, tl = tk % kTokPerOwner;
-                    const int buf = us.j % kBufs;
-                    float v[kPartF];
-#pragma unroll
-                    for (int i = 0; i < kMix; ++i) v[i] = 0.0f;
-#pragma unroll
-                    for (int w = 0; w < kMmaWarps; ++w) {
-                        const float *e = sMma + (w * kT + tk) * kMix;
-#pragma unroll
-                        for (int i = 0; i < kMix; ++i) v[i] += e[i];
-                    }
-                    const float2 ss = *reinterpret_cast<const float2 *>(sSS + ((us.j & 1) * kT + tk) * 2);
-                    v[kMix] = ss.x;
-                    v[kMix + 1] = ss.y;
-                    v[kMix + 2] = v[kMix + 3] = 0.0f;
-                    const uint32_t dst = mapa(smem_u32(sPart + ((buf * kC + rank) * kTokPerOwner + tl) * kPartF), owner);
-#pragma unroll
-                    for (int q = 0; q < kPartF / 4; ++q)
-                        st_cluster_v4(dst + 16 * q, v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-                    mbar_arrive_remote(mapa(part_bar(buf), owner));
-                }
-                mbar_arrive(mma_bar2);
-                const bool met = mbar_wait_warp<false>(mma_bar2, (uint32_t)tiles_done & 1u, &s_abort);
+                mbar_arrive(mma_full);
                 ++tiles_done;
-                if (!met) break;
             }
         }
     } else if (warp == kWarpProducer) {
@@ -492,6 +464,43 @@ k_block_cluster(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 }
             }
         }
+    } else if (warp == kWarpSender) {
+        // ------------------------------------------------------------ partial sums -> owners
+        // Per tile: wait for the four MMA warps' partial dots and the CUDA-core
+        // warps' sums of squares, add them up and send each token's numbers to its
+        // owner CTA, then hand the partial buffer back to the MMA warps.  Lane l
+        // serves tokens 2l and 2l + 1, which have the same owner.  This warp makes no
+        // global stores, so its cluster-scope releases do not wait on any.
+        for (int j = 0; j < J; ++j) {
+            if (!mbar_wait_warp<false>(mma_full, (uint32_t)j & 1u, &s_abort)) break;
+            if (!mbar_wait_warp<false>(ss_bar(j & 1), (uint32_t)(j >> 1) & 1u, &s_abort)) break;
+            const int buf = j % kBufs;
+            const int owner = lane >> 1;
+#pragma unroll
+            for (int i2 = 0; i2 < 2; ++i2) {
+                const int tk = 2 * lane + i2;  // token within the tile
+                const int tl = tk % kTokPerOwner;
+                float v[kPartF];
+#pragma unroll
+                for (int i = 0; i < kMix; ++i) v[i] = 0.0f;
+#pragma unroll
+                for (int w = 0; w < kMmaWarps; ++w) {
+                    const float *e = sMma + (w * kT + tk) * kMix;
+#pragma unroll
+                    for (int i = 0; i < kMix; ++i) v[i] += e[i];
+                }
+                const float2 ss = *reinterpret_cast<const float2 *>(sSS + ((j & 1) * kT + tk) * 2);
+                v[kMix] = ss.x;
+                v[kMix + 1] = ss.y;
+                v[kMix + 2] = v[kMix + 3] = 0.0f;
+                const uint32_t dst = mapa(smem_u32(sPart + ((buf * kC + rank) * kTokPerOwner + tl) * kPartF), owner);
+#pragma unroll
+                for (int q = 0; q < kPartF / 4; ++q)
+                    st_cluster_v4(dst + 16 * q, v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+            }
+            mbar_arrive_remote(mapa(part_bar(buf), owner));
+            mbar_arrive(mma_free);  // this lane's reads of the partial buffer are done
+        }
     } else {
         // ------------------------------------------------------------ CUDA-core streaming math
         // 256 threads; per slot, thread tc handles token row r = tc / 4 and the
@@ -525,8 +534,13 @@ k_block_cluster(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                     xr[it][s] = *reinterpret_cast<const uint4 *>(sb + s * kBoxBytes + swz(r, uu + 4 * it));
                 if (us.p3) fr[it] = *reinterpret_cast<const uint4 *>(sb + kStageXBytes + swz(r, uu + 4 * it));
             }
+            // The loads above are still in flight: nothing has used their values yet,
+            // and an mbarrier arrive alone does not wait for them (measured: the ring
+            // refilled the slot under the later loads of a warp that went on to wait
+            // for its coefficients).  A CTA-scope fence completes them first.
+            __threadfence_block();
             __syncwarp();
-            if (lane == 0) mbar_arrive(empty_bar(slot));  // after this warp's loads of the slot
+            if (lane == 0) mbar_arrive(empty_bar(slot));
             if (us.cb == 0) {
                 // pre_mix of this thread's token (copied in with the tile's first slot)
                 float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
