@@ -208,10 +208,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 k_block_cluster(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_f,
                 const Params p) {
     extern __shared__ uint8_t smem_raw[];
-    // (measured: accesses through this generic base pointer are faster here than
-    // through one kept in the shared address space or through explicit ld.shared)
+    // The same 1024-byte aligned base twice: a generic pointer (measured faster for
+    // the handoff buffers) and one derived from the shared array itself, which the
+    // compiler keeps in the shared address space (ld.shared for the slot reads of
+    // the CUDA-core warps, measured faster there).
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~uintptr_t(1023));
+    const uint8_t *smem_ring = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     __shared__ volatile int s_abort;
     const Layout L = make_layout(p.d);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -503,14 +506,17 @@ k_block_cluster(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
         }
     } else {
         // ------------------------------------------------------------ CUDA-core streaming math
-        // 256 threads; per slot, thread tc handles token row r = tc / 4 and the
+        // 256 threads; per slot, each thread handles one token row r and the
         // 8-column units uu + 4i (i < kItems), as four packed fp32 pairs per stream.
+        // Warp w covers rows 8w .. 8w + 7; each quarter-warp takes rows r and r + 4,
+        // whose 16-byte units the 128-byte swizzle puts on complementary halves of
+        // the banks, so its 16-byte loads are free of bank conflicts.
         // The slot's data is copied to registers and the slot released at once, so
         // the ring reloads while this warp computes; outputs go out with 16-byte
         // global stores.
         const int tc = threadIdx.x - kWarpCuda * 32;  // 0..255
-        const int uu = tc & 3;
-        const int r = tc >> 2;
+        const int uu = lane & 3;
+        const int r = 8 * (tc >> 5) + (lane >> 3) + 4 * ((lane >> 2) & 1);
         f32x2 pm[kHC];  // pre_mix of the token, duplicated into both lanes
         f32x2 ssx2 = f2_dup(0.0f), ssh2 = f2_dup(0.0f);
         f32x2 cf2[kHC + kHC * kHC];  // post, comb of the token, duplicated into both lanes
@@ -525,7 +531,7 @@ k_block_cluster(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             const Use us = decode_use(u, ncb, J, kFull);
             const int tile = cid + us.j * ncl;
             const int64_t tok = (int64_t)tile * kT + r;
-            const uint8_t *sb = smem + slot * kSlotBytes;
+            const uint8_t *sb = smem_ring + slot * kSlotBytes;
             uint4 xr[kItems][kHC], fr[kItems];
 #pragma unroll
             for (int it = 0; it < kItems; ++it) {
