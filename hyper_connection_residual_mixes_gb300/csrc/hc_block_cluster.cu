@@ -173,10 +173,10 @@ struct Use {
     int j;
     int cb;
 };
-__device__ __forceinline__ Use decode_use(int u, int ncb, int J, bool full) {
+// Block b (ncb consecutive uses) -> (phase 3?, local tile j); no division.
+__device__ __forceinline__ Use block_use(int b, int J, bool full) {
     Use r;
-    r.cb = u % ncb;
-    const int b = u / ncb;
+    r.cb = 0;
     if (!full) {
         r.p3 = false;
         r.j = b;
@@ -197,6 +197,11 @@ __device__ __forceinline__ Use decode_use(int u, int ncb, int J, bool full) {
     }
     r.p3 = true;
     r.j = pairs + (c - 2 * pairs);
+    return r;
+}
+__device__ __forceinline__ Use decode_use(int u, int ncb, int J, bool full) {
+    Use r = block_use(u / ncb, J, full);
+    r.cb = u % ncb;
     return r;
 }
 __device__ __forceinline__ int total_uses(int ncb, int J, bool full) {
@@ -517,84 +522,53 @@ k_block_cluster(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
         const int tc = threadIdx.x - kWarpCuda * 32;  // 0..255
         const int uu = lane & 3;
         const int r = 8 * (tc >> 5) + (lane >> 3) + 4 * ((lane >> 2) & 1);
-        f32x2 pm[kHC];  // pre_mix of the token, duplicated into both lanes
-        f32x2 ssx2 = f2_dup(0.0f), ssh2 = f2_dup(0.0f);
-        f32x2 cf2[kHC + kHC * kHC];  // post, comb of the token, duplicated into both lanes
-        f32x2 rs2 = f2_dup(0.0f);     // RMSNorm scale of the token
-        int cur_coef_tile = -1;
         const uint64_t pol_out = HC_STORE_EVICT_FIRST ? policy_evict_first() : policy_evict_normal();
         const float4 *sPm = reinterpret_cast<const float4 *>(smem + L.off_pm);
-        for (int u = 0; u < U; ++u) {
-            const int slot = u % kSlots;
-            const uint32_t ph = (uint32_t)(u / kSlots) & 1u;
-            if (!mbar_wait_warp<false>(full_bar(slot), ph, &s_abort)) break;
-            const Use us = decode_use(u, ncb, J, kFull);
-            const int tile = cid + us.j * ncl;
+        // One block = the ncb slots of one phase of one tile.  Registers are scoped
+        // per block: the coefficients live only through a phase-3 block, and
+        // phase 1 keeps one sum-of-squares accumulator per stream (short chains).
+        const int nblk = kFull ? 2 * J : J;
+        int u = 0;  // ring use index
+        bool ok = true;
+        for (int b = 0; b < nblk && ok; ++b) {
+            const Use bu = block_use(b, J, kFull);
+            const int tile = cid + bu.j * ncl;
             const int64_t tok = (int64_t)tile * kT + r;
-            const uint8_t *sb = smem_ring + slot * kSlotBytes;
-            uint4 xr[kItems][kHC], fr[kItems];
+            const bool live = tok < p.n;
+            if (!bu.p3) {
+                f32x2 pm[kHC];
+                f32x2 ssx2[kHC], ssh2[kItems];
 #pragma unroll
-            for (int it = 0; it < kItems; ++it) {
+                for (int s = 0; s < kHC; ++s) ssx2[s] = f2_dup(0.0f);
 #pragma unroll
-                for (int s = 0; s < kHC; ++s)
-                    xr[it][s] = *reinterpret_cast<const uint4 *>(sb + s * kBoxBytes + swz(r, uu + 4 * it));
-                if (us.p3) fr[it] = *reinterpret_cast<const uint4 *>(sb + kStageXBytes + swz(r, uu + 4 * it));
-            }
-            // The loads above are still in flight: nothing has used their values yet,
-            // and an mbarrier arrive alone does not wait for them (measured: the ring
-            // refilled the slot under the later loads of a warp that went on to wait
-            // for its coefficients).  A CTA-scope fence completes them first.
-            __threadfence_block();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(empty_bar(slot));
-            if (us.cb == 0) {
-                // pre_mix of this thread's token (copied in with the tile's first slot)
-                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (kFull && tok < p.n) v = sPm[(us.j % kPmBufs) * kT + r];
-                pm[0] = f2_dup(v.x); pm[1] = f2_dup(v.y); pm[2] = f2_dup(v.z); pm[3] = f2_dup(v.w);
-            }
-            if (!us.p3) {
-#pragma unroll
-                for (int it = 0; it < kItems; ++it) {
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        f32x2 xs[kHC];
-#pragma unroll
-                        for (int s = 0; s < kHC; ++s) {
-                            const uint4 &w = xr[it][s];
-                            xs[s] = f2_from_bf16x2(q == 0 ? w.x : q == 1 ? w.y : q == 2 ? w.z : w.w);
-                            ssx2 = f2_fma(xs[s], xs[s], ssx2);
-                        }
-                        if (kFull) {
-                            f32x2 h = f2_mul(pm[0], xs[0]);
-                            h = f2_fma(pm[1], xs[1], h);
-                            h = f2_fma(pm[2], xs[2], h);
-                            h = f2_fma(pm[3], xs[3], h);
-                            const f32x2 hr = f2_from_bf16x2(f2_to_bf16x2(h));
-                            ssh2 = f2_fma(hr, hr, ssh2);
-                        }
+                for (int it = 0; it < kItems; ++it) ssh2[it] = f2_dup(0.0f);
+                for (int cb = 0; cb < ncb; ++cb, ++u) {
+                    const int slot = u % kSlots;
+                    if (!mbar_wait_warp<false>(full_bar(slot), (uint32_t)(u / kSlots) & 1u, &s_abort)) {
+                        ok = false;
+                        break;
                     }
-                }
-            } else {
-                const int buf = us.j % kBufs;
-                if (cur_coef_tile != us.j) {
-                    if (!mbar_wait_warp<true>(coef_bar(buf), (uint32_t)(us.j / kBufs) & 1u, &s_abort)) break;
-                    cur_coef_tile = us.j;
-                    const float *c = sCoef + (buf * kT + r) * kCoefF;
+                    const uint8_t *sb = smem_ring + slot * kSlotBytes;
+                    uint4 xr[kItems][kHC];
 #pragma unroll
-                    for (int q = 0; q < kHC + kHC * kHC; ++q) cf2[q] = f2_dup(c[q]);
-                    rs2 = f2_dup(c[kHC + kHC * kHC]);
-                }
-                if (tok < p.n) {
+                    for (int it = 0; it < kItems; ++it)
+#pragma unroll
+                        for (int s = 0; s < kHC; ++s)
+                            xr[it][s] = *reinterpret_cast<const uint4 *>(sb + s * kBoxBytes + swz(r, uu + 4 * it));
+                    // The loads above are still in flight: nothing has used their values
+                    // yet, and an mbarrier arrive alone does not wait for them (measured:
+                    // the ring refilled the slot under the later loads of a warp that went
+                    // on to wait).  A CTA-scope fence completes them first.
+                    __threadfence_block();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(empty_bar(slot));
+                    if (kFull && cb == 0) {
+                        // pre_mix of this thread's token (copied in with this slot)
+                        const float4 v = live ? sPm[(bu.j % kPmBufs) * kT + r] : make_float4(0.f, 0.f, 0.f, 0.f);
+                        pm[0] = f2_dup(v.x); pm[1] = f2_dup(v.y); pm[2] = f2_dup(v.z); pm[3] = f2_dup(v.w);
+                    }
 #pragma unroll
                     for (int it = 0; it < kItems; ++it) {
-                        const int un = uu + 4 * it;
-                        const float4 *nw = reinterpret_cast<const float4 *>(sNormW + us.cb * kCB + un * 8);
-                        const float4 w0 = nw[0], w1 = nw[1];
-                        const f32x2 wv[4] = {f2_make(w0.x, w0.y), f2_make(w0.z, w0.w), f2_make(w1.x, w1.y),
-                                             f2_make(w1.z, w1.w)};
-                        const int64_t cbase = (int64_t)rank * dc + us.cb * kCB + un * 8;
-                        uint32_t yo[kHC][4], ho[4];
 #pragma unroll
                         for (int q = 0; q < 4; ++q) {
                             f32x2 xs[kHC];
@@ -602,46 +576,110 @@ k_block_cluster(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                             for (int s = 0; s < kHC; ++s) {
                                 const uint4 &w = xr[it][s];
                                 xs[s] = f2_from_bf16x2(q == 0 ? w.x : q == 1 ? w.y : q == 2 ? w.z : w.w);
+                                ssx2[s] = f2_fma(xs[s], xs[s], ssx2[s]);
                             }
-                            const uint4 &fw = fr[it];
-                            const f32x2 fv = f2_from_bf16x2(q == 0 ? fw.x : q == 1 ? fw.y : q == 2 ? fw.z : fw.w);
-#pragma unroll
-                            for (int k = 0; k < kHC; ++k) {
-                                f32x2 a = f2_mul(cf2[k], fv);
-#pragma unroll
-                                for (int jj = 0; jj < kHC; ++jj) a = f2_fma(cf2[kHC + jj * kHC + k], xs[jj], a);
-                                yo[k][q] = f2_to_bf16x2(a);
+                            if (kFull) {
+                                f32x2 h = f2_mul(pm[0], xs[0]);
+                                h = f2_fma(pm[1], xs[1], h);
+                                h = f2_fma(pm[2], xs[2], h);
+                                h = f2_fma(pm[3], xs[3], h);
+                                const f32x2 hr = f2_from_bf16x2(f2_to_bf16x2(h));
+                                ssh2[it] = f2_fma(hr, hr, ssh2[it]);
                             }
-                            f32x2 h = f2_mul(pm[0], xs[0]);
-                            h = f2_fma(pm[1], xs[1], h);
-                            h = f2_fma(pm[2], xs[2], h);
-                            h = f2_fma(pm[3], xs[3], h);
-                            const f32x2 hr = f2_from_bf16x2(f2_to_bf16x2(h));
-                            ho[q] = f2_to_bf16x2(f2_mul(f2_mul(hr, rs2), wv[q]));
                         }
-                        // outputs are written once and not read here again: keep them from
-                        // displacing the tiles of x that phase 3 still has to re-read from L2
-#pragma unroll
-                        for (int k = 0; k < kHC; ++k)
-                            st_global_v4_hint(p.y + (tok * kHC + k) * d + cbase, yo[k][0], yo[k][1], yo[k][2],
-                                              yo[k][3], pol_out);
-                        st_global_v4_hint(p.h_norm + tok * d + cbase, ho[0], ho[1], ho[2], ho[3], pol_out);
                     }
                 }
-            }
-            if (!us.p3 && us.cb == ncb - 1) {
-                // tile finished: this CTA's sums of squares of the token go to the MMA warps
-                float ssx = f2_hsum(ssx2), ssh = f2_hsum(ssh2);
+                if (!ok) break;
+                // tile finished: this CTA's sums of squares of the token go to the sender
+                float ssx = f2_hsum(f2_add(f2_add(ssx2[0], ssx2[1]), f2_add(ssx2[2], ssx2[3])));
+                float ssh = f2_hsum(f2_add(ssh2[0], ssh2[1]));
                 ssx += __shfl_xor_sync(0xffffffffu, ssx, 1);
                 ssx += __shfl_xor_sync(0xffffffffu, ssx, 2);
                 ssh += __shfl_xor_sync(0xffffffffu, ssh, 1);
                 ssh += __shfl_xor_sync(0xffffffffu, ssh, 2);
                 if (uu == 0) {
-                    // CTA-local hand-off to the MMA warps, which send it with the dots
-                    *reinterpret_cast<float2 *>(sSS + ((us.j & 1) * kT + r) * 2) = make_float2(ssx, ssh);
-                    mbar_arrive(ss_bar(us.j & 1));
+                    *reinterpret_cast<float2 *>(sSS + ((bu.j & 1) * kT + r) * 2) = make_float2(ssx, ssh);
+                    mbar_arrive(ss_bar(bu.j & 1));
                 }
-                ssx2 = ssh2 = f2_dup(0.0f);
+            } else {
+                f32x2 pm[kHC];
+                f32x2 cf2[kHC + kHC * kHC];  // post, comb of the token, duplicated into both lanes
+                f32x2 rs2;                   // RMSNorm scale of the token
+                for (int cb = 0; cb < ncb; ++cb, ++u) {
+                    const int slot = u % kSlots;
+                    if (!mbar_wait_warp<false>(full_bar(slot), (uint32_t)(u / kSlots) & 1u, &s_abort)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint8_t *sb = smem_ring + slot * kSlotBytes;
+                    uint4 xr[kItems][kHC], fr[kItems];
+#pragma unroll
+                    for (int it = 0; it < kItems; ++it) {
+#pragma unroll
+                        for (int s = 0; s < kHC; ++s)
+                            xr[it][s] = *reinterpret_cast<const uint4 *>(sb + s * kBoxBytes + swz(r, uu + 4 * it));
+                        fr[it] = *reinterpret_cast<const uint4 *>(sb + kStageXBytes + swz(r, uu + 4 * it));
+                    }
+                    __threadfence_block();  // (see phase 1)
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(empty_bar(slot));
+                    if (cb == 0) {
+                        const float4 v = live ? sPm[(bu.j % kPmBufs) * kT + r] : make_float4(0.f, 0.f, 0.f, 0.f);
+                        pm[0] = f2_dup(v.x); pm[1] = f2_dup(v.y); pm[2] = f2_dup(v.z); pm[3] = f2_dup(v.w);
+                        const int buf = bu.j % kBufs;
+                        if (!mbar_wait_warp<true>(coef_bar(buf), (uint32_t)(bu.j / kBufs) & 1u, &s_abort)) {
+                            ok = false;
+                            break;
+                        }
+                        const float *c = sCoef + (buf * kT + r) * kCoefF;
+#pragma unroll
+                        for (int q = 0; q < kHC + kHC * kHC; ++q) cf2[q] = f2_dup(c[q]);
+                        rs2 = f2_dup(c[kHC + kHC * kHC]);
+                    }
+                    if (live) {
+#pragma unroll
+                        for (int it = 0; it < kItems; ++it) {
+                            const int un = uu + 4 * it;
+                            const float4 *nw = reinterpret_cast<const float4 *>(sNormW + cb * kCB + un * 8);
+                            const float4 w0 = nw[0], w1 = nw[1];
+                            const f32x2 wv[4] = {f2_make(w0.x, w0.y), f2_make(w0.z, w0.w), f2_make(w1.x, w1.y),
+                                                 f2_make(w1.z, w1.w)};
+                            const int64_t cbase = (int64_t)rank * dc + cb * kCB + un * 8;
+                            uint32_t yo[kHC][4], ho[4];
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                f32x2 xs[kHC];
+#pragma unroll
+                                for (int s = 0; s < kHC; ++s) {
+                                    const uint4 &w = xr[it][s];
+                                    xs[s] = f2_from_bf16x2(q == 0 ? w.x : q == 1 ? w.y : q == 2 ? w.z : w.w);
+                                }
+                                const uint4 &fw = fr[it];
+                                const f32x2 fv = f2_from_bf16x2(q == 0 ? fw.x : q == 1 ? fw.y : q == 2 ? fw.z : fw.w);
+#pragma unroll
+                                for (int k = 0; k < kHC; ++k) {
+                                    f32x2 a = f2_mul(cf2[k], fv);
+#pragma unroll
+                                    for (int jj = 0; jj < kHC; ++jj) a = f2_fma(cf2[kHC + jj * kHC + k], xs[jj], a);
+                                    yo[k][q] = f2_to_bf16x2(a);
+                                }
+                                f32x2 h = f2_mul(pm[0], xs[0]);
+                                h = f2_fma(pm[1], xs[1], h);
+                                h = f2_fma(pm[2], xs[2], h);
+                                h = f2_fma(pm[3], xs[3], h);
+                                const f32x2 hr = f2_from_bf16x2(f2_to_bf16x2(h));
+                                ho[q] = f2_to_bf16x2(f2_mul(f2_mul(hr, rs2), wv[q]));
+                            }
+                            // outputs are written once and not read here again: keep them from
+                            // displacing the tiles of x that phase 3 still has to re-read from L2
+#pragma unroll
+                            for (int k = 0; k < kHC; ++k)
+                                st_global_v4_hint(p.y + (tok * kHC + k) * d + cbase, yo[k][0], yo[k][1], yo[k][2],
+                                                  yo[k][3], pol_out);
+                            st_global_v4_hint(p.h_norm + tok * d + cbase, ho[0], ho[1], ho[2], ho[3], pol_out);
+                        }
+                    }
+                }
             }
         }
     }
