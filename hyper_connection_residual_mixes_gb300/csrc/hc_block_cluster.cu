@@ -603,7 +603,7 @@ k_block_cluster(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 }
             } else {
                 f32x2 pm[kHC];
-                f32x2 cf2[kHC + kHC * kHC];  // post, comb of the token, duplicated into both lanes
+                float cf[kHC + kHC * kHC];  // post, comb of the token
                 f32x2 rs2;                   // RMSNorm scale of the token
                 for (int cb = 0; cb < ncb; ++cb, ++u) {
                     const int slot = u % kSlots;
@@ -633,7 +633,7 @@ k_block_cluster(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                         }
                         const float *c = sCoef + (buf * kT + r) * kCoefF;
 #pragma unroll
-                        for (int q = 0; q < kHC + kHC * kHC; ++q) cf2[q] = f2_dup(c[q]);
+                        for (int q = 0; q < kHC + kHC * kHC; ++q) cf[q] = c[q];
                         rs2 = f2_dup(c[kHC + kHC * kHC]);
                     }
                     if (live) {
@@ -658,9 +658,9 @@ k_block_cluster(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                                 const f32x2 fv = f2_from_bf16x2(q == 0 ? fw.x : q == 1 ? fw.y : q == 2 ? fw.z : fw.w);
 #pragma unroll
                                 for (int k = 0; k < kHC; ++k) {
-                                    f32x2 a = f2_mul(cf2[k], fv);
+                                    f32x2 a = f2_mul(f2_dup(cf[k]), fv);
 #pragma unroll
-                                    for (int jj = 0; jj < kHC; ++jj) a = f2_fma(cf2[kHC + jj * kHC + k], xs[jj], a);
+                                    for (int jj = 0; jj < kHC; ++jj) a = f2_fma(f2_dup(cf[kHC + jj * kHC + k]), xs[jj], a);
                                     yo[k][q] = f2_to_bf16x2(a);
                                 }
                                 f32x2 h = f2_mul(pm[0], xs[0]);
