@@ -299,52 +299,87 @@ def run_e2e(args, dev, case, seed, world):
     pm_h = case.pre_mix.cpu().pin_memory()
     y_h = torch.empty((n, HC, d), dtype=torch.bfloat16, pin_memory=True)
     pre_h = torch.empty((n, HC), dtype=torch.float32, pin_memory=True)
-    x_d = torch.empty((n, HC, d), dtype=torch.bfloat16, device=dev)
-    pm_d = torch.empty((n, HC), device=dev)
+    # Device buffers: x and pre_mix double-buffered across steps, f across sides.
+    x_d = [torch.empty((n, HC, d), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    pm_d = [torch.empty((n, HC), device=dev) for _ in range(2)]
     f_d = [torch.empty((n, d), dtype=torch.bfloat16, device=dev) for _ in range(2)]
-    ys = [torch.empty_like(x_d), torch.empty_like(x_d)]
+    ys = [torch.empty((n, HC, d), dtype=torch.bfloat16, device=dev) for _ in range(2)]
     pres = [torch.empty((n, HC), device=dev), torch.empty((n, HC), device=dev)]
+    y_last = torch.empty((n, HC, d), dtype=torch.bfloat16, device=dev)
+    pre_last = torch.empty((n, HC), device=dev)
     h_norm = torch.empty((n, d), dtype=torch.bfloat16, device=dev)
     params = [p.astuple() for p in case.params]
     comp = torch.cuda.current_stream(dev)
-    copy = torch.cuda.Stream(dev)
-    f_ready = [torch.cuda.Event() for _ in range(2)]
-    f_free = [torch.cuda.Event() for _ in range(2)]
+    # Each host-to-device copy is split over several streams, so that several copy
+    # engines share it; every chunk is one cudaMemcpyAsync.
+    n_copy = 4
+    copies = [torch.cuda.Stream(dev) for _ in range(n_copy)]
+    d2h = torch.cuda.Stream(dev)
+    rows = [(c * n // n_copy, (c + 1) * n // n_copy) for c in range(n_copy)]
+    f_free = [torch.cuda.Event() for _ in range(2)]   # kernel done with f_d[b]
+    x_free = [torch.cuda.Event() for _ in range(2)]   # kernel done with x_d[b]
+    y_free = torch.cuda.Event()                       # y_last read back
+    ready = {}
 
-    def step():
-        with torch.cuda.stream(copy):
-            copy.wait_event(f_free[0])
-            x_d.copy_(x_h, non_blocking=True)
-            pm_d.copy_(pm_h, non_blocking=True)
-            f_d[0].copy_(f_h[0], non_blocking=True)
-            f_ready[0].record(copy)
-        x, pm = x_d, pm_d
-        for s in range(SIDES):
+    def issue_inputs(g):
+        """Copies for global side g (step g // SIDES, side g % SIDES)."""
+        i, s = divmod(g, SIDES)
+        fb, xb = g % 2, i % 2
+        evs = []
+        for c, st in enumerate(copies):
+            a, b = rows[c]
+            with torch.cuda.stream(st):
+                st.wait_event(f_free[fb])
+                f_d[fb][a:b].copy_(f_h[s % n_host_f][a:b], non_blocking=True)
+                if s == 0:
+                    st.wait_event(x_free[xb])
+                    x_d[xb][a:b].copy_(x_h[a:b], non_blocking=True)
+                    pm_d[xb][a:b].copy_(pm_h[a:b], non_blocking=True)
+                e = torch.cuda.Event()
+                e.record(st)
+                evs.append(e)
+        ready[g] = evs
+
+    def run(steps):
+        total = steps * SIDES
+        issue_inputs(0)
+        x = pm = None
+        for g in range(total):
+            i, s = divmod(g, SIDES)
+            if g + 1 < total:
+                issue_inputs(g + 1)  # prefetch: the next side's f (and the next step's x)
+            for e in ready.pop(g):
+                comp.wait_event(e)
+            if s == 0:
+                x, pm = x_d[i % 2], pm_d[i % 2]
             b = s % 2
-            if s + 1 < SIDES:
-                nb = (s + 1) % 2
-                with torch.cuda.stream(copy):
-                    copy.wait_event(f_free[nb])
-                    f_d[nb].copy_(f_h[(s + 1) % n_host_f], non_blocking=True)
-                    f_ready[nb].record(copy)
-            comp.wait_event(f_ready[b])
-            hcg.hc_block_step(x, pm, f_d[b], *params[s], h_norm=h_norm, y=ys[b], pre_out=pres[b],
+            last = s == SIDES - 1
+            out, pre_o = (y_last, pre_last) if last else (ys[b], pres[b])
+            if last:
+                comp.wait_event(y_free)  # the previous step's result has been read back
+            hcg.hc_block_step(x, pm, f_d[g % 2], *params[s], h_norm=h_norm, y=out, pre_out=pre_o,
                               stream=comp)
-            f_free[b].record(comp)
-            x, pm = ys[b], pres[b]
-        y_h.copy_(x, non_blocking=True)
-        pre_h.copy_(pm, non_blocking=True)
+            f_free[g % 2].record(comp)
+            if s == 0:
+                x_free[i % 2].record(comp)
+            x, pm = out, pre_o
+            if last:
+                # the step's result back to the host
+                d2h.wait_stream(comp)
+                with torch.cuda.stream(d2h):
+                    y_h.copy_(y_last, non_blocking=True)
+                    pre_h.copy_(pre_last, non_blocking=True)
+                    y_free.record(d2h)
 
-    for e in f_free:
+    for e in f_free + x_free + [y_free]:
         e.record(comp)
-    step()
+    run(1)
     torch.cuda.synchronize(dev)
     if world > 1:
         torch.distributed.barrier()
     steps = max(1, min(args.steps, 5))
     t0 = time.perf_counter()
-    for _ in range(steps):
-        step()
+    run(steps)
     torch.cuda.synchronize(dev)
     dt = time.perf_counter() - t0
     if world > 1:
@@ -357,7 +392,8 @@ def run_e2e(args, dev, case, seed, world):
             "d2h_bytes_per_step": d2h, "steps": steps,
             "host_f_buffers": n_host_f,
             "note": "pinned host buffers; H2D of x and all 80 f per step, D2H of final y and pre; "
-                    "f copies double-buffered against the kernels"
+                    "copies split over 4 streams and double-buffered against the kernels (the next "
+                    "side's f and the next step's x load while a side computes)"
                     + ("" if n_host_f == SIDES else "; host f pool of %d reused cyclically" % n_host_f)}
 
 

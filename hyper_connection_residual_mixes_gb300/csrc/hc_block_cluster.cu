@@ -17,13 +17,14 @@
 //    memory for the whole launch: one 32-lane TMEM quadrant per MMA warp, one
 //    stream per MMA warp.  Weights are never re-read per token and take no
 //    shared memory.
-//  * A cluster walks 64-token tiles.  Each tile's streams pass through an
-//    8-slot TMA ring (32 columns x 64 tokens x 4 streams per slot, 64-byte
-//    swizzle) twice: phase 1 (the projection, sum of squares, and the sum of
-//    squares of the bf16-rounded h) and phase 3 (y and h_norm).  The second
-//    read comes from L2 (the first read is tagged evict_last, the second
-//    evict_first); phase 1 of the next tile runs between them so the
-//    cross-CTA reduction of a tile is hidden behind useful streaming.
+//  * A cluster walks 64-token tiles.  Each tile's streams pass through a
+//    4-slot TMA ring (64 columns x 64 tokens x 4 streams per slot, 128-byte
+//    swizzle, plus the f box in phase 3) twice: phase 1 (the projection, sum
+//    of squares, and the sum of squares of the bf16-rounded h) and phase 3
+//    (y and h_norm).  The second read comes from L2 (the first read is tagged
+//    evict_last, the second evict_first); phase 1 of the next tile runs
+//    between them so the cross-CTA reduction of a tile is hidden behind
+//    useful streaming.
 //  * The projection runs on the tensor cores (mma.sync m16n8k16, bf16 in,
 //    fp32 accumulate); x is bf16 and enters exactly; the three weight parts
 //    accumulate into the same fp32 sums.
@@ -36,8 +37,8 @@
 // Warp roles (480 threads): warps 0-3 tensor-core MMA (warp w: stream w, TMEM
 // quadrant w); warp 4 TMA producer; warp 5 owner-side reduction + Sinkhorn +
 // broadcast; warps 6-13 CUDA-core streaming math (two 8-column units of one
-// token per thread per slot, packed f32x2 arithmetic); warp 14 sends each
-// tile's partial sums to the owners.
+// token per thread per slot, packed f32x2 arithmetic, one block of slots per
+// tile phase); warp 14 sends each tile's partial sums to the owners.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -69,14 +70,14 @@ static_assert(kCB == 32 || kCB == 64, "column block must be 32 or 64");
 #ifndef HC_STORE_EVICT_FIRST
 #define HC_STORE_EVICT_FIRST 1
 #endif
-constexpr int kSlots = HC_SLOTS;  // TMA ring depth (20 KB per slot)
+constexpr int kSlots = HC_SLOTS;  // TMA ring depth (40 KB per slot)
 constexpr int kLag = HC_LAG;      // phase 3 of tile j runs after phase 1 of tile j + kLag
 constexpr int kBufs = kLag + 1; // partial / coefficient buffers in rotation
 constexpr uint32_t kTmemCols = 512;  // the whole tensor memory of the SM (1 CTA per SM)
 constexpr int kThreads = 480;
-constexpr int kBoxBytes = kT * kCB * 2;             // 64 tokens x kCB bf16
-constexpr int kStageXBytes = kHC * kBoxBytes;       // 16384
-constexpr int kSlotBytes = kStageXBytes + kBoxBytes;  // + f box = 20480
+constexpr int kBoxBytes = kT * kCB * 2;             // 64 tokens x kCB bf16 = 8 KB
+constexpr int kStageXBytes = kHC * kBoxBytes;       // 4 streams = 32 KB
+constexpr int kSlotBytes = kStageXBytes + kBoxBytes;  // + f box = 40 KB
 constexpr int kTokPerOwner = kT / kC;               // 4
 constexpr int kPartF = 28;      // 24 partial dots, sum x^2, sum h^2, 2 pad
 constexpr int kCoefF = 24;      // post[4], comb[16], rs_h, 3 pad
@@ -113,7 +114,7 @@ struct Params {
 // Shared-memory layout (byte offsets from a 1024-aligned base).
 struct Layout {
     int dc;        // columns per CTA per stream = d / 16
-    int ncb;       // slots per tile = dc / 32
+    int ncb;       // slots per tile phase = dc / kCB
     int wcols;     // tensor-memory columns per MMA warp: 18 per k16 step, 2*ncb steps
     int off_coef, off_part, off_mma, off_ss, off_pm, off_normw, off_bar, off_tmem, total;
 };
@@ -710,7 +711,7 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
     return fn;
 }
 
-// rows x cols bf16 matrix (row stride `cols` elements), box of 64 rows x 32 columns, 64B swizzle
+// rows x cols bf16 matrix (row stride `cols` elements), box of kT rows x kCB columns (128-byte swizzle for kCB = 64)
 bool make_tmap(CUtensorMap *m, const void *base, int64_t rows, int64_t cols) {
     auto enc = get_encode();
     if (!enc) return false;
