@@ -433,8 +433,10 @@ k_block_cluster(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             float pr[kHC], po[kHC], c[kHC * kHC];
             split_sinkhorn_token<true>(mm, s0, s1, s2, p.hc_base, p.iters, p.eps, pr, po, c);
             const float rs_h = rsqrtf(ssh / (float)d + p.norm_eps);
-            if (kFull) {
-                // broadcast first: lane l -> destination CTA l % 16, tokens 2*(l/16) + {0, 1}
+            {
+                // broadcast first: lane l -> destination CTA l % 16, tokens 2*(l/16) + {0, 1}.
+                // Without phase 3 (hc_mixes) the data goes unused, but the arrivals still
+                // pace the CUDA-core warps, which keeps every hand-off buffer in order.
                 const int dest = lane & 15;
                 const int ta = 2 * (lane >> 4);
 #pragma unroll
@@ -536,6 +538,14 @@ k_block_cluster(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             const int tile = cid + bu.j * ncl;
             const int64_t tok = (int64_t)tile * kT + r;
             const bool live = tok < p.n;
+            if (!kFull && b > kLag) {
+                // Phase 1 alone: wait, as phase 3 would, for the coefficients of tile
+                // b - kLag - 1 before starting tile b, so that no hand-off buffer (the
+                // sums of squares here, the partials at the owners) is refilled before
+                // it has been read.
+                const int jw = b - kLag - 1;
+                if (!mbar_wait_warp<true>(coef_bar(jw % kBufs), (uint32_t)(jw / kBufs) & 1u, &s_abort)) break;
+            }
             if (!bu.p3) {
                 f32x2 pm[kHC];
                 f32x2 ssx2[kHC], ssh2[kItems];

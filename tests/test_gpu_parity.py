@@ -119,7 +119,7 @@ def test_split_sinkhorn_empty():
 
 
 # ----------------------------------------------------------------- a1-a3
-@pytest.mark.parametrize("n,d", [(1, 5120), (16, 5120), (37, 5120), (130, 5120), (9, 64),
+@pytest.mark.parametrize("n,d", [(1, 5120), (16, 5120), (37, 5120), (130, 5120), (1000, 5120), (9, 64),
                                  (21, 1024), (3, 16384)])
 def test_mixes(n, d):
     case = inputs.tiny(seed=11 + n, n=n, d=d)
@@ -194,6 +194,36 @@ def test_block_step_shapes(n, d):
     out = _gpu_side(case.x.to(DEV), case.pre_mix.to(DEV), case.fs[0].to(DEV), p.to(DEV))
     torch.cuda.synchronize()
     _check_side(out, _oracle_side(case.x, case.pre_mix, case.fs[0], p))
+
+
+@pytest.mark.parametrize("n,d", [(1361, 1024), (917, 3072), (530, 7168)])
+def test_block_step_cluster_widths_many_tiles(n, d):
+    """The cluster kernel at other widths: 1, 3 and 7 column blocks per tile
+    phase (at d = 7168 the weight fragments fill 504 of the 512 tensor-memory
+    columns), with enough tokens that every cluster walks several tiles and
+    the last tile is ragged.  All elements checked."""
+    case = inputs.tiny(seed=300 + d, n=n, d=d)
+    p = case.params[0]
+    out = _gpu_side(case.x.to(DEV), case.pre_mix.to(DEV), case.fs[0].to(DEV), p.to(DEV))
+    torch.cuda.synchronize()
+    _check_side(out, _oracle_side(case.x, case.pre_mix, case.fs[0], p))
+
+
+def test_mixes_cluster_many_tiles():
+    """hc_mixes through the cluster kernel (phase 1 only) over many tiles."""
+    n, d = 1361, 1024
+    case = inputs.tiny(seed=77, n=n, d=d)
+    p = case.params[0]
+    pre, post, comb, mixes = hcg.hc_mixes(case.x.to(DEV), p.hc_fn.to(DEV), p.hc_scale.to(DEV),
+                                          p.hc_base.to(DEV), return_mixes=True)
+    torch.cuda.synchronize()
+    rm = oracle.mixes(bits(case.x), _np(p.hc_fn))
+    err = np.abs(_np(mixes).astype(np.float64) - rm)
+    assert np.all(err <= 1e-5 + 1e-5 * np.abs(rm)), err.max()
+    rp, rq, rc = oracle.split_sinkhorn(rm, _np(p.hc_scale), _np(p.hc_base))
+    check_fp32("pre", pre, rp)
+    check_fp32("post", post, rq)
+    check_fp32("comb", comb, rc)
 
 
 def test_block_step_decode_config_two_sides():
