@@ -53,6 +53,20 @@ def dist_env():
             int(os.environ.get("WORLD_SIZE", 1)))
 
 
+def rank_seed(base_seed, rank):
+    """Each replica draws its own batch; rank 0 runs exactly the workload's seed."""
+    return base_seed + 1000 * rank
+
+
+def max_over_ranks(value, device="cpu"):
+    """The slowest rank's time (the job ends when the last replica does)."""
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
 def measured_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
@@ -154,7 +168,7 @@ WORKLOADS = {
 
 def build_workload(device, rank, name="long_prefill"):
     gen, base_seed, _ = WORKLOADS[name]
-    seed = base_seed + 1000 * rank  # rank 0 runs exactly the workload's seed
+    seed = rank_seed(base_seed, rank)
     if name == "long_prefill":
         case = inputs.long_prefill(device=device, seed=seed, materialize_f=False)
         fs = [inputs.long_prefill_f(s, case.n, case.d, device, seed) for s in range(SIDES)]
@@ -217,9 +231,7 @@ def run_ours(args, rank, local_rank, world):
     launch_ms = [a.elapsed_time(b) for e in ev for (a, b) in e]
     gpu_launches = launches["n"]
     if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+        elapsed_ms = max_over_ranks(elapsed_ms, dev)
 
     e2e = None if (args.no_e2e or args.workload != "long_prefill") else \
         run_e2e(args, dev, case, seed, world)
@@ -383,9 +395,7 @@ def run_e2e(args, dev, case, seed, world):
     torch.cuda.synchronize(dev)
     dt = time.perf_counter() - t0
     if world > 1:
-        t = torch.tensor([dt], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        dt = float(t.item())
+        dt = max_over_ranks(dt, dev)
     h2d = n * HC * d * 2 + n * HC * 4 + SIDES * f_bytes
     d2h = n * HC * d * 2 + n * HC * 4
     return {"value": world * n * steps / dt, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
@@ -499,8 +509,9 @@ def main():
         out = run_ours(args, rank, local_rank, world)
     if out is not None and rank == 0:
         print(json.dumps(out), flush=True)
-    if world > 1 and args.impl == "ours":
-        torch.distributed.barrier()
+    if world > 1:
+        if args.impl == "ours":
+            torch.distributed.barrier()
         torch.distributed.destroy_process_group()
 
 

@@ -151,7 +151,7 @@ def test_mixes_zero_streams_closed_form():
 
 
 # ----------------------------------------------------------------- a4-a5, a6
-@pytest.mark.parametrize("n,d", [(1, 5120), (16, 5120), (33, 64), (5, 16384)])
+@pytest.mark.parametrize("n,d", [(1, 5120), (16, 5120), (3000, 5120), (33, 64), (5, 16384)])
 def test_pre_norm(n, d):
     g = torch.Generator().manual_seed(50 + n)
     x = inputs.streams(g, n, 4, d, outlier_p=0.01)
@@ -163,7 +163,7 @@ def test_pre_norm(n, d):
     check_bf16("h_norm", out, ref, abs_allow=h_norm_allowance(x, _np(pm), _np(w), ref))
 
 
-@pytest.mark.parametrize("n,d", [(1, 5120), (16, 5120), (33, 64), (5, 16384)])
+@pytest.mark.parametrize("n,d", [(1, 5120), (16, 5120), (3000, 5120), (33, 64), (5, 16384)])
 def test_post(n, d):
     g = torch.Generator().manual_seed(80 + n)
     x = inputs.streams(g, n, 4, d)
@@ -187,7 +187,7 @@ def test_block_step_tiny_config():
 
 
 @pytest.mark.parametrize("n,d", [(1, 5120), (3, 5120), (37, 5120), (200, 5120), (70, 64),
-                                 (19, 2048), (4, 16384)])
+                                 (19, 2048), (4, 16384), (301, 8192)])
 def test_block_step_shapes(n, d):
     case = inputs.tiny(seed=200 + n, n=n, d=d)
     p = case.params[0]
