@@ -89,7 +89,11 @@ constexpr int kWarpCuda = 6;    // warps 6..13
 constexpr int kCudaWarps = 8;
 constexpr int kWarpSender = 14; // adds up each tile's partial sums and sends them to the owners
 constexpr int kWCols = 18;      // TMEM columns per k16 step: 3 n-tiles x (hi, mid, lo) x (b0, b1)
-constexpr int kPmBufs = 3;      // pre_mix tile buffers: tile j's stays until its phase 3 is under way
+// pre_mix tile buffers: tile j's rows must survive until phase 3 of tile j has
+// read them.  With one column block per tile phase (d = 1024) the ring can load
+// phase 1 of tile j + 3 as soon as phase 1 of tile j + 1 is released, which may
+// precede phase 3 of tile j; a fourth buffer keeps tile j + 4 further out.
+constexpr int kPmBufs = 4;
 
 struct Params {
     const float *pre_mix;
@@ -326,7 +330,6 @@ k_block_cluster(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 for (int hp = 0; hp < kStepsPerSlot / 2; ++hp) {  // pairs of k16 steps
                     uint32_t bw[36];
                     tmem_ld36(tw + kWCols * (us.cb * kStepsPerSlot + 2 * hp), bw);
-                    tmem_wait_ld36(bw);
 #pragma unroll
                     for (int h2 = 0; h2 < 2; ++h2) {
                         const int h = 2 * hp + h2;
@@ -346,6 +349,11 @@ k_block_cluster(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                     }
                 }
             }
+            // The slot's last ldmatrix loads may still be in flight here: nothing
+            // forces the mma.sync that consumes them ahead of the arrive, and an
+            // mbarrier arrive does not wait for loads.  A CTA-scope fence completes
+            // them before the producer may refill the slot.
+            __threadfence_block();
             __syncwarp();
             if (lane == 0) mbar_arrive(empty_bar(slot));
             if (!us.p3 && us.cb == ncb - 1) {

@@ -156,6 +156,35 @@ __device__ __forceinline__ void st_global_v4_hint(void *ptr, uint32_t a, uint32_
                  : "memory");
 }
 
+// 2D tiled tensor store from this CTA's shared memory (box at `src`, laid out
+// as the tensor map's swizzle says), tracked by the bulk async-group of the
+// issuing thread.  c0 is the innermost coordinate; it must be a multiple of 16
+// bytes.  Rows or columns beyond the tensor's extent are not written.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *tmap, uint32_t src, int c0, int c1,
+                                             uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group.L2::cache_hint [%0, {%2, %3}], [%1], %4;" ::"l"(
+            reinterpret_cast<uint64_t>(tmap)),
+        "r"(src), "r"(c0), "r"(c1), "l"(policy)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// wait until at most N committed bulk groups of this thread still read shared memory
+template <int N>
+__device__ __forceinline__ void bulk_wait_group_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// wait until at most N committed bulk groups of this thread are still in flight
+template <int N>
+__device__ __forceinline__ void bulk_wait_group() {
+    asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+// make this thread's earlier generic-proxy writes to shared memory visible to
+// later async-proxy reads (a TMA store issued after a barrier hand-off)
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // 2D tiled tensor load into this CTA's shared memory, completing on `bar`.
 // c0 is the innermost coordinate (elements); it must be a multiple of 16 bytes.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, uint32_t bar, int c0,
@@ -234,56 +263,28 @@ __device__ __forceinline__ void tmem_st2(uint32_t taddr, uint32_t a, uint32_t b)
     asm volatile("tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1, %2};" ::"r"(taddr), "r"(a), "r"(b)
                  : "memory");
 }
-// 36 consecutive columns of this lane (x32 + x4); use only after tmem_wait_ld36.
+// 36 consecutive columns of this lane (x32 + x4), waited for in the same asm
+// statement.  tcgen05.ld fills its destination registers asynchronously; with the
+// load and tcgen05.wait::ld in two statements the compiler may copy a
+// destination register between them (it sees the load's outputs as final),
+// and such a copy reads a value the load has not yet written.
 __device__ __forceinline__ void tmem_ld36(uint32_t taddr, uint32_t (&v)[36]) {
     asm volatile(
+        "{\n\t.reg .b32 hi;\n\t"
+        "add.u32 hi, %36, 32;\n\t"
         "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
         "%12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, "
-        "%30, %31}, [%32];"
+        "%30, %31}, [%36];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x4.b32 {%32, %33, %34, %35}, [hi];\n\t"
+        "tcgen05.wait::ld.sync.aligned;\n\t}"
         : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
           "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
           "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]),
           "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]),
-          "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+          "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31]),
+          "=r"(v[32]), "=r"(v[33]), "=r"(v[34]), "=r"(v[35])
         : "r"(taddr)
         : "memory");
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v[32]), "=r"(v[33]), "=r"(v[34]), "=r"(v[35])
-                 : "r"(taddr + 32u)
-                 : "memory");
-}
-__device__ __forceinline__ void tmem_wait_ld36(uint32_t (&v)[36]) {
-    asm volatile("tcgen05.wait::ld.sync.aligned;"
-                 : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]),
-                   "+r"(v[6]), "+r"(v[7]), "+r"(v[8]), "+r"(v[9]), "+r"(v[10]), "+r"(v[11]),
-                   "+r"(v[12]), "+r"(v[13]), "+r"(v[14]), "+r"(v[15]), "+r"(v[16]), "+r"(v[17]),
-                   "+r"(v[18]), "+r"(v[19]), "+r"(v[20]), "+r"(v[21]), "+r"(v[22]), "+r"(v[23]),
-                   "+r"(v[24]), "+r"(v[25]), "+r"(v[26]), "+r"(v[27]), "+r"(v[28]), "+r"(v[29]),
-                   "+r"(v[30]), "+r"(v[31]), "+r"(v[32]), "+r"(v[33]), "+r"(v[34]), "+r"(v[35])
-                 :
-                 : "memory");
-}
-// 12 consecutive columns of this lane (x8 + x4); the values may only be used
-// after tmem_wait_ld12 on the same registers.
-__device__ __forceinline__ void tmem_ld12(uint32_t taddr, uint32_t (&v)[12]) {
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
-                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]),
-                   "=r"(v[6]), "=r"(v[7])
-                 : "r"(taddr)
-                 : "memory");
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11])
-                 : "r"(taddr + 8u)
-                 : "memory");
-}
-// Wait for this warp's outstanding tcgen05.ld; the registers are tied to the
-// wait so no use can be scheduled before it.
-__device__ __forceinline__ void tmem_wait_ld12(uint32_t (&v)[12]) {
-    asm volatile("tcgen05.wait::ld.sync.aligned;"
-                 : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]),
-                   "+r"(v[6]), "+r"(v[7]), "+r"(v[8]), "+r"(v[9]), "+r"(v[10]), "+r"(v[11])
-                 :
-                 : "memory");
 }
 
 }  // namespace hc
