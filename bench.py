@@ -86,10 +86,11 @@ def source_digest():
     return h.hexdigest()[:16]
 
 
-def ncu_traffic_per_launch(n_tokens):
+def ncu_traffic_per_launch(n_tokens, path_kind="step"):
     """DRAM bytes per launch from the committed ncu summary, scaled by tokens;
     None when it was taken on other kernel sources."""
-    path = os.path.join(ROOT, "profiles", "hc_block_step_traffic.json")
+    path = os.path.join(ROOT, "profiles", "hc_chain_side_traffic.json" if path_kind == "chain"
+                        else "hc_block_step_traffic.json")
     try:
         with open(path) as fh:
             rec = json.load(fh)
@@ -178,6 +179,34 @@ def build_workload(device, rank, name="long_prefill"):
     return case, fs, seed
 
 
+def run_chain(case, x0, pm0, fs, ys, pres, h_norm, states, events=None, stream=None,
+              y_last=None, pre_last=None):
+    """The 80 sides through the fused chain.  Side s reads state s and writes
+    state s + 1 (two buffers in rotation); y of side s lands in ys[s % 2]
+    (or y_last for the last side), its pre in pres."""
+    P = case.params
+    sides = len(P)
+    hcg.hc_chain_begin(x0, pm0, P[0].hc_fn, P[0].hc_scale, P[0].hc_base, state_out=states[0],
+                       pre_out=pres[0], stream=stream)
+    x = x0
+    for s in range(sides):
+        if events is not None:
+            events[s][0].record(stream)
+        last = s + 1 == sides
+        y = y_last if (last and y_last is not None) else ys[s % 2]
+        if not last:
+            q = P[s + 1]
+            hcg.hc_chain_side(x, fs[s], states[s % 2], P[s].norm_w, q.hc_fn, q.hc_scale, q.hc_base,
+                              h_norm=h_norm, y=y, state_out=states[(s + 1) % 2],
+                              pre_out=(pre_last if (s + 2 == sides and pre_last is not None)
+                                       else pres[(s + 1) % 2]), stream=stream)
+        else:
+            hcg.hc_chain_side(x, fs[s], states[s % 2], P[s].norm_w, h_norm=h_norm, y=y, stream=stream)
+        if events is not None:
+            events[s][1].record(stream)
+        x = y
+
+
 def run_ours(args, rank, local_rank, world):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
@@ -192,8 +221,15 @@ def run_ours(args, rank, local_rank, world):
     params = [p.astuple() for p in case.params]
     stream = torch.cuda.current_stream(dev)
     launches = {"n": 0}
+    chain = args.path == "chain"
+    states = [torch.empty((n, hcg.STATE_FLOATS), device=dev) for _ in range(2)] if chain else None
 
     def step(events=None):
+        if chain:
+            # the sides fused across sides: each launch finishes side s and starts s + 1
+            run_chain(case, x0, pm0, fs, ys, pres, h_norm, states, events, stream)
+            launches["n"] += sides + 1
+            return
         x, pm = x0, pm0
         for s in range(sides):
             if events is not None:
@@ -228,7 +264,9 @@ def run_ours(args, rank, local_rank, world):
     if world > 1:
         torch.distributed.barrier()
     elapsed_ms = t0.elapsed_time(t1)
-    launch_ms = [a.elapsed_time(b) for e in ev for (a, b) in e]
+    # the dominant kernel's launches: every side step, or for the chain the sides
+    # that also start the next side (all but the last)
+    launch_ms = [a.elapsed_time(b) for e in ev for (a, b) in (e[:-1] if chain else e)]
     gpu_launches = launches["n"]
     if world > 1:
         elapsed_ms = max_over_ranks(elapsed_ms, dev)
@@ -263,6 +301,9 @@ def run_ours(args, rank, local_rank, world):
             "config": {"workload": args.workload, "description": WORKLOADS[args.workload][2],
                        "tokens": n, "hc": HC, "d": d, "side_steps": sides,
                        "sinkhorn_iters": 20, "seed": seed, "parallelism": "replicas" if world > 1 else "single",
+                       "path": ("chain: hc_chain_begin + 80 hc_chain_side, each side's launch also "
+                                "computing the next side's coefficients; outputs equal hc_block_step's "
+                                "bit for bit") if chain else "step: 80 hc_block_step launches",
                        "l2": ("inputs larger than L2 (x is %.2f GB per side, L2 %.0f MB); no flush"
                               % (n * HC * d * 2 / 1e9, L2_BYTES / 1e6))
                              if n * HC * d * 2 > L2_BYTES else
@@ -270,11 +311,13 @@ def run_ours(args, rank, local_rank, world):
                              % (n * HC * d * 2 / 1e6)},
             "hbm_gbs_step": step_bytes / (ms_per_step / 1e3) / 1e9,
             "hbm_frac_step": step_bytes / (ms_per_step / 1e3) / 1e9 / peak,
-            "roofline": {"kernel": KERNEL_NAME, "bound": "hbm", "achieved": achieved,
+            "roofline": {"kernel": ("hc_chain_side (k_chain, side i's y and h_norm fused with side "
+                                    "i + 1's mixes)") if chain else KERNEL_NAME,
+                         "bound": "hbm", "achieved": achieved,
                          "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                          "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs)"
                          if peak_kind == "measured" else peak_kind,
-                         "traffic": ncu_traffic_per_launch(n),
+                         "traffic": ncu_traffic_per_launch(n, "chain" if chain else "step"),
                          "algorithmic_bytes_per_launch": alg_bytes,
                          "avg_launch_us": avg_launch_s * 1e6, "launches_timed": len(launch_ms)},
             "clocks": clk,
@@ -321,6 +364,8 @@ def run_e2e(args, dev, case, seed, world):
     pre_last = torch.empty((n, HC), device=dev)
     h_norm = torch.empty((n, d), dtype=torch.bfloat16, device=dev)
     params = [p.astuple() for p in case.params]
+    chain = args.path == "chain"
+    states = [torch.empty((n, hcg.STATE_FLOATS), device=dev) for _ in range(2)] if chain else None
     comp = torch.cuda.current_stream(dev)
     # Each host-to-device copy is split over several streams, so that several copy
     # engines share it; every chunk is one cudaMemcpyAsync.
@@ -367,10 +412,28 @@ def run_e2e(args, dev, case, seed, world):
             b = s % 2
             last = s == SIDES - 1
             out, pre_o = (y_last, pre_last) if last else (ys[b], pres[b])
-            if last:
-                comp.wait_event(y_free)  # the previous step's result has been read back
-            hcg.hc_block_step(x, pm, f_d[g % 2], *params[s], h_norm=h_norm, y=out, pre_out=pre_o,
-                              stream=comp)
+            if chain:
+                P = case.params
+                if s == 0:
+                    hcg.hc_chain_begin(x, pm, P[0].hc_fn, P[0].hc_scale, P[0].hc_base,
+                                       state_out=states[0], pre_out=pres[0], stream=comp)
+                if s == SIDES - 2:
+                    comp.wait_event(y_free)  # the previous step's result has been read back
+                if not last:
+                    q = P[s + 1]
+                    # launch s writes side s + 1's pre (the last side's into pre_last)
+                    nxt_pre = pre_last if s == SIDES - 2 else pres[(s + 1) % 2]
+                    hcg.hc_chain_side(x, f_d[g % 2], states[s % 2], P[s].norm_w, q.hc_fn, q.hc_scale,
+                                      q.hc_base, h_norm=h_norm, y=out, state_out=states[(s + 1) % 2],
+                                      pre_out=nxt_pre, stream=comp)
+                else:
+                    hcg.hc_chain_side(x, f_d[g % 2], states[s % 2], P[s].norm_w, h_norm=h_norm, y=out,
+                                      stream=comp)
+            else:
+                if last:
+                    comp.wait_event(y_free)  # the previous step's result has been read back
+                hcg.hc_block_step(x, pm, f_d[g % 2], *params[s], h_norm=h_norm, y=out, pre_out=pre_o,
+                                  stream=comp)
             f_free[g % 2].record(comp)
             if s == 0:
                 x_free[i % 2].record(comp)
@@ -496,6 +559,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling runs)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--reference-tokens", type=int, default=4)
+    ap.add_argument("--path", choices=["chain", "step"], default="chain",
+                    help="chain: the sides fused across sides (hc_chain_*); step: one hc_block_step per side")
     args = ap.parse_args()
     rank, local_rank, world = dist_env()
     if world > 1:

@@ -20,11 +20,12 @@ from . import _lib
 from ._lib import HcError
 
 __all__ = ["hc_mixes", "hc_split_sinkhorn", "hc_pre_norm", "hc_post", "hc_block_step",
-           "HcError", "library_path", "version"]
+           "hc_chain_begin", "hc_chain_side", "STATE_FLOATS", "HcError", "library_path", "version"]
 
 HC_EPS = 1e-6
 NORM_EPS = 1e-20
 SINKHORN_ITERS = 20
+STATE_FLOATS = 32  # per-token state row of the chained side steps (HC_STATE_FLOATS)
 
 
 def library_path() -> str:
@@ -175,3 +176,56 @@ def hc_block_step(x, pre_mix, f, hc_fn, hc_scale, hc_base, norm_w,
     if return_post_comb:
         return h_norm, y, pre_out, post_out, comb_out
     return h_norm, y, pre_out
+
+
+def hc_chain_begin(x, pre_mix, hc_fn, hc_scale, hc_base, sinkhorn_iters=SINKHORN_ITERS,
+                   eps=HC_EPS, norm_eps=NORM_EPS, state_out=None, pre_out=None, stream=None):
+    """a1-a3 of the first side of a chain and its RMSNorm statistic.  Returns
+    the state [n, 32] of the first side (and fills pre_out [n, hc] if given)."""
+    _check(x, "x", torch.bfloat16)
+    dev = x.device
+    hc, d = x.shape[-2], x.shape[-1]
+    lead = tuple(x.shape[:-2])
+    n = x.numel() // (hc * d) if x.numel() else 0
+    for t, nm in ((pre_mix, "pre_mix"), (hc_fn, "hc_fn"), (hc_scale, "hc_scale"), (hc_base, "hc_base")):
+        _check(t, nm, torch.float32, dev)
+    state_out = _out(state_out, "state_out", lead + (STATE_FLOATS,), torch.float32, dev)
+    if pre_out is not None:
+        pre_out = _out(pre_out, "pre_out", lead + (hc,), torch.float32, dev)
+    with torch.cuda.device(dev):
+        _lib.call("hc_chain_begin", _ptr(x), _ptr(pre_mix), _ptr(hc_fn), _ptr(hc_scale), _ptr(hc_base),
+                  n, hc, d, sinkhorn_iters, eps, norm_eps, _ptr(state_out), _ptr(pre_out), _stream(stream))
+    return state_out
+
+
+def hc_chain_side(x, f, state_in, norm_w, hc_fn_next=None, hc_scale_next=None, hc_base_next=None,
+                  sinkhorn_iters=SINKHORN_ITERS, eps=HC_EPS, norm_eps=NORM_EPS, h_norm=None, y=None,
+                  state_out=None, pre_out=None, stream=None):
+    """a4-a6 of side i from its state, fused with a1-a3 of side i + 1 on the y it
+    produces.  Returns (h_norm, y, state_out); state_out is None for the last
+    side (no next-side weights)."""
+    _check(x, "x", torch.bfloat16)
+    dev = x.device
+    hc, d = x.shape[-2], x.shape[-1]
+    lead = tuple(x.shape[:-2])
+    n = x.numel() // (hc * d) if x.numel() else 0
+    _check(f, "f", torch.bfloat16, dev)
+    _check(state_in, "state_in", torch.float32, dev)
+    _check(norm_w, "norm_w", torch.float32, dev)
+    nxt = hc_fn_next is not None
+    if nxt:
+        for t, nm in ((hc_fn_next, "hc_fn_next"), (hc_scale_next, "hc_scale_next"),
+                      (hc_base_next, "hc_base_next")):
+            _check(t, nm, torch.float32, dev)
+        state_out = _out(state_out, "state_out", lead + (STATE_FLOATS,), torch.float32, dev)
+        if pre_out is not None:
+            pre_out = _out(pre_out, "pre_out", lead + (hc,), torch.float32, dev)
+    else:
+        state_out = pre_out = None
+    h_norm = _out(h_norm, "h_norm", lead + (d,), torch.bfloat16, dev)
+    y = _out(y, "y", tuple(x.shape), torch.bfloat16, dev)
+    with torch.cuda.device(dev):
+        _lib.call("hc_chain_side", _ptr(x), _ptr(f), _ptr(state_in), _ptr(norm_w), _ptr(hc_fn_next),
+                  _ptr(hc_scale_next), _ptr(hc_base_next), n, hc, d, sinkhorn_iters, eps, norm_eps,
+                  _ptr(h_norm), _ptr(y), _ptr(state_out), _ptr(pre_out), _stream(stream))
+    return h_norm, y, state_out

@@ -33,6 +33,8 @@ SIGNATURES = {
     "hc_pre_norm": [P, P, P, I64, I32, I32, F32, P, P],
     "hc_post": [P, P, P, P, I64, I32, I32, P, P],
     "hc_block_step": [P, P, P, P, P, P, P, I64, I32, I32, I32, F32, F32, P, P, P, P, P, P],
+    "hc_chain_begin": [P, P, P, P, P, I64, I32, I32, I32, F32, F32, P, P, P],
+    "hc_chain_side": [P, P, P, P, P, P, P, I64, I32, I32, I32, F32, F32, P, P, P, P, P],
 }
 
 STATUS = {

@@ -87,10 +87,12 @@ int hc_last_cuda_error(void) { return g_last_cuda_error; }
 int hc_version(void) { return 100; }
 
 hc_status hc_consume_device_error(cudaStream_t stream) {
-    unsigned int flag = 0;
+    unsigned int flag = 0, flag_chain = 0;
     hc_status st = cuda_status(hc::consume_device_error(stream, &flag));
     if (st != HC_OK) return st;
-    return flag ? HC_ERR_TIMEOUT : HC_OK;
+    st = cuda_status(hc::consume_chain_device_error(stream, &flag_chain));
+    if (st != HC_OK) return st;
+    return (flag | flag_chain) ? HC_ERR_TIMEOUT : HC_OK;
 }
 
 hc_status hc_split_sinkhorn(const float *mixes, const float *hc_scale, const float *hc_base,
@@ -210,6 +212,74 @@ hc_status hc_block_step(const uint16_t *x, const float *pre_mix, const uint16_t 
     return cuda_status(hc::launch_tokens_simple(x, pre_mix, f, hc_fn, hc_scale, hc_base, norm_w, n,
                                                 d, sinkhorn_iters, eps, norm_eps, h_norm, y,
                                                 pre_out, post_out, comb_out, nullptr, stream));
+}
+
+hc_status hc_chain_begin(const uint16_t *x, const float *pre_mix, const float *hc_fn,
+                         const float *hc_scale, const float *hc_base, int64_t n, int hc, int d,
+                         int sinkhorn_iters, float eps, float norm_eps, float *state_out,
+                         float *pre_out, cudaStream_t stream) {
+    hc_status st = check_shape(n, hc, d, true);
+    if (st != HC_OK) return st;
+    if (sinkhorn_iters < 1 || !finite_nonneg(eps) || !finite_nonneg(norm_eps))
+        return HC_ERR_INVALID_ARG;
+    if (!hc::chain_supported(d)) return HC_ERR_UNSUPPORTED;
+    if (n == 0) return HC_OK;
+    if (!x || !pre_mix || !hc_fn || !hc_scale || !hc_base || !state_out) return HC_ERR_INVALID_ARG;
+    const void *ptrs[] = {x, pre_mix, hc_fn, hc_scale, hc_base, state_out};
+    for (const void *p : ptrs)
+        if (!aligned16(p)) return HC_ERR_MISALIGNED;
+    if (pre_out && !aligned16(pre_out)) return HC_ERR_MISALIGNED;
+    const int64_t mix = (int64_t)(2 + hc) * hc, K = (int64_t)hc * d;
+    const Span ins[] = {span(x, n * K * 2), span(pre_mix, n * hc * 4), span(hc_fn, mix * K * 4),
+                        span(hc_scale, 12), span(hc_base, mix * 4)};
+    const Span outs[] = {span(state_out, n * HC_STATE_FLOATS * 4), span(pre_out, pre_out ? n * hc * 4 : 0)};
+    if ((st = check_alias(outs, 2, ins, 5)) != HC_OK) return st;
+    return cuda_status(hc::launch_chain_begin(x, pre_mix, hc_fn, hc_scale, hc_base, n, d,
+                                              sinkhorn_iters, eps, norm_eps, state_out, pre_out,
+                                              stream));
+}
+
+hc_status hc_chain_side(const uint16_t *x, const uint16_t *f, const float *state_in,
+                        const float *norm_w, const float *hc_fn_next, const float *hc_scale_next,
+                        const float *hc_base_next, int64_t n, int hc, int d, int sinkhorn_iters,
+                        float eps, float norm_eps, uint16_t *h_norm, uint16_t *y,
+                        float *state_out, float *pre_out, cudaStream_t stream) {
+    hc_status st = check_shape(n, hc, d, true);
+    if (st != HC_OK) return st;
+    if (sinkhorn_iters < 1 || !finite_nonneg(eps) || !finite_nonneg(norm_eps))
+        return HC_ERR_INVALID_ARG;
+    if (!hc::chain_supported(d)) return HC_ERR_UNSUPPORTED;
+    if (n == 0) return HC_OK;
+    const bool next = hc_fn_next != nullptr;
+    if (!x || !f || !state_in || !norm_w || !h_norm || !y) return HC_ERR_INVALID_ARG;
+    // the next side's weights come all together, with a state to write, or not at all
+    if (next != (hc_scale_next != nullptr) || next != (hc_base_next != nullptr)) return HC_ERR_INVALID_ARG;
+    if (next && !state_out) return HC_ERR_INVALID_ARG;
+    const void *ptrs[] = {x, f, state_in, norm_w, h_norm, y};
+    for (const void *p : ptrs)
+        if (!aligned16(p)) return HC_ERR_MISALIGNED;
+    if (next) {
+        const void *nptrs[] = {hc_fn_next, hc_scale_next, hc_base_next, state_out};
+        for (const void *p : nptrs)
+            if (!aligned16(p)) return HC_ERR_MISALIGNED;
+    }
+    if (pre_out && !aligned16(pre_out)) return HC_ERR_MISALIGNED;
+    const int64_t mix = (int64_t)(2 + hc) * hc, K = (int64_t)hc * d;
+    const Span ins[] = {span(x, n * K * 2),
+                        span(f, n * d * 2),
+                        span(state_in, n * HC_STATE_FLOATS * 4),
+                        span(norm_w, d * 4),
+                        span(hc_fn_next, next ? mix * K * 4 : 0),
+                        span(hc_scale_next, next ? 12 : 0),
+                        span(hc_base_next, next ? mix * 4 : 0)};
+    const Span outs[] = {span(h_norm, n * d * 2), span(y, n * K * 2),
+                         span(state_out, next ? n * HC_STATE_FLOATS * 4 : 0),
+                         span(pre_out, (next && pre_out) ? n * hc * 4 : 0)};
+    if ((st = check_alias(outs, 4, ins, 7)) != HC_OK) return st;
+    return cuda_status(hc::launch_chain_side(x, f, state_in, norm_w, hc_fn_next, hc_scale_next,
+                                             hc_base_next, n, d, sinkhorn_iters, eps, norm_eps,
+                                             h_norm, y, next ? state_out : nullptr,
+                                             next ? pre_out : nullptr, stream));
 }
 
 }  // extern "C"

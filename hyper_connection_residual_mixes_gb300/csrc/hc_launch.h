@@ -28,8 +28,8 @@ cudaError_t launch_tokens_simple(const uint16_t *x, const float *pre_mix, const 
                                  cudaStream_t s);
 
 // The fused persistent-cluster path (hc_block_cluster.cu).  Supported when d
-// is a multiple of 512 and the per-CTA weight slice fits in shared memory
-// (d <= 5120).  With f == nullptr it computes a1-a3 only.
+// is a multiple of 1024 and one stream's weight fragments fit a tensor-memory
+// quadrant (d <= 7168).  With f == nullptr it computes a1-a3 only.
 bool cluster_path_supported(int d);
 
 cudaError_t launch_block_cluster(const uint16_t *x, const float *pre_mix, const uint16_t *f,
@@ -39,8 +39,25 @@ cudaError_t launch_block_cluster(const uint16_t *x, const float *pre_mix, const 
                                  float *post_out, float *comb_out, float *mixes_out,
                                  cudaStream_t s);
 
+// The chain of side steps fused across sides (hc_chain.cu); same support as
+// the cluster path.
+bool chain_supported(int d);
+
+cudaError_t launch_chain_begin(const uint16_t *x, const float *pre_mix, const float *hc_fn,
+                               const float *hc_scale, const float *hc_base, int64_t n, int d,
+                               int iters, float eps, float norm_eps, float *state_out,
+                               float *pre_out, cudaStream_t s);
+
+// hc_fn_next == nullptr: the last side (no phase 1 of a next side).
+cudaError_t launch_chain_side(const uint16_t *x, const uint16_t *f, const float *state_in,
+                              const float *norm_w, const float *hc_fn_next,
+                              const float *hc_scale_next, const float *hc_base_next, int64_t n,
+                              int d, int iters, float eps, float norm_eps, uint16_t *h_norm,
+                              uint16_t *y, float *state_out, float *pre_out, cudaStream_t s);
+
 // Synchronise `s`, then read and clear the device flag that bounded waits set
-// when they time out.
+// when they time out (each of the two kernel files keeps its own flag).
 cudaError_t consume_device_error(cudaStream_t s, unsigned int *flag);
+cudaError_t consume_chain_device_error(cudaStream_t s, unsigned int *flag);
 
 }  // namespace hc

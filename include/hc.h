@@ -152,6 +152,52 @@ hc_status hc_block_step(const uint16_t *x, const float *pre_mix, const uint16_t 
                         float *pre_out, float *post_out, float *comb_out,
                         cudaStream_t stream);
 
+/*
+ * A chain of fused side steps, fused across sides (the Block page's
+ * Block.forward: the streams a side reads are the y the previous side wrote,
+ * and each side reads its sublayer input with the previous side's pre).  The
+ * results equal, bit for bit, those of calling hc_block_step side after side;
+ * each launch reads its side's streams from HBM once.
+ *
+ * State rows.  A state buffer holds, per token, HC_STATE_FLOATS = 32 fp32:
+ *   [0:4] post, [4:20] comb (row-major j*hc+k), [20] RMSNorm scale
+ *   rsqrt(mean(h^2) + norm_eps), [21:24] zero, [24:28] pre (the side's pre:
+ *   the next side's pre_mix), [28:32] pre_mix (the one the side reads with).
+ * The caller allocates it ([n, 32] fp32, 16-byte aligned) and keeps two of
+ * them in rotation: side i reads the state of side i and writes that of side
+ * i + 1 (the two may not overlap: HC_ERR_ALIAS).  Supported when d is a
+ * multiple of 1024 and d <= 7168 (HC_ERR_UNSUPPORTED otherwise).
+ *
+ * hc_chain_begin: a1-a3 of the first side and its RMSNorm statistic.
+ *   x [n, hc, d] bf16, pre_mix [n, hc] fp32, hc_fn, hc_scale, hc_base of the
+ *   first side                                                       in
+ *   state_out [n, 32] fp32   out: state of the first side
+ *   pre_out [n, hc] fp32     out, optional (NULL: not written): its pre
+ *
+ * hc_chain_side: a4-a6 of side i from its state, fused with a1-a3 of side
+ * i + 1 on the y it produces.
+ *   x [n, hc, d] bf16 (side i's streams), f [n, d] bf16, state_in [n, 32]
+ *   (side i), norm_w [d] (side i), hc_fn_next, hc_scale_next, hc_base_next
+ *   (side i + 1; all three NULL for the last side)                    in
+ *   h_norm [n, d] bf16, y [n, hc, d] bf16   out: as hc_block_step's
+ *   state_out [n, 32] fp32   out: state of side i + 1 (unused for the last side)
+ *   pre_out [n, hc] fp32     out, optional: side i + 1's pre
+ * No cited passage has a counterpart for the state rows: they carry one side's
+ * coefficients to the next launch.
+ */
+#define HC_STATE_FLOATS 32
+
+hc_status hc_chain_begin(const uint16_t *x, const float *pre_mix, const float *hc_fn,
+                         const float *hc_scale, const float *hc_base, int64_t n, int hc, int d,
+                         int sinkhorn_iters, float eps, float norm_eps, float *state_out,
+                         float *pre_out, cudaStream_t stream);
+
+hc_status hc_chain_side(const uint16_t *x, const uint16_t *f, const float *state_in,
+                        const float *norm_w, const float *hc_fn_next, const float *hc_scale_next,
+                        const float *hc_base_next, int64_t n, int hc, int d, int sinkhorn_iters,
+                        float eps, float norm_eps, uint16_t *h_norm, uint16_t *y,
+                        float *state_out, float *pre_out, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

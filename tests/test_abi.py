@@ -125,6 +125,60 @@ def test_pre_norm_and_post_validation(lib):
                     FAKE2 * 0x300 + 8, None) == 3
 
 
+def _side(**kw):
+    a = dict(x=FAKE, f=FAKE + 0x100000, state_in=FAKE + 0x200000, norm_w=FAKE + 0x300000,
+             fn=FAKE + 0x400000, scale=FAKE + 0x500000, base=FAKE + 0x600000, n=16, hc=4, d=5120,
+             iters=20, eps=1e-6, norm_eps=1e-20, h_norm=FAKE2 * 0x100, y=FAKE2 * 0x200,
+             state_out=FAKE2 * 0x300, pre_out=None, stream=None)
+    a.update(kw)
+    return _lib.raw("hc_chain_side", a["x"], a["f"], a["state_in"], a["norm_w"], a["fn"], a["scale"],
+                    a["base"], a["n"], a["hc"], a["d"], a["iters"], a["eps"], a["norm_eps"], a["h_norm"],
+                    a["y"], a["state_out"], a["pre_out"], a["stream"])
+
+
+def _begin(**kw):
+    a = dict(x=FAKE, pre_mix=FAKE + 0x100000, fn=FAKE + 0x200000, scale=FAKE + 0x300000,
+             base=FAKE + 0x400000, n=16, hc=4, d=5120, iters=20, eps=1e-6, norm_eps=1e-20,
+             state_out=FAKE2 * 0x100, pre_out=None, stream=None)
+    a.update(kw)
+    return _lib.raw("hc_chain_begin", a["x"], a["pre_mix"], a["fn"], a["scale"], a["base"], a["n"],
+                    a["hc"], a["d"], a["iters"], a["eps"], a["norm_eps"], a["state_out"], a["pre_out"],
+                    a["stream"])
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(scale=None), 1),                 # next-side weights come all together or not at all
+    (dict(base=None), 1),
+    (dict(state_out=None), 1),             # a next side needs a state to write
+    (dict(d=320), 2),                      # the chain needs d a multiple of 1024 ...
+    (dict(d=8192), 2),                     # ... and d <= 7168
+    (dict(hc=3), 2),
+    (dict(state_in=FAKE + 0x200008), 3),
+    (dict(y=FAKE + 64), 4),                # y overlaps x
+    (dict(state_out=FAKE + 0x200010), 4),  # state_out overlaps state_in
+    (dict(n=-1), 1),
+])
+def test_chain_side_validation(lib, kw, expect):
+    assert _side(**kw) == expect
+
+
+def test_chain_side_last_needs_no_state_and_empty_is_ok(lib):
+    # the last side: no next weights, no state to write (still validated, then empty)
+    assert _side(n=0, fn=None, scale=None, base=None, state_out=None) == 0
+    assert _side(n=0) == 0
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(d=2048 + 64), 2),
+    (dict(state_out=None), 1),
+    (dict(state_out=FAKE2 * 0x100 + 4), 3),
+    (dict(state_out=FAKE + 0x100), 4),     # state_out overlaps x
+    (dict(iters=0), 1),
+])
+def test_chain_begin_validation(lib, kw, expect):
+    assert _begin(**kw) == expect
+
+
 def test_binding_rejects_cpu_tensors():
     import torch
     import hyper_connection_residual_mixes_gb300 as hcg
