@@ -47,7 +47,12 @@ constexpr int kCB = 64;          // columns per slot per stream (128-byte box ro
 constexpr int kItems = 2;        // 8-column items per CUDA-core thread per slot
 constexpr int kStepsPerSlot = kCB / 16;
 constexpr int kSlots = 4;        // TMA ring depth (40 KB per slot)
-constexpr int kBufs = 2;         // partial-sum buffers at the owners, in rotation
+// Tiles in flight between the CUDA-core warps and the owners: the partial-sum
+// buffers at the owners and the sum-of-squares buffers rotate over kBufs, and
+// the CUDA-core warps start tile j once the owners are done with tile j - kBufs.
+// The owners' reduction + Sinkhorn latency sits in that loop; with two tiles the
+// loop had no slack (measured: the launch time tracked the Sinkhorn rounds).
+constexpr int kBufs = 3;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kThreads = 512;
 constexpr int kBoxBytes = kT * kCB * 2;                // 8 KB
@@ -66,7 +71,7 @@ constexpr int kWarpSender = 14;
 constexpr int kWarpStore = 15;
 constexpr int kWCols = 18;       // TMEM columns per k16 step: 3 n-tiles x (hi, mid, lo) x (b0, b1)
 constexpr int kBegin = 0, kSide = 1, kLast = 2;
-constexpr int kNumBars = 3 * kSlots + 2 * kBufs + 2 + 2 + 2;  // full, empty, staged, part, coef, mma, ss, state
+constexpr int kNumBars = 3 * kSlots + 3 * kBufs + 2 + 2;  // full, empty, staged, part, coef, ss, mma, state
 
 struct Params {
     const float *state_in;   // [n, 32]: state of side i (kSide, kLast)
@@ -104,7 +109,7 @@ __host__ __device__ inline Layout make_layout(int d) {
     L.off_part = o;
     o += kBufs * kC * kTokPerOwner * kPartF * 4;
     L.off_ss = o;
-    o += 2 * kT * 2 * 4;
+    o += kBufs * kT * 2 * 4;
     L.off_normw = o;
     o += L.dc * 4;
     o = (o + 15) & ~15;
@@ -168,7 +173,7 @@ k_chain(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtens
     const uint32_t mma_free = bar0 + 8u * (3 * kSlots + 2 * kBufs + 1);
     auto ss_bar = [&](int b) { return bar0 + 8u * (3 * kSlots + 2 * kBufs + 2 + b); };
     // the CUDA-core warps are done with a tile's state rows (buffer b)
-    auto state_free = [&](int b) { return bar0 + 8u * (3 * kSlots + 2 * kBufs + 4 + b); };
+    auto state_free = [&](int b) { return bar0 + 8u * (3 * kSlots + 3 * kBufs + 2 + b); };
     const uint32_t slot0 = smem_u32(smem);
 
     if (threadIdx.x == kWarpProducer * 32) {
@@ -182,11 +187,9 @@ k_chain(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtens
         for (int b = 0; b < kBufs; ++b) {
             mbar_init(part_bar(b), kC * 2);
             mbar_init(coef_bar(b), kC * 2);
-        }
-        for (int b = 0; b < 2; ++b) {
             mbar_init(ss_bar(b), kT);
-            mbar_init(state_free(b), kCudaWarps);
         }
+        for (int b = 0; b < 2; ++b) mbar_init(state_free(b), kCudaWarps);
         mbar_init(mma_full, kMmaWarps * 32);
         mbar_init(mma_free, 32);
         fence_mbar_init_cluster();
@@ -366,7 +369,7 @@ k_chain(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtens
                 split_sinkhorn_token<true>(mm, s0, s1, s2, p.hc_base, p.iters, p.eps, pr, po, c);
                 const float rs_h = rsqrtf(ssh / (float)d + p.norm_eps);
                 // pace the CUDA-core warps of every CTA: they wait for this arrival of
-                // tile j before starting tile j + 2 (lane l -> destination CTA l % 16)
+                // tile j before starting tile j + kBufs (lane l -> destination CTA l % 16)
                 // the partials read above complete before the senders may overwrite them
                 __threadfence_block();
                 mbar_arrive_remote(mapa(coef_bar(buf), lane & 15));
@@ -392,7 +395,7 @@ k_chain(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtens
         if (kP1) {
             for (int j = 0; j < J; ++j) {
                 if (!mbar_wait_warp<false>(mma_full, (uint32_t)j & 1u, &s_abort)) break;
-                if (!mbar_wait_warp<false>(ss_bar(j & 1), (uint32_t)(j >> 1) & 1u, &s_abort)) break;
+                if (!mbar_wait_warp<false>(ss_bar(j % kBufs), (uint32_t)(j / kBufs) & 1u, &s_abort)) break;
                 const int buf = j % kBufs;
                 const int owner = lane >> 1;
 #pragma unroll
@@ -408,7 +411,7 @@ k_chain(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtens
 #pragma unroll
                         for (int i = 0; i < kMix; ++i) v[i] += e[i];
                     }
-                    const float2 ss = *reinterpret_cast<const float2 *>(sSS + ((j & 1) * kT + tk) * 2);
+                    const float2 ss = *reinterpret_cast<const float2 *>(sSS + ((j % kBufs) * kT + tk) * 2);
                     v[kMix] = ss.x;
                     v[kMix + 1] = ss.y;
                     v[kMix + 2] = v[kMix + 3] = 0.0f;
@@ -454,10 +457,10 @@ k_chain(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtens
         int u = 0;
         bool ok = true;
         for (int j = 0; j < J && ok; ++j) {
-            if (kP1 && j >= 2) {
-                // Wait for the owners' signal for tile j - 2: every hand-off buffer of
-                // that tile (sums of squares here, partials at the owners) has been read.
-                const int jw = j - 2;
+            if (kP1 && j >= kBufs) {
+                // Wait for the owners' signal for tile j - kBufs: every hand-off buffer
+                // of that tile (sums of squares here, partials at the owners) has been read.
+                const int jw = j - kBufs;
                 if (!mbar_wait_warp<true>(coef_bar(jw % kBufs), (uint32_t)(jw / kBufs) & 1u, &s_abort)) break;
             }
             const int64_t tok = (int64_t)(cid + j * ncl) * kT + r;
@@ -599,8 +602,8 @@ k_chain(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtens
                 ssh += __shfl_xor_sync(0xffffffffu, ssh, 1);
                 ssh += __shfl_xor_sync(0xffffffffu, ssh, 2);
                 if (uu == 0) {
-                    *reinterpret_cast<float2 *>(sSS + ((j & 1) * kT + r) * 2) = make_float2(ssx, ssh);
-                    mbar_arrive(ss_bar(j & 1));
+                    *reinterpret_cast<float2 *>(sSS + ((j % kBufs) * kT + r) * 2) = make_float2(ssx, ssh);
+                    mbar_arrive(ss_bar(j % kBufs));
                 }
             }
         }
