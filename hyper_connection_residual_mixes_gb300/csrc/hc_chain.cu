@@ -137,7 +137,7 @@ template <int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
 k_chain(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_f,
         const __grid_constant__ CUtensorMap tm_y, const __grid_constant__ CUtensorMap tm_h,
-        const Params p) {
+        const __grid_constant__ CUtensorMap tm_s, const Params p) {
     constexpr bool kP1 = kMode != kLast;   // phase 1 of a side runs here
     constexpr bool kP3 = kMode != kBegin;  // phase 3 of side i runs here
     extern __shared__ uint8_t smem_raw[];
@@ -198,6 +198,7 @@ k_chain(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtens
             prefetch_tmap(&tm_f);
             prefetch_tmap(&tm_y);
             prefetch_tmap(&tm_h);
+            prefetch_tmap(&tm_s);
         }
     }
     if (kP1 && warp == kWarpMma) {
@@ -297,6 +298,7 @@ k_chain(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtens
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();  // every byte is read once
+            const uint64_t pol_state = policy_evict_normal();  // the 16 CTAs of a cluster read each state row
             int armed = 0, j = 0, cb = 0;
             for (int u = 0; u < U; ++u) {
                 const int slot = u % kSlots;
@@ -314,7 +316,8 @@ k_chain(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtens
                         break;
                     const int64_t rows_left = p.n - (int64_t)row;
                     const uint32_t rows = (uint32_t)(rows_left < kT ? rows_left : kT);
-                    side_bytes = (kMode == kBegin ? 16u : 4u * kStateF) * rows;
+                    // a TMA box always delivers all its bytes (rows past n read as zero)
+                    side_bytes = kMode == kBegin ? 16u * rows : 4u * kStateF * kT;
                 }
                 mbar_arrive_expect_tx(full_bar(slot), (kP3 ? kSlotBytes : kStageXBytes) + side_bytes);
                 if (cb == 0) {
@@ -322,7 +325,7 @@ k_chain(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtens
                     if (kMode == kBegin)
                         bulk_load(sdst, p.pre_mix + (int64_t)row * kHC, side_bytes, full_bar(slot));
                     else
-                        bulk_load(sdst, p.state_in + (int64_t)row * kStateF, side_bytes, full_bar(slot));
+                        tma_load_2d(sdst, &tm_s, full_bar(slot), 0, row, pol_state);
                 }
                 for (int s = 0; s < kHC; ++s) tma_load_2d(dst + s * kBoxBytes, &tm_x, full_bar(slot), s * d + col, row, pol);
                 if (kP3) tma_load_2d(dst + kStageXBytes, &tm_f, full_bar(slot), col, row, pol);
@@ -465,8 +468,9 @@ k_chain(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtens
             }
             const int64_t tok = (int64_t)(cid + j * ncl) * kT + r;
             const bool live = tok < p.n;
-            // this tile's state row of the token (kBegin: its pre_mix row, 4 floats at r * kHC)
-            const float *srow = sState + ((j & 1) * kT + r) * kStateF;
+            // this tile's state rows (kSide, kLast: 128-byte rows with the 128-byte swizzle,
+            // so the eight rows of a warp read distinct banks; kBegin: pre_mix rows)
+            const uint8_t *srow = reinterpret_cast<const uint8_t *>(sState) + (j & 1) * kT * kStateF * 4;
             f32x2 ssx2[kHC], ssh2[kItems];
 #pragma unroll
             for (int s = 0; s < kHC; ++s) ssx2[s] = f2_dup(0.0f);
@@ -517,6 +521,17 @@ k_chain(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtens
                     const uint4 fr0 = *reinterpret_cast<const uint4 *>(sb + kStageXBytes + swz(r, uu));
                     const uint4 fr1 = *reinterpret_cast<const uint4 *>(sb + kStageXBytes + swz(r, uu + 4));
                     if (live) {
+                        float cf[kHC + kHC * kHC];  // post, comb: 16-byte chunks 0-4 of the row
+#pragma unroll
+                        for (int c = 0; c < 5; ++c) {
+                            const float4 v = *reinterpret_cast<const float4 *>(srow + swz(r, c));
+                            cf[4 * c] = v.x;
+                            cf[4 * c + 1] = v.y;
+                            cf[4 * c + 2] = v.z;
+                            cf[4 * c + 3] = v.w;
+                        }
+                        const float rs = *reinterpret_cast<const float *>(srow + swz(r, 5));
+                        const float4 pmv = *reinterpret_cast<const float4 *>(srow + swz(r, 7));
 #pragma unroll
                         for (int it = 0; it < kItems; ++it) {
                             const uint4 &fw = it == 0 ? fr0 : fr1;
@@ -525,11 +540,6 @@ k_chain(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtens
                             const float4 w0 = nw[0], w1 = nw[1];
                             const f32x2 wv[4] = {f2_make(w0.x, w0.y), f2_make(w0.z, w0.w), f2_make(w1.x, w1.y),
                                                  f2_make(w1.z, w1.w)};
-                            float cf[kHC + kHC * kHC];
-#pragma unroll
-                            for (int q = 0; q < kHC + kHC * kHC; ++q) cf[q] = srow[q];
-                            const float rs = srow[20];
-                            const float4 pmv = *reinterpret_cast<const float4 *>(srow + 28);
                             uint32_t yo[kHC][4], ho[4];
 #pragma unroll
                             for (int q = 0; q < 4; ++q) {
@@ -562,7 +572,7 @@ k_chain(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtens
                             *reinterpret_cast<uint4 *>(wb + kStageXBytes) = make_uint4(ho[0], ho[1], ho[2], ho[3]);
                             if (kMode == kSide) {
                                 // phase 1 of side i+1 on this y: its x is y, its pre_mix side i's pre
-                                const float4 pn = *reinterpret_cast<const float4 *>(srow + 24);
+                                const float4 pn = *reinterpret_cast<const float4 *>(srow + swz(r, 6));
 #pragma unroll
                                 for (int q = 0; q < 4; ++q) {
                                     f32x2 ys[kHC];
@@ -648,6 +658,19 @@ bool chain_tmap(CUtensorMap *m, const void *base, int64_t rows, int64_t cols) {
                CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// n x 32 fp32 state rows, box of 64 rows x 32 floats (128 bytes), 128-byte swizzle
+bool chain_state_tmap(CUtensorMap *m, const float *base, int64_t rows) {
+    auto enc = chain_encode();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)ch::kStateF, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)ch::kStateF * 4};
+    cuuint32_t box[2] = {(cuuint32_t)ch::kStateF, (cuuint32_t)ch::kT};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int g_chain_clusters[64] = {};
 
 template <int kMode>
@@ -684,18 +707,18 @@ cudaError_t launch_chain_impl(const ch::Params &prm, const uint16_t *x, const ui
     const int ncl = (int)(tiles < mc ? tiles : mc);
     cfg.gridDim = dim3(ch::kC * ncl);
     const int d = prm.d;
-    CUtensorMap tmx, tmf, tmy, tmh;
+    CUtensorMap tmx, tmf, tmy, tmh, tms;
     if (!chain_tmap(&tmx, x, prm.n, (int64_t)kHC * d)) return cudaErrorInvalidValue;
     if (kMode != ch::kBegin) {
         if (!chain_tmap(&tmf, f, prm.n, d) || !chain_tmap(&tmy, y, prm.n, (int64_t)kHC * d) ||
-            !chain_tmap(&tmh, h_norm, prm.n, d))
+            !chain_tmap(&tmh, h_norm, prm.n, d) || !chain_state_tmap(&tms, prm.state_in, prm.n))
             return cudaErrorInvalidValue;
     } else {
-        tmf = tmy = tmh = tmx;
+        tmf = tmy = tmh = tms = tmx;
     }
     ch::Params p = prm;
     p.num_tiles = (int)tiles;
-    e = cudaLaunchKernelEx(&cfg, kern, tmx, tmf, tmy, tmh, p);
+    e = cudaLaunchKernelEx(&cfg, kern, tmx, tmf, tmy, tmh, tms, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
