@@ -344,11 +344,24 @@ k_chain(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtens
         if (kP1) {
             const float s0 = __ldg(p.hc_scale), s1 = __ldg(p.hc_scale + 1), s2 = __ldg(p.hc_scale + 2);
             const int tl = lane >> 3, sub = lane & 7;
+            const int tk = (int)rank * kTokPerOwner + tl;
+            // The pre_mix the side reads with (the first side's input, or the previous
+            // side's pre, kept in the previous side's state) goes into the state row.  It
+            // is read from global memory one tile ahead, so that its latency does not hold
+            // up the next tile's reduction.
+            auto load_pmx = [&](int jj) {
+                const int64_t t = (int64_t)(cid + jj * ncl) * kT + tk;
+                if (jj >= J || t >= p.n) return make_float4(0.f, 0.f, 0.f, 0.f);
+                return kMode == kBegin ? __ldg(reinterpret_cast<const float4 *>(p.pre_mix) + t)
+                                       : __ldg(reinterpret_cast<const float4 *>(p.state_in + t * kStateF + 24));
+            };
+            float4 pmx_next = load_pmx(0);
             for (int j = 0; j < J; ++j) {
+                const float4 pmx = pmx_next;
+                pmx_next = load_pmx(j + 1);
                 const int buf = j % kBufs;
                 if (!mbar_wait_warp<true>(part_bar(buf), (uint32_t)(j / kBufs) & 1u, &s_abort)) break;
                 const int tile = cid + j * ncl;
-                const int tk = (int)rank * kTokPerOwner + tl;
                 const int64_t tok = (int64_t)tile * kT + tk;
                 float m[kMix + 2];
                 {
@@ -377,11 +390,6 @@ k_chain(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtens
                 __threadfence_block();
                 mbar_arrive_remote(mapa(coef_bar(buf), lane & 15));
                 if (sub == 0 && tok < p.n) {
-                    // the pre_mix this side reads with: the first side's input, or the
-                    // previous side's pre (kept in the previous side's state)
-                    const float4 pmx = kMode == kBegin
-                                           ? reinterpret_cast<const float4 *>(p.pre_mix)[tok]
-                                           : *reinterpret_cast<const float4 *>(p.state_in + tok * kStateF + 24);
                     float4 *st = reinterpret_cast<float4 *>(p.state_out + tok * kStateF);
                     st[0] = make_float4(po[0], po[1], po[2], po[3]);
 #pragma unroll

@@ -135,6 +135,14 @@ __device__ __forceinline__ void split_sinkhorn_token(const float (&m)[kMix], flo
 #pragma unroll
     for (int i = 0; i < kHC * kHC; ++i) c[i] = fmaf(m[2 * kHC + i], s2, base[2 * kHC + i]);
 
+    // Pairs of adjacent entries of a row, P[j][h] = (c[j][2h], c[j][2h+1]), for the
+    // packed multiplies and column sums.  Every element sees exactly the scalar
+    // operations in the scalar order (rows summed left to right, columns top to
+    // bottom, then + eps, a reciprocal and a multiply), so the results are those of
+    // the plain per-element loops, with fewer instructions.
+    static_assert(kHC == 4, "a row is two packed pairs");
+    const f32x2 eps2 = f2_dup(eps);
+    f32x2 P[kHC][2];
     // first round: row softmax + eps
 #pragma unroll
     for (int j = 0; j < kHC; ++j) {
@@ -147,39 +155,38 @@ __device__ __forceinline__ void split_sinkhorn_token(const float (&m)[kMix], flo
             c[j * kHC + k] = expo<kFast>(c[j * kHC + k] - mx);
             s += c[j * kHC + k];
         }
-        const float r = recip<kFast>(s);
-#pragma unroll
-        for (int k = 0; k < kHC; ++k) c[j * kHC + k] = fmaf(c[j * kHC + k], r, eps);
+        const f32x2 r = f2_dup(recip<kFast>(s));
+        P[j][0] = f2_fma(f2_make(c[j * kHC], c[j * kHC + 1]), r, eps2);
+        P[j][1] = f2_fma(f2_make(c[j * kHC + 2], c[j * kHC + 3]), r, eps2);
     }
-    // first round: columns
+    auto columns = [&]() {
 #pragma unroll
-    for (int k = 0; k < kHC; ++k) {
-        float s = 0.0f;
+        for (int h = 0; h < 2; ++h) {
+            const f32x2 sum = f2_add(f2_add(f2_add(f2_add(P[0][h], P[1][h]), P[2][h]), P[3][h]), eps2);
+            float s0c, s1c;
+            f2_split(sum, s0c, s1c);
+            const f32x2 r = f2_make(recip<kFast>(s0c), recip<kFast>(s1c));
 #pragma unroll
-        for (int j = 0; j < kHC; ++j) s += c[j * kHC + k];
-        const float r = recip<kFast>(s + eps);
-#pragma unroll
-        for (int j = 0; j < kHC; ++j) c[j * kHC + k] *= r;
-    }
+            for (int j = 0; j < kHC; ++j) P[j][h] = f2_mul(P[j][h], r);
+        }
+    };
+    columns();  // first round: columns
     for (int it = 1; it < iters; ++it) {
 #pragma unroll
         for (int j = 0; j < kHC; ++j) {
-            float s = 0.0f;
-#pragma unroll
-            for (int k = 0; k < kHC; ++k) s += c[j * kHC + k];
-            const float r = recip<kFast>(s + eps);
-#pragma unroll
-            for (int k = 0; k < kHC; ++k) c[j * kHC + k] *= r;
+            float a0, a1, a2, a3;
+            f2_split(P[j][0], a0, a1);
+            f2_split(P[j][1], a2, a3);
+            const f32x2 r = f2_dup(recip<kFast>(((a0 + a1) + a2) + a3 + eps));
+            P[j][0] = f2_mul(P[j][0], r);
+            P[j][1] = f2_mul(P[j][1], r);
         }
+        columns();
+    }
 #pragma unroll
-        for (int k = 0; k < kHC; ++k) {
-            float s = 0.0f;
-#pragma unroll
-            for (int j = 0; j < kHC; ++j) s += c[j * kHC + k];
-            const float r = recip<kFast>(s + eps);
-#pragma unroll
-            for (int j = 0; j < kHC; ++j) c[j * kHC + k] *= r;
-        }
+    for (int j = 0; j < kHC; ++j) {
+        f2_split(P[j][0], c[j * kHC], c[j * kHC + 1]);
+        f2_split(P[j][1], c[j * kHC + 2], c[j * kHC + 3]);
     }
 }
 
