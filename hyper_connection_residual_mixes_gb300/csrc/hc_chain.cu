@@ -185,7 +185,7 @@ k_chain(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtens
             mbar_init(staged_bar(s), kCudaWarps);
         }
         for (int b = 0; b < kBufs; ++b) {
-            mbar_init(part_bar(b), kC * 2);
+            mbar_init(part_bar(b), kC * 4);
             mbar_init(coef_bar(b), kC * 2);
             mbar_init(ss_bar(b), kT);
         }
@@ -408,11 +408,11 @@ k_chain(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtens
                 if (!mbar_wait_warp<false>(mma_full, (uint32_t)j & 1u, &s_abort)) break;
                 if (!mbar_wait_warp<false>(ss_bar(j % kBufs), (uint32_t)(j / kBufs) & 1u, &s_abort)) break;
                 const int buf = j % kBufs;
-                const int owner = lane >> 1;
 #pragma unroll
                 for (int i2 = 0; i2 < 2; ++i2) {
-                    const int tk = 2 * lane + i2;
-                    const int tl = tk % kTokPerOwner;
+                    // tokens lane and lane + 32: neighbouring lanes read neighbouring rows
+                    const int tk = lane + 32 * i2;
+                    const int owner = tk / kTokPerOwner, tl = tk % kTokPerOwner;
                     float v[kPartF];
 #pragma unroll
                     for (int i = 0; i < kMix; ++i) v[i] = 0.0f;
@@ -430,8 +430,8 @@ k_chain(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtens
 #pragma unroll
                     for (int q = 0; q < kPartF / 4; ++q)
                         st_cluster_v4(dst + 16 * q, v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                    mbar_arrive_remote(mapa(part_bar(buf), owner));
                 }
-                mbar_arrive_remote(mapa(part_bar(buf), owner));
                 mbar_arrive(mma_free);
             }
         }
