@@ -1,12 +1,15 @@
 #!/usr/bin/env python3
-"""Benchmark of the fused hyper-connection side step (hc_block_step).
+"""Benchmark of the fused hyper-connection side steps.
 
 Workload (default): long prefill -- 4 x 16384 = 65,536 tokens, hc = 4,
 d = 5120, through 40 layers = 80 side steps, each side with its own seeded
 parameters and its own N(0, 2) sublayer stand-in output.  One benchmark
 "step" is one pass of all 80 side steps over the batch.  Metric: tokens/s
-through the full depth (plus achieved HBM GB/s of the side-step kernel
-against the measured HBM peak).
+through the full depth (plus achieved HBM GB/s of the dominant kernel
+against the measured HBM peak).  By default the sides run as the chain
+fused across sides (hc_chain_begin + one hc_chain_side per side, outputs
+equal to hc_block_step's bit for bit); the same sides as one hc_block_step
+launch each are timed beside it (--path step makes them the headline).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -224,12 +227,12 @@ def run_ours(args, rank, local_rank, world):
     chain = args.path == "chain"
     states = [torch.empty((n, hcg.STATE_FLOATS), device=dev) for _ in range(2)] if chain else None
 
-    def step(events=None):
-        if chain:
-            # the sides fused across sides: each launch finishes side s and starts s + 1
-            run_chain(case, x0, pm0, fs, ys, pres, h_norm, states, events, stream)
-            launches["n"] += sides + 1
-            return
+    def step_chain(events=None):
+        # the sides fused across sides: each launch finishes side s and starts s + 1
+        run_chain(case, x0, pm0, fs, ys, pres, h_norm, states, events, stream)
+        launches["n"] += sides + 1
+
+    def step_blocks(events=None):
         x, pm = x0, pm0
         for s in range(sides):
             if events is not None:
@@ -240,6 +243,8 @@ def run_ours(args, rank, local_rank, world):
                 events[s][1].record(stream)
             launches["n"] += 1
             x, pm = ys[s % 2], pres[s % 2]
+
+    step = step_chain if chain else step_blocks
 
     for _ in range(args.warmup):
         step()
@@ -271,6 +276,24 @@ def run_ours(args, rank, local_rank, world):
     if world > 1:
         elapsed_ms = max_over_ranks(elapsed_ms, dev)
 
+    # The same workload through one hc_block_step launch per side, timed the same
+    # way on fewer steps, beside the chain's figures.
+    blocks = None
+    if chain and args.workload == "long_prefill" and not args.no_step_path:
+        k_b = max(2, args.steps // 2)
+        step_blocks()
+        torch.cuda.synchronize(dev)
+        evb = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(sides)] for _ in range(k_b)]
+        b0 = torch.cuda.Event(enable_timing=True)
+        b1 = torch.cuda.Event(enable_timing=True)
+        b0.record(stream)
+        for k in range(k_b):
+            step_blocks(evb[k])
+        b1.record(stream)
+        torch.cuda.synchronize(dev)
+        blocks = (b0.elapsed_time(b1) / k_b, [a.elapsed_time(b) for e in evb for (a, b) in e], k_b)
+
     e2e = None if (args.no_e2e or args.workload != "long_prefill") else \
         run_e2e(args, dev, case, seed, world)
     out = None
@@ -301,9 +324,9 @@ def run_ours(args, rank, local_rank, world):
             "config": {"workload": args.workload, "description": WORKLOADS[args.workload][2],
                        "tokens": n, "hc": HC, "d": d, "side_steps": sides,
                        "sinkhorn_iters": 20, "seed": seed, "parallelism": "replicas" if world > 1 else "single",
-                       "path": ("chain: hc_chain_begin + 80 hc_chain_side, each side's launch also "
+                       "path": ("chain: hc_chain_begin + %d hc_chain_side, each side's launch also "
                                 "computing the next side's coefficients; outputs equal hc_block_step's "
-                                "bit for bit") if chain else "step: 80 hc_block_step launches",
+                                "bit for bit" % sides) if chain else "step: %d hc_block_step launches" % sides,
                        "l2": ("inputs larger than L2 (x is %.2f GB per side, L2 %.0f MB); no flush"
                               % (n * HC * d * 2 / 1e9, L2_BYTES / 1e6))
                              if n * HC * d * 2 > L2_BYTES else
@@ -324,6 +347,15 @@ def run_ours(args, rank, local_rank, world):
             "gpu_launches": gpu_launches,
             "e2e": e2e,
         }
+        if blocks is not None:
+            b_ms, b_launch, k_b = blocks
+            b_avg_s = statistics.mean(b_launch) / 1e3
+            out["hc_block_step_path"] = {
+                "value": world * n / (b_ms / 1e3), "unit": "tokens/s", "ms_per_step": b_ms, "steps": k_b,
+                "roofline_frac": alg_bytes / b_avg_s / 1e9 / peak, "avg_launch_us": b_avg_s * 1e6,
+                "traffic": ncu_traffic_per_launch(n, "step"),
+                "note": "the same sides as one hc_block_step launch each, timed after the chain's "
+                        "steps (rank 0's clock); outputs identical to the chain's bit for bit"}
         if world == 1 and not args.no_cpu_baseline and args.workload == "long_prefill":
             out["cpu_baseline"] = cpu_baseline_sample(case, fs, target_s=args.cpu_seconds)
     return out
@@ -559,6 +591,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling runs)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--reference-tokens", type=int, default=4)
+    ap.add_argument("--no-step-path", action="store_true",
+                    help="with the chain, skip timing the one-launch-per-side path beside it")
     ap.add_argument("--path", choices=["chain", "step"], default="chain",
                     help="chain: the sides fused across sides (hc_chain_*); step: one hc_block_step per side")
     args = ap.parse_args()
