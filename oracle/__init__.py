@@ -15,7 +15,8 @@ ctypes.  Every function cites the page passage it follows in the C source:
 * DeepSeek-V4.1 "Stream combination" page, Code section -- the split of the
   24 mix numbers and the Sinkhorn rounds.
 * DeepSeek V4.1 Flash diagram -- the Cast, sigma, 2 sigma, x + eps_hc,
-  First Sinkhorn Round and Sinkhorn Round blocks.
+  First Sinkhorn Round and Sinkhorn Round blocks, and the Cast to MXFP8
+  block (groups of 32, UE8M0 scale, E4M3 elements).
 * DeepSeek-R1 dossier, RMSNorm records -- the RMSNorm body (the V4.1 body is
   not on the pages).
 
@@ -69,8 +70,11 @@ def _load():
         lib.hco_post.argtypes = [P, P, P, P, i64, i32, i32, P]
         lib.hco_block_step.argtypes = [P, P, P, P, P, P, P, i64, i32, i32, i32, f64, f64,
                                        P, P, P, P, P, P]
+        lib.hco_e4m3_from_double.argtypes = [f64]
+        lib.hco_e4m3_from_double.restype = ctypes.c_uint8
+        lib.hco_mxfp8.argtypes = [P, i64, i32, P, P]
         for name in ("hco_mixes", "hco_split_sinkhorn", "hco_pre", "hco_rmsnorm",
-                     "hco_post", "hco_block_step"):
+                     "hco_post", "hco_block_step", "hco_mxfp8"):
             getattr(lib, name).restype = i32
         _lib = lib
         return lib
@@ -165,6 +169,40 @@ def rmsnorm(h, w, eps=1e-20):
     _check(_load().hco_rmsnorm(hp, wp, n, d, float(eps), out.ctypes.data_as(ctypes.c_void_p)),
            "rmsnorm")
     return out
+
+
+def e4m3_from_f64(v) -> np.ndarray:
+    """E4M3 bytes of doubles within [-448, 448] (nearest, ties to even)."""
+    lib = _load()
+    v = np.asarray(v, dtype=np.float64)
+    flat = v.reshape(-1)
+    out = np.empty(flat.shape, dtype=np.uint8)
+    for i in range(flat.size):
+        out[i] = lib.hco_e4m3_from_double(float(flat[i]))
+    return out.reshape(v.shape)
+
+
+def e4m3_to_f64(codes) -> np.ndarray:
+    """Value of E4M3 bytes (field 0: m * 2^-9; else (1 + m/8) * 2^(e-7))."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = c & 0x7
+    mag = np.where(e == 0, m * 2.0 ** -9, (1.0 + m / 8.0) * np.exp2(e - 7.0))
+    return sign * mag
+
+
+def mxfp8(x):
+    """The MXFP8 cast of bf16 rows [rows, d] (d a multiple of 32) ->
+    (E4M3 codes [rows, d] uint8, UE8M0 scale bytes [rows, d/32] uint8)."""
+    x = bf16_bits(x)
+    rows, d = x.shape
+    xa, xp = _arr(x, np.uint16)
+    codes = np.empty((rows, d), dtype=np.uint8)
+    scales = np.empty((rows, d // 32), dtype=np.uint8)
+    _check(_load().hco_mxfp8(xp, rows, d, codes.ctypes.data_as(ctypes.c_void_p),
+                             scales.ctypes.data_as(ctypes.c_void_p)), "mxfp8")
+    return codes, scales
 
 
 def post(f, residual, post_, comb):

@@ -24,6 +24,11 @@
  *           FP32->BF16 to the nearest), "sigma", "2 sigma",
  *           "x + eps_hc", "First Sinkhorn Round", "Sinkhorn Round",
  *           "Mixing Coefficients", "Single-Pass mHC".
+ *  [MX]     DeepSeek V4.1 Flash diagram, block "Cast to MXFP8": groups of
+ *           32 channels of a row, the UE8M0 scale (the group's largest
+ *           magnitude, kept at or above 1e-4, over 448, rounded up to a power
+ *           of two), each channel over the scale, kept within [-448, 448],
+ *           written as the nearest E4M3 number.
  *  [RMS]    DeepSeek-R1 dossier, RMSNorm records (mean square over the last
  *           axis, multiply by 1/sqrt(mean + eps), then by the learned gain,
  *           then restore the input dtype). The V4.1 RMSNorm body itself is
@@ -314,4 +319,73 @@ int hco_block_step(const uint16_t *x, const double *pre_mix, const uint16_t *f,
     if (rc)
         return rc;
     return hco_post(f, x, post, comb, n, hc, d, y);
+}
+
+/* ------------------------------------------------------------------------ */
+/* [MX] E4M3 element: sign bit, 4 exponent bits with bias 7, 3 mantissa bits;
+ * exponent field 0 holds the subnormals m * 2^-9; the largest finite value is
+ * 1.75 * 2^8 = 448 (field 15, mantissa 6).  "Nearest" ties to even (the
+ * pages do not say; IEEE default).  |v| <= 448 (the cast clamps first). */
+uint8_t hco_e4m3_from_double(double v)
+{
+    uint8_t sign = signbit(v) ? 0x80u : 0u;
+    double a = fabs(v);
+    if (a == 0.0)
+        return sign;
+    int e;
+    frexp(a, &e);
+    int ex = e - 1; /* a in [2^ex, 2^(ex+1)) */
+    if (ex < -6)
+        ex = -6; /* subnormals share the spacing of the smallest normal binade */
+    double ulp = ldexp(1.0, ex - 3); /* 3 mantissa bits */
+    double r = round_half_even(a / ulp) * ulp;
+    if (r == 0.0)
+        return sign;
+    frexp(r, &e);
+    ex = e - 1;
+    if (ex < -6) /* subnormal: r = m * 2^-9, m in 1..7 */
+        return (uint8_t)(sign | (uint8_t)(r / ldexp(1.0, -9)));
+    int mant = (int)((r / ldexp(1.0, ex) - 1.0) * 8.0); /* exact */
+    return (uint8_t)(sign | (uint8_t)((ex + 7) << 3) | (uint8_t)mant);
+}
+
+/* [MX] The cast of bf16 rows, d a multiple of 32.  Per group of 32 channels:
+ * amax = the largest |x| (exact), kept at or above 1e-4; the scale is the
+ * smallest power of two at or above amax / 448, where 1e-4 and the division
+ * are fp32 (the reading taken: the scale is decided in the kernel's fp32);
+ * scales[g] = log2(scale) + 127 (UE8M0); codes[c] = E4M3 of x[c] / scale
+ * (exact in double), clamped to [-448, 448].
+ * in: [rows, d] bf16 bits; codes: [rows, d]; scales: [rows, d/32]. */
+int hco_mxfp8(const uint16_t *in, int64_t rows, int d, uint8_t *codes, uint8_t *scales)
+{
+    if (rows < 0 || d <= 0 || d % 32 != 0 || (rows > 0 && (!in || !codes || !scales)))
+        return HCO_EINVAL;
+    const int groups = d / 32;
+    for (int64_t t = 0; t < rows; ++t) {
+        for (int g = 0; g < groups; ++g) {
+            const uint16_t *xg = in + t * d + 32 * g;
+            float amax = 0.0f;
+            for (int i = 0; i < 32; ++i) {
+                float a = (float)fabs(hco_bf16_to_double(xg[i]));
+                if (a > amax)
+                    amax = a;
+            }
+            if (amax < 1e-4f)
+                amax = 1e-4f;
+            volatile float q = amax / 448.0f; /* fp32 division, correctly rounded */
+            int e;
+            float m = frexpf(q, &e); /* q = m * 2^e, m in [0.5, 1) */
+            int ex = (m == 0.5f) ? e - 1 : e; /* smallest power of two >= q is 2^ex */
+            scales[t * groups + g] = (uint8_t)(ex + 127);
+            for (int i = 0; i < 32; ++i) {
+                double v = ldexp(hco_bf16_to_double(xg[i]), -ex); /* exact */
+                if (v > 448.0)
+                    v = 448.0;
+                if (v < -448.0)
+                    v = -448.0;
+                codes[t * d + 32 * g + i] = hco_e4m3_from_double(v);
+            }
+        }
+    }
+    return HCO_OK;
 }

@@ -43,6 +43,13 @@ MUTANTS = {
     "round_ties_away": ("    return (fmod(r, 2.0) == 0.0) ? r : r + 1.0;", "    return r + 1.0;"),
     "round_truncate": ("    if (frac > 0.5)\n        return r + 1.0;", "    if (frac > 2.0)\n        return r + 1.0;"),
     "block_reads_with_own_pre": ("rc = hco_pre(x, pre_mix, n, hc, d, h);", "rc = hco_pre(x, pre, n, hc, d, h);"),
+    "mx_scale_rounded_down": ("int ex = (m == 0.5f) ? e - 1 : e;", "int ex = e - 1;"),
+    "mx_no_1e4_floor": ("            if (amax < 1e-4f)\n                amax = 1e-4f;\n", ""),
+    "mx_scale_bias": ("scales[t * groups + g] = (uint8_t)(ex + 127);", "scales[t * groups + g] = (uint8_t)(ex + 128);"),
+    "e4m3_two_mantissa_bits": ("double ulp = ldexp(1.0, ex - 3); /* 3 mantissa bits */",
+                               "double ulp = ldexp(1.0, ex - 2); /* 3 mantissa bits */"),
+    "e4m3_subnormal_threshold": ("    if (ex < -6)\n        ex = -6; /* subnormals share",
+                                 "    if (ex < -7)\n        ex = -7; /* subnormals share"),
 }
 
 # the pin tests run against each mutant (all take no fixtures except golden_constants)

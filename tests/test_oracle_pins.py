@@ -442,3 +442,127 @@ def test_param_counts_match_pages(golden_constants):
     hc = g["hc_mult"]
     assert hc * hc + 1 == g["comb_params_per_instance"]
     assert (2 + hc) * hc == g["comb_in_out_shapes"]["in_mix_numbers"]
+
+
+# ---------------------------------------------------------------- MXFP8 cast
+# DeepSeek V4.1 Flash diagram, block "Cast to MXFP8": groups of 32 channels,
+# UE8M0 scale = the group's largest magnitude (at least 1e-4) over 448 rounded
+# up to a power of two, E4M3 elements of x / scale kept within [-448, 448].
+
+def _torch_e4m3_bits(v32):
+    t = torch.from_numpy(np.asarray(v32, dtype=np.float32)).to(torch.float8_e4m3fn)
+    return t.view(torch.uint8).numpy()
+
+
+def _all_e4m3_values():
+    codes = np.arange(0, 0x7F, dtype=np.uint8)   # 0x7F is NaN
+    return torch.from_numpy(codes).view(torch.float8_e4m3fn).float().numpy().astype(np.float64)
+
+
+def test_e4m3_round_matches_torch():
+    # torch's fp32 -> float8_e4m3fn conversion rounds to nearest, ties to even:
+    # a library reference.  Values: log-uniform magnitudes across the normal and
+    # subnormal range, every representable value, and every midpoint (ties).
+    mags = np.exp2(RNG.uniform(-12.0, math.log2(448.0), 6000))
+    vals = _all_e4m3_values()
+    mids = (vals[1:] + vals[:-1]) / 2.0
+    v = np.concatenate([mags, -mags, vals, -vals, mids, -mids, [448.0, -448.0, 0.0, -0.0]])
+    v = v.astype(np.float32).astype(np.float64)     # fp32 inputs, as the cast sees them
+    assert np.array_equal(oracle.e4m3_from_f64(v), _torch_e4m3_bits(v))
+
+
+@pytest.mark.parametrize("value, code", [
+    (448.0, 0x7E), (-448.0, 0xFE), (1.0, 0x38), (2.0 ** -6, 0x08), (2.0 ** -9, 0x01),
+    (0.75 * 2.0 ** -9, 0x01), (0.5 * 2.0 ** -9, 0x00), (1.5 * 2.0 ** -9, 0x02),
+    (2.5 * 2.0 ** -9, 0x02), (1.0625, 0x38), (1.1875, 0x3A), (-0.0, 0x80), (240.0, 0x77),
+])
+def test_e4m3_hand_values(value, code):
+    # field 0: m * 2^-9; field e > 0: (1 + m/8) * 2^(e-7); ties go to the even mantissa
+    assert int(oracle.e4m3_from_f64(np.array([value]))[0]) == code
+
+
+def _bits(v):
+    return _torch_bf16_bits_from_f32(np.asarray(v, dtype=np.float32)).reshape(1, -1)
+
+
+def test_mxfp8_scale_closed_forms():
+    g = np.zeros(32)
+    g[5] = 448.0          # 448 / 448 = 1 = 2^0
+    codes, sc = oracle.mxfp8(_bits(g))
+    assert sc[0, 0] == 127 and codes[0, 5] == 0x7E and not codes[0, np.arange(32) != 5].any()
+    g[5] = 449.0 - 1.0    # 448 again (bf16 of 448 exactly)
+    g[7] = -452.0         # 452/448 > 1 -> 2^1; -452/2 = -226 -> nearest E4M3 -224
+    codes, sc = oracle.mxfp8(_bits(g))
+    assert sc[0, 0] == 128 and codes[0, 7] == 0xF6 and codes[0, 5] == 0x76  # 448/2 = 224 = 1.75 * 2^7
+    g = np.zeros(32)
+    g[0] = 224.0          # 224/448 = 0.5 exactly -> 2^-1, and 224 / 0.5 = 448
+    codes, sc = oracle.mxfp8(_bits(g))
+    assert sc[0, 0] == 126 and codes[0, 0] == 0x7E
+    # all zeros: the largest magnitude is kept at 1e-4; fp32(1e-4)/448 = 2.23e-7
+    # lies in (2^-23, 2^-22], so the scale is 2^-22 (byte 105); -0 keeps its sign
+    z = np.zeros(32)
+    z[3] = -0.0
+    codes, sc = oracle.mxfp8(_bits(z))
+    assert sc[0, 0] == 127 - 22 and codes[0, 3] == 0x80 and not (codes[0] & 0x7F).any()
+    # a tiny group is scaled by the same 2^-22: 1e-5 * 2^22 = 41.9 -> E4M3 40 (0x64)
+    t = np.zeros(32)
+    t[1] = 1e-5
+    codes, sc = oracle.mxfp8(_bits(t))
+    assert sc[0, 0] == 105 and codes[0, 1] == _torch_e4m3_bits(
+        [float(inputs_bf16_value(1e-5)) * 2.0 ** 22])[0]
+
+
+def inputs_bf16_value(v):
+    return oracle.bf16_to_f64(_torch_bf16_bits_from_f32(np.array([v], np.float32)))[0]
+
+
+def _decode(codes, scales):
+    vals = torch.from_numpy(np.ascontiguousarray(codes)).view(torch.float8_e4m3fn).float().numpy()
+    return vals.astype(np.float64) * np.exp2(np.repeat(scales.astype(np.float64) - 127.0, 32, axis=1))
+
+
+def test_mxfp8_round_trip_bound_and_minimal_scale():
+    g = torch.Generator().manual_seed(7)
+    x = inputs.streams(g, 24, 1, 256, outlier_p=0.02).reshape(24, 256)
+    x[3, :32] = 0                                              # an all-zero group
+    x[4, 32:64] *= 1e-6                                        # a group below the 1e-4 floor
+    bits = oracle.bf16_bits(x)
+    codes, scales = oracle.mxfp8(bits)
+    xv = oracle.bf16_to_f64(bits)
+    back = _decode(codes, scales)
+    scale = np.exp2(np.repeat(scales.astype(np.float64) - 127.0, 32, axis=1))
+    q = np.abs(xv) / scale
+    # half an E4M3 step at q's binade (normal: 2^(e-3); subnormal: 2^-9), scaled back
+    e = np.floor(np.log2(np.maximum(q, 2.0 ** -6)))
+    half_step = np.exp2(e - 4.0) * scale
+    assert np.all(np.abs(back - xv) <= half_step * (1 + 1e-12))
+    # the scale is the smallest power of two with every |x| / scale <= 448
+    amax = np.maximum(np.abs(xv).reshape(24, -1, 32).max(-1), np.float32(1e-4))
+    s = np.exp2(scales.astype(np.float64) - 127.0)
+    assert np.all(amax / s <= 448.0) and np.all(amax / (s / 2) > 448.0 * (1 - 2.0 ** -23))
+
+
+def test_mxfp8_power_of_two_invariance():
+    # scaling a row by 2^k leaves every code unchanged and moves every scale by k
+    # (groups well above the 1e-4 floor)
+    g = torch.Generator().manual_seed(9)
+    x = inputs.streams(g, 8, 1, 128).reshape(8, 128)
+    c0, s0 = oracle.mxfp8(oracle.bf16_bits(x))
+    for k in (-5, -1, 3, 7):
+        ck, sk = oracle.mxfp8(oracle.bf16_bits(x * 2.0 ** k))
+        assert np.array_equal(ck, c0) and np.array_equal(sk.astype(int), s0.astype(int) + k)
+
+
+def test_mxfp8_every_e4m3_value_round_trips():
+    # a group holding exactly v * 2^ex for every representable v reproduces v's code
+    vals = _all_e4m3_values()
+    codes_all = np.arange(0, 0x7F, dtype=np.uint8)
+    for ex in (-3, 0, 5):
+        for start in range(0, len(vals), 31):
+            v = vals[start:start + 31]
+            grp = np.zeros(32)
+            grp[:len(v)] = v * 2.0 ** ex
+            grp[31] = 448.0 * 2.0 ** ex                 # pins the scale to 2^ex
+            codes, sc = oracle.mxfp8(_bits(grp))
+            assert sc[0, 0] == 127 + ex
+            assert np.array_equal(codes[0, :len(v)], codes_all[start:start + 31])
