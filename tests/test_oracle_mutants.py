@@ -22,7 +22,7 @@ MUTANTS = {
     "rsqrt_divides": ("mixes[t * mix + i] = acc * r;", "mixes[t * mix + i] = acc / r;"),
     "pre_no_eps": ("sigmoid(m[j] * s0 + (double)hc_base[j]) + eps;", "sigmoid(m[j] * s0 + (double)hc_base[j]);"),
     "post_not_doubled": ("post[t * hc + j] = 2.0 * sigmoid", "post[t * hc + j] = sigmoid"),
-    "post_wrong_scale": ("m[hc + j] * s1", "m[hc + j] * s0"),
+    "post_wrong_scale": ("2.0 * sigmoid(m[hc + j] * s1", "2.0 * sigmoid(m[hc + j] * s0"),
     "comb_transposed_read": ("int i = 2 * hc + j * hc + k;", "int i = 2 * hc + k * hc + j;"),
     "softmax_eps_inside": ("c[j * hc + k] = c[j * hc + k] / s + eps;", "c[j * hc + k] = c[j * hc + k] / (s + eps);"),
     "softmax_no_max_shift_sign": ("exp(c[j * hc + k] - mx)", "exp(mx - c[j * hc + k])"),
@@ -105,7 +105,7 @@ def tmpdir_mut():
 def test_mutant_is_caught(name, tmpdir_mut):
     src = open(SRC).read()
     old, new = MUTANTS[name]
-    assert src.count(old) >= 1, "mutation anchor for %s not found in the oracle source" % name
+    assert src.count(old) == 1, "mutation anchor for %s must occur exactly once in the oracle" % name
     mutated = src.replace(old, new, 1)
     c_path = os.path.join(tmpdir_mut, name + ".c")
     so_path = os.path.join(tmpdir_mut, name + ".so")
@@ -117,7 +117,8 @@ def test_mutant_is_caught(name, tmpdir_mut):
     try:
         lib = ctypes.CDLL(so_path)
         for attr in ("hco_bf16_to_double", "hco_bf16_from_double", "hco_mixes", "hco_split_sinkhorn",
-                     "hco_pre", "hco_rmsnorm", "hco_post", "hco_block_step"):
+                     "hco_pre", "hco_rmsnorm", "hco_post", "hco_block_step", "hco_e4m3_from_double",
+                     "hco_mxfp8"):
             f, g = getattr(lib, attr), getattr(real, attr)
             f.argtypes, f.restype = g.argtypes, g.restype
         oracle._lib = lib

@@ -219,9 +219,13 @@ def test_sinkhorn_2x2_limit_closed_form():
     # eps = 0: scaling preserves the cross ratio P00 P11 / (P01 P10) = exp(delta),
     # delta = c00 + c11 - c01 - c10; the doubly stochastic 2x2 limit is
     # [[p, 1-p], [1-p, p]] with p / (1 - p) = exp(delta / 2).
+    # The limit is reached within the 400 rounds only for moderate logits (std 1:
+    # worst error 2e-16 over 300 draws; std 2 leaves up to 1e-4), and the pin uses
+    # its own stream so that it does not depend on which tests ran before it.
     hc = 2
+    rng = np.random.default_rng(218)
     for _ in range(10):
-        m = RNG.standard_normal((1, 8)) * 2.0
+        m = rng.standard_normal((1, 8)) * 1.0
         _, _, comb = oracle.split_sinkhorn(m, np.ones(3, np.float32), np.zeros(8, np.float32),
                                            hc=hc, iters=400, eps=0.0)
         c = m[0, 4:].reshape(2, 2)
@@ -463,7 +467,8 @@ def test_e4m3_round_matches_torch():
     # torch's fp32 -> float8_e4m3fn conversion rounds to nearest, ties to even:
     # a library reference.  Values: log-uniform magnitudes across the normal and
     # subnormal range, every representable value, and every midpoint (ties).
-    mags = np.exp2(RNG.uniform(-12.0, math.log2(448.0), 6000))
+    rng = np.random.default_rng(4321)   # its own stream: the shared one feeds other pins
+    mags = np.exp2(rng.uniform(-12.0, math.log2(448.0), 6000))
     vals = _all_e4m3_values()
     mids = (vals[1:] + vals[:-1]) / 2.0
     v = np.concatenate([mags, -mags, vals, -vals, mids, -mids, [448.0, -448.0, 0.0, -0.0]])
