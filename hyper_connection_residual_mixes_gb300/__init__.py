@@ -20,7 +20,8 @@ from . import _lib
 from ._lib import HcError
 
 __all__ = ["hc_mixes", "hc_split_sinkhorn", "hc_pre_norm", "hc_post", "hc_block_step",
-           "hc_chain_begin", "hc_chain_side", "STATE_FLOATS", "HcError", "library_path", "version"]
+           "hc_chain_begin", "hc_chain_side", "hc_mxfp8_cast", "hc_pre_norm_mxfp8", "STATE_FLOATS",
+           "HcError", "library_path", "version"]
 
 HC_EPS = 1e-6
 NORM_EPS = 1e-20
@@ -129,6 +130,46 @@ def hc_pre_norm(x, pre_mix, norm_w, norm_eps=NORM_EPS, out=None, stream=None):
         _lib.call("hc_pre_norm", _ptr(x), _ptr(pre_mix), _ptr(norm_w), n, hc, d, norm_eps,
                   _ptr(out), _stream(stream))
     return out
+
+
+def hc_mxfp8_cast(x, codes=None, scales=None, stream=None):
+    """The MXFP8 cast of bf16 rows x [..., d] (d a multiple of 32) ->
+    (E4M3 codes [..., d] uint8, UE8M0 scale bytes [..., d/32] uint8)."""
+    _check(x, "x", torch.bfloat16)
+    dev = x.device
+    d = x.shape[-1]
+    lead = tuple(x.shape[:-1])
+    rows = x.numel() // d if x.numel() else 0
+    codes = _out(codes, "codes", lead + (d,), torch.uint8, dev)
+    scales = _out(scales, "scales", lead + (d // 32,), torch.uint8, dev)
+    with torch.cuda.device(dev):
+        _lib.call("hc_mxfp8_cast", _ptr(x), rows, d, _ptr(codes), _ptr(scales), _stream(stream))
+    return codes, scales
+
+
+def hc_pre_norm_mxfp8(x, pre_mix, norm_w, norm_eps=NORM_EPS, h_norm=None, codes=None, scales=None,
+                      return_h_norm=False, stream=None):
+    """a4-a5 then the MXFP8 cast of h_norm in one pass: x [..., hc, d] bf16,
+    pre_mix [..., hc] -> (codes [..., d] uint8, scales [..., d/32] uint8)
+    [+ h_norm [..., d] bf16 when return_h_norm or h_norm is given]."""
+    _check(x, "x", torch.bfloat16)
+    dev = x.device
+    hc, d = x.shape[-2], x.shape[-1]
+    lead = tuple(x.shape[:-2])
+    n = x.numel() // (hc * d) if x.numel() else 0
+    _check(pre_mix, "pre_mix", torch.float32, dev)
+    _check(norm_w, "norm_w", torch.float32, dev)
+    if return_h_norm or h_norm is not None:
+        h_norm = _out(h_norm, "h_norm", lead + (d,), torch.bfloat16, dev)
+    codes = _out(codes, "codes", lead + (d,), torch.uint8, dev)
+    scales = _out(scales, "scales", lead + (d // 32,), torch.uint8, dev)
+    with torch.cuda.device(dev):
+        _lib.call("hc_pre_norm_mxfp8", _ptr(x), _ptr(pre_mix), _ptr(norm_w), n, hc, d, norm_eps,
+                  _ptr(h_norm) if h_norm is not None else None, _ptr(codes), _ptr(scales),
+                  _stream(stream))
+    if h_norm is not None:
+        return codes, scales, h_norm
+    return codes, scales
 
 
 def hc_post(f, residual, post, comb, y=None, stream=None):

@@ -31,6 +31,8 @@ SIGNATURES = {
     "hc_mixes": [P, P, P, P, I64, I32, I32, I32, F32, F32, P, P, P, P, P],
     "hc_split_sinkhorn": [P, P, P, I64, I32, I32, F32, P, P, P, P],
     "hc_pre_norm": [P, P, P, I64, I32, I32, F32, P, P],
+    "hc_mxfp8_cast": [P, I64, I32, P, P, P],
+    "hc_pre_norm_mxfp8": [P, P, P, I64, I32, I32, F32, P, P, P, P],
     "hc_post": [P, P, P, P, I64, I32, I32, P, P],
     "hc_block_step": [P, P, P, P, P, P, P, I64, I32, I32, I32, F32, F32, P, P, P, P, P, P],
     "hc_chain_begin": [P, P, P, P, P, I64, I32, I32, I32, F32, F32, P, P, P],

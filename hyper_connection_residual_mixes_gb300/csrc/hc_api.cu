@@ -161,6 +161,41 @@ hc_status hc_pre_norm(const uint16_t *x, const float *pre_mix, const float *norm
     return cuda_status(hc::launch_pre_norm(x, pre_mix, norm_w, n, d, norm_eps, out, stream));
 }
 
+hc_status hc_mxfp8_cast(const uint16_t *in, int64_t rows, int d, uint8_t *codes, uint8_t *scales,
+                        cudaStream_t stream) {
+    if (rows < 0 || d <= 0) return HC_ERR_INVALID_ARG;
+    if (d % 32 != 0) return HC_ERR_UNSUPPORTED;
+    if (rows > (INT64_MAX / 8) / d) return HC_ERR_INVALID_ARG;
+    if (rows == 0) return HC_OK;
+    if (!in || !codes || !scales) return HC_ERR_INVALID_ARG;
+    if (!aligned16(in) || !aligned16(codes)) return HC_ERR_MISALIGNED;
+    const Span ins[] = {span(in, rows * d * 2)};
+    const Span outs[] = {span(codes, rows * d), span(scales, rows * (d / 32))};
+    hc_status st = check_alias(outs, 2, ins, 1);
+    if (st != HC_OK) return st;
+    return cuda_status(hc::launch_mxfp8_cast(in, rows, d, codes, scales, stream));
+}
+
+hc_status hc_pre_norm_mxfp8(const uint16_t *x, const float *pre_mix, const float *norm_w, int64_t n,
+                            int hc, int d, float norm_eps, uint16_t *h_norm_out, uint8_t *codes,
+                            uint8_t *scales, cudaStream_t stream) {
+    hc_status st = check_shape(n, hc, d, true);
+    if (st != HC_OK) return st;
+    if (!finite_nonneg(norm_eps)) return HC_ERR_INVALID_ARG;
+    if (n == 0) return HC_OK;
+    if (!x || !pre_mix || !norm_w || !codes || !scales) return HC_ERR_INVALID_ARG;
+    const void *ptrs[] = {x, pre_mix, norm_w, codes};
+    for (const void *p : ptrs)
+        if (!aligned16(p)) return HC_ERR_MISALIGNED;
+    if (h_norm_out && !aligned16(h_norm_out)) return HC_ERR_MISALIGNED;
+    const Span ins[] = {span(x, n * hc * d * 2), span(pre_mix, n * hc * 4), span(norm_w, d * 4)};
+    const Span outs[] = {span(codes, n * d), span(scales, n * (d / 32)),
+                         span(h_norm_out, h_norm_out ? n * d * 2 : 0)};
+    if ((st = check_alias(outs, 3, ins, 3)) != HC_OK) return st;
+    return cuda_status(hc::launch_pre_norm_mxfp8(x, pre_mix, norm_w, n, d, norm_eps, h_norm_out,
+                                                 codes, scales, stream));
+}
+
 hc_status hc_post(const uint16_t *f, const uint16_t *residual, const float *post,
                   const float *comb, int64_t n, int hc, int d, uint16_t *y,
                   cudaStream_t stream) {

@@ -7,6 +7,8 @@
 //                    pre_mix, round to bf16, RMSNorm with gain (Block page,
 //                    Block.hc_pre + attn_norm).
 //  k_post            a6, one CTA per token (Block page, Block.hc_post).
+//  k_mxfp8_cast      the MXFP8 cast of bf16 rows (Flash diagram, Cast to MXFP8).
+//  k_pre_norm_mxfp8  a4-a5 with the cast in its epilogue.
 //  k_tokens_simple   a1-a3 and optionally a4-a6 for TOK whole tokens per CTA
 //                    (Block page, Block.hc_mixes and Block.forward).
 //
@@ -118,6 +120,146 @@ cudaError_t launch_pre_norm(const uint16_t *x, const float *pre_mix, const float
                                          (int)smem);
     if (e != cudaSuccess) return e;
     k_pre_norm<<<(unsigned)n, kRowThreads, smem, s>>>(x, pre_mix, norm_w, d, norm_eps, out);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ MXFP8 cast
+// DeepSeek V4.1 Flash diagram, block "Cast to MXFP8".  The channels of a row
+// are cut into groups of 32.  A group's scale is the smallest power of two at
+// or above max(amax, 1e-4) / 448 (the division in fp32, correctly rounded),
+// written as its biased exponent (UE8M0); every channel is written as the
+// E4M3 number nearest to x / scale (ties to even) after clamping to
+// [-448, 448].  Each thread holds one 8-channel chunk, so a group is four
+// consecutive lanes; every loop below runs the same number of times in all
+// lanes of a warp, so the group shuffles always see a full warp.
+__device__ __forceinline__ int mx_scale_exp(float amax) {
+    const float q = __fdiv_rn(fmaxf(amax, 1e-4f), 448.0f);  // a normal float here
+    const uint32_t b = __float_as_uint(q);
+    // ceil(log2(q)): the exponent, plus one unless q is a power of two
+    return (int)((b >> 23) & 0xffu) - 127 + ((b & 0x7fffffu) ? 1 : 0);
+}
+// two fp32 values -> two E4M3 bytes (lo in the low byte), nearest even, saturating
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+// eight channels (exact bf16 values) of a group with scale 2^ex -> eight bytes
+__device__ __forceinline__ uint2 mx_codes8(const float (&v)[8], int ex) {
+    const float inv = __uint_as_float((uint32_t)(127 - ex) << 23);  // 2^-ex, exact
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        w[i] = e4m3x2(fminf(fmaxf(v[2 * i] * inv, -448.0f), 448.0f),
+                      fminf(fmaxf(v[2 * i + 1] * inv, -448.0f), 448.0f));
+    return make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16));
+}
+// the largest magnitude of the group (four lanes), then its scale exponent
+__device__ __forceinline__ int mx_group_exp(const float (&v)[8]) {
+    float am = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) am = fmaxf(am, fabsf(v[i]));
+    am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
+    am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
+    return mx_scale_exp(am);
+}
+
+constexpr int kCastThreads = 256;
+
+// bf16 rows -> E4M3 codes + UE8M0 scale bytes; chunks = rows * d / 8 (a multiple of 4)
+__global__ void __launch_bounds__(kCastThreads)
+k_mxfp8_cast(const uint16_t *__restrict__ in, int64_t chunks, uint8_t *__restrict__ codes,
+             uint8_t *__restrict__ scales) {
+    const uint4 *in8 = reinterpret_cast<const uint4 *>(in);
+    uint2 *out8 = reinterpret_cast<uint2 *>(codes);
+    for (int64_t base = (int64_t)blockIdx.x * kCastThreads; base < chunks;
+         base += (int64_t)gridDim.x * kCastThreads) {
+        const int64_t c = base + threadIdx.x;
+        const bool live = c < chunks;
+        float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        if (live) unpack8(__ldg(in8 + c), v);
+        const int ex = mx_group_exp(v);
+        if (live) {
+            out8[c] = mx_codes8(v, ex);
+            if ((c & 3) == 0) scales[c >> 2] = (uint8_t)(ex + 127);
+        }
+    }
+}
+
+cudaError_t launch_mxfp8_cast(const uint16_t *in, int64_t rows, int d, uint8_t *codes,
+                              uint8_t *scales, cudaStream_t s) {
+    const int64_t chunks = rows * (int64_t)(d / 8);
+    int64_t blocks = (chunks + kCastThreads - 1) / kCastThreads;
+    if (blocks > 152 * 16) blocks = 152 * 16;  // grid-stride beyond 16 CTAs per SM
+    k_mxfp8_cast<<<(unsigned)blocks, kCastThreads, 0, s>>>(in, chunks, codes, scales);
+    return cudaGetLastError();
+}
+
+// a4-a5 and the cast in one pass: h_norm as k_pre_norm computes it, then its
+// MXFP8 codes and scales; the bf16 h_norm is written too when out is given.
+__global__ void __launch_bounds__(kRowThreads)
+k_pre_norm_mxfp8(const uint16_t *__restrict__ x, const float *__restrict__ pre_mix,
+                 const float *__restrict__ norm_w, int d, float norm_eps,
+                 uint16_t *__restrict__ out, uint8_t *__restrict__ codes,
+                 uint8_t *__restrict__ scales) {
+    extern __shared__ uint4 hbuf[];  // d/8 chunks of 8 bf16
+    __shared__ float red[kRowThreads / 32];
+    const int64_t t = blockIdx.x;
+    const int d8 = d >> 3;
+    const uint4 *xs = reinterpret_cast<const uint4 *>(x + t * kHC * d);
+    const float p0 = __ldg(pre_mix + t * kHC), p1 = __ldg(pre_mix + t * kHC + 1),
+                p2 = __ldg(pre_mix + t * kHC + 2), p3 = __ldg(pre_mix + t * kHC + 3);
+    float ss = 0.0f;
+    for (int c = threadIdx.x; c < d8; c += kRowThreads) {
+        float a[8], b[8], e[8], g[8], h[8];
+        unpack8(__ldg(xs + c), a);
+        unpack8(__ldg(xs + d8 + c), b);
+        unpack8(__ldg(xs + 2 * d8 + c), e);
+        unpack8(__ldg(xs + 3 * d8 + c), g);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) h[i] = fmaf(p3, g[i], fmaf(p2, e[i], fmaf(p1, b[i], p0 * a[i])));
+        const uint4 hb = pack8(h);
+        hbuf[c] = hb;
+        float r[8];
+        unpack8(hb, r);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) ss = fmaf(r[i], r[i], ss);
+    }
+    const float tot = block_sum<kRowThreads>(ss, red);
+    const float rs = rsqrtf(tot / (float)d + norm_eps);
+    const float4 *w4 = reinterpret_cast<const float4 *>(norm_w);
+    for (int base = 0; base < d8; base += kRowThreads) {
+        const int c = base + threadIdx.x;
+        const bool live = c < d8;
+        float h[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        if (live) {
+            unpack8(hbuf[c], h);
+            const float4 wa = __ldg(w4 + 2 * c), wb = __ldg(w4 + 2 * c + 1);
+            const float wv[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) h[i] = (h[i] * rs) * wv[i];
+        }
+        const uint4 hb = pack8(h);  // h_norm, rounded to bf16
+        float hn[8];
+        unpack8(hb, hn);
+        const int ex = mx_group_exp(hn);
+        if (live) {
+            if (out) reinterpret_cast<uint4 *>(out + t * d)[c] = hb;
+            reinterpret_cast<uint2 *>(codes + t * d)[c] = mx_codes8(hn, ex);
+            if ((c & 3) == 0) scales[t * (d >> 5) + (c >> 2)] = (uint8_t)(ex + 127);
+        }
+    }
+}
+
+cudaError_t launch_pre_norm_mxfp8(const uint16_t *x, const float *pre_mix, const float *norm_w,
+                                  int64_t n, int d, float norm_eps, uint16_t *out, uint8_t *codes,
+                                  uint8_t *scales, cudaStream_t s) {
+    const size_t smem = (size_t)d * 2;
+    cudaError_t e = cudaFuncSetAttribute(k_pre_norm_mxfp8,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    k_pre_norm_mxfp8<<<(unsigned)n, kRowThreads, smem, s>>>(x, pre_mix, norm_w, d, norm_eps, out,
+                                                            codes, scales);
     return cudaGetLastError();
 }
 

@@ -15,6 +15,11 @@ cudaError_t launch_split_sinkhorn(const float *mixes, const float *hc_scale, con
 cudaError_t launch_pre_norm(const uint16_t *x, const float *pre_mix, const float *norm_w,
                             int64_t n, int d, float norm_eps, uint16_t *out, cudaStream_t s);
 
+cudaError_t launch_mxfp8_cast(const uint16_t *in, int64_t rows, int d, uint8_t *codes,
+                              uint8_t *scales, cudaStream_t s);
+cudaError_t launch_pre_norm_mxfp8(const uint16_t *x, const float *pre_mix, const float *norm_w,
+                                  int64_t n, int d, float norm_eps, uint16_t *out, uint8_t *codes,
+                                  uint8_t *scales, cudaStream_t s);
 cudaError_t launch_post(const uint16_t *f, const uint16_t *residual, const float *post,
                         const float *comb, int64_t n, int d, uint16_t *y, cudaStream_t s);
 

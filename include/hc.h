@@ -153,6 +153,38 @@ hc_status hc_block_step(const uint16_t *x, const float *pre_mix, const uint16_t 
                         cudaStream_t stream);
 
 /*
+ * The MXFP8 cast (DeepSeek V4.1 Flash diagram, block "Cast to MXFP8"): the
+ * rounding the released code runs in front of every FP8/FP4-weight
+ * projection, here for the sublayer input h_norm.  The channels of a row are
+ * cut into groups of 32.  Per group, scale = the smallest power of two at or
+ * above max(amax, 1e-4) / 448, amax the largest |x| of the group, the
+ * division in fp32 (correctly rounded); every channel is written as the E4M3
+ * number (1 sign, 4 exponent bits with bias 7, 3 mantissa bits; no infinity)
+ * nearest to x / scale, ties to even, after clamping x / scale to
+ * [-448, 448].  The value a code stands for is its E4M3 value times the
+ * group's scale.  NaN or infinite inputs are outside the cast's definition.
+ *
+ * hc_mxfp8_cast: bf16 rows of any origin.
+ *   in [rows, d] bf16, d a multiple of 32 (else HC_ERR_UNSUPPORTED)     in
+ *   codes [rows, d] uint8: the E4M3 byte of every channel             out
+ *   scales [rows, d/32] uint8: log2(scale) + 127 per group (UE8M0)     out
+ *   in and codes 16-byte aligned; scales byte-aligned.
+ *
+ * hc_pre_norm_mxfp8: a4 + a5 as hc_pre_norm computes them, then the cast of
+ * the bf16 h_norm in the same pass (nothing written to HBM in between).
+ *   x, pre_mix, norm_w as hc_pre_norm                                  in
+ *   h_norm_out [n, d] bf16, optional (NULL: not written); when given it
+ *   equals hc_pre_norm's output bit for bit                            out
+ *   codes [n, d], scales [n, d/32] as for hc_mxfp8_cast of h_norm      out
+ */
+hc_status hc_mxfp8_cast(const uint16_t *in, int64_t rows, int d, uint8_t *codes, uint8_t *scales,
+                        cudaStream_t stream);
+
+hc_status hc_pre_norm_mxfp8(const uint16_t *x, const float *pre_mix, const float *norm_w, int64_t n,
+                            int hc, int d, float norm_eps, uint16_t *h_norm_out, uint8_t *codes,
+                            uint8_t *scales, cudaStream_t stream);
+
+/*
  * A chain of fused side steps, fused across sides (the Block page's
  * Block.forward: the streams a side reads are the y the previous side wrote,
  * and each side reads its sublayer input with the previous side's pre).  The

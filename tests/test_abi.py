@@ -185,3 +185,57 @@ def test_binding_rejects_cpu_tensors():
     x = torch.zeros(2, 4, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError, match="CUDA"):
         hcg.hc_pre_norm(x, torch.zeros(2, 4), torch.ones(64))
+
+
+def _cast(**kw):
+    a = dict(x=FAKE, rows=16, d=5120, codes=FAKE2 * 0x100, scales=FAKE2 * 0x200, stream=None)
+    a.update(kw)
+    return _lib.raw("hc_mxfp8_cast", a["x"], a["rows"], a["d"], a["codes"], a["scales"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(d=48), 2),                        # groups of 32 channels
+    (dict(d=0), 1),
+    (dict(rows=-1), 1),
+    (dict(codes=None), 1),
+    (dict(scales=None), 1),
+    (dict(x=FAKE + 2), 3),
+    (dict(codes=FAKE2 * 0x100 + 8), 3),
+    (dict(codes=FAKE + 0x100), 4),          # codes overlap the input
+    (dict(scales=FAKE2 * 0x100 + 0x40), 4),  # scales overlap the codes
+])
+def test_mxfp8_cast_validation(lib, kw, expect):
+    assert _cast(**kw) == expect
+
+
+def test_mxfp8_cast_empty_and_unaligned_scales_ok(lib):
+    assert _cast(rows=0) == 0
+    assert _cast(rows=0, scales=FAKE2 * 0x200 + 1) == 0
+
+
+def _pnq(**kw):
+    a = dict(x=FAKE, pre_mix=FAKE + 0x100000, norm_w=FAKE + 0x200000, n=16, hc=4, d=5120,
+             norm_eps=1e-20, h_norm=None, codes=FAKE2 * 0x100, scales=FAKE2 * 0x200, stream=None)
+    a.update(kw)
+    return _lib.raw("hc_pre_norm_mxfp8", a["x"], a["pre_mix"], a["norm_w"], a["n"], a["hc"], a["d"],
+                    a["norm_eps"], a["h_norm"], a["codes"], a["scales"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(hc=3), 2),
+    (dict(d=96), 2),
+    (dict(norm_eps=-1.0), 1),
+    (dict(codes=None), 1),
+    (dict(scales=None), 1),
+    (dict(h_norm=FAKE2 * 0x300 + 4), 3),
+    (dict(codes=FAKE + 0x80), 4),            # codes overlap x
+    (dict(h_norm=FAKE2 * 0x100), 4),         # h_norm overlaps the codes
+    (dict(n=-1), 1),
+])
+def test_pre_norm_mxfp8_validation(lib, kw, expect):
+    assert _pnq(**kw) == expect
+
+
+def test_pre_norm_mxfp8_empty_is_ok(lib):
+    assert _pnq(n=0) == 0
+    assert _pnq(n=0, h_norm=FAKE2 * 0x300) == 0
