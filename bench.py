@@ -579,6 +579,75 @@ def run_reference(args, rank, world):
     }
 
 
+def run_op(args, local_rank):
+    """One kernel of the widened rows, timed alone at the long-prefill size
+    (65,536 tokens x d = 5120): the MXFP8 cast of the bf16 h_norm
+    (hc_mxfp8_cast) or RMSNorm(hc_pre) with the cast in its epilogue
+    (hc_pre_norm_mxfp8).  One step is one launch over the whole batch; the
+    inputs are larger than L2.  The oracle is timed beside it on a sample."""
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    hcg._lib.load()
+    case = inputs.long_prefill(device=dev, materialize_f=False)
+    n, d = case.n, case.d
+    p = case.params[0]
+    codes = torch.empty((n, d), dtype=torch.uint8, device=dev)
+    scales = torch.empty((n, d // 32), dtype=torch.uint8, device=dev)
+    h = hcg.hc_pre_norm(case.x, case.pre_mix, p.norm_w)
+    if args.op == "mxfp8_cast":
+        fn = lambda: hcg.hc_mxfp8_cast(h, codes, scales)
+        alg = n * d * 2 + n * d + n * d // 32
+        what = "MXFP8 cast of bf16 rows (hc_mxfp8_cast)"
+    else:
+        fn = lambda: hcg.hc_pre_norm_mxfp8(case.x, case.pre_mix, p.norm_w, codes=codes, scales=scales)
+        alg = n * HC * d * 2 + n * HC * 4 + d * 4 + n * d + n * d // 32
+        what = "RMSNorm(hc_pre) cast to MXFP8 in one pass (hc_pre_norm_mxfp8)"
+    for _ in range(args.warmup):
+        fn()
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    stream = torch.cuda.current_stream(dev)
+    for a, b in evs:
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    peak, peak_kind = measured_peaks()
+    out = {"metric": "tokens/s through %s, 65,536 tokens x d = 5120" % what, "value": n / (ms / 1e3),
+           "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+           "dtype": "bf16 in, fp32 arithmetic, e4m3 + ue8m0 out", "data": "synthetic, seeded",
+           "config": {"workload": "long_prefill, one side's h_norm", "op": args.op, "tokens": n, "d": d,
+                      "l2": "inputs larger than L2; no flush"},
+           "roofline": {"bound": "hbm", "achieved": alg / (ms / 1e3) / 1e9, "peak": peak, "unit": "GB/s",
+                        "frac": alg / (ms / 1e3) / 1e9 / peak, "traffic": None,
+                        "peak_source": peak_kind, "algorithmic_bytes_per_launch": alg},
+           "clocks": clk, "gpu_launches": args.steps, "e2e": None}
+    if not args.no_cpu_baseline:
+        import oracle
+        rows = torch.arange(0, n, n // 64, device=dev)
+        hs = oracle.bf16_bits(h.index_select(0, rows).cpu())
+        xs = oracle.bf16_bits(case.x.index_select(0, rows).cpu())
+        pms = case.pre_mix.index_select(0, rows).cpu().numpy().astype(np.float64)
+        w = p.norm_w.cpu().numpy()
+        oracle.mxfp8(hs[:1])
+        t0 = time.perf_counter()
+        if args.op == "mxfp8_cast":
+            oracle.mxfp8(hs)
+        else:
+            oracle.mxfp8(oracle.rmsnorm(oracle.pre(xs, pms), w))
+        dt = time.perf_counter() - t0
+        out["cpu_baseline"] = {"value": len(rows) / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                               "sample": "%d of %d tokens (%.2f s)" % (len(rows), n, dt)}
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -595,8 +664,15 @@ def main():
                     help="with the chain, skip timing the one-launch-per-side path beside it")
     ap.add_argument("--path", choices=["chain", "step"], default="chain",
                     help="chain: the sides fused across sides (hc_chain_*); step: one hc_block_step per side")
+    ap.add_argument("--op", choices=["mxfp8_cast", "pre_norm_mxfp8"], default=None,
+                    help="time one kernel of the widened rows alone instead of the side steps")
     args = ap.parse_args()
     rank, local_rank, world = dist_env()
+    if args.op is not None and args.impl == "ours":
+        out = run_op(args, local_rank) if rank == 0 else None
+        if out is not None:
+            print(json.dumps(out), flush=True)
+        return
     if world > 1:
         backend = "nccl" if (args.impl == "ours" and torch.cuda.is_available()) else "gloo"
         if backend == "nccl":
