@@ -42,7 +42,7 @@ hc_status cuda_status(cudaError_t e) {
 hc_status check_shape(int64_t n, int hc, int d, bool uses_d) {
     if (n < 0) return HC_ERR_INVALID_ARG;
     if (hc <= 0) return HC_ERR_INVALID_ARG;
-    if (hc != 4) return HC_ERR_UNSUPPORTED;  // the compiled stream count
+    if (hc != 2 && hc != 4 && hc != 8) return HC_ERR_UNSUPPORTED;  // the compiled stream counts
     if (uses_d) {
         if (d <= 0) return HC_ERR_INVALID_ARG;
         if (d % 64 != 0 || d > kMaxD) return HC_ERR_UNSUPPORTED;
@@ -110,7 +110,7 @@ hc_status hc_split_sinkhorn(const float *mixes, const float *hc_scale, const flo
     const Span ins[] = {span(mixes, n * mix * 4), span(hc_scale, 12), span(hc_base, mix * 4)};
     const Span outs[] = {span(pre, n * hc * 4), span(post, n * hc * 4), span(comb, n * hc * hc * 4)};
     if ((st = check_alias(outs, 3, ins, 3)) != HC_OK) return st;
-    return cuda_status(hc::launch_split_sinkhorn(mixes, hc_scale, hc_base, n, sinkhorn_iters, eps,
+    return cuda_status(hc::launch_split_sinkhorn(mixes, hc_scale, hc_base, n, hc, sinkhorn_iters, eps,
                                                  pre, post, comb, stream));
 }
 
@@ -134,13 +134,13 @@ hc_status hc_mixes(const uint16_t *x, const float *hc_fn, const float *hc_scale,
     const Span outs[] = {span(pre, n * hc * 4), span(post, n * hc * 4),
                          span(comb, n * hc * hc * 4), span(mixes_out, mixes_out ? n * mix * 4 : 0)};
     if ((st = check_alias(outs, 4, ins, 4)) != HC_OK) return st;
-    if (hc::cluster_path_supported(d))
+    if (hc == 4 && hc::cluster_path_supported(d))
         return cuda_status(hc::launch_block_cluster(x, nullptr, nullptr, hc_fn, hc_scale, hc_base,
                                                     nullptr, n, d, sinkhorn_iters, eps, norm_eps,
                                                     nullptr, nullptr, pre, post, comb, mixes_out,
                                                     stream));
     return cuda_status(hc::launch_tokens_simple(x, nullptr, nullptr, hc_fn, hc_scale, hc_base,
-                                                nullptr, n, d, sinkhorn_iters, eps, norm_eps,
+                                                nullptr, n, hc, d, sinkhorn_iters, eps, norm_eps,
                                                 nullptr, nullptr, pre, post, comb, mixes_out,
                                                 stream));
 }
@@ -158,7 +158,7 @@ hc_status hc_pre_norm(const uint16_t *x, const float *pre_mix, const float *norm
     const Span ins[] = {span(x, n * hc * d * 2), span(pre_mix, n * hc * 4), span(norm_w, d * 4)};
     const Span outs[] = {span(out, n * d * 2)};
     if ((st = check_alias(outs, 1, ins, 3)) != HC_OK) return st;
-    return cuda_status(hc::launch_pre_norm(x, pre_mix, norm_w, n, d, norm_eps, out, stream));
+    return cuda_status(hc::launch_pre_norm(x, pre_mix, norm_w, n, hc, d, norm_eps, out, stream));
 }
 
 hc_status hc_mxfp8_cast(const uint16_t *in, int64_t rows, int d, uint8_t *codes, uint8_t *scales,
@@ -192,7 +192,7 @@ hc_status hc_pre_norm_mxfp8(const uint16_t *x, const float *pre_mix, const float
     const Span outs[] = {span(codes, n * d), span(scales, n * (d / 32)),
                          span(h_norm_out, h_norm_out ? n * d * 2 : 0)};
     if ((st = check_alias(outs, 3, ins, 3)) != HC_OK) return st;
-    return cuda_status(hc::launch_pre_norm_mxfp8(x, pre_mix, norm_w, n, d, norm_eps, h_norm_out,
+    return cuda_status(hc::launch_pre_norm_mxfp8(x, pre_mix, norm_w, n, hc, d, norm_eps, h_norm_out,
                                                  codes, scales, stream));
 }
 
@@ -210,7 +210,7 @@ hc_status hc_post(const uint16_t *f, const uint16_t *residual, const float *post
                         span(comb, n * hc * hc * 4)};
     const Span outs[] = {span(y, n * hc * d * 2)};
     if ((st = check_alias(outs, 1, ins, 4)) != HC_OK) return st;
-    return cuda_status(hc::launch_post(f, residual, post, comb, n, d, y, stream));
+    return cuda_status(hc::launch_post(f, residual, post, comb, n, hc, d, y, stream));
 }
 
 hc_status hc_block_step(const uint16_t *x, const float *pre_mix, const uint16_t *f,
@@ -240,12 +240,12 @@ hc_status hc_block_step(const uint16_t *x, const float *pre_mix, const uint16_t 
                          span(post_out, post_out ? n * hc * 4 : 0),
                          span(comb_out, comb_out ? n * hc * hc * 4 : 0)};
     if ((st = check_alias(outs, 5, ins, 7)) != HC_OK) return st;
-    if (hc::cluster_path_supported(d))
+    if (hc == 4 && hc::cluster_path_supported(d))
         return cuda_status(hc::launch_block_cluster(x, pre_mix, f, hc_fn, hc_scale, hc_base, norm_w,
                                                     n, d, sinkhorn_iters, eps, norm_eps, h_norm, y,
                                                     pre_out, post_out, comb_out, nullptr, stream));
     return cuda_status(hc::launch_tokens_simple(x, pre_mix, f, hc_fn, hc_scale, hc_base, norm_w, n,
-                                                d, sinkhorn_iters, eps, norm_eps, h_norm, y,
+                                                hc, d, sinkhorn_iters, eps, norm_eps, h_norm, y,
                                                 pre_out, post_out, comb_out, nullptr, stream));
 }
 
@@ -257,7 +257,7 @@ hc_status hc_chain_begin(const uint16_t *x, const float *pre_mix, const float *h
     if (st != HC_OK) return st;
     if (sinkhorn_iters < 1 || !finite_nonneg(eps) || !finite_nonneg(norm_eps))
         return HC_ERR_INVALID_ARG;
-    if (!hc::chain_supported(d)) return HC_ERR_UNSUPPORTED;
+    if (hc != 4 || !hc::chain_supported(d)) return HC_ERR_UNSUPPORTED;
     if (n == 0) return HC_OK;
     if (!x || !pre_mix || !hc_fn || !hc_scale || !hc_base || !state_out) return HC_ERR_INVALID_ARG;
     const void *ptrs[] = {x, pre_mix, hc_fn, hc_scale, hc_base, state_out};
@@ -283,7 +283,7 @@ hc_status hc_chain_side(const uint16_t *x, const uint16_t *f, const float *state
     if (st != HC_OK) return st;
     if (sinkhorn_iters < 1 || !finite_nonneg(eps) || !finite_nonneg(norm_eps))
         return HC_ERR_INVALID_ARG;
-    if (!hc::chain_supported(d)) return HC_ERR_UNSUPPORTED;
+    if (hc != 4 || !hc::chain_supported(d)) return HC_ERR_UNSUPPORTED;
     if (n == 0) return HC_OK;
     const bool next = hc_fn_next != nullptr;
     if (!x || !f || !state_in || !norm_w || !h_norm || !y) return HC_ERR_INVALID_ARG;

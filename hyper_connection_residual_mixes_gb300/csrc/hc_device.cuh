@@ -190,4 +190,65 @@ __device__ __forceinline__ void split_sinkhorn_token(const float (&m)[kMix], flo
     }
 }
 
+// The same split + Sinkhorn for HC streams (mix = (2 + HC) * HC numbers), in
+// plain per-element loops; for HC = 4 the packed version above, which gives
+// exactly the same results.
+template <int HC, bool kFast = false>
+__device__ __forceinline__ void split_sinkhorn_token_hc(const float *m, float s0, float s1, float s2,
+                                                        const float *__restrict__ base, int iters,
+                                                        float eps, float (&pre)[HC],
+                                                        float (&post)[HC], float (&c)[HC * HC]) {
+    if constexpr (HC == kHC) {
+        float mm[kMix];
+#pragma unroll
+        for (int i = 0; i < kMix; ++i) mm[i] = m[i];
+        split_sinkhorn_token<kFast>(mm, s0, s1, s2, base, iters, eps, pre, post, c);
+    } else {
+#pragma unroll
+        for (int j = 0; j < HC; ++j) pre[j] = sigmoid<kFast>(fmaf(m[j], s0, base[j])) + eps;
+#pragma unroll
+        for (int j = 0; j < HC; ++j) post[j] = 2.0f * sigmoid<kFast>(fmaf(m[HC + j], s1, base[HC + j]));
+#pragma unroll
+        for (int i = 0; i < HC * HC; ++i) c[i] = fmaf(m[2 * HC + i], s2, base[2 * HC + i]);
+        // first round: row softmax + eps, then columns
+#pragma unroll
+        for (int j = 0; j < HC; ++j) {
+            float mx = c[j * HC];
+#pragma unroll
+            for (int k = 1; k < HC; ++k) mx = fmaxf(mx, c[j * HC + k]);
+            float s = 0.0f;
+#pragma unroll
+            for (int k = 0; k < HC; ++k) {
+                c[j * HC + k] = expo<kFast>(c[j * HC + k] - mx);
+                s += c[j * HC + k];
+            }
+            const float r = recip<kFast>(s);
+#pragma unroll
+            for (int k = 0; k < HC; ++k) c[j * HC + k] = fmaf(c[j * HC + k], r, eps);
+        }
+        for (int it = 0; it < iters; ++it) {
+            if (it > 0) {
+#pragma unroll
+                for (int j = 0; j < HC; ++j) {
+                    float s = 0.0f;
+#pragma unroll
+                    for (int k = 0; k < HC; ++k) s += c[j * HC + k];
+                    const float r = recip<kFast>(s + eps);
+#pragma unroll
+                    for (int k = 0; k < HC; ++k) c[j * HC + k] *= r;
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < HC; ++k) {
+                float s = 0.0f;
+#pragma unroll
+                for (int j = 0; j < HC; ++j) s += c[j * HC + k];
+                const float r = recip<kFast>(s + eps);
+#pragma unroll
+                for (int j = 0; j < HC; ++j) c[j * HC + k] *= r;
+            }
+        }
+    }
+}
+
 }  // namespace hc

@@ -20,36 +20,45 @@
 namespace hc {
 
 // ------------------------------------------------------------------ a2-a3
+// HC streams: mix = (2 + HC) * HC numbers per row, a multiple of 4 for HC = 2, 4, 8.
+template <int HC>
 __global__ void __launch_bounds__(128)
 k_split_sinkhorn(const float *__restrict__ mixes, const float *__restrict__ hc_scale,
                  const float *__restrict__ hc_base, int64_t n, int iters, float eps,
                  float *__restrict__ pre, float *__restrict__ post, float *__restrict__ comb) {
+    constexpr int MIX = (2 + HC) * HC;
     const int64_t row = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (row >= n) return;
-    float m[kMix];
-    const float4 *src = reinterpret_cast<const float4 *>(mixes + row * kMix);
+    float m[MIX];
+    const float4 *src = reinterpret_cast<const float4 *>(mixes + row * MIX);
 #pragma unroll
-    for (int q = 0; q < kMix / 4; ++q) {
+    for (int q = 0; q < MIX / 4; ++q) {
         const float4 v = __ldg(src + q);
         m[4 * q + 0] = v.x; m[4 * q + 1] = v.y; m[4 * q + 2] = v.z; m[4 * q + 3] = v.w;
     }
-    float pr[kHC], po[kHC], c[kHC * kHC];
-    split_sinkhorn_token(m, __ldg(hc_scale), __ldg(hc_scale + 1), __ldg(hc_scale + 2), hc_base,
-                         iters, eps, pr, po, c);
-    reinterpret_cast<float4 *>(pre)[row] = make_float4(pr[0], pr[1], pr[2], pr[3]);
-    reinterpret_cast<float4 *>(post)[row] = make_float4(po[0], po[1], po[2], po[3]);
-    float4 *cd = reinterpret_cast<float4 *>(comb + row * kHC * kHC);
+    float pr[HC], po[HC], c[HC * HC];
+    split_sinkhorn_token_hc<HC>(m, __ldg(hc_scale), __ldg(hc_scale + 1), __ldg(hc_scale + 2), hc_base,
+                                iters, eps, pr, po, c);
 #pragma unroll
-    for (int q = 0; q < 4; ++q) cd[q] = make_float4(c[4 * q], c[4 * q + 1], c[4 * q + 2], c[4 * q + 3]);
+    for (int k = 0; k < HC; ++k) {
+        pre[row * HC + k] = pr[k];
+        post[row * HC + k] = po[k];
+    }
+#pragma unroll
+    for (int i = 0; i < HC * HC; ++i) comb[row * HC * HC + i] = c[i];
 }
 
 cudaError_t launch_split_sinkhorn(const float *mixes, const float *hc_scale, const float *hc_base,
-                                  int64_t n, int iters, float eps, float *pre, float *post,
+                                  int64_t n, int hc, int iters, float eps, float *pre, float *post,
                                   float *comb, cudaStream_t s) {
     const int threads = 128;
-    const int64_t blocks = (n + threads - 1) / threads;
-    k_split_sinkhorn<<<(unsigned)blocks, threads, 0, s>>>(mixes, hc_scale, hc_base, n, iters, eps,
-                                                           pre, post, comb);
+    const unsigned blocks = (unsigned)((n + threads - 1) / threads);
+    switch (hc) {
+        case 2: k_split_sinkhorn<2><<<blocks, threads, 0, s>>>(mixes, hc_scale, hc_base, n, iters, eps, pre, post, comb); break;
+        case 4: k_split_sinkhorn<4><<<blocks, threads, 0, s>>>(mixes, hc_scale, hc_base, n, iters, eps, pre, post, comb); break;
+        case 8: k_split_sinkhorn<8><<<blocks, threads, 0, s>>>(mixes, hc_scale, hc_base, n, iters, eps, pre, post, comb); break;
+        default: return cudaErrorInvalidValue;
+    }
     return cudaGetLastError();
 }
 
@@ -72,6 +81,24 @@ __device__ __forceinline__ float block_sum(float v, float *scratch /* NT/32 floa
 // out[c] = bf16((h[c] * rsqrt(mean(h^2) + eps)) * w[c]).
 constexpr int kRowThreads = 256;
 
+// h_c = bf16(sum_s pre_mix[s] * x[s][c]): the product with stream 0, then a
+// fused multiply-add per further stream, in stream order.
+template <int HC>
+__device__ __forceinline__ uint4 collapse8(const uint4 *xs, int d8, int c, const float (&p)[HC]) {
+    float h[8], v[8];
+    unpack8(__ldg(xs + c), v);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) h[i] = p[0] * v[i];
+#pragma unroll
+    for (int s = 1; s < HC; ++s) {
+        unpack8(__ldg(xs + s * d8 + c), v);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) h[i] = fmaf(p[s], v[i], h[i]);
+    }
+    return pack8(h);
+}
+
+template <int HC>
 __global__ void __launch_bounds__(kRowThreads)
 k_pre_norm(const uint16_t *__restrict__ x, const float *__restrict__ pre_mix,
            const float *__restrict__ norm_w, int d, float norm_eps, uint16_t *__restrict__ out) {
@@ -79,19 +106,13 @@ k_pre_norm(const uint16_t *__restrict__ x, const float *__restrict__ pre_mix,
     __shared__ float red[kRowThreads / 32];
     const int64_t t = blockIdx.x;
     const int d8 = d >> 3;
-    const uint4 *xs = reinterpret_cast<const uint4 *>(x + t * kHC * d);
-    const float p0 = __ldg(pre_mix + t * kHC), p1 = __ldg(pre_mix + t * kHC + 1),
-                p2 = __ldg(pre_mix + t * kHC + 2), p3 = __ldg(pre_mix + t * kHC + 3);
+    const uint4 *xs = reinterpret_cast<const uint4 *>(x + t * HC * d);
+    float p[HC];
+#pragma unroll
+    for (int s = 0; s < HC; ++s) p[s] = __ldg(pre_mix + t * HC + s);
     float ss = 0.0f;
     for (int c = threadIdx.x; c < d8; c += kRowThreads) {
-        float a[8], b[8], e[8], g[8], h[8];
-        unpack8(__ldg(xs + c), a);
-        unpack8(__ldg(xs + d8 + c), b);
-        unpack8(__ldg(xs + 2 * d8 + c), e);
-        unpack8(__ldg(xs + 3 * d8 + c), g);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) h[i] = fmaf(p3, g[i], fmaf(p2, e[i], fmaf(p1, b[i], p0 * a[i])));
-        const uint4 hb = pack8(h);
+        const uint4 hb = collapse8<HC>(xs, d8, c, p);
         hbuf[c] = hb;
         float r[8];
         unpack8(hb, r);
@@ -113,14 +134,25 @@ k_pre_norm(const uint16_t *__restrict__ x, const float *__restrict__ pre_mix,
     }
 }
 
-cudaError_t launch_pre_norm(const uint16_t *x, const float *pre_mix, const float *norm_w,
-                            int64_t n, int d, float norm_eps, uint16_t *out, cudaStream_t s) {
+template <int HC>
+cudaError_t launch_pre_norm_hc(const uint16_t *x, const float *pre_mix, const float *norm_w,
+                               int64_t n, int d, float norm_eps, uint16_t *out, cudaStream_t s) {
     const size_t smem = (size_t)d * 2;
-    cudaError_t e = cudaFuncSetAttribute(k_pre_norm, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(k_pre_norm<HC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
-    k_pre_norm<<<(unsigned)n, kRowThreads, smem, s>>>(x, pre_mix, norm_w, d, norm_eps, out);
+    k_pre_norm<HC><<<(unsigned)n, kRowThreads, smem, s>>>(x, pre_mix, norm_w, d, norm_eps, out);
     return cudaGetLastError();
+}
+
+cudaError_t launch_pre_norm(const uint16_t *x, const float *pre_mix, const float *norm_w,
+                            int64_t n, int hc, int d, float norm_eps, uint16_t *out, cudaStream_t s) {
+    switch (hc) {
+        case 2: return launch_pre_norm_hc<2>(x, pre_mix, norm_w, n, d, norm_eps, out, s);
+        case 4: return launch_pre_norm_hc<4>(x, pre_mix, norm_w, n, d, norm_eps, out, s);
+        case 8: return launch_pre_norm_hc<8>(x, pre_mix, norm_w, n, d, norm_eps, out, s);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 // ------------------------------------------------------------------ MXFP8 cast
@@ -197,6 +229,7 @@ cudaError_t launch_mxfp8_cast(const uint16_t *in, int64_t rows, int d, uint8_t *
 
 // a4-a5 and the cast in one pass: h_norm as k_pre_norm computes it, then its
 // MXFP8 codes and scales; the bf16 h_norm is written too when out is given.
+template <int HC>
 __global__ void __launch_bounds__(kRowThreads)
 k_pre_norm_mxfp8(const uint16_t *__restrict__ x, const float *__restrict__ pre_mix,
                  const float *__restrict__ norm_w, int d, float norm_eps,
@@ -206,19 +239,13 @@ k_pre_norm_mxfp8(const uint16_t *__restrict__ x, const float *__restrict__ pre_m
     __shared__ float red[kRowThreads / 32];
     const int64_t t = blockIdx.x;
     const int d8 = d >> 3;
-    const uint4 *xs = reinterpret_cast<const uint4 *>(x + t * kHC * d);
-    const float p0 = __ldg(pre_mix + t * kHC), p1 = __ldg(pre_mix + t * kHC + 1),
-                p2 = __ldg(pre_mix + t * kHC + 2), p3 = __ldg(pre_mix + t * kHC + 3);
+    const uint4 *xs = reinterpret_cast<const uint4 *>(x + t * HC * d);
+    float p[HC];
+#pragma unroll
+    for (int s = 0; s < HC; ++s) p[s] = __ldg(pre_mix + t * HC + s);
     float ss = 0.0f;
     for (int c = threadIdx.x; c < d8; c += kRowThreads) {
-        float a[8], b[8], e[8], g[8], h[8];
-        unpack8(__ldg(xs + c), a);
-        unpack8(__ldg(xs + d8 + c), b);
-        unpack8(__ldg(xs + 2 * d8 + c), e);
-        unpack8(__ldg(xs + 3 * d8 + c), g);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) h[i] = fmaf(p3, g[i], fmaf(p2, e[i], fmaf(p1, b[i], p0 * a[i])));
-        const uint4 hb = pack8(h);
+        const uint4 hb = collapse8<HC>(xs, d8, c, p);
         hbuf[c] = hb;
         float r[8];
         unpack8(hb, r);
@@ -251,47 +278,60 @@ k_pre_norm_mxfp8(const uint16_t *__restrict__ x, const float *__restrict__ pre_m
     }
 }
 
-cudaError_t launch_pre_norm_mxfp8(const uint16_t *x, const float *pre_mix, const float *norm_w,
-                                  int64_t n, int d, float norm_eps, uint16_t *out, uint8_t *codes,
-                                  uint8_t *scales, cudaStream_t s) {
+template <int HC>
+cudaError_t launch_pre_norm_mxfp8_hc(const uint16_t *x, const float *pre_mix, const float *norm_w,
+                                     int64_t n, int d, float norm_eps, uint16_t *out, uint8_t *codes,
+                                     uint8_t *scales, cudaStream_t s) {
     const size_t smem = (size_t)d * 2;
-    cudaError_t e = cudaFuncSetAttribute(k_pre_norm_mxfp8,
+    cudaError_t e = cudaFuncSetAttribute(k_pre_norm_mxfp8<HC>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    k_pre_norm_mxfp8<<<(unsigned)n, kRowThreads, smem, s>>>(x, pre_mix, norm_w, d, norm_eps, out,
-                                                            codes, scales);
+    k_pre_norm_mxfp8<HC><<<(unsigned)n, kRowThreads, smem, s>>>(x, pre_mix, norm_w, d, norm_eps, out,
+                                                                codes, scales);
     return cudaGetLastError();
+}
+
+cudaError_t launch_pre_norm_mxfp8(const uint16_t *x, const float *pre_mix, const float *norm_w,
+                                  int64_t n, int hc, int d, float norm_eps, uint16_t *out,
+                                  uint8_t *codes, uint8_t *scales, cudaStream_t s) {
+    switch (hc) {
+        case 2: return launch_pre_norm_mxfp8_hc<2>(x, pre_mix, norm_w, n, d, norm_eps, out, codes, scales, s);
+        case 4: return launch_pre_norm_mxfp8_hc<4>(x, pre_mix, norm_w, n, d, norm_eps, out, codes, scales, s);
+        case 8: return launch_pre_norm_mxfp8_hc<8>(x, pre_mix, norm_w, n, d, norm_eps, out, codes, scales, s);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 // ------------------------------------------------------------------ a6
 // y[k][c] = bf16(post[k] * f[c] + sum_j comb[j][k] * x[j][c]), fp32, j in order.
+template <int HC>
 __global__ void __launch_bounds__(kRowThreads)
 k_post(const uint16_t *__restrict__ f, const uint16_t *__restrict__ residual,
        const float *__restrict__ post, const float *__restrict__ comb, int d,
        uint16_t *__restrict__ y) {
     const int64_t t = blockIdx.x;
     const int d8 = d >> 3;
-    float po[kHC], cm[kHC * kHC];
+    float po[HC], cm[HC * HC];
 #pragma unroll
-    for (int k = 0; k < kHC; ++k) po[k] = __ldg(post + t * kHC + k);
+    for (int k = 0; k < HC; ++k) po[k] = __ldg(post + t * HC + k);
 #pragma unroll
-    for (int i = 0; i < kHC * kHC; ++i) cm[i] = __ldg(comb + t * kHC * kHC + i);
+    for (int i = 0; i < HC * HC; ++i) cm[i] = __ldg(comb + t * HC * HC + i);
     const uint4 *fs = reinterpret_cast<const uint4 *>(f + t * d);
-    const uint4 *xs = reinterpret_cast<const uint4 *>(residual + t * kHC * d);
-    uint4 *ys = reinterpret_cast<uint4 *>(y + t * kHC * d);
+    const uint4 *xs = reinterpret_cast<const uint4 *>(residual + t * HC * d);
+    uint4 *ys = reinterpret_cast<uint4 *>(y + t * HC * d);
     for (int c = threadIdx.x; c < d8; c += kRowThreads) {
-        float fv[8], xv[kHC][8];
+        float fv[8], xv[HC][8];
         unpack8(__ldg(fs + c), fv);
 #pragma unroll
-        for (int j = 0; j < kHC; ++j) unpack8(__ldg(xs + j * d8 + c), xv[j]);
+        for (int j = 0; j < HC; ++j) unpack8(__ldg(xs + j * d8 + c), xv[j]);
 #pragma unroll
-        for (int k = 0; k < kHC; ++k) {
+        for (int k = 0; k < HC; ++k) {
             float o[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 float acc = po[k] * fv[i];
 #pragma unroll
-                for (int j = 0; j < kHC; ++j) acc = fmaf(cm[j * kHC + k], xv[j][i], acc);
+                for (int j = 0; j < HC; ++j) acc = fmaf(cm[j * HC + k], xv[j][i], acc);
                 o[i] = acc;
             }
             ys[k * d8 + c] = pack8(o);
@@ -299,10 +339,21 @@ k_post(const uint16_t *__restrict__ f, const uint16_t *__restrict__ residual,
     }
 }
 
-cudaError_t launch_post(const uint16_t *f, const uint16_t *residual, const float *post,
-                        const float *comb, int64_t n, int d, uint16_t *y, cudaStream_t s) {
-    k_post<<<(unsigned)n, kRowThreads, 0, s>>>(f, residual, post, comb, d, y);
+template <int HC>
+cudaError_t launch_post_hc(const uint16_t *f, const uint16_t *residual, const float *post,
+                           const float *comb, int64_t n, int d, uint16_t *y, cudaStream_t s) {
+    k_post<HC><<<(unsigned)n, kRowThreads, 0, s>>>(f, residual, post, comb, d, y);
     return cudaGetLastError();
+}
+
+cudaError_t launch_post(const uint16_t *f, const uint16_t *residual, const float *post,
+                        const float *comb, int64_t n, int hc, int d, uint16_t *y, cudaStream_t s) {
+    switch (hc) {
+        case 2: return launch_post_hc<2>(f, residual, post, comb, n, d, y, s);
+        case 4: return launch_post_hc<4>(f, residual, post, comb, n, d, y, s);
+        case 8: return launch_post_hc<8>(f, residual, post, comb, n, d, y, s);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 // ------------------------------------------------------------------ a1-a6, TOK tokens per CTA
@@ -312,10 +363,13 @@ cudaError_t launch_post(const uint16_t *f, const uint16_t *residual, const float
 // r = rsqrt(mean(x^2) + norm_eps), mixes = dot * r, and the split + Sinkhorn.
 // Phase 2 (side step only): y and h for every token (x re-read through L1/L2),
 // sum of squares of the rounded h, then h_norm.
-constexpr int kTok = 4;
 constexpr int kTokThreads = 256;
 
-template <bool kFull>
+// tokens per CTA: the accumulators are (2 + HC) * HC per token
+template <int HC>
+__host__ __device__ constexpr int tok_per_cta() { return HC <= 4 ? 4 : 1; }
+
+template <bool kFull, int HC>
 __global__ void __launch_bounds__(kTokThreads)
 k_tokens_simple(const uint16_t *__restrict__ x, const float *__restrict__ pre_mix,
                 const uint16_t *__restrict__ f, const float *__restrict__ hc_fn,
@@ -324,22 +378,24 @@ k_tokens_simple(const uint16_t *__restrict__ x, const float *__restrict__ pre_mi
                 float norm_eps, uint16_t *__restrict__ h_norm, uint16_t *__restrict__ y,
                 float *__restrict__ pre_out, float *__restrict__ post_out,
                 float *__restrict__ comb_out, float *__restrict__ mixes_out) {
-    constexpr int kVals = kMix * kTok + kTok;  // 24 dots per token + sum of squares per token
+    constexpr int kTok = tok_per_cta<HC>();
+    constexpr int MIX = (2 + HC) * HC;
+    constexpr int kVals = MIX * kTok + kTok;  // MIX dots per token + sum of squares per token
     extern __shared__ uint4 hbuf[];            // kTok * d/8 chunks (side step only)
     __shared__ float red[kTokThreads / 32][kVals];
     __shared__ float tot[kVals];
-    __shared__ float coef[kTok][kHC + kHC * kHC];
+    __shared__ float coef[kTok][HC + HC * HC];
     __shared__ float ssh[kTokThreads / 32][kTok];
 
     const int64_t t0 = (int64_t)blockIdx.x * kTok;
     const int ntok = (n - t0 < kTok) ? (int)(n - t0) : kTok;
-    const int K = kHC * d, K8 = K >> 3;
+    const int K = HC * d, K8 = K >> 3;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    float acc[kMix][kTok];
+    float acc[MIX][kTok];
     float ss[kTok];
 #pragma unroll
-    for (int i = 0; i < kMix; ++i)
+    for (int i = 0; i < MIX; ++i)
 #pragma unroll
         for (int u = 0; u < kTok; ++u) acc[i][u] = 0.0f;
 #pragma unroll
@@ -359,7 +415,7 @@ k_tokens_simple(const uint16_t *__restrict__ x, const float *__restrict__ pre_mi
             for (int e = 0; e < 8; ++e) ss[u] = fmaf(xv[u][e], xv[u][e], ss[u]);
         }
 #pragma unroll
-        for (int i = 0; i < kMix; ++i) {
+        for (int i = 0; i < MIX; ++i) {
             const float4 *wp = reinterpret_cast<const float4 *>(hc_fn + (int64_t)i * K) + 2 * ch;
             const float4 wa = __ldg(wp), wb = __ldg(wp + 1);
             const float w[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
@@ -371,7 +427,7 @@ k_tokens_simple(const uint16_t *__restrict__ x, const float *__restrict__ pre_mi
     }
     // block reduction of the 24*kTok dots and kTok sums of squares
 #pragma unroll
-    for (int i = 0; i < kMix; ++i)
+    for (int i = 0; i < MIX; ++i)
 #pragma unroll
         for (int u = 0; u < kTok; ++u) {
             const float v = warp_sum(acc[i][u]);
@@ -380,7 +436,7 @@ k_tokens_simple(const uint16_t *__restrict__ x, const float *__restrict__ pre_mi
 #pragma unroll
     for (int u = 0; u < kTok; ++u) {
         const float v = warp_sum(ss[u]);
-        if (lane == 0) red[warp][kMix * kTok + u] = v;
+        if (lane == 0) red[warp][MIX * kTok + u] = v;
     }
     __syncthreads();
     for (int v = threadIdx.x; v < kVals; v += kTokThreads) {
@@ -393,31 +449,30 @@ k_tokens_simple(const uint16_t *__restrict__ x, const float *__restrict__ pre_mi
     if (threadIdx.x < ntok) {
         const int u = threadIdx.x;
         const int64_t t = t0 + u;
-        const float r = rsqrtf(tot[kMix * kTok + u] / (float)K + norm_eps);
-        float m[kMix];
+        const float r = rsqrtf(tot[MIX * kTok + u] / (float)K + norm_eps);
+        float m[MIX];
 #pragma unroll
-        for (int i = 0; i < kMix; ++i) m[i] = tot[i * kTok + u] * r;
-        float pr[kHC], po[kHC], c[kHC * kHC];
-        split_sinkhorn_token(m, __ldg(hc_scale), __ldg(hc_scale + 1), __ldg(hc_scale + 2), hc_base,
-                             iters, eps, pr, po, c);
-        if (pre_out) reinterpret_cast<float4 *>(pre_out)[t] = make_float4(pr[0], pr[1], pr[2], pr[3]);
-        if (post_out) reinterpret_cast<float4 *>(post_out)[t] = make_float4(po[0], po[1], po[2], po[3]);
+        for (int i = 0; i < MIX; ++i) m[i] = tot[i * kTok + u] * r;
+        float pr[HC], po[HC], c[HC * HC];
+        split_sinkhorn_token_hc<HC>(m, __ldg(hc_scale), __ldg(hc_scale + 1), __ldg(hc_scale + 2),
+                                    hc_base, iters, eps, pr, po, c);
+#pragma unroll
+        for (int k = 0; k < HC; ++k) {
+            if (pre_out) pre_out[t * HC + k] = pr[k];
+            if (post_out) post_out[t * HC + k] = po[k];
+        }
         if (comb_out) {
-            float4 *cd = reinterpret_cast<float4 *>(comb_out + t * kHC * kHC);
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-                cd[q] = make_float4(c[4 * q], c[4 * q + 1], c[4 * q + 2], c[4 * q + 3]);
+            for (int i = 0; i < HC * HC; ++i) comb_out[t * HC * HC + i] = c[i];
         }
         if (mixes_out) {
-            float4 *md = reinterpret_cast<float4 *>(mixes_out + t * kMix);
 #pragma unroll
-            for (int q = 0; q < kMix / 4; ++q)
-                md[q] = make_float4(m[4 * q], m[4 * q + 1], m[4 * q + 2], m[4 * q + 3]);
+            for (int i = 0; i < MIX; ++i) mixes_out[t * MIX + i] = m[i];
         }
 #pragma unroll
-        for (int k = 0; k < kHC; ++k) coef[u][k] = po[k];
+        for (int k = 0; k < HC; ++k) coef[u][k] = po[k];
 #pragma unroll
-        for (int i = 0; i < kHC * kHC; ++i) coef[u][kHC + i] = c[i];
+        for (int i = 0; i < HC * HC; ++i) coef[u][HC + i] = c[i];
     }
     if constexpr (!kFull) return;
     __syncthreads();
@@ -431,32 +486,36 @@ k_tokens_simple(const uint16_t *__restrict__ x, const float *__restrict__ pre_mi
     for (int u = 0; u < kTok; ++u) {
         if (u >= ntok) break;
         const int64_t t = t0 + u;
-        const float p0 = __ldg(pre_mix + t * kHC), p1 = __ldg(pre_mix + t * kHC + 1),
-                    p2 = __ldg(pre_mix + t * kHC + 2), p3 = __ldg(pre_mix + t * kHC + 3);
+        float pm[HC];
+#pragma unroll
+        for (int s = 0; s < HC; ++s) pm[s] = __ldg(pre_mix + t * HC + s);
         const uint4 *xs = reinterpret_cast<const uint4 *>(x + t * K);
         const uint4 *fs = reinterpret_cast<const uint4 *>(f + t * d);
         uint4 *ys = reinterpret_cast<uint4 *>(y + t * K);
         for (int c = threadIdx.x; c < d8; c += kTokThreads) {
-            float fv[8], xv[kHC][8];
+            float fv[8], xv[HC][8];
             unpack8(__ldg(fs + c), fv);
 #pragma unroll
-            for (int j = 0; j < kHC; ++j) unpack8(__ldg(xs + j * d8 + c), xv[j]);
+            for (int j = 0; j < HC; ++j) unpack8(__ldg(xs + j * d8 + c), xv[j]);
 #pragma unroll
-            for (int k = 0; k < kHC; ++k) {
+            for (int k = 0; k < HC; ++k) {
                 float o[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     float a = coef[u][k] * fv[i];
 #pragma unroll
-                    for (int j = 0; j < kHC; ++j) a = fmaf(coef[u][kHC + j * kHC + k], xv[j][i], a);
+                    for (int j = 0; j < HC; ++j) a = fmaf(coef[u][HC + j * HC + k], xv[j][i], a);
                     o[i] = a;
                 }
                 ys[k * d8 + c] = pack8(o);
             }
             float h[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-                h[i] = fmaf(p3, xv[3][i], fmaf(p2, xv[2][i], fmaf(p1, xv[1][i], p0 * xv[0][i])));
+            for (int i = 0; i < 8; ++i) {
+                h[i] = pm[0] * xv[0][i];
+#pragma unroll
+                for (int s2 = 1; s2 < HC; ++s2) h[i] = fmaf(pm[s2], xv[s2][i], h[i]);
+            }
             const uint4 hb = pack8(h);
             hbuf[u * d8 + c] = hb;
             float r8[8];
@@ -490,28 +549,48 @@ k_tokens_simple(const uint16_t *__restrict__ x, const float *__restrict__ pre_mi
     }
 }
 
-cudaError_t launch_tokens_simple(const uint16_t *x, const float *pre_mix, const uint16_t *f,
-                                 const float *hc_fn, const float *hc_scale, const float *hc_base,
-                                 const float *norm_w, int64_t n, int d, int iters, float eps,
-                                 float norm_eps, uint16_t *h_norm, uint16_t *y, float *pre_out,
-                                 float *post_out, float *comb_out, float *mixes_out,
-                                 cudaStream_t s) {
+template <int HC>
+cudaError_t launch_tokens_simple_hc(const uint16_t *x, const float *pre_mix, const uint16_t *f,
+                                    const float *hc_fn, const float *hc_scale, const float *hc_base,
+                                    const float *norm_w, int64_t n, int d, int iters, float eps,
+                                    float norm_eps, uint16_t *h_norm, uint16_t *y, float *pre_out,
+                                    float *post_out, float *comb_out, float *mixes_out,
+                                    cudaStream_t s) {
+    constexpr int kTok = tok_per_cta<HC>();
     const int64_t blocks = (n + kTok - 1) / kTok;
     cudaError_t e;
     if (f) {
         const size_t smem = (size_t)kTok * d * 2;
-        e = cudaFuncSetAttribute(k_tokens_simple<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem);
+        e = cudaFuncSetAttribute(k_tokens_simple<true, HC>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        k_tokens_simple<true><<<(unsigned)blocks, kTokThreads, smem, s>>>(
+        k_tokens_simple<true, HC><<<(unsigned)blocks, kTokThreads, smem, s>>>(
             x, pre_mix, f, hc_fn, hc_scale, hc_base, norm_w, n, d, iters, eps, norm_eps, h_norm, y,
             pre_out, post_out, comb_out, mixes_out);
     } else {
-        k_tokens_simple<false><<<(unsigned)blocks, kTokThreads, 0, s>>>(
+        k_tokens_simple<false, HC><<<(unsigned)blocks, kTokThreads, 0, s>>>(
             x, pre_mix, f, hc_fn, hc_scale, hc_base, norm_w, n, d, iters, eps, norm_eps, h_norm, y,
             pre_out, post_out, comb_out, mixes_out);
     }
     return cudaGetLastError();
+}
+
+cudaError_t launch_tokens_simple(const uint16_t *x, const float *pre_mix, const uint16_t *f,
+                                 const float *hc_fn, const float *hc_scale, const float *hc_base,
+                                 const float *norm_w, int64_t n, int hc, int d, int iters, float eps,
+                                 float norm_eps, uint16_t *h_norm, uint16_t *y, float *pre_out,
+                                 float *post_out, float *comb_out, float *mixes_out,
+                                 cudaStream_t s) {
+#define HC_TOKENS(H) launch_tokens_simple_hc<H>(x, pre_mix, f, hc_fn, hc_scale, hc_base, norm_w, n, d, \
+                                                 iters, eps, norm_eps, h_norm, y, pre_out, post_out,   \
+                                                 comb_out, mixes_out, s)
+    switch (hc) {
+        case 2: return HC_TOKENS(2);
+        case 4: return HC_TOKENS(4);
+        case 8: return HC_TOKENS(8);
+        default: return cudaErrorInvalidValue;
+    }
+#undef HC_TOKENS
 }
 
 }  // namespace hc

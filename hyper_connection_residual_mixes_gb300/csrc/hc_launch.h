@@ -1,6 +1,7 @@
 // hc_launch.h -- internal launcher prototypes (host side of libhc).
 // Arguments have been validated by hc_api.cu before any of these is called:
-// hc == 4, d a multiple of 64 in [64, 16384], n >= 1, pointers 16-byte aligned.
+// hc in {2, 4, 8} (4 only for the cluster and chain paths), d a multiple of 64 in
+// [64, 16384], n >= 1, pointers 16-byte aligned.
 #pragma once
 
 #include <cstdint>
@@ -9,25 +10,25 @@
 namespace hc {
 
 cudaError_t launch_split_sinkhorn(const float *mixes, const float *hc_scale, const float *hc_base,
-                                  int64_t n, int iters, float eps, float *pre, float *post,
+                                  int64_t n, int hc, int iters, float eps, float *pre, float *post,
                                   float *comb, cudaStream_t s);
 
 cudaError_t launch_pre_norm(const uint16_t *x, const float *pre_mix, const float *norm_w,
-                            int64_t n, int d, float norm_eps, uint16_t *out, cudaStream_t s);
+                            int64_t n, int hc, int d, float norm_eps, uint16_t *out, cudaStream_t s);
 
 cudaError_t launch_mxfp8_cast(const uint16_t *in, int64_t rows, int d, uint8_t *codes,
                               uint8_t *scales, cudaStream_t s);
 cudaError_t launch_pre_norm_mxfp8(const uint16_t *x, const float *pre_mix, const float *norm_w,
-                                  int64_t n, int d, float norm_eps, uint16_t *out, uint8_t *codes,
-                                  uint8_t *scales, cudaStream_t s);
+                                  int64_t n, int hc, int d, float norm_eps, uint16_t *out,
+                                  uint8_t *codes, uint8_t *scales, cudaStream_t s);
 cudaError_t launch_post(const uint16_t *f, const uint16_t *residual, const float *post,
-                        const float *comb, int64_t n, int d, uint16_t *y, cudaStream_t s);
+                        const float *comb, int64_t n, int hc, int d, uint16_t *y, cudaStream_t s);
 
 // a1-a3 (write pre/post/comb, optional mixes) or, when `f` is non-null, the
 // whole side step a1-a6.  Simple path: a CTA owns a few whole tokens.
 cudaError_t launch_tokens_simple(const uint16_t *x, const float *pre_mix, const uint16_t *f,
                                  const float *hc_fn, const float *hc_scale, const float *hc_base,
-                                 const float *norm_w, int64_t n, int d, int iters, float eps,
+                                 const float *norm_w, int64_t n, int hc, int d, int iters, float eps,
                                  float norm_eps, uint16_t *h_norm, uint16_t *y, float *pre_out,
                                  float *post_out, float *comb_out, float *mixes_out,
                                  cudaStream_t s);

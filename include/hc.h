@@ -36,8 +36,11 @@
  *    launches nothing and returns a non-zero status.  n == 0 is valid and
  *    does nothing.  A failed launch returns HC_ERR_CUDA and records the CUDA
  *    error code for hc_last_cuda_error() (per host thread).
- *  - Compiled fast paths: hc == 4 and d a positive multiple of 64 with
- *    d <= 16384; anything else returns HC_ERR_UNSUPPORTED.
+ *  - Compiled stream counts: hc = 2, 4 or 8 (the pages' kernel takes any
+ *    hc_mult; the released model uses 4), with d a positive multiple of 64,
+ *    d <= 16384; anything else returns HC_ERR_UNSUPPORTED.  The tensor-core
+ *    cluster path of hc_mixes / hc_block_step and the chain (hc_chain_*)
+ *    serve hc = 4; the other counts run on the whole-token kernels.
  *  - Output ranges must not overlap input ranges or each other
  *    (HC_ERR_ALIAS), except where an entry point says otherwise.
  */
@@ -55,7 +58,7 @@ extern "C" {
 typedef enum {
     HC_OK = 0,
     HC_ERR_INVALID_ARG = 1,  /* null pointer, negative size, iters < 1, non-finite or negative eps */
-    HC_ERR_UNSUPPORTED = 2,  /* hc != 4, or d not a multiple of 64 in [64, 16384] */
+    HC_ERR_UNSUPPORTED = 2,  /* hc not 2, 4 or 8, or d not a multiple of 64 in [64, 16384] */
     HC_ERR_MISALIGNED = 3,   /* a pointer that is not 16-byte aligned */
     HC_ERR_ALIAS = 4,        /* an output range overlaps an input or another output */
     HC_ERR_CUDA = 5,         /* a CUDA runtime call failed; see hc_last_cuda_error() */
@@ -198,7 +201,7 @@ hc_status hc_pre_norm_mxfp8(const uint16_t *x, const float *pre_mix, const float
  * The caller allocates it ([n, 32] fp32, 16-byte aligned) and keeps two of
  * them in rotation: side i reads the state of side i and writes that of side
  * i + 1 (the two may not overlap: HC_ERR_ALIAS).  Supported when d is a
- * multiple of 1024 and d <= 7168 (HC_ERR_UNSUPPORTED otherwise).
+ * multiple of 1024 and d <= 7168, with hc = 4 (HC_ERR_UNSUPPORTED otherwise).
  *
  * hc_chain_begin: a1-a3 of the first side and its RMSNorm statistic.
  *   x [n, hc, d] bf16, pre_mix [n, hc] fp32, hc_fn, hc_scale, hc_base of the

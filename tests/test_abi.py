@@ -104,7 +104,8 @@ def test_split_sinkhorn_validation(lib):
                               FAKE2 + 0x2000, None)
     assert r(n=0) == 0
     assert r(n=-3) == 1
-    assert r(hc=2) == 2
+    assert r(hc=3) == 2    # stream counts 2, 4 and 8 are compiled
+    assert r(hc=16) == 2
     assert r(iters=0) == 1
     assert r(mixes=None) == 1
     assert r(mixes=FAKE + 4) == 3

@@ -571,3 +571,57 @@ def test_mxfp8_every_e4m3_value_round_trips():
             codes, sc = oracle.mxfp8(_bits(grp))
             assert sc[0, 0] == 127 + ex
             assert np.array_equal(codes[0, :len(v)], codes_all[start:start + 31])
+
+
+# ------------------------------------------------ other stream counts (hc = 8)
+# The oracle is written for any hc; these pins repeat the library and
+# independent-restatement checks at hc = 8 (mix = 80), each on its own random
+# stream.
+
+def test_hc8_mixes_matches_numpy():
+    rng = np.random.default_rng(801)
+    n, hc, d = 3, 8, 16
+    x = inputs.bf16_bits_np(torch.from_numpy(rng.standard_normal((n, hc, d))).to(torch.bfloat16))
+    w = (rng.standard_normal(((2 + hc) * hc, hc * d)) * 0.1).astype(np.float32)
+    got = oracle.mixes(x, w, norm_eps=1e-6)
+    xf = oracle.bf16_to_f64(x).reshape(n, hc * d)
+    want = (xf @ w.astype(np.float64).T) / np.sqrt(np.mean(xf * xf, axis=1, keepdims=True) + 1e-6)
+    np.testing.assert_allclose(got, want, rtol=1e-13, atol=1e-15)
+
+
+@pytest.mark.parametrize("iters", [1, 2, 20])
+@pytest.mark.parametrize("eps", [1e-6, 0.0])
+def test_hc8_sinkhorn_matches_vector_form(iters, eps):
+    rng = np.random.default_rng(802 + iters)
+    hc = 8
+    mix = (2 + hc) * hc
+    m = rng.standard_normal((4, mix)) * 2.0
+    scale = np.array([0.7, 1.3, 0.9], np.float32)
+    base = rng.standard_normal(mix).astype(np.float32)
+    from scipy.special import expit
+    pre, post, comb = oracle.split_sinkhorn(m, scale, base, hc=hc, iters=iters, eps=eps)
+    for t in range(4):
+        logits = (m[t, 2 * hc:] * float(scale[2]) + base[2 * hc:].astype(np.float64)).reshape(hc, hc)
+        np.testing.assert_allclose(comb[t], _vector_form_sinkhorn(logits, iters, eps), rtol=1e-12, atol=1e-15)
+    np.testing.assert_allclose(pre, expit(m[:, :hc] * float(scale[0]) + base[:hc]) + eps, rtol=1e-14, atol=1e-16)
+    np.testing.assert_allclose(post, 2.0 * expit(m[:, hc:2 * hc] * float(scale[1]) + base[hc:2 * hc]),
+                               rtol=1e-14, atol=1e-16)
+
+
+def test_hc8_pre_and_post_match_numpy():
+    rng = np.random.default_rng(803)
+    n, hc, d = 5, 8, 40
+    x = inputs.bf16_bits_np(torch.from_numpy(rng.standard_normal((n, hc, d))).to(torch.bfloat16))
+    pm = rng.uniform(0.1, 1.0, (n, hc))
+    got = oracle.pre(x, pm)
+    xf = oracle.bf16_to_f64(x)
+    want = oracle.bf16_from_f64(np.einsum("ts,tsd->td", pm, xf))
+    diff = np.abs(got.astype(np.int32) - want.astype(np.int32))
+    assert diff.max() <= 1 and np.mean(diff) < 1e-3
+    f = inputs.bf16_bits_np(torch.from_numpy(rng.standard_normal((n, d))).to(torch.bfloat16))
+    post = rng.uniform(0, 2, (n, hc))
+    comb = rng.uniform(0, 1, (n, hc, hc))
+    got = oracle.post(f, x, post, comb)
+    ref = post[:, :, None] * oracle.bf16_to_f64(f)[:, None, :] + np.einsum("tjk,tjd->tkd", comb, xf)
+    diff = np.abs(got.astype(np.int32) - oracle.bf16_from_f64(ref).astype(np.int32))
+    assert diff.max() <= 1 and np.mean(diff) < 1e-3
