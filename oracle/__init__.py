@@ -70,11 +70,16 @@ def _load():
         lib.hco_post.argtypes = [P, P, P, P, i64, i32, i32, P]
         lib.hco_block_step.argtypes = [P, P, P, P, P, P, P, i64, i32, i32, i32, f64, f64,
                                        P, P, P, P, P, P]
+        lib.hco_side_f64.argtypes = [P, P, P, P, P, P, P, i64, i32, i32, i32, f64, f64, i32,
+                                     P, P, P, P, P]
+        lib.hco_side_backward_f64.argtypes = [P, P, P, P, P, P, P, i64, i32, i32, i32, f64, f64,
+                                              P, P, P, i32, P, P, P, P, P, P, P]
         lib.hco_e4m3_from_double.argtypes = [f64]
         lib.hco_e4m3_from_double.restype = ctypes.c_uint8
         lib.hco_mxfp8.argtypes = [P, i64, i32, P, P]
         for name in ("hco_mixes", "hco_split_sinkhorn", "hco_pre", "hco_rmsnorm",
-                     "hco_post", "hco_block_step", "hco_mxfp8"):
+                     "hco_post", "hco_block_step", "hco_mxfp8", "hco_side_f64",
+                     "hco_side_backward_f64"):
             getattr(lib, name).restype = i32
         _lib = lib
         return lib
@@ -168,6 +173,49 @@ def rmsnorm(h, w, eps=1e-20):
     out = np.empty((n, d), dtype=np.uint16)
     _check(_load().hco_rmsnorm(hp, wp, n, d, float(eps), out.ctypes.data_as(ctypes.c_void_p)),
            "rmsnorm")
+    return out
+
+
+def side_f64(x, pre_mix, f, hc_fn, hc_scale, hc_base, norm_w, iters=20, eps=1e-6,
+             norm_eps=1e-20, rounded=True):
+    """The side step on double inputs x [n, hc, d], pre_mix [n, hc], f [n, d]
+    (and the parameters): dict of h_norm, y, pre, post, comb (doubles).  With
+    rounded=True the three bf16 casts are applied, as in block_step."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    n, hc, d = x.shape
+    args = [_arr(a, np.float64) for a in (x, pre_mix, f, hc_fn, hc_scale, hc_base, norm_w)]
+    out = dict(h_norm=np.empty((n, d)), y=np.empty((n, hc, d)), pre=np.empty((n, hc)),
+               post=np.empty((n, hc)), comb=np.empty((n, hc, hc)))
+    V = ctypes.c_void_p
+    _check(_load().hco_side_f64(*(p for _, p in args), n, hc, d, int(iters), float(eps),
+                                float(norm_eps), int(bool(rounded)),
+                                *(out[k].ctypes.data_as(V) for k in ("h_norm", "y", "pre", "post",
+                                                                     "comb"))), "side_f64")
+    return out
+
+
+def side_backward(x, pre_mix, f, hc_fn, hc_scale, hc_base, norm_w, g_h_norm, g_y, g_pre=None,
+                  iters=20, eps=1e-6, norm_eps=1e-20, rounded=True):
+    """Backward of side_f64 for upstream gradients g_h_norm [n, d], g_y
+    [n, hc, d], g_pre [n, hc] (None: zero) -> dict of g_x, g_pre_mix, g_f
+    (per token) and g_hc_fn, g_hc_scale, g_hc_base, g_norm_w (summed over
+    tokens), all doubles."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    n, hc, d = x.shape
+    mix = (2 + hc) * hc
+    args = [_arr(a, np.float64) for a in (x, pre_mix, f, hc_fn, hc_scale, hc_base, norm_w,
+                                          g_h_norm, g_y)]
+    gp = _arr(g_pre, np.float64) if g_pre is not None else (None, None)
+    out = dict(g_x=np.empty((n, hc, d)), g_pre_mix=np.empty((n, hc)), g_f=np.empty((n, d)),
+               g_hc_fn=np.empty((mix, hc * d)), g_hc_scale=np.empty(3), g_hc_base=np.empty(mix),
+               g_norm_w=np.empty(d))
+    V = ctypes.c_void_p
+    _check(_load().hco_side_backward_f64(*(p for _, p in args[:7]), n, hc, d, int(iters), float(eps),
+                                         float(norm_eps), args[7][1], args[8][1], gp[1],
+                                         int(bool(rounded)),
+                                         *(out[k].ctypes.data_as(V) for k in
+                                           ("g_x", "g_pre_mix", "g_f", "g_hc_fn", "g_hc_scale",
+                                            "g_hc_base", "g_norm_w"))), "side_backward")
     return out
 
 

@@ -389,3 +389,294 @@ int hco_mxfp8(const uint16_t *in, int64_t rows, int d, uint8_t *codes, uint8_t *
     }
     return HCO_OK;
 }
+
+/* ------------------------------------------------------------------------ */
+/* f3: the backward of one side step.  The pages give no backward pass; this
+ * is the derivative of a1-a6 exactly as defined above ([BLOCK], [COMB]),
+ * token by token, with the parameter gradients summed over tokens in index
+ * order.  Inputs are doubles (for the bf16 tensors: their exact values).
+ * rnd = 1: the forward's three bf16 casts (h, h_norm, y) are applied as in
+ * hco_block_step, and gradients pass through a cast unchanged (its
+ * derivative is taken as 1, as for a dtype cast in autograd); rnd = 0: no
+ * cast anywhere, so the result is the exact derivative of that unrounded
+ * forward (which the pins check with finite differences). */
+
+static double rnd_bf16(double v, int rnd) { return rnd ? hco_bf16_to_double(hco_bf16_from_double(v)) : v; }
+
+/* Sinkhorn with every intermediate kept: S = the row softmax of L; P[0] =
+ * S + eps; then steps k = 1 .. 2*iters - 1, a column step for odd k and a row
+ * step for even k, each dividing by (sum + eps).  P holds 2*iters matrices. */
+static void sinkhorn_ckpt(const double *L, int hc, int iters, double eps, double *S, double *P)
+{
+    const int q = hc * hc;
+    for (int j = 0; j < hc; ++j) {
+        double mx = L[j * hc];
+        for (int k = 1; k < hc; ++k)
+            if (L[j * hc + k] > mx)
+                mx = L[j * hc + k];
+        double s = 0.0;
+        for (int k = 0; k < hc; ++k) {
+            S[j * hc + k] = exp(L[j * hc + k] - mx);
+            s += S[j * hc + k];
+        }
+        for (int k = 0; k < hc; ++k) {
+            S[j * hc + k] = S[j * hc + k] / s;
+            P[j * hc + k] = S[j * hc + k] + eps;
+        }
+    }
+    for (int st = 1; st < 2 * iters; ++st) {
+        const double *a = P + (st - 1) * q;
+        double *b = P + st * q;
+        for (int i = 0; i < hc; ++i) {
+            double s = 0.0;
+            for (int o = 0; o < hc; ++o)
+                s += (st & 1) ? a[o * hc + i] : a[i * hc + o]; /* odd: column i; even: row i */
+            for (int o = 0; o < hc; ++o) {
+                int idx = (st & 1) ? o * hc + i : i * hc + o;
+                b[idx] = a[idx] / (s + eps);
+            }
+        }
+    }
+}
+
+/* Reverse of sinkhorn_ckpt: g (the gradient of the last matrix) -> gL. */
+static void sinkhorn_back(const double *S, const double *P, int hc, int iters, double eps,
+                          double *g, double *gL)
+{
+    const int q = hc * hc;
+    for (int st = 2 * iters - 1; st >= 1; --st) {
+        const double *a = P + (st - 1) * q; /* the step's input */
+        const double *b = P + st * q;       /* its output */
+        for (int i = 0; i < hc; ++i) {
+            double s = 0.0, dot = 0.0;
+            for (int o = 0; o < hc; ++o) {
+                int idx = (st & 1) ? o * hc + i : i * hc + o;
+                s += a[idx];
+                dot += g[idx] * b[idx];
+            }
+            /* out = in / D: d(out_o)/d(in_o') = (delta - out_o) / D along the line */
+            for (int o = 0; o < hc; ++o) {
+                int idx = (st & 1) ? o * hc + i : i * hc + o;
+                g[idx] = (g[idx] - dot) / (s + eps);
+            }
+        }
+    }
+    /* P[0] = softmax(L) + eps, row by row */
+    for (int j = 0; j < hc; ++j) {
+        double dot = 0.0;
+        for (int k = 0; k < hc; ++k)
+            dot += g[j * hc + k] * S[j * hc + k];
+        for (int k = 0; k < hc; ++k)
+            gL[j * hc + k] = S[j * hc + k] * (g[j * hc + k] - dot);
+    }
+}
+
+/* The side step on double inputs (any hc), the casts applied when rnd = 1.
+ * x [n, hc, d], pre_mix [n, hc], f [n, d], hc_fn [mix, hc*d], hc_scale [3],
+ * hc_base [mix], norm_w [d] -> h_norm [n, d], y [n, hc, d], pre, post [n, hc],
+ * comb [n, hc, hc]. */
+int hco_side_f64(const double *x, const double *pre_mix, const double *f, const double *hc_fn,
+                 const double *hc_scale, const double *hc_base, const double *norm_w, int64_t n,
+                 int hc, int d, int iters, double eps, double norm_eps, int rnd, double *h_norm,
+                 double *y, double *pre, double *post, double *comb)
+{
+    if (n < 0 || hc <= 0 || hc > 64 || d <= 0 || iters < 1)
+        return HCO_EINVAL;
+    const int mix = (2 + hc) * hc, q = hc * hc;
+    const int64_t K = (int64_t)hc * d;
+    double *m = malloc(sizeof(double) * mix), *S = malloc(sizeof(double) * q),
+           *P = malloc(sizeof(double) * (size_t)(2 * iters) * q), *h = malloc(sizeof(double) * d);
+    if (!m || !S || !P || !h) {
+        free(m); free(S); free(P); free(h);
+        return HCO_ENOMEM;
+    }
+    for (int64_t t = 0; t < n; ++t) {
+        const double *xt = x + t * K;
+        double ss = 0.0;
+        for (int64_t k = 0; k < K; ++k)
+            ss += xt[k] * xt[k];
+        const double r = 1.0 / sqrt(ss / (double)K + norm_eps);
+        for (int i = 0; i < mix; ++i) {
+            double acc = 0.0;
+            for (int64_t k = 0; k < K; ++k)
+                acc += xt[k] * hc_fn[i * K + k];
+            m[i] = acc * r;
+        }
+        for (int j = 0; j < hc; ++j) {
+            pre[t * hc + j] = sigmoid(m[j] * hc_scale[0] + hc_base[j]) + eps;
+            post[t * hc + j] = 2.0 * sigmoid(m[hc + j] * hc_scale[1] + hc_base[hc + j]);
+        }
+        double L[64 * 64];
+        for (int i = 0; i < q; ++i)
+            L[i] = m[2 * hc + i] * hc_scale[2] + hc_base[2 * hc + i];
+        sinkhorn_ckpt(L, hc, iters, eps, S, P);
+        memcpy(comb + t * q, P + (size_t)(2 * iters - 1) * q, sizeof(double) * q);
+        double sh = 0.0;
+        for (int c = 0; c < d; ++c) {
+            double acc = 0.0;
+            for (int s = 0; s < hc; ++s)
+                acc += pre_mix[t * hc + s] * xt[(int64_t)s * d + c];
+            h[c] = rnd_bf16(acc, rnd);
+            sh += h[c] * h[c];
+        }
+        const double rs = 1.0 / sqrt(sh / (double)d + norm_eps);
+        for (int c = 0; c < d; ++c)
+            h_norm[t * d + c] = rnd_bf16((h[c] * rs) * norm_w[c], rnd);
+        for (int k = 0; k < hc; ++k)
+            for (int c = 0; c < d; ++c) {
+                double acc = post[t * hc + k] * f[t * d + c];
+                for (int j = 0; j < hc; ++j)
+                    acc += comb[t * q + j * hc + k] * xt[(int64_t)j * d + c];
+                y[(t * hc + k) * d + c] = rnd_bf16(acc, rnd);
+            }
+    }
+    free(m); free(S); free(P); free(h);
+    return HCO_OK;
+}
+
+/* The backward of hco_side_f64.  Upstream gradients g_hn [n, d], g_y
+ * [n, hc, d], g_pre [n, hc] (NULL: zero).  Out: g_x [n, hc, d], g_pm [n, hc],
+ * g_f [n, d] per token; g_fn [mix, hc*d], g_scale [3], g_base [mix], g_w [d]
+ * summed over the tokens. */
+int hco_side_backward_f64(const double *x, const double *pre_mix, const double *f,
+                          const double *hc_fn, const double *hc_scale, const double *hc_base,
+                          const double *norm_w, int64_t n, int hc, int d, int iters, double eps,
+                          double norm_eps, const double *g_hn, const double *g_y,
+                          const double *g_pre, int rnd, double *g_x, double *g_pm, double *g_f,
+                          double *g_fn, double *g_scale, double *g_base, double *g_w)
+{
+    if (n < 0 || hc <= 0 || hc > 64 || d <= 0 || iters < 1)
+        return HCO_EINVAL;
+    const int mix = (2 + hc) * hc, q = hc * hc;
+    const int64_t K = (int64_t)hc * d;
+    double *a = malloc(sizeof(double) * mix), *m = malloc(sizeof(double) * mix),
+           *gm = malloc(sizeof(double) * mix), *S = malloc(sizeof(double) * q),
+           *P = malloc(sizeof(double) * (size_t)(2 * iters) * q), *h = malloc(sizeof(double) * d),
+           *gh = malloc(sizeof(double) * d), *pre = malloc(sizeof(double) * hc),
+           *post = malloc(sizeof(double) * hc), *gpost = malloc(sizeof(double) * hc),
+           *gcomb = malloc(sizeof(double) * q), *gL = malloc(sizeof(double) * q);
+    if (!a || !m || !gm || !S || !P || !h || !gh || !pre || !post || !gpost || !gcomb || !gL) {
+        free(a); free(m); free(gm); free(S); free(P); free(h); free(gh); free(pre); free(post);
+        free(gpost); free(gcomb); free(gL);
+        return HCO_ENOMEM;
+    }
+    memset(g_fn, 0, sizeof(double) * (size_t)mix * (size_t)K);
+    memset(g_scale, 0, sizeof(double) * 3);
+    memset(g_base, 0, sizeof(double) * mix);
+    memset(g_w, 0, sizeof(double) * d);
+    for (int64_t t = 0; t < n; ++t) {
+        const double *xt = x + t * K;
+        double *gxt = g_x + t * K;
+        /* forward, as hco_side_f64 */
+        double ss = 0.0;
+        for (int64_t k = 0; k < K; ++k)
+            ss += xt[k] * xt[k];
+        const double r = 1.0 / sqrt(ss / (double)K + norm_eps);
+        for (int i = 0; i < mix; ++i) {
+            double acc = 0.0;
+            for (int64_t k = 0; k < K; ++k)
+                acc += xt[k] * hc_fn[i * K + k];
+            a[i] = acc;
+            m[i] = acc * r;
+        }
+        double L[64 * 64];
+        for (int i = 0; i < q; ++i)
+            L[i] = m[2 * hc + i] * hc_scale[2] + hc_base[2 * hc + i];
+        sinkhorn_ckpt(L, hc, iters, eps, S, P);
+        const double *comb = P + (size_t)(2 * iters - 1) * q;
+        for (int j = 0; j < hc; ++j)
+            post[j] = 2.0 * sigmoid(m[hc + j] * hc_scale[1] + hc_base[hc + j]);
+        double sh = 0.0;
+        for (int c = 0; c < d; ++c) {
+            double acc = 0.0;
+            for (int s = 0; s < hc; ++s)
+                acc += pre_mix[t * hc + s] * xt[(int64_t)s * d + c];
+            h[c] = rnd_bf16(acc, rnd);
+            sh += h[c] * h[c];
+        }
+        const double rs = 1.0 / sqrt(sh / (double)d + norm_eps);
+        /* a6: y_k = post_k f + sum_j comb[j][k] x_j */
+        for (int k = 0; k < hc; ++k) {
+            gpost[k] = 0.0;
+            for (int c = 0; c < d; ++c)
+                gpost[k] += f[t * d + c] * g_y[(t * hc + k) * d + c];
+        }
+        for (int j = 0; j < hc; ++j)
+            for (int k = 0; k < hc; ++k) {
+                double acc = 0.0;
+                for (int c = 0; c < d; ++c)
+                    acc += xt[(int64_t)j * d + c] * g_y[(t * hc + k) * d + c];
+                gcomb[j * hc + k] = acc;
+            }
+        for (int c = 0; c < d; ++c) {
+            double acc = 0.0;
+            for (int k = 0; k < hc; ++k)
+                acc += post[k] * g_y[(t * hc + k) * d + c];
+            g_f[t * d + c] = acc;
+        }
+        for (int j = 0; j < hc; ++j)
+            for (int c = 0; c < d; ++c) {
+                double acc = 0.0;
+                for (int k = 0; k < hc; ++k)
+                    acc += comb[j * hc + k] * g_y[(t * hc + k) * d + c];
+                gxt[(int64_t)j * d + c] = acc;
+            }
+        /* a5: h_norm = (h * rs) * w, rs = 1/sqrt(sum h^2 / d + eps) */
+        double T = 0.0;
+        for (int c = 0; c < d; ++c) {
+            const double gu = norm_w[c] * g_hn[t * d + c];
+            g_w[c] += (h[c] * rs) * g_hn[t * d + c];
+            gh[c] = gu;
+            T += h[c] * gu;
+        }
+        for (int c = 0; c < d; ++c)
+            gh[c] = rs * gh[c] - rs * rs * rs / (double)d * h[c] * T;
+        /* a4: h = sum_s pre_mix[s] x_s */
+        for (int s = 0; s < hc; ++s) {
+            double acc = 0.0;
+            for (int c = 0; c < d; ++c) {
+                acc += xt[(int64_t)s * d + c] * gh[c];
+                gxt[(int64_t)s * d + c] += pre_mix[t * hc + s] * gh[c];
+            }
+            g_pm[t * hc + s] = acc;
+        }
+        /* a2-a3: pre, post, comb from m */
+        for (int j = 0; j < hc; ++j) {
+            const double sp = sigmoid(m[j] * hc_scale[0] + hc_base[j]);
+            const double gz = (g_pre ? g_pre[t * hc + j] : 0.0) * sp * (1.0 - sp);
+            gm[j] = gz * hc_scale[0];
+            g_scale[0] += gz * m[j];
+            g_base[j] += gz;
+            const double sq = sigmoid(m[hc + j] * hc_scale[1] + hc_base[hc + j]);
+            const double gq = gpost[j] * 2.0 * sq * (1.0 - sq);
+            gm[hc + j] = gq * hc_scale[1];
+            g_scale[1] += gq * m[hc + j];
+            g_base[hc + j] += gq;
+        }
+        sinkhorn_back(S, P, hc, iters, eps, gcomb, gL);
+        for (int i = 0; i < q; ++i) {
+            gm[2 * hc + i] = gL[i] * hc_scale[2];
+            g_scale[2] += gL[i] * m[2 * hc + i];
+            g_base[2 * hc + i] += gL[i];
+        }
+        /* a1: m = a * r, a = x . hc_fn^T, r = 1/sqrt(sum x^2 / K + norm_eps) */
+        double gr = 0.0;
+        for (int i = 0; i < mix; ++i)
+            gr += gm[i] * a[i];
+        const double cr = -gr * r * r * r / (double)K;
+        for (int64_t k = 0; k < K; ++k) {
+            double acc = cr * xt[k];
+            for (int i = 0; i < mix; ++i)
+                acc += gm[i] * r * hc_fn[i * K + k];
+            gxt[k] += acc;
+        }
+        for (int i = 0; i < mix; ++i) {
+            const double ga = gm[i] * r;
+            for (int64_t k = 0; k < K; ++k)
+                g_fn[i * K + k] += ga * xt[k];
+        }
+    }
+    free(a); free(m); free(gm); free(S); free(P); free(h); free(gh); free(pre); free(post);
+    free(gpost); free(gcomb); free(gL);
+    return HCO_OK;
+}

@@ -21,7 +21,7 @@ MUTANTS = {
                           "for (int64_t k = 0; k < d; ++k) {\n            double v = hco_bf16_to_double(xt[k]);\n            ss += v * v;"),
     "rsqrt_divides": ("mixes[t * mix + i] = acc * r;", "mixes[t * mix + i] = acc / r;"),
     "pre_no_eps": ("sigmoid(m[j] * s0 + (double)hc_base[j]) + eps;", "sigmoid(m[j] * s0 + (double)hc_base[j]);"),
-    "post_not_doubled": ("post[t * hc + j] = 2.0 * sigmoid", "post[t * hc + j] = sigmoid"),
+    "post_not_doubled": ("post[t * hc + j] = 2.0 * sigmoid(m[hc + j] * s1", "post[t * hc + j] = sigmoid(m[hc + j] * s1"),
     "post_wrong_scale": ("2.0 * sigmoid(m[hc + j] * s1", "2.0 * sigmoid(m[hc + j] * s0"),
     "comb_transposed_read": ("int i = 2 * hc + j * hc + k;", "int i = 2 * hc + k * hc + j;"),
     "softmax_eps_inside": ("c[j * hc + k] = c[j * hc + k] / s + eps;", "c[j * hc + k] = c[j * hc + k] / (s + eps);"),
@@ -48,6 +48,14 @@ MUTANTS = {
     "mx_scale_bias": ("scales[t * groups + g] = (uint8_t)(ex + 127);", "scales[t * groups + g] = (uint8_t)(ex + 128);"),
     "e4m3_two_mantissa_bits": ("double ulp = ldexp(1.0, ex - 3); /* 3 mantissa bits */",
                                "double ulp = ldexp(1.0, ex - 2); /* 3 mantissa bits */"),
+    "bwd_no_rs3_term": ("gh[c] = rs * gh[c] - rs * rs * rs / (double)d * h[c] * T;", "gh[c] = rs * gh[c];"),
+    "bwd_sigmoid_derivative": ("const double gq = gpost[j] * 2.0 * sq * (1.0 - sq);",
+                               "const double gq = gpost[j] * 2.0 * sq;"),
+    "bwd_sinkhorn_step_no_projection": ("g[idx] = (g[idx] - dot) / (s + eps);", "g[idx] = g[idx] / (s + eps);"),
+    "bwd_no_statistic_term": ("const double cr = -gr * r * r * r / (double)K;", "const double cr = 0.0;"),
+    "bwd_softmax_not_centred": ("gL[j * hc + k] = S[j * hc + k] * (g[j * hc + k] - dot);",
+                                "gL[j * hc + k] = S[j * hc + k] * g[j * hc + k];"),
+    "bwd_norm_w_unnormalised": ("g_w[c] += (h[c] * rs) * g_hn[t * d + c];", "g_w[c] += h[c] * g_hn[t * d + c];"),
     "e4m3_subnormal_threshold": ("    if (ex < -6)\n        ex = -6; /* subnormals share",
                                  "    if (ex < -7)\n        ex = -7; /* subnormals share"),
 }
@@ -118,7 +126,7 @@ def test_mutant_is_caught(name, tmpdir_mut):
         lib = ctypes.CDLL(so_path)
         for attr in ("hco_bf16_to_double", "hco_bf16_from_double", "hco_mixes", "hco_split_sinkhorn",
                      "hco_pre", "hco_rmsnorm", "hco_post", "hco_block_step", "hco_e4m3_from_double",
-                     "hco_mxfp8"):
+                     "hco_mxfp8", "hco_side_f64", "hco_side_backward_f64"):
             f, g = getattr(lib, attr), getattr(real, attr)
             f.argtypes, f.restype = g.argtypes, g.restype
         oracle._lib = lib

@@ -625,3 +625,77 @@ def test_hc8_pre_and_post_match_numpy():
     ref = post[:, :, None] * oracle.bf16_to_f64(f)[:, None, :] + np.einsum("tjk,tjd->tkd", comb, xf)
     diff = np.abs(got.astype(np.int32) - oracle.bf16_from_f64(ref).astype(np.int32))
     assert diff.max() <= 1 and np.mean(diff) < 1e-3
+
+
+# --------------------------------------------------- f3: the side step backward
+# The pages give no backward; the oracle's is the derivative of a1-a6.  Pinned
+# by central finite differences of the (separately pinned) forward, with the
+# bf16 casts switched off so that the forward is smooth.
+
+def test_side_f64_with_casts_equals_block_step():
+    case = inputs.tiny(n=3, d=64, seed=31)
+    p = case.params[0]
+    xb, fb = oracle.bf16_bits(case.x), oracle.bf16_bits(case.fs[0])
+    pm = case.pre_mix.numpy().astype(np.float64)
+    ref = oracle.block_step(xb, pm, fb, *(t.numpy() for t in p.astuple()))
+    got = oracle.side_f64(oracle.bf16_to_f64(xb), pm, oracle.bf16_to_f64(fb),
+                          *(t.numpy().astype(np.float64) for t in p.astuple()), rounded=True)
+    assert np.array_equal(got["h_norm"], oracle.bf16_to_f64(ref["h_norm"]))
+    assert np.array_equal(got["y"], oracle.bf16_to_f64(ref["y"]))
+    for k in ("pre", "post", "comb"):
+        assert np.array_equal(got[k], ref[k])
+
+
+def _bwd_case(rng, n, hc, d):
+    mix = (2 + hc) * hc
+    return dict(x=rng.standard_normal((n, hc, d)), pre_mix=rng.uniform(0.1, 1.0, (n, hc)),
+                f=rng.standard_normal((n, d)), hc_fn=rng.standard_normal((mix, hc * d)) * 0.3,
+                hc_scale=rng.uniform(0.5, 2.0, 3), hc_base=rng.standard_normal(mix),
+                norm_w=rng.uniform(0.5, 1.5, d))
+
+
+@pytest.mark.parametrize("hc", [2, 4])
+@pytest.mark.parametrize("iters,eps", [(1, 1e-6), (3, 0.05), (20, 1e-6)])
+def test_side_backward_matches_finite_differences(hc, iters, eps):
+    rng = np.random.default_rng(1000 + 10 * hc + iters)
+    n, d = 2, 8
+    inp = _bwd_case(rng, n, hc, d)
+    g_hn, g_y, g_pre = rng.standard_normal((n, d)), rng.standard_normal((n, hc, d)), rng.standard_normal((n, hc))
+
+    def loss(v):
+        o = oracle.side_f64(**v, iters=iters, eps=eps, norm_eps=1e-6, rounded=False)
+        return float(np.sum(o["h_norm"] * g_hn) + np.sum(o["y"] * g_y) + np.sum(o["pre"] * g_pre))
+
+    grads = oracle.side_backward(**inp, g_h_norm=g_hn, g_y=g_y, g_pre=g_pre, iters=iters, eps=eps,
+                                 norm_eps=1e-6, rounded=False)
+    names = {"x": "g_x", "pre_mix": "g_pre_mix", "f": "g_f", "hc_fn": "g_hc_fn",
+             "hc_scale": "g_hc_scale", "hc_base": "g_hc_base", "norm_w": "g_norm_w"}
+    for name, gname in names.items():
+        flat = inp[name].reshape(-1)
+        picks = rng.choice(flat.size, size=min(flat.size, 8), replace=False)
+        for i in picks:
+            h = 1e-5 * max(1.0, abs(flat[i]))
+            up, dn = {k: v.copy() for k, v in inp.items()}, {k: v.copy() for k, v in inp.items()}
+            up[name].reshape(-1)[i] += h
+            dn[name].reshape(-1)[i] -= h
+            fd = (loss(up) - loss(dn)) / (2 * h)
+            got = grads[gname].reshape(-1)[i]
+            assert abs(got - fd) <= 1e-6 * max(1.0, abs(fd)), (name, int(i), got, fd)
+
+
+def test_side_backward_casts_enter_only_through_h():
+    # With pre_mix one-hot and x bf16-representable, h = x_s is exactly a bf16
+    # value, so casting h changes nothing; the backward never reads h_norm or y
+    # themselves, so the rounded and unrounded backward are then identical.
+    rng = np.random.default_rng(77)
+    n, hc, d = 3, 4, 16
+    inp = _bwd_case(rng, n, hc, d)
+    inp["x"] = oracle.bf16_to_f64(oracle.bf16_from_f64(inp["x"]))
+    inp["pre_mix"] = np.zeros((n, hc))
+    inp["pre_mix"][:, 2] = 1.0
+    g = dict(g_h_norm=rng.standard_normal((n, d)), g_y=rng.standard_normal((n, hc, d)),
+             g_pre=rng.standard_normal((n, hc)))
+    a = oracle.side_backward(**inp, **g, rounded=True)
+    b = oracle.side_backward(**inp, **g, rounded=False)
+    for k in a:
+        assert np.array_equal(a[k], b[k]), k
