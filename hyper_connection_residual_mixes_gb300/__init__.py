@@ -20,7 +20,8 @@ from . import _lib
 from ._lib import HcError
 
 __all__ = ["hc_mixes", "hc_split_sinkhorn", "hc_pre_norm", "hc_post", "hc_block_step",
-           "hc_chain_begin", "hc_chain_side", "hc_mxfp8_cast", "hc_pre_norm_mxfp8", "STATE_FLOATS",
+           "hc_chain_begin", "hc_chain_side", "hc_mxfp8_cast", "hc_pre_norm_mxfp8",
+           "hc_block_step_backward", "STATE_FLOATS",
            "HcError", "library_path", "version"]
 
 HC_EPS = 1e-6
@@ -129,6 +130,46 @@ def hc_pre_norm(x, pre_mix, norm_w, norm_eps=NORM_EPS, out=None, stream=None):
     with torch.cuda.device(dev):
         _lib.call("hc_pre_norm", _ptr(x), _ptr(pre_mix), _ptr(norm_w), n, hc, d, norm_eps,
                   _ptr(out), _stream(stream))
+    return out
+
+
+def hc_block_step_backward(x, pre_mix, f, hc_fn, hc_scale, hc_base, norm_w, g_h_norm, g_y,
+                           g_pre=None, sinkhorn_iters=SINKHORN_ITERS, eps=HC_EPS, norm_eps=NORM_EPS,
+                           workspace=None, stream=None):
+    """The backward of hc_block_step (fp32 gradients): returns a dict of
+    g_x [..., hc, d], g_pre_mix [..., hc], g_f [..., d] and the parameter
+    gradients g_hc_fn, g_hc_scale, g_hc_base, g_norm_w summed over tokens.
+    workspace: a uint8 device tensor of at least the size the library asks
+    for (allocated here when None)."""
+    _check(x, "x", torch.bfloat16)
+    dev = x.device
+    hc, d = x.shape[-2], x.shape[-1]
+    lead = tuple(x.shape[:-2])
+    n = x.numel() // (hc * d) if x.numel() else 0
+    for t, nm, dt in ((pre_mix, "pre_mix", torch.float32), (f, "f", torch.bfloat16),
+                      (hc_fn, "hc_fn", torch.float32), (hc_scale, "hc_scale", torch.float32),
+                      (hc_base, "hc_base", torch.float32), (norm_w, "norm_w", torch.float32),
+                      (g_h_norm, "g_h_norm", torch.float32), (g_y, "g_y", torch.float32)):
+        _check(t, nm, dt, dev)
+    if g_pre is not None:
+        _check(g_pre, "g_pre", torch.float32, dev)
+    out = dict(g_x=torch.empty(tuple(x.shape), dtype=torch.float32, device=dev),
+               g_pre_mix=torch.empty(lead + (hc,), dtype=torch.float32, device=dev),
+               g_f=torch.empty(lead + (d,), dtype=torch.float32, device=dev),
+               g_hc_fn=torch.empty(tuple(hc_fn.shape), dtype=torch.float32, device=dev),
+               g_hc_scale=torch.empty(3, dtype=torch.float32, device=dev),
+               g_hc_base=torch.empty(tuple(hc_base.shape), dtype=torch.float32, device=dev),
+               g_norm_w=torch.empty(d, dtype=torch.float32, device=dev))
+    need = _lib.load().hc_block_step_backward_workspace_bytes(n, hc, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        _lib.call("hc_block_step_backward", _ptr(x), _ptr(pre_mix), _ptr(f), _ptr(hc_fn),
+                  _ptr(hc_scale), _ptr(hc_base), _ptr(norm_w), n, hc, d, sinkhorn_iters, eps,
+                  norm_eps, _ptr(g_h_norm), _ptr(g_y), _ptr(g_pre),
+                  *(_ptr(out[k]) for k in ("g_x", "g_pre_mix", "g_f", "g_hc_fn", "g_hc_scale",
+                                           "g_hc_base", "g_norm_w")),
+                  _ptr(workspace), workspace.numel(), _stream(stream))
     return out
 
 

@@ -32,6 +32,9 @@ SIGNATURES = {
     "hc_split_sinkhorn": [P, P, P, I64, I32, I32, F32, P, P, P, P],
     "hc_pre_norm": [P, P, P, I64, I32, I32, F32, P, P],
     "hc_mxfp8_cast": [P, I64, I32, P, P, P],
+    "hc_block_step_backward_workspace_bytes": [I64, I32, I32],
+    "hc_block_step_backward": [P, P, P, P, P, P, P, I64, I32, I32, I32, F32, F32, P, P, P,
+                               P, P, P, P, P, P, P, P, ctypes.c_size_t, P],
     "hc_pre_norm_mxfp8": [P, P, P, I64, I32, I32, F32, P, P, P, P],
     "hc_post": [P, P, P, P, I64, I32, I32, P, P],
     "hc_block_step": [P, P, P, P, P, P, P, I64, I32, I32, I32, F32, F32, P, P, P, P, P, P],
@@ -73,6 +76,7 @@ def load():
             fn.argtypes = argtypes
             fn.restype = I32
         lib.hc_status_string.restype = ctypes.c_char_p
+        lib.hc_block_step_backward_workspace_bytes.restype = ctypes.c_size_t
         _lib = lib
         return lib
 

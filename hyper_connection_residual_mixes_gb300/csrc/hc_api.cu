@@ -161,6 +161,49 @@ hc_status hc_pre_norm(const uint16_t *x, const float *pre_mix, const float *norm
     return cuda_status(hc::launch_pre_norm(x, pre_mix, norm_w, n, hc, d, norm_eps, out, stream));
 }
 
+size_t hc_block_step_backward_workspace_bytes(int64_t n, int hc, int d) {
+    if (check_shape(n, hc, d, true) != HC_OK || hc != 4) return 0;
+    return hc::backward_workspace_bytes(n, d);
+}
+
+hc_status hc_block_step_backward(const uint16_t *x, const float *pre_mix, const uint16_t *f,
+                                 const float *hc_fn, const float *hc_scale, const float *hc_base,
+                                 const float *norm_w, int64_t n, int hc, int d, int sinkhorn_iters,
+                                 float eps, float norm_eps, const float *g_h_norm, const float *g_y,
+                                 const float *g_pre, float *g_x, float *g_pre_mix, float *g_f,
+                                 float *g_hc_fn, float *g_hc_scale, float *g_hc_base,
+                                 float *g_norm_w, void *workspace, size_t workspace_bytes,
+                                 cudaStream_t stream) {
+    hc_status st = check_shape(n, hc, d, true);
+    if (st != HC_OK) return st;
+    if (hc != 4) return HC_ERR_UNSUPPORTED;
+    if (sinkhorn_iters < 1 || sinkhorn_iters > 128 || !finite_nonneg(eps) || !finite_nonneg(norm_eps))
+        return HC_ERR_INVALID_ARG;
+    if (n == 0) return HC_OK;
+    if (!x || !pre_mix || !f || !hc_fn || !hc_scale || !hc_base || !norm_w || !g_h_norm || !g_y ||
+        !g_x || !g_pre_mix || !g_f || !g_hc_fn || !g_hc_scale || !g_hc_base || !g_norm_w || !workspace)
+        return HC_ERR_INVALID_ARG;
+    if (workspace_bytes < hc::backward_workspace_bytes(n, d)) return HC_ERR_INVALID_ARG;
+    const void *ptrs[] = {x, pre_mix, f, hc_fn, hc_scale, hc_base, norm_w, g_h_norm, g_y, g_x,
+                          g_pre_mix, g_f, g_hc_fn, g_hc_scale, g_hc_base, g_norm_w, workspace};
+    for (const void *p : ptrs)
+        if (!aligned16(p)) return HC_ERR_MISALIGNED;
+    if (g_pre && !aligned16(g_pre)) return HC_ERR_MISALIGNED;
+    const int64_t mix = (int64_t)(2 + hc) * hc, K = (int64_t)hc * d;
+    const Span ins[] = {span(x, n * K * 2), span(pre_mix, n * hc * 4), span(f, n * d * 2),
+                        span(hc_fn, mix * K * 4), span(hc_scale, 12), span(hc_base, mix * 4),
+                        span(norm_w, d * 4), span(g_h_norm, n * d * 4), span(g_y, n * K * 4),
+                        span(g_pre, g_pre ? n * hc * 4 : 0)};
+    const Span outs[] = {span(g_x, n * K * 4), span(g_pre_mix, n * hc * 4), span(g_f, n * d * 4),
+                         span(g_hc_fn, mix * K * 4), span(g_hc_scale, 12), span(g_hc_base, mix * 4),
+                         span(g_norm_w, d * 4), span(workspace, (int64_t)workspace_bytes)};
+    if ((st = check_alias(outs, 8, ins, 10)) != HC_OK) return st;
+    return cuda_status(hc::launch_block_step_backward(
+        x, pre_mix, f, hc_fn, hc_scale, hc_base, norm_w, n, d, sinkhorn_iters, eps, norm_eps,
+        g_h_norm, g_y, g_pre, g_x, g_pre_mix, g_f, g_hc_fn, g_hc_scale, g_hc_base, g_norm_w,
+        workspace, stream));
+}
+
 hc_status hc_mxfp8_cast(const uint16_t *in, int64_t rows, int d, uint8_t *codes, uint8_t *scales,
                         cudaStream_t stream) {
     if (rows < 0 || d <= 0) return HC_ERR_INVALID_ARG;

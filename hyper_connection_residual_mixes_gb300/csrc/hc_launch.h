@@ -33,6 +33,16 @@ cudaError_t launch_tokens_simple(const uint16_t *x, const float *pre_mix, const 
                                  float *post_out, float *comb_out, float *mixes_out,
                                  cudaStream_t s);
 
+// The backward of one side step (hc_backward.cu), hc == 4.
+size_t backward_workspace_bytes(int64_t n, int d);
+cudaError_t launch_block_step_backward(const uint16_t *x, const float *pre_mix, const uint16_t *f,
+                                       const float *hc_fn, const float *hc_scale,
+                                       const float *hc_base, const float *norm_w, int64_t n, int d,
+                                       int iters, float eps, float norm_eps, const float *g_hn,
+                                       const float *g_y, const float *g_pre, float *g_x,
+                                       float *g_pm, float *g_f, float *g_fn, float *g_scale,
+                                       float *g_base, float *g_w, void *workspace, cudaStream_t s);
+
 // The fused persistent-cluster path (hc_block_cluster.cu).  Supported when d
 // is a multiple of 1024 and one stream's weight fragments fit a tensor-memory
 // quadrant (d <= 7168).  With f == nullptr it computes a1-a3 only.

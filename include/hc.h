@@ -156,6 +156,36 @@ hc_status hc_block_step(const uint16_t *x, const float *pre_mix, const uint16_t 
                         cudaStream_t stream);
 
 /*
+ * The backward of one side step a1-a6 (hc = 4).  The pages give no backward
+ * pass; this is the derivative of hc_block_step's definition (Block page,
+ * Code section; "Stream combination" page), with the three bf16 casts (h,
+ * h_norm, y) passing gradients through unchanged (as a dtype cast does in
+ * autograd) and the forward's rounded h used where the forward used it.
+ * Every gradient tensor is fp32.
+ *   x, pre_mix, f, hc_fn, hc_scale, hc_base, norm_w as hc_block_step     in
+ *   g_h_norm [n, d], g_y [n, hc, d]: the gradients of h_norm and y        in
+ *   g_pre [n, hc]: the gradient of pre (the next side's pre_mix); NULL: 0 in
+ *   g_x [n, hc, d], g_pre_mix [n, hc], g_f [n, d]                        out
+ *   g_hc_fn [mix, hc*d], g_hc_scale [3], g_hc_base [mix], g_norm_w [d]:
+ *   summed over the n tokens (overwritten, not accumulated)             out
+ *   workspace: device scratch of at least
+ *   hc_block_step_backward_workspace_bytes(n, hc, d) bytes, 16-byte
+ *   aligned, owned by the caller (the library allocates nothing)
+ * Results are deterministic: the token sums run in a fixed order.
+ * sinkhorn_iters must be in [1, 128] (HC_ERR_INVALID_ARG otherwise).
+ */
+size_t hc_block_step_backward_workspace_bytes(int64_t n, int hc, int d);
+
+hc_status hc_block_step_backward(const uint16_t *x, const float *pre_mix, const uint16_t *f,
+                                 const float *hc_fn, const float *hc_scale, const float *hc_base,
+                                 const float *norm_w, int64_t n, int hc, int d, int sinkhorn_iters,
+                                 float eps, float norm_eps, const float *g_h_norm, const float *g_y,
+                                 const float *g_pre, float *g_x, float *g_pre_mix, float *g_f,
+                                 float *g_hc_fn, float *g_hc_scale, float *g_hc_base,
+                                 float *g_norm_w, void *workspace, size_t workspace_bytes,
+                                 cudaStream_t stream);
+
+/*
  * The MXFP8 cast (DeepSeek V4.1 Flash diagram, block "Cast to MXFP8"): the
  * rounding the released code runs in front of every FP8/FP4-weight
  * projection, here for the sublayer input h_norm.  The channels of a row are

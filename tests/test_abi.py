@@ -240,3 +240,41 @@ def test_pre_norm_mxfp8_validation(lib, kw, expect):
 def test_pre_norm_mxfp8_empty_is_ok(lib):
     assert _pnq(n=0) == 0
     assert _pnq(n=0, h_norm=FAKE2 * 0x300) == 0
+
+
+def _bwd(**kw):
+    a = dict(x=FAKE, pm=FAKE + 0x100000, f=FAKE + 0x200000, fn=FAKE + 0x300000, sc=FAKE + 0x400000,
+             base=FAKE + 0x500000, w=FAKE + 0x600000, n=16, hc=4, d=5120, iters=20, eps=1e-6,
+             norm_eps=1e-20, g_hn=FAKE + 0x700000, g_y=FAKE + 0x800000, g_pre=None,
+             g_x=FAKE2 * 0x100, g_pm=FAKE2 * 0x200, g_f=FAKE2 * 0x300, g_fn=FAKE2 * 0x400,
+             g_sc=FAKE2 * 0x500, g_base=FAKE2 * 0x600, g_w=FAKE2 * 0x700, ws=FAKE2 * 0x800,
+             ws_bytes=1 << 30, stream=None)
+    a.update(kw)
+    return _lib.raw("hc_block_step_backward", a["x"], a["pm"], a["f"], a["fn"], a["sc"], a["base"],
+                    a["w"], a["n"], a["hc"], a["d"], a["iters"], a["eps"], a["norm_eps"], a["g_hn"],
+                    a["g_y"], a["g_pre"], a["g_x"], a["g_pm"], a["g_f"], a["g_fn"], a["g_sc"],
+                    a["g_base"], a["g_w"], a["ws"], a["ws_bytes"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(hc=2), 2),                         # the backward is compiled for four streams
+    (dict(hc=3), 2),
+    (dict(iters=0), 1),
+    (dict(iters=129), 1),
+    (dict(ws=None), 1),
+    (dict(ws_bytes=1000), 1),                # smaller than the library asks for
+    (dict(g_x=None), 1),
+    (dict(g_pre=FAKE2 * 0x900 + 4), 3),
+    (dict(g_f=FAKE + 0x200000 + 64), 4),     # g_f overlaps f
+    (dict(n=-1), 1),
+])
+def test_block_step_backward_validation(lib, kw, expect):
+    assert _bwd(**kw) == expect
+
+
+def test_block_step_backward_workspace_size(lib):
+    f = lib.hc_block_step_backward_workspace_bytes
+    assert f(0, 4, 5120) >= 0
+    assert f(1000, 4, 5120) > f(10, 4, 5120) > 0
+    assert f(16, 2, 5120) == 0 and f(16, 4, 100) == 0
+    assert _bwd(n=0) == 0

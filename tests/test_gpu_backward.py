@@ -1,0 +1,133 @@
+"""GPU: the side step's backward (hc_block_step_backward) against the CPU
+oracle's (oracle.side_backward, fp64, with the forward's bf16 casts applied
+and gradients passed through them unchanged).
+
+Tolerances.  Per-token gradients (g_x, g_f, g_pre_mix) come from fp32 sums of
+up to hc*d = 20,480 products, some of which cancel (the RMSNorm statistic's
+term against the direct one), and a fp32 Sinkhorn backward of 40 steps:
+|err| <= RTOL_TOK * |ref| + ATOL * max|ref|.  The parameter gradients are fp32
+sums over all tokens: |err| <= RTOL_PAR * |ref| + ATOL * max|ref|.
+
+The backward also reads the forward's bf16 h.  Where the GPU's fp32 sum of
+pre_mix * x and the oracle's fp64 sum round to different bf16 neighbours (one
+element in about 30,000), h differs by one bf16 ulp there and that token's
+term of g_norm_w moves by 2^-8 of itself.  The main tests draw pre_mix from
+powers of two, which makes the sum exact in fp32 (four bf16 products), so no
+such flip can occur and every gradient is held to the bounds above;
+test_backward_general_pre_mix keeps general pre_mix values and gives g_norm_w
+an allowance of a few such flips per column."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import hyper_connection_residual_mixes_gb300 as hcg
+from hyper_connection_residual_mixes_gb300 import _lib, inputs
+from hyper_connection_residual_mixes_gb300 import build as hc_build
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda:0")
+RTOL_TOK, RTOL_PAR, ATOL = 1e-4, 1e-3, 1e-4
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    hc_build.build()
+    _lib.load()
+
+
+def _np(t):
+    return t.detach().cpu().numpy()
+
+
+def _case(seed, n, d, with_pre=True, dyadic=True):
+    case = inputs.tiny(seed=seed, n=n, d=d)
+    g = torch.Generator().manual_seed(seed + 1)
+    if dyadic:   # pre_mix in {1, 1/2, 1/4, 1/8}: the fp32 sum of pre_mix * x is exact
+        case.pre_mix.copy_(torch.exp2(-torch.randint(0, 4, tuple(case.pre_mix.shape), generator=g).float()))
+    up = dict(g_h_norm=torch.randn((n, d), generator=g), g_y=torch.randn((n, 4, d), generator=g),
+              g_pre=torch.randn((n, 4), generator=g) if with_pre else None)
+    return case, up
+
+
+def _run(case, up, iters=20):
+    p = case.params[0]
+    return hcg.hc_block_step_backward(
+        case.x.to(DEV), case.pre_mix.to(DEV), case.fs[0].to(DEV), *p.to(DEV).astuple(),
+        up["g_h_norm"].to(DEV), up["g_y"].to(DEV),
+        g_pre=up["g_pre"].to(DEV) if up["g_pre"] is not None else None, sinkhorn_iters=iters)
+
+
+def _ref(case, up, iters=20):
+    p = case.params[0]
+    return oracle.side_backward(
+        oracle.bf16_to_f64(oracle.bf16_bits(case.x)), _np(case.pre_mix).astype(np.float64),
+        oracle.bf16_to_f64(oracle.bf16_bits(case.fs[0])), *(_np(t).astype(np.float64) for t in p.astuple()),
+        _np(up["g_h_norm"]).astype(np.float64), _np(up["g_y"]).astype(np.float64),
+        None if up["g_pre"] is None else _np(up["g_pre"]).astype(np.float64), iters=iters, rounded=True)
+
+
+def _compare(got, ref, extra=None):
+    worst = {}
+    for k, r in ref.items():
+        g = _np(got[k]).astype(np.float64)
+        rt = RTOL_TOK if k in ("g_x", "g_f", "g_pre_mix") else RTOL_PAR
+        scale = np.abs(r).max()
+        err = np.abs(g - r)
+        bound = rt * np.abs(r) + ATOL * scale + (extra.get(k, 0.0) if extra else 0.0)
+        worst[k] = float((err / np.maximum(bound, 1e-300)).max())
+        assert np.all(err <= bound), "%s: worst err/bound %.3g (max err %.3g, scale %.3g)" % (
+            k, worst[k], err.max(), scale)
+    return worst
+
+
+@pytest.mark.parametrize("n,d,iters,with_pre", [(16, 5120, 20, True), (37, 1024, 20, False),
+                                                 (3, 64, 1, True), (5, 2048, 7, True)])
+def test_backward_matches_oracle(n, d, iters, with_pre):
+    case, up = _case(40 + n, n, d, with_pre)
+    got = _run(case, up, iters)
+    torch.cuda.synchronize()
+    _compare(got, _ref(case, up, iters))
+    assert _lib.raw("hc_consume_device_error", None) == 0
+
+
+def test_backward_across_token_blocks_and_repeatable():
+    """1,030 tokens: the parameter sums cross a 1,024-token block; two runs
+    give the same bits."""
+    case, up = _case(77, 1030, 256)
+    a = _run(case, up)
+    b = _run(case, up)
+    torch.cuda.synchronize()
+    for k in a:
+        assert torch.equal(a[k], b[k]), k
+    _compare(a, _ref(case, up))
+
+
+def test_backward_zero_upstream_is_zero():
+    case, up = _case(5, 8, 1024)
+    up = {k: (torch.zeros_like(v) if v is not None else None) for k, v in up.items()}
+    got = _run(case, up)
+    torch.cuda.synchronize()
+    for k, v in got.items():
+        assert torch.count_nonzero(v).item() == 0, k
+
+
+def test_backward_general_pre_mix():
+    """General pre_mix values: every gradient but g_norm_w to the same bounds;
+    g_norm_w with room for up to four one-ulp flips of h per column."""
+    case, up = _case(91, 300, 1024, dyadic=False)
+    got = _run(case, up)
+    torch.cuda.synchronize()
+    ref = _ref(case, up)
+    # the largest single term h * rs_h * g_hn of each column, from the oracle's forward
+    p = case.params[0]
+    fw = oracle.side_f64(oracle.bf16_to_f64(oracle.bf16_bits(case.x)), _np(case.pre_mix).astype(np.float64),
+                         oracle.bf16_to_f64(oracle.bf16_bits(case.fs[0])),
+                         *(_np(t).astype(np.float64) for t in p.astuple()), rounded=True)
+    w = _np(p.norm_w).astype(np.float64)
+    u = fw["h_norm"] / w                       # h * rs_h, up to the final cast
+    term = np.abs(u * _np(up["g_h_norm"]).astype(np.float64)).max(axis=0)
+    _compare(got, ref, extra={"g_norm_w": 4 * 2.0 ** -8 * term * 1.01})
