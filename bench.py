@@ -583,7 +583,8 @@ def run_op(args, local_rank):
     """One kernel of the widened rows, timed alone at the long-prefill size
     (65,536 tokens x d = 5120): the MXFP8 cast of the bf16 h_norm
     (hc_mxfp8_cast) or RMSNorm(hc_pre) with the cast in its epilogue
-    (hc_pre_norm_mxfp8).  One step is one launch over the whole batch; the
+    (hc_pre_norm_mxfp8), or the side step's backward (hc_block_step_backward,
+    its launches over the batch).  One step is one call over the whole batch; the
     inputs are larger than L2.  The oracle is timed beside it on a sample."""
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
@@ -598,6 +599,22 @@ def run_op(args, local_rank):
         fn = lambda: hcg.hc_mxfp8_cast(h, codes, scales)
         alg = n * d * 2 + n * d + n * d // 32
         what = "MXFP8 cast of bf16 rows (hc_mxfp8_cast)"
+    elif args.op == "backward":
+        del codes, scales
+        g = torch.Generator(device=dev).manual_seed(5)
+        g_hn = torch.randn((n, d), device=dev, generator=g)
+        g_y = torch.randn((n, HC, d), device=dev, generator=g)
+        g_pre = torch.randn((n, HC), device=dev, generator=g)
+        f0 = inputs.long_prefill_f(0, n, d, dev)
+        ws = torch.empty(hcg._lib.load().hc_block_step_backward_workspace_bytes(n, HC, d),
+                         dtype=torch.uint8, device=dev)
+        fn = lambda: hcg.hc_block_step_backward(case.x, case.pre_mix, f0, *p.astuple(), g_hn, g_y,
+                                                g_pre, workspace=ws)
+        # inputs x, f, pre_mix, g_h_norm, g_y, g_pre; outputs g_x, g_pre_mix, g_f; the
+        # parameters and their gradients once
+        alg = (n * (HC * d * 2 + d * 2 + HC * 4 + d * 4 + HC * d * 4 + HC * 4)
+               + n * (HC * d * 4 + HC * 4 + d * 4) + 2 * BYTES_WEIGHTS)
+        what = "the side step's backward (hc_block_step_backward)"
     else:
         fn = lambda: hcg.hc_pre_norm_mxfp8(case.x, case.pre_mix, p.norm_w, codes=codes, scales=scales)
         alg = n * HC * d * 2 + n * HC * 4 + d * 4 + n * d + n * d // 32
@@ -622,13 +639,15 @@ def run_op(args, local_rank):
     out = {"metric": "tokens/s through %s, 65,536 tokens x d = 5120" % what, "value": n / (ms / 1e3),
            "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-           "dtype": "bf16 in, fp32 arithmetic, e4m3 + ue8m0 out", "data": "synthetic, seeded",
-           "config": {"workload": "long_prefill, one side's h_norm", "op": args.op, "tokens": n, "d": d,
+           "dtype": ("bf16 + fp32 in, fp32 arithmetic, fp32 gradients out" if args.op == "backward"
+                     else "bf16 in, fp32 arithmetic, e4m3 + ue8m0 out"), "data": "synthetic, seeded",
+           "config": {"workload": ("long_prefill, one side step" if args.op == "backward"
+                                   else "long_prefill, one side's h_norm"), "op": args.op, "tokens": n, "d": d,
                       "l2": "inputs larger than L2; no flush"},
            "roofline": {"bound": "hbm", "achieved": alg / (ms / 1e3) / 1e9, "peak": peak, "unit": "GB/s",
                         "frac": alg / (ms / 1e3) / 1e9 / peak, "traffic": None,
                         "peak_source": peak_kind, "algorithmic_bytes_per_launch": alg},
-           "clocks": clk, "gpu_launches": args.steps, "e2e": None}
+           "clocks": clk, "gpu_launches": args.steps * (6 if args.op == "backward" else 1), "e2e": None}
     if not args.no_cpu_baseline:
         import oracle
         rows = torch.arange(0, n, n // 64, device=dev)
@@ -640,6 +659,13 @@ def run_op(args, local_rank):
         t0 = time.perf_counter()
         if args.op == "mxfp8_cast":
             oracle.mxfp8(hs)
+        elif args.op == "backward":
+            rows = rows[:4]
+            sel = lambda tt: tt.index_select(0, rows).cpu().numpy().astype(np.float64)
+            oracle.side_backward(oracle.bf16_to_f64(xs[:4]), pms[:4], oracle.bf16_to_f64(
+                oracle.bf16_bits(f0.index_select(0, rows).cpu())),
+                *(t.cpu().numpy().astype(np.float64) for t in p.astuple()), sel(g_hn), sel(g_y),
+                sel(g_pre))
         else:
             oracle.mxfp8(oracle.rmsnorm(oracle.pre(xs, pms), w))
         dt = time.perf_counter() - t0
@@ -664,7 +690,7 @@ def main():
                     help="with the chain, skip timing the one-launch-per-side path beside it")
     ap.add_argument("--path", choices=["chain", "step"], default="chain",
                     help="chain: the sides fused across sides (hc_chain_*); step: one hc_block_step per side")
-    ap.add_argument("--op", choices=["mxfp8_cast", "pre_norm_mxfp8"], default=None,
+    ap.add_argument("--op", choices=["mxfp8_cast", "pre_norm_mxfp8", "backward"], default=None,
                     help="time one kernel of the widened rows alone instead of the side steps")
     args = ap.parse_args()
     rank, local_rank, world = dist_env()
