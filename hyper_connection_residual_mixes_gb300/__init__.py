@@ -21,7 +21,7 @@ from ._lib import HcError
 
 __all__ = ["hc_mixes", "hc_split_sinkhorn", "hc_pre_norm", "hc_post", "hc_block_step",
            "hc_chain_begin", "hc_chain_side", "hc_mxfp8_cast", "hc_pre_norm_mxfp8",
-           "hc_block_step_backward", "STATE_FLOATS",
+           "hc_block_step_backward", "hc_block_step_backward_no_workspace", "STATE_FLOATS",
            "HcError", "library_path", "version"]
 
 HC_EPS = 1e-6
@@ -170,6 +170,32 @@ def hc_block_step_backward(x, pre_mix, f, hc_fn, hc_scale, hc_base, norm_w, g_h_
                   *(_ptr(out[k]) for k in ("g_x", "g_pre_mix", "g_f", "g_hc_fn", "g_hc_scale",
                                            "g_hc_base", "g_norm_w")),
                   _ptr(workspace), workspace.numel(), _stream(stream))
+    return out
+
+
+def hc_block_step_backward_no_workspace(x, pre_mix, f, hc_fn, hc_scale, hc_base, norm_w, g_h_norm,
+                                        g_y, g_pre=None, sinkhorn_iters=SINKHORN_ITERS, eps=HC_EPS,
+                                        norm_eps=NORM_EPS, stream=None):
+    """hc_block_step_backward with the library's own fixed scratch (no
+    workspace argument, nothing allocated by the call); same results."""
+    _check(x, "x", torch.bfloat16)
+    dev = x.device
+    hc, d = x.shape[-2], x.shape[-1]
+    lead = tuple(x.shape[:-2])
+    n = x.numel() // (hc * d) if x.numel() else 0
+    out = dict(g_x=torch.empty(tuple(x.shape), dtype=torch.float32, device=dev),
+               g_pre_mix=torch.empty(lead + (hc,), dtype=torch.float32, device=dev),
+               g_f=torch.empty(lead + (d,), dtype=torch.float32, device=dev),
+               g_hc_fn=torch.empty(tuple(hc_fn.shape), dtype=torch.float32, device=dev),
+               g_hc_scale=torch.empty(3, dtype=torch.float32, device=dev),
+               g_hc_base=torch.empty(tuple(hc_base.shape), dtype=torch.float32, device=dev),
+               g_norm_w=torch.empty(d, dtype=torch.float32, device=dev))
+    with torch.cuda.device(dev):
+        _lib.call("hc_block_step_backward_no_workspace", _ptr(x), _ptr(pre_mix), _ptr(f), _ptr(hc_fn),
+                  _ptr(hc_scale), _ptr(hc_base), _ptr(norm_w), n, hc, d, sinkhorn_iters, eps,
+                  norm_eps, _ptr(g_h_norm), _ptr(g_y), _ptr(g_pre),
+                  *(_ptr(out[k]) for k in ("g_x", "g_pre_mix", "g_f", "g_hc_fn", "g_hc_scale",
+                                           "g_hc_base", "g_norm_w")), _stream(stream))
     return out
 
 

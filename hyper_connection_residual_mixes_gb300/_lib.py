@@ -33,6 +33,8 @@ SIGNATURES = {
     "hc_pre_norm": [P, P, P, I64, I32, I32, F32, P, P],
     "hc_mxfp8_cast": [P, I64, I32, P, P, P],
     "hc_block_step_backward_workspace_bytes": [I64, I32, I32],
+    "hc_block_step_backward_no_workspace": [P, P, P, P, P, P, P, I64, I32, I32, I32, F32, F32,
+                                            P, P, P, P, P, P, P, P, P, P, P],
     "hc_block_step_backward": [P, P, P, P, P, P, P, I64, I32, I32, I32, F32, F32, P, P, P,
                                P, P, P, P, P, P, P, P, ctypes.c_size_t, P],
     "hc_pre_norm_mxfp8": [P, P, P, I64, I32, I32, F32, P, P, P, P],

@@ -204,6 +204,25 @@ hc_status hc_block_step_backward(const uint16_t *x, const float *pre_mix, const 
         workspace, stream));
 }
 
+hc_status hc_block_step_backward_no_workspace(
+    const uint16_t *x, const float *pre_mix, const uint16_t *f, const float *hc_fn,
+    const float *hc_scale, const float *hc_base, const float *norm_w, int64_t n, int hc, int d,
+    int sinkhorn_iters, float eps, float norm_eps, const float *g_h_norm, const float *g_y,
+    const float *g_pre, float *g_x, float *g_pre_mix, float *g_f, float *g_hc_fn, float *g_hc_scale,
+    float *g_hc_base, float *g_norm_w, cudaStream_t stream) {
+    hc_status st = check_shape(n, hc, d, true);
+    if (st != HC_OK) return st;
+    if (hc != 4 || hc::backward_workspace_bytes(n, d) > hc::backward_static_scratch_bytes())
+        return HC_ERR_UNSUPPORTED;
+    if (n == 0) return HC_OK;
+    void *scratch = nullptr;
+    if ((st = cuda_status(hc::backward_static_scratch(&scratch))) != HC_OK) return st;
+    return hc_block_step_backward(x, pre_mix, f, hc_fn, hc_scale, hc_base, norm_w, n, hc, d,
+                                  sinkhorn_iters, eps, norm_eps, g_h_norm, g_y, g_pre, g_x,
+                                  g_pre_mix, g_f, g_hc_fn, g_hc_scale, g_hc_base, g_norm_w, scratch,
+                                  hc::backward_static_scratch_bytes(), stream);
+}
+
 hc_status hc_mxfp8_cast(const uint16_t *in, int64_t rows, int d, uint8_t *codes, uint8_t *scales,
                         cudaStream_t stream) {
     if (rows < 0 || d <= 0) return HC_ERR_INVALID_ARG;

@@ -389,6 +389,16 @@ k_bwd_small(const float *__restrict__ ws, int64_t n, float *__restrict__ g_base,
 
 }  // namespace bw
 
+// Scratch for the backward without a caller workspace: a fixed array in
+// device memory, part of the module image, so a call allocates nothing.
+// One array per process and device: such calls must not run concurrently.
+constexpr size_t kStaticScratchBytes = size_t(64) << 20;
+static __device__ __align__(256) unsigned char g_bwd_scratch[kStaticScratchBytes];
+
+size_t backward_static_scratch_bytes() { return kStaticScratchBytes; }
+
+cudaError_t backward_static_scratch(void **ptr) { return cudaGetSymbolAddress(ptr, g_bwd_scratch); }
+
 size_t backward_workspace_bytes(int64_t n, int d) {
     const int64_t blocks = (n + bw::kTokBlock - 1) / bw::kTokBlock;
     const int64_t K = (int64_t)kHC * d;

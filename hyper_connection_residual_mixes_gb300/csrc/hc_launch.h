@@ -35,6 +35,8 @@ cudaError_t launch_tokens_simple(const uint16_t *x, const float *pre_mix, const 
 
 // The backward of one side step (hc_backward.cu), hc == 4.
 size_t backward_workspace_bytes(int64_t n, int d);
+size_t backward_static_scratch_bytes();
+cudaError_t backward_static_scratch(void **ptr);
 cudaError_t launch_block_step_backward(const uint16_t *x, const float *pre_mix, const uint16_t *f,
                                        const float *hc_fn, const float *hc_scale,
                                        const float *hc_base, const float *norm_w, int64_t n, int d,

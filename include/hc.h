@@ -176,6 +176,22 @@ hc_status hc_block_step(const uint16_t *x, const float *pre_mix, const uint16_t 
  */
 size_t hc_block_step_backward_workspace_bytes(int64_t n, int hc, int d);
 
+/*
+ * hc_block_step_backward without a caller workspace: the scratch is a fixed
+ * 64 MiB array in device memory that is part of the library's module, so the
+ * call allocates nothing.  Inputs whose workspace would not fit (for d = 5120,
+ * more than 29,696 tokens) return HC_ERR_UNSUPPORTED.  There is one such
+ * array per process and device: calls must not overlap in time (for
+ * instance, issue them on one stream).  Results equal
+ * hc_block_step_backward's bit for bit.
+ */
+hc_status hc_block_step_backward_no_workspace(
+    const uint16_t *x, const float *pre_mix, const uint16_t *f, const float *hc_fn,
+    const float *hc_scale, const float *hc_base, const float *norm_w, int64_t n, int hc, int d,
+    int sinkhorn_iters, float eps, float norm_eps, const float *g_h_norm, const float *g_y,
+    const float *g_pre, float *g_x, float *g_pre_mix, float *g_f, float *g_hc_fn, float *g_hc_scale,
+    float *g_hc_base, float *g_norm_w, cudaStream_t stream);
+
 hc_status hc_block_step_backward(const uint16_t *x, const float *pre_mix, const uint16_t *f,
                                  const float *hc_fn, const float *hc_scale, const float *hc_base,
                                  const float *norm_w, int64_t n, int hc, int d, int sinkhorn_iters,
