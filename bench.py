@@ -79,27 +79,40 @@ def measured_peaks():
         return 6800.0, "fallback"
 
 
-def source_digest():
+def source_digest(unit):
+    """Hash of one translation unit under csrc/ and of every local header it
+    includes (recursively): the sources a kernel in that unit is built from."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "hyper_connection_residual_mixes_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, name), "rb") as fh:
-            h.update(name.encode())
-            h.update(fh.read())
+    todo, seen = [os.path.join(csrc, unit)], set()
+    while todo:
+        path = os.path.normpath(todo.pop(0))
+        if path in seen:
+            continue
+        seen.add(path)
+        with open(path, "rb") as fh:
+            text = fh.read()
+        h.update(os.path.relpath(path, ROOT).encode())
+        h.update(text)
+        for line in text.decode().splitlines():
+            line = line.strip()
+            if line.startswith('#include "'):
+                todo.append(os.path.join(os.path.dirname(path), line.split('"')[1]))
     return h.hexdigest()[:16]
 
 
 def ncu_traffic_per_launch(n_tokens, path_kind="step"):
     """DRAM bytes per launch from the committed ncu summary, scaled by tokens;
-    None when it was taken on other kernel sources."""
+    None when the kernel's sources have changed since it was taken."""
     path = os.path.join(ROOT, "profiles", "hc_chain_side_traffic.json" if path_kind == "chain"
                         else "hc_block_step_traffic.json")
+    unit = "hc_chain.cu" if path_kind == "chain" else "hc_block_cluster.cu"
     try:
         with open(path) as fh:
             rec = json.load(fh)
     except Exception:
         return None
-    if rec.get("source_digest") != source_digest():
+    if rec.get("source_digest") != source_digest(unit):
         return None
     return int(rec["dram_bytes_per_token"] * n_tokens + rec.get("dram_bytes_fixed", 0))
 

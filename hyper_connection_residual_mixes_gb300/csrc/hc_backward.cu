@@ -10,12 +10,18 @@
 // the backward reads the forward's bf16-rounded h where the forward did.
 // Sinkhorn is differentiated step by step through its stored intermediates.
 //
-// How: k_bwd_token, one CTA per token, recomputes the forward quantities it
-// needs (the projection, the statistics, h, the split and the Sinkhorn
-// iterates), runs the Sinkhorn backward on one thread, and writes the
-// token's gradients (x, pre_mix, f) plus, into the workspace, the per-token
-// terms of the parameter gradients.  The parameter gradients are then summed
-// over fixed token blocks and the blocks added in a fixed order, so every
+// How, in three passes over the batch:
+//   k_bwd_proj   16 tokens per CTA: the projection a = x W^T and sum x^2,
+//                x staged through shared memory with cp.async, each weight
+//                row read once per tile (W is the 24 x hc*d matrix hc_fn);
+//   k_bwd_token  one CTA per token: h, the statistics, the split and
+//                Sinkhorn forward with its iterates, the Sinkhorn backward on
+//                one thread, g_pre_mix; writes a per-token record;
+//   k_bwd_gx     one CTA per (64 columns of d, all four streams) x (block of
+//                1,024 tokens), the column's 24 weights in registers: g_x,
+//                g_f, and the block's partial sums of g_hc_fn, g_norm_w and
+//                the per-token terms of g_hc_base / g_hc_scale.
+// The partial sums are then added over the blocks in a fixed order, so every
 // result is deterministic (no atomics).
 #include "hc_device.cuh"
 #include "hc_launch.h"
@@ -26,9 +32,34 @@ namespace bw {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kWs = 64;          // workspace floats per token: g_a[24], g_z[24], gzm[3], rs_h
 constexpr int kTokBlock = 1024;  // tokens per partial sum of a parameter gradient
-constexpr int kMaxIters = 128;
+
+// The per-token record in the workspace (floats).  [0, kRec) is what k_bwd_gx
+// stages for each token; the rest feeds the hc_base / hc_scale sums or comes
+// from k_bwd_proj.
+constexpr int kWs = 112;
+constexpr int kGa = 0;      // g_a[24]: the gradient of the projection a
+constexpr int kPost = 24;   // post[4]
+constexpr int kComb = 28;   // comb[16]
+constexpr int kPm = 44;     // pre_mix[4]
+constexpr int kRs = 48;     // rs_h = 1 / RMS(h)
+constexpr int kCr = 49;     // the statistic's coefficient of x in g_x
+constexpr int kK3 = 50;     // rs_h^3 / d * sum(h w g_hn)
+constexpr int kRec = 52;
+constexpr int kGz = 52;     // g_z[24]: the gradient of the pre-activations (= g_hc_base terms)
+constexpr int kGzm = 76;    // gzm[3]: the g_hc_scale terms
+constexpr int kA = 80;      // a[24] (k_bwd_proj)
+constexpr int kSS = 104;    // sum x^2 (k_bwd_proj)
+constexpr int kSmall = 32;  // partial sums per block for hc_base (24) and hc_scale (3)
+
+constexpr int kProjTok = 16;    // tokens per CTA of k_bwd_proj
+constexpr int kProjCols = 256;  // columns of x per stage
+constexpr int kProjStages = 4;
+constexpr int kGxCols = 64;     // columns of d per CTA of k_bwd_gx
+constexpr int kGxTile = 16;     // tokens per staged tile of k_bwd_gx
+constexpr int kGxStages = 3;
+static_assert(kProjTok == 2 * kWarps, "each warp sums x^2 of two tokens");
+static_assert(kThreads == kHC * kGxCols, "k_bwd_gx: one thread per (stream, column)");
 
 // Sum of V per-thread values over the CTA; the totals land in tot[0..V).
 template <int V>
@@ -56,56 +87,107 @@ __device__ __forceinline__ void load8f(const float *p, float (&o)[8]) {
     const float4 b = __ldg(reinterpret_cast<const float4 *>(p) + 1);
     o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w; o[4] = b.x; o[5] = b.y; o[6] = b.z; o[7] = b.w;
 }
-__device__ __forceinline__ void store8f(float *p, const float (&o)[8]) {
-    reinterpret_cast<float4 *>(p)[0] = make_float4(o[0], o[1], o[2], o[3]);
-    reinterpret_cast<float4 *>(p)[1] = make_float4(o[4], o[5], o[6], o[7]);
+// 16-byte asynchronous copy global -> shared; src_bytes = 0 fills zeros
+// (the source address is not read then).
+__device__ __forceinline__ void cp_async16(void *sdst, const void *gsrc, int src_bytes) {
+    const uint32_t sa = (uint32_t)__cvta_generic_to_shared(sdst);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(sa), "l"(gsrc), "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// Shared memory: h of the token (d bf16), then the Sinkhorn iterates
-// (2 * iters matrices of 16) and the row softmax (16).
+// a_i = sum_k x_k W_ik and sum_k x_k^2 for kProjTok tokens.  Warp w owns the
+// weight rows 3w .. 3w+2; lane l the columns 8l .. 8l+7 of each 256-column
+// stage.  Tokens past n are zero-filled and not written.
+__global__ void __launch_bounds__(kThreads, 2)
+k_bwd_proj(const uint16_t *__restrict__ x, const float *__restrict__ hc_fn, int64_t n, int K,
+           float *__restrict__ ws) {
+    constexpr int kChunks = kProjTok * kProjCols / 8;  // 16-byte chunks per stage
+    __shared__ __align__(16) uint4 sx[kProjStages][kChunks];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t t0 = (int64_t)blockIdx.x * kProjTok;
+    const int nst = K / kProjCols;
+    auto issue = [&](int st) {
+        if (st < nst) {
+            uint4 *dst = sx[st % kProjStages];
+            for (int q = threadIdx.x; q < kChunks; q += kThreads) {
+                const int tt = q / (kProjCols / 8), kc = q % (kProjCols / 8);
+                const bool ok = t0 + tt < n;
+                const uint16_t *src = ok ? x + (t0 + tt) * K + (int64_t)st * kProjCols + kc * 8 : x;
+                cp_async16(dst + q, src, ok ? 16 : 0);
+            }
+        }
+        cp_async_commit();  // an empty group past the end keeps the count uniform
+    };
+    float acc[kProjTok][3], ss[2] = {0.0f, 0.0f};
+#pragma unroll
+    for (int tt = 0; tt < kProjTok; ++tt)
+#pragma unroll
+        for (int j = 0; j < 3; ++j) acc[tt][j] = 0.0f;
+#pragma unroll
+    for (int st = 0; st < kProjStages - 1; ++st) issue(st);
+    for (int st = 0; st < nst; ++st) {
+        cp_async_wait<kProjStages - 2>();
+        __syncthreads();  // stage st landed for every thread; slot (st - 1) is free
+        issue(st + kProjStages - 1);
+        const uint4 *tile = sx[st % kProjStages];
+        float w[3][8];
+#pragma unroll
+        for (int j = 0; j < 3; ++j)
+            load8f(hc_fn + (int64_t)(3 * warp + j) * K + (int64_t)st * kProjCols + lane * 8, w[j]);
+#pragma unroll
+        for (int tt = 0; tt < kProjTok; ++tt) {
+            float xv[8];
+            unpack8(tile[tt * (kProjCols / 8) + lane], xv);
+#pragma unroll
+            for (int j = 0; j < 3; ++j)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[tt][j] = fmaf(xv[e], w[j][e], acc[tt][j]);
+            if ((tt >> 1) == warp)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) ss[tt & 1] = fmaf(xv[e], xv[e], ss[tt & 1]);
+        }
+    }
+    cp_async_wait<0>();
+#pragma unroll
+    for (int tt = 0; tt < kProjTok; ++tt)
+#pragma unroll
+        for (int j = 0; j < 3; ++j) {
+            const float v = warp_sum(acc[tt][j]);
+            if (lane == 0 && t0 + tt < n) ws[(t0 + tt) * kWs + kA + 3 * warp + j] = v;
+        }
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        const float v = warp_sum(ss[q]);
+        if (lane == 0 && t0 + 2 * warp + q < n) ws[(t0 + 2 * warp + q) * kWs + kSS] = v;
+    }
+}
+
+// One token per CTA.  Shared memory: h of the token (d bf16), then the
+// Sinkhorn iterates and the reciprocals of their sums (2 * iters matrices of
+// 16 each).  Reads a and sum x^2 from the record (k_bwd_proj), writes the
+// rest of it.
 __global__ void __launch_bounds__(kThreads)
 k_bwd_token(const uint16_t *__restrict__ x, const float *__restrict__ pre_mix,
-            const uint16_t *__restrict__ f, const float *__restrict__ hc_fn,
-            const float *__restrict__ hc_scale, const float *__restrict__ hc_base,
-            const float *__restrict__ norm_w, int d, int iters, float eps, float norm_eps,
-            const float *__restrict__ g_hn, const float *__restrict__ g_y,
-            const float *__restrict__ g_pre, float *__restrict__ g_x, float *__restrict__ g_pm,
-            float *__restrict__ g_f, float *__restrict__ ws) {
+            const uint16_t *__restrict__ f, const float *__restrict__ hc_scale,
+            const float *__restrict__ hc_base, const float *__restrict__ norm_w, int d, int iters,
+            float eps, float norm_eps, const float *__restrict__ g_hn, const float *__restrict__ g_y,
+            const float *__restrict__ g_pre, float *__restrict__ g_pm, float *__restrict__ ws) {
     extern __shared__ uint4 smem_u4[];
     uint4 *sh = smem_u4;                                             // d/8 chunks of h
     float *sP = reinterpret_cast<float *>(smem_u4 + (d >> 3));      // 2*iters*16 iterates
-    float *sS = sP + 2 * iters * kHC * kHC;                         // row softmax
+    float *sI = sP + 2 * iters * kHC * kHC;                         // their 1 / (sum + eps)
     __shared__ float red[kWarps][32];
     __shared__ float tot[32];
-    __shared__ float sa[32];  // the projection a[24] and sum x^2
-    // g_a[24], the statistic's term cr, rs_h, post[4], comb[16]
-    __shared__ float sc[48];
+    __shared__ float sGz[kMix];
     const int64_t t = blockIdx.x;
-    const int K = kHC * d, K8 = K >> 3, d8 = d >> 3;
+    const int K = kHC * d, d8 = d >> 3;
     const uint16_t *xt = x + t * K;
-
-    // (a) the projection a_i = sum_k x_k W_ik and the statistic sum x^2
-    {
-        float v[kMix + 1];
-#pragma unroll
-        for (int i = 0; i <= kMix; ++i) v[i] = 0.0f;
-        for (int ch = threadIdx.x; ch < K8; ch += kThreads) {
-            float xv[8];
-            unpack8(__ldg(reinterpret_cast<const uint4 *>(xt) + ch), xv);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) v[kMix] = fmaf(xv[e], xv[e], v[kMix]);
-#pragma unroll
-            for (int i = 0; i < kMix; ++i) {
-                float w[8];
-                load8f(hc_fn + (int64_t)i * K + 8 * ch, w);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) v[i] = fmaf(xv[e], w[e], v[i]);
-            }
-        }
-        block_sums<kMix + 1>(v, red, tot);
-        if (threadIdx.x <= kMix) sa[threadIdx.x] = tot[threadIdx.x];
-        __syncthreads();
-    }
+    float *wt = ws + t * kWs;
     float pm[kHC];
 #pragma unroll
     for (int s = 0; s < kHC; ++s) pm[s] = __ldg(pre_mix + t * kHC + s);
@@ -149,155 +231,124 @@ k_bwd_token(const uint16_t *__restrict__ x, const float *__restrict__ pre_mix,
         block_sums<2 + kHC + kHC * kHC>(v, red, tot);
     }
 
-    // (c) one thread: split + Sinkhorn forward with its iterates, then back
-    if (threadIdx.x == 0) {
-        const float *a = sa;
-        const float r = rsqrtf(sa[kMix] / (float)K + norm_eps);
-        const float rs = rsqrtf(tot[0] / (float)d + norm_eps);
-        const float s0 = __ldg(hc_scale), s1 = __ldg(hc_scale + 1), s2 = __ldg(hc_scale + 2);
-        float m[kMix];
-#pragma unroll
-        for (int i = 0; i < kMix; ++i) m[i] = a[i] * r;
-        // the row softmax S and P[0] = S + eps
-        for (int j = 0; j < kHC; ++j) {
-            float L[kHC], mx = -INFINITY, s = 0.0f;
-            for (int k = 0; k < kHC; ++k) {
-                L[k] = fmaf(m[2 * kHC + j * kHC + k], s2, __ldg(hc_base + 2 * kHC + j * kHC + k));
-                mx = fmaxf(mx, L[k]);
-            }
-            for (int k = 0; k < kHC; ++k) {
-                L[k] = expf(L[k] - mx);
-                s += L[k];
-            }
-            for (int k = 0; k < kHC; ++k) {
-                sS[j * kHC + k] = L[k] / s;
-                sP[j * kHC + k] = sS[j * kHC + k] + eps;
-            }
-        }
-        // steps 1 .. 2*iters-1: a column step for odd, a row step for even steps
-        for (int st = 1; st < 2 * iters; ++st) {
-            const float *pa = sP + (st - 1) * 16;
-            float *pb = sP + st * 16;
-            for (int i = 0; i < kHC; ++i) {
-                float s = 0.0f;
-                for (int o = 0; o < kHC; ++o) s += (st & 1) ? pa[o * kHC + i] : pa[i * kHC + o];
-                const float inv = 1.0f / (s + eps);
-                for (int o = 0; o < kHC; ++o) {
-                    const int idx = (st & 1) ? o * kHC + i : i * kHC + o;
-                    pb[idx] = pa[idx] * inv;
-                }
-            }
-        }
-        const float *comb = sP + (2 * iters - 1) * 16;
-        // back through the steps: g (the gradient of the current iterate)
-        float g[kHC * kHC];
-        for (int i = 0; i < kHC * kHC; ++i) g[i] = tot[2 + kHC + i];
-        for (int st = 2 * iters - 1; st >= 1; --st) {
-            const float *pa = sP + (st - 1) * 16, *pb = sP + st * 16;
-            for (int i = 0; i < kHC; ++i) {
-                float s = 0.0f, dot = 0.0f;
-                for (int o = 0; o < kHC; ++o) {
-                    const int idx = (st & 1) ? o * kHC + i : i * kHC + o;
-                    s += pa[idx];
-                    dot = fmaf(g[idx], pb[idx], dot);
-                }
-                const float inv = 1.0f / (s + eps);
-                for (int o = 0; o < kHC; ++o) {
-                    const int idx = (st & 1) ? o * kHC + i : i * kHC + o;
-                    g[idx] = (g[idx] - dot) * inv;
-                }
-            }
-        }
-        float gm[kMix], gz[kMix];
-        for (int j = 0; j < kHC; ++j) {
-            float dot = 0.0f;
-            for (int k = 0; k < kHC; ++k) dot = fmaf(g[j * kHC + k], sS[j * kHC + k], dot);
-            for (int k = 0; k < kHC; ++k) gz[2 * kHC + j * kHC + k] = sS[j * kHC + k] * (g[j * kHC + k] - dot);
-        }
-        float gzm0 = 0.0f, gzm1 = 0.0f, gzm2 = 0.0f;
-        for (int j = 0; j < kHC; ++j) {
-            const float sp = sigm(fmaf(m[j], s0, __ldg(hc_base + j)));
-            gz[j] = (g_pre ? __ldg(g_pre + t * kHC + j) : 0.0f) * sp * (1.0f - sp);
-            const float sq = sigm(fmaf(m[kHC + j], s1, __ldg(hc_base + kHC + j)));
-            gz[kHC + j] = tot[2 + j] * 2.0f * sq * (1.0f - sq);
-            sc[26 + j] = 2.0f * sq;  // post
-            gm[j] = gz[j] * s0;
-            gm[kHC + j] = gz[kHC + j] * s1;
-            gzm0 = fmaf(gz[j], m[j], gzm0);
-            gzm1 = fmaf(gz[kHC + j], m[kHC + j], gzm1);
-        }
-        for (int i = 2 * kHC; i < kMix; ++i) {
-            gm[i] = gz[i] * s2;
-            gzm2 = fmaf(gz[i], m[i], gzm2);
-        }
-        float gr = 0.0f;
-        for (int i = 0; i < kMix; ++i) gr = fmaf(gm[i], a[i], gr);
-        float *wt = ws + t * kWs;
-        for (int i = 0; i < kMix; ++i) {
-            wt[i] = gm[i] * r;       // g_a
-            wt[kMix + i] = gz[i];    // g_z
-            sc[i] = gm[i] * r;
-        }
-        wt[2 * kMix] = gzm0;
-        wt[2 * kMix + 1] = gzm1;
-        wt[2 * kMix + 2] = gzm2;
-        wt[2 * kMix + 3] = rs;
-        sc[24] = -gr * r * r * r / (float)K;  // the statistic's term: cr * x_k
-        sc[25] = rs;
-        for (int i = 0; i < kHC * kHC; ++i) sc[30 + i] = comb[i];
-    }
-    __syncthreads();
+    const float rs = rsqrtf(tot[0] / (float)d + norm_eps);
+    const float k3 = rs * rs * rs / (float)d * tot[1];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    // (d) g_h, g_x, g_f; g_pre_mix partial sums
-    {
-        const float rs = sc[25], cr = sc[24], T = tot[1];
-        const float k3 = rs * rs * rs / (float)d * T;
-        float ga[kMix], post[kHC], comb[kHC * kHC];
-#pragma unroll
-        for (int i = 0; i < kMix; ++i) ga[i] = sc[i];
-#pragma unroll
-        for (int k = 0; k < kHC; ++k) post[k] = sc[26 + k];
-#pragma unroll
-        for (int i = 0; i < kHC * kHC; ++i) comb[i] = sc[30 + i];
-        float gp[kHC] = {0.0f, 0.0f, 0.0f, 0.0f};
-        for (int c = threadIdx.x; c < d8; c += kThreads) {
-            float h[8], w[8], gh[8], gy[kHC][8], gu[8];
-            unpack8(sh[c], h);
-            load8f(norm_w + 8 * c, w);
-            load8f(g_hn + t * d + 8 * c, gh);
-#pragma unroll
-            for (int k = 0; k < kHC; ++k) load8f(g_y + (t * kHC + k) * d + 8 * c, gy[k]);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) gu[e] = rs * (w[e] * gh[e]) - k3 * h[e];  // g_h
-            float gf[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                float acc = post[0] * gy[0][e];
-#pragma unroll
-                for (int k = 1; k < kHC; ++k) acc = fmaf(post[k], gy[k][e], acc);
-                gf[e] = acc;
+    if (warp == 0) {
+        // (c) warp 0: the comb part of the split and Sinkhorn, one matrix
+        // element per lane (lane & 15 = 4j + k; lanes 16-31 repeat 0-15);
+        // the row sums reduce over lanes ^1, ^2, the column sums over ^4, ^8.
+        const int e = lane & 15;
+        const float r = rsqrtf(wt[kSS] / (float)K + norm_eps);
+        const float s2 = __ldg(hc_scale + 2);
+        const float L = fmaf(wt[kA + 2 * kHC + e] * r, s2, __ldg(hc_base + 2 * kHC + e));
+        float mx = fmaxf(L, __shfl_xor_sync(0xffffffffu, L, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        const float ex = expf(L - mx);
+        float sum = ex + __shfl_xor_sync(0xffffffffu, ex, 1);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+        const float S = ex / sum;
+        float P = S + eps;
+        if (lane < 16) sP[e] = P;
+        // steps 1 .. 2*iters-1: a column step for odd, a row step for even
+        // steps; sI keeps each step's 1 / (sum + eps)
+        for (int st = 1; st < 2 * iters; ++st) {
+            const int m1 = (st & 1) ? 4 : 1, m2 = (st & 1) ? 8 : 2;
+            float q = P + __shfl_xor_sync(0xffffffffu, P, m1);
+            q += __shfl_xor_sync(0xffffffffu, q, m2);
+            const float inv = 1.0f / (q + eps);
+            P *= inv;
+            if (lane < 16) {
+                sP[st * 16 + e] = P;
+                sI[st * 16 + e] = inv;
             }
-            store8f(g_f + t * d + 8 * c, gf);
+        }
+        if (lane < 16) wt[kComb + e] = P;
+        // back through the steps: g, the gradient of the current iterate
+        float g = tot[2 + kHC + e];
+        __syncwarp();
+        for (int st = 2 * iters - 1; st >= 1; --st) {
+            const int m1 = (st & 1) ? 4 : 1, m2 = (st & 1) ? 8 : 2;
+            const float pb = sP[st * 16 + e], inv = sI[st * 16 + e];
+            float dot = g * pb;
+            dot += __shfl_xor_sync(0xffffffffu, dot, m1);
+            dot += __shfl_xor_sync(0xffffffffu, dot, m2);
+            g = (g - dot) * inv;
+        }
+        // through the row softmax
+        float dot = g * S;
+        dot += __shfl_xor_sync(0xffffffffu, dot, 1);
+        dot += __shfl_xor_sync(0xffffffffu, dot, 2);
+        const float gzc = S * (g - dot);
+        if (lane < 16) sGz[2 * kHC + e] = gzc;
+        __syncwarp();
+        if (lane == 0) {
+            // pre and post (sigmoids), then the gradient of the projection
+            const float s0 = __ldg(hc_scale), s1 = __ldg(hc_scale + 1);
+            float a[kMix], m[kMix], gz[kMix], gm[kMix];
 #pragma unroll
-            for (int s = 0; s < kHC; ++s) {
-                float xv[8], gx[8];
-                unpack8(__ldg(reinterpret_cast<const uint4 *>(xt + s * d) + c), xv);
+            for (int i = 0; i < kMix; ++i) {
+                a[i] = wt[kA + i];
+                m[i] = a[i] * r;
+            }
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    gp[s] = fmaf(xv[e], gu[e], gp[s]);
-                    float acc = fmaf(pm[s], gu[e], cr * xv[e]);
+            for (int i = 2 * kHC; i < kMix; ++i) gz[i] = sGz[i];
+            float gzm0 = 0.0f, gzm1 = 0.0f, gzm2 = 0.0f;
 #pragma unroll
-                    for (int k = 0; k < kHC; ++k) acc = fmaf(comb[s * kHC + k], gy[k][e], acc);
-                    gx[e] = acc;
+            for (int j = 0; j < kHC; ++j) {
+                const float sp = sigm(fmaf(m[j], s0, __ldg(hc_base + j)));
+                gz[j] = (g_pre ? __ldg(g_pre + t * kHC + j) : 0.0f) * sp * (1.0f - sp);
+                const float sq = sigm(fmaf(m[kHC + j], s1, __ldg(hc_base + kHC + j)));
+                gz[kHC + j] = tot[2 + j] * 2.0f * sq * (1.0f - sq);
+                wt[kPost + j] = 2.0f * sq;
+                wt[kPm + j] = pm[j];
+                gm[j] = gz[j] * s0;
+                gm[kHC + j] = gz[kHC + j] * s1;
+                gzm0 = fmaf(gz[j], m[j], gzm0);
+                gzm1 = fmaf(gz[kHC + j], m[kHC + j], gzm1);
+            }
+#pragma unroll
+            for (int i = 2 * kHC; i < kMix; ++i) {
+                gm[i] = gz[i] * s2;
+                gzm2 = fmaf(gz[i], m[i], gzm2);
+            }
+            float gr = 0.0f;
+#pragma unroll
+            for (int i = 0; i < kMix; ++i) gr = fmaf(gm[i], a[i], gr);
+#pragma unroll
+            for (int i = 0; i < kMix; ++i) {
+                wt[kGa + i] = gm[i] * r;
+                wt[kGz + i] = gz[i];
+            }
+            wt[kGzm] = gzm0;
+            wt[kGzm + 1] = gzm1;
+            wt[kGzm + 2] = gzm2;
+            wt[kRs] = rs;
+            wt[kCr] = -gr * r * r * r / (float)K;  // the statistic's term: cr * x_k
+            wt[kK3] = k3;
+        }
+    }
+
+    // (d) warps 1-7, beside (c): g_pre_mix_s = sum_c x_s g_h, with
+    // g_h = rs w g_hn - k3 h
+    {
+        float gp[kHC] = {0.0f, 0.0f, 0.0f, 0.0f};
+        if (warp != 0) {
+            for (int c = threadIdx.x - 32; c < d8; c += kThreads - 32) {
+                float h[8], w[8], gh[8], gu[8];
+                unpack8(sh[c], h);
+                load8f(norm_w + 8 * c, w);
+                load8f(g_hn + t * d + 8 * c, gh);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) gu[e] = rs * (w[e] * gh[e]) - k3 * h[e];
+#pragma unroll
+                for (int s = 0; s < kHC; ++s) {
+                    float xv[8];
+                    unpack8(__ldg(reinterpret_cast<const uint4 *>(xt + s * d) + c), xv);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) gp[s] = fmaf(xv[e], gu[e], gp[s]);
                 }
-#pragma unroll
-                for (int i = 0; i < kMix; ++i) {
-                    float wv[8];
-                    load8f(hc_fn + (int64_t)i * K + (int64_t)s * d + 8 * c, wv);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) gx[e] = fmaf(ga[i], wv[e], gx[e]);
-                }
-                store8f(g_x + t * K + (int64_t)s * d + 8 * c, gx);
             }
         }
         block_sums<kHC>(gp, red, tot);
@@ -305,58 +356,135 @@ k_bwd_token(const uint16_t *__restrict__ x, const float *__restrict__ pre_mix,
     }
 }
 
-// g_hc_fn partial sums over a block of kTokBlock tokens: partial[b][i][k] =
-// sum over the block's tokens of g_a[t][i] * x[t][k]; one thread per column k.
-__global__ void __launch_bounds__(kThreads)
-k_bwd_fn_partial(const uint16_t *__restrict__ x, const float *__restrict__ ws, int64_t n, int K,
-                 float *__restrict__ part) {
-    __shared__ float sga[32][kMix];
-    const int k = blockIdx.x * kThreads + threadIdx.x;
+// g_x, g_f and the block's partial sums of the parameter gradients.  Thread
+// (s, c): stream s, column c of d; it holds W[i][s*d + c] for the 24 rows and
+// sums g_a[t][i] * x[t][s][c] over the block's tokens.  Per token:
+//   g_h  = rs_h w_c g_hn - k3 h_c                  (h_c as the forward rounded it)
+//   g_x  = pm_s g_h + cr x_s + sum_k comb_sk g_y_k + sum_i g_a_i W_i
+//   g_f  = sum_k post_k g_y_k                       (s = 0 only)
+//   g_norm_w partial += h_c rs_h g_hn              (s = 0 only)
+// The CTAs of column block 0 also sum the block's g_z and gzm (the hc_base
+// and hc_scale terms).  Tiles of kGxTile tokens (their x, g_y and g_hn for
+// the CTA's columns, and their records) are staged through a kGxStages-deep
+// cp.async ring; tokens past the block are zero-filled and skipped.
+struct GxStage {
+    uint16_t x[kGxTile][kHC][kGxCols];
+    float gy[kGxTile][kHC][kGxCols];
+    float ghn[kGxTile][kGxCols];
+    float rec[kGxTile][kA];
+};
+constexpr size_t kGxSmem = sizeof(GxStage) * kGxStages;
+
+__global__ void __launch_bounds__(kThreads, 2)
+k_bwd_gx(const uint16_t *__restrict__ x, const float *__restrict__ hc_fn,
+         const float *__restrict__ norm_w, const float *__restrict__ g_hn,
+         const float *__restrict__ g_y, const float *__restrict__ ws, int64_t n, int d,
+         float *__restrict__ g_x, float *__restrict__ g_f, float *__restrict__ part_fn,
+         float *__restrict__ part_w, float *__restrict__ part_s) {
+    extern __shared__ uint4 smem_u4[];
+    GxStage *stg = reinterpret_cast<GxStage *>(smem_u4);
+    const int s = threadIdx.x / kGxCols;  // warp-uniform
+    const int cl = threadIdx.x % kGxCols;
+    const int c0 = blockIdx.x * kGxCols;
+    const int c = c0 + cl;
+    const int64_t K = (int64_t)kHC * d;
+    const int64_t col = (int64_t)s * d + c;
     const int64_t t0 = (int64_t)blockIdx.y * kTokBlock;
     const int64_t t1 = (t0 + kTokBlock < n) ? t0 + kTokBlock : n;
-    float acc[kMix];
+    const int ntiles = (int)((t1 - t0 + kGxTile - 1) / kGxTile);
+    const bool small = blockIdx.x == 0;
+    const int rec4 = (small ? kA : kRec) / 4;  // float4s staged per token record
+
+    auto issue = [&](int it) {
+        if (it < ntiles) {
+            GxStage &g = stg[it % kGxStages];
+            const int64_t tb = t0 + (int64_t)it * kGxTile;
+            for (int q = threadIdx.x; q < kGxTile * kHC * (kGxCols / 8); q += kThreads) {
+                const int u = q / (kHC * kGxCols / 8), j = (q / (kGxCols / 8)) % kHC, v = q % (kGxCols / 8);
+                const bool ok = tb + u < t1;
+                cp_async16(&g.x[u][j][8 * v], ok ? x + ((tb + u) * kHC + j) * d + c0 + 8 * v : x, ok ? 16 : 0);
+            }
+            for (int q = threadIdx.x; q < kGxTile * kHC * (kGxCols / 4); q += kThreads) {
+                const int u = q / (kHC * kGxCols / 4), j = (q / (kGxCols / 4)) % kHC, v = q % (kGxCols / 4);
+                const bool ok = tb + u < t1;
+                cp_async16(&g.gy[u][j][4 * v], ok ? g_y + ((tb + u) * kHC + j) * d + c0 + 4 * v : g_y,
+                           ok ? 16 : 0);
+            }
+            for (int q = threadIdx.x; q < kGxTile * (kGxCols / 4); q += kThreads) {
+                const int u = q / (kGxCols / 4), v = q % (kGxCols / 4);
+                const bool ok = tb + u < t1;
+                cp_async16(&g.ghn[u][4 * v], ok ? g_hn + (tb + u) * d + c0 + 4 * v : g_hn, ok ? 16 : 0);
+            }
+            for (int q = threadIdx.x; q < kGxTile * rec4; q += kThreads) {
+                const int u = q / rec4, v = q % rec4;
+                const bool ok = tb + u < t1;
+                cp_async16(&g.rec[u][4 * v], ok ? ws + (tb + u) * kWs + 4 * v : ws, ok ? 16 : 0);
+            }
+        }
+        cp_async_commit();
+    };
+
+    float W[kMix], gW[kMix];
 #pragma unroll
-    for (int i = 0; i < kMix; ++i) acc[i] = 0.0f;
-    for (int64_t tb = t0; tb < t1; tb += 32) {
-        const int cnt = (int)((t1 - tb < 32) ? t1 - tb : 32);
-        __syncthreads();
-        for (int q = threadIdx.x; q < cnt * kMix; q += kThreads)
-            sga[q / kMix][q % kMix] = ws[(tb + q / kMix) * kWs + q % kMix];
-        __syncthreads();
-        if (k < K) {
-            for (int u = 0; u < cnt; ++u) {
-                const float xv = __uint_as_float((uint32_t)x[(tb + u) * K + k] << 16);
+    for (int i = 0; i < kMix; ++i) {
+        W[i] = __ldg(hc_fn + i * K + col);
+        gW[i] = 0.0f;
+    }
+    const float wn = __ldg(norm_w + c);
+    float gw = 0.0f, sm = 0.0f;
 #pragma unroll
-                for (int i = 0; i < kMix; ++i) acc[i] = fmaf(sga[u][i], xv, acc[i]);
+    for (int it = 0; it < kGxStages - 1; ++it) issue(it);
+    for (int it = 0; it < ntiles; ++it) {
+        cp_async_wait<kGxStages - 2>();
+        __syncthreads();  // tile it landed for every thread; slot (it - 1) is free
+        issue(it + kGxStages - 1);
+        const GxStage &g = stg[it % kGxStages];
+        const int64_t tb = t0 + (int64_t)it * kGxTile;
+        const int cnt = (int)((t1 - tb < kGxTile) ? t1 - tb : kGxTile);
+        if (small && threadIdx.x < kMix + 3)
+            for (int u = 0; u < cnt; ++u) sm += g.rec[u][kGz + threadIdx.x];
+#pragma unroll 4
+        for (int u = 0; u < cnt; ++u) {
+            const int64_t t = tb + u;
+            const float *rec = g.rec[u];
+            float xv[kHC], gy[kHC];
+#pragma unroll
+            for (int j = 0; j < kHC; ++j) {
+                xv[j] = bf16lo(g.x[u][j][cl]);
+                gy[j] = g.gy[u][j][cl];
+            }
+            const float ghn = g.ghn[u][cl];
+            float h = rec[kPm] * xv[0];
+#pragma unroll
+            for (int j = 1; j < kHC; ++j) h = fmaf(rec[kPm + j], xv[j], h);
+            h = bf16lo(pack_bf16x2(h, 0.0f));  // the forward's bf16 h
+            const float rs = rec[kRs];
+            const float gh = rs * (wn * ghn) - rec[kK3] * h;
+            const float xs = s == 0 ? xv[0] : s == 1 ? xv[1] : s == 2 ? xv[2] : xv[3];
+            float gx = fmaf(rec[kPm + s], gh, rec[kCr] * xs);
+#pragma unroll
+            for (int k = 0; k < kHC; ++k) gx = fmaf(rec[kComb + s * kHC + k], gy[k], gx);
+#pragma unroll
+            for (int i = 0; i < kMix; ++i) {
+                const float ga = rec[kGa + i];
+                gx = fmaf(ga, W[i], gx);
+                gW[i] = fmaf(ga, xs, gW[i]);
+            }
+            g_x[(t * kHC + s) * d + c] = gx;
+            if (s == 0) {
+                gw = fmaf(h * rs, ghn, gw);
+                float gf = rec[kPost] * gy[0];
+#pragma unroll
+                for (int k = 1; k < kHC; ++k) gf = fmaf(rec[kPost + k], gy[k], gf);
+                g_f[t * d + c] = gf;
             }
         }
     }
-    if (k < K)
+    cp_async_wait<0>();
 #pragma unroll
-        for (int i = 0; i < kMix; ++i) part[((int64_t)blockIdx.y * kMix + i) * K + k] = acc[i];
-}
-
-// g_norm_w partial sums: partial[b][c] = sum over the block's tokens of
-// h[t][c] * rs_h[t] * g_hn[t][c], h recomputed exactly as k_bwd_token does.
-__global__ void __launch_bounds__(kThreads)
-k_bwd_w_partial(const uint16_t *__restrict__ x, const float *__restrict__ pre_mix,
-                const float *__restrict__ g_hn, const float *__restrict__ ws, int64_t n, int d,
-                float *__restrict__ part) {
-    const int c = blockIdx.x * kThreads + threadIdx.x;
-    const int64_t t0 = (int64_t)blockIdx.y * kTokBlock;
-    const int64_t t1 = (t0 + kTokBlock < n) ? t0 + kTokBlock : n;
-    if (c >= d) return;
-    float acc = 0.0f;
-    for (int64_t t = t0; t < t1; ++t) {
-        const uint16_t *xt = x + t * kHC * d;
-        float h = __ldg(pre_mix + t * kHC) * __uint_as_float((uint32_t)xt[c] << 16);
-#pragma unroll
-        for (int s = 1; s < kHC; ++s)
-            h = fmaf(__ldg(pre_mix + t * kHC + s), __uint_as_float((uint32_t)xt[s * d + c] << 16), h);
-        h = bf16lo(pack_bf16x2(h, 0.0f));  // the forward's bf16 h
-        acc = fmaf(h * __ldg(ws + t * kWs + 2 * kMix + 3), __ldg(g_hn + t * d + c), acc);
-    }
-    part[(int64_t)blockIdx.y * d + c] = acc;
+    for (int i = 0; i < kMix; ++i) part_fn[((int64_t)blockIdx.y * kMix + i) * K + col] = gW[i];
+    if (s == 0) part_w[(int64_t)blockIdx.y * d + c] = gw;
+    if (small && threadIdx.x < kMix + 3) part_s[(int64_t)blockIdx.y * kSmall + threadIdx.x] = sm;
 }
 
 // out[j] = sum_b part[b][j], blocks in order.
@@ -369,22 +497,16 @@ __global__ void k_bwd_sum_blocks(const float *__restrict__ part, int blocks, int
     out[j] = s;
 }
 
-// g_hc_base[i] = sum_t g_z[t][i], g_hc_scale[j] = sum_t gzm[t][j]: one CTA,
-// each thread a fixed stride of tokens, then a fixed tree.
-__global__ void __launch_bounds__(kThreads)
-k_bwd_small(const float *__restrict__ ws, int64_t n, float *__restrict__ g_base,
-            float *__restrict__ g_scale) {
-    __shared__ float red[kWarps][32];
-    __shared__ float tot[32];
-    float v[kMix + 3];
-#pragma unroll
-    for (int i = 0; i < kMix + 3; ++i) v[i] = 0.0f;
-    for (int64_t t = threadIdx.x; t < n; t += kThreads)
-#pragma unroll
-        for (int i = 0; i < kMix + 3; ++i) v[i] += ws[t * kWs + kMix + i];
-    block_sums<kMix + 3>(v, red, tot);
-    if (threadIdx.x < kMix) g_base[threadIdx.x] = tot[threadIdx.x];
-    else if (threadIdx.x < kMix + 3) g_scale[threadIdx.x - kMix] = tot[threadIdx.x];
+// g_hc_base[i] = sum_b part_s[b][i], g_hc_scale[j] = sum_b part_s[b][24 + j],
+// blocks in order.
+__global__ void k_bwd_small(const float *__restrict__ part_s, int blocks, float *__restrict__ g_base,
+                            float *__restrict__ g_scale) {
+    const int j = threadIdx.x;
+    if (j >= kMix + 3) return;
+    float s = 0.0f;
+    for (int b = 0; b < blocks; ++b) s += part_s[(int64_t)b * kSmall + j];
+    if (j < kMix) g_base[j] = s;
+    else g_scale[j - kMix] = s;
 }
 
 }  // namespace bw
@@ -402,7 +524,7 @@ cudaError_t backward_static_scratch(void **ptr) { return cudaGetSymbolAddress(pt
 size_t backward_workspace_bytes(int64_t n, int d) {
     const int64_t blocks = (n + bw::kTokBlock - 1) / bw::kTokBlock;
     const int64_t K = (int64_t)kHC * d;
-    return (size_t)(n * bw::kWs + blocks * kMix * K + blocks * d) * sizeof(float);
+    return (size_t)(n * bw::kWs + blocks * (kMix * K + d + bw::kSmall)) * sizeof(float);
 }
 
 cudaError_t launch_block_step_backward(const uint16_t *x, const float *pre_mix, const uint16_t *f,
@@ -418,21 +540,22 @@ cudaError_t launch_block_step_backward(const uint16_t *x, const float *pre_mix, 
     float *ws = reinterpret_cast<float *>(workspace);
     float *part_fn = ws + n * kWs;
     float *part_w = part_fn + (int64_t)blocks * kMix * K;
-    const size_t smem = (size_t)d * 2 + (size_t)(2 * iters + 1) * kHC * kHC * sizeof(float);
+    float *part_s = part_w + (int64_t)blocks * d;
+    const size_t smem = (size_t)d * 2 + (size_t)(4 * iters) * kHC * kHC * sizeof(float);
     cudaError_t e = cudaFuncSetAttribute(k_bwd_token, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
-    k_bwd_token<<<(unsigned)n, kThreads, smem, s>>>(x, pre_mix, f, hc_fn, hc_scale, hc_base, norm_w,
-                                                   d, iters, eps, norm_eps, g_hn, g_y, g_pre, g_x,
-                                                   g_pm, g_f, ws);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    k_bwd_fn_partial<<<dim3((unsigned)((K + kThreads - 1) / kThreads), (unsigned)blocks), kThreads, 0, s>>>(
-        x, ws, n, (int)K, part_fn);
+    k_bwd_proj<<<(unsigned)((n + kProjTok - 1) / kProjTok), kThreads, 0, s>>>(x, hc_fn, n, (int)K, ws);
+    k_bwd_token<<<(unsigned)n, kThreads, smem, s>>>(x, pre_mix, f, hc_scale, hc_base, norm_w, d, iters,
+                                                   eps, norm_eps, g_hn, g_y, g_pre, g_pm, ws);
+    if ((e = cudaFuncSetAttribute(k_bwd_gx, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGxSmem)) !=
+        cudaSuccess)
+        return e;
+    k_bwd_gx<<<dim3((unsigned)(d / kGxCols), (unsigned)blocks), kThreads, kGxSmem, s>>>(
+        x, hc_fn, norm_w, g_hn, g_y, ws, n, d, g_x, g_f, part_fn, part_w, part_s);
     k_bwd_sum_blocks<<<(unsigned)((kMix * K + 255) / 256), 256, 0, s>>>(part_fn, blocks, kMix * K, g_fn);
-    k_bwd_w_partial<<<dim3((unsigned)((d + kThreads - 1) / kThreads), (unsigned)blocks), kThreads, 0, s>>>(
-        x, pre_mix, g_hn, ws, n, d, part_w);
     k_bwd_sum_blocks<<<(unsigned)((d + 255) / 256), 256, 0, s>>>(part_w, blocks, d, g_w);
-    k_bwd_small<<<1, kThreads, 0, s>>>(ws, n, g_base, g_scale);
+    k_bwd_small<<<1, 32, 0, s>>>(part_s, blocks, g_base, g_scale);
     return cudaGetLastError();
 }
 

@@ -180,7 +180,7 @@ size_t hc_block_step_backward_workspace_bytes(int64_t n, int hc, int d);
  * hc_block_step_backward without a caller workspace: the scratch is a fixed
  * 64 MiB array in device memory that is part of the library's module, so the
  * call allocates nothing.  Inputs whose workspace would not fit (for d = 5120,
- * more than 29,696 tokens) return HC_ERR_UNSUPPORTED.  There is one such
+ * more than 27,648 tokens) return HC_ERR_UNSUPPORTED.  There is one such
  * array per process and device: calls must not overlap in time (for
  * instance, issue them on one stream).  Results equal
  * hc_block_step_backward's bit for bit.

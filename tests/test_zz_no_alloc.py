@@ -31,7 +31,7 @@ def _raw(lib, n, hc=4, d=5120):
 
 
 def test_no_workspace_entry_refuses_what_does_not_fit(lib):
-    assert _raw(lib, 29697) == 2          # beyond the fixed scratch at d = 5120
+    assert _raw(lib, 27649) == 2          # one token beyond the fixed scratch at d = 5120
     assert _raw(lib, 16, hc=2) == 2
     assert _raw(lib, 0) == 0
 
