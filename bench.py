@@ -602,7 +602,7 @@ def run_op(args, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     hcg._lib.load()
-    case = inputs.long_prefill(device=dev, materialize_f=False)
+    case = inputs.long_prefill(device=dev, materialize_f=False, n=args.tokens or TOKENS)
     n, d = case.n, case.d
     p = case.params[0]
     codes = torch.empty((n, d), dtype=torch.uint8, device=dev)
@@ -649,7 +649,7 @@ def run_op(args, local_rank):
     clk = clocks.stop()
     ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
     peak, peak_kind = measured_peaks()
-    out = {"metric": "tokens/s through %s, 65,536 tokens x d = 5120" % what, "value": n / (ms / 1e3),
+    out = {"metric": "tokens/s through %s, %s tokens x d = %d" % (what, format(n, ","), d), "value": n / (ms / 1e3),
            "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
            "dtype": ("bf16 + fp32 in, fp32 arithmetic, fp32 gradients out" if args.op == "backward"
@@ -705,6 +705,8 @@ def main():
                     help="chain: the sides fused across sides (hc_chain_*); step: one hc_block_step per side")
     ap.add_argument("--op", choices=["mxfp8_cast", "pre_norm_mxfp8", "backward"], default=None,
                     help="time one kernel of the widened rows alone instead of the side steps")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="with --op: tokens in the batch (default 65,536; smaller for profiler captures)")
     args = ap.parse_args()
     rank, local_rank, world = dist_env()
     if args.op is not None and args.impl == "ours":

@@ -11,10 +11,11 @@
 // Sinkhorn is differentiated step by step through its stored intermediates.
 //
 // How, in three passes over the batch:
-//   k_bwd_proj   16 tokens per CTA: the projection a = x W^T and sum x^2,
-//                x staged through shared memory with cp.async, each weight
-//                row read once per tile (W is the 24 x hc*d matrix hc_fn);
-//   k_bwd_token  one CTA per token: h, the statistics, the split and
+//   k_bwd_proj   16 tokens per CTA: the projection a = x W^T, x and W
+//                staged through shared memory with cp.async, W read once
+//                per tile (W is the 24 x hc*d matrix hc_fn);
+//   k_bwd_token  one CTA per token: h, the statistics (sum x^2 among
+//                them), the split and
 //                Sinkhorn forward with its iterates, the Sinkhorn backward on
 //                one thread, g_pre_mix; writes a per-token record;
 //   k_bwd_gx     one CTA per (64 columns of d, all four streams) x (block of
@@ -49,17 +50,16 @@ constexpr int kRec = 52;
 constexpr int kGz = 52;     // g_z[24]: the gradient of the pre-activations (= g_hc_base terms)
 constexpr int kGzm = 76;    // gzm[3]: the g_hc_scale terms
 constexpr int kA = 80;      // a[24] (k_bwd_proj)
-constexpr int kSS = 104;    // sum x^2 (k_bwd_proj)
 constexpr int kSmall = 32;  // partial sums per block for hc_base (24) and hc_scale (3)
 
+constexpr int kProjThreads = 512;
 constexpr int kProjTok = 16;    // tokens per CTA of k_bwd_proj
-constexpr int kProjCols = 256;  // columns of x per stage
-constexpr int kProjStages = 4;
+constexpr int kProjCols = 256;  // columns of x and W per stage
+constexpr int kProjStages = 3;
 constexpr int kGxCols = 64;     // columns of d per CTA of k_bwd_gx
 constexpr int kGxTile = 16;     // tokens per staged tile of k_bwd_gx
-constexpr int kGxStages = 3;
-static_assert(kProjTok == 2 * kWarps, "each warp sums x^2 of two tokens");
-static_assert(kThreads == kHC * kGxCols, "k_bwd_gx: one thread per (stream, column)");
+constexpr int kGxStages = 4;
+static_assert(kProjThreads == 32 * 8 * (kProjTok / 8) && kMix == 3 * 8, "k_bwd_proj's warp map");
 
 // Sum of V per-thread values over the CTA; the totals land in tot[0..V).
 template <int V>
@@ -100,78 +100,90 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// a_i = sum_k x_k W_ik and sum_k x_k^2 for kProjTok tokens.  Warp w owns the
-// weight rows 3w .. 3w+2; lane l the columns 8l .. 8l+7 of each 256-column
-// stage.  Tokens past n are zero-filled and not written.
-__global__ void __launch_bounds__(kThreads, 2)
+// a_i = sum_k x_k W_ik for kProjTok tokens.  Each stage stages 256 columns
+// of x (the tile's tokens) and of W (all 24 rows) through a cp.async ring.
+// Warp w owns the weight rows 3(w mod 8) .. +2 and the tokens 8(w / 8) .. +7;
+// lane l the columns 8l .. 8l+7 of the stage, summed as (even, odd) column
+// pairs with the packed fp32 FMA.  Tokens past n are zero-filled and not
+// written.
+struct ProjStage {
+    uint4 x[kProjTok][kProjCols / 8];
+    float w[kMix][kProjCols];
+};
+constexpr size_t kProjSmem = sizeof(ProjStage) * kProjStages;
+
+__global__ void __launch_bounds__(kProjThreads, 1)
 k_bwd_proj(const uint16_t *__restrict__ x, const float *__restrict__ hc_fn, int64_t n, int K,
            float *__restrict__ ws) {
-    constexpr int kChunks = kProjTok * kProjCols / 8;  // 16-byte chunks per stage
-    __shared__ __align__(16) uint4 sx[kProjStages][kChunks];
+    extern __shared__ uint4 smem_u4[];
+    ProjStage *stg = reinterpret_cast<ProjStage *>(smem_u4);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int rb = 3 * (warp & 7), tb = 8 * (warp >> 3);
     const int64_t t0 = (int64_t)blockIdx.x * kProjTok;
     const int nst = K / kProjCols;
     auto issue = [&](int st) {
         if (st < nst) {
-            uint4 *dst = sx[st % kProjStages];
-            for (int q = threadIdx.x; q < kChunks; q += kThreads) {
+            ProjStage &g = stg[st % kProjStages];
+            for (int q = threadIdx.x; q < kProjTok * (kProjCols / 8); q += kProjThreads) {
                 const int tt = q / (kProjCols / 8), kc = q % (kProjCols / 8);
                 const bool ok = t0 + tt < n;
-                const uint16_t *src = ok ? x + (t0 + tt) * K + (int64_t)st * kProjCols + kc * 8 : x;
-                cp_async16(dst + q, src, ok ? 16 : 0);
+                cp_async16(&g.x[tt][kc], ok ? x + (t0 + tt) * K + (int64_t)st * kProjCols + kc * 8 : x,
+                           ok ? 16 : 0);
+            }
+            for (int q = threadIdx.x; q < kMix * (kProjCols / 4); q += kProjThreads) {
+                const int i = q / (kProjCols / 4), kc = q % (kProjCols / 4);
+                cp_async16(&g.w[i][4 * kc], hc_fn + (int64_t)i * K + (int64_t)st * kProjCols + 4 * kc, 16);
             }
         }
         cp_async_commit();  // an empty group past the end keeps the count uniform
     };
-    float acc[kProjTok][3], ss[2] = {0.0f, 0.0f};
+    f32x2 acc[8][3];
 #pragma unroll
-    for (int tt = 0; tt < kProjTok; ++tt)
+    for (int tt = 0; tt < 8; ++tt)
 #pragma unroll
-        for (int j = 0; j < 3; ++j) acc[tt][j] = 0.0f;
+        for (int j = 0; j < 3; ++j) acc[tt][j] = 0ull;
 #pragma unroll
     for (int st = 0; st < kProjStages - 1; ++st) issue(st);
     for (int st = 0; st < nst; ++st) {
         cp_async_wait<kProjStages - 2>();
         __syncthreads();  // stage st landed for every thread; slot (st - 1) is free
         issue(st + kProjStages - 1);
-        const uint4 *tile = sx[st % kProjStages];
-        float w[3][8];
+        const ProjStage &g = stg[st % kProjStages];
+        f32x2 w2[3][4];
 #pragma unroll
-        for (int j = 0; j < 3; ++j)
-            load8f(hc_fn + (int64_t)(3 * warp + j) * K + (int64_t)st * kProjCols + lane * 8, w[j]);
+        for (int j = 0; j < 3; ++j) {
+            const ulonglong2 *wr = reinterpret_cast<const ulonglong2 *>(&g.w[rb + j][lane * 8]);
+            const ulonglong2 a = wr[0], b = wr[1];
+            w2[j][0] = a.x; w2[j][1] = a.y; w2[j][2] = b.x; w2[j][3] = b.y;
+        }
 #pragma unroll
-        for (int tt = 0; tt < kProjTok; ++tt) {
-            float xv[8];
-            unpack8(tile[tt * (kProjCols / 8) + lane], xv);
+        for (int tt = 0; tt < 8; ++tt) {
+            const uint4 q = g.x[tb + tt][lane];
+            const f32x2 x2[4] = {f2_from_bf16x2(q.x), f2_from_bf16x2(q.y), f2_from_bf16x2(q.z),
+                                 f2_from_bf16x2(q.w)};
 #pragma unroll
             for (int j = 0; j < 3; ++j)
 #pragma unroll
-                for (int e = 0; e < 8; ++e) acc[tt][j] = fmaf(xv[e], w[j][e], acc[tt][j]);
-            if ((tt >> 1) == warp)
-#pragma unroll
-                for (int e = 0; e < 8; ++e) ss[tt & 1] = fmaf(xv[e], xv[e], ss[tt & 1]);
+                for (int p = 0; p < 4; ++p) acc[tt][j] = f2_fma(x2[p], w2[j][p], acc[tt][j]);
         }
     }
     cp_async_wait<0>();
 #pragma unroll
-    for (int tt = 0; tt < kProjTok; ++tt)
+    for (int tt = 0; tt < 8; ++tt)
 #pragma unroll
         for (int j = 0; j < 3; ++j) {
-            const float v = warp_sum(acc[tt][j]);
-            if (lane == 0 && t0 + tt < n) ws[(t0 + tt) * kWs + kA + 3 * warp + j] = v;
+            float lo, hi;
+            f2_split(acc[tt][j], lo, hi);
+            const float v = warp_sum(lo + hi);
+            const int64_t t = t0 + tb + tt;
+            if (lane == 0 && t < n) ws[t * kWs + kA + rb + j] = v;
         }
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-        const float v = warp_sum(ss[q]);
-        if (lane == 0 && t0 + 2 * warp + q < n) ws[(t0 + 2 * warp + q) * kWs + kSS] = v;
-    }
 }
 
 // One token per CTA.  Shared memory: h of the token (d bf16), then the
 // Sinkhorn iterates and the reciprocals of their sums (2 * iters matrices of
-// 16 each).  Reads a and sum x^2 from the record (k_bwd_proj), writes the
-// rest of it.
-__global__ void __launch_bounds__(kThreads)
+// 16 each).  Reads a from the record (k_bwd_proj), writes the rest of it.
+__global__ void __launch_bounds__(kThreads, 3)
 k_bwd_token(const uint16_t *__restrict__ x, const float *__restrict__ pre_mix,
             const uint16_t *__restrict__ f, const float *__restrict__ hc_scale,
             const float *__restrict__ hc_base, const float *__restrict__ norm_w, int d, int iters,
@@ -192,11 +204,12 @@ k_bwd_token(const uint16_t *__restrict__ x, const float *__restrict__ pre_mix,
 #pragma unroll
     for (int s = 0; s < kHC; ++s) pm[s] = __ldg(pre_mix + t * kHC + s);
 
-    // (b) h (kept), sum h^2, T = sum h w g_hn, g_post_k, g_comb_jk
+    // (b) h (kept), sum h^2, T = sum h w g_hn, g_post_k, g_comb_jk, sum x^2
+    constexpr int kSumX2 = 2 + kHC + kHC * kHC;
     {
-        float v[2 + kHC + kHC * kHC];
+        float v[kSumX2 + 1];
 #pragma unroll
-        for (int i = 0; i < 2 + kHC + kHC * kHC; ++i) v[i] = 0.0f;
+        for (int i = 0; i <= kSumX2; ++i) v[i] = 0.0f;
         for (int c = threadIdx.x; c < d8; c += kThreads) {
             float xv[kHC][8], fv[8], gy[kHC][8], gh[8], w[8], h[8];
 #pragma unroll
@@ -222,13 +235,15 @@ k_bwd_token(const uint16_t *__restrict__ x, const float *__restrict__ pre_mix,
 #pragma unroll
                 for (int k = 0; k < kHC; ++k) v[2 + k] = fmaf(fv[e], gy[k][e], v[2 + k]);
 #pragma unroll
-                for (int j = 0; j < kHC; ++j)
+                for (int j = 0; j < kHC; ++j) {
+                    v[kSumX2] = fmaf(xv[j][e], xv[j][e], v[kSumX2]);
 #pragma unroll
                     for (int k = 0; k < kHC; ++k)
                         v[2 + kHC + j * kHC + k] = fmaf(xv[j][e], gy[k][e], v[2 + kHC + j * kHC + k]);
+                }
             }
         }
-        block_sums<2 + kHC + kHC * kHC>(v, red, tot);
+        block_sums<kSumX2 + 1>(v, red, tot);
     }
 
     const float rs = rsqrtf(tot[0] / (float)d + norm_eps);
@@ -240,7 +255,7 @@ k_bwd_token(const uint16_t *__restrict__ x, const float *__restrict__ pre_mix,
         // element per lane (lane & 15 = 4j + k; lanes 16-31 repeat 0-15);
         // the row sums reduce over lanes ^1, ^2, the column sums over ^4, ^8.
         const int e = lane & 15;
-        const float r = rsqrtf(wt[kSS] / (float)K + norm_eps);
+        const float r = rsqrtf(tot[kSumX2] / (float)K + norm_eps);
         const float s2 = __ldg(hc_scale + 2);
         const float L = fmaf(wt[kA + 2 * kHC + e] * r, s2, __ldg(hc_base + 2 * kHC + e));
         float mx = fmaxf(L, __shfl_xor_sync(0xffffffffu, L, 1));
@@ -356,26 +371,65 @@ k_bwd_token(const uint16_t *__restrict__ x, const float *__restrict__ pre_mix,
     }
 }
 
-// g_x, g_f and the block's partial sums of the parameter gradients.  Thread
-// (s, c): stream s, column c of d; it holds W[i][s*d + c] for the 24 rows and
-// sums g_a[t][i] * x[t][s][c] over the block's tokens.  Per token:
+// tf32 helpers for the two small contractions of k_bwd_gx.  A value a is
+// carried as hi + lo, hi = tf32(a), lo = tf32(a - hi); products take
+// hi*hi + lo*hi + hi*lo (the lo*lo term is below fp32 rounding of the sum).
+__device__ __forceinline__ uint32_t tf32_of(float a) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(a));
+    return r;
+}
+__device__ __forceinline__ void tf32_split(float a, uint32_t &hi, uint32_t &lo) {
+    hi = tf32_of(a);
+    lo = tf32_of(a - __uint_as_float(hi));
+}
+// D += A (16x8, row) * B (8x8, col), tf32 inputs, fp32 accumulators
+__device__ __forceinline__ void mma_tf32(float (&dacc)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+        "{%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(dacc[0]), "+f"(dacc[1]), "+f"(dacc[2]), "+f"(dacc[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// g_x, g_f and the block's partial sums of the parameter gradients, for one
+// block of 1,024 tokens and 64 columns c of d (all four streams: 256 columns
+// of hc*d).  Per token t and column (s, c):
 //   g_h  = rs_h w_c g_hn - k3 h_c                  (h_c as the forward rounded it)
-//   g_x  = pm_s g_h + cr x_s + sum_k comb_sk g_y_k + sum_i g_a_i W_i
-//   g_f  = sum_k post_k g_y_k                       (s = 0 only)
-//   g_norm_w partial += h_c rs_h g_hn              (s = 0 only)
-// The CTAs of column block 0 also sum the block's g_z and gzm (the hc_base
-// and hc_scale terms).  Tiles of kGxTile tokens (their x, g_y and g_hn for
-// the CTA's columns, and their records) are staged through a kGxStages-deep
-// cp.async ring; tokens past the block are zero-filled and skipped.
+//   g_x  = pm_s g_h + cr x_s + sum_k comb_sk g_y_k + sum_i g_a_i W[i][s, c]
+//   g_f  = sum_k post_k g_y_k
+// and summed over the block: g_hc_fn[i][s, c] += g_a_i x_s, g_norm_w[c] +=
+// h_c rs_h g_hn.  The CTAs of column block 0 also sum the block's g_z and gzm
+// (the hc_base and hc_scale terms).
+// Tiles of kGxTile = 16 tokens (x, g_y, g_hn for the CTA's columns and the
+// token records) are staged through a cp.async ring.  Warp w owns the
+// columns c0 + 8w .. +7 of all four streams.  The two contractions over the
+// 24 mix rows run on the tensor cores (mma m16n8k8, tf32 split in hi + lo):
+//   g_a (16 tokens x 24) . W (24 x the warp's 32 columns), n-tile = stream;
+//   g_a^T (24, padded to 32, x 16 tokens) . x (16 tokens x 32 columns),
+//   accumulated over the block in registers.
+// The rest is per (token, column) in the accumulator layout: lane (g, q) =
+// (lane / 4, lane % 4) holds tokens g and g + 8, columns c0 + 8w + 2q and +1,
+// for the four streams.  The staged rows are padded so that these loads hit
+// distinct shared-memory banks.  Tokens past the block are zero-filled and
+// skipped.
+constexpr int kXRow = kHC * kGxCols + 8;   // bf16 per token row of the x tile
+constexpr int kGyRow = kHC * kGxCols + 8;  // floats per token row of the g_y tile
+constexpr int kGhRow = kGxCols + 8;        // floats per token row of the g_hn tile
+constexpr int kRecRow = kA + 4;            // floats per staged token record
 struct GxStage {
-    uint16_t x[kGxTile][kHC][kGxCols];
-    float gy[kGxTile][kHC][kGxCols];
-    float ghn[kGxTile][kGxCols];
-    float rec[kGxTile][kA];
+    uint16_t x[kGxTile][kXRow];
+    float gy[kGxTile][kGyRow];
+    float ghn[kGxTile][kGhRow];
+    float rec[kGxTile][kRecRow];
 };
 constexpr size_t kGxSmem = sizeof(GxStage) * kGxStages;
+static_assert(sizeof(GxStage) % 16 == 0 && (kXRow * 2) % 16 == 0 && (kGyRow * 4) % 16 == 0 &&
+                  (kGhRow * 4) % 16 == 0 && (kRecRow * 4) % 16 == 0,
+              "staged rows must keep 16-byte alignment");
+static_assert(kGxTile == 16 && kGxCols == 8 * kWarps && kMix == 24, "k_bwd_gx's fragment map");
 
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 1)
 k_bwd_gx(const uint16_t *__restrict__ x, const float *__restrict__ hc_fn,
          const float *__restrict__ norm_w, const float *__restrict__ g_hn,
          const float *__restrict__ g_y, const float *__restrict__ ws, int64_t n, int d,
@@ -383,107 +437,206 @@ k_bwd_gx(const uint16_t *__restrict__ x, const float *__restrict__ hc_fn,
          float *__restrict__ part_w, float *__restrict__ part_s) {
     extern __shared__ uint4 smem_u4[];
     GxStage *stg = reinterpret_cast<GxStage *>(smem_u4);
-    const int s = threadIdx.x / kGxCols;  // warp-uniform
-    const int cl = threadIdx.x % kGxCols;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, q = lane & 3;
     const int c0 = blockIdx.x * kGxCols;
-    const int c = c0 + cl;
+    const int cw = 8 * warp;                 // the warp's first column within the block
     const int64_t K = (int64_t)kHC * d;
-    const int64_t col = (int64_t)s * d + c;
     const int64_t t0 = (int64_t)blockIdx.y * kTokBlock;
     const int64_t t1 = (t0 + kTokBlock < n) ? t0 + kTokBlock : n;
     const int ntiles = (int)((t1 - t0 + kGxTile - 1) / kGxTile);
     const bool small = blockIdx.x == 0;
-    const int rec4 = (small ? kA : kRec) / 4;  // float4s staged per token record
 
     auto issue = [&](int it) {
         if (it < ntiles) {
-            GxStage &g = stg[it % kGxStages];
+            GxStage &S = stg[it % kGxStages];
             const int64_t tb = t0 + (int64_t)it * kGxTile;
-            for (int q = threadIdx.x; q < kGxTile * kHC * (kGxCols / 8); q += kThreads) {
-                const int u = q / (kHC * kGxCols / 8), j = (q / (kGxCols / 8)) % kHC, v = q % (kGxCols / 8);
+            for (int k = threadIdx.x; k < kGxTile * kHC * (kGxCols / 8); k += kThreads) {
+                const int u = k / (kHC * kGxCols / 8), j = (k / (kGxCols / 8)) % kHC, v = k % (kGxCols / 8);
                 const bool ok = tb + u < t1;
-                cp_async16(&g.x[u][j][8 * v], ok ? x + ((tb + u) * kHC + j) * d + c0 + 8 * v : x, ok ? 16 : 0);
-            }
-            for (int q = threadIdx.x; q < kGxTile * kHC * (kGxCols / 4); q += kThreads) {
-                const int u = q / (kHC * kGxCols / 4), j = (q / (kGxCols / 4)) % kHC, v = q % (kGxCols / 4);
-                const bool ok = tb + u < t1;
-                cp_async16(&g.gy[u][j][4 * v], ok ? g_y + ((tb + u) * kHC + j) * d + c0 + 4 * v : g_y,
+                cp_async16(&S.x[u][j * kGxCols + 8 * v], ok ? x + ((tb + u) * kHC + j) * d + c0 + 8 * v : x,
                            ok ? 16 : 0);
             }
-            for (int q = threadIdx.x; q < kGxTile * (kGxCols / 4); q += kThreads) {
-                const int u = q / (kGxCols / 4), v = q % (kGxCols / 4);
+            for (int k = threadIdx.x; k < kGxTile * kHC * (kGxCols / 4); k += kThreads) {
+                const int u = k / (kHC * kGxCols / 4), j = (k / (kGxCols / 4)) % kHC, v = k % (kGxCols / 4);
                 const bool ok = tb + u < t1;
-                cp_async16(&g.ghn[u][4 * v], ok ? g_hn + (tb + u) * d + c0 + 4 * v : g_hn, ok ? 16 : 0);
+                cp_async16(&S.gy[u][j * kGxCols + 4 * v], ok ? g_y + ((tb + u) * kHC + j) * d + c0 + 4 * v : g_y,
+                           ok ? 16 : 0);
             }
-            for (int q = threadIdx.x; q < kGxTile * rec4; q += kThreads) {
-                const int u = q / rec4, v = q % rec4;
+            for (int k = threadIdx.x; k < kGxTile * (kGxCols / 4); k += kThreads) {
+                const int u = k / (kGxCols / 4), v = k % (kGxCols / 4);
                 const bool ok = tb + u < t1;
-                cp_async16(&g.rec[u][4 * v], ok ? ws + (tb + u) * kWs + 4 * v : ws, ok ? 16 : 0);
+                cp_async16(&S.ghn[u][4 * v], ok ? g_hn + (tb + u) * d + c0 + 4 * v : g_hn, ok ? 16 : 0);
+            }
+            for (int k = threadIdx.x; k < kGxTile * (kA / 4); k += kThreads) {
+                const int u = k / (kA / 4), v = k % (kA / 4);
+                const bool ok = tb + u < t1;
+                cp_async16(&S.rec[u][4 * v], ok ? ws + (tb + u) * kWs + 4 * v : ws, ok ? 16 : 0);
             }
         }
         cp_async_commit();
     };
 
-    float W[kMix], gW[kMix];
+    // W fragments (B of the first contraction): stream nt, mix rows 8ks + q (+4),
+    // column c0 + cw + g, as tf32 hi + lo
+    uint32_t bh[kHC][3][2], bl[kHC][3][2];
 #pragma unroll
-    for (int i = 0; i < kMix; ++i) {
-        W[i] = __ldg(hc_fn + i * K + col);
-        gW[i] = 0.0f;
-    }
-    const float wn = __ldg(norm_w + c);
-    float gw = 0.0f, sm = 0.0f;
+    for (int nt = 0; nt < kHC; ++nt)
+#pragma unroll
+        for (int ks = 0; ks < 3; ++ks)
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+                tf32_split(__ldg(hc_fn + (8 * ks + q + 4 * h) * K + (int64_t)nt * d + c0 + cw + g),
+                           bh[nt][ks][h], bl[nt][ks][h]);
+    float accW[2][kHC][4];  // g_hc_fn: rows 16mt + g (+8), stream nt, columns 2q, 2q + 1
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < kHC; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) accW[mt][nt][e] = 0.0f;
+    const int cc0 = c0 + cw + 2 * q;         // the lane's two columns of d: cc0, cc0 + 1
+    const float wn0 = __ldg(norm_w + cc0), wn1 = __ldg(norm_w + cc0 + 1);
+    float gw0 = 0.0f, gw1 = 0.0f, sm = 0.0f;
+
 #pragma unroll
     for (int it = 0; it < kGxStages - 1; ++it) issue(it);
     for (int it = 0; it < ntiles; ++it) {
         cp_async_wait<kGxStages - 2>();
         __syncthreads();  // tile it landed for every thread; slot (it - 1) is free
         issue(it + kGxStages - 1);
-        const GxStage &g = stg[it % kGxStages];
+        const GxStage &S = stg[it % kGxStages];
         const int64_t tb = t0 + (int64_t)it * kGxTile;
         const int cnt = (int)((t1 - tb < kGxTile) ? t1 - tb : kGxTile);
         if (small && threadIdx.x < kMix + 3)
-            for (int u = 0; u < cnt; ++u) sm += g.rec[u][kGz + threadIdx.x];
-#pragma unroll 4
-        for (int u = 0; u < cnt; ++u) {
-            const int64_t t = tb + u;
-            const float *rec = g.rec[u];
-            float xv[kHC], gy[kHC];
+            for (int u = 0; u < cnt; ++u) sm += S.rec[u][kGz + threadIdx.x];
+
+        // (1) D[t][s, c] = sum_i g_a[t][i] W[i][s, c]; tokens g, g + 8
+        float dA[kHC][4];
 #pragma unroll
-            for (int j = 0; j < kHC; ++j) {
-                xv[j] = bf16lo(g.x[u][j][cl]);
-                gy[j] = g.gy[u][j][cl];
+        for (int nt = 0; nt < kHC; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) dA[nt][e] = 0.0f;
+#pragma unroll
+        for (int ks = 0; ks < 3; ++ks) {
+            uint32_t ah[4], al[4];
+            tf32_split(S.rec[g][kGa + 8 * ks + q], ah[0], al[0]);
+            tf32_split(S.rec[g + 8][kGa + 8 * ks + q], ah[1], al[1]);
+            tf32_split(S.rec[g][kGa + 8 * ks + q + 4], ah[2], al[2]);
+            tf32_split(S.rec[g + 8][kGa + 8 * ks + q + 4], ah[3], al[3]);
+#pragma unroll
+            for (int nt = 0; nt < kHC; ++nt) {
+                mma_tf32(dA[nt], al, bh[nt][ks][0], bh[nt][ks][1]);
+                mma_tf32(dA[nt], ah, bl[nt][ks][0], bl[nt][ks][1]);
+                mma_tf32(dA[nt], ah, bh[nt][ks][0], bh[nt][ks][1]);
             }
-            const float ghn = g.ghn[u][cl];
-            float h = rec[kPm] * xv[0];
+        }
+
+        // (2) g_hc_fn[i][s, c] += sum_t g_a[t][i] x[t][s][c]; x is exact in tf32
 #pragma unroll
-            for (int j = 1; j < kHC; ++j) h = fmaf(rec[kPm + j], xv[j], h);
-            h = bf16lo(pack_bf16x2(h, 0.0f));  // the forward's bf16 h
-            const float rs = rec[kRs];
-            const float gh = rs * (wn * ghn) - rec[kK3] * h;
-            const float xs = s == 0 ? xv[0] : s == 1 ? xv[1] : s == 2 ? xv[2] : xv[3];
-            float gx = fmaf(rec[kPm + s], gh, rec[kCr] * xs);
+        for (int ks = 0; ks < 2; ++ks) {
+            const int ta = 8 * ks + q, tb4 = ta + 4;
+            uint32_t bx[kHC][2];
 #pragma unroll
-            for (int k = 0; k < kHC; ++k) gx = fmaf(rec[kComb + s * kHC + k], gy[k], gx);
-#pragma unroll
-            for (int i = 0; i < kMix; ++i) {
-                const float ga = rec[kGa + i];
-                gx = fmaf(ga, W[i], gx);
-                gW[i] = fmaf(ga, xs, gW[i]);
+            for (int nt = 0; nt < kHC; ++nt) {
+                bx[nt][0] = (uint32_t)S.x[ta][nt * kGxCols + cw + g] << 16;
+                bx[nt][1] = (uint32_t)S.x[tb4][nt * kGxCols + cw + g] << 16;
             }
-            g_x[(t * kHC + s) * d + c] = gx;
-            if (s == 0) {
-                gw = fmaf(h * rs, ghn, gw);
-                float gf = rec[kPost] * gy[0];
 #pragma unroll
-                for (int k = 1; k < kHC; ++k) gf = fmaf(rec[kPost + k], gy[k], gf);
-                g_f[t * d + c] = gf;
+            for (int mt = 0; mt < 2; ++mt) {
+                uint32_t ah[4], al[4];
+                tf32_split(S.rec[ta][kGa + 16 * mt + g], ah[0], al[0]);
+                tf32_split(S.rec[tb4][kGa + 16 * mt + g], ah[2], al[2]);
+                if (mt == 0) {
+                    tf32_split(S.rec[ta][kGa + g + 8], ah[1], al[1]);
+                    tf32_split(S.rec[tb4][kGa + g + 8], ah[3], al[3]);
+                } else {  // rows 24 .. 31 are padding
+                    ah[1] = al[1] = ah[3] = al[3] = 0u;
+                }
+#pragma unroll
+                for (int nt = 0; nt < kHC; ++nt) {
+                    mma_tf32(accW[mt][nt], al, bx[nt][0], bx[nt][1]);
+                    mma_tf32(accW[mt][nt], ah, bx[nt][0], bx[nt][1]);
+                }
+            }
+        }
+
+        // (3) the rest, per (token, column)
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const int u = g + 8 * r;
+            if (u < cnt) {
+                const int64_t t = tb + u;
+                const float *rec = S.rec[u];
+                const float4 pm4 = *reinterpret_cast<const float4 *>(rec + kPm);
+                const float4 sc4 = *reinterpret_cast<const float4 *>(rec + kRs);  // rs, cr, k3
+                const float pm[kHC] = {pm4.x, pm4.y, pm4.z, pm4.w};
+                const float rs = sc4.x, cr = sc4.y, k3 = sc4.z;
+                float xv[kHC][2], gy[kHC][2];
+#pragma unroll
+                for (int j = 0; j < kHC; ++j) {
+                    const uint32_t xp = *reinterpret_cast<const uint32_t *>(&S.x[u][j * kGxCols + cw + 2 * q]);
+                    xv[j][0] = bf16lo(xp);
+                    xv[j][1] = __uint_as_float(xp & 0xffff0000u);
+                    const float2 gp = *reinterpret_cast<const float2 *>(&S.gy[u][j * kGxCols + cw + 2 * q]);
+                    gy[j][0] = gp.x;
+                    gy[j][1] = gp.y;
+                }
+                const float2 gh2 = *reinterpret_cast<const float2 *>(&S.ghn[u][cw + 2 * q]);
+                const float ghn[2] = {gh2.x, gh2.y}, wn[2] = {wn0, wn1};
+                float gx[kHC][2], gf[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    float h = pm[0] * xv[0][e];
+#pragma unroll
+                    for (int j = 1; j < kHC; ++j) h = fmaf(pm[j], xv[j][e], h);
+                    h = bf16lo(pack_bf16x2(h, 0.0f));  // the forward's bf16 h
+                    const float gh = rs * (wn[e] * ghn[e]) - k3 * h;
+#pragma unroll
+                    for (int sI = 0; sI < kHC; ++sI) {
+                        const float4 cb = *reinterpret_cast<const float4 *>(rec + kComb + sI * kHC);
+                        float v = fmaf(pm[sI], gh, cr * xv[sI][e]);
+                        v = fmaf(cb.x, gy[0][e], v);
+                        v = fmaf(cb.y, gy[1][e], v);
+                        v = fmaf(cb.z, gy[2][e], v);
+                        v = fmaf(cb.w, gy[3][e], v);
+                        gx[sI][e] = v + dA[sI][2 * r + e];
+                    }
+                    const float4 po = *reinterpret_cast<const float4 *>(rec + kPost);
+                    float f = po.x * gy[0][e];
+                    f = fmaf(po.y, gy[1][e], f);
+                    f = fmaf(po.z, gy[2][e], f);
+                    f = fmaf(po.w, gy[3][e], f);
+                    gf[e] = f;
+                    if (e == 0) gw0 = fmaf(h * rs, ghn[e], gw0);
+                    else gw1 = fmaf(h * rs, ghn[e], gw1);
+                }
+#pragma unroll
+                for (int sI = 0; sI < kHC; ++sI)
+                    *reinterpret_cast<float2 *>(g_x + (t * kHC + sI) * d + cc0) = make_float2(gx[sI][0], gx[sI][1]);
+                *reinterpret_cast<float2 *>(g_f + t * d + cc0) = make_float2(gf[0], gf[1]);
             }
         }
     }
     cp_async_wait<0>();
+    // g_hc_fn partials: accumulator (row 16mt + g (+8), stream nt, columns 2q, 2q + 1)
 #pragma unroll
-    for (int i = 0; i < kMix; ++i) part_fn[((int64_t)blockIdx.y * kMix + i) * K + col] = gW[i];
-    if (s == 0) part_w[(int64_t)blockIdx.y * d + c] = gw;
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < kHC; ++nt) {
+            const int64_t colx = (int64_t)nt * d + cc0;
+            float *row = part_fn + ((int64_t)blockIdx.y * kMix + 16 * mt + g) * K + colx;
+            *reinterpret_cast<float2 *>(row) = make_float2(accW[mt][nt][0], accW[mt][nt][1]);
+            if (mt == 0)
+                *reinterpret_cast<float2 *>(row + 8 * K) = make_float2(accW[mt][nt][2], accW[mt][nt][3]);
+        }
+    // g_norm_w partials: sum over the eight token rows g (lanes q, q+4, ..., q+28)
+#pragma unroll
+    for (int m = 4; m < 32; m <<= 1) {
+        gw0 += __shfl_xor_sync(0xffffffffu, gw0, m);
+        gw1 += __shfl_xor_sync(0xffffffffu, gw1, m);
+    }
+    if (g == 0) *reinterpret_cast<float2 *>(part_w + (int64_t)blockIdx.y * d + cc0) = make_float2(gw0, gw1);
     if (small && threadIdx.x < kMix + 3) part_s[(int64_t)blockIdx.y * kSmall + threadIdx.x] = sm;
 }
 
@@ -545,7 +698,11 @@ cudaError_t launch_block_step_backward(const uint16_t *x, const float *pre_mix, 
     cudaError_t e = cudaFuncSetAttribute(k_bwd_token, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
-    k_bwd_proj<<<(unsigned)((n + kProjTok - 1) / kProjTok), kThreads, 0, s>>>(x, hc_fn, n, (int)K, ws);
+    if ((e = cudaFuncSetAttribute(k_bwd_proj, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)kProjSmem)) != cudaSuccess)
+        return e;
+    k_bwd_proj<<<(unsigned)((n + kProjTok - 1) / kProjTok), kProjThreads, kProjSmem, s>>>(x, hc_fn, n,
+                                                                                       (int)K, ws);
     k_bwd_token<<<(unsigned)n, kThreads, smem, s>>>(x, pre_mix, f, hc_scale, hc_base, norm_w, d, iters,
                                                    eps, norm_eps, g_hn, g_y, g_pre, g_pm, ws);
     if ((e = cudaFuncSetAttribute(k_bwd_gx, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGxSmem)) !=
