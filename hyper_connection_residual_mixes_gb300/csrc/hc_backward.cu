@@ -11,9 +11,9 @@
 // Sinkhorn is differentiated step by step through its stored intermediates.
 //
 // How, in three passes over the batch:
-//   k_bwd_proj   16 tokens per CTA: the projection a = x W^T, x and W
-//                staged through shared memory with cp.async, W read once
-//                per tile (W is the 24 x hc*d matrix hc_fn);
+//   k_bwd_proj   32 tokens per CTA: the projection a = x W^T on the tensor
+//                cores, x and W staged through shared memory with cp.async,
+//                W read once per tile (W is the 24 x hc*d matrix hc_fn);
 //   k_bwd_token  one CTA per token: h, the statistics (sum x^2 among
 //                them), the split and
 //                Sinkhorn forward with its iterates, the Sinkhorn backward on
@@ -52,14 +52,12 @@ constexpr int kGzm = 76;    // gzm[3]: the g_hc_scale terms
 constexpr int kA = 80;      // a[24] (k_bwd_proj)
 constexpr int kSmall = 32;  // partial sums per block for hc_base (24) and hc_scale (3)
 
-constexpr int kProjThreads = 512;
-constexpr int kProjTok = 16;    // tokens per CTA of k_bwd_proj
+constexpr int kProjTok = 32;    // tokens per CTA of k_bwd_proj
 constexpr int kProjCols = 256;  // columns of x and W per stage
 constexpr int kProjStages = 3;
 constexpr int kGxCols = 64;     // columns of d per CTA of k_bwd_gx
 constexpr int kGxTile = 16;     // tokens per staged tile of k_bwd_gx
 constexpr int kGxStages = 4;
-static_assert(kProjThreads == 32 * 8 * (kProjTok / 8) && kMix == 3 * 8, "k_bwd_proj's warp map");
 
 // Sum of V per-thread values over the CTA; the totals land in tot[0..V).
 template <int V>
@@ -100,84 +98,129 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// a_i = sum_k x_k W_ik for kProjTok tokens.  Each stage stages 256 columns
-// of x (the tile's tokens) and of W (all 24 rows) through a cp.async ring.
-// Warp w owns the weight rows 3(w mod 8) .. +2 and the tokens 8(w / 8) .. +7;
-// lane l the columns 8l .. 8l+7 of the stage, summed as (even, odd) column
-// pairs with the packed fp32 FMA.  Tokens past n are zero-filled and not
+// tf32 helpers for the tensor-core contractions (k_bwd_proj, k_bwd_gx).  A value a is
+// carried as hi + lo, hi = tf32(a), lo = tf32(a - hi); products take
+// hi*hi + lo*hi + hi*lo (the lo*lo term is below fp32 rounding of the sum).
+__device__ __forceinline__ uint32_t tf32_of(float a) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(a));
+    return r;
+}
+__device__ __forceinline__ void tf32_split(float a, uint32_t &hi, uint32_t &lo) {
+    hi = tf32_of(a);
+    lo = tf32_of(a - __uint_as_float(hi));
+}
+// D += A (16x8, row) * B (8x8, col), tf32 inputs, fp32 accumulators
+__device__ __forceinline__ void mma_tf32(float (&dacc)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+        "{%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(dacc[0]), "+f"(dacc[1]), "+f"(dacc[2]), "+f"(dacc[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// a_i = sum_k x_k W_ik for kProjTok = 32 tokens, on the tensor cores (mma
+// m16n8k8 tf32: x is exact in tf32, W is split in hi + lo).  Each stage
+// stages 256 columns of x (the tile's tokens) and of W (all 24 rows)
+// through a cp.async ring; warp w takes the columns 32w .. 32w+31 of every
+// stage (four k-steps of 8).  The eight warps' partial sums are added in
+// warp order through shared memory at the end.  Rows are padded so that the
+// fragment loads hit distinct banks.  Tokens past n are zero-filled and not
 // written.
+constexpr int kPxRow = kProjCols + 8;  // bf16 per staged token row of x
+constexpr int kPwRow = kProjCols + 4;  // floats per staged row of W
 struct ProjStage {
-    uint4 x[kProjTok][kProjCols / 8];
-    float w[kMix][kProjCols];
+    uint16_t x[kProjTok][kPxRow];
+    float w[kMix][kPwRow];
 };
 constexpr size_t kProjSmem = sizeof(ProjStage) * kProjStages;
+static_assert(sizeof(ProjStage) % 16 == 0 && (kPxRow * 2) % 16 == 0 && (kPwRow * 4) % 16 == 0,
+              "staged rows must keep 16-byte alignment");
+static_assert(kProjSmem >= sizeof(float) * kWarps * kProjTok * kMix, "the partial sums reuse the ring");
+static_assert(kProjTok == 32 && kProjCols == 32 * kWarps, "k_bwd_proj's fragment map");
 
-__global__ void __launch_bounds__(kProjThreads, 1)
+__global__ void __launch_bounds__(kThreads, 1)
 k_bwd_proj(const uint16_t *__restrict__ x, const float *__restrict__ hc_fn, int64_t n, int K,
            float *__restrict__ ws) {
     extern __shared__ uint4 smem_u4[];
     ProjStage *stg = reinterpret_cast<ProjStage *>(smem_u4);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int rb = 3 * (warp & 7), tb = 8 * (warp >> 3);
+    const int g = lane >> 2, q = lane & 3;
     const int64_t t0 = (int64_t)blockIdx.x * kProjTok;
     const int nst = K / kProjCols;
     auto issue = [&](int st) {
         if (st < nst) {
-            ProjStage &g = stg[st % kProjStages];
-            for (int q = threadIdx.x; q < kProjTok * (kProjCols / 8); q += kProjThreads) {
-                const int tt = q / (kProjCols / 8), kc = q % (kProjCols / 8);
+            ProjStage &S = stg[st % kProjStages];
+            for (int k = threadIdx.x; k < kProjTok * (kProjCols / 8); k += kThreads) {
+                const int tt = k / (kProjCols / 8), kc = k % (kProjCols / 8);
                 const bool ok = t0 + tt < n;
-                cp_async16(&g.x[tt][kc], ok ? x + (t0 + tt) * K + (int64_t)st * kProjCols + kc * 8 : x,
+                cp_async16(&S.x[tt][kc * 8], ok ? x + (t0 + tt) * K + (int64_t)st * kProjCols + kc * 8 : x,
                            ok ? 16 : 0);
             }
-            for (int q = threadIdx.x; q < kMix * (kProjCols / 4); q += kProjThreads) {
-                const int i = q / (kProjCols / 4), kc = q % (kProjCols / 4);
-                cp_async16(&g.w[i][4 * kc], hc_fn + (int64_t)i * K + (int64_t)st * kProjCols + 4 * kc, 16);
+            for (int k = threadIdx.x; k < kMix * (kProjCols / 4); k += kThreads) {
+                const int i = k / (kProjCols / 4), kc = k % (kProjCols / 4);
+                cp_async16(&S.w[i][4 * kc], hc_fn + (int64_t)i * K + (int64_t)st * kProjCols + 4 * kc, 16);
             }
         }
         cp_async_commit();  // an empty group past the end keeps the count uniform
     };
-    f32x2 acc[8][3];
+    float acc[2][3][4];  // tokens 16mt + g (+8), rows 8nt + 2q (+1)
 #pragma unroll
-    for (int tt = 0; tt < 8; ++tt)
+    for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-        for (int j = 0; j < 3; ++j) acc[tt][j] = 0ull;
+        for (int nt = 0; nt < 3; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[mt][nt][e] = 0.0f;
 #pragma unroll
     for (int st = 0; st < kProjStages - 1; ++st) issue(st);
     for (int st = 0; st < nst; ++st) {
         cp_async_wait<kProjStages - 2>();
         __syncthreads();  // stage st landed for every thread; slot (st - 1) is free
         issue(st + kProjStages - 1);
-        const ProjStage &g = stg[st % kProjStages];
-        f32x2 w2[3][4];
+        const ProjStage &S = stg[st % kProjStages];
 #pragma unroll
-        for (int j = 0; j < 3; ++j) {
-            const ulonglong2 *wr = reinterpret_cast<const ulonglong2 *>(&g.w[rb + j][lane * 8]);
-            const ulonglong2 a = wr[0], b = wr[1];
-            w2[j][0] = a.x; w2[j][1] = a.y; w2[j][2] = b.x; w2[j][3] = b.y;
-        }
+        for (int ks = 0; ks < 4; ++ks) {
+            const int k0 = 32 * warp + 8 * ks;
+            uint32_t bh[3][2], bl[3][2];
 #pragma unroll
-        for (int tt = 0; tt < 8; ++tt) {
-            const uint4 q = g.x[tb + tt][lane];
-            const f32x2 x2[4] = {f2_from_bf16x2(q.x), f2_from_bf16x2(q.y), f2_from_bf16x2(q.z),
-                                 f2_from_bf16x2(q.w)};
+            for (int nt = 0; nt < 3; ++nt) {
+                tf32_split(S.w[8 * nt + g][k0 + q], bh[nt][0], bl[nt][0]);
+                tf32_split(S.w[8 * nt + g][k0 + q + 4], bh[nt][1], bl[nt][1]);
+            }
 #pragma unroll
-            for (int j = 0; j < 3; ++j)
+            for (int mt = 0; mt < 2; ++mt) {
+                const uint32_t a[4] = {(uint32_t)S.x[16 * mt + g][k0 + q] << 16,
+                                       (uint32_t)S.x[16 * mt + g + 8][k0 + q] << 16,
+                                       (uint32_t)S.x[16 * mt + g][k0 + q + 4] << 16,
+                                       (uint32_t)S.x[16 * mt + g + 8][k0 + q + 4] << 16};
 #pragma unroll
-                for (int p = 0; p < 4; ++p) acc[tt][j] = f2_fma(x2[p], w2[j][p], acc[tt][j]);
+                for (int nt = 0; nt < 3; ++nt) {
+                    mma_tf32(acc[mt][nt], a, bl[nt][0], bl[nt][1]);
+                    mma_tf32(acc[mt][nt], a, bh[nt][0], bh[nt][1]);
+                }
+            }
         }
     }
     cp_async_wait<0>();
+    __syncthreads();  // every warp is done with the ring: reuse it for the partial sums
+    float *red = reinterpret_cast<float *>(smem_u4);  // [warp][token][row]
 #pragma unroll
-    for (int tt = 0; tt < 8; ++tt)
+    for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-        for (int j = 0; j < 3; ++j) {
-            float lo, hi;
-            f2_split(acc[tt][j], lo, hi);
-            const float v = warp_sum(lo + hi);
-            const int64_t t = t0 + tb + tt;
-            if (lane == 0 && t < n) ws[t * kWs + kA + rb + j] = v;
-        }
+        for (int nt = 0; nt < 3; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int tt = 16 * mt + g + 8 * (e >> 1), i = 8 * nt + 2 * q + (e & 1);
+                red[(warp * kProjTok + tt) * kMix + i] = acc[mt][nt][e];
+            }
+    __syncthreads();
+    for (int o = threadIdx.x; o < kProjTok * kMix; o += kThreads) {
+        const int tt = o / kMix, i = o % kMix;
+        float v = red[tt * kMix + i];
+#pragma unroll
+        for (int w = 1; w < kWarps; ++w) v += red[(w * kProjTok + tt) * kMix + i];
+        if (t0 + tt < n) ws[(t0 + tt) * kWs + kA + i] = v;
+    }
 }
 
 // One token per CTA.  Shared memory: h of the token (d bf16), then the
@@ -369,27 +412,6 @@ k_bwd_token(const uint16_t *__restrict__ x, const float *__restrict__ pre_mix,
         block_sums<kHC>(gp, red, tot);
         if (threadIdx.x < kHC) g_pm[t * kHC + threadIdx.x] = tot[threadIdx.x];
     }
-}
-
-// tf32 helpers for the two small contractions of k_bwd_gx.  A value a is
-// carried as hi + lo, hi = tf32(a), lo = tf32(a - hi); products take
-// hi*hi + lo*hi + hi*lo (the lo*lo term is below fp32 rounding of the sum).
-__device__ __forceinline__ uint32_t tf32_of(float a) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(a));
-    return r;
-}
-__device__ __forceinline__ void tf32_split(float a, uint32_t &hi, uint32_t &lo) {
-    hi = tf32_of(a);
-    lo = tf32_of(a - __uint_as_float(hi));
-}
-// D += A (16x8, row) * B (8x8, col), tf32 inputs, fp32 accumulators
-__device__ __forceinline__ void mma_tf32(float (&dacc)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
-        "{%8, %9}, {%0, %1, %2, %3};"
-        : "+f"(dacc[0]), "+f"(dacc[1]), "+f"(dacc[2]), "+f"(dacc[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
 // g_x, g_f and the block's partial sums of the parameter gradients, for one
@@ -701,8 +723,8 @@ cudaError_t launch_block_step_backward(const uint16_t *x, const float *pre_mix, 
     if ((e = cudaFuncSetAttribute(k_bwd_proj, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   (int)kProjSmem)) != cudaSuccess)
         return e;
-    k_bwd_proj<<<(unsigned)((n + kProjTok - 1) / kProjTok), kProjThreads, kProjSmem, s>>>(x, hc_fn, n,
-                                                                                       (int)K, ws);
+    k_bwd_proj<<<(unsigned)((n + kProjTok - 1) / kProjTok), kThreads, kProjSmem, s>>>(x, hc_fn, n, (int)K,
+                                                                                   ws);
     k_bwd_token<<<(unsigned)n, kThreads, smem, s>>>(x, pre_mix, f, hc_scale, hc_base, norm_w, d, iters,
                                                    eps, norm_eps, g_hn, g_y, g_pre, g_pm, ws);
     if ((e = cudaFuncSetAttribute(k_bwd_gx, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGxSmem)) !=
