@@ -14,10 +14,10 @@
 //   k_bwd_proj   32 tokens per CTA: the projection a = x W^T on the tensor
 //                cores, x and W staged through shared memory with cp.async,
 //                W read once per tile (W is the 24 x hc*d matrix hc_fn);
-//   k_bwd_token  one CTA per token: h, the statistics (sum x^2 among
-//                them), the split and
-//                Sinkhorn forward with its iterates, the Sinkhorn backward on
-//                one thread, g_pre_mix; writes a per-token record;
+//   k_bwd_token  one warp per token: h, the statistics (sum x^2 among
+//                them), g_pre_mix, the split and Sinkhorn forward with its
+//                iterates and the Sinkhorn backward (one matrix element per
+//                lane); writes a per-token record;
 //   k_bwd_gx     one CTA per (64 columns of d, all four streams) x (block of
 //                1,024 tokens), the column's 24 weights in registers: g_x,
 //                g_f, and the block's partial sums of g_hc_fn, g_norm_w and
@@ -35,9 +35,8 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kTokBlock = 1024;  // tokens per partial sum of a parameter gradient
 
-// The per-token record in the workspace (floats).  [0, kRec) is what k_bwd_gx
-// stages for each token; the rest feeds the hc_base / hc_scale sums or comes
-// from k_bwd_proj.
+// The per-token record in the workspace (floats).  [0, kA) is what k_bwd_gx
+// stages for each token; [kA, kA + 24) comes from k_bwd_proj.
 constexpr int kWs = 112;
 constexpr int kGa = 0;      // g_a[24]: the gradient of the projection a
 constexpr int kPost = 24;   // post[4]
@@ -46,7 +45,6 @@ constexpr int kPm = 44;     // pre_mix[4]
 constexpr int kRs = 48;     // rs_h = 1 / RMS(h)
 constexpr int kCr = 49;     // the statistic's coefficient of x in g_x
 constexpr int kK3 = 50;     // rs_h^3 / d * sum(h w g_hn)
-constexpr int kRec = 52;
 constexpr int kGz = 52;     // g_z[24]: the gradient of the pre-activations (= g_hc_base terms)
 constexpr int kGzm = 76;    // gzm[3]: the g_hc_scale terms
 constexpr int kA = 80;      // a[24] (k_bwd_proj)
@@ -55,28 +53,10 @@ constexpr int kSmall = 32;  // partial sums per block for hc_base (24) and hc_sc
 constexpr int kProjTok = 32;    // tokens per CTA of k_bwd_proj
 constexpr int kProjCols = 256;  // columns of x and W per stage
 constexpr int kProjStages = 3;
+constexpr int kTokWarps = 4;    // tokens (one warp each) per CTA of k_bwd_token
 constexpr int kGxCols = 64;     // columns of d per CTA of k_bwd_gx
 constexpr int kGxTile = 16;     // tokens per staged tile of k_bwd_gx
 constexpr int kGxStages = 4;
-
-// Sum of V per-thread values over the CTA; the totals land in tot[0..V).
-template <int V>
-__device__ __forceinline__ void block_sums(const float (&v)[V], float (*red)[32], float *tot) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-#pragma unroll
-    for (int i = 0; i < V; ++i) {
-        const float s = warp_sum(v[i]);
-        if (lane == 0) red[warp][i] = s;
-    }
-    __syncthreads();
-    if (threadIdx.x < V) {
-        float s = 0.0f;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) s += red[w][threadIdx.x];
-        tot[threadIdx.x] = s;
-    }
-    __syncthreads();
-}
 
 __device__ __forceinline__ float sigm(float z) { return 1.0f / (1.0f + expf(-z)); }
 
@@ -223,24 +203,27 @@ k_bwd_proj(const uint16_t *__restrict__ x, const float *__restrict__ hc_fn, int6
     }
 }
 
-// One token per CTA.  Shared memory: h of the token (d bf16), then the
-// Sinkhorn iterates and the reciprocals of their sums (2 * iters matrices of
-// 16 each).  Reads a from the record (k_bwd_proj), writes the rest of it.
-__global__ void __launch_bounds__(kThreads, 3)
+// One warp per token, kTokWarps tokens per CTA; no CTA-wide barrier, so
+// while one warp runs its Sinkhorn the others keep streaming.  Shared memory
+// per warp: h of the token (d bf16), then the Sinkhorn iterates and the
+// reciprocals of their sums (2 * iters matrices of 16 each).  Reads a from
+// the record (k_bwd_proj), writes the rest of it.
+__global__ void __launch_bounds__(kTokWarps * 32, 3)
 k_bwd_token(const uint16_t *__restrict__ x, const float *__restrict__ pre_mix,
             const uint16_t *__restrict__ f, const float *__restrict__ hc_scale,
-            const float *__restrict__ hc_base, const float *__restrict__ norm_w, int d, int iters,
-            float eps, float norm_eps, const float *__restrict__ g_hn, const float *__restrict__ g_y,
-            const float *__restrict__ g_pre, float *__restrict__ g_pm, float *__restrict__ ws) {
+            const float *__restrict__ hc_base, const float *__restrict__ norm_w, int64_t n, int d,
+            int iters, float eps, float norm_eps, const float *__restrict__ g_hn,
+            const float *__restrict__ g_y, const float *__restrict__ g_pre, float *__restrict__ g_pm,
+            float *__restrict__ ws) {
     extern __shared__ uint4 smem_u4[];
-    uint4 *sh = smem_u4;                                             // d/8 chunks of h
-    float *sP = reinterpret_cast<float *>(smem_u4 + (d >> 3));      // 2*iters*16 iterates
-    float *sI = sP + 2 * iters * kHC * kHC;                         // their 1 / (sum + eps)
-    __shared__ float red[kWarps][32];
-    __shared__ float tot[32];
-    __shared__ float sGz[kMix];
-    const int64_t t = blockIdx.x;
-    const int K = kHC * d, d8 = d >> 3;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t t = (int64_t)blockIdx.x * kTokWarps + warp;
+    if (t >= n) return;  // warp-uniform; nothing below synchronises the CTA
+    const int d8 = d >> 3, K = kHC * d;
+    const size_t per_warp = (size_t)d * 2 + (size_t)4 * iters * kHC * kHC * sizeof(float);
+    uint4 *sh = reinterpret_cast<uint4 *>(reinterpret_cast<unsigned char *>(smem_u4) + warp * per_warp);
+    float *sP = reinterpret_cast<float *>(sh + d8);  // 2*iters*16 iterates
+    float *sI = sP + 2 * iters * kHC * kHC;          // their 1 / (sum + eps)
     const uint16_t *xt = x + t * K;
     float *wt = ws + t * kWs;
     float pm[kHC];
@@ -249,168 +232,165 @@ k_bwd_token(const uint16_t *__restrict__ x, const float *__restrict__ pre_mix,
 
     // (b) h (kept), sum h^2, T = sum h w g_hn, g_post_k, g_comb_jk, sum x^2
     constexpr int kSumX2 = 2 + kHC + kHC * kHC;
-    {
-        float v[kSumX2 + 1];
+    float v[kSumX2 + 1];
 #pragma unroll
-        for (int i = 0; i <= kSumX2; ++i) v[i] = 0.0f;
-        for (int c = threadIdx.x; c < d8; c += kThreads) {
-            float xv[kHC][8], fv[8], gy[kHC][8], gh[8], w[8], h[8];
+    for (int i = 0; i <= kSumX2; ++i) v[i] = 0.0f;
+    for (int c = lane; c < d8; c += 32) {
+        float xv[kHC][8], fv[8], gy[kHC][8], gh[8], w[8], h[8];
 #pragma unroll
-            for (int s = 0; s < kHC; ++s) unpack8(__ldg(reinterpret_cast<const uint4 *>(xt + s * d) + c), xv[s]);
-            unpack8(__ldg(reinterpret_cast<const uint4 *>(f + t * d) + c), fv);
+        for (int s = 0; s < kHC; ++s) unpack8(__ldg(reinterpret_cast<const uint4 *>(xt + s * d) + c), xv[s]);
+        unpack8(__ldg(reinterpret_cast<const uint4 *>(f + t * d) + c), fv);
 #pragma unroll
-            for (int k = 0; k < kHC; ++k) load8f(g_y + (t * kHC + k) * d + 8 * c, gy[k]);
-            load8f(g_hn + t * d + 8 * c, gh);
-            load8f(norm_w + 8 * c, w);
+        for (int k = 0; k < kHC; ++k) load8f(g_y + (t * kHC + k) * d + 8 * c, gy[k]);
+        load8f(g_hn + t * d + 8 * c, gh);
+        load8f(norm_w + 8 * c, w);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                h[e] = pm[0] * xv[0][e];
+        for (int e = 0; e < 8; ++e) {
+            h[e] = pm[0] * xv[0][e];
 #pragma unroll
-                for (int s = 1; s < kHC; ++s) h[e] = fmaf(pm[s], xv[s][e], h[e]);
-            }
-            const uint4 hb = pack8(h);
-            sh[c] = hb;
-            unpack8(hb, h);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                v[0] = fmaf(h[e], h[e], v[0]);
-                v[1] = fmaf(h[e] * w[e], gh[e], v[1]);
-#pragma unroll
-                for (int k = 0; k < kHC; ++k) v[2 + k] = fmaf(fv[e], gy[k][e], v[2 + k]);
-#pragma unroll
-                for (int j = 0; j < kHC; ++j) {
-                    v[kSumX2] = fmaf(xv[j][e], xv[j][e], v[kSumX2]);
-#pragma unroll
-                    for (int k = 0; k < kHC; ++k)
-                        v[2 + kHC + j * kHC + k] = fmaf(xv[j][e], gy[k][e], v[2 + kHC + j * kHC + k]);
-                }
-            }
+            for (int s = 1; s < kHC; ++s) h[e] = fmaf(pm[s], xv[s][e], h[e]);
         }
-        block_sums<kSumX2 + 1>(v, red, tot);
-    }
-
-    const float rs = rsqrtf(tot[0] / (float)d + norm_eps);
-    const float k3 = rs * rs * rs / (float)d * tot[1];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-    if (warp == 0) {
-        // (c) warp 0: the comb part of the split and Sinkhorn, one matrix
-        // element per lane (lane & 15 = 4j + k; lanes 16-31 repeat 0-15);
-        // the row sums reduce over lanes ^1, ^2, the column sums over ^4, ^8.
-        const int e = lane & 15;
-        const float r = rsqrtf(tot[kSumX2] / (float)K + norm_eps);
-        const float s2 = __ldg(hc_scale + 2);
-        const float L = fmaf(wt[kA + 2 * kHC + e] * r, s2, __ldg(hc_base + 2 * kHC + e));
-        float mx = fmaxf(L, __shfl_xor_sync(0xffffffffu, L, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        const float ex = expf(L - mx);
-        float sum = ex + __shfl_xor_sync(0xffffffffu, ex, 1);
-        sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-        const float S = ex / sum;
-        float P = S + eps;
-        if (lane < 16) sP[e] = P;
-        // steps 1 .. 2*iters-1: a column step for odd, a row step for even
-        // steps; sI keeps each step's 1 / (sum + eps)
-        for (int st = 1; st < 2 * iters; ++st) {
-            const int m1 = (st & 1) ? 4 : 1, m2 = (st & 1) ? 8 : 2;
-            float q = P + __shfl_xor_sync(0xffffffffu, P, m1);
-            q += __shfl_xor_sync(0xffffffffu, q, m2);
-            const float inv = 1.0f / (q + eps);
-            P *= inv;
-            if (lane < 16) {
-                sP[st * 16 + e] = P;
-                sI[st * 16 + e] = inv;
-            }
-        }
-        if (lane < 16) wt[kComb + e] = P;
-        // back through the steps: g, the gradient of the current iterate
-        float g = tot[2 + kHC + e];
-        __syncwarp();
-        for (int st = 2 * iters - 1; st >= 1; --st) {
-            const int m1 = (st & 1) ? 4 : 1, m2 = (st & 1) ? 8 : 2;
-            const float pb = sP[st * 16 + e], inv = sI[st * 16 + e];
-            float dot = g * pb;
-            dot += __shfl_xor_sync(0xffffffffu, dot, m1);
-            dot += __shfl_xor_sync(0xffffffffu, dot, m2);
-            g = (g - dot) * inv;
-        }
-        // through the row softmax
-        float dot = g * S;
-        dot += __shfl_xor_sync(0xffffffffu, dot, 1);
-        dot += __shfl_xor_sync(0xffffffffu, dot, 2);
-        const float gzc = S * (g - dot);
-        if (lane < 16) sGz[2 * kHC + e] = gzc;
-        __syncwarp();
-        if (lane == 0) {
-            // pre and post (sigmoids), then the gradient of the projection
-            const float s0 = __ldg(hc_scale), s1 = __ldg(hc_scale + 1);
-            float a[kMix], m[kMix], gz[kMix], gm[kMix];
+        const uint4 hb = pack8(h);
+        sh[c] = hb;
+        unpack8(hb, h);
 #pragma unroll
-            for (int i = 0; i < kMix; ++i) {
-                a[i] = wt[kA + i];
-                m[i] = a[i] * r;
-            }
+        for (int e = 0; e < 8; ++e) {
+            v[0] = fmaf(h[e], h[e], v[0]);
+            v[1] = fmaf(h[e] * w[e], gh[e], v[1]);
 #pragma unroll
-            for (int i = 2 * kHC; i < kMix; ++i) gz[i] = sGz[i];
-            float gzm0 = 0.0f, gzm1 = 0.0f, gzm2 = 0.0f;
+            for (int k = 0; k < kHC; ++k) v[2 + k] = fmaf(fv[e], gy[k][e], v[2 + k]);
 #pragma unroll
             for (int j = 0; j < kHC; ++j) {
-                const float sp = sigm(fmaf(m[j], s0, __ldg(hc_base + j)));
-                gz[j] = (g_pre ? __ldg(g_pre + t * kHC + j) : 0.0f) * sp * (1.0f - sp);
-                const float sq = sigm(fmaf(m[kHC + j], s1, __ldg(hc_base + kHC + j)));
-                gz[kHC + j] = tot[2 + j] * 2.0f * sq * (1.0f - sq);
-                wt[kPost + j] = 2.0f * sq;
-                wt[kPm + j] = pm[j];
-                gm[j] = gz[j] * s0;
-                gm[kHC + j] = gz[kHC + j] * s1;
-                gzm0 = fmaf(gz[j], m[j], gzm0);
-                gzm1 = fmaf(gz[kHC + j], m[kHC + j], gzm1);
-            }
+                v[kSumX2] = fmaf(xv[j][e], xv[j][e], v[kSumX2]);
 #pragma unroll
-            for (int i = 2 * kHC; i < kMix; ++i) {
-                gm[i] = gz[i] * s2;
-                gzm2 = fmaf(gz[i], m[i], gzm2);
+                for (int k = 0; k < kHC; ++k)
+                    v[2 + kHC + j * kHC + k] = fmaf(xv[j][e], gy[k][e], v[2 + kHC + j * kHC + k]);
             }
-            float gr = 0.0f;
-#pragma unroll
-            for (int i = 0; i < kMix; ++i) gr = fmaf(gm[i], a[i], gr);
-#pragma unroll
-            for (int i = 0; i < kMix; ++i) {
-                wt[kGa + i] = gm[i] * r;
-                wt[kGz + i] = gz[i];
-            }
-            wt[kGzm] = gzm0;
-            wt[kGzm + 1] = gzm1;
-            wt[kGzm + 2] = gzm2;
-            wt[kRs] = rs;
-            wt[kCr] = -gr * r * r * r / (float)K;  // the statistic's term: cr * x_k
-            wt[kK3] = k3;
         }
     }
+#pragma unroll
+    for (int i = 0; i <= kSumX2; ++i) v[i] = warp_sum(v[i]);  // every lane holds the totals
+    __syncwarp();  // h in shared memory is visible to the whole warp
+    const float rs = rsqrtf(v[0] / (float)d + norm_eps);
+    const float k3 = rs * rs * rs / (float)d * v[1];
+    const float r = rsqrtf(v[kSumX2] / (float)K + norm_eps);
 
-    // (d) warps 1-7, beside (c): g_pre_mix_s = sum_c x_s g_h, with
-    // g_h = rs w g_hn - k3 h
+    // (d) g_pre_mix_s = sum_c x_s g_h, with g_h = rs w g_hn - k3 h
     {
         float gp[kHC] = {0.0f, 0.0f, 0.0f, 0.0f};
-        if (warp != 0) {
-            for (int c = threadIdx.x - 32; c < d8; c += kThreads - 32) {
-                float h[8], w[8], gh[8], gu[8];
-                unpack8(sh[c], h);
-                load8f(norm_w + 8 * c, w);
-                load8f(g_hn + t * d + 8 * c, gh);
+        for (int c = lane; c < d8; c += 32) {
+            float h[8], w[8], gh[8], gu[8];
+            unpack8(sh[c], h);
+            load8f(norm_w + 8 * c, w);
+            load8f(g_hn + t * d + 8 * c, gh);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) gu[e] = rs * (w[e] * gh[e]) - k3 * h[e];
+            for (int e = 0; e < 8; ++e) gu[e] = rs * (w[e] * gh[e]) - k3 * h[e];
 #pragma unroll
-                for (int s = 0; s < kHC; ++s) {
-                    float xv[8];
-                    unpack8(__ldg(reinterpret_cast<const uint4 *>(xt + s * d) + c), xv);
+            for (int s = 0; s < kHC; ++s) {
+                float xv[8];
+                unpack8(__ldg(reinterpret_cast<const uint4 *>(xt + s * d) + c), xv);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) gp[s] = fmaf(xv[e], gu[e], gp[s]);
-                }
+                for (int e = 0; e < 8; ++e) gp[s] = fmaf(xv[e], gu[e], gp[s]);
             }
         }
-        block_sums<kHC>(gp, red, tot);
-        if (threadIdx.x < kHC) g_pm[t * kHC + threadIdx.x] = tot[threadIdx.x];
+#pragma unroll
+        for (int s = 0; s < kHC; ++s) gp[s] = warp_sum(gp[s]);
+        if (lane == 0) *reinterpret_cast<float4 *>(g_pm + t * kHC) = make_float4(gp[0], gp[1], gp[2], gp[3]);
+    }
+
+    // (c) the comb part of the split and Sinkhorn, one matrix element per lane
+    // (lane & 15 = 4j + k; lanes 16-31 repeat 0-15); the row sums reduce over
+    // lanes ^1, ^2, the column sums over ^4, ^8.
+    const int e = lane & 15;
+    const float s2 = __ldg(hc_scale + 2);
+    const float L = fmaf(wt[kA + 2 * kHC + e] * r, s2, __ldg(hc_base + 2 * kHC + e));
+    float mx = fmaxf(L, __shfl_xor_sync(0xffffffffu, L, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    const float ex = expf(L - mx);
+    float sum = ex + __shfl_xor_sync(0xffffffffu, ex, 1);
+    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+    const float S = ex / sum;
+    float P = S + eps;
+    // steps 1 .. 2*iters-1: a column step for odd, a row step for even steps;
+    // sI keeps each step's 1 / (sum + eps)
+    for (int st = 1; st < 2 * iters; ++st) {
+        const int m1 = (st & 1) ? 4 : 1, m2 = (st & 1) ? 8 : 2;
+        float q = P + __shfl_xor_sync(0xffffffffu, P, m1);
+        q += __shfl_xor_sync(0xffffffffu, q, m2);
+        const float inv = 1.0f / (q + eps);
+        P *= inv;
+        if (lane < 16) {
+            sP[st * 16 + e] = P;
+            sI[st * 16 + e] = inv;
+        }
+    }
+    if (lane < 16) wt[kComb + e] = P;
+    // back through the steps: g, the gradient of the current iterate
+    float g = 0.0f;
+#pragma unroll
+    for (int k = 0; k < kHC * kHC; ++k)
+        if (e == k) g = v[2 + kHC + k];
+    __syncwarp();
+    for (int st = 2 * iters - 1; st >= 1; --st) {
+        const int m1 = (st & 1) ? 4 : 1, m2 = (st & 1) ? 8 : 2;
+        const float pb = sP[st * 16 + e], inv = sI[st * 16 + e];
+        float dot = g * pb;
+        dot += __shfl_xor_sync(0xffffffffu, dot, m1);
+        dot += __shfl_xor_sync(0xffffffffu, dot, m2);
+        g = (g - dot) * inv;
+    }
+    // through the row softmax
+    float dot = g * S;
+    dot += __shfl_xor_sync(0xffffffffu, dot, 1);
+    dot += __shfl_xor_sync(0xffffffffu, dot, 2);
+    const float gzc = S * (g - dot);
+
+    // pre and post (sigmoids), then the gradient of the projection; lane i
+    // takes mix row i (lanes 0-3 pre, 4-7 post, 8-23 comb)
+    const float s0 = __ldg(hc_scale), s1 = __ldg(hc_scale + 1);
+    const int i = lane < kMix ? lane : 0;
+    const float a = wt[kA + i];
+    const float m = a * r;
+    const float gzc_i = __shfl_sync(0xffffffffu, gzc, (i - 2 * kHC) & 15);
+    float gz, gm;
+    if (i < kHC) {
+        const float sp = sigm(fmaf(m, s0, __ldg(hc_base + i)));
+        gz = (g_pre ? __ldg(g_pre + t * kHC + i) : 0.0f) * sp * (1.0f - sp);
+        gm = gz * s0;
+    } else if (i < 2 * kHC) {
+        const float sq = sigm(fmaf(m, s1, __ldg(hc_base + i)));
+        float gpost = 0.0f;  // g_post of stream i - hc
+#pragma unroll
+        for (int k = 0; k < kHC; ++k)
+            if (i - kHC == k) gpost = v[2 + k];
+        gz = gpost * 2.0f * sq * (1.0f - sq);
+        gm = gz * s1;
+        if (lane < kMix) wt[kPost + i - kHC] = 2.0f * sq;
+    } else {
+        gz = gzc_i;
+        gm = gz * s2;
+    }
+    const bool live = lane < kMix;
+    const float zm = live ? gz * m : 0.0f;
+    // gzm per group (pre 0-3, post 4-7, comb 8-23) and gr = sum_i gm_i a_i
+    float z0 = (lane < kHC) ? zm : 0.0f, z1 = (lane >= kHC && lane < 2 * kHC) ? zm : 0.0f,
+          z2 = (lane >= 2 * kHC) ? zm : 0.0f, gr = live ? gm * a : 0.0f;
+    z0 = warp_sum(z0);
+    z1 = warp_sum(z1);
+    z2 = warp_sum(z2);
+    gr = warp_sum(gr);
+    if (live) {
+        wt[kGa + i] = gm * r;
+        wt[kGz + i] = gz;
+    }
+    if (lane == 0) {
+        *reinterpret_cast<float4 *>(wt + kPm) = make_float4(pm[0], pm[1], pm[2], pm[3]);
+        wt[kGzm] = z0;
+        wt[kGzm + 1] = z1;
+        wt[kGzm + 2] = z2;
+        wt[kRs] = rs;
+        wt[kCr] = -gr * r * r * r / (float)K;  // the statistic's term: cr * x_k
+        wt[kK3] = k3;
     }
 }
 
@@ -716,7 +696,7 @@ cudaError_t launch_block_step_backward(const uint16_t *x, const float *pre_mix, 
     float *part_fn = ws + n * kWs;
     float *part_w = part_fn + (int64_t)blocks * kMix * K;
     float *part_s = part_w + (int64_t)blocks * d;
-    const size_t smem = (size_t)d * 2 + (size_t)(4 * iters) * kHC * kHC * sizeof(float);
+    const size_t smem = kTokWarps * ((size_t)d * 2 + (size_t)(4 * iters) * kHC * kHC * sizeof(float));
     cudaError_t e = cudaFuncSetAttribute(k_bwd_token, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
@@ -725,8 +705,8 @@ cudaError_t launch_block_step_backward(const uint16_t *x, const float *pre_mix, 
         return e;
     k_bwd_proj<<<(unsigned)((n + kProjTok - 1) / kProjTok), kThreads, kProjSmem, s>>>(x, hc_fn, n, (int)K,
                                                                                    ws);
-    k_bwd_token<<<(unsigned)n, kThreads, smem, s>>>(x, pre_mix, f, hc_scale, hc_base, norm_w, d, iters,
-                                                   eps, norm_eps, g_hn, g_y, g_pre, g_pm, ws);
+    k_bwd_token<<<(unsigned)((n + kTokWarps - 1) / kTokWarps), kTokWarps * 32, smem, s>>>(
+        x, pre_mix, f, hc_scale, hc_base, norm_w, n, d, iters, eps, norm_eps, g_hn, g_y, g_pre, g_pm, ws);
     if ((e = cudaFuncSetAttribute(k_bwd_gx, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGxSmem)) !=
         cudaSuccess)
         return e;
