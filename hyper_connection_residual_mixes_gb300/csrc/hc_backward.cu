@@ -56,7 +56,7 @@ constexpr int kProjStages = 3;
 constexpr int kTokWarps = 4;    // tokens (one warp each) per CTA of k_bwd_token
 constexpr int kGxCols = 64;     // columns of d per CTA of k_bwd_gx
 constexpr int kGxTile = 16;     // tokens per staged tile of k_bwd_gx
-constexpr int kGxStages = 4;
+constexpr int kGxStages = 3;
 
 __device__ __forceinline__ float sigm(float z) { return 1.0f / (1.0f + expf(-z)); }
 
@@ -431,7 +431,7 @@ static_assert(sizeof(GxStage) % 16 == 0 && (kXRow * 2) % 16 == 0 && (kGyRow * 4)
               "staged rows must keep 16-byte alignment");
 static_assert(kGxTile == 16 && kGxCols == 8 * kWarps && kMix == 24, "k_bwd_gx's fragment map");
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
 k_bwd_gx(const uint16_t *__restrict__ x, const float *__restrict__ hc_fn,
          const float *__restrict__ norm_w, const float *__restrict__ g_hn,
          const float *__restrict__ g_y, const float *__restrict__ ws, int64_t n, int d,
