@@ -52,7 +52,7 @@ constexpr int kSmall = 32;  // partial sums per block for hc_base (24) and hc_sc
 
 constexpr int kProjTok = 32;    // tokens per CTA of k_bwd_proj
 constexpr int kProjCols = 256;  // columns of x and W per stage
-constexpr int kProjStages = 3;
+constexpr int kProjStages = 2;
 constexpr int kTokWarps = 4;    // tokens (one warp each) per CTA of k_bwd_token
 constexpr int kGxCols = 64;     // columns of d per CTA of k_bwd_gx
 constexpr int kGxTile = 16;     // tokens per staged tile of k_bwd_gx
@@ -119,7 +119,7 @@ static_assert(sizeof(ProjStage) % 16 == 0 && (kPxRow * 2) % 16 == 0 && (kPwRow *
 static_assert(kProjSmem >= sizeof(float) * kWarps * kProjTok * kMix, "the partial sums reuse the ring");
 static_assert(kProjTok == 32 && kProjCols == 32 * kWarps, "k_bwd_proj's fragment map");
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
 k_bwd_proj(const uint16_t *__restrict__ x, const float *__restrict__ hc_fn, int64_t n, int K,
            float *__restrict__ ws) {
     extern __shared__ uint4 smem_u4[];

@@ -131,3 +131,50 @@ def test_backward_general_pre_mix():
     u = fw["h_norm"] / w                       # h * rs_h, up to the final cast
     term = np.abs(u * _np(up["g_h_norm"]).astype(np.float64)).max(axis=0)
     _compare(got, ref, extra={"g_norm_w": 4 * 2.0 ** -8 * term * 1.01})
+
+
+def test_backward_long_prefill_sampled_tokens_and_additivity():
+    """The long-prefill size (65,536 tokens x d = 5120) with the workspace
+    entry, as the backward bench calls it.  Each token's gradients depend on
+    that token alone, so g_x, g_pre_mix and g_f are checked against the oracle
+    on sampled tokens (the last one among them).  The parameter gradients are
+    sums over all 64 token blocks; the full batch must equal the sum of its
+    two halves."""
+    case = inputs.long_prefill(device=DEV, materialize_f=False)
+    n, d = case.n, case.d
+    p = case.params[0]
+    f0 = inputs.long_prefill_f(0, n, d, DEV)
+    g = torch.Generator(device=DEV).manual_seed(5)
+    g_hn = torch.randn((n, d), device=DEV, generator=g)
+    g_y = torch.randn((n, 4, d), device=DEV, generator=g)
+    g_pre = torch.randn((n, 4), device=DEV, generator=g)
+    full = hcg.hc_block_step_backward(case.x, case.pre_mix, f0, *p.astuple(), g_hn, g_y, g_pre)
+    half = n // 2
+    parts = [hcg.hc_block_step_backward(case.x[a:b], case.pre_mix[a:b], f0[a:b], *p.astuple(), g_hn[a:b],
+                                        g_y[a:b], g_pre[a:b]) for a, b in ((0, half), (half, n))]
+    torch.cuda.synchronize()
+    assert _lib.raw("hc_consume_device_error", None) == 0
+    for k in ("g_x", "g_pre_mix", "g_f"):   # per token: the halves give the same bits
+        assert torch.equal(full[k][:half], parts[0][k]) and torch.equal(full[k][half:], parts[1][k]), k
+    for k in ("g_hc_fn", "g_hc_scale", "g_hc_base", "g_norm_w"):
+        a = _np(full[k]).astype(np.float64)
+        b = _np(parts[0][k]).astype(np.float64) + _np(parts[1][k]).astype(np.float64)
+        # the same 64 block partials, associated differently at the top: rounding only;
+        # a dropped or misplaced block moves a sum by a sizeable part of its scale
+        assert np.all(np.abs(a - b) <= 1e-5 * np.abs(a) + 1e-4 * np.abs(a).max()), k
+    rows = np.sort(np.random.default_rng(17).choice(n - 1, 5, replace=False)).tolist() + [n - 1]
+    sel = torch.tensor(rows, device=DEV)
+    pick = lambda t: t.index_select(0, sel).cpu()
+    ref = oracle.side_backward(
+        oracle.bf16_to_f64(oracle.bf16_bits(pick(case.x))), _np(pick(case.pre_mix)).astype(np.float64),
+        oracle.bf16_to_f64(oracle.bf16_bits(pick(f0))), *(_np(t).astype(np.float64) for t in p.astuple()),
+        _np(pick(g_hn)).astype(np.float64), _np(pick(g_y)).astype(np.float64),
+        _np(pick(g_pre)).astype(np.float64), rounded=True)
+    for k in ("g_x", "g_pre_mix", "g_f"):
+        got = _np(pick(full[k])).astype(np.float64)
+        r = ref[k]
+        # general pre_mix: an h flip moves g_x / g_pre_mix by at most the term it feeds;
+        # the per-token bound of the other tests, with ATOL on each token's own scale
+        scale = np.abs(r).reshape(len(rows), -1).max(axis=1).reshape((-1,) + (1,) * (r.ndim - 1))
+        err = np.abs(got - r)
+        assert np.all(err <= RTOL_TOK * np.abs(r) + 2 * ATOL * scale), (k, float(err.max()))
