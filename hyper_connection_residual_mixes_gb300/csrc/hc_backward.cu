@@ -78,17 +78,15 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// tf32 helpers for the tensor-core contractions (k_bwd_proj, k_bwd_gx).  A value a is
-// carried as hi + lo, hi = tf32(a), lo = tf32(a - hi); products take
-// hi*hi + lo*hi + hi*lo (the lo*lo term is below fp32 rounding of the sum).
-__device__ __forceinline__ uint32_t tf32_of(float a) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(a));
-    return r;
-}
+// tf32 helpers for the tensor-core contractions (k_bwd_proj, k_bwd_gx).  A
+// value a is carried as hi + lo: hi = a with its low 13 mantissa bits
+// cleared (a tf32 value), lo = a - hi (exact in fp32).  The MMA reads the top
+// 19 bits of each operand, so lo enters with a relative error below 2^-10 of
+// itself, i.e. 2^-20 of a.  Products take hi*hi + lo*hi + hi*lo; the lo*lo
+// term is of the same order and is dropped.
 __device__ __forceinline__ void tf32_split(float a, uint32_t &hi, uint32_t &lo) {
-    hi = tf32_of(a);
-    lo = tf32_of(a - __uint_as_float(hi));
+    hi = __float_as_uint(a) & 0xffffe000u;
+    lo = __float_as_uint(a - __uint_as_float(hi));
 }
 // D += A (16x8, row) * B (8x8, col), tf32 inputs, fp32 accumulators
 __device__ __forceinline__ void mma_tf32(float (&dacc)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
