@@ -19,13 +19,17 @@
 //                iterates and the Sinkhorn backward (one matrix element per
 //                lane); writes a per-token record;
 //   k_bwd_gx     one CTA per (64 columns of d, all four streams) x (block of
-//                1,024 tokens), the column's 24 weights in registers: g_x,
+//                1,024 tokens), inputs staged by bulk copies, the two 24-row
+//                contractions on the tensor cores: g_x,
 //                g_f, and the block's partial sums of g_hc_fn, g_norm_w and
 //                the per-token terms of g_hc_base / g_hc_scale.
 // The partial sums are then added over the blocks in a fixed order, so every
 // result is deterministic (no atomics).
+#include <cuda.h>
+
 #include "hc_device.cuh"
 #include "hc_launch.h"
+#include "hc_ptx.cuh"
 
 namespace hc {
 
@@ -402,7 +406,8 @@ k_bwd_token(const uint16_t *__restrict__ x, const float *__restrict__ pre_mix,
 // h_c rs_h g_hn.  The CTAs of column block 0 also sum the block's g_z and gzm
 // (the hc_base and hc_scale terms).
 // Tiles of kGxTile = 16 tokens (x, g_y, g_hn for the CTA's columns and the
-// token records) are staged through a cp.async ring.  Warp w owns the
+// token records) are staged through a ring of bulk copies, one per staged
+// row (160 per tile), each stage completing on its mbarrier.  Warp w owns the
 // columns c0 + 8w .. +7 of all four streams.  The two contractions over the
 // 24 mix rows run on the tensor cores (mma m16n8k8, tf32 split in hi + lo):
 //   g_a (16 tokens x 24) . W (24 x the warp's 32 columns), n-tile = stream;
@@ -411,8 +416,9 @@ k_bwd_token(const uint16_t *__restrict__ x, const float *__restrict__ pre_mix,
 // The rest is per (token, column) in the accumulator layout: lane (g, q) =
 // (lane / 4, lane % 4) holds tokens g and g + 8, columns c0 + 8w + 2q and +1,
 // for the four streams.  The staged rows are padded so that these loads hit
-// distinct shared-memory banks.  Tokens past the block are zero-filled and
-// skipped.
+// distinct shared-memory banks.  Rows past the block are not copied: they
+// keep finite values (the ring is zeroed once), their g_a is masked to zero in
+// the g_hc_fn sum, and their outputs are not written.
 constexpr int kXRow = kHC * kGxCols + 8;   // bf16 per token row of the x tile
 constexpr int kGyRow = kHC * kGxCols + 8;  // floats per token row of the g_y tile
 constexpr int kGhRow = kGxCols + 8;        // floats per token row of the g_hn tile
@@ -447,34 +453,50 @@ k_bwd_gx(const uint16_t *__restrict__ x, const float *__restrict__ hc_fn,
     const int ntiles = (int)((t1 - t0 + kGxTile - 1) / kGxTile);
     const bool small = blockIdx.x == 0;
 
+    __shared__ __align__(8) uint64_t full_bar[kGxStages];
+    __shared__ volatile int s_abort;
+    constexpr uint32_t kRowBytes = kHC * kGxCols * 2 + kHC * kGxCols * 4 + kGxCols * 4 + kA * 4;  // per token
+    {
+        // zero the ring once (finite values in rows that partial tiles do not copy)
+        uint4 *z = smem_u4;
+        for (size_t k = threadIdx.x; k < kGxSmem / 16; k += kThreads) z[k] = make_uint4(0u, 0u, 0u, 0u);
+        if (threadIdx.x == 0) {
+            for (int k = 0; k < kGxStages; ++k) mbar_init(smem_u32(&full_bar[k]), 1);
+            s_abort = 0;
+            fence_mbar_init_cluster();
+        }
+        fence_proxy_async_smem();  // the zeros before any bulk copy into the ring
+        __syncthreads();
+    }
+    // One bulk copy per staged row: thread k < 160 copies row k of the tile
+    // (x rows (u, stream) 128 B, g_y rows 256 B, g_hn rows 256 B, records 320 B).
     auto issue = [&](int it) {
-        if (it < ntiles) {
-            GxStage &S = stg[it % kGxStages];
-            const int64_t tb = t0 + (int64_t)it * kGxTile;
-            for (int k = threadIdx.x; k < kGxTile * kHC * (kGxCols / 8); k += kThreads) {
-                const int u = k / (kHC * kGxCols / 8), j = (k / (kGxCols / 8)) % kHC, v = k % (kGxCols / 8);
-                const bool ok = tb + u < t1;
-                cp_async16(&S.x[u][j * kGxCols + 8 * v], ok ? x + ((tb + u) * kHC + j) * d + c0 + 8 * v : x,
-                           ok ? 16 : 0);
-            }
-            for (int k = threadIdx.x; k < kGxTile * kHC * (kGxCols / 4); k += kThreads) {
-                const int u = k / (kHC * kGxCols / 4), j = (k / (kGxCols / 4)) % kHC, v = k % (kGxCols / 4);
-                const bool ok = tb + u < t1;
-                cp_async16(&S.gy[u][j * kGxCols + 4 * v], ok ? g_y + ((tb + u) * kHC + j) * d + c0 + 4 * v : g_y,
-                           ok ? 16 : 0);
-            }
-            for (int k = threadIdx.x; k < kGxTile * (kGxCols / 4); k += kThreads) {
-                const int u = k / (kGxCols / 4), v = k % (kGxCols / 4);
-                const bool ok = tb + u < t1;
-                cp_async16(&S.ghn[u][4 * v], ok ? g_hn + (tb + u) * d + c0 + 4 * v : g_hn, ok ? 16 : 0);
-            }
-            for (int k = threadIdx.x; k < kGxTile * (kA / 4); k += kThreads) {
-                const int u = k / (kA / 4), v = k % (kA / 4);
-                const bool ok = tb + u < t1;
-                cp_async16(&S.rec[u][4 * v], ok ? ws + (tb + u) * kWs + 4 * v : ws, ok ? 16 : 0);
+        if (it >= ntiles) return;
+        const int slot = it % kGxStages;
+        GxStage &S = stg[slot];
+        const int64_t tb = t0 + (int64_t)it * kGxTile;
+        const int cnt = (int)((t1 - tb < kGxTile) ? t1 - tb : kGxTile);
+        const uint32_t bar = smem_u32(&full_bar[slot]);
+        const int k = threadIdx.x;
+        if (k == 0) mbar_arrive_expect_tx(bar, (uint32_t)cnt * kRowBytes);
+        if (k < 2 * kGxTile * kHC + 2 * kGxTile) {
+            fence_proxy_async_smem();  // the slot's earlier reads before the async writes
+            if (k < kGxTile * kHC) {
+                const int u = k / kHC, j = k % kHC;
+                if (u < cnt)
+                    bulk_load(smem_u32(&S.x[u][j * kGxCols]), x + ((tb + u) * kHC + j) * d + c0, kGxCols * 2, bar);
+            } else if (k < 2 * kGxTile * kHC) {
+                const int u = (k - kGxTile * kHC) / kHC, j = (k - kGxTile * kHC) % kHC;
+                if (u < cnt)
+                    bulk_load(smem_u32(&S.gy[u][j * kGxCols]), g_y + ((tb + u) * kHC + j) * d + c0, kGxCols * 4, bar);
+            } else if (k < 2 * kGxTile * kHC + kGxTile) {
+                const int u = k - 2 * kGxTile * kHC;
+                if (u < cnt) bulk_load(smem_u32(&S.ghn[u][0]), g_hn + (tb + u) * d + c0, kGxCols * 4, bar);
+            } else {
+                const int u = k - 2 * kGxTile * kHC - kGxTile;
+                if (u < cnt) bulk_load(smem_u32(&S.rec[u][0]), ws + (tb + u) * kWs, kA * 4, bar);
             }
         }
-        cp_async_commit();
     };
 
     // W fragments (B of the first contraction): stream nt, mix rows 8ks + q (+4),
@@ -502,9 +524,9 @@ k_bwd_gx(const uint16_t *__restrict__ x, const float *__restrict__ hc_fn,
 #pragma unroll
     for (int it = 0; it < kGxStages - 1; ++it) issue(it);
     for (int it = 0; it < ntiles; ++it) {
-        cp_async_wait<kGxStages - 2>();
-        __syncthreads();  // tile it landed for every thread; slot (it - 1) is free
+        __syncthreads();  // every thread is done with tile it - 1: its slot is free
         issue(it + kGxStages - 1);
+        mbar_wait<false>(smem_u32(&full_bar[it % kGxStages]), (uint32_t)(it / kGxStages) & 1u, &s_abort);
         const GxStage &S = stg[it % kGxStages];
         const int64_t tb = t0 + (int64_t)it * kGxTile;
         const int cnt = (int)((t1 - tb < kGxTile) ? t1 - tb : kGxTile);
@@ -542,14 +564,15 @@ k_bwd_gx(const uint16_t *__restrict__ x, const float *__restrict__ hc_fn,
                 bx[nt][0] = (uint32_t)S.x[ta][nt * kGxCols + cw + g] << 16;
                 bx[nt][1] = (uint32_t)S.x[tb4][nt * kGxCols + cw + g] << 16;
             }
+            const bool va = ta < cnt, vb = tb4 < cnt;  // rows past the tile take no part
 #pragma unroll
             for (int mt = 0; mt < 2; ++mt) {
                 uint32_t ah[4], al[4];
-                tf32_split(S.rec[ta][kGa + 16 * mt + g], ah[0], al[0]);
-                tf32_split(S.rec[tb4][kGa + 16 * mt + g], ah[2], al[2]);
+                tf32_split(va ? S.rec[ta][kGa + 16 * mt + g] : 0.0f, ah[0], al[0]);
+                tf32_split(vb ? S.rec[tb4][kGa + 16 * mt + g] : 0.0f, ah[2], al[2]);
                 if (mt == 0) {
-                    tf32_split(S.rec[ta][kGa + g + 8], ah[1], al[1]);
-                    tf32_split(S.rec[tb4][kGa + g + 8], ah[3], al[3]);
+                    tf32_split(va ? S.rec[ta][kGa + g + 8] : 0.0f, ah[1], al[1]);
+                    tf32_split(vb ? S.rec[tb4][kGa + g + 8] : 0.0f, ah[3], al[3]);
                 } else {  // rows 24 .. 31 are padding
                     ah[1] = al[1] = ah[3] = al[3] = 0u;
                 }
@@ -618,7 +641,6 @@ k_bwd_gx(const uint16_t *__restrict__ x, const float *__restrict__ hc_fn,
             }
         }
     }
-    cp_async_wait<0>();
     // g_hc_fn partials: accumulator (row 16mt + g (+8), stream nt, columns 2q, 2q + 1)
 #pragma unroll
     for (int mt = 0; mt < 2; ++mt)
@@ -671,6 +693,20 @@ constexpr size_t kStaticScratchBytes = size_t(64) << 20;
 static __device__ __align__(256) unsigned char g_bwd_scratch[kStaticScratchBytes];
 
 size_t backward_static_scratch_bytes() { return kStaticScratchBytes; }
+
+cudaError_t consume_backward_device_error(cudaStream_t s, unsigned int *flag) {
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return e;
+    unsigned int v = 0;
+    e = cudaMemcpyFromSymbol(&v, g_device_error, sizeof v);
+    if (e != cudaSuccess) return e;
+    *flag = v;
+    if (v) {
+        const unsigned int zero = 0;
+        e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof zero);
+    }
+    return e;
+}
 
 cudaError_t backward_static_scratch(void **ptr) { return cudaGetSymbolAddress(ptr, g_bwd_scratch); }
 

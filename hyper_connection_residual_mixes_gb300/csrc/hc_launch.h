@@ -77,5 +77,6 @@ cudaError_t launch_chain_side(const uint16_t *x, const uint16_t *f, const float 
 // when they time out (each of the two kernel files keeps its own flag).
 cudaError_t consume_device_error(cudaStream_t s, unsigned int *flag);
 cudaError_t consume_chain_device_error(cudaStream_t s, unsigned int *flag);
+cudaError_t consume_backward_device_error(cudaStream_t s, unsigned int *flag);
 
 }  // namespace hc

@@ -10,8 +10,9 @@
 namespace hc {
 
 // Set by any kernel whose bounded wait ran out; read and cleared by
-// hc_consume_device_error().  Only one translation unit (hc_block_cluster.cu)
-// includes this header, so this file-scope variable is the library's one flag.
+// hc_consume_device_error().  Each translation unit that includes this header
+// has its own copy of this file-scope flag and its own consume function, and
+// hc_consume_device_error() reads them all.
 static __device__ unsigned int g_device_error = 0;
 
 constexpr unsigned int kErrWaitTimeout = 1u;
