@@ -58,6 +58,7 @@ constexpr int kProjTok = 32;    // tokens per CTA of k_bwd_proj
 constexpr int kProjCols = 256;  // columns of x and W per stage
 constexpr int kProjStages = 2;
 constexpr int kTokWarps = 4;    // tokens (one warp each) per CTA of k_bwd_token
+constexpr int kTokMinCtas = 5;  // CTAs of k_bwd_token per SM the register budget aims at
 constexpr int kGxCols = 64;     // columns of d per CTA of k_bwd_gx
 constexpr int kGxTile = 16;     // tokens per staged tile of k_bwd_gx
 constexpr int kGxStages = 3;
@@ -69,6 +70,31 @@ __device__ __forceinline__ void load8f(const float *p, float (&o)[8]) {
     const float4 b = __ldg(reinterpret_cast<const float4 *>(p) + 1);
     o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w; o[4] = b.x; o[5] = b.y; o[6] = b.z; o[7] = b.w;
 }
+__device__ __forceinline__ void unpack4(const uint2 &v, float (&o)[4]) {
+    o[0] = bf16lo(v.x);
+    o[1] = __uint_as_float(v.x & 0xffff0000u);
+    o[2] = bf16lo(v.y);
+    o[3] = __uint_as_float(v.y & 0xffff0000u);
+}
+__device__ __forceinline__ void load4f(const float *p, float (&o)[4]) {
+    const float4 a = __ldg(reinterpret_cast<const float4 *>(p));
+    o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w;
+}
+// h = bf16(sum_s pm_s x_s) for four channels, as the forward rounds it
+__device__ __forceinline__ void hc_pre4(const float (&pm)[kHC], const float (&xv)[kHC][4], float (&h)[4]) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        h[e] = pm[0] * xv[0][e];
+#pragma unroll
+        for (int s = 1; s < kHC; ++s) h[e] = fmaf(pm[s], xv[s][e], h[e]);
+    }
+    const uint32_t a = pack_bf16x2(h[0], h[1]), b = pack_bf16x2(h[2], h[3]);
+    h[0] = bf16lo(a);
+    h[1] = __uint_as_float(a & 0xffff0000u);
+    h[2] = bf16lo(b);
+    h[3] = __uint_as_float(b & 0xffff0000u);
+}
+
 // 16-byte asynchronous copy global -> shared; src_bytes = 0 fills zeros
 // (the source address is not read then).
 __device__ __forceinline__ void cp_async16(void *sdst, const void *gsrc, int src_bytes) {
@@ -206,11 +232,13 @@ k_bwd_proj(const uint16_t *__restrict__ x, const float *__restrict__ hc_fn, int6
 }
 
 // One warp per token, kTokWarps tokens per CTA; no CTA-wide barrier, so
-// while one warp runs its Sinkhorn the others keep streaming.  Shared memory
-// per warp: h of the token (d bf16), then the Sinkhorn iterates and the
-// reciprocals of their sums (2 * iters matrices of 16 each).  Reads a from
-// the record (k_bwd_proj), writes the rest of it.
-__global__ void __launch_bounds__(kTokWarps * 32, 3)
+// while one warp runs its Sinkhorn the others keep streaming.  The token is
+// read once, in chunks of four channels (small register footprint, many
+// warps in flight).  Shared memory per warp: the Sinkhorn iterates and the
+// reciprocals of their sums
+// (2 * iters matrices of 16 each).  Reads a from the record (k_bwd_proj),
+// writes the rest of it.
+__global__ void __launch_bounds__(kTokWarps * 32, kTokMinCtas)
 k_bwd_token(const uint16_t *__restrict__ x, const float *__restrict__ pre_mix,
             const uint16_t *__restrict__ f, const float *__restrict__ hc_scale,
             const float *__restrict__ hc_base, const float *__restrict__ norm_w, int64_t n, int d,
@@ -221,49 +249,45 @@ k_bwd_token(const uint16_t *__restrict__ x, const float *__restrict__ pre_mix,
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t t = (int64_t)blockIdx.x * kTokWarps + warp;
     if (t >= n) return;  // warp-uniform; nothing below synchronises the CTA
-    const int d8 = d >> 3, K = kHC * d;
-    const size_t per_warp = (size_t)d * 2 + (size_t)4 * iters * kHC * kHC * sizeof(float);
-    uint4 *sh = reinterpret_cast<uint4 *>(reinterpret_cast<unsigned char *>(smem_u4) + warp * per_warp);
-    float *sP = reinterpret_cast<float *>(sh + d8);  // 2*iters*16 iterates
-    float *sI = sP + 2 * iters * kHC * kHC;          // their 1 / (sum + eps)
+    const int d4 = d >> 2, K = kHC * d;
+    float *sP = reinterpret_cast<float *>(smem_u4) + (size_t)warp * 4 * iters * kHC * kHC;  // 2*iters*16 iterates
+    float *sI = sP + 2 * iters * kHC * kHC;                                                // their 1 / (sum + eps)
     const uint16_t *xt = x + t * K;
     float *wt = ws + t * kWs;
     float pm[kHC];
 #pragma unroll
     for (int s = 0; s < kHC; ++s) pm[s] = __ldg(pre_mix + t * kHC + s);
 
-    // (b) h (kept), sum h^2, T = sum h w g_hn, g_post_k, g_comb_jk, sum x^2
-    constexpr int kSumX2 = 2 + kHC + kHC * kHC;
-    float v[kSumX2 + 1];
+    // (b) one pass over the token: sum h^2, T = sum h w g_hn, g_post_k,
+    // g_comb_jk, sum x^2, and for g_pre_mix the sums A_s = sum_c x_s w g_hn and
+    // B_s = sum_c x_s h, since g_pre_mix_s = sum_c x_s (rs w g_hn - k3 h)
+    // = rs A_s - k3 B_s (rs and k3 are known only after the pass)
+    constexpr int kSumX2 = 2 + kHC + kHC * kHC, kSumA = kSumX2 + 1, kSumB = kSumA + kHC;
+    float v[kSumB + kHC];
 #pragma unroll
-    for (int i = 0; i <= kSumX2; ++i) v[i] = 0.0f;
-    for (int c = lane; c < d8; c += 32) {
-        float xv[kHC][8], fv[8], gy[kHC][8], gh[8], w[8], h[8];
+    for (int i = 0; i < kSumB + kHC; ++i) v[i] = 0.0f;
+    for (int c = lane; c < d4; c += 32) {
+        float xv[kHC][4], fv[4], gy[kHC][4], gh[4], w[4], h[4];
 #pragma unroll
-        for (int s = 0; s < kHC; ++s) unpack8(__ldg(reinterpret_cast<const uint4 *>(xt + s * d) + c), xv[s]);
-        unpack8(__ldg(reinterpret_cast<const uint4 *>(f + t * d) + c), fv);
+        for (int s = 0; s < kHC; ++s) unpack4(__ldg(reinterpret_cast<const uint2 *>(xt + s * d) + c), xv[s]);
+        unpack4(__ldg(reinterpret_cast<const uint2 *>(f + t * d) + c), fv);
 #pragma unroll
-        for (int k = 0; k < kHC; ++k) load8f(g_y + (t * kHC + k) * d + 8 * c, gy[k]);
-        load8f(g_hn + t * d + 8 * c, gh);
-        load8f(norm_w + 8 * c, w);
+        for (int k = 0; k < kHC; ++k) load4f(g_y + (t * kHC + k) * d + 4 * c, gy[k]);
+        load4f(g_hn + t * d + 4 * c, gh);
+        load4f(norm_w + 4 * c, w);
+        hc_pre4(pm, xv, h);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            h[e] = pm[0] * xv[0][e];
-#pragma unroll
-            for (int s = 1; s < kHC; ++s) h[e] = fmaf(pm[s], xv[s][e], h[e]);
-        }
-        const uint4 hb = pack8(h);
-        sh[c] = hb;
-        unpack8(hb, h);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
+        for (int e = 0; e < 4; ++e) {
+            const float wg = w[e] * gh[e];
             v[0] = fmaf(h[e], h[e], v[0]);
-            v[1] = fmaf(h[e] * w[e], gh[e], v[1]);
+            v[1] = fmaf(h[e], wg, v[1]);
 #pragma unroll
             for (int k = 0; k < kHC; ++k) v[2 + k] = fmaf(fv[e], gy[k][e], v[2 + k]);
 #pragma unroll
             for (int j = 0; j < kHC; ++j) {
                 v[kSumX2] = fmaf(xv[j][e], xv[j][e], v[kSumX2]);
+                v[kSumA + j] = fmaf(xv[j][e], wg, v[kSumA + j]);
+                v[kSumB + j] = fmaf(xv[j][e], h[e], v[kSumB + j]);
 #pragma unroll
                 for (int k = 0; k < kHC; ++k)
                     v[2 + kHC + j * kHC + k] = fmaf(xv[j][e], gy[k][e], v[2 + kHC + j * kHC + k]);
@@ -271,33 +295,15 @@ k_bwd_token(const uint16_t *__restrict__ x, const float *__restrict__ pre_mix,
         }
     }
 #pragma unroll
-    for (int i = 0; i <= kSumX2; ++i) v[i] = warp_sum(v[i]);  // every lane holds the totals
-    __syncwarp();  // h in shared memory is visible to the whole warp
+    for (int i = 0; i < kSumB + kHC; ++i) v[i] = warp_sum(v[i]);  // every lane holds the totals
     const float rs = rsqrtf(v[0] / (float)d + norm_eps);
     const float k3 = rs * rs * rs / (float)d * v[1];
     const float r = rsqrtf(v[kSumX2] / (float)K + norm_eps);
-
-    // (d) g_pre_mix_s = sum_c x_s g_h, with g_h = rs w g_hn - k3 h
-    {
-        float gp[kHC] = {0.0f, 0.0f, 0.0f, 0.0f};
-        for (int c = lane; c < d8; c += 32) {
-            float h[8], w[8], gh[8], gu[8];
-            unpack8(sh[c], h);
-            load8f(norm_w + 8 * c, w);
-            load8f(g_hn + t * d + 8 * c, gh);
+    if (lane == 0) {
+        float gp[kHC];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) gu[e] = rs * (w[e] * gh[e]) - k3 * h[e];
-#pragma unroll
-            for (int s = 0; s < kHC; ++s) {
-                float xv[8];
-                unpack8(__ldg(reinterpret_cast<const uint4 *>(xt + s * d) + c), xv);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) gp[s] = fmaf(xv[e], gu[e], gp[s]);
-            }
-        }
-#pragma unroll
-        for (int s = 0; s < kHC; ++s) gp[s] = warp_sum(gp[s]);
-        if (lane == 0) *reinterpret_cast<float4 *>(g_pm + t * kHC) = make_float4(gp[0], gp[1], gp[2], gp[3]);
+        for (int s = 0; s < kHC; ++s) gp[s] = rs * v[kSumA + s] - k3 * v[kSumB + s];
+        *reinterpret_cast<float4 *>(g_pm + t * kHC) = make_float4(gp[0], gp[1], gp[2], gp[3]);
     }
 
     // (c) the comb part of the split and Sinkhorn, one matrix element per lane
@@ -730,7 +736,7 @@ cudaError_t launch_block_step_backward(const uint16_t *x, const float *pre_mix, 
     float *part_fn = ws + n * kWs;
     float *part_w = part_fn + (int64_t)blocks * kMix * K;
     float *part_s = part_w + (int64_t)blocks * d;
-    const size_t smem = kTokWarps * ((size_t)d * 2 + (size_t)(4 * iters) * kHC * kHC * sizeof(float));
+    const size_t smem = kTokWarps * (size_t)(4 * iters) * kHC * kHC * sizeof(float);
     cudaError_t e = cudaFuncSetAttribute(k_bwd_token, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
