@@ -460,6 +460,7 @@ k_bwd_gx(const uint16_t *__restrict__ x, const float *__restrict__ hc_fn,
     const bool small = blockIdx.x == 0;
 
     __shared__ __align__(8) uint64_t full_bar[kGxStages];
+    __shared__ __align__(8) uint64_t empty_bar[kGxStages];  // one arrive per warp when done with a tile
     __shared__ volatile int s_abort;
     constexpr uint32_t kRowBytes = kHC * kGxCols * 2 + kHC * kGxCols * 4 + kGxCols * 4 + kA * 4;  // per token
     {
@@ -467,7 +468,10 @@ k_bwd_gx(const uint16_t *__restrict__ x, const float *__restrict__ hc_fn,
         uint4 *z = smem_u4;
         for (size_t k = threadIdx.x; k < kGxSmem / 16; k += kThreads) z[k] = make_uint4(0u, 0u, 0u, 0u);
         if (threadIdx.x == 0) {
-            for (int k = 0; k < kGxStages; ++k) mbar_init(smem_u32(&full_bar[k]), 1);
+            for (int k = 0; k < kGxStages; ++k) {
+                mbar_init(smem_u32(&full_bar[k]), 1);
+                mbar_init(smem_u32(&empty_bar[k]), kWarps);
+            }
             s_abort = 0;
             fence_mbar_init_cluster();
         }
@@ -484,9 +488,12 @@ k_bwd_gx(const uint16_t *__restrict__ x, const float *__restrict__ hc_fn,
         const int cnt = (int)((t1 - tb < kGxTile) ? t1 - tb : kGxTile);
         const uint32_t bar = smem_u32(&full_bar[slot]);
         const int k = threadIdx.x;
-        if (k == 0) mbar_arrive_expect_tx(bar, (uint32_t)cnt * kRowBytes);
         if (k < 2 * kGxTile * kHC + 2 * kGxTile) {
+            // the slot's previous tile (it - kGxStages) is done in every warp
+            if (it >= kGxStages)
+                mbar_wait<false>(smem_u32(&empty_bar[slot]), (uint32_t)(it / kGxStages - 1) & 1u, &s_abort);
             fence_proxy_async_smem();  // the slot's earlier reads before the async writes
+            if (k == 0) mbar_arrive_expect_tx(bar, (uint32_t)cnt * kRowBytes);
             if (k < kGxTile * kHC) {
                 const int u = k / kHC, j = k % kHC;
                 if (u < cnt)
@@ -527,11 +534,12 @@ k_bwd_gx(const uint16_t *__restrict__ x, const float *__restrict__ hc_fn,
     const float wn0 = __ldg(norm_w + cc0), wn1 = __ldg(norm_w + cc0 + 1);
     float gw0 = 0.0f, gw1 = 0.0f, sm = 0.0f;
 
-#pragma unroll
-    for (int it = 0; it < kGxStages - 1; ++it) issue(it);
+    // One tile ahead: tile it + 1 goes into the slot of tile it + 1 - kGxStages,
+    // which every warp released at least one tile ago, so warps drift apart by
+    // up to a tile without waiting for one another.
+    issue(0);
     for (int it = 0; it < ntiles; ++it) {
-        __syncthreads();  // every thread is done with tile it - 1: its slot is free
-        issue(it + kGxStages - 1);
+        issue(it + 1);
         mbar_wait<false>(smem_u32(&full_bar[it % kGxStages]), (uint32_t)(it / kGxStages) & 1u, &s_abort);
         const GxStage &S = stg[it % kGxStages];
         const int64_t tb = t0 + (int64_t)it * kGxTile;
@@ -646,6 +654,10 @@ k_bwd_gx(const uint16_t *__restrict__ x, const float *__restrict__ hc_fn,
                 *reinterpret_cast<float2 *>(g_f + t * d + cc0) = make_float2(gf[0], gf[1]);
             }
         }
+        // this warp is done with the slot: its loads have completed before the arrive
+        __threadfence_block();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&empty_bar[it % kGxStages]));
     }
     // g_hc_fn partials: accumulator (row 16mt + g (+8), stream nt, columns 2q, 2q + 1)
 #pragma unroll
