@@ -28,6 +28,7 @@ SIGNATURES = {
     "hc_last_cuda_error": [],
     "hc_version": [],
     "hc_consume_device_error": [P],
+    "hc_selftest_barrier_timeout": [P],
     "hc_mixes": [P, P, P, P, I64, I32, I32, I32, F32, F32, P, P, P, P, P],
     "hc_split_sinkhorn": [P, P, P, I64, I32, I32, F32, P, P, P, P],
     "hc_pre_norm": [P, P, P, I64, I32, I32, F32, P, P],

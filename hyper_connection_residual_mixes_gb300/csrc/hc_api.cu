@@ -97,6 +97,10 @@ hc_status hc_consume_device_error(cudaStream_t stream) {
     return (flag | flag_chain | flag_bwd) ? HC_ERR_TIMEOUT : HC_OK;
 }
 
+hc_status hc_selftest_barrier_timeout(cudaStream_t stream) {
+    return cuda_status(hc::launch_selftest_wait(stream));
+}
+
 hc_status hc_split_sinkhorn(const float *mixes, const float *hc_scale, const float *hc_base,
                             int64_t n, int hc, int sinkhorn_iters, float eps, float *pre,
                             float *post, float *comb, cudaStream_t stream) {

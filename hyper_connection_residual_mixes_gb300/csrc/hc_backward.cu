@@ -712,6 +712,28 @@ static __device__ __align__(256) unsigned char g_bwd_scratch[kStaticScratchBytes
 
 size_t backward_static_scratch_bytes() { return kStaticScratchBytes; }
 
+// Self-test of the bounded waits: one warp waits on an mbarrier that nothing
+// arrives on.  The wait runs out, sets this unit's device flag and returns
+// false; the kernel then ends normally.
+__global__ void k_selftest_wait(unsigned int *completed) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ volatile int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        abort_flag = 0;
+        fence_mbar_init_cluster();
+    }
+    __syncthreads();
+    const bool ok = mbar_wait<false>(smem_u32(&bar), 0u, &abort_flag);
+    if (!ok) return;
+    if (completed) atomicAdd(completed, 1u);  // not reached: no arrival is ever made
+}
+
+cudaError_t launch_selftest_wait(cudaStream_t s) {
+    k_selftest_wait<<<1, 32, 0, s>>>(nullptr);
+    return cudaGetLastError();
+}
+
 cudaError_t consume_backward_device_error(cudaStream_t s, unsigned int *flag) {
     cudaError_t e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return e;

@@ -78,5 +78,7 @@ cudaError_t launch_chain_side(const uint16_t *x, const uint16_t *f, const float 
 cudaError_t consume_device_error(cudaStream_t s, unsigned int *flag);
 cudaError_t consume_chain_device_error(cudaStream_t s, unsigned int *flag);
 cudaError_t consume_backward_device_error(cudaStream_t s, unsigned int *flag);
+// one warp waits on a barrier nothing arrives on (the bounded-wait self-test)
+cudaError_t launch_selftest_wait(cudaStream_t s);
 
 }  // namespace hc

@@ -85,6 +85,17 @@ int hc_version(void);
 hc_status hc_consume_device_error(cudaStream_t stream);
 
 /*
+ * Self-test of the path above: launches one warp that waits on a barrier
+ * nothing ever arrives on.  The bounded wait gives up (after about half a
+ * minute),
+ * records the device flag and the kernel returns, leaving the context
+ * usable; the next hc_consume_device_error(stream) returns HC_ERR_TIMEOUT.
+ * Returns HC_ERR_CUDA if the launch failed, HC_OK otherwise.  Not part of
+ * the method.
+ */
+hc_status hc_selftest_barrier_timeout(cudaStream_t stream);
+
+/*
  * a1-a3 (DeepSeek-V4.1 Block page, Block.hc_mixes, and the "Stream
  * combination" page's hc_split_sinkhorn): from the streams x of n tokens,
  * the 24 mix numbers (one rsqrt statistic over all hc*d values per token,
