@@ -86,10 +86,10 @@ hc_status hc_consume_device_error(cudaStream_t stream);
 
 /*
  * Self-test of the path above: launches one warp that waits on a barrier
- * nothing ever arrives on.  The bounded wait gives up (after about half a
- * minute),
- * records the device flag and the kernel returns, leaving the context
- * usable; the next hc_consume_device_error(stream) returns HC_ERR_TIMEOUT.
+ * nothing ever arrives on.  The bounded wait gives up after about half a
+ * minute, records the device flag and the kernel returns, leaving the
+ * context usable; the next hc_consume_device_error(stream) returns
+ * HC_ERR_TIMEOUT.
  * Returns HC_ERR_CUDA if the launch failed, HC_OK otherwise.  Not part of
  * the method.
  */
