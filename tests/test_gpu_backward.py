@@ -178,3 +178,22 @@ def test_backward_long_prefill_sampled_tokens_and_additivity():
         scale = np.abs(r).reshape(len(rows), -1).max(axis=1).reshape((-1,) + (1,) * (r.ndim - 1))
         err = np.abs(got - r)
         assert np.all(err <= RTOL_TOK * np.abs(r) + 2 * ATOL * scale), (k, float(err.max()))
+
+
+@pytest.mark.parametrize("iters,eps", [(128, 1e-6), (20, 0.0)])
+def test_backward_iteration_limits(iters, eps):
+    """128 Sinkhorn rounds (the largest accepted; the per-token kernel keeps
+    256 iterates per token in shared memory) and eps = 0."""
+    case, up = _case(120 + iters, 6, 256)
+    p = case.params[0]
+    got = hcg.hc_block_step_backward(
+        case.x.to(DEV), case.pre_mix.to(DEV), case.fs[0].to(DEV), *p.to(DEV).astuple(),
+        up["g_h_norm"].to(DEV), up["g_y"].to(DEV), g_pre=up["g_pre"].to(DEV), sinkhorn_iters=iters, eps=eps)
+    torch.cuda.synchronize()
+    ref = oracle.side_backward(
+        oracle.bf16_to_f64(oracle.bf16_bits(case.x)), _np(case.pre_mix).astype(np.float64),
+        oracle.bf16_to_f64(oracle.bf16_bits(case.fs[0])), *(_np(t).astype(np.float64) for t in p.astuple()),
+        _np(up["g_h_norm"]).astype(np.float64), _np(up["g_y"]).astype(np.float64),
+        _np(up["g_pre"]).astype(np.float64), iters=iters, eps=eps, rounded=True)
+    _compare(got, ref)
+    assert _lib.raw("hc_consume_device_error", None) == 0

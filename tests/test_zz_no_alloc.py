@@ -68,3 +68,28 @@ def test_no_workspace_equals_workspace_and_allocates_nothing(n, d):
     assert free1 == free0
     for k in ref:
         assert torch.equal(outs[k], ref[k]), k
+
+
+@pytest.mark.gpu
+def test_no_workspace_at_its_capacity():
+    """27,648 tokens at d = 5120, the most the fixed scratch holds: it runs and
+    equals the workspace entry bit for bit."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    hc_build.build()
+    _lib.load()
+    dev = torch.device("cuda:0")
+    n, d = 27648, 5120
+    g = torch.Generator(device=dev).manual_seed(31)
+    x = inputs.streams(g, n, 4, d, device=dev)
+    pm = inputs.pre_mix(g, n, device=dev)
+    f = inputs.sublayer_out(g, n, d, device=dev)
+    p = inputs.side_params(g, d=d, device=dev)
+    args = (x, pm, f, *p.astuple(), torch.randn((n, d), device=dev, generator=g),
+            torch.randn((n, 4, d), device=dev, generator=g))
+    ref = hcg.hc_block_step_backward(*args)
+    got = hcg.hc_block_step_backward_no_workspace(*args)
+    torch.cuda.synchronize()
+    for k in ref:
+        assert torch.equal(got[k], ref[k]), k
+    assert _lib.raw("hc_consume_device_error", None) == 0
