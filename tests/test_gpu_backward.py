@@ -85,7 +85,9 @@ def _compare(got, ref, extra=None):
 
 
 @pytest.mark.parametrize("n,d,iters,with_pre", [(16, 5120, 20, True), (37, 1024, 20, False),
-                                                 (3, 64, 1, True), (5, 2048, 7, True)])
+                                                 (3, 64, 1, True), (5, 2048, 7, True),
+                                                 (4, 7168, 20, True), (3, 16384, 20, True),
+                                                 (1, 5120, 20, True)])
 def test_backward_matches_oracle(n, d, iters, with_pre):
     case, up = _case(40 + n, n, d, with_pre)
     got = _run(case, up, iters)
