@@ -6,6 +6,7 @@
 #include <cstring>
 
 #include "../../include/hc.h"
+#include "hc_backward_generic.h"
 #include "hc_launch.h"
 
 namespace {
@@ -168,8 +169,8 @@ hc_status hc_pre_norm(const uint16_t *x, const float *pre_mix, const float *norm
 }
 
 size_t hc_block_step_backward_workspace_bytes(int64_t n, int hc, int d) {
-    if (check_shape(n, hc, d, true) != HC_OK || hc != 4) return 0;
-    return hc::backward_workspace_bytes(n, d);
+    if (check_shape(n, hc, d, true) != HC_OK) return 0;
+    return hc == 4 ? hc::backward_workspace_bytes(n, d) : hc::backward_generic_workspace_bytes(n, hc, d);
 }
 
 hc_status hc_block_step_backward(const uint16_t *x, const float *pre_mix, const uint16_t *f,
@@ -182,14 +183,13 @@ hc_status hc_block_step_backward(const uint16_t *x, const float *pre_mix, const 
                                  cudaStream_t stream) {
     hc_status st = check_shape(n, hc, d, true);
     if (st != HC_OK) return st;
-    if (hc != 4) return HC_ERR_UNSUPPORTED;
     if (sinkhorn_iters < 1 || sinkhorn_iters > 128 || !finite_nonneg(eps) || !finite_nonneg(norm_eps))
         return HC_ERR_INVALID_ARG;
     if (n == 0) return HC_OK;
     if (!x || !pre_mix || !f || !hc_fn || !hc_scale || !hc_base || !norm_w || !g_h_norm || !g_y ||
         !g_x || !g_pre_mix || !g_f || !g_hc_fn || !g_hc_scale || !g_hc_base || !g_norm_w || !workspace)
         return HC_ERR_INVALID_ARG;
-    if (workspace_bytes < hc::backward_workspace_bytes(n, d)) return HC_ERR_INVALID_ARG;
+    if (workspace_bytes < hc_block_step_backward_workspace_bytes(n, hc, d)) return HC_ERR_INVALID_ARG;
     const void *ptrs[] = {x, pre_mix, f, hc_fn, hc_scale, hc_base, norm_w, g_h_norm, g_y, g_x,
                           g_pre_mix, g_f, g_hc_fn, g_hc_scale, g_hc_base, g_norm_w, workspace};
     for (const void *p : ptrs)
@@ -204,6 +204,11 @@ hc_status hc_block_step_backward(const uint16_t *x, const float *pre_mix, const 
                          span(g_hc_fn, mix * K * 4), span(g_hc_scale, 12), span(g_hc_base, mix * 4),
                          span(g_norm_w, d * 4), span(workspace, (int64_t)workspace_bytes)};
     if ((st = check_alias(outs, 8, ins, 10)) != HC_OK) return st;
+    if (hc != 4)  // two or eight streams: the plain kernels of hc_backward_generic.cu
+        return cuda_status(hc::launch_block_step_backward_generic(
+            hc, x, pre_mix, f, hc_fn, hc_scale, hc_base, norm_w, n, d, sinkhorn_iters, eps, norm_eps,
+            g_h_norm, g_y, g_pre, g_x, g_pre_mix, g_f, g_hc_fn, g_hc_scale, g_hc_base, g_norm_w,
+            workspace, stream));
     return cuda_status(hc::launch_block_step_backward(
         x, pre_mix, f, hc_fn, hc_scale, hc_base, norm_w, n, d, sinkhorn_iters, eps, norm_eps,
         g_h_norm, g_y, g_pre, g_x, g_pre_mix, g_f, g_hc_fn, g_hc_scale, g_hc_base, g_norm_w,

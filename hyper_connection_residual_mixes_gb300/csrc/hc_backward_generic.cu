@@ -1,0 +1,480 @@
+// hc_backward_generic.cu -- the backward of one hyper-connection side step
+// (a1-a6) for two and eight streams.
+//
+// The same derivative as hc_backward.cu (DeepSeek-V4.1 Block page, Code
+// section: Block.hc_mixes, Block.hc_pre, attn_norm / ffn_norm,
+// Block.hc_post; "Stream combination" page: hc_split_sinkhorn, whose kernel
+// takes the stream count hc as a parameter): the bf16 casts pass gradients
+// through unchanged, the forward's rounded h is used where the forward used
+// it, and Sinkhorn is differentiated step by step through its iterates.
+//
+// These kernels favour plainness over speed; the four-stream model runs the
+// tensor-core kernels of hc_backward.cu.  One CTA per token:
+//   kg_proj   the projection a = x W^T (a warp per mix row);
+//   kg_token  the token's sums in one pass, the split, Sinkhorn forward with
+//             its iterates and backward (one thread), g_pre_mix and the
+//             per-token record;
+//   kg_gx     g_x and g_f;
+// then partial sums of the parameter gradients over blocks of 1,024 tokens,
+// added block by block in a fixed order (deterministic, no atomics).
+#include "hc_backward_generic.h"
+#include "hc_device.cuh"
+
+namespace hc {
+namespace bwg {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kTokBlock = 1024;  // tokens per partial sum of a parameter gradient
+constexpr int kFnTile = 16;      // tokens per staged g_a tile in kg_fn_partial
+
+// The per-token record in the workspace (floats).
+template <int HC>
+struct Lay {
+    static constexpr int kMix = (2 + HC) * HC;
+    static constexpr int kA = 0;                // a[mix]: the projection (kg_proj)
+    static constexpr int kGa = kMix;            // g_a[mix]: the gradient of a
+    static constexpr int kGz = 2 * kMix;        // g_z[mix]: the g_hc_base terms
+    static constexpr int kGzm = 3 * kMix;       // gzm[3]: the g_hc_scale terms
+    static constexpr int kPost = 3 * kMix + 4;  // post[HC]
+    static constexpr int kComb = kPost + HC;    // comb[HC * HC]
+    static constexpr int kPm = kComb + HC * HC; // pre_mix[HC]
+    static constexpr int kRs = kPm + HC;        // 1 / RMS(h)
+    static constexpr int kCr = kRs + 1;         // the statistic's coefficient of x in g_x
+    static constexpr int kK3 = kRs + 2;         // rs^3 / d * sum(h w g_hn)
+    static constexpr int kWs = (kK3 + 1 + 3) / 4 * 4;
+    static constexpr int kSmall = (kMix + 3 + 3) / 4 * 4;  // per-block partials of g_hc_base, g_hc_scale
+    // token sums of kg_token: sum h^2, T = sum h w g_hn, sum x^2, g_post[HC],
+    // g_comb[HC*HC], A[HC] = sum x_s w g_hn, B[HC] = sum x_s h
+    static constexpr int kSH2 = 0, kST = 1, kSX2 = 2, kSPost = 3, kSComb = 3 + HC,
+                         kSA = 3 + HC + HC * HC, kSB = kSA + HC, kSums = kSB + HC;
+};
+
+__device__ __forceinline__ float sigm(float z) { return 1.0f / (1.0f + expf(-z)); }
+
+__device__ __forceinline__ void ld4bf(const uint16_t *p, float (&o)[4]) {
+    const uint2 v = __ldg(reinterpret_cast<const uint2 *>(p));
+    o[0] = bf16lo(v.x);
+    o[1] = __uint_as_float(v.x & 0xffff0000u);
+    o[2] = bf16lo(v.y);
+    o[3] = __uint_as_float(v.y & 0xffff0000u);
+}
+__device__ __forceinline__ void ld4f(const float *p, float (&o)[4]) {
+    const float4 v = __ldg(reinterpret_cast<const float4 *>(p));
+    o[0] = v.x; o[1] = v.y; o[2] = v.z; o[3] = v.w;
+}
+__device__ __forceinline__ float round_bf16(float v) { return bf16lo(pack_bf16x2(v, 0.0f)); }
+
+// a_i = sum_k x_k W_ik: warp w takes the rows w, w + 8, ...
+template <int HC>
+__global__ void __launch_bounds__(kThreads)
+kg_proj(const uint16_t *__restrict__ x, const float *__restrict__ hc_fn, int d, float *__restrict__ ws) {
+    using L = Lay<HC>;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t t = blockIdx.x;
+    const int K = HC * d;
+    const uint16_t *xt = x + t * K;
+    for (int i = warp; i < L::kMix; i += kWarps) {
+        const float *wr = hc_fn + (int64_t)i * K;
+        float acc = 0.0f;
+        for (int c = lane; c < K / 4; c += 32) {
+            float xv[4], wv[4];
+            ld4bf(xt + 4 * c, xv);
+            ld4f(wr + 4 * c, wv);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc = fmaf(xv[e], wv[e], acc);
+        }
+        acc = warp_sum(acc);
+        if (lane == 0) ws[t * L::kWs + L::kA + i] = acc;
+    }
+}
+
+// One pass over the token for its sums, then (one thread) the split, the
+// Sinkhorn iterates and their backward, the gradients of the mix numbers,
+// g_pre_mix and the record.  Dynamic shared memory: 2 * iters iterates of
+// HC*HC, then the row softmax.
+template <int HC>
+__global__ void __launch_bounds__(kThreads)
+kg_token(const uint16_t *__restrict__ x, const float *__restrict__ pre_mix,
+         const uint16_t *__restrict__ f, const float *__restrict__ hc_scale,
+         const float *__restrict__ hc_base, const float *__restrict__ norm_w, int d, int iters,
+         float eps, float norm_eps, const float *__restrict__ g_hn, const float *__restrict__ g_y,
+         const float *__restrict__ g_pre, float *__restrict__ g_pm, float *__restrict__ ws) {
+    using L = Lay<HC>;
+    constexpr int M = L::kMix, H2 = HC * HC;
+    extern __shared__ float sdyn[];
+    __shared__ float red[kWarps][L::kSums];
+    __shared__ float tot[L::kSums];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t t = blockIdx.x;
+    const int K = HC * d;
+    const uint16_t *xt = x + t * K;
+    float *wt = ws + t * L::kWs;
+    float pm[HC];
+#pragma unroll
+    for (int s = 0; s < HC; ++s) pm[s] = __ldg(pre_mix + t * HC + s);
+    float v[L::kSums];
+#pragma unroll
+    for (int i = 0; i < L::kSums; ++i) v[i] = 0.0f;
+    for (int c = threadIdx.x; c < d / 4; c += kThreads) {
+        float xv[HC][4], fv[4], gh[4], w[4], h[4];
+#pragma unroll
+        for (int s = 0; s < HC; ++s) ld4bf(xt + (int64_t)s * d + 4 * c, xv[s]);
+        ld4bf(f + t * d + 4 * c, fv);
+        ld4f(g_hn + t * d + 4 * c, gh);
+        ld4f(norm_w + 4 * c, w);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            float hv = pm[0] * xv[0][e];
+#pragma unroll
+            for (int s = 1; s < HC; ++s) hv = fmaf(pm[s], xv[s][e], hv);
+            h[e] = round_bf16(hv);  // the forward's bf16 h
+            const float wg = w[e] * gh[e];
+            v[L::kSH2] = fmaf(h[e], h[e], v[L::kSH2]);
+            v[L::kST] = fmaf(h[e], wg, v[L::kST]);
+#pragma unroll
+            for (int j = 0; j < HC; ++j) {
+                v[L::kSX2] = fmaf(xv[j][e], xv[j][e], v[L::kSX2]);
+                v[L::kSA + j] = fmaf(xv[j][e], wg, v[L::kSA + j]);
+                v[L::kSB + j] = fmaf(xv[j][e], h[e], v[L::kSB + j]);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < HC; ++k) {
+            float gy[4];
+            ld4f(g_y + (t * HC + k) * d + 4 * c, gy);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                v[L::kSPost + k] = fmaf(fv[e], gy[e], v[L::kSPost + k]);
+#pragma unroll
+                for (int j = 0; j < HC; ++j)
+                    v[L::kSComb + j * HC + k] = fmaf(xv[j][e], gy[e], v[L::kSComb + j * HC + k]);
+            }
+        }
+    }
+    // the CTA's sums, added in a fixed order
+#pragma unroll
+    for (int i = 0; i < L::kSums; ++i) {
+        const float sv = warp_sum(v[i]);
+        if (lane == 0) red[warp][i] = sv;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < L::kSums; i += kThreads) {
+        float sv = 0.0f;
+        for (int w2 = 0; w2 < kWarps; ++w2) sv += red[w2][i];
+        tot[i] = sv;
+    }
+    __syncthreads();
+    if (threadIdx.x != 0) return;
+
+    const float r = rsqrtf(tot[L::kSX2] / (float)K + norm_eps);
+    const float rs = rsqrtf(tot[L::kSH2] / (float)d + norm_eps);
+    const float k3 = rs * rs * rs / (float)d * tot[L::kST];
+    const float s0 = __ldg(hc_scale), s1 = __ldg(hc_scale + 1), s2 = __ldg(hc_scale + 2);
+    float *sP = sdyn;
+    float *sS = sdyn + 2 * iters * H2;
+    float m[M];
+    for (int i = 0; i < M; ++i) m[i] = wt[L::kA + i] * r;
+    // the row softmax S and P[0] = S + eps
+    for (int j = 0; j < HC; ++j) {
+        float Lg[HC], mx = -INFINITY, sum = 0.0f;
+        for (int k = 0; k < HC; ++k) {
+            Lg[k] = fmaf(m[2 * HC + j * HC + k], s2, __ldg(hc_base + 2 * HC + j * HC + k));
+            mx = fmaxf(mx, Lg[k]);
+        }
+        for (int k = 0; k < HC; ++k) {
+            Lg[k] = expf(Lg[k] - mx);
+            sum += Lg[k];
+        }
+        for (int k = 0; k < HC; ++k) {
+            sS[j * HC + k] = Lg[k] / sum;
+            sP[j * HC + k] = sS[j * HC + k] + eps;
+        }
+    }
+    // steps 1 .. 2*iters-1: a column step for odd, a row step for even steps
+    for (int st = 1; st < 2 * iters; ++st) {
+        const float *pa = sP + (st - 1) * H2;
+        float *pb = sP + st * H2;
+        for (int i = 0; i < HC; ++i) {
+            float sum = 0.0f;
+            for (int o = 0; o < HC; ++o) sum += (st & 1) ? pa[o * HC + i] : pa[i * HC + o];
+            const float inv = 1.0f / (sum + eps);
+            for (int o = 0; o < HC; ++o) {
+                const int idx = (st & 1) ? o * HC + i : i * HC + o;
+                pb[idx] = pa[idx] * inv;
+            }
+        }
+    }
+    const float *comb = sP + (2 * iters - 1) * H2;
+    for (int i = 0; i < H2; ++i) wt[L::kComb + i] = comb[i];
+    // back through the steps: g, the gradient of the current iterate
+    float g[H2];
+    for (int i = 0; i < H2; ++i) g[i] = tot[L::kSComb + i];
+    for (int st = 2 * iters - 1; st >= 1; --st) {
+        const float *pa = sP + (st - 1) * H2, *pb = sP + st * H2;
+        for (int i = 0; i < HC; ++i) {
+            float sum = 0.0f, dot = 0.0f;
+            for (int o = 0; o < HC; ++o) {
+                const int idx = (st & 1) ? o * HC + i : i * HC + o;
+                sum += pa[idx];
+                dot = fmaf(g[idx], pb[idx], dot);
+            }
+            const float inv = 1.0f / (sum + eps);
+            for (int o = 0; o < HC; ++o) {
+                const int idx = (st & 1) ? o * HC + i : i * HC + o;
+                g[idx] = (g[idx] - dot) * inv;
+            }
+        }
+    }
+    float gz[M], gm[M];
+    for (int j = 0; j < HC; ++j) {  // through the row softmax
+        float dot = 0.0f;
+        for (int k = 0; k < HC; ++k) dot = fmaf(g[j * HC + k], sS[j * HC + k], dot);
+        for (int k = 0; k < HC; ++k) gz[2 * HC + j * HC + k] = sS[j * HC + k] * (g[j * HC + k] - dot);
+    }
+    float gzm0 = 0.0f, gzm1 = 0.0f, gzm2 = 0.0f;
+    for (int j = 0; j < HC; ++j) {  // pre and post: the sigmoids
+        const float sp = sigm(fmaf(m[j], s0, __ldg(hc_base + j)));
+        gz[j] = (g_pre ? __ldg(g_pre + t * HC + j) : 0.0f) * sp * (1.0f - sp);
+        const float sq = sigm(fmaf(m[HC + j], s1, __ldg(hc_base + HC + j)));
+        gz[HC + j] = tot[L::kSPost + j] * 2.0f * sq * (1.0f - sq);
+        wt[L::kPost + j] = 2.0f * sq;
+        wt[L::kPm + j] = pm[j];
+        gm[j] = gz[j] * s0;
+        gm[HC + j] = gz[HC + j] * s1;
+        gzm0 = fmaf(gz[j], m[j], gzm0);
+        gzm1 = fmaf(gz[HC + j], m[HC + j], gzm1);
+    }
+    for (int i = 2 * HC; i < M; ++i) {
+        gm[i] = gz[i] * s2;
+        gzm2 = fmaf(gz[i], m[i], gzm2);
+    }
+    float gr = 0.0f;
+    for (int i = 0; i < M; ++i) gr = fmaf(gm[i], wt[L::kA + i], gr);
+    for (int i = 0; i < M; ++i) {
+        wt[L::kGa + i] = gm[i] * r;
+        wt[L::kGz + i] = gz[i];
+    }
+    wt[L::kGzm] = gzm0;
+    wt[L::kGzm + 1] = gzm1;
+    wt[L::kGzm + 2] = gzm2;
+    wt[L::kRs] = rs;
+    wt[L::kCr] = -gr * r * r * r / (float)K;  // the statistic's term: cr * x_k
+    wt[L::kK3] = k3;
+    // g_pre_mix_s = sum_c x_s (rs w g_hn - k3 h) = rs A_s - k3 B_s
+    for (int s = 0; s < HC; ++s) g_pm[t * HC + s] = rs * tot[L::kSA + s] - k3 * tot[L::kSB + s];
+}
+
+// g_x[s][c] = pm_s g_h + cr x_s + sum_k comb_sk g_y_k + sum_i g_a_i W[i][s*d + c],
+// g_h = rs w g_hn - k3 h; g_f[c] = sum_k post_k g_y_k.  Four channels per step.
+template <int HC>
+__global__ void __launch_bounds__(kThreads)
+kg_gx(const uint16_t *__restrict__ x, const float *__restrict__ hc_fn, const float *__restrict__ norm_w,
+      const float *__restrict__ g_hn, const float *__restrict__ g_y, const float *__restrict__ ws, int d,
+      float *__restrict__ g_x, float *__restrict__ g_f) {
+    using L = Lay<HC>;
+    __shared__ float rec[L::kWs];
+    const int64_t t = blockIdx.x;
+    const int64_t K = (int64_t)HC * d;
+    for (int i = threadIdx.x; i < L::kWs; i += kThreads) rec[i] = ws[t * L::kWs + i];
+    __syncthreads();
+    const float rs = rec[L::kRs], cr = rec[L::kCr], k3 = rec[L::kK3];
+    for (int c = threadIdx.x; c < d / 4; c += kThreads) {
+        float xv[HC][4], gy[HC][4], gh[4], w[4], ghh[4], gf[4];
+#pragma unroll
+        for (int s = 0; s < HC; ++s) {
+            ld4bf(x + t * K + (int64_t)s * d + 4 * c, xv[s]);
+            ld4f(g_y + (t * HC + s) * d + 4 * c, gy[s]);
+        }
+        ld4f(g_hn + t * d + 4 * c, gh);
+        ld4f(norm_w + 4 * c, w);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            float hv = rec[L::kPm] * xv[0][e];
+#pragma unroll
+            for (int s = 1; s < HC; ++s) hv = fmaf(rec[L::kPm + s], xv[s][e], hv);
+            ghh[e] = rs * (w[e] * gh[e]) - k3 * round_bf16(hv);
+            float fvv = rec[L::kPost] * gy[0][e];
+#pragma unroll
+            for (int k = 1; k < HC; ++k) fvv = fmaf(rec[L::kPost + k], gy[k][e], fvv);
+            gf[e] = fvv;
+        }
+        *reinterpret_cast<float4 *>(g_f + t * d + 4 * c) = make_float4(gf[0], gf[1], gf[2], gf[3]);
+#pragma unroll
+        for (int s = 0; s < HC; ++s) {
+            float gx[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                float a = fmaf(rec[L::kPm + s], ghh[e], cr * xv[s][e]);
+#pragma unroll
+                for (int k = 0; k < HC; ++k) a = fmaf(rec[L::kComb + s * HC + k], gy[k][e], a);
+                gx[e] = a;
+            }
+            for (int i = 0; i < L::kMix; ++i) {
+                float wv[4];
+                ld4f(hc_fn + i * K + (int64_t)s * d + 4 * c, wv);
+                const float ga = rec[L::kGa + i];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) gx[e] = fmaf(ga, wv[e], gx[e]);
+            }
+            *reinterpret_cast<float4 *>(g_x + (t * HC + s) * d + 4 * c) = make_float4(gx[0], gx[1], gx[2], gx[3]);
+        }
+    }
+}
+
+// g_hc_fn partial sums over a block of tokens: part[b][i][k] = sum_t g_a[t][i] x[t][k];
+// one thread per column k of hc*d.
+template <int HC>
+__global__ void __launch_bounds__(kThreads)
+kg_fn_partial(const uint16_t *__restrict__ x, const float *__restrict__ ws, int64_t n, int K,
+              float *__restrict__ part) {
+    using L = Lay<HC>;
+    constexpr int M = L::kMix;
+    __shared__ float sga[kFnTile][M];
+    const int k = blockIdx.x * kThreads + threadIdx.x;
+    const int64_t t0 = (int64_t)blockIdx.y * kTokBlock;
+    const int64_t t1 = (t0 + kTokBlock < n) ? t0 + kTokBlock : n;
+    float acc[M];
+#pragma unroll
+    for (int i = 0; i < M; ++i) acc[i] = 0.0f;
+    for (int64_t tb = t0; tb < t1; tb += kFnTile) {
+        const int cnt = (int)((t1 - tb < kFnTile) ? t1 - tb : kFnTile);
+        __syncthreads();
+        for (int q = threadIdx.x; q < cnt * M; q += kThreads)
+            sga[q / M][q % M] = ws[(tb + q / M) * L::kWs + L::kGa + q % M];
+        __syncthreads();
+        if (k < K)
+            for (int u = 0; u < cnt; ++u) {
+                const float xv = __uint_as_float((uint32_t)x[(tb + u) * K + k] << 16);
+#pragma unroll
+                for (int i = 0; i < M; ++i) acc[i] = fmaf(sga[u][i], xv, acc[i]);
+            }
+    }
+    if (k < K)
+#pragma unroll
+        for (int i = 0; i < M; ++i) part[((int64_t)blockIdx.y * M + i) * K + k] = acc[i];
+}
+
+// g_norm_w partial sums: part[b][c] = sum_t h[t][c] rs_h[t] g_hn[t][c], h as the forward rounds it.
+template <int HC>
+__global__ void __launch_bounds__(kThreads)
+kg_w_partial(const uint16_t *__restrict__ x, const float *__restrict__ g_hn, const float *__restrict__ ws,
+             int64_t n, int d, float *__restrict__ part) {
+    using L = Lay<HC>;
+    const int c = blockIdx.x * kThreads + threadIdx.x;
+    const int64_t t0 = (int64_t)blockIdx.y * kTokBlock;
+    const int64_t t1 = (t0 + kTokBlock < n) ? t0 + kTokBlock : n;
+    if (c >= d) return;
+    float acc = 0.0f;
+    for (int64_t t = t0; t < t1; ++t) {
+        const float *rec = ws + t * L::kWs;
+        const uint16_t *xt = x + t * HC * d;
+        float hv = __ldg(rec + L::kPm) * __uint_as_float((uint32_t)xt[c] << 16);
+#pragma unroll
+        for (int s = 1; s < HC; ++s) hv = fmaf(__ldg(rec + L::kPm + s), __uint_as_float((uint32_t)xt[s * d + c] << 16), hv);
+        acc = fmaf(round_bf16(hv) * __ldg(rec + L::kRs), __ldg(g_hn + t * d + c), acc);
+    }
+    part[(int64_t)blockIdx.y * d + c] = acc;
+}
+
+// per block: the sums over its tokens of g_z (g_hc_base terms) and gzm (g_hc_scale terms)
+template <int HC>
+__global__ void kg_small_partial(const float *__restrict__ ws, int64_t n, float *__restrict__ part) {
+    using L = Lay<HC>;
+    const int i = threadIdx.x;
+    if (i >= L::kMix + 3) return;
+    const int64_t t0 = (int64_t)blockIdx.x * kTokBlock;
+    const int64_t t1 = (t0 + kTokBlock < n) ? t0 + kTokBlock : n;
+    float acc = 0.0f;
+    for (int64_t t = t0; t < t1; ++t) acc += ws[t * L::kWs + L::kGz + i];  // kGz + kMix = kGzm
+    part[(int64_t)blockIdx.x * L::kSmall + i] = acc;
+}
+
+// out[j] = sum_b part[b][j], blocks in order.
+__global__ void kg_sum_blocks(const float *__restrict__ part, int blocks, int64_t len, float *__restrict__ out) {
+    const int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (j >= len) return;
+    float s = 0.0f;
+    for (int b = 0; b < blocks; ++b) s += part[(int64_t)b * len + j];
+    out[j] = s;
+}
+
+template <int HC>
+__global__ void kg_small_final(const float *__restrict__ part, int blocks, float *__restrict__ g_base,
+                               float *__restrict__ g_scale) {
+    using L = Lay<HC>;
+    const int j = threadIdx.x;
+    if (j >= L::kMix + 3) return;
+    float s = 0.0f;
+    for (int b = 0; b < blocks; ++b) s += part[(int64_t)b * L::kSmall + j];
+    if (j < L::kMix) g_base[j] = s;
+    else g_scale[j - L::kMix] = s;
+}
+
+template <int HC>
+size_t ws_bytes(int64_t n, int d) {
+    using L = Lay<HC>;
+    const int64_t blocks = (n + kTokBlock - 1) / kTokBlock;
+    const int64_t K = (int64_t)HC * d;
+    return (size_t)(n * L::kWs + blocks * (L::kMix * K + d + L::kSmall)) * sizeof(float);
+}
+
+template <int HC>
+cudaError_t launch(const uint16_t *x, const float *pre_mix, const uint16_t *f, const float *hc_fn,
+                   const float *hc_scale, const float *hc_base, const float *norm_w, int64_t n, int d,
+                   int iters, float eps, float norm_eps, const float *g_hn, const float *g_y,
+                   const float *g_pre, float *g_x, float *g_pm, float *g_f, float *g_fn, float *g_scale,
+                   float *g_base, float *g_w, void *workspace, cudaStream_t s) {
+    using L = Lay<HC>;
+    constexpr int M = L::kMix;
+    const int64_t K = (int64_t)HC * d;
+    const int blocks = (int)((n + kTokBlock - 1) / kTokBlock);
+    float *ws = reinterpret_cast<float *>(workspace);
+    float *part_fn = ws + n * L::kWs;
+    float *part_w = part_fn + (int64_t)blocks * M * K;
+    float *part_s = part_w + (int64_t)blocks * d;
+    const size_t smem = (size_t)(2 * iters + 1) * HC * HC * sizeof(float);
+    cudaError_t e = cudaFuncSetAttribute(kg_token<HC>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    kg_proj<HC><<<(unsigned)n, kThreads, 0, s>>>(x, hc_fn, d, ws);
+    kg_token<HC><<<(unsigned)n, kThreads, smem, s>>>(x, pre_mix, f, hc_scale, hc_base, norm_w, d, iters, eps,
+                                                     norm_eps, g_hn, g_y, g_pre, g_pm, ws);
+    kg_gx<HC><<<(unsigned)n, kThreads, 0, s>>>(x, hc_fn, norm_w, g_hn, g_y, ws, d, g_x, g_f);
+    kg_fn_partial<HC><<<dim3((unsigned)((K + kThreads - 1) / kThreads), (unsigned)blocks), kThreads, 0, s>>>(
+        x, ws, n, (int)K, part_fn);
+    kg_sum_blocks<<<(unsigned)((M * K + 255) / 256), 256, 0, s>>>(part_fn, blocks, M * K, g_fn);
+    kg_w_partial<HC><<<dim3((unsigned)((d + kThreads - 1) / kThreads), (unsigned)blocks), kThreads, 0, s>>>(
+        x, g_hn, ws, n, d, part_w);
+    kg_sum_blocks<<<(unsigned)((d + 255) / 256), 256, 0, s>>>(part_w, blocks, d, g_w);
+    kg_small_partial<HC><<<(unsigned)blocks, 128, 0, s>>>(ws, n, part_s);
+    kg_small_final<HC><<<1, 128, 0, s>>>(part_s, blocks, g_base, g_scale);
+    return cudaGetLastError();
+}
+
+}  // namespace bwg
+
+size_t backward_generic_workspace_bytes(int64_t n, int hc, int d) {
+    if (hc == 2) return bwg::ws_bytes<2>(n, d);
+    if (hc == 8) return bwg::ws_bytes<8>(n, d);
+    return 0;
+}
+
+cudaError_t launch_block_step_backward_generic(int hc, const uint16_t *x, const float *pre_mix,
+                                               const uint16_t *f, const float *hc_fn,
+                                               const float *hc_scale, const float *hc_base,
+                                               const float *norm_w, int64_t n, int d, int iters,
+                                               float eps, float norm_eps, const float *g_hn,
+                                               const float *g_y, const float *g_pre, float *g_x,
+                                               float *g_pm, float *g_f, float *g_fn, float *g_scale,
+                                               float *g_base, float *g_w, void *workspace,
+                                               cudaStream_t s) {
+    if (hc == 2)
+        return bwg::launch<2>(x, pre_mix, f, hc_fn, hc_scale, hc_base, norm_w, n, d, iters, eps, norm_eps, g_hn,
+                              g_y, g_pre, g_x, g_pm, g_f, g_fn, g_scale, g_base, g_w, workspace, s);
+    if (hc == 8)
+        return bwg::launch<8>(x, pre_mix, f, hc_fn, hc_scale, hc_base, norm_w, n, d, iters, eps, norm_eps, g_hn,
+                              g_y, g_pre, g_x, g_pm, g_f, g_fn, g_scale, g_base, g_w, workspace, s);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace hc

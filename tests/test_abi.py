@@ -257,7 +257,7 @@ def _bwd(**kw):
 
 
 @pytest.mark.parametrize("kw,expect", [
-    (dict(hc=2), 2),                         # the backward is compiled for four streams
+    (dict(hc=3), 2),                         # the backward is compiled for 2, 4 and 8 streams
     (dict(hc=3), 2),
     (dict(iters=0), 1),
     (dict(iters=129), 1),
@@ -276,5 +276,6 @@ def test_block_step_backward_workspace_size(lib):
     f = lib.hc_block_step_backward_workspace_bytes
     assert f(0, 4, 5120) >= 0
     assert f(1000, 4, 5120) > f(10, 4, 5120) > 0
-    assert f(16, 2, 5120) == 0 and f(16, 4, 100) == 0
+    assert f(16, 3, 5120) == 0 and f(16, 4, 100) == 0
+    assert f(16, 2, 5120) > 0 and f(16, 8, 5120) > f(16, 4, 5120)
     assert _bwd(n=0) == 0

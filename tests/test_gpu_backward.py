@@ -199,3 +199,34 @@ def test_backward_iteration_limits(iters, eps):
         _np(up["g_pre"]).astype(np.float64), iters=iters, eps=eps, rounded=True)
     _compare(got, ref)
     assert _lib.raw("hc_consume_device_error", None) == 0
+
+
+@pytest.mark.parametrize("hc,n,d,iters", [(2, 5, 256, 20), (8, 5, 256, 20), (2, 37, 1024, 7),
+                                          (8, 9, 1024, 1), (8, 1030, 64, 20)])
+def test_backward_other_stream_counts(hc, n, d, iters):
+    """Two and eight streams (the plain kernels) against the oracle; 1,030
+    tokens cross a parameter-sum block."""
+    case = inputs.tiny(seed=200 + hc + n, n=n, d=d, hc=hc)
+    g = torch.Generator().manual_seed(300 + hc + n)
+    case.pre_mix.copy_(torch.exp2(-torch.randint(0, 4, tuple(case.pre_mix.shape), generator=g).float()))
+    up = dict(g_h_norm=torch.randn((n, d), generator=g), g_y=torch.randn((n, hc, d), generator=g),
+              g_pre=torch.randn((n, hc), generator=g))
+    p = case.params[0]
+    got = hcg.hc_block_step_backward(
+        case.x.to(DEV), case.pre_mix.to(DEV), case.fs[0].to(DEV), *p.to(DEV).astuple(),
+        up["g_h_norm"].to(DEV), up["g_y"].to(DEV), g_pre=up["g_pre"].to(DEV), sinkhorn_iters=iters)
+    torch.cuda.synchronize()
+    assert got["g_x"].shape == (n, hc, d) and got["g_hc_fn"].shape == ((2 + hc) * hc, hc * d)
+    ref = oracle.side_backward(
+        oracle.bf16_to_f64(oracle.bf16_bits(case.x)), _np(case.pre_mix).astype(np.float64),
+        oracle.bf16_to_f64(oracle.bf16_bits(case.fs[0])), *(_np(t).astype(np.float64) for t in p.astuple()),
+        _np(up["g_h_norm"]).astype(np.float64), _np(up["g_y"]).astype(np.float64),
+        _np(up["g_pre"]).astype(np.float64), iters=iters, rounded=True)
+    _compare(got, ref)
+    again = hcg.hc_block_step_backward(
+        case.x.to(DEV), case.pre_mix.to(DEV), case.fs[0].to(DEV), *p.to(DEV).astuple(),
+        up["g_h_norm"].to(DEV), up["g_y"].to(DEV), g_pre=up["g_pre"].to(DEV), sinkhorn_iters=iters)
+    torch.cuda.synchronize()
+    for k in got:
+        assert torch.equal(got[k], again[k]), k
+    assert _lib.raw("hc_consume_device_error", None) == 0
