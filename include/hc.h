@@ -40,7 +40,9 @@
  *    hc_mult; the released model uses 4), with d a positive multiple of 64,
  *    d <= 16384; anything else returns HC_ERR_UNSUPPORTED.  The tensor-core
  *    cluster path of hc_mixes / hc_block_step and the chain (hc_chain_*)
- *    serve hc = 4; the other counts run on the whole-token kernels.
+ *    serve hc = 4; the other counts run on the whole-token kernels.  The
+ *    backward serves all three (tensor-core kernels at hc = 4, plain
+ *    per-token kernels at 2 and 8); its no-workspace entry serves hc = 4.
  *  - Output ranges must not overlap input ranges or each other
  *    (HC_ERR_ALIAS), except where an entry point says otherwise.
  */
@@ -167,7 +169,7 @@ hc_status hc_block_step(const uint16_t *x, const float *pre_mix, const uint16_t 
                         cudaStream_t stream);
 
 /*
- * The backward of one side step a1-a6 (hc = 4).  The pages give no backward
+ * The backward of one side step a1-a6 (hc = 2, 4 or 8).  The pages give no backward
  * pass; this is the derivative of hc_block_step's definition (Block page,
  * Code section; "Stream combination" page), with the three bf16 casts (h,
  * h_norm, y) passing gradients through unchanged (as a dtype cast does in
@@ -190,8 +192,8 @@ size_t hc_block_step_backward_workspace_bytes(int64_t n, int hc, int d);
 /*
  * hc_block_step_backward without a caller workspace: the scratch is a fixed
  * 64 MiB array in device memory that is part of the library's module, so the
- * call allocates nothing.  Inputs whose workspace would not fit (for d = 5120,
- * more than 27,648 tokens) return HC_ERR_UNSUPPORTED.  There is one such
+ * call allocates nothing.  hc = 4 only.  Inputs whose workspace would not fit
+ * (for d = 5120, more than 27,648 tokens) return HC_ERR_UNSUPPORTED.  There is one such
  * array per process and device: calls must not overlap in time (for
  * instance, issue them on one stream).  Results equal
  * hc_block_step_backward's bit for bit.
