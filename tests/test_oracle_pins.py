@@ -654,7 +654,7 @@ def _bwd_case(rng, n, hc, d):
                 norm_w=rng.uniform(0.5, 1.5, d))
 
 
-@pytest.mark.parametrize("hc", [2, 4])
+@pytest.mark.parametrize("hc", [2, 4, 8])
 @pytest.mark.parametrize("iters,eps", [(1, 1e-6), (3, 0.05), (20, 1e-6)])
 def test_side_backward_matches_finite_differences(hc, iters, eps):
     rng = np.random.default_rng(1000 + 10 * hc + iters)
