@@ -65,11 +65,6 @@ constexpr int kGxStages = 3;
 
 __device__ __forceinline__ float sigm(float z) { return 1.0f / (1.0f + expf(-z)); }
 
-__device__ __forceinline__ void load8f(const float *p, float (&o)[8]) {
-    const float4 a = __ldg(reinterpret_cast<const float4 *>(p));
-    const float4 b = __ldg(reinterpret_cast<const float4 *>(p) + 1);
-    o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w; o[4] = b.x; o[5] = b.y; o[6] = b.z; o[7] = b.w;
-}
 __device__ __forceinline__ void unpack4(const uint2 &v, float (&o)[4]) {
     o[0] = bf16lo(v.x);
     o[1] = __uint_as_float(v.x & 0xffff0000u);
