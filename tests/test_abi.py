@@ -258,7 +258,9 @@ def _bwd(**kw):
 
 @pytest.mark.parametrize("kw,expect", [
     (dict(hc=3), 2),                         # the backward is compiled for 2, 4 and 8 streams
-    (dict(hc=3), 2),
+    (dict(hc=16), 2),
+    (dict(hc=2, ws_bytes=1000), 1),          # the workspace asked for depends on hc
+    (dict(hc=8, ws_bytes=1000), 1),
     (dict(iters=0), 1),
     (dict(iters=129), 1),
     (dict(ws=None), 1),
@@ -278,4 +280,4 @@ def test_block_step_backward_workspace_size(lib):
     assert f(1000, 4, 5120) > f(10, 4, 5120) > 0
     assert f(16, 3, 5120) == 0 and f(16, 4, 100) == 0
     assert f(16, 2, 5120) > 0 and f(16, 8, 5120) > f(16, 4, 5120)
-    assert _bwd(n=0) == 0
+    assert _bwd(n=0) == 0 and _bwd(n=0, hc=2) == 0 and _bwd(n=0, hc=8) == 0
