@@ -133,6 +133,57 @@ def hc_pre_norm(x, pre_mix, norm_w, norm_eps=NORM_EPS, out=None, stream=None):
     return out
 
 
+def _backward_args(x, pre_mix, f, hc_fn, hc_scale, hc_base, norm_w, g_h_norm, g_y, g_pre):
+    """Checks every input of the two backward entry points before anything is
+    launched: dtype, contiguity and shape of each tensor first, then that all
+    of them are CUDA tensors on x's device.  Returns (device, hc, d, lead, n)."""
+    if not isinstance(x, torch.Tensor):
+        raise TypeError("x must be a torch.Tensor")
+    if x.dim() < 2:
+        raise ValueError("x must be [..., hc, d]")
+    hc, d = x.shape[-2], x.shape[-1]
+    lead = tuple(x.shape[:-2])
+    mix = (2 + hc) * hc
+    specs = [(x, "x", torch.bfloat16, tuple(x.shape)),
+             (pre_mix, "pre_mix", torch.float32, lead + (hc,)),
+             (f, "f", torch.bfloat16, lead + (d,)),
+             (hc_fn, "hc_fn", torch.float32, (mix, hc * d)),
+             (hc_scale, "hc_scale", torch.float32, (3,)),
+             (hc_base, "hc_base", torch.float32, (mix,)),
+             (norm_w, "norm_w", torch.float32, (d,)),
+             (g_h_norm, "g_h_norm", torch.float32, lead + (d,)),
+             (g_y, "g_y", torch.float32, tuple(x.shape))]
+    if g_pre is not None:
+        specs.append((g_pre, "g_pre", torch.float32, lead + (hc,)))
+    for t, nm, dt, shape in specs:
+        if not isinstance(t, torch.Tensor):
+            raise TypeError("%s must be a torch.Tensor" % nm)
+        if t.dtype != dt:
+            raise TypeError("%s must be %s, got %s" % (nm, dt, t.dtype))
+        if not t.is_contiguous():
+            raise ValueError("%s must be contiguous" % nm)
+        if tuple(t.shape) != shape:
+            raise ValueError("%s has shape %s, expected %s" % (nm, tuple(t.shape), shape))
+    dev = x.device
+    for t, nm, dt, shape in specs:
+        _check(t, nm, dt, dev)
+    n = x.numel() // (hc * d) if x.numel() else 0
+    return dev, hc, d, lead, n
+
+
+def _backward_outputs(x, hc_fn, hc_base, dev, hc, d, lead):
+    return dict(g_x=torch.empty(tuple(x.shape), dtype=torch.float32, device=dev),
+                g_pre_mix=torch.empty(lead + (hc,), dtype=torch.float32, device=dev),
+                g_f=torch.empty(lead + (d,), dtype=torch.float32, device=dev),
+                g_hc_fn=torch.empty(tuple(hc_fn.shape), dtype=torch.float32, device=dev),
+                g_hc_scale=torch.empty(3, dtype=torch.float32, device=dev),
+                g_hc_base=torch.empty(tuple(hc_base.shape), dtype=torch.float32, device=dev),
+                g_norm_w=torch.empty(d, dtype=torch.float32, device=dev))
+
+
+_GRAD_KEYS = ("g_x", "g_pre_mix", "g_f", "g_hc_fn", "g_hc_scale", "g_hc_base", "g_norm_w")
+
+
 def hc_block_step_backward(x, pre_mix, f, hc_fn, hc_scale, hc_base, norm_w, g_h_norm, g_y,
                            g_pre=None, sinkhorn_iters=SINKHORN_ITERS, eps=HC_EPS, norm_eps=NORM_EPS,
                            workspace=None, stream=None):
@@ -141,34 +192,19 @@ def hc_block_step_backward(x, pre_mix, f, hc_fn, hc_scale, hc_base, norm_w, g_h_
     gradients g_hc_fn, g_hc_scale, g_hc_base, g_norm_w summed over tokens.
     workspace: a uint8 device tensor of at least the size the library asks
     for (allocated here when None)."""
-    _check(x, "x", torch.bfloat16)
-    dev = x.device
-    hc, d = x.shape[-2], x.shape[-1]
-    lead = tuple(x.shape[:-2])
-    n = x.numel() // (hc * d) if x.numel() else 0
-    for t, nm, dt in ((pre_mix, "pre_mix", torch.float32), (f, "f", torch.bfloat16),
-                      (hc_fn, "hc_fn", torch.float32), (hc_scale, "hc_scale", torch.float32),
-                      (hc_base, "hc_base", torch.float32), (norm_w, "norm_w", torch.float32),
-                      (g_h_norm, "g_h_norm", torch.float32), (g_y, "g_y", torch.float32)):
-        _check(t, nm, dt, dev)
-    if g_pre is not None:
-        _check(g_pre, "g_pre", torch.float32, dev)
-    out = dict(g_x=torch.empty(tuple(x.shape), dtype=torch.float32, device=dev),
-               g_pre_mix=torch.empty(lead + (hc,), dtype=torch.float32, device=dev),
-               g_f=torch.empty(lead + (d,), dtype=torch.float32, device=dev),
-               g_hc_fn=torch.empty(tuple(hc_fn.shape), dtype=torch.float32, device=dev),
-               g_hc_scale=torch.empty(3, dtype=torch.float32, device=dev),
-               g_hc_base=torch.empty(tuple(hc_base.shape), dtype=torch.float32, device=dev),
-               g_norm_w=torch.empty(d, dtype=torch.float32, device=dev))
+    dev, hc, d, lead, n = _backward_args(x, pre_mix, f, hc_fn, hc_scale, hc_base, norm_w,
+                                         g_h_norm, g_y, g_pre)
+    out = _backward_outputs(x, hc_fn, hc_base, dev, hc, d, lead)
     need = _lib.load().hc_block_step_backward_workspace_bytes(n, hc, d)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    else:
+        _check(workspace, "workspace", torch.uint8, dev)
     with torch.cuda.device(dev):
         _lib.call("hc_block_step_backward", _ptr(x), _ptr(pre_mix), _ptr(f), _ptr(hc_fn),
                   _ptr(hc_scale), _ptr(hc_base), _ptr(norm_w), n, hc, d, sinkhorn_iters, eps,
                   norm_eps, _ptr(g_h_norm), _ptr(g_y), _ptr(g_pre),
-                  *(_ptr(out[k]) for k in ("g_x", "g_pre_mix", "g_f", "g_hc_fn", "g_hc_scale",
-                                           "g_hc_base", "g_norm_w")),
+                  *(_ptr(out[k]) for k in _GRAD_KEYS),
                   _ptr(workspace), workspace.numel(), _stream(stream))
     return out
 
@@ -177,25 +213,16 @@ def hc_block_step_backward_no_workspace(x, pre_mix, f, hc_fn, hc_scale, hc_base,
                                         g_y, g_pre=None, sinkhorn_iters=SINKHORN_ITERS, eps=HC_EPS,
                                         norm_eps=NORM_EPS, stream=None):
     """hc_block_step_backward with the library's own fixed scratch (no
-    workspace argument, nothing allocated by the call); same results."""
-    _check(x, "x", torch.bfloat16)
-    dev = x.device
-    hc, d = x.shape[-2], x.shape[-1]
-    lead = tuple(x.shape[:-2])
-    n = x.numel() // (hc * d) if x.numel() else 0
-    out = dict(g_x=torch.empty(tuple(x.shape), dtype=torch.float32, device=dev),
-               g_pre_mix=torch.empty(lead + (hc,), dtype=torch.float32, device=dev),
-               g_f=torch.empty(lead + (d,), dtype=torch.float32, device=dev),
-               g_hc_fn=torch.empty(tuple(hc_fn.shape), dtype=torch.float32, device=dev),
-               g_hc_scale=torch.empty(3, dtype=torch.float32, device=dev),
-               g_hc_base=torch.empty(tuple(hc_base.shape), dtype=torch.float32, device=dev),
-               g_norm_w=torch.empty(d, dtype=torch.float32, device=dev))
+    workspace argument, nothing allocated by the call); same results.  The
+    inputs are checked exactly as hc_block_step_backward checks them."""
+    dev, hc, d, lead, n = _backward_args(x, pre_mix, f, hc_fn, hc_scale, hc_base, norm_w,
+                                         g_h_norm, g_y, g_pre)
+    out = _backward_outputs(x, hc_fn, hc_base, dev, hc, d, lead)
     with torch.cuda.device(dev):
         _lib.call("hc_block_step_backward_no_workspace", _ptr(x), _ptr(pre_mix), _ptr(f), _ptr(hc_fn),
                   _ptr(hc_scale), _ptr(hc_base), _ptr(norm_w), n, hc, d, sinkhorn_iters, eps,
                   norm_eps, _ptr(g_h_norm), _ptr(g_y), _ptr(g_pre),
-                  *(_ptr(out[k]) for k in ("g_x", "g_pre_mix", "g_f", "g_hc_fn", "g_hc_scale",
-                                           "g_hc_base", "g_norm_w")), _stream(stream))
+                  *(_ptr(out[k]) for k in _GRAD_KEYS), _stream(stream))
     return out
 
 

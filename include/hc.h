@@ -183,7 +183,10 @@ hc_status hc_block_step(const uint16_t *x, const float *pre_mix, const uint16_t 
  *   summed over the n tokens (overwritten, not accumulated)             out
  *   workspace: device scratch of at least
  *   hc_block_step_backward_workspace_bytes(n, hc, d) bytes, 16-byte
- *   aligned, owned by the caller (the library allocates nothing)
+ *   aligned, owned by the caller (the library allocates nothing); at hc = 4
+ *   that is 4 * (112 n + B (24 * 4d + d + 32)) bytes, B = ceil(n / 1024):
+ *   a 112-float record per token, then per block of 1,024 tokens the partial
+ *   sums of g_hc_fn, g_norm_w and g_hc_base / g_hc_scale
  * Results are deterministic: the token sums run in a fixed order.
  * sinkhorn_iters must be in [1, 128] (HC_ERR_INVALID_ARG otherwise).
  */

@@ -14,13 +14,20 @@ before the final rounding, derived from the operation:
     and rounds 5 times in fp32: a = dc (|f| + sum_j |x[j]|) + 6 u S with
     S = |post[k] f| + sum_j |comb[j][k] x[j]| and u = 2^-24.
   h_norm = bf16((bf16(sum_s pm[s] x[s]) * rs) * w)
-    The fp32 sum of 4 products rounds 4 times before its bf16 rounding, so
-    h can land on the other side of a bf16 rounding boundary, off by up to
-    5 u S_h with S_h = sum_s |pm[s] x[s]|; scaled by rs |w| on the way out:
-    a = (ulp_bf16(h) + 5 u S_h) rs |w| + 4 u |ref|.
+    The GPU sums the hc products in fp32 with hc roundings (a product, then
+    fused multiply-adds), so its h is within hc u S_h of the exact sum, with
+    S_h = sum_s |pm[s] x[s]|.  Only where the exact h lies that close to a
+    bf16 rounding midpoint (within (hc + 1) u S_h) can the fp32 sum round to
+    the other bf16 neighbour of h; there, and only there, h_norm may be off by
+    one bf16 spacing of h, scaled by rs |w|.  Every element also gets
+    4 u |ref| for the fp32 products (h rs) w:
+    a = [h near a midpoint] spacing_bf16(h) rs |w| + 4 u |ref|.
+    Everywhere else the bound is 1 ulp + 1e-3 |ref| + 4 u |ref|, so an h
+    rounded the wrong way (truncated, toward zero) or an h_norm two ulps off
+    fails it.
 
-Away from cancellation `a` is far below 1e-3 |ref|; it only matters where the
-result is tiny compared to the terms it is summed from.
+So `a` matters only where a result is tiny next to the terms it is summed
+from, or (h_norm) where h sits on a bf16 rounding midpoint.
 """
 import numpy as np
 
@@ -97,17 +104,43 @@ def y_allowance(f_bits, x_bits, post_ref, comb_ref, post_got=None, comb_got=None
     return dc[:, None, None] * (np.abs(f)[:, None, :] + ax.sum(axis=1)[:, None, :]) + 6 * U32 * S
 
 
+def _bf16_mag(bits):
+    """|value| of bf16 bit patterns (the sign bit dropped)."""
+    return bf16_to_f64(np.asarray(bits, dtype=np.uint16) & np.uint16(0x7FFF))
+
+
+def h_midpoint_window(x_bits, pre_mix):
+    """For h = sum_s pm[s] x[s]: a mask of the elements whose exact h lies
+    within (hc + 1) u S_h of a bf16 rounding midpoint (where an fp32
+    evaluation may round to the other neighbour), and the bf16 spacing of h
+    on the side of that midpoint.  The rounded h is the oracle's own hc_pre
+    (fp64 sum, one round to nearest even)."""
+    from . import pre as oracle_pre
+    xb = _bits(x_bits)
+    x = bf16_to_f64(xb)                              # [n, hc, d]
+    hc = x.shape[1]
+    pm = np.asarray(pre_mix, np.float64)             # [n, hc]
+    terms = pm[:, :, None] * x
+    a = np.abs(terms.sum(axis=1))                    # |h|
+    S_h = np.abs(terms).sum(axis=1)
+    hb = oracle_pre(xb, pm) & np.uint16(0x7FFF)      # bits of |bf16(h)|
+    mag = _bf16_mag(hb)
+    up = _bf16_mag(hb + np.uint16(1))                # the next bf16 magnitude above
+    dn = np.where(hb == 0, -up, _bf16_mag(np.maximum(hb, np.uint16(1)) - np.uint16(1)))
+    d_up = np.abs(a - 0.5 * (mag + up))
+    d_dn = np.abs(a - 0.5 * (mag + dn))
+    near = np.minimum(d_up, d_dn) <= (hc + 1) * U32 * S_h
+    spacing = np.where(d_up <= d_dn, up - mag, mag - dn)
+    return near, spacing
+
+
 def h_norm_allowance(x_bits, pre_mix, norm_w, h_norm_ref_bits, eps=1e-20):
     """Absolute allowance for h_norm [n, d] (see the module docstring)."""
-    x = bf16_to_f64(_bits(x_bits))                   # [n, hc, d]
+    from . import pre as oracle_pre
     pm = np.asarray(pre_mix, np.float64)             # [n, hc]
     w = np.abs(np.asarray(norm_w, np.float64))       # [d]
-    terms = pm[:, :, None] * x
-    h = terms.sum(axis=1)
-    S_h = np.abs(terms).sum(axis=1)
-    from . import bf16_from_f64
-    hb = bf16_to_f64(bf16_from_f64(h)) if h.size <= 200000 else h
+    hb = bf16_to_f64(oracle_pre(_bits(x_bits), pm))
     rs = 1.0 / np.sqrt(np.mean(hb * hb, axis=1, keepdims=True) + eps)
-    ulp_h = np.abs(h) * 2.0 ** -7 + 1e-40
+    near, spacing = h_midpoint_window(x_bits, pm)
     ref = np.abs(bf16_to_f64(_bits(h_norm_ref_bits)))
-    return (ulp_h + 5 * U32 * S_h) * rs * w[None, :] + 4 * U32 * ref
+    return np.where(near, spacing * rs * w[None, :], 0.0) + 4 * U32 * ref

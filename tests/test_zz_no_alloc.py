@@ -22,10 +22,10 @@ def lib():
     return _lib.load()
 
 
-def _raw(lib, n, hc=4, d=5120):
+def _raw(lib, n, hc=4, d=5120, iters=20):
     return lib.hc_block_step_backward_no_workspace(
         FAKE, FAKE + 0x100000, FAKE + 0x200000, FAKE + 0x300000, FAKE + 0x400000, FAKE + 0x500000,
-        FAKE + 0x600000, n, hc, d, 20, 1e-6, 1e-20, FAKE + 0x700000, FAKE + 0x800000, None,
+        FAKE + 0x600000, n, hc, d, iters, 1e-6, 1e-20, FAKE + 0x700000, FAKE + 0x800000, None,
         FAKE2 * 0x100, FAKE2 * 0x200, FAKE2 * 0x300, FAKE2 * 0x400, FAKE2 * 0x500, FAKE2 * 0x600,
         FAKE2 * 0x700, None)
 
@@ -34,6 +34,66 @@ def test_no_workspace_entry_refuses_what_does_not_fit(lib):
     assert _raw(lib, 27649) == 2          # one token beyond the fixed scratch at d = 5120
     assert _raw(lib, 16, hc=2) == 2
     assert _raw(lib, 0) == 0
+
+
+def _documented_workspace_bytes(n, d):
+    """The backward's workspace at four streams as include/hc.h states it:
+    112 fp32 per token, then per block of 1,024 tokens the partial sums of
+    g_hc_fn (24 x 4d), g_norm_w (d) and g_hc_base / g_hc_scale (32)."""
+    blocks = -(-n // 1024)
+    return 4 * (112 * n + blocks * (24 * 4 * d + d + 32))
+
+
+@pytest.mark.parametrize("d", [1024, 2048, 5120])
+def test_no_workspace_capacity_edge_at_other_widths(lib, d):
+    """The largest batch that fits the fixed 64 MiB scratch, from the documented
+    formula: it passes the capacity check, one more token does not.  Both calls
+    pass sinkhorn_iters = 0, so the one that passes the capacity check stops at
+    argument validation (or, without a GPU, at the scratch lookup) and nothing
+    is launched."""
+    cap = 64 << 20
+    n = 1
+    while _documented_workspace_bytes(2 * n, d) <= cap:
+        n *= 2
+    lo, hi = n, 2 * n                    # fits at lo, not at hi
+    while hi - lo > 1:
+        mid = (lo + hi) // 2
+        lo, hi = (mid, hi) if _documented_workspace_bytes(mid, d) <= cap else (lo, mid)
+    assert lib.hc_block_step_backward_workspace_bytes(lo, 4, d) == _documented_workspace_bytes(lo, d)
+    assert _raw(lib, lo, d=d, iters=0) != 2
+    assert _raw(lib, lo + 1, d=d, iters=0) == 2
+    if d == 5120:
+        assert lo == 27648
+
+
+def test_no_workspace_wrapper_checks_every_input():
+    """The Python wrapper refuses a wrong dtype, a non-contiguous tensor or a
+    wrong shape on any input before it calls the library, exactly as the
+    workspace wrapper does (CPU tensors here: the dtype, layout and shape checks
+    come before the device check)."""
+    n, d = 6, 64
+    g = torch.Generator().manual_seed(1)
+    x = inputs.streams(g, n, 4, d)
+    p = inputs.side_params(g, d=d)
+    good = dict(x=x, pre_mix=inputs.pre_mix(g, n), f=inputs.sublayer_out(g, n, d),
+                hc_fn=p.hc_fn, hc_scale=p.hc_scale, hc_base=p.hc_base, norm_w=p.norm_w,
+                g_h_norm=torch.randn(n, d), g_y=torch.randn(n, 4, d), g_pre=torch.randn(n, 4))
+    bad_cases = [
+        ("g_y", good["g_y"].to(torch.bfloat16), TypeError),
+        ("g_h_norm", good["g_h_norm"].to(torch.bfloat16), TypeError),
+        ("pre_mix", torch.randn(4, n).t(), ValueError),            # not contiguous
+        ("g_y", torch.randn(n, 4, d + 64), ValueError),             # wrong shape
+        ("hc_fn", torch.randn(24, 4 * d + 64), ValueError),
+        ("f", good["f"].float(), TypeError),
+    ]
+    for fn in (hcg.hc_block_step_backward_no_workspace, hcg.hc_block_step_backward):
+        for name, t, err in bad_cases:
+            kw = dict(good)
+            kw[name] = t
+            with pytest.raises(err, match=name):
+                fn(**kw)
+        with pytest.raises(ValueError, match="CUDA"):
+            fn(**good)
 
 
 @pytest.mark.gpu
