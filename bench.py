@@ -371,7 +371,254 @@ def run_ours(args, rank, local_rank, world):
                         "steps (rank 0's clock); outputs identical to the chain's bit for bit"}
         if world == 1 and not args.no_cpu_baseline and args.workload == "long_prefill":
             out["cpu_baseline"] = cpu_baseline_sample(case, fs, target_s=args.cpu_seconds)
+        if chain and args.workload == "long_prefill" and not args.no_configs:
+            out["chain_equals_step"] = chain_equals_steps(case, fs, dev, stream)
+    if rank == 0 and world == 1 and args.workload == "long_prefill" and not args.no_configs:
+        del fs, case, ys, h_norm, states
+        torch.cuda.empty_cache()
+        out["configs"] = run_configs(dev, measured_peaks()[0], stream)
     return out
+
+
+def _event_ms(fn, k, stream, flush=None):
+    """CUDA-event durations (ms) of k calls of fn on `stream`.  With `flush` (a
+    device buffer larger than L2) the buffer is rewritten before every call,
+    outside the timed events, so that no call finds its inputs in L2."""
+    out = []
+    for _ in range(k):
+        if flush is not None:
+            flush.add_(1)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        out.append((a, b))
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in out]
+
+
+def _oracle_rate(fn, units, what):
+    """The oracle on a sample, timed on one host core: units per second."""
+    t0 = time.perf_counter()
+    fn()
+    dt = time.perf_counter() - t0
+    return {"value": units / dt, "cores": 1, "kind": "oracle", "sample": "%s (%.2f s)" % (what, dt)}
+
+
+def run_configs(dev, peak, stream):
+    """Every workload besides the long prefill, timed with CUDA events on the
+    launching stream: tiny (16 tokens, one side), decode (128 tokens, two
+    sides), the Sinkhorn-only stress (2^20 rows) and the prefill (8,192 tokens
+    with outliers, two sides, through one hc_block_step per side and through
+    the chain).  Inputs smaller than L2 are timed with L2 flushed before every
+    call; each record carries its roofline fraction and the oracle timed on a
+    sample of the same inputs."""
+    import oracle
+    oracle.build()
+    flush = torch.empty(64 << 20, dtype=torch.int32, device=dev)   # 256 MB, twice the L2
+    recs = {}
+    side_bytes = lambda n: n * BYTES_PER_TOKEN + BYTES_WEIGHTS
+    np_params = lambda p: tuple(t.detach().cpu().numpy() for t in p.astuple())
+
+    # tiny: one side step on 16 tokens
+    case = inputs.tiny(device=dev)
+    p = case.params[0]
+    h = torch.empty((case.n, case.d), dtype=torch.bfloat16, device=dev)
+    y = torch.empty_like(case.x)
+    pre = torch.empty_like(case.pre_mix)
+    fn = lambda: hcg.hc_block_step(case.x, case.pre_mix, case.fs[0], *p.astuple(), h_norm=h, y=y,
+                                   pre_out=pre, stream=stream)
+    for _ in range(5):
+        fn()
+    cold = _event_ms(fn, 50, stream, flush)
+    warm = _event_ms(fn, 50, stream)
+    alg = side_bytes(case.n)
+    xb, fb = inputs.bf16_bits_np(case.x), inputs.bf16_bits_np(case.fs[0])
+    pmn = case.pre_mix.cpu().numpy().astype(np.float64)
+    cpu = _oracle_rate(lambda: oracle.block_step(xb, pmn, fb, *np_params(p)), case.n,
+                       "all 16 tokens, one side step")
+    cpu["unit"] = "tokens/s"
+    recs["tiny"] = {
+        "workload": "tiny: B=1, T=16, one hc_block_step side (seed 0)", "tokens": case.n, "sides": 1,
+        "us_per_side": 1e3 * statistics.mean(cold), "us_per_side_median": 1e3 * statistics.median(cold),
+        "us_per_side_l2_warm": 1e3 * statistics.mean(warm),
+        "tokens_per_s": case.n / (statistics.mean(cold) / 1e3),
+        "algorithmic_bytes": alg, "hbm_gbs": alg / (statistics.mean(cold) / 1e3) / 1e9,
+        "roofline_frac": alg / (statistics.mean(cold) / 1e3) / 1e9 / peak,
+        "l2": "flushed before every call (256 MB written); l2_warm: back to back", "calls": len(cold),
+        "cpu_baseline": cpu}
+
+    # decode: 128 tokens, attention side then FFN side (the FFN side reads with the attention side's pre)
+    case = inputs.decode(device=dev)
+    pa, pf = case.params
+    ya, yf = torch.empty_like(case.x), torch.empty_like(case.x)
+    ha = torch.empty((case.n, case.d), dtype=torch.bfloat16, device=dev)
+    prea, pref = torch.empty_like(case.pre_mix), torch.empty_like(case.pre_mix)
+
+    def two_sides():
+        hcg.hc_block_step(case.x, case.pre_mix, case.fs[0], *pa.astuple(), h_norm=ha, y=ya, pre_out=prea,
+                          stream=stream)
+        hcg.hc_block_step(ya, prea, case.fs[1], *pf.astuple(), h_norm=ha, y=yf, pre_out=pref, stream=stream)
+    for _ in range(5):
+        two_sides()
+    cold = _event_ms(two_sides, 50, stream, flush)
+    alg = 2 * side_bytes(case.n)
+    xb = inputs.bf16_bits_np(case.x)
+    fbs = [inputs.bf16_bits_np(f) for f in case.fs]
+    pmn = case.pre_mix.cpu().numpy().astype(np.float64)
+
+    def oracle_two():
+        o = oracle.block_step(xb, pmn, fbs[0], *np_params(pa))
+        oracle.block_step(o["y"], o["pre"], fbs[1], *np_params(pf))
+    cpu = _oracle_rate(oracle_two, case.n, "all 128 tokens through both sides")
+    cpu["unit"] = "tokens/s"
+    recs["decode"] = {
+        "workload": "decode: B=128, T=1, attention + FFN side, two hc_block_step launches (seed 1)",
+        "tokens": case.n, "sides": 2, "us_per_side": 1e3 * statistics.mean(cold) / 2,
+        "us_two_sides_median": 1e3 * statistics.median(cold),
+        "tokens_per_s": case.n / (statistics.mean(cold) / 1e3),
+        "algorithmic_bytes": alg, "hbm_gbs": alg / (statistics.mean(cold) / 1e3) / 1e9,
+        "roofline_frac": alg / (statistics.mean(cold) / 1e3) / 1e9 / peak,
+        "l2": "flushed before every two-side call (the 1.99 MB of weights per side counted)",
+        "calls": len(cold), "cpu_baseline": cpu}
+    del ya, yf, ha
+
+    # Sinkhorn-only stress: 2^20 rows of N(0, 3) mixes
+    m, sc, base = (t.to(dev) for t in inputs.sinkhorn_stress(device="cpu"))
+    rows = m.shape[0]
+    pre_s = torch.empty((rows, HC), device=dev)
+    post_s = torch.empty((rows, HC), device=dev)
+    comb_s = torch.empty((rows, HC, HC), device=dev)
+    fn = lambda: hcg.hc_split_sinkhorn(m, sc, base, pre=pre_s, post=post_s, comb=comb_s, stream=stream)
+    for _ in range(5):
+        fn()
+    cold = _event_ms(fn, 30, stream, flush)
+    alg = rows * 192 + 12 + MIX * 4
+    ms = m[:16384].cpu().numpy().astype(np.float64)
+    cpu = _oracle_rate(lambda: oracle.split_sinkhorn(ms, sc.cpu().numpy(), base.cpu().numpy()), len(ms),
+                       "16,384 of 1,048,576 rows")
+    cpu["unit"] = "rows/s"
+    recs["sinkhorn_stress"] = {
+        "workload": "Sinkhorn-only stress: 1,048,576 rows, hc_split_sinkhorn, 20 rounds (seed 2)",
+        "rows": rows, "us_per_call": 1e3 * statistics.mean(cold), "rows_per_s": rows / (statistics.mean(cold) / 1e3),
+        "algorithmic_bytes": alg, "bytes_per_row": 192, "hbm_gbs": alg / (statistics.mean(cold) / 1e3) / 1e9,
+        "roofline_frac": alg / (statistics.mean(cold) / 1e3) / 1e9 / peak,
+        "l2": "flushed before every call (inputs 100.7 MB, under L2)", "calls": len(cold), "cpu_baseline": cpu}
+    del m, pre_s, post_s, comb_s
+
+    # prefill: 8,192 tokens with outliers, two sides, through hc_block_step and through the chain
+    case = inputs.prefill(device=dev)
+    pa, pf = case.params
+    n = case.n
+    ys = [torch.empty_like(case.x), torch.empty_like(case.x)]
+    hn = torch.empty((n, case.d), dtype=torch.bfloat16, device=dev)
+    pres = [torch.empty_like(case.pre_mix), torch.empty_like(case.pre_mix)]
+    states = [torch.empty((n, hcg.STATE_FLOATS), device=dev) for _ in range(2)]
+    evs_step = []
+
+    def steps(record):
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        e[0].record(stream)
+        hcg.hc_block_step(case.x, case.pre_mix, case.fs[0], *pa.astuple(), h_norm=hn, y=ys[0],
+                          pre_out=pres[0], stream=stream)
+        e[1].record(stream)
+        hcg.hc_block_step(ys[0], pres[0], case.fs[1], *pf.astuple(), h_norm=hn, y=ys[1], pre_out=pres[1],
+                          stream=stream)
+        e[2].record(stream)
+        if record:
+            evs_step.append(e)
+    evs_chain = []
+
+    def chain(record):
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        e[0].record(stream)
+        hcg.hc_chain_begin(case.x, case.pre_mix, pa.hc_fn, pa.hc_scale, pa.hc_base, state_out=states[0],
+                           pre_out=pres[0], stream=stream)
+        e[1].record(stream)
+        hcg.hc_chain_side(case.x, case.fs[0], states[0], pa.norm_w, pf.hc_fn, pf.hc_scale, pf.hc_base,
+                          h_norm=hn, y=ys[0], state_out=states[1], pre_out=pres[1], stream=stream)
+        e[2].record(stream)
+        hcg.hc_chain_side(ys[0], case.fs[1], states[1], pf.norm_w, h_norm=hn, y=ys[1], stream=stream)
+        e[3].record(stream)
+        if record:
+            evs_chain.append(e)
+    for _ in range(3):
+        steps(False)
+        chain(False)
+    for _ in range(10):
+        steps(True)
+    for _ in range(10):
+        chain(True)
+    torch.cuda.synchronize()
+    alg = side_bytes(n)
+    st_launch = [e[i].elapsed_time(e[i + 1]) for e in evs_step for i in range(2)]
+    st_pair = [e[0].elapsed_time(e[2]) for e in evs_step]
+    ch_pair = [e[0].elapsed_time(e[3]) for e in evs_chain]
+    ch_fused = [e[1].elapsed_time(e[2]) for e in evs_chain]
+    rows_o = np.sort(np.random.default_rng(3).choice(n, 64, replace=False))
+    ri = torch.from_numpy(rows_o).to(dev)
+    xb = inputs.bf16_bits_np(case.x.index_select(0, ri))
+    fbs = [inputs.bf16_bits_np(f.index_select(0, ri)) for f in case.fs]
+    pmn = case.pre_mix.index_select(0, ri).cpu().numpy().astype(np.float64)
+
+    def oracle_two():
+        o = oracle.block_step(xb, pmn, fbs[0], *np_params(pa))
+        oracle.block_step(o["y"], o["pre"], fbs[1], *np_params(pf))
+    cpu = _oracle_rate(oracle_two, len(rows_o), "64 of 8,192 tokens through both sides")
+    cpu["unit"] = "tokens/s"
+    recs["prefill"] = {
+        "workload": "prefill: B=1, T=8192, 1% outliers x50, attention + FFN side (seed 3)",
+        "tokens": n, "sides": 2, "algorithmic_bytes_per_side": alg,
+        "l2": "inputs larger than L2 (x is 335.5 MB); no flush",
+        "step": {"path": "two hc_block_step launches", "us_per_side": 1e3 * statistics.mean(st_launch),
+                 "tokens_per_s": n / (statistics.mean(st_pair) / 1e3),
+                 "roofline_frac": alg / (statistics.mean(st_launch) / 1e3) / 1e9 / peak,
+                 "meets_0_70": alg / (statistics.mean(st_launch) / 1e3) / 1e9 / peak >= 0.70},
+        "chain": {"path": "hc_chain_begin + fused hc_chain_side + last hc_chain_side",
+                  "us_both_sides": 1e3 * statistics.mean(ch_pair),
+                  "tokens_per_s": n / (statistics.mean(ch_pair) / 1e3),
+                  "roofline_frac_both_sides": 2 * alg / (statistics.mean(ch_pair) / 1e3) / 1e9 / peak,
+                  "us_fused_launch": 1e3 * statistics.mean(ch_fused),
+                  "roofline_frac_fused_launch": alg / (statistics.mean(ch_fused) / 1e3) / 1e9 / peak,
+                  "meets_0_70": 2 * alg / (statistics.mean(ch_pair) / 1e3) / 1e9 / peak >= 0.70},
+        "calls": len(evs_step), "cpu_baseline": cpu}
+    return recs
+
+
+def chain_equals_steps(case, fs, dev, stream):
+    """The long prefill's 80 sides through the chain and through one
+    hc_block_step per side, side by side on the same inputs: h_norm, y and pre
+    of every side compared bit for bit."""
+    n, d = case.n, case.d
+    P = case.params
+    ys = [torch.empty_like(case.x) for _ in range(2)]
+    yc = [torch.empty_like(case.x) for _ in range(2)]
+    hs = torch.empty((n, d), dtype=torch.bfloat16, device=dev)
+    hcn = torch.empty_like(hs)
+    ps = [torch.empty_like(case.pre_mix) for _ in range(2)]
+    pc = [torch.empty_like(case.pre_mix) for _ in range(2)]
+    st = [torch.empty((n, hcg.STATE_FLOATS), device=dev) for _ in range(2)]
+    hcg.hc_chain_begin(case.x, case.pre_mix, P[0].hc_fn, P[0].hc_scale, P[0].hc_base, state_out=st[0],
+                       pre_out=pc[0], stream=stream)
+    xs, pms, xc = case.x, case.pre_mix, case.x
+    first = None
+    for s in range(len(P)):
+        b = s % 2
+        hcg.hc_block_step(xs, pms, fs[s], *P[s].astuple(), h_norm=hs, y=ys[b], pre_out=ps[b], stream=stream)
+        if s + 1 < len(P):
+            q = P[s + 1]
+            hcg.hc_chain_side(xc, fs[s], st[b], P[s].norm_w, q.hc_fn, q.hc_scale, q.hc_base, h_norm=hcn,
+                              y=yc[b], state_out=st[1 - b], pre_out=pc[1 - b], stream=stream)
+        else:
+            hcg.hc_chain_side(xc, fs[s], st[b], P[s].norm_w, h_norm=hcn, y=yc[b], stream=stream)
+        for name, u, v in (("h_norm", hs, hcn), ("y", ys[b], yc[b]), ("pre", ps[b], pc[b])):
+            if first is None and not torch.equal(u.view(torch.int16) if u.dtype == torch.bfloat16 else u,
+                                                 v.view(torch.int16) if v.dtype == torch.bfloat16 else v):
+                first = "side %d %s" % (s, name)
+        xs, pms, xc = ys[b], ps[b], yc[b]
+    torch.cuda.synchronize()
+    return {"sides": len(P), "equal": first is None, "first_difference": first,
+            "compared": "h_norm, y and pre of every side, bit for bit"}
 
 
 def run_e2e(args, dev, case, seed, world):
@@ -699,6 +946,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling runs)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--reference-tokens", type=int, default=4)
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other workloads' sub-records and the chain/step comparison")
     ap.add_argument("--no-step-path", action="store_true",
                     help="with the chain, skip timing the one-launch-per-side path beside it")
     ap.add_argument("--path", choices=["chain", "step"], default="chain",

@@ -18,10 +18,12 @@ before the final rounding, derived from the operation:
     fused multiply-adds), so its h is within hc u S_h of the exact sum, with
     S_h = sum_s |pm[s] x[s]|.  Only where the exact h lies that close to a
     bf16 rounding midpoint (within (hc + 1) u S_h) can the fp32 sum round to
-    the other bf16 neighbour of h; there, and only there, h_norm may be off by
-    one bf16 spacing of h, scaled by rs |w|.  Every element also gets
-    4 u |ref| for the fp32 products (h rs) w:
-    a = [h near a midpoint] spacing_bf16(h) rs |w| + 4 u |ref|.
+    another bf16 value than the exact h does; there, and only there, the two
+    rounded h differ by at most (hc + 1) u S_h + one bf16 spacing of h (more
+    than one spacing only under cancellation, S_h >> |h|), scaled by rs |w|
+    on the way out.  Every element also gets 4 u |ref| for the fp32 products
+    (h rs) w:
+    a = [h near a midpoint] (spacing_bf16(h) + (hc + 1) u S_h) rs |w| + 4 u |ref|.
     Everywhere else the bound is 1 ulp + 1e-3 |ref| + 4 u |ref|, so an h
     rounded the wrong way (truncated, toward zero) or an h_norm two ulps off
     fails it.
@@ -111,10 +113,10 @@ def _bf16_mag(bits):
 
 def h_midpoint_window(x_bits, pre_mix):
     """For h = sum_s pm[s] x[s]: a mask of the elements whose exact h lies
-    within (hc + 1) u S_h of a bf16 rounding midpoint (where an fp32
-    evaluation may round to the other neighbour), and the bf16 spacing of h
-    on the side of that midpoint.  The rounded h is the oracle's own hc_pre
-    (fp64 sum, one round to nearest even)."""
+    within the fp32 error window (hc + 1) u S_h of a bf16 rounding midpoint
+    (where an fp32 evaluation may round differently), the bf16 spacing of h
+    on the side of that midpoint, and the window itself.  The rounded h is
+    the oracle's own hc_pre (fp64 sum, one round to nearest even)."""
     from . import pre as oracle_pre
     xb = _bits(x_bits)
     x = bf16_to_f64(xb)                              # [n, hc, d]
@@ -129,9 +131,10 @@ def h_midpoint_window(x_bits, pre_mix):
     dn = np.where(hb == 0, -up, _bf16_mag(np.maximum(hb, np.uint16(1)) - np.uint16(1)))
     d_up = np.abs(a - 0.5 * (mag + up))
     d_dn = np.abs(a - 0.5 * (mag + dn))
-    near = np.minimum(d_up, d_dn) <= (hc + 1) * U32 * S_h
+    window = (hc + 1) * U32 * S_h
+    near = np.minimum(d_up, d_dn) <= window
     spacing = np.where(d_up <= d_dn, up - mag, mag - dn)
-    return near, spacing
+    return near, spacing, window
 
 
 def h_norm_allowance(x_bits, pre_mix, norm_w, h_norm_ref_bits, eps=1e-20):
@@ -141,6 +144,6 @@ def h_norm_allowance(x_bits, pre_mix, norm_w, h_norm_ref_bits, eps=1e-20):
     w = np.abs(np.asarray(norm_w, np.float64))       # [d]
     hb = bf16_to_f64(oracle_pre(_bits(x_bits), pm))
     rs = 1.0 / np.sqrt(np.mean(hb * hb, axis=1, keepdims=True) + eps)
-    near, spacing = h_midpoint_window(x_bits, pm)
+    near, spacing, window = h_midpoint_window(x_bits, pm)
     ref = np.abs(bf16_to_f64(_bits(h_norm_ref_bits)))
-    return np.where(near, spacing * rs * w[None, :], 0.0) + 4 * U32 * ref
+    return np.where(near, (spacing + window) * rs * w[None, :], 0.0) + 4 * U32 * ref

@@ -155,3 +155,19 @@ def test_chain_against_oracle_sampled():
         check_bf16("side %d y" % i, sel(y), ref["y"],
                    abs_allow=y_allowance(bits(fsel), bits(xs), ref["post"], ref["comb"], post_g, comb_g))
         x, pm = y, pre
+
+
+def test_chain_equals_block_steps_80_sides_8192_tokens():
+    """A full 40-layer stack (80 sides, each with its own parameters and f) at
+    8,192 tokens: every side's h_norm, y and pre through the chain equal those
+    of 80 hc_block_step calls bit for bit."""
+    n = 8192
+    case = inputs.long_prefill(device=DEV, n=n, materialize_f=False)
+    S = len(case.params)
+    assert S == 80
+    fs = [inputs.long_prefill_f(s, n, case.d, DEV) for s in range(S)]
+    ref = _steps(case.x, case.pre_mix, fs, case.params)
+    got = _chain(case.x, case.pre_mix, fs, case.params)
+    torch.cuda.synchronize()
+    _compare(ref, got)
+    assert _lib.raw("hc_consume_device_error", None) == 0

@@ -39,7 +39,7 @@ def test_h_midpoint_window_is_rare_and_correct():
     (hc + 1) u S_h of a bf16 rounding midpoint: few of them, and each one is
     checked against the definition directly."""
     case, p, xb, fb, pm, ref = _case(n=8, d=1024, seed=3)
-    near, spacing = parity.h_midpoint_window(xb, pm)
+    near, spacing, window = parity.h_midpoint_window(xb, pm)
     assert near.mean() < 1e-3
     x = oracle.bf16_to_f64(xb)
     h = np.einsum("ts,tsd->td", pm, x)
@@ -61,6 +61,32 @@ def test_h_midpoint_window_is_rare_and_correct():
         mids.append(0.5 * (hi + oracle.bf16_to_f64(np.array([hi_b + 1], np.uint16))[0]))
         dist = min(abs(v - m) for m in mids)
         assert near[t, c] == (dist <= 5 * parity.U32 * S[t, c]), (t, c, dist, S[t, c])
+        assert window[t, c] == 5 * parity.U32 * S[t, c]
+
+
+def test_cancelled_h_keeps_the_fp32_window():
+    """Where h cancels to far below its terms (here h ~ 1e-7 from O(1) terms),
+    an fp32 sum may be off by many bf16 spacings of h; the allowance of such an
+    element covers the whole fp32 error window, so an h_norm computed from any
+    h inside that window passes."""
+    n, d = 1, 64
+    x = np.zeros((n, 4, d))
+    x[0, 0, :] = 1.0
+    x[0, 1, :] = -1.0
+    x[0, 2, 0::2] = 1.0      # odd columns cancel to -0.75 * 2^-22, even ones do not
+    xb = oracle.bf16_from_f64(x)
+    pm = np.array([[0.75, 0.75 * (1 + 2.0 ** -22), 1.0, 0.0]])
+    w = np.ones(d)
+    ref = oracle.rmsnorm(oracle.pre(xb, pm), w)
+    ha = parity.h_norm_allowance(xb, pm, w, ref)
+    near, spacing, window = parity.h_midpoint_window(xb, pm)
+    h = np.einsum("ts,tsd->td", pm, oracle.bf16_to_f64(xb))
+    # an h off by the full window, rounded and normalised as the kernel would
+    worst = oracle.rmsnorm(oracle.bf16_from_f64(h + window), w)
+    c = 1
+    assert abs(h[0, c]) < 2e-7
+    assert near[0, c] and window[0, c] > 10 * spacing[0, c]
+    parity.check_bf16("h_norm", worst[:, c:c + 1], ref[:, c:c + 1], abs_allow=ha[:, c:c + 1])
 
 
 def test_two_ulp_error_is_caught():
@@ -80,7 +106,7 @@ def test_two_ulp_h_norm_error_is_caught():
     case, p, xb, fb, pm, ref = _case()
     ha = parity.h_norm_allowance(xb, pm, p.norm_w.numpy(), ref["h_norm"])
     parity.check_bf16("h_norm", ref["h_norm"], ref["h_norm"], abs_allow=ha)
-    near, _ = parity.h_midpoint_window(xb, pm)
+    near, _, _ = parity.h_midpoint_window(xb, pm)
     h64 = np.abs(oracle.bf16_to_f64(ref["h_norm"]))
     cand = np.argwhere((h64 > 0.5) & ~near)
     assert len(cand) > 0
