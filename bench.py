@@ -106,13 +106,14 @@ def ncu_traffic_per_launch(n_tokens, path_kind="step"):
     None when the kernel's sources have changed since it was taken."""
     path = os.path.join(ROOT, "profiles", "hc_chain_side_traffic.json" if path_kind == "chain"
                         else "hc_block_step_traffic.json")
-    unit = "hc_chain.cu" if path_kind == "chain" else "hc_block_cluster.cu"
+    unit = "hc_slices.cu"  # both the chain and hc_block_step run its kernel
     try:
         with open(path) as fh:
             rec = json.load(fh)
+        digest = source_digest(unit)
     except Exception:
         return None
-    if rec.get("source_digest") != source_digest(unit):
+    if rec.get("source_digest") != digest:
         return None
     return int(rec["dram_bytes_per_token"] * n_tokens + rec.get("dram_bytes_fixed", 0))
 
@@ -238,7 +239,7 @@ def run_ours(args, rank, local_rank, world):
     stream = torch.cuda.current_stream(dev)
     launches = {"n": 0}
     chain = args.path == "chain"
-    states = [torch.empty((n, hcg.STATE_FLOATS), device=dev) for _ in range(2)] if chain else None
+    states = [hcg.chain_state(n, d, dev) for _ in range(2)] if chain else None
 
     def step_chain(events=None):
         # the sides fused across sides: each launch finishes side s and starts s + 1
@@ -513,7 +514,7 @@ def run_configs(dev, peak, stream):
     ys = [torch.empty_like(case.x), torch.empty_like(case.x)]
     hn = torch.empty((n, case.d), dtype=torch.bfloat16, device=dev)
     pres = [torch.empty_like(case.pre_mix), torch.empty_like(case.pre_mix)]
-    states = [torch.empty((n, hcg.STATE_FLOATS), device=dev) for _ in range(2)]
+    states = [hcg.chain_state(n, case.d, dev) for _ in range(2)]
     evs_step = []
 
     def steps(record):
@@ -597,7 +598,7 @@ def chain_equals_steps(case, fs, dev, stream):
     hcn = torch.empty_like(hs)
     ps = [torch.empty_like(case.pre_mix) for _ in range(2)]
     pc = [torch.empty_like(case.pre_mix) for _ in range(2)]
-    st = [torch.empty((n, hcg.STATE_FLOATS), device=dev) for _ in range(2)]
+    st = [hcg.chain_state(n, d, dev) for _ in range(2)]
     hcg.hc_chain_begin(case.x, case.pre_mix, P[0].hc_fn, P[0].hc_scale, P[0].hc_base, state_out=st[0],
                        pre_out=pc[0], stream=stream)
     xs, pms, xc = case.x, case.pre_mix, case.x
@@ -657,7 +658,7 @@ def run_e2e(args, dev, case, seed, world):
     h_norm = torch.empty((n, d), dtype=torch.bfloat16, device=dev)
     params = [p.astuple() for p in case.params]
     chain = args.path == "chain"
-    states = [torch.empty((n, hcg.STATE_FLOATS), device=dev) for _ in range(2)] if chain else None
+    states = [hcg.chain_state(n, d, dev) for _ in range(2)] if chain else None
     comp = torch.cuda.current_stream(dev)
     # Each host-to-device copy is split over several streams, so that several copy
     # engines share it; every chunk is one cudaMemcpyAsync.

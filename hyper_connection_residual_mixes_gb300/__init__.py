@@ -20,7 +20,8 @@ from . import _lib
 from ._lib import HcError
 
 __all__ = ["hc_mixes", "hc_split_sinkhorn", "hc_pre_norm", "hc_post", "hc_block_step",
-           "hc_chain_begin", "hc_chain_side", "hc_mxfp8_cast", "hc_pre_norm_mxfp8",
+           "hc_chain_begin", "hc_chain_side", "hc_chain_norm", "chain_state", "hc_mxfp8_cast",
+           "hc_pre_norm_mxfp8",
            "hc_block_step_backward", "hc_block_step_backward_no_workspace", "STATE_FLOATS",
            "HcError", "library_path", "version"]
 
@@ -313,10 +314,40 @@ def hc_block_step(x, pre_mix, f, hc_fn, hc_scale, hc_base, norm_w,
     return h_norm, y, pre_out
 
 
+def chain_state(n, d, device, hc=4):
+    """A state buffer of the chain for n tokens of width d: an fp32 tensor of
+    hc_chain_state_bytes / 128 rows of 32 floats.  Its first n rows are the
+    coefficient rows (state[:n]); the rows after them are the kernels' scratch."""
+    nbytes = _lib.load().hc_chain_state_bytes(n, hc, d)
+    if nbytes == 0:
+        raise ValueError("the chain does not serve n=%d, hc=%d, d=%d" % (n, hc, d))
+    return torch.empty(((nbytes + 127) // 128, STATE_FLOATS), dtype=torch.float32, device=device)
+
+
+def _state_or_new(state, name, n, d, hc, dev):
+    """The caller's state buffer (checked), a new one, or None where the chain
+    does not serve the shape (the library then refuses the call)."""
+    if state is not None:
+        return _state_arg(state, name, n, d, hc, dev)
+    return chain_state(n, d, dev, hc) if _lib.load().hc_chain_state_bytes(n, hc, d) else None
+
+
+def _state_arg(state, name, n, d, hc, dev):
+    _check(state, name, torch.float32, dev)
+    need = _lib.load().hc_chain_state_bytes(n, hc, d)
+    if state.dim() != 2 or state.shape[1] != STATE_FLOATS or state.numel() * 4 < need:
+        raise ValueError("%s must be a chain_state(n, d) buffer (%d bytes, rows of %d floats)"
+                         % (name, need, STATE_FLOATS))
+    return state
+
+
 def hc_chain_begin(x, pre_mix, hc_fn, hc_scale, hc_base, sinkhorn_iters=SINKHORN_ITERS,
-                   eps=HC_EPS, norm_eps=NORM_EPS, state_out=None, pre_out=None, stream=None):
+                   eps=HC_EPS, norm_eps=NORM_EPS, state_out=None, pre_out=None, h_pre_out=None,
+                   stream=None):
     """a1-a3 of the first side of a chain and its RMSNorm statistic.  Returns
-    the state [n, 32] of the first side (and fills pre_out [n, hc] if given)."""
+    the state buffer of the first side (chain_state; its first n rows are the
+    coefficient rows) and fills pre_out [n, hc] and h_pre_out [n, d] (the
+    side's bf16 h, for hc_chain_norm) when given."""
     _check(x, "x", torch.bfloat16)
     dev = x.device
     hc, d = x.shape[-2], x.shape[-1]
@@ -324,21 +355,27 @@ def hc_chain_begin(x, pre_mix, hc_fn, hc_scale, hc_base, sinkhorn_iters=SINKHORN
     n = x.numel() // (hc * d) if x.numel() else 0
     for t, nm in ((pre_mix, "pre_mix"), (hc_fn, "hc_fn"), (hc_scale, "hc_scale"), (hc_base, "hc_base")):
         _check(t, nm, torch.float32, dev)
-    state_out = _out(state_out, "state_out", lead + (STATE_FLOATS,), torch.float32, dev)
+    state_out = _state_or_new(state_out, "state_out", n, d, hc, dev)
     if pre_out is not None:
         pre_out = _out(pre_out, "pre_out", lead + (hc,), torch.float32, dev)
+    if h_pre_out is not None:
+        h_pre_out = _out(h_pre_out, "h_pre_out", lead + (d,), torch.bfloat16, dev)
     with torch.cuda.device(dev):
         _lib.call("hc_chain_begin", _ptr(x), _ptr(pre_mix), _ptr(hc_fn), _ptr(hc_scale), _ptr(hc_base),
-                  n, hc, d, sinkhorn_iters, eps, norm_eps, _ptr(state_out), _ptr(pre_out), _stream(stream))
+                  n, hc, d, sinkhorn_iters, eps, norm_eps, _ptr(state_out),
+                  state_out.numel() * 4 if state_out is not None else 0,
+                  _ptr(pre_out), _ptr(h_pre_out), _stream(stream))
     return state_out
 
 
 def hc_chain_side(x, f, state_in, norm_w, hc_fn_next=None, hc_scale_next=None, hc_base_next=None,
                   sinkhorn_iters=SINKHORN_ITERS, eps=HC_EPS, norm_eps=NORM_EPS, h_norm=None, y=None,
-                  state_out=None, pre_out=None, stream=None):
+                  state_out=None, pre_out=None, h_pre_out=None, write_h_norm=True, stream=None):
     """a4-a6 of side i from its state, fused with a1-a3 of side i + 1 on the y it
-    produces.  Returns (h_norm, y, state_out); state_out is None for the last
-    side (no next-side weights)."""
+    produces.  Returns (h_norm, y, state_out): h_norm is None when it is not
+    written (write_h_norm=False, or model order with h_pre_out given);
+    state_out is None for the last side (no next-side weights).  h_pre_out
+    [n, d] receives side i + 1's bf16 h (model order)."""
     _check(x, "x", torch.bfloat16)
     dev = x.device
     hc, d = x.shape[-2], x.shape[-1]
@@ -352,15 +389,53 @@ def hc_chain_side(x, f, state_in, norm_w, hc_fn_next=None, hc_scale_next=None, h
         for t, nm in ((hc_fn_next, "hc_fn_next"), (hc_scale_next, "hc_scale_next"),
                       (hc_base_next, "hc_base_next")):
             _check(t, nm, torch.float32, dev)
-        state_out = _out(state_out, "state_out", lead + (STATE_FLOATS,), torch.float32, dev)
+        state_out = _state_or_new(state_out, "state_out", n, d, hc, dev)
         if pre_out is not None:
             pre_out = _out(pre_out, "pre_out", lead + (hc,), torch.float32, dev)
+        if h_pre_out is not None:
+            h_pre_out = _out(h_pre_out, "h_pre_out", lead + (d,), torch.bfloat16, dev)
     else:
         state_out = pre_out = None
-    h_norm = _out(h_norm, "h_norm", lead + (d,), torch.bfloat16, dev)
+        if h_pre_out is not None:
+            raise ValueError("h_pre_out needs the next side's weights")
+    if h_pre_out is not None or not write_h_norm:
+        if h_norm is not None:
+            raise ValueError("h_norm is not written in model order (h_pre_out) or with write_h_norm=False")
+    else:
+        h_norm = _out(h_norm, "h_norm", lead + (d,), torch.bfloat16, dev)
     y = _out(y, "y", tuple(x.shape), torch.bfloat16, dev)
     with torch.cuda.device(dev):
         _lib.call("hc_chain_side", _ptr(x), _ptr(f), _ptr(state_in), _ptr(norm_w), _ptr(hc_fn_next),
                   _ptr(hc_scale_next), _ptr(hc_base_next), n, hc, d, sinkhorn_iters, eps, norm_eps,
-                  _ptr(h_norm), _ptr(y), _ptr(state_out), _ptr(pre_out), _stream(stream))
+                  _ptr(h_norm), _ptr(y), _ptr(state_out), state_out.numel() * 4 if state_out is not None else 0,
+                  _ptr(pre_out), _ptr(h_pre_out), _stream(stream))
     return h_norm, y, state_out
+
+
+def hc_chain_norm(h_pre, state, norm_w, h_norm=None, codes=None, scales=None, mxfp8=False,
+                  return_h_norm=True, stream=None):
+    """a5 of the chain in model order: h_norm = bf16((h * rs) * norm_w) from the
+    bf16 h a chain launch wrote and the statistic in its state.  Returns
+    h_norm, or with mxfp8 (or codes / scales given) (h_norm or None, codes,
+    scales) -- the MXFP8 cast of h_norm."""
+    _check(h_pre, "h_pre", torch.bfloat16)
+    dev = h_pre.device
+    d = h_pre.shape[-1]
+    lead = tuple(h_pre.shape[:-1])
+    n = h_pre.numel() // d if h_pre.numel() else 0
+    _check(state, "state", torch.float32, dev)
+    _check(norm_w, "norm_w", torch.float32, dev)
+    if state.dim() != 2 or state.shape[1] != STATE_FLOATS or state.shape[0] < n:
+        raise ValueError("state must hold the %d coefficient rows of the chain" % n)
+    cast = mxfp8 or codes is not None or scales is not None
+    if return_h_norm or h_norm is not None or not cast:
+        h_norm = _out(h_norm, "h_norm", lead + (d,), torch.bfloat16, dev)
+    if cast:
+        codes = _out(codes, "codes", lead + (d,), torch.uint8, dev)
+        scales = _out(scales, "scales", lead + (d // 32,), torch.uint8, dev)
+    with torch.cuda.device(dev):
+        _lib.call("hc_chain_norm", _ptr(h_pre), _ptr(state), _ptr(norm_w), n, d, _ptr(h_norm),
+                  _ptr(codes), _ptr(scales), _stream(stream))
+    if cast:
+        return h_norm, codes, scales
+    return h_norm

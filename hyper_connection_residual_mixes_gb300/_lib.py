@@ -41,8 +41,11 @@ SIGNATURES = {
     "hc_pre_norm_mxfp8": [P, P, P, I64, I32, I32, F32, P, P, P, P],
     "hc_post": [P, P, P, P, I64, I32, I32, P, P],
     "hc_block_step": [P, P, P, P, P, P, P, I64, I32, I32, I32, F32, F32, P, P, P, P, P, P],
-    "hc_chain_begin": [P, P, P, P, P, I64, I32, I32, I32, F32, F32, P, P, P],
-    "hc_chain_side": [P, P, P, P, P, P, P, I64, I32, I32, I32, F32, F32, P, P, P, P, P],
+    "hc_chain_state_bytes": [I64, I32, I32],
+    "hc_chain_begin": [P, P, P, P, P, I64, I32, I32, I32, F32, F32, P, ctypes.c_size_t, P, P, P],
+    "hc_chain_side": [P, P, P, P, P, P, P, I64, I32, I32, I32, F32, F32, P, P, P, ctypes.c_size_t,
+                      P, P, P],
+    "hc_chain_norm": [P, P, P, I64, I32, P, P, P, P],
 }
 
 STATUS = {
@@ -80,6 +83,7 @@ def load():
             fn.restype = I32
         lib.hc_status_string.restype = ctypes.c_char_p
         lib.hc_block_step_backward_workspace_bytes.restype = ctypes.c_size_t
+        lib.hc_chain_state_bytes.restype = ctypes.c_size_t
         _lib = lib
         return lib
 

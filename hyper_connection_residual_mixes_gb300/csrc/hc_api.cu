@@ -91,7 +91,7 @@ hc_status hc_consume_device_error(cudaStream_t stream) {
     unsigned int flag = 0, flag_chain = 0, flag_bwd = 0;
     hc_status st = cuda_status(hc::consume_device_error(stream, &flag));
     if (st != HC_OK) return st;
-    st = cuda_status(hc::consume_chain_device_error(stream, &flag_chain));
+    st = cuda_status(hc::consume_slices_device_error(stream, &flag_chain));
     if (st != HC_OK) return st;
     st = cuda_status(hc::consume_backward_device_error(stream, &flag_bwd));
     if (st != HC_OK) return st;
@@ -322,50 +322,62 @@ hc_status hc_block_step(const uint16_t *x, const float *pre_mix, const uint16_t 
                                                 pre_out, post_out, comb_out, nullptr, stream));
 }
 
+size_t hc_chain_state_bytes(int64_t n, int hc, int d) {
+    if (check_shape(n, hc, d, true) != HC_OK || hc != 4 || !hc::slices_supported(d)) return 0;
+    return hc::chain_state_bytes(n);
+}
+
 hc_status hc_chain_begin(const uint16_t *x, const float *pre_mix, const float *hc_fn,
                          const float *hc_scale, const float *hc_base, int64_t n, int hc, int d,
                          int sinkhorn_iters, float eps, float norm_eps, float *state_out,
-                         float *pre_out, cudaStream_t stream) {
+                         size_t state_bytes, float *pre_out, uint16_t *h_pre_out,
+                         cudaStream_t stream) {
     hc_status st = check_shape(n, hc, d, true);
     if (st != HC_OK) return st;
     if (sinkhorn_iters < 1 || !finite_nonneg(eps) || !finite_nonneg(norm_eps))
         return HC_ERR_INVALID_ARG;
-    if (hc != 4 || !hc::chain_supported(d)) return HC_ERR_UNSUPPORTED;
+    if (hc != 4 || !hc::slices_supported(d)) return HC_ERR_UNSUPPORTED;
     if (n == 0) return HC_OK;
     if (!x || !pre_mix || !hc_fn || !hc_scale || !hc_base || !state_out) return HC_ERR_INVALID_ARG;
+    if (state_bytes < hc::chain_state_bytes(n)) return HC_ERR_INVALID_ARG;
     const void *ptrs[] = {x, pre_mix, hc_fn, hc_scale, hc_base, state_out};
     for (const void *p : ptrs)
         if (!aligned16(p)) return HC_ERR_MISALIGNED;
-    if (pre_out && !aligned16(pre_out)) return HC_ERR_MISALIGNED;
+    if ((pre_out && !aligned16(pre_out)) || (h_pre_out && !aligned16(h_pre_out))) return HC_ERR_MISALIGNED;
     const int64_t mix = (int64_t)(2 + hc) * hc, K = (int64_t)hc * d;
     const Span ins[] = {span(x, n * K * 2), span(pre_mix, n * hc * 4), span(hc_fn, mix * K * 4),
                         span(hc_scale, 12), span(hc_base, mix * 4)};
-    const Span outs[] = {span(state_out, n * HC_STATE_FLOATS * 4), span(pre_out, pre_out ? n * hc * 4 : 0)};
-    if ((st = check_alias(outs, 2, ins, 5)) != HC_OK) return st;
-    return cuda_status(hc::launch_chain_begin(x, pre_mix, hc_fn, hc_scale, hc_base, n, d,
-                                              sinkhorn_iters, eps, norm_eps, state_out, pre_out,
-                                              stream));
+    const Span outs[] = {span(state_out, (int64_t)state_bytes), span(pre_out, pre_out ? n * hc * 4 : 0),
+                         span(h_pre_out, h_pre_out ? n * d * 2 : 0)};
+    if ((st = check_alias(outs, 3, ins, 5)) != HC_OK) return st;
+    return cuda_status(hc::launch_slices_begin(x, pre_mix, hc_fn, hc_scale, hc_base, n, d,
+                                               sinkhorn_iters, eps, norm_eps, state_out, pre_out,
+                                               h_pre_out, stream));
 }
 
 hc_status hc_chain_side(const uint16_t *x, const uint16_t *f, const float *state_in,
                         const float *norm_w, const float *hc_fn_next, const float *hc_scale_next,
                         const float *hc_base_next, int64_t n, int hc, int d, int sinkhorn_iters,
                         float eps, float norm_eps, uint16_t *h_norm, uint16_t *y,
-                        float *state_out, float *pre_out, cudaStream_t stream) {
+                        float *state_out, size_t state_bytes, float *pre_out, uint16_t *h_pre_out,
+                        cudaStream_t stream) {
     hc_status st = check_shape(n, hc, d, true);
     if (st != HC_OK) return st;
     if (sinkhorn_iters < 1 || !finite_nonneg(eps) || !finite_nonneg(norm_eps))
         return HC_ERR_INVALID_ARG;
-    if (hc != 4 || !hc::chain_supported(d)) return HC_ERR_UNSUPPORTED;
+    if (hc != 4 || !hc::slices_supported(d)) return HC_ERR_UNSUPPORTED;
     if (n == 0) return HC_OK;
     const bool next = hc_fn_next != nullptr;
-    if (!x || !f || !state_in || !norm_w || !h_norm || !y) return HC_ERR_INVALID_ARG;
+    if (!x || !f || !state_in || !norm_w || !y) return HC_ERR_INVALID_ARG;
     // the next side's weights come all together, with a state to write, or not at all
     if (next != (hc_scale_next != nullptr) || next != (hc_base_next != nullptr)) return HC_ERR_INVALID_ARG;
-    if (next && !state_out) return HC_ERR_INVALID_ARG;
-    const void *ptrs[] = {x, f, state_in, norm_w, h_norm, y};
+    if (next && (!state_out || state_bytes < hc::chain_state_bytes(n))) return HC_ERR_INVALID_ARG;
+    // the next side's bf16 h needs a next side; it and this side's h_norm are one or the other
+    if (h_pre_out && (!next || h_norm)) return HC_ERR_INVALID_ARG;
+    const void *ptrs[] = {x, f, state_in, norm_w, y};
     for (const void *p : ptrs)
         if (!aligned16(p)) return HC_ERR_MISALIGNED;
+    if ((h_norm && !aligned16(h_norm)) || (h_pre_out && !aligned16(h_pre_out))) return HC_ERR_MISALIGNED;
     if (next) {
         const void *nptrs[] = {hc_fn_next, hc_scale_next, hc_base_next, state_out};
         for (const void *p : nptrs)
@@ -380,14 +392,36 @@ hc_status hc_chain_side(const uint16_t *x, const uint16_t *f, const float *state
                         span(hc_fn_next, next ? mix * K * 4 : 0),
                         span(hc_scale_next, next ? 12 : 0),
                         span(hc_base_next, next ? mix * 4 : 0)};
-    const Span outs[] = {span(h_norm, n * d * 2), span(y, n * K * 2),
-                         span(state_out, next ? n * HC_STATE_FLOATS * 4 : 0),
-                         span(pre_out, (next && pre_out) ? n * hc * 4 : 0)};
-    if ((st = check_alias(outs, 4, ins, 7)) != HC_OK) return st;
-    return cuda_status(hc::launch_chain_side(x, f, state_in, norm_w, hc_fn_next, hc_scale_next,
-                                             hc_base_next, n, d, sinkhorn_iters, eps, norm_eps,
-                                             h_norm, y, next ? state_out : nullptr,
-                                             next ? pre_out : nullptr, stream));
+    const Span outs[] = {span(h_norm, h_norm ? n * d * 2 : 0), span(y, n * K * 2),
+                         span(state_out, next ? (int64_t)state_bytes : 0),
+                         span(pre_out, (next && pre_out) ? n * hc * 4 : 0),
+                         span(h_pre_out, h_pre_out ? n * d * 2 : 0)};
+    if ((st = check_alias(outs, 5, ins, 7)) != HC_OK) return st;
+    return cuda_status(hc::launch_slices_side(x, f, state_in, norm_w, hc_fn_next, hc_scale_next,
+                                              hc_base_next, n, d, sinkhorn_iters, eps, norm_eps,
+                                              h_norm, y, next ? state_out : nullptr,
+                                              next ? pre_out : nullptr, h_pre_out, stream));
+}
+
+hc_status hc_chain_norm(const uint16_t *h_pre, const float *state, const float *norm_w, int64_t n,
+                        int d, uint16_t *h_norm, uint8_t *codes, uint8_t *scales,
+                        cudaStream_t stream) {
+    if (n < 0 || d <= 0) return HC_ERR_INVALID_ARG;
+    if (d % 64 != 0 || d > kMaxD) return HC_ERR_UNSUPPORTED;
+    if (n > (INT64_MAX / 8) / d) return HC_ERR_INVALID_ARG;
+    if (n == 0) return HC_OK;
+    if (!h_pre || !state || !norm_w) return HC_ERR_INVALID_ARG;
+    if ((codes == nullptr) != (scales == nullptr) || (!h_norm && !codes)) return HC_ERR_INVALID_ARG;
+    const void *ptrs[] = {h_pre, state, norm_w};
+    for (const void *p : ptrs)
+        if (!aligned16(p)) return HC_ERR_MISALIGNED;
+    if ((h_norm && !aligned16(h_norm)) || (codes && !aligned16(codes))) return HC_ERR_MISALIGNED;
+    const Span ins[] = {span(h_pre, n * d * 2), span(state, n * HC_STATE_FLOATS * 4), span(norm_w, d * 4)};
+    const Span outs[] = {span(h_norm, h_norm ? n * d * 2 : 0), span(codes, codes ? n * d : 0),
+                         span(scales, scales ? n * (d / 32) : 0)};
+    hc_status st = check_alias(outs, 3, ins, 3);
+    if (st != HC_OK) return st;
+    return cuda_status(hc::launch_chain_norm(h_pre, state, norm_w, n, d, h_norm, codes, scales, stream));
 }
 
 }  // extern "C"

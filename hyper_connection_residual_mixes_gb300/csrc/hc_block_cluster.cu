@@ -574,13 +574,6 @@ k_block_cluster(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
 #pragma unroll
                         for (int s = 0; s < kHC; ++s)
                             xr[it][s] = *reinterpret_cast<const uint4 *>(sb + s * kBoxBytes + swz(r, uu + 4 * it));
-                    // The loads above are still in flight: nothing has used their values
-                    // yet, and an mbarrier arrive alone does not wait for them (measured:
-                    // the ring refilled the slot under the later loads of a warp that went
-                    // on to wait).  A CTA-scope fence completes them first.
-                    __threadfence_block();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(empty_bar(slot));
                     if (kFull && cb == 0) {
                         // pre_mix of this thread's token (copied in with this slot)
                         const float4 v = live ? sPm[(bu.j % kPmBufs) * kT + r] : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -607,6 +600,13 @@ k_block_cluster(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                             }
                         }
                     }
+                    // The slot goes once every value loaded from it has been used.  A
+                    // release right after the loads, behind a CTA-scope fence, still let
+                    // the ring refill the slot under a warp's loads (measured on the
+                    // kernel of hc_slices.cu, whose phase 1 is this code).
+                    __threadfence_block();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(empty_bar(slot));
                 }
                 if (!ok) break;
                 // tile finished: this CTA's sums of squares of the token go to the sender
@@ -639,9 +639,6 @@ k_block_cluster(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                             xr[it][s] = *reinterpret_cast<const uint4 *>(sb + s * kBoxBytes + swz(r, uu + 4 * it));
                         fr[it] = *reinterpret_cast<const uint4 *>(sb + kStageXBytes + swz(r, uu + 4 * it));
                     }
-                    __threadfence_block();  // (see phase 1)
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(empty_bar(slot));
                     if (cb == 0) {
                         const float4 v = live ? sPm[(bu.j % kPmBufs) * kT + r] : make_float4(0.f, 0.f, 0.f, 0.f);
                         pm[0] = f2_dup(v.x); pm[1] = f2_dup(v.y); pm[2] = f2_dup(v.z); pm[3] = f2_dup(v.w);
@@ -698,6 +695,10 @@ k_block_cluster(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                             st_global_v4_hint(p.h_norm + tok * d + cbase, ho[0], ho[1], ho[2], ho[3], pol_out);
                         }
                     }
+                    // the slot goes once the values loaded from it have been used (see phase 1)
+                    __threadfence_block();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(empty_bar(slot));
                 }
             }
         }

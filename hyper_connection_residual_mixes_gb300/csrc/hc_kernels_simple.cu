@@ -227,6 +227,57 @@ cudaError_t launch_mxfp8_cast(const uint16_t *in, int64_t rows, int d, uint8_t *
     return cudaGetLastError();
 }
 
+// a5 for the chain in model order: the chain's launch for side i wrote side
+// i + 1's bf16 h (hc_pre of y_i with side i's pre) and the RMSNorm statistic of
+// that h into the coefficient rows; here h_norm = bf16((h * rs) * w), the
+// products of the fused kernels, with rs read from the rows (index 20), and
+// optionally its MXFP8 codes and scales (the cast above).  chunks = n * d / 8.
+__global__ void __launch_bounds__(kCastThreads)
+k_chain_norm(const uint16_t *__restrict__ h_pre, const float *__restrict__ state,
+             const float *__restrict__ norm_w, int d8, int64_t chunks, uint16_t *__restrict__ out,
+             uint8_t *__restrict__ codes, uint8_t *__restrict__ scales) {
+    const uint4 *in8 = reinterpret_cast<const uint4 *>(h_pre);
+    const float4 *w4 = reinterpret_cast<const float4 *>(norm_w);
+    for (int64_t base = (int64_t)blockIdx.x * kCastThreads; base < chunks;
+         base += (int64_t)gridDim.x * kCastThreads) {
+        const int64_t c = base + threadIdx.x;
+        const bool live = c < chunks;
+        float h[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        if (live) {
+            const int64_t t = c / d8;
+            const int cc = (int)(c - t * d8);
+            const float rs = __ldg(state + t * 32 + 20);
+            unpack8(__ldg(in8 + c), h);
+            const float4 wa = __ldg(w4 + 2 * cc), wb = __ldg(w4 + 2 * cc + 1);
+            const float wv[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) h[i] = (h[i] * rs) * wv[i];
+        }
+        const uint4 hb = pack8(h);
+        if (live && out) reinterpret_cast<uint4 *>(out)[c] = hb;
+        if (codes) {  // uniform across the grid: the group shuffles see full warps
+            float hn[8];
+            unpack8(hb, hn);
+            const int ex = mx_group_exp(hn);
+            if (live) {
+                reinterpret_cast<uint2 *>(codes)[c] = mx_codes8(hn, ex);
+                if ((c & 3) == 0) scales[c >> 2] = (uint8_t)(ex + 127);
+            }
+        }
+    }
+}
+
+cudaError_t launch_chain_norm(const uint16_t *h_pre, const float *state, const float *norm_w,
+                              int64_t n, int d, uint16_t *out, uint8_t *codes, uint8_t *scales,
+                              cudaStream_t s) {
+    const int64_t chunks = n * (int64_t)(d / 8);
+    int64_t blocks = (chunks + kCastThreads - 1) / kCastThreads;
+    if (blocks > 152 * 16) blocks = 152 * 16;
+    k_chain_norm<<<(unsigned)blocks, kCastThreads, 0, s>>>(h_pre, state, norm_w, d / 8, chunks, out,
+                                                           codes, scales);
+    return cudaGetLastError();
+}
+
 // a4-a5 and the cast in one pass: h_norm as k_pre_norm computes it, then its
 // MXFP8 codes and scales; the bf16 h_norm is written too when out is given.
 template <int HC>

@@ -57,26 +57,38 @@ cudaError_t launch_block_cluster(const uint16_t *x, const float *pre_mix, const 
                                  float *post_out, float *comb_out, float *mixes_out,
                                  cudaStream_t s);
 
-// The chain of side steps fused across sides (hc_chain.cu); same support as
-// the cluster path.
-bool chain_supported(int d);
+// The chain kernel (hc_slices.cu): supported when d is a multiple of 1024 and
+// one stream's weight fragments fit a tensor-memory quadrant (d <= 7168).
+bool slices_supported(int d);
 
-cudaError_t launch_chain_begin(const uint16_t *x, const float *pre_mix, const float *hc_fn,
-                               const float *hc_scale, const float *hc_base, int64_t n, int d,
-                               int iters, float eps, float norm_eps, float *state_out,
-                               float *pre_out, cudaStream_t s);
+// The chain of side steps fused across sides (hc_slices.cu).  A state buffer
+// holds the [n, 32] coefficient rows, then the kernel's scratch.
+size_t chain_state_bytes(int64_t n);
 
-// hc_fn_next == nullptr: the last side (no phase 1 of a next side).
-cudaError_t launch_chain_side(const uint16_t *x, const uint16_t *f, const float *state_in,
-                              const float *norm_w, const float *hc_fn_next,
-                              const float *hc_scale_next, const float *hc_base_next, int64_t n,
-                              int d, int iters, float eps, float norm_eps, uint16_t *h_norm,
-                              uint16_t *y, float *state_out, float *pre_out, cudaStream_t s);
+cudaError_t launch_slices_begin(const uint16_t *x, const float *pre_mix, const float *hc_fn,
+                                const float *hc_scale, const float *hc_base, int64_t n, int d,
+                                int iters, float eps, float norm_eps, float *state_out,
+                                float *pre_out, uint16_t *h_pre_out, cudaStream_t s);
+
+// hc_fn_next == nullptr: the last side (no phase 1 of a next side).  At most one
+// of h_norm (this side's) and h_pre_out (the next side's bf16 h) is given.
+cudaError_t launch_slices_side(const uint16_t *x, const uint16_t *f, const float *state_in,
+                               const float *norm_w, const float *hc_fn_next,
+                               const float *hc_scale_next, const float *hc_base_next, int64_t n,
+                               int d, int iters, float eps, float norm_eps, uint16_t *h_norm,
+                               uint16_t *y, float *state_out, float *pre_out, uint16_t *h_pre_out,
+                               cudaStream_t s);
+
+// a5 of the chain in model order: h_norm (and / or its MXFP8 cast) from the
+// bf16 h and the statistic in the coefficient rows (hc_kernels_simple.cu).
+cudaError_t launch_chain_norm(const uint16_t *h_pre, const float *state, const float *norm_w,
+                              int64_t n, int d, uint16_t *out, uint8_t *codes, uint8_t *scales,
+                              cudaStream_t s);
 
 // Synchronise `s`, then read and clear the device flag that bounded waits set
-// when they time out (each of the two kernel files keeps its own flag).
+// when they time out (each kernel file keeps its own flag).
 cudaError_t consume_device_error(cudaStream_t s, unsigned int *flag);
-cudaError_t consume_chain_device_error(cudaStream_t s, unsigned int *flag);
+cudaError_t consume_slices_device_error(cudaStream_t s, unsigned int *flag);
 cudaError_t consume_backward_device_error(cudaStream_t s, unsigned int *flag);
 // one warp waits on a barrier nothing arrives on (the bounded-wait self-test)
 cudaError_t launch_selftest_wait(cudaStream_t s);

@@ -95,6 +95,40 @@ __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, vo
     return __all_sync(0xffffffffu, ok) != 0;
 }
 
+// ---------------------------------------------------------------- flags in global memory
+// 64-bit flag words written by one CTA and polled by others in the same launch.
+// The writer makes its earlier global writes visible (each writing lane runs
+// __threadfence()) and then stores the flag with release semantics; a reader
+// that sees the flag with acquire semantics sees those writes.
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long *p) {
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_u64(unsigned long long *p, unsigned long long v) {
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+// Bounded wait until *p == v (the same limits as mbar_wait).
+__device__ __forceinline__ bool flag_wait(const unsigned long long *p, unsigned long long v,
+                                          volatile int *abort) {
+    for (uint32_t i = 0; i < 256u; ++i)
+        if (ld_acquire_u64(p) == v) return true;
+    for (uint32_t i = 0; i < (1u << 23); ++i) {
+        if (ld_acquire_u64(p) == v) return true;
+        if (*abort) return false;
+        __nanosleep(256);
+    }
+    *abort = 1;
+    atomicOr(&g_device_error, kErrWaitTimeout);
+    return false;
+}
+// Order this thread's earlier generic-proxy accesses of global memory (an
+// acquire of a flag) before its later async-proxy accesses (a TMA load or
+// store of the data the flag guards).
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- cluster
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;

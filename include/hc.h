@@ -39,8 +39,9 @@
  *  - Compiled stream counts: hc = 2, 4 or 8 (the pages' kernel takes any
  *    hc_mult; the released model uses 4), with d a positive multiple of 64,
  *    d <= 16384; anything else returns HC_ERR_UNSUPPORTED.  The tensor-core
- *    cluster path of hc_mixes / hc_block_step and the chain (hc_chain_*)
- *    serve hc = 4; the other counts run on the whole-token kernels.  The
+ *    paths of hc_mixes / hc_block_step and the chain (hc_chain_*) serve
+ *    hc = 4 with d a multiple of 1024 up to 7168; other shapes run on the
+ *    whole-token kernels (the chain refuses them).  The
  *    backward serves all three (tensor-core kernels at hc = 4, plain
  *    per-token kernels at 2 and 8); its no-workspace entry serves hc = 4.
  *  - Output ranges must not overlap input ranges or each other
@@ -254,46 +255,84 @@ hc_status hc_pre_norm_mxfp8(const uint16_t *x, const float *pre_mix, const float
  * Block.forward: the streams a side reads are the y the previous side wrote,
  * and each side reads its sublayer input with the previous side's pre).  The
  * results equal, bit for bit, those of calling hc_block_step side after side;
- * each launch reads its side's streams from HBM once.
+ * each launch reads its side's streams from HBM once.  Supported when d is a
+ * multiple of 1024 and d <= 7168, with hc = 4 (HC_ERR_UNSUPPORTED otherwise).
  *
- * State rows.  A state buffer holds, per token, HC_STATE_FLOATS = 32 fp32:
+ * State buffers.  A state buffer is hc_chain_state_bytes(n, hc, d) bytes of
+ * device memory owned by the caller (16-byte aligned).  It starts with the
+ * coefficient rows, HC_STATE_FLOATS = 32 fp32 per token:
  *   [0:4] post, [4:20] comb (row-major j*hc+k), [20] RMSNorm scale
  *   rsqrt(mean(h^2) + norm_eps), [21:24] zero, [24:28] pre (the side's pre:
- *   the next side's pre_mix), [28:32] pre_mix (the one the side reads with).
- * The caller allocates it ([n, 32] fp32, 16-byte aligned) and keeps two of
- * them in rotation: side i reads the state of side i and writes that of side
- * i + 1 (the two may not overlap: HC_ERR_ALIAS).  Supported when d is a
- * multiple of 1024 and d <= 7168, with hc = 4 (HC_ERR_UNSUPPORTED otherwise).
+ *   the next side's pre_mix), [28:32] pre_mix (the one the side reads with);
+ * the rest is the kernels' scratch for one launch (partial sums of the
+ * cross-slice reductions and their arrival flags; nothing in it needs
+ * clearing).  The caller keeps two buffers in rotation: side i reads the rows
+ * of side i and writes the buffer of side i + 1 (the two may not overlap:
+ * HC_ERR_ALIAS).  No cited passage has a counterpart for the state: it
+ * carries one side's coefficients to the next launch.
+ *
+ * Two orders of work are served:
+ *  - given the sublayer outputs f up front (the benchmark form): every
+ *    hc_chain_side launch writes side i's h_norm and y;
+ *  - model order (f_i = sublayer(h_norm_i)): hc_chain_side writes side i's y
+ *    and side i + 1's bf16 h (h_pre_out, hc_pre of that y with side i's pre)
+ *    with its RMSNorm statistic in the next state; hc_chain_norm then turns
+ *    that h into h_norm_{i+1} (and / or its MXFP8 cast) for the sublayer, whose
+ *    output is the next launch's f.  hc_chain_begin writes the first side's h
+ *    the same way.  Every h_norm equals hc_block_step's bit for bit.
  *
  * hc_chain_begin: a1-a3 of the first side and its RMSNorm statistic.
  *   x [n, hc, d] bf16, pre_mix [n, hc] fp32, hc_fn, hc_scale, hc_base of the
  *   first side                                                       in
- *   state_out [n, 32] fp32   out: state of the first side
+ *   state_out, state_bytes   out: state buffer of the first side
  *   pre_out [n, hc] fp32     out, optional (NULL: not written): its pre
+ *   h_pre_out [n, d] bf16    out, optional: its bf16 h = hc_pre(x, pre_mix)
  *
  * hc_chain_side: a4-a6 of side i from its state, fused with a1-a3 of side
  * i + 1 on the y it produces.
- *   x [n, hc, d] bf16 (side i's streams), f [n, d] bf16, state_in [n, 32]
- *   (side i), norm_w [d] (side i), hc_fn_next, hc_scale_next, hc_base_next
- *   (side i + 1; all three NULL for the last side)                    in
- *   h_norm [n, d] bf16, y [n, hc, d] bf16   out: as hc_block_step's
- *   state_out [n, 32] fp32   out: state of side i + 1 (unused for the last side)
+ *   x [n, hc, d] bf16 (side i's streams), f [n, d] bf16, state_in (side i's
+ *   state buffer; its first n rows are read), norm_w [d] (side i),
+ *   hc_fn_next, hc_scale_next, hc_base_next (side i + 1; all three NULL for
+ *   the last side)                                                    in
+ *   y [n, hc, d] bf16        out: as hc_block_step's
+ *   h_norm [n, d] bf16       out, optional: side i's, as hc_block_step's
+ *   state_out, state_bytes   out: state buffer of side i + 1 (unused for the last side)
  *   pre_out [n, hc] fp32     out, optional: side i + 1's pre
- * No cited passage has a counterpart for the state rows: they carry one side's
- * coefficients to the next launch.
+ *   h_pre_out [n, d] bf16    out, optional: side i + 1's bf16 h; needs the
+ *   next side's weights and excludes h_norm (HC_ERR_INVALID_ARG)
+ *
+ * hc_chain_norm: a5 in model order.  h_norm = bf16((h * rs) * norm_w) with
+ * rs the RMSNorm scale in the state's rows (what hc_block_step computes).
+ *   h_pre [n, d] bf16, state (n rows), norm_w [d] fp32                 in
+ *   h_norm [n, d] bf16, optional                                       out
+ *   codes [n, d], scales [n, d/32] uint8, optional pair: the MXFP8 cast of
+ *   h_norm as hc_mxfp8_cast computes it                                out
+ *   At least one of h_norm and codes; d a multiple of 64.
+ *
+ * Launch notes.  The chain kernels run one CTA on each of 16 * floor(SMs / 16)
+ * SMs as a cooperative launch: they need that many SMs free to start, and a
+ * CTA waits (bounded) on flags other CTAs write into the state buffer.
  */
 #define HC_STATE_FLOATS 32
+
+size_t hc_chain_state_bytes(int64_t n, int hc, int d);
 
 hc_status hc_chain_begin(const uint16_t *x, const float *pre_mix, const float *hc_fn,
                          const float *hc_scale, const float *hc_base, int64_t n, int hc, int d,
                          int sinkhorn_iters, float eps, float norm_eps, float *state_out,
-                         float *pre_out, cudaStream_t stream);
+                         size_t state_bytes, float *pre_out, uint16_t *h_pre_out,
+                         cudaStream_t stream);
 
 hc_status hc_chain_side(const uint16_t *x, const uint16_t *f, const float *state_in,
                         const float *norm_w, const float *hc_fn_next, const float *hc_scale_next,
                         const float *hc_base_next, int64_t n, int hc, int d, int sinkhorn_iters,
                         float eps, float norm_eps, uint16_t *h_norm, uint16_t *y,
-                        float *state_out, float *pre_out, cudaStream_t stream);
+                        float *state_out, size_t state_bytes, float *pre_out, uint16_t *h_pre_out,
+                        cudaStream_t stream);
+
+hc_status hc_chain_norm(const uint16_t *h_pre, const float *state, const float *norm_w, int64_t n,
+                        int d, uint16_t *h_norm, uint8_t *codes, uint8_t *scales,
+                        cudaStream_t stream);
 
 #ifdef __cplusplus
 }

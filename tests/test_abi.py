@@ -126,37 +126,52 @@ def test_pre_norm_and_post_validation(lib):
                     FAKE2 * 0x300 + 8, None) == 3
 
 
+def _state_bytes(n=16, d=5120):
+    return _lib.load().hc_chain_state_bytes(n, 4, d)
+
+
 def _side(**kw):
     a = dict(x=FAKE, f=FAKE + 0x100000, state_in=FAKE + 0x200000, norm_w=FAKE + 0x300000,
              fn=FAKE + 0x400000, scale=FAKE + 0x500000, base=FAKE + 0x600000, n=16, hc=4, d=5120,
              iters=20, eps=1e-6, norm_eps=1e-20, h_norm=FAKE2 * 0x100, y=FAKE2 * 0x200,
-             state_out=FAKE2 * 0x300, pre_out=None, stream=None)
+             state_out=FAKE2 * 0x300, state_bytes=None, pre_out=None, h_pre_out=None, stream=None)
     a.update(kw)
+    if a["state_bytes"] is None:
+        a["state_bytes"] = _state_bytes(max(a["n"], 0), a["d"])
     return _lib.raw("hc_chain_side", a["x"], a["f"], a["state_in"], a["norm_w"], a["fn"], a["scale"],
                     a["base"], a["n"], a["hc"], a["d"], a["iters"], a["eps"], a["norm_eps"], a["h_norm"],
-                    a["y"], a["state_out"], a["pre_out"], a["stream"])
+                    a["y"], a["state_out"], a["state_bytes"], a["pre_out"], a["h_pre_out"], a["stream"])
 
 
 def _begin(**kw):
     a = dict(x=FAKE, pre_mix=FAKE + 0x100000, fn=FAKE + 0x200000, scale=FAKE + 0x300000,
              base=FAKE + 0x400000, n=16, hc=4, d=5120, iters=20, eps=1e-6, norm_eps=1e-20,
-             state_out=FAKE2 * 0x100, pre_out=None, stream=None)
+             state_out=FAKE2 * 0x100, state_bytes=None, pre_out=None, h_pre_out=None, stream=None)
     a.update(kw)
+    if a["state_bytes"] is None:
+        a["state_bytes"] = _state_bytes(max(a["n"], 0), a["d"])
     return _lib.raw("hc_chain_begin", a["x"], a["pre_mix"], a["fn"], a["scale"], a["base"], a["n"],
-                    a["hc"], a["d"], a["iters"], a["eps"], a["norm_eps"], a["state_out"], a["pre_out"],
-                    a["stream"])
+                    a["hc"], a["d"], a["iters"], a["eps"], a["norm_eps"], a["state_out"], a["state_bytes"],
+                    a["pre_out"], a["h_pre_out"], a["stream"])
 
 
+# Every case below fails validation (or has n == 0), so nothing is launched even
+# on a machine with a GPU: the pointers are not real allocations.
 @pytest.mark.parametrize("kw,expect", [
     (dict(scale=None), 1),                 # next-side weights come all together or not at all
     (dict(base=None), 1),
     (dict(state_out=None), 1),             # a next side needs a state to write
+    (dict(state_bytes=64), 1),             # ... of hc_chain_state_bytes bytes
+    (dict(h_pre_out=FAKE2 * 0x400), 1),    # the next side's h excludes this side's h_norm
+    (dict(h_norm=None, h_pre_out=FAKE2 * 0x400 + 8), 3),
+    (dict(h_norm=None, h_pre_out=FAKE + 0x10), 4),   # it overlaps x
     (dict(d=320), 2),                      # the chain needs d a multiple of 1024 ...
     (dict(d=8192), 2),                     # ... and d <= 7168
     (dict(hc=3), 2),
     (dict(state_in=FAKE + 0x200008), 3),
     (dict(y=FAKE + 64), 4),                # y overlaps x
     (dict(state_out=FAKE + 0x200010), 4),  # state_out overlaps state_in
+    (dict(y=None), 1),
     (dict(n=-1), 1),
 ])
 def test_chain_side_validation(lib, kw, expect):
@@ -167,13 +182,29 @@ def test_chain_side_last_needs_no_state_and_empty_is_ok(lib):
     # the last side: no next weights, no state to write (still validated, then empty)
     assert _side(n=0, fn=None, scale=None, base=None, state_out=None) == 0
     assert _side(n=0) == 0
+    # the last side has no next side whose h it could write
+    assert _side(fn=None, scale=None, base=None, state_out=None, h_norm=None, h_pre_out=FAKE2 * 0x400) == 1
+
+
+def test_chain_state_bytes(lib):
+    """Coefficient rows (128 bytes per token, rounded up to 256), then 16 x 28
+    fp32 partial sums per token, then 16 eight-byte flags per 64-token tile."""
+    for n in (1, 64, 65, 1000, 65536):
+        tiles = -(-n // 64)
+        assert lib.hc_chain_state_bytes(n, 4, 5120) == ((128 * n + 255) // 256) * 256 + 1792 * n + 128 * tiles
+    assert lib.hc_chain_state_bytes(16, 4, 320) == 0      # not served by the chain
+    assert lib.hc_chain_state_bytes(16, 2, 5120) == 0
+    assert lib.hc_chain_state_bytes(-1, 4, 5120) == 0
 
 
 @pytest.mark.parametrize("kw,expect", [
     (dict(d=2048 + 64), 2),
     (dict(state_out=None), 1),
+    (dict(state_bytes=1024), 1),
     (dict(state_out=FAKE2 * 0x100 + 4), 3),
     (dict(state_out=FAKE + 0x100), 4),     # state_out overlaps x
+    (dict(h_pre_out=FAKE + 0x100), 4),     # h_pre_out overlaps x
+    (dict(h_pre_out=FAKE2 * 0x200 + 2), 3),
     (dict(iters=0), 1),
 ])
 def test_chain_begin_validation(lib, kw, expect):
@@ -281,3 +312,27 @@ def test_block_step_backward_workspace_size(lib):
     assert f(16, 3, 5120) == 0 and f(16, 4, 100) == 0
     assert f(16, 2, 5120) > 0 and f(16, 8, 5120) > f(16, 4, 5120)
     assert _bwd(n=0) == 0 and _bwd(n=0, hc=2) == 0 and _bwd(n=0, hc=8) == 0
+
+
+def _norm(**kw):
+    a = dict(h_pre=FAKE, state=FAKE + 0x100000, norm_w=FAKE + 0x200000, n=16, d=5120,
+             h_norm=FAKE2 * 0x100, codes=None, scales=None, stream=None)
+    a.update(kw)
+    return _lib.raw("hc_chain_norm", a["h_pre"], a["state"], a["norm_w"], a["n"], a["d"], a["h_norm"],
+                    a["codes"], a["scales"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(h_norm=None), 1),                        # nothing to write
+    (dict(codes=FAKE2 * 0x200), 1),                # codes and scales come together
+    (dict(scales=FAKE2 * 0x300), 1),
+    (dict(d=100), 2),
+    (dict(n=-1), 1),
+    (dict(h_pre=None), 1),
+    (dict(state=FAKE + 0x100004), 3),
+    (dict(h_norm=FAKE + 0x100), 4),                # h_norm overlaps h_pre
+    (dict(codes=FAKE2 * 0x200, scales=FAKE + 0x200010), 4),  # scales overlap norm_w
+    (dict(n=0), 0),
+])
+def test_chain_norm_validation(lib, kw, expect):
+    assert _norm(**kw) == expect

@@ -40,13 +40,15 @@ def test_digest_follows_local_includes_only(tmp_path, monkeypatch):
 def test_traffic_used_only_while_the_digest_matches(tmp_path, monkeypatch):
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     csrc = _tree(tmp_path)
-    (csrc / "hc_chain.cu").write_text('#include "h1.h"\nint chain;\n')
+    (csrc / "hc_slices.cu").write_text('#include "h1.h"\nint chain;\n')
     (tmp_path / "profiles").mkdir()
-    rec = {"source_digest": bench.source_digest("hc_chain.cu"), "dram_bytes_per_token": 100.5,
+    rec = {"source_digest": bench.source_digest("hc_slices.cu"), "dram_bytes_per_token": 100.5,
            "dram_bytes_fixed": 7}
     (tmp_path / "profiles" / "hc_chain_side_traffic.json").write_text(json.dumps(rec))
     assert bench.ncu_traffic_per_launch(1000, "chain") == int(100.5 * 1000 + 7)
     (csrc / "h1.h").write_text('#include "h2.cuh"\nint edited;\n')
     assert bench.ncu_traffic_per_launch(1000, "chain") is None
     assert bench.ncu_traffic_per_launch(1000, "step") is None  # no record for the step kernel here
+    (csrc / "hc_slices.cu").unlink()
+    assert bench.ncu_traffic_per_launch(1000, "chain") is None  # no source: no figure
 

@@ -171,3 +171,91 @@ def test_chain_equals_block_steps_80_sides_8192_tokens():
     torch.cuda.synchronize()
     _compare(ref, got)
     assert _lib.raw("hc_consume_device_error", None) == 0
+
+
+def _chain_model(x, pm, fs, params, sublayer=None, mxfp8=None):
+    """The chain in model order: the first launch writes side 0's bf16 h; each
+    side's h_norm comes from hc_chain_norm before the side's launch; launch i
+    writes y_i and side i + 1's bf16 h.  f_i = sublayer(h_norm_i) when a
+    sublayer is given (else fs[i]).  Returns per side (h_norm, y, pre, f)."""
+    S = len(params)
+    n, d = x.shape[0], x.shape[-1]
+    p0 = params[0]
+    hp = torch.empty((n, d), dtype=torch.bfloat16, device=x.device)
+    pre0 = torch.empty_like(pm)
+    state = hcg.hc_chain_begin(x, pm, p0.hc_fn, p0.hc_scale, p0.hc_base, pre_out=pre0, h_pre_out=hp)
+    pres = [pre0]
+    out = []
+    for i in range(S):
+        p = params[i]
+        if mxfp8 is not None:
+            h, codes, scales = hcg.hc_chain_norm(hp, state, p.norm_w, mxfp8=True)
+            mxfp8.append((h, codes, scales))
+        else:
+            h = hcg.hc_chain_norm(hp, state, p.norm_w)
+        f = sublayer(h) if sublayer is not None else fs[i]
+        if i + 1 < S:
+            q = params[i + 1]
+            hp = torch.empty_like(hp)
+            pre_next = torch.empty_like(pm)
+            _, y, st_next = hcg.hc_chain_side(x, f, state, p.norm_w, q.hc_fn, q.hc_scale, q.hc_base,
+                                              pre_out=pre_next, h_pre_out=hp)
+            pres.append(pre_next)
+        else:
+            _, y, st_next = hcg.hc_chain_side(x, f, state, p.norm_w, write_h_norm=False)
+        out.append((h, y, pres[i], f, state))
+        x, state = y, st_next
+    return out
+
+
+@pytest.mark.parametrize("n,d,sides", [(128, 5120, 2), (8192, 5120, 4), (1361, 1024, 3), (530, 7168, 3)])
+def test_chain_model_order_equals_block_steps(n, d, sides):
+    """Model order with the sublayer outputs given: every side's h_norm (from
+    hc_chain_norm), y and pre equal hc_block_step's bit for bit."""
+    g = torch.Generator().manual_seed(900 + n + d)
+    x = inputs.streams(g, n, 4, d).to(DEV)
+    pm = inputs.pre_mix(g, n).to(DEV)
+    params = [inputs.side_params(g, d=d).to(DEV) for _ in range(sides)]
+    fs = [inputs.sublayer_out(g, n, d).to(DEV) for _ in range(sides)]
+    ref = _steps(x, pm, fs, params)
+    casts = []
+    got = _chain_model(x, pm, fs, params, mxfp8=casts)
+    torch.cuda.synchronize()
+    _compare(ref, [o[:3] for o in got])
+    # the cast in the same pass equals the standalone cast of the same h_norm
+    for i, (h, codes, scales) in enumerate(casts):
+        c2, s2 = hcg.hc_mxfp8_cast(ref[i][0])
+        _same("side %d codes" % i, codes, c2)
+        _same("side %d scales" % i, scales, s2)
+    assert _lib.raw("hc_consume_device_error", None) == 0
+
+
+def test_chain_model_order_with_a_sublayer_against_oracle():
+    """A stand-in sublayer that depends on its input (f = bf16(2 tanh(h_norm)),
+    torch on the GPU): the chain in model order, checked side by side against
+    the oracle fed the same x, pre_mix and f."""
+    n, d, sides = 300, 2048, 4
+    g = torch.Generator().manual_seed(77)
+    x = inputs.streams(g, n, 4, d).to(DEV)
+    pm = inputs.pre_mix(g, n).to(DEV)
+    params = [inputs.side_params(g, d=d).to(DEV) for _ in range(sides)]
+    sub = lambda h: (2.0 * torch.tanh(h.float())).to(torch.bfloat16)
+    got = _chain_model(x, pm, None, params, sublayer=sub)
+    torch.cuda.synchronize()
+    xs, pms = x, pm
+    for i, (h, y, pre, f, st) in enumerate(got):
+        p = params[i].to("cpu")
+        rows = st[:n].cpu()
+        post_g, comb_g = rows[:, 0:4], rows[:, 4:20].reshape(-1, 4, 4)
+        xb, fb = bits(xs.cpu()), bits(f.cpu())
+        pmn = pms.cpu().numpy().astype(np.float64)
+        ref = oracle.block_step(xb, pmn, fb, *(t.numpy() for t in p.astuple()))
+        check_fp32("side %d pre" % i, pre.cpu(), ref["pre"])
+        check_fp32("side %d post" % i, post_g, ref["post"])
+        check_fp32("side %d comb" % i, comb_g, ref["comb"])
+        check_bf16("side %d h_norm" % i, h.cpu(), ref["h_norm"],
+                   abs_allow=h_norm_allowance(xb, pmn, p.norm_w.numpy(), ref["h_norm"]))
+        check_bf16("side %d y" % i, y.cpu(), ref["y"],
+                   abs_allow=y_allowance(fb, xb, ref["post"], ref["comb"], post_g, comb_g))
+        xs, pms = y, pre
+    assert _lib.raw("hc_consume_device_error", None) == 0
