@@ -143,7 +143,7 @@ __host__ __device__ inline Layout make_layout(int d) {
     o += L.dc * 4;
     o = (o + 15) & ~15;
     L.off_bar = o;
-    o += (2 * kSlots + 2 * kBufs + 4) * 8;  // full[], empty[], part[], coef[], 2 MMA meetings, ss[2]
+    o += (2 * kSlots + 2 * kBufs + 6) * 8;  // full[], empty[], part[], coef[], 2 MMA meetings, ss[2], weights
     o = (o + 15) & ~15;
     L.off_tmem = o;
     o += 16;
@@ -251,6 +251,10 @@ k_block_cluster(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     const uint32_t mma_free = bar0 + 8u * (2 * kSlots + 2 * kBufs + 1);
     // the CUDA-core warps hand each tile's sums of squares to the sender warp
     auto ss_bar = [&](int b) { return bar0 + 8u * (2 * kSlots + 2 * kBufs + 2 + b); };
+    // this CTA's slice of hc_fn, bulk-copied into the (still empty) ring at launch
+    // (wload), and the MMA warps done reading it from there (wfree)
+    const uint32_t wload_bar = bar0 + 8u * (2 * kSlots + 2 * kBufs + 4);
+    const uint32_t wfree_bar = bar0 + 8u * (2 * kSlots + 2 * kBufs + 5);
     float *sSS = reinterpret_cast<float *>(smem + L.off_ss);
     const uint32_t slot0 = smem_u32(smem);
 
@@ -269,6 +273,8 @@ k_block_cluster(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
         for (int b = 0; b < 2; ++b) mbar_init(ss_bar(b), kT);  // one lane per token
         mbar_init(mma_full, kMmaWarps * 32);
         mbar_init(mma_free, 32);
+        mbar_init(wload_bar, 1);
+        mbar_init(wfree_bar, kMmaWarps);
         fence_mbar_init_cluster();
         prefetch_tmap(&tm_x);
         if (kFull) prefetch_tmap(&tm_f);
@@ -294,13 +300,16 @@ k_block_cluster(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
         // hi(b0), hi(b1), mid(b0), mid(b1), lo(b0), lo(b1) of
         // W[nt*8+g][k0+2t, k0+2t+1] (b0) and W[nt*8+g][k0+8+2t, k0+9+2t] (b1).
         const uint32_t tw = tmem_base + ((uint32_t)(32 * (warp & 3)) << 16);
-        for (int q = 0; q < dc / 16; ++q) {  // k16 step q = columns 16q .. 16q + 15 of the slice
-            const int64_t col = (int64_t)s * d + (int64_t)rank * dc + 16 * q + 2 * t;
+        // the slice was bulk-copied into the ring at launch: row i of stream s at floats (s*24 + i) * dc
+        const bool wok = mbar_wait_warp<false>(wload_bar, 0u, &s_abort);
+        const float *wsm = reinterpret_cast<const float *>(smem) + (int64_t)s * kMix * dc;
+        for (int q = 0; wok && q < dc / 16; ++q) {  // k16 step q = columns 16q .. 16q + 15 of the slice
+            const int col = 16 * q + 2 * t;
 #pragma unroll
             for (int nt = 0; nt < 3; ++nt) {
-                const float *wr = p.hc_fn + (int64_t)(nt * 8 + g) * K + col;
-                const float2 p0 = __ldg(reinterpret_cast<const float2 *>(wr));
-                const float2 p1 = __ldg(reinterpret_cast<const float2 *>(wr + 8));
+                const float *wr = wsm + (nt * 8 + g) * dc + col;
+                const float2 p0 = *reinterpret_cast<const float2 *>(wr);
+                const float2 p1 = *reinterpret_cast<const float2 *>(wr + 8);
                 uint32_t h0, m0, l0, h1, m1, l1;
                 split3(p0.x, p0.y, h0, m0, l0);
                 split3(p1.x, p1.y, h1, m1, l1);
@@ -311,6 +320,10 @@ k_block_cluster(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             }
         }
         tmem_wait_st();
+        // every value read from the ring has gone into tensor memory: the ring is the producer's
+        __threadfence_block();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(wfree_bar);
         float acc[4][3][4];
 #pragma unroll
         for (int a = 0; a < 4; ++a)
@@ -319,7 +332,7 @@ k_block_cluster(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
 #pragma unroll
                 for (int c = 0; c < 4; ++c) acc[a][b][c] = 0.0f;
         int tiles_done = 0;
-        for (int u = 0; u < U; ++u) {
+        for (int u = 0; wok && u < U; ++u) {
             const int slot = u % kSlots;
             const uint32_t ph = (uint32_t)(u / kSlots) & 1u;
             if (!mbar_wait_warp<false>(full_bar(slot), ph, &s_abort)) break;
@@ -379,7 +392,16 @@ k_block_cluster(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
         if (lane == 0) {
             const uint64_t pol_keep = policy_evict_last(), pol_stream = policy_evict_first();
             int armed = 0;
-            for (int u = 0; u < U; ++u) {
+            // the slice of hc_fn into the ring (4 streams x 24 rows of dc floats); the ring
+            // is used for streaming once the MMA warps have moved it into tensor memory
+            mbar_arrive_expect_tx(wload_bar, (uint32_t)(kHC * kMix * dc * 4));
+            for (int s = 0; s < kHC; ++s)
+                for (int i = 0; i < kMix; ++i)
+                    bulk_load(slot0 + (uint32_t)((s * kMix + i) * dc * 4),
+                              p.hc_fn + (int64_t)i * K + (int64_t)s * d + (int64_t)rank * dc,
+                              (uint32_t)(dc * 4), wload_bar);
+            const bool wok = mbar_wait<false>(wfree_bar, 0u, &s_abort);
+            for (int u = 0; wok && u < U; ++u) {
                 const int slot = u % kSlots;
                 const uint32_t ph = (uint32_t)(u / kSlots) & 1u;
                 if (!mbar_wait<false>(empty_bar(slot), ph ^ 1u, &s_abort)) break;
@@ -756,8 +778,12 @@ bool cluster_path_supported(int d) {
     if (d % (cl::kC * cl::kCB) != 0 || d <= 0) return false;
     const cl::Layout L = cl::make_layout(d);
     // the weight fragments of one MMA warp must fit its 512 tensor-memory columns,
-    // and the CTA must be alone on its SM (it takes the whole tensor memory)
-    return L.wcols <= (int)cl::kTmemCols && L.total <= 232448 && 2 * L.total > 233472;
+    // and the CTA must be alone on its SM (it takes the whole tensor memory).  The
+    // weight slice is staged at launch over the ring and the coefficient buffers
+    // (written only after every CTA of the cluster is past its staging), never over
+    // the partial-sum buffers that peers write from the start.
+    const bool staged_fits = kHC * kMix * L.dc * 4 <= L.off_part;
+    return L.wcols <= (int)cl::kTmemCols && staged_fits && L.total <= 232448 && 2 * L.total > 233472;
 }
 
 template <bool kFull>

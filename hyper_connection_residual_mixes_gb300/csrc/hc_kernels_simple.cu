@@ -37,15 +37,23 @@ k_split_sinkhorn(const float *__restrict__ mixes, const float *__restrict__ hc_s
         m[4 * q + 0] = v.x; m[4 * q + 1] = v.y; m[4 * q + 2] = v.z; m[4 * q + 3] = v.w;
     }
     float pr[HC], po[HC], c[HC * HC];
-    split_sinkhorn_token_hc<HC>(m, __ldg(hc_scale), __ldg(hc_scale + 1), __ldg(hc_scale + 2), hc_base,
-                                iters, eps, pr, po, c);
+    // the fast reciprocal and exponential, as the fused kernels' owners use them
+    split_sinkhorn_token_hc<HC, true>(m, __ldg(hc_scale), __ldg(hc_scale + 1), __ldg(hc_scale + 2),
+                                      hc_base, iters, eps, pr, po, c);
+    // 16-byte stores (hc = 2: pre and post are 8 bytes per row)
+    if constexpr (HC % 4 == 0) {
 #pragma unroll
-    for (int k = 0; k < HC; ++k) {
-        pre[row * HC + k] = pr[k];
-        post[row * HC + k] = po[k];
+        for (int k = 0; k < HC; k += 4) {
+            reinterpret_cast<float4 *>(pre + row * HC + k)[0] = make_float4(pr[k], pr[k + 1], pr[k + 2], pr[k + 3]);
+            reinterpret_cast<float4 *>(post + row * HC + k)[0] = make_float4(po[k], po[k + 1], po[k + 2], po[k + 3]);
+        }
+    } else {
+        reinterpret_cast<float2 *>(pre + row * HC)[0] = make_float2(pr[0], pr[1]);
+        reinterpret_cast<float2 *>(post + row * HC)[0] = make_float2(po[0], po[1]);
     }
 #pragma unroll
-    for (int i = 0; i < HC * HC; ++i) comb[row * HC * HC + i] = c[i];
+    for (int i = 0; i < HC * HC; i += 4)
+        reinterpret_cast<float4 *>(comb + row * HC * HC + i)[0] = make_float4(c[i], c[i + 1], c[i + 2], c[i + 3]);
 }
 
 cudaError_t launch_split_sinkhorn(const float *mixes, const float *hc_scale, const float *hc_base,

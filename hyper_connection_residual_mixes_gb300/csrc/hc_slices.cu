@@ -99,7 +99,7 @@ constexpr int kUseP1 = 0, kUseP3 = 1, kUseSide = 2;
 // the bf16 box written over the f box: none, h_norm of the phase-3 side, or the
 // unnormalised bf16 h of the side whose phase 1 runs here
 constexpr int kHNone = 0, kHNorm = 1, kHPre = 2;
-constexpr int kNumBars = 3 * kSlots + 2 * kBufs + 2 + 2 + 2;
+constexpr int kNumBars = 3 * kSlots + 2 * kBufs + 2 + 2 + 2 + 2;
 
 struct Params {
     const float *state_in;   // kSide, kLast: coefficient rows of side i [n, 32]
@@ -231,6 +231,10 @@ k_slices(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUten
     // the CUDA-core warps are done with a tile's coefficient rows / pre_mix rows (buffer b)
     auto state_free = [&](int b) { return bar0 + 8u * (3 * kSlots + 2 * kBufs + 2 + b); };
     auto pm_free = [&](int b) { return bar0 + 8u * (3 * kSlots + 2 * kBufs + 4 + b); };
+    // this CTA's slice of hc_fn, bulk-copied into the (still empty) ring at launch
+    // (wload), and the MMA warps done reading it from there (wfree)
+    const uint32_t wload_bar = bar0 + 8u * (3 * kSlots + 2 * kBufs + 6);
+    const uint32_t wfree_bar = bar0 + 8u * (3 * kSlots + 2 * kBufs + 7);
     const uint32_t slot0 = smem_u32(smem);
 
     if (threadIdx.x == kWarpProducer * 32) {
@@ -250,6 +254,8 @@ k_slices(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUten
         }
         mbar_init(mma_full, kMmaWarps * 32);
         mbar_init(mma_free, 1);
+        mbar_init(wload_bar, 1);
+        mbar_init(wfree_bar, kMmaWarps);
         fence_mbar_init_cluster();
         prefetch_tmap(&tm_x);
         if (kAnyP3) {
@@ -275,27 +281,38 @@ k_slices(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUten
         const int s = warp - kWarpMma;
         const int gq = lane >> 2, t = lane & 3;
         const uint32_t tw = tmem_base + ((uint32_t)(32 * (warp & 3)) << 16);
+        bool wok = true;
         if (kAnyP1) {
             // B fragments of this slice's weights: k16 step q occupies TMEM columns
             // 18q .. 18q + 17 as, per n-tile nt, hi(b0), hi(b1), mid(b0), mid(b1),
-            // lo(b0), lo(b1) of W[nt*8+gq][k0+2t, +1] (b0) and W[nt*8+gq][k0+8+2t, +1] (b1)
-            for (int q = 0; q < dc / 16; ++q) {
-                const int64_t col = (int64_t)s * d + (int64_t)c * dc + 16 * q + 2 * t;
+            // lo(b0), lo(b1) of W[nt*8+gq][k0+2t, +1] (b0) and W[nt*8+gq][k0+8+2t, +1] (b1).
+            // The slice was bulk-copied into the ring at launch: row i of stream s at
+            // floats (s * kMix + i) * dc.
+            wok = mbar_wait_warp<false>(wload_bar, 0u, &s_abort);
+            if (wok) {
+                const float *wsm = reinterpret_cast<const float *>(smem) + (int64_t)s * kMix * dc;
+                for (int q = 0; q < dc / 16; ++q) {
+                    const int col = 16 * q + 2 * t;
 #pragma unroll
-                for (int nt = 0; nt < 3; ++nt) {
-                    const float *wr = p.hc_fn + (int64_t)(nt * 8 + gq) * K + col;
-                    const float2 p0 = __ldg(reinterpret_cast<const float2 *>(wr));
-                    const float2 p1 = __ldg(reinterpret_cast<const float2 *>(wr + 8));
-                    uint32_t h0, m0, l0, h1, m1, l1;
-                    split3(p0.x, p0.y, h0, m0, l0);
-                    split3(p1.x, p1.y, h1, m1, l1);
-                    const uint32_t c0 = tw + kWCols * q + 6 * nt;
-                    tmem_st2(c0 + 0, h0, h1);
-                    tmem_st2(c0 + 2, m0, m1);
-                    tmem_st2(c0 + 4, l0, l1);
+                    for (int nt = 0; nt < 3; ++nt) {
+                        const float *wr = wsm + (nt * 8 + gq) * dc + col;
+                        const float2 p0 = *reinterpret_cast<const float2 *>(wr);
+                        const float2 p1 = *reinterpret_cast<const float2 *>(wr + 8);
+                        uint32_t h0, m0, l0, h1, m1, l1;
+                        split3(p0.x, p0.y, h0, m0, l0);
+                        split3(p1.x, p1.y, h1, m1, l1);
+                        const uint32_t c0 = tw + kWCols * q + 6 * nt;
+                        tmem_st2(c0 + 0, h0, h1);
+                        tmem_st2(c0 + 2, m0, m1);
+                        tmem_st2(c0 + 4, l0, l1);
+                    }
                 }
             }
             tmem_wait_st();
+            // every value read from the ring has gone into tensor memory: the ring is the producer's
+            __threadfence_block();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(wfree_bar);
         }
         float acc[4][3][4];
 #pragma unroll
@@ -305,7 +322,7 @@ k_slices(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUten
 #pragma unroll
                 for (int e = 0; e < 4; ++e) acc[a][b][e] = 0.0f;
         int u = 0, tiles_done = 0;
-        bool ok = true;
+        bool ok = wok;
         for (int b = 0; b < NB && ok; ++b) {
             int type, k;
             block_of<kMode>(b, J, type, k);
@@ -375,6 +392,16 @@ k_slices(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUten
             int armed = 0, u = 0;
             int n_p1 = 0, n_p3 = 0;  // tiles whose phase 1 / phase 3 has started here
             bool ok = true;
+            if (kAnyP1) {
+                // the slice of hc_fn into the ring: 4 streams x 24 rows of dc floats
+                mbar_arrive_expect_tx(wload_bar, (uint32_t)(kHC * kMix * dc * 4));
+                for (int s = 0; s < kHC; ++s)
+                    for (int i = 0; i < kMix; ++i)
+                        bulk_load(slot0 + (uint32_t)((s * kMix + i) * dc * 4),
+                                  p.hc_fn + (int64_t)i * K + (int64_t)s * d + (int64_t)c * dc,
+                                  (uint32_t)(dc * 4), wload_bar);
+                ok = mbar_wait<false>(wfree_bar, 0u, &s_abort);
+            }
             for (int b = 0; b < NB && ok; ++b) {
                 int type, k;
                 block_of<kMode>(b, J, type, k);
@@ -959,7 +986,10 @@ void set_chain_scratch(sl::Params &p, float *state_out) {
 bool slices_supported(int d) {
     if (d <= 0 || d % (sl::kS * sl::kCB) != 0) return false;
     const sl::Layout L = sl::make_layout(d);
-    return L.wcols <= (int)sl::kTmemCols && L.total <= 232448 && 2 * L.total > 233472;
+    // the weight slice is staged at launch over the ring and the row buffers
+    // after it, which nothing uses before the MMA warps have read it
+    const bool staged_fits = kHC * kMix * L.dc * 4 <= L.off_mma;
+    return L.wcols <= (int)sl::kTmemCols && staged_fits && L.total <= 232448 && 2 * L.total > 233472;
 }
 
 size_t chain_state_bytes(int64_t n) { return chain_scratch(n).total; }
