@@ -106,7 +106,7 @@ def ncu_traffic_per_launch(n_tokens, path_kind="step"):
     None when the kernel's sources have changed since it was taken."""
     path = os.path.join(ROOT, "profiles", "hc_chain_side_traffic.json" if path_kind == "chain"
                         else "hc_block_step_traffic.json")
-    unit = "hc_slices.cu"  # both the chain and hc_block_step run its kernel
+    unit = "hc_slices.cu" if path_kind == "chain" else "hc_block_cluster.cu"
     try:
         with open(path) as fh:
             rec = json.load(fh)
@@ -348,8 +348,9 @@ def run_ours(args, rank, local_rank, world):
                              % (n * HC * d * 2 / 1e6)},
             "hbm_gbs_step": step_bytes / (ms_per_step / 1e3) / 1e9,
             "hbm_frac_step": step_bytes / (ms_per_step / 1e3) / 1e9 / peak,
-            "roofline": {"kernel": ("hc_chain_side (k_chain, side i's y and h_norm fused with side "
-                                    "i + 1's mixes)") if chain else KERNEL_NAME,
+            "roofline": {"kernel": ("hc_chain_side (k_slices<kSide>: side i's y and h_norm fused with side "
+                                    "i + 1's mixes, one CTA per SM in groups of 16)") if chain else
+                                   KERNEL_NAME + " (k_block_cluster)",
                          "bound": "hbm", "achieved": achieved,
                          "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                          "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs)"
@@ -374,10 +375,12 @@ def run_ours(args, rank, local_rank, world):
             out["cpu_baseline"] = cpu_baseline_sample(case, fs, target_s=args.cpu_seconds)
         if chain and args.workload == "long_prefill" and not args.no_configs:
             out["chain_equals_step"] = chain_equals_steps(case, fs, dev, stream)
+            out["model_order"] = run_model_order(case, fs, ys, h_norm, states, dev, stream)
     if rank == 0 and world == 1 and args.workload == "long_prefill" and not args.no_configs:
         del fs, case, ys, h_norm, states
         torch.cuda.empty_cache()
         out["configs"] = run_configs(dev, measured_peaks()[0], stream)
+        out["stream_counts"] = run_stream_counts(dev, stream)
     return out
 
 
@@ -584,6 +587,103 @@ def run_configs(dev, peak, stream):
                   "meets_0_70": 2 * alg / (statistics.mean(ch_pair) / 1e3) / 1e9 / peak >= 0.70},
         "calls": len(evs_step), "cpu_baseline": cpu}
     return recs
+
+
+def run_model_order(case, fs, ys, h_norm, states, dev, stream, steps=3):
+    """The long prefill in model order (Block page, Block.forward: the sublayer
+    reads h_norm_i before its output f_i exists): per side one hc_chain_side
+    launch writing y_i and side i + 1's bf16 h, then hc_chain_norm making
+    h_norm_{i+1} (here f_i is the stand-in sublayer output, given).  Timed with
+    CUDA events per launch; the side's algorithmic bytes are counted once per
+    side against the time of its two launches."""
+    P = case.params
+    n, d = case.n, case.d
+    hp = torch.empty((n, d), dtype=torch.bfloat16, device=dev)
+    evs = []
+
+    def one(record):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        hcg.hc_chain_begin(case.x, case.pre_mix, P[0].hc_fn, P[0].hc_scale, P[0].hc_base,
+                           state_out=states[0], h_pre_out=hp, stream=stream)
+        x = case.x
+        marks = []
+        for s in range(len(P)):
+            a = torch.cuda.Event(enable_timing=True)
+            m = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            hcg.hc_chain_norm(hp, states[s % 2], P[s].norm_w, h_norm=h_norm, stream=stream)
+            m.record(stream)
+            y = ys[s % 2]
+            if s + 1 < len(P):
+                q = P[s + 1]
+                hcg.hc_chain_side(x, fs[s], states[s % 2], P[s].norm_w, q.hc_fn, q.hc_scale, q.hc_base,
+                                  y=y, state_out=states[(s + 1) % 2], h_pre_out=hp, stream=stream)
+            else:
+                hcg.hc_chain_side(x, fs[s], states[s % 2], P[s].norm_w, y=y, write_h_norm=False,
+                                  stream=stream)
+            b.record(stream)
+            marks.append((a, m, b))
+            x = y
+        e1 = torch.cuda.Event(enable_timing=True)
+        e1.record(stream)
+        if record:
+            evs.append((e0, e1, marks))
+    one(False)
+    for _ in range(steps):
+        one(True)
+    torch.cuda.synchronize()
+    step_ms = statistics.mean(e0.elapsed_time(e1) for e0, e1, _ in evs)
+    # the sides that also start the next side (all but the last): norm + chain launch
+    pair_us = [a.elapsed_time(b) * 1e3 for _, _, mk in evs for (a, _, b) in mk[:-1]]
+    norm_us = [a.elapsed_time(m) * 1e3 for _, _, mk in evs for (a, m, _) in mk]
+    alg = n * BYTES_PER_TOKEN + BYTES_WEIGHTS
+    peak = measured_peaks()[0]
+    return {"path": "hc_chain_begin(h_pre_out) + 80 x [hc_chain_norm + hc_chain_side(h_pre_out)]",
+            "ms_per_step": step_ms, "tokens_per_s": n / (step_ms / 1e3), "steps": steps,
+            "us_per_side": statistics.mean(pair_us),
+            "us_norm_launch": statistics.mean(norm_us),
+            "roofline_frac_per_side": alg / (statistics.mean(pair_us) * 1e-6) / 1e9 / peak,
+            "note": "fraction: the side's algorithmic bytes (102,432 per token + weights) over the time of "
+                    "its chain launch and its hc_chain_norm launch (which moves 20,480 more bytes per token)"}
+
+
+def run_stream_counts(dev, stream, n=8192, d=D):
+    """Two and eight streams (the pages' kernel is generic in hc): one
+    hc_block_step and one hc_block_step_backward at 8,192 tokens x d = 5120,
+    timed with CUDA events (inputs larger than L2)."""
+    peak = measured_peaks()[0]
+    out = {}
+    for hc in (2, 8):
+        g = torch.Generator(device=dev).manual_seed(40 + hc)
+        x = inputs.streams(g, n, hc, d, device=dev)
+        pm = inputs.pre_mix(g, n, hc, device=dev)
+        f = inputs.sublayer_out(g, n, d, device=dev)
+        p = inputs.side_params(g, hc, d, device=dev)
+        mix = (2 + hc) * hc
+        fwd = lambda: hcg.hc_block_step(x, pm, f, *p.astuple(), stream=stream)
+        ws = torch.empty(hcg._lib.load().hc_block_step_backward_workspace_bytes(n, hc, d), dtype=torch.uint8,
+                         device=dev)
+        g_hn = torch.randn((n, d), device=dev, generator=g)
+        g_y = torch.randn((n, hc, d), device=dev, generator=g)
+        bwd = lambda: hcg.hc_block_step_backward(x, pm, f, *p.astuple(), g_hn, g_y, workspace=ws, stream=stream)
+        for _ in range(3):
+            fwd()
+            bwd()
+        t_f = statistics.mean(_event_ms(fwd, 10, stream))
+        t_b = statistics.mean(_event_ms(bwd, 5, stream))
+        w_bytes = mix * hc * d * 4 + 12 + mix * 4 + d * 4
+        alg_f = n * (hc * d * 2 + d * 2 + hc * 4 + hc * d * 2 + d * 2 + hc * 4) + w_bytes
+        alg_b = n * (hc * d * 2 + d * 2 + hc * 4 + d * 4 + hc * d * 4 + hc * d * 4 + hc * 4 + d * 4) + 2 * w_bytes
+        out["hc%d" % hc] = {
+            "tokens": n, "d": d, "mix": mix,
+            "forward": {"entry": "hc_block_step", "us": t_f * 1e3, "tokens_per_s": n / (t_f / 1e3),
+                        "algorithmic_bytes": alg_f, "roofline_frac": alg_f / (t_f / 1e3) / 1e9 / peak},
+            "backward": {"entry": "hc_block_step_backward", "us": t_b * 1e3, "tokens_per_s": n / (t_b / 1e3),
+                         "algorithmic_bytes": alg_b, "roofline_frac": alg_b / (t_b / 1e3) / 1e9 / peak}}
+        del x, f, g_hn, g_y, ws
+    return out
 
 
 def chain_equals_steps(case, fs, dev, stream):

@@ -48,7 +48,7 @@ def test_traffic_used_only_while_the_digest_matches(tmp_path, monkeypatch):
     assert bench.ncu_traffic_per_launch(1000, "chain") == int(100.5 * 1000 + 7)
     (csrc / "h1.h").write_text('#include "h2.cuh"\nint edited;\n')
     assert bench.ncu_traffic_per_launch(1000, "chain") is None
-    assert bench.ncu_traffic_per_launch(1000, "step") is None  # no record for the step kernel here
+    assert bench.ncu_traffic_per_launch(1000, "step") is None  # no record (nor source) for the step kernel here
     (csrc / "hc_slices.cu").unlink()
     assert bench.ncu_traffic_per_launch(1000, "chain") is None  # no source: no figure
 
