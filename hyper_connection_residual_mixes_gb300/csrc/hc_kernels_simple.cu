@@ -10,12 +10,20 @@
 //  k_mxfp8_cast      the MXFP8 cast of bf16 rows (Flash diagram, Cast to MXFP8).
 //  k_pre_norm_mxfp8  a4-a5 with the cast in its epilogue.
 //  k_tokens_simple   a1-a3 and optionally a4-a6 for TOK whole tokens per CTA
-//                    (Block page, Block.hc_mixes and Block.forward).
+//                    (Block page, Block.hc_mixes and Block.forward); with
+//                    kCoefIn, a4-a6 only, from coefficients computed before.
+//  k_mixes_tiled     a1-a3 for 32 tokens per CTA with hc_fn streamed through
+//                    shared memory (the projection on the tensor cores), for
+//                    the stream counts and widths the fused kernel does not
+//                    serve.
 //
-// These are the small-n and standalone paths; the fused large-n side step
-// lives in hc_block_cluster.cu.
+// The fused side step for hc = 4 and d a multiple of 1024 lives in
+// hc_block_cluster.cu and hc_slices.cu.
+#include <cuda.h>
+
 #include "hc_device.cuh"
 #include "hc_launch.h"
+#include "hc_ptx.cuh"
 
 namespace hc {
 
@@ -423,12 +431,15 @@ cudaError_t launch_post(const uint16_t *f, const uint16_t *residual, const float
 // Phase 2 (side step only): y and h for every token (x re-read through L1/L2),
 // sum of squares of the rounded h, then h_norm.
 constexpr int kTokThreads = 256;
+// from this many tokens on, a1-a3 run on token tiles (k_mixes_tiled): below it the
+// 32-token tiles would leave most SMs idle
+constexpr int64_t kTiledMinTokens = 128;
 
 // tokens per CTA: the accumulators are (2 + HC) * HC per token
 template <int HC>
 __host__ __device__ constexpr int tok_per_cta() { return HC <= 4 ? 4 : 1; }
 
-template <bool kFull, int HC>
+template <bool kFull, int HC, bool kCoefIn = false>
 __global__ void __launch_bounds__(kTokThreads)
 k_tokens_simple(const uint16_t *__restrict__ x, const float *__restrict__ pre_mix,
                 const uint16_t *__restrict__ f, const float *__restrict__ hc_fn,
@@ -450,6 +461,15 @@ k_tokens_simple(const uint16_t *__restrict__ x, const float *__restrict__ pre_mi
     const int ntok = (n - t0 < kTok) ? (int)(n - t0) : kTok;
     const int K = HC * d, K8 = K >> 3;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if constexpr (kCoefIn) {
+        // post and comb of each token, parked by k_mixes_tiled at the start of the
+        // token's own y row (read here before this CTA writes that row)
+        if (threadIdx.x < ntok) {
+            const float *src = reinterpret_cast<const float *>(y + (t0 + threadIdx.x) * K);
+#pragma unroll
+            for (int i = 0; i < HC + HC * HC; ++i) coef[threadIdx.x][i] = src[i];
+        }
+    } else {
 
     float acc[MIX][kTok];
     float ss[kTok];
@@ -533,6 +553,7 @@ k_tokens_simple(const uint16_t *__restrict__ x, const float *__restrict__ pre_mi
 #pragma unroll
         for (int i = 0; i < HC * HC; ++i) coef[u][HC + i] = c[i];
     }
+    }  // kCoefIn
     if constexpr (!kFull) return;
     __syncthreads();
 
@@ -608,6 +629,218 @@ k_tokens_simple(const uint16_t *__restrict__ x, const float *__restrict__ pre_mi
     }
 }
 
+// ------------------------------------------------------------------ a1-a3, token tiles on the tensor cores
+// m_i = r * sum_k x_k W_ik for 32 tokens per CTA (Block page, Block.hc_mixes),
+// then the split + Sinkhorn ("Stream combination" page) per token.  Each stage
+// stages COLS columns of x (the tile's tokens, bf16) and of W (all MIX rows,
+// fp32) through a two-deep cp.async ring.  The warps form RG row groups x CG
+// column groups: warp (rg, cg) takes rows rg*MIX/RG .. of W and 32 columns of
+// every stage, in k-steps of 8 on mma.sync m16n8k8 tf32 (x is exact in tf32;
+// W is split into tf32 hi + lo, two MMAs).  The tensor core's fp32
+// accumulation is not rounded to nearest, and over the thousands of k-steps of
+// a row of hc*d columns its error grows past the 1e-5 budget; so each stage's
+// products go to a fresh accumulator (8 MMAs) that is then added to the
+// running total with an ordinary fp32 add.  The sum of squares of x comes from
+// the same A fragments (row group 0: every element once).  The column groups'
+// totals are added in order through shared memory; then one thread per token
+// finishes.  Columns past K and tokens past n are zero-filled.
+constexpr int kMxTok = 32;
+constexpr int kMxThreads = 256;
+
+template <int HC>
+struct Mx {
+    static constexpr int MIX = (2 + HC) * HC;  // 8, 24, 80: whole 8-row n-tiles
+    static constexpr int NT = MIX / 8;
+    static constexpr int RG = HC == 8 ? 2 : 1;  // row groups of warps
+    static constexpr int CG = 8 / RG;           // column groups of warps
+    static constexpr int NTW = NT / RG;         // n-tiles per warp
+    static constexpr int COLS = 32 * CG;        // columns per stage (32 per warp)
+    static constexpr int KS = 4;                // k-steps of 8 per warp per stage
+    static constexpr int XROW = COLS + 8;       // bf16 per staged row of x (bank spread)
+    static constexpr int WROW = COLS + 4;       // floats per staged row of W
+    struct Stage {
+        uint16_t x[kMxTok][XROW];
+        float w[MIX][WROW];
+    };
+    static constexpr size_t SMEM = 2 * sizeof(Stage);
+    static_assert(MIX % 8 == 0 && NT % RG == 0, "whole n-tiles per row group");
+    static_assert(sizeof(Stage) % 16 == 0 && (XROW * 2) % 16 == 0 && (WROW * 4) % 16 == 0, "16-byte rows");
+    static_assert(SMEM >= sizeof(float) * CG * kMxTok * (MIX + 1), "the partial sums reuse the ring");
+};
+
+template <int HC>
+__global__ void __launch_bounds__(kMxThreads, 2)
+k_mixes_tiled(const uint16_t *__restrict__ x, const float *__restrict__ hc_fn,
+              const float *__restrict__ hc_scale, const float *__restrict__ hc_base, int64_t n, int d,
+              int iters, float eps, float norm_eps, float *__restrict__ pre_out,
+              float *__restrict__ post_out, float *__restrict__ comb_out, float *__restrict__ mixes_out,
+              uint16_t *__restrict__ coef_rows) {
+    using M = Mx<HC>;
+    constexpr int MIX = M::MIX, NTW = M::NTW, COLS = M::COLS, CG = M::CG;
+    extern __shared__ uint4 smem_u4[];
+    typename M::Stage *stg = reinterpret_cast<typename M::Stage *>(smem_u4);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, q = lane & 3;
+    const int rg = warp / CG, cg = warp % CG;
+    const int r0 = rg * NTW * 8;  // this warp's first row of W
+    const int64_t t0 = (int64_t)blockIdx.x * kMxTok;
+    const int K = HC * d;
+    const int nst = (K + COLS - 1) / COLS;
+    auto issue = [&](int st) {
+        if (st < nst) {
+            typename M::Stage &S = stg[st & 1];
+            const int c0 = st * COLS;
+            for (int k = threadIdx.x; k < kMxTok * (COLS / 8); k += kMxThreads) {
+                const int tt = k / (COLS / 8), kc = k % (COLS / 8);
+                const bool ok = t0 + tt < n && c0 + kc * 8 < K;
+                cp_async16(&S.x[tt][kc * 8], ok ? x + (t0 + tt) * K + c0 + kc * 8 : x, ok ? 16 : 0);
+            }
+            for (int k = threadIdx.x; k < MIX * (COLS / 4); k += kMxThreads) {
+                const int i = k / (COLS / 4), kc = k % (COLS / 4);
+                const bool ok = c0 + kc * 4 < K;
+                cp_async16(&S.w[i][4 * kc], ok ? hc_fn + (int64_t)i * K + c0 + 4 * kc : hc_fn, ok ? 16 : 0);
+            }
+        }
+        cp_async_commit();  // an empty group past the end keeps the count uniform
+    };
+    float tot[2][NTW][4];  // tokens 16mt + g (+8), rows r0 + 8nt + 2q (+1)
+    float ss[2][2];        // sum of squares of tokens 16mt + g, 16mt + g + 8 (this lane's columns)
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt) {
+        ss[mt][0] = ss[mt][1] = 0.0f;
+#pragma unroll
+        for (int nt = 0; nt < NTW; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) tot[mt][nt][e] = 0.0f;
+    }
+    issue(0);
+    for (int st = 0; st < nst; ++st) {
+        cp_async_wait<0>();
+        __syncthreads();  // stage st landed for every thread; the other slot is free
+        issue(st + 1);
+        const typename M::Stage &S = stg[st & 1];
+        float acc[2][NTW][4];
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < NTW; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[mt][nt][e] = 0.0f;
+#pragma unroll
+        for (int ks = 0; ks < M::KS; ++ks) {
+            const int k0 = 32 * cg + 8 * ks;
+            uint32_t a[2][4];
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt) {
+                a[mt][0] = (uint32_t)S.x[16 * mt + g][k0 + q] << 16;
+                a[mt][1] = (uint32_t)S.x[16 * mt + g + 8][k0 + q] << 16;
+                a[mt][2] = (uint32_t)S.x[16 * mt + g][k0 + q + 4] << 16;
+                a[mt][3] = (uint32_t)S.x[16 * mt + g + 8][k0 + q + 4] << 16;
+                if (rg == 0) {
+                    const float v0 = __uint_as_float(a[mt][0]), v1 = __uint_as_float(a[mt][1]);
+                    const float v2 = __uint_as_float(a[mt][2]), v3 = __uint_as_float(a[mt][3]);
+                    ss[mt][0] = fmaf(v2, v2, fmaf(v0, v0, ss[mt][0]));
+                    ss[mt][1] = fmaf(v3, v3, fmaf(v1, v1, ss[mt][1]));
+                }
+            }
+#pragma unroll
+            for (int nt = 0; nt < NTW; ++nt) {
+                uint32_t bh0, bl0, bh1, bl1;
+                tf32_split(S.w[r0 + 8 * nt + g][k0 + q], bh0, bl0);
+                tf32_split(S.w[r0 + 8 * nt + g][k0 + q + 4], bh1, bl1);
+#pragma unroll
+                for (int mt = 0; mt < 2; ++mt) {
+                    mma_tf32(acc[mt][nt], a[mt], bl0, bl1);
+                    mma_tf32(acc[mt][nt], a[mt], bh0, bh1);
+                }
+            }
+        }
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < NTW; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) tot[mt][nt][e] += acc[mt][nt][e];
+    }
+    cp_async_wait<0>();
+    __syncthreads();  // every warp is done with the ring: reuse it for the partial sums
+    float *red = reinterpret_cast<float *>(smem_u4);  // [column group][token][MIX + 1]
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt) {
+#pragma unroll
+        for (int nt = 0; nt < NTW; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int tt = 16 * mt + g + 8 * (e >> 1), i = r0 + 8 * nt + 2 * q + (e & 1);
+                red[(cg * kMxTok + tt) * (MIX + 1) + i] = tot[mt][nt][e];
+            }
+        if (rg == 0) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                float v = ss[mt][h];
+                v += __shfl_xor_sync(0xffffffffu, v, 1);
+                v += __shfl_xor_sync(0xffffffffu, v, 2);
+                if (q == 0) red[(cg * kMxTok + 16 * mt + g + 8 * h) * (MIX + 1) + MIX] = v;
+            }
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x < kMxTok && t0 + threadIdx.x < n) {
+        const int tt = threadIdx.x;
+        const int64_t t = t0 + tt;
+        float m[MIX];
+        float s2 = 0.0f;
+#pragma unroll
+        for (int w = 0; w < CG; ++w) s2 += red[(w * kMxTok + tt) * (MIX + 1) + MIX];
+        const float r = rsqrtf(s2 / (float)K + norm_eps);
+#pragma unroll
+        for (int i = 0; i < MIX; ++i) {
+            float v = 0.0f;
+#pragma unroll
+            for (int w = 0; w < CG; ++w) v += red[(w * kMxTok + tt) * (MIX + 1) + i];
+            m[i] = v * r;
+        }
+        float pr[HC], po[HC], c[HC * HC];
+        split_sinkhorn_token_hc<HC>(m, __ldg(hc_scale), __ldg(hc_scale + 1), __ldg(hc_scale + 2), hc_base,
+                                    iters, eps, pr, po, c);
+#pragma unroll
+        for (int k = 0; k < HC; ++k) {
+            if (pre_out) pre_out[t * HC + k] = pr[k];
+            if (post_out) post_out[t * HC + k] = po[k];
+        }
+        if (comb_out) {
+#pragma unroll
+            for (int i = 0; i < HC * HC; ++i) comb_out[t * HC * HC + i] = c[i];
+        }
+        if (mixes_out) {
+#pragma unroll
+            for (int i = 0; i < MIX; ++i) mixes_out[t * MIX + i] = m[i];
+        }
+        if (coef_rows) {  // post and comb for the a4-a6 pass, at the start of the token's y row
+            float *dst = reinterpret_cast<float *>(coef_rows + t * K);
+#pragma unroll
+            for (int k = 0; k < HC; ++k) dst[k] = po[k];
+#pragma unroll
+            for (int i = 0; i < HC * HC; ++i) dst[HC + i] = c[i];
+        }
+    }
+}
+
+template <int HC>
+cudaError_t launch_mixes_tiled_hc(const uint16_t *x, const float *hc_fn, const float *hc_scale,
+                                  const float *hc_base, int64_t n, int d, int iters, float eps,
+                                  float norm_eps, float *pre_out, float *post_out, float *comb_out,
+                                  float *mixes_out, uint16_t *coef_rows, cudaStream_t s) {
+    const int smem = (int)Mx<HC>::SMEM;
+    cudaError_t e = cudaFuncSetAttribute(k_mixes_tiled<HC>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    const int64_t blocks = (n + kMxTok - 1) / kMxTok;
+    k_mixes_tiled<HC><<<(unsigned)blocks, kMxThreads, smem, s>>>(x, hc_fn, hc_scale, hc_base, n, d, iters, eps,
+                                                                 norm_eps, pre_out, post_out, comb_out, mixes_out,
+                                                                 coef_rows);
+    return cudaGetLastError();
+}
+
 template <int HC>
 cudaError_t launch_tokens_simple_hc(const uint16_t *x, const float *pre_mix, const uint16_t *f,
                                     const float *hc_fn, const float *hc_scale, const float *hc_base,
@@ -618,6 +851,21 @@ cudaError_t launch_tokens_simple_hc(const uint16_t *x, const float *pre_mix, con
     constexpr int kTok = tok_per_cta<HC>();
     const int64_t blocks = (n + kTok - 1) / kTok;
     cudaError_t e;
+    if (n >= kTiledMinTokens) {
+        // a1-a3 on token tiles (hc_fn read once per 32 tokens), then a4-a6 per token from
+        // the coefficients parked in the y rows
+        e = launch_mixes_tiled_hc<HC>(x, hc_fn, hc_scale, hc_base, n, d, iters, eps, norm_eps, pre_out,
+                                      post_out, comb_out, mixes_out, f ? y : nullptr, s);
+        if (e != cudaSuccess || !f) return e;
+        const size_t smem = (size_t)kTok * d * 2;
+        e = cudaFuncSetAttribute(k_tokens_simple<true, HC, true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        k_tokens_simple<true, HC, true><<<(unsigned)blocks, kTokThreads, smem, s>>>(
+            x, pre_mix, f, hc_fn, hc_scale, hc_base, norm_w, n, d, iters, eps, norm_eps, h_norm, y,
+            nullptr, nullptr, nullptr, nullptr);
+        return cudaGetLastError();
+    }
     if (f) {
         const size_t smem = (size_t)kTok * d * 2;
         e = cudaFuncSetAttribute(k_tokens_simple<true, HC>,

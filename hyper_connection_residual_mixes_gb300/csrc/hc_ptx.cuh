@@ -244,6 +244,39 @@ __device__ __forceinline__ void prefetch_tmap(const void *tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
 
+// ---------------------------------------------------------------- cp.async and tf32 mma.sync
+// 16-byte asynchronous copy global -> shared; src_bytes = 0 fills zeros
+// (the source address is not read then).
+__device__ __forceinline__ void cp_async16(void *sdst, const void *gsrc, int src_bytes) {
+    const uint32_t sa = (uint32_t)__cvta_generic_to_shared(sdst);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(sa), "l"(gsrc), "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// tf32 helpers for the mma.sync contractions (projections, backward).  A
+// value a is carried as hi + lo: hi = a with its low 13 mantissa bits
+// cleared (a tf32 value), lo = a - hi (exact in fp32).  The MMA reads the top
+// 19 bits of each operand, so lo enters with a relative error below 2^-10 of
+// itself, i.e. 2^-20 of a.  Products take hi*hi + lo*hi + hi*lo; the lo*lo
+// term is of the same order and is dropped.
+__device__ __forceinline__ void tf32_split(float a, uint32_t &hi, uint32_t &lo) {
+    hi = __float_as_uint(a) & 0xffffe000u;
+    lo = __float_as_uint(a - __uint_as_float(hi));
+}
+// D += A (16x8, row) * B (8x8, col), tf32 inputs, fp32 accumulators
+__device__ __forceinline__ void mma_tf32(float (&dacc)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+        "{%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(dacc[0]), "+f"(dacc[1]), "+f"(dacc[2]), "+f"(dacc[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
 // ---------------------------------------------------------------- tensor core
 __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
                                             uint32_t &r3) {

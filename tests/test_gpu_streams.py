@@ -4,9 +4,12 @@ The pages' split + Sinkhorn kernel is written for any hc_mult (Stream
 combination page, Code section: the kernel's hc parameter); the released
 model uses 4.  The standalone paths (hc_split_sinkhorn, hc_mixes,
 hc_pre_norm, hc_pre_norm_mxfp8, hc_post and hc_block_step through the
-whole-token kernel) are compiled for 2, 4 and 8 streams; the cluster kernel
-and the chain stay at 4 (other counts are refused with HC_ERR_UNSUPPORTED).
-Tolerances are those of test_gpu_parity.py."""
+whole-token kernel below 128 tokens, through the token-tiled projection from
+128 tokens on) are compiled for 2, 4 and 8 streams; the cluster kernel and the
+chain stay at 4 (other counts are refused with HC_ERR_UNSUPPORTED).  The
+tiled cases include four streams at widths the cluster kernel does not serve
+(3072, and 5184, whose 20,736 columns leave a ragged last stage) and ragged
+last token tiles.  Tolerances are those of test_gpu_parity.py."""
 import numpy as np
 import pytest
 import torch
@@ -53,7 +56,9 @@ def test_split_sinkhorn_hc(hc, iters):
     check_fp32("comb", comb, rc)
 
 
-@pytest.mark.parametrize("hc,n,d", [(2, 37, 5120), (8, 37, 5120), (2, 9, 64), (8, 5, 1024)])
+@pytest.mark.parametrize("hc,n,d", [(2, 37, 5120), (8, 37, 5120), (2, 9, 64), (8, 5, 1024),
+                                    (2, 300, 5120), (8, 200, 5120), (8, 129, 64), (2, 1000, 1024),
+                                    (4, 300, 3072), (4, 257, 5184), (8, 160, 2048)])
 def test_mixes_hc(hc, n, d):
     case = inputs.tiny(seed=40 + n, n=n, d=d, hc=hc)
     p = case.params[0]
@@ -91,7 +96,9 @@ def test_pre_norm_and_post_hc(hc, n, d):
     assert np.array_equal(_np(codes), rc) and np.array_equal(_np(scales), rs)
 
 
-@pytest.mark.parametrize("hc,n,d", [(2, 16, 5120), (8, 16, 5120), (2, 41, 1024), (8, 9, 2048)])
+@pytest.mark.parametrize("hc,n,d", [(2, 16, 5120), (8, 16, 5120), (2, 41, 1024), (8, 9, 2048),
+                                    (2, 300, 5120), (8, 160, 5120), (8, 130, 64), (4, 200, 3072),
+                                    (4, 131, 5184)])
 def test_block_step_hc(hc, n, d):
     case = inputs.tiny(seed=70 + n + hc, n=n, d=d, hc=hc)
     p = case.params[0]
