@@ -9,8 +9,8 @@
 // it, and Sinkhorn is differentiated step by step through its iterates.
 //
 // These kernels favour plainness over speed; the four-stream model runs the
-// tensor-core kernels of hc_backward.cu.  One CTA per token:
-//   kg_proj   the projection a = x W^T (a warp per mix row);
+// tensor-core kernels of hc_backward.cu.  The projection a = x W^T runs on
+// token tiles (launch_proj_tiled, hc_kernels_simple.cu); then one CTA per token:
 //   kg_token  the token's sums in one pass, the split, Sinkhorn forward with
 //             its iterates and backward (one thread), g_pre_mix and the
 //             per-token record;
@@ -18,6 +18,7 @@
 // then partial sums of the parameter gradients over blocks of 1,024 tokens,
 // added block by block in a fixed order (deterministic, no atomics).
 #include "hc_backward_generic.h"
+#include "hc_launch.h"
 #include "hc_device.cuh"
 
 namespace hc {
@@ -64,30 +65,6 @@ __device__ __forceinline__ void ld4f(const float *p, float (&o)[4]) {
     o[0] = v.x; o[1] = v.y; o[2] = v.z; o[3] = v.w;
 }
 __device__ __forceinline__ float round_bf16(float v) { return bf16lo(pack_bf16x2(v, 0.0f)); }
-
-// a_i = sum_k x_k W_ik: warp w takes the rows w, w + 8, ...
-template <int HC>
-__global__ void __launch_bounds__(kThreads)
-kg_proj(const uint16_t *__restrict__ x, const float *__restrict__ hc_fn, int d, float *__restrict__ ws) {
-    using L = Lay<HC>;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t t = blockIdx.x;
-    const int K = HC * d;
-    const uint16_t *xt = x + t * K;
-    for (int i = warp; i < L::kMix; i += kWarps) {
-        const float *wr = hc_fn + (int64_t)i * K;
-        float acc = 0.0f;
-        for (int c = lane; c < K / 4; c += 32) {
-            float xv[4], wv[4];
-            ld4bf(xt + 4 * c, xv);
-            ld4f(wr + 4 * c, wv);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) acc = fmaf(xv[e], wv[e], acc);
-        }
-        acc = warp_sum(acc);
-        if (lane == 0) ws[t * L::kWs + L::kA + i] = acc;
-    }
-}
 
 // One pass over the token for its sums, then (one thread) the split, the
 // Sinkhorn iterates and their backward, the gradients of the mix numbers,
@@ -436,7 +413,8 @@ cudaError_t launch(const uint16_t *x, const float *pre_mix, const uint16_t *f, c
     const size_t smem = (size_t)(2 * iters + 1) * HC * HC * sizeof(float);
     cudaError_t e = cudaFuncSetAttribute(kg_token<HC>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kg_proj<HC><<<(unsigned)n, kThreads, 0, s>>>(x, hc_fn, d, ws);
+    e = launch_proj_tiled(x, hc_fn, n, HC, d, ws + L::kA, L::kWs, s);  // hc_fn read once per 32 tokens
+    if (e != cudaSuccess) return e;
     kg_token<HC><<<(unsigned)n, kThreads, smem, s>>>(x, pre_mix, f, hc_scale, hc_base, norm_w, d, iters, eps,
                                                      norm_eps, g_hn, g_y, g_pre, g_pm, ws);
     kg_gx<HC><<<(unsigned)n, kThreads, 0, s>>>(x, hc_fn, norm_w, g_hn, g_y, ws, d, g_x, g_f);

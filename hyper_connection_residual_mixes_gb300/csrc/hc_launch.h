@@ -24,6 +24,11 @@ cudaError_t launch_pre_norm_mxfp8(const uint16_t *x, const float *pre_mix, const
 cudaError_t launch_post(const uint16_t *f, const uint16_t *residual, const float *post,
                         const float *comb, int64_t n, int hc, int d, uint16_t *y, cudaStream_t s);
 
+// The projection a = x hc_fn^T alone (no statistic, no split), on token tiles
+// (hc_kernels_simple.cu): a[t][i] at dots[t * dots_stride + i].
+cudaError_t launch_proj_tiled(const uint16_t *x, const float *hc_fn, int64_t n, int hc, int d, float *dots,
+                              int dots_stride, cudaStream_t s);
+
 // a1-a3 (write pre/post/comb, optional mixes) or, when `f` is non-null, the
 // whole side step a1-a6.  Simple path: a CTA owns a few whole tokens.
 cudaError_t launch_tokens_simple(const uint16_t *x, const float *pre_mix, const uint16_t *f,
