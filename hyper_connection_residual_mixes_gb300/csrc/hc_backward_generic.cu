@@ -299,6 +299,84 @@ kg_gx(const uint16_t *__restrict__ x, const float *__restrict__ hc_fn, const flo
     }
 }
 
+// The same g_x and g_f for 16 tokens per CTA, so that hc_fn is read once per 16
+// tokens (kg_gx reads all of it per token: 13 MB at eight streams).  The CTA
+// walks d in chunks of 64 columns (32 at eight streams): first the projection term
+// D[t][s][c] = sum_i g_a[t][i] W[i][s*d + c] for its tokens into shared memory
+// (each thread two (stream, column) pairs, W read from L2 once per chunk),
+// then the rest per (token, column) as kg_gx computes it, plus D.  Sums are
+// fp32 in index order (i, then the terms in kg_gx's order), as kg_gx.
+constexpr int kGxT = 16;     // tokens per CTA
+template <int HC>
+__host__ __device__ constexpr int gx_cols() { return HC == 8 ? 32 : 64; }  // columns of d per chunk
+template <int HC>
+__global__ void __launch_bounds__(kThreads)
+kg_gx_tiled(const uint16_t *__restrict__ x, const float *__restrict__ hc_fn, const float *__restrict__ norm_w,
+            const float *__restrict__ g_hn, const float *__restrict__ g_y, const float *__restrict__ ws,
+            int64_t n, int d, float *__restrict__ g_x, float *__restrict__ g_f) {
+    using L = Lay<HC>;
+    constexpr int M = L::kMix;
+    constexpr int kGxC = gx_cols<HC>();
+    __shared__ float rec[kGxT][L::kWs];
+    __shared__ float dsum[kGxT][HC][kGxC];  // at most 48 KB with rec
+    const int64_t t0 = (int64_t)blockIdx.x * kGxT;
+    const int cnt = (int)((n - t0 < kGxT) ? n - t0 : kGxT);
+    const int64_t K = (int64_t)HC * d;
+    for (int q = threadIdx.x; q < kGxT * L::kWs; q += kThreads) {
+        const int u = q / L::kWs, j = q % L::kWs;
+        rec[u][j] = u < cnt ? ws[(t0 + u) * L::kWs + j] : 0.0f;
+    }
+    for (int c0 = 0; c0 < d; c0 += kGxC) {
+        __syncthreads();  // the records are in; the previous chunk's D has been used
+        // (1) D for (stream, column) pairs p = threadIdx.x + kThreads * j
+        for (int pr = threadIdx.x; pr < HC * kGxC; pr += kThreads) {
+            const int sI = pr / kGxC, cc = pr % kGxC;
+            if (c0 + cc >= d) continue;
+            float acc[kGxT];
+#pragma unroll
+            for (int u = 0; u < kGxT; ++u) acc[u] = 0.0f;
+            const float *wcol = hc_fn + (int64_t)sI * d + c0 + cc;
+            for (int i = 0; i < M; ++i) {
+                const float w = __ldg(wcol + (int64_t)i * K);
+#pragma unroll
+                for (int u = 0; u < kGxT; ++u) acc[u] = fmaf(rec[u][L::kGa + i], w, acc[u]);
+            }
+#pragma unroll
+            for (int u = 0; u < kGxT; ++u) dsum[u][sI][cc] = acc[u];
+        }
+        __syncthreads();
+        // (2) per (token, column)
+        for (int q = threadIdx.x; q < cnt * kGxC; q += kThreads) {
+            const int u = q / kGxC, cc = q % kGxC;
+            const int c = c0 + cc;
+            if (c >= d) continue;
+            const int64_t t = t0 + u;
+            const float *r = rec[u];
+            float xv[HC], gy[HC];
+#pragma unroll
+            for (int sI = 0; sI < HC; ++sI) {
+                xv[sI] = __uint_as_float((uint32_t)x[t * K + (int64_t)sI * d + c] << 16);
+                gy[sI] = __ldg(g_y + (t * HC + sI) * d + c);
+            }
+            float hv = r[L::kPm] * xv[0];
+#pragma unroll
+            for (int sI = 1; sI < HC; ++sI) hv = fmaf(r[L::kPm + sI], xv[sI], hv);
+            const float ghh = r[L::kRs] * (__ldg(norm_w + c) * __ldg(g_hn + t * d + c)) - r[L::kK3] * round_bf16(hv);
+            float fvv = r[L::kPost] * gy[0];
+#pragma unroll
+            for (int k = 1; k < HC; ++k) fvv = fmaf(r[L::kPost + k], gy[k], fvv);
+            g_f[t * d + c] = fvv;
+#pragma unroll
+            for (int sI = 0; sI < HC; ++sI) {
+                float a = fmaf(r[L::kPm + sI], ghh, r[L::kCr] * xv[sI]);
+#pragma unroll
+                for (int k = 0; k < HC; ++k) a = fmaf(r[L::kComb + sI * HC + k], gy[k], a);
+                g_x[(t * HC + sI) * d + c] = a + dsum[u][sI][cc];
+            }
+        }
+    }
+}
+
 // g_hc_fn partial sums over a block of tokens: part[b][i][k] = sum_t g_a[t][i] x[t][k];
 // one thread per column k of hc*d.
 template <int HC>
@@ -417,7 +495,11 @@ cudaError_t launch(const uint16_t *x, const float *pre_mix, const uint16_t *f, c
     if (e != cudaSuccess) return e;
     kg_token<HC><<<(unsigned)n, kThreads, smem, s>>>(x, pre_mix, f, hc_scale, hc_base, norm_w, d, iters, eps,
                                                      norm_eps, g_hn, g_y, g_pre, g_pm, ws);
-    kg_gx<HC><<<(unsigned)n, kThreads, 0, s>>>(x, hc_fn, norm_w, g_hn, g_y, ws, d, g_x, g_f);
+    if (HC >= 8)  // hc_fn of 13 MB: read once per 16 tokens; at two streams (330 KB) the per-token kernel wins
+        kg_gx_tiled<HC><<<(unsigned)((n + kGxT - 1) / kGxT), kThreads, 0, s>>>(x, hc_fn, norm_w, g_hn, g_y, ws,
+                                                                             n, d, g_x, g_f);
+    else
+        kg_gx<HC><<<(unsigned)n, kThreads, 0, s>>>(x, hc_fn, norm_w, g_hn, g_y, ws, d, g_x, g_f);
     kg_fn_partial<HC><<<dim3((unsigned)((K + kThreads - 1) / kThreads), (unsigned)blocks), kThreads, 0, s>>>(
         x, ws, n, (int)K, part_fn);
     kg_sum_blocks<<<(unsigned)((M * K + 255) / 256), 256, 0, s>>>(part_fn, blocks, M * K, g_fn);
