@@ -88,14 +88,16 @@ int hc_last_cuda_error(void) { return g_last_cuda_error; }
 int hc_version(void) { return 100; }
 
 hc_status hc_consume_device_error(cudaStream_t stream) {
-    unsigned int flag = 0, flag_chain = 0, flag_bwd = 0;
+    unsigned int flag = 0, flag_chain = 0, flag_bwd = 0, flag_proj = 0;
     hc_status st = cuda_status(hc::consume_device_error(stream, &flag));
     if (st != HC_OK) return st;
     st = cuda_status(hc::consume_slices_device_error(stream, &flag_chain));
     if (st != HC_OK) return st;
     st = cuda_status(hc::consume_backward_device_error(stream, &flag_bwd));
     if (st != HC_OK) return st;
-    return (flag | flag_chain | flag_bwd) ? HC_ERR_TIMEOUT : HC_OK;
+    st = cuda_status(hc::consume_proj_device_error(stream, &flag_proj));
+    if (st != HC_OK) return st;
+    return (flag | flag_chain | flag_bwd | flag_proj) ? HC_ERR_TIMEOUT : HC_OK;
 }
 
 hc_status hc_selftest_barrier_timeout(cudaStream_t stream) {

@@ -11,9 +11,9 @@
 // Sinkhorn is differentiated step by step through its stored intermediates.
 //
 // How, in three passes over the batch:
-//   k_bwd_proj   32 tokens per CTA: the projection a = x W^T on the tensor
-//                cores, x and W staged through shared memory with cp.async,
-//                W read once per tile (W is the 24 x hc*d matrix hc_fn);
+//   the projection a = x W^T (W is the 24 x hc*d matrix hc_fn) on the
+//                fifth-generation tensor cores (hc_proj_umma.cu), into the
+//                per-token records;
 //   k_bwd_token  one warp per token: h, the statistics (sum x^2 among
 //                them), g_pre_mix, the split and Sinkhorn forward with its
 //                iterates and the Sinkhorn backward (one matrix element per
@@ -40,7 +40,7 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kTokBlock = 1024;  // tokens per partial sum of a parameter gradient
 
 // The per-token record in the workspace (floats).  [0, kA) is what k_bwd_gx
-// stages for each token; [kA, kA + 24) comes from k_bwd_proj.
+// stages for each token; [kA, kA + 24) comes from the projection.
 constexpr int kWs = 112;
 constexpr int kGa = 0;      // g_a[24]: the gradient of the projection a
 constexpr int kPost = 24;   // post[4]
@@ -51,12 +51,9 @@ constexpr int kCr = 49;     // the statistic's coefficient of x in g_x
 constexpr int kK3 = 50;     // rs_h^3 / d * sum(h w g_hn)
 constexpr int kGz = 52;     // g_z[24]: the gradient of the pre-activations (= g_hc_base terms)
 constexpr int kGzm = 76;    // gzm[3]: the g_hc_scale terms
-constexpr int kA = 80;      // a[24] (k_bwd_proj)
+constexpr int kA = 80;      // a[24] (the projection)
 constexpr int kSmall = 32;  // partial sums per block for hc_base (24) and hc_scale (3)
 
-constexpr int kProjTok = 32;    // tokens per CTA of k_bwd_proj
-constexpr int kProjCols = 256;  // columns of x and W per stage
-constexpr int kProjStages = 2;
 constexpr int kTokWarps = 4;    // tokens (one warp each) per CTA of k_bwd_token
 constexpr int kTokMinCtas = 5;  // CTAs of k_bwd_token per SM the register budget aims at
 constexpr int kGxCols = 64;     // columns of d per CTA of k_bwd_gx
@@ -90,116 +87,12 @@ __device__ __forceinline__ void hc_pre4(const float (&pm)[kHC], const float (&xv
     h[3] = __uint_as_float(b & 0xffff0000u);
 }
 
-// a_i = sum_k x_k W_ik for kProjTok = 32 tokens, on the tensor cores (mma
-// m16n8k8 tf32: x is exact in tf32, W is split in hi + lo).  Each stage
-// stages 256 columns of x (the tile's tokens) and of W (all 24 rows)
-// through a cp.async ring; warp w takes the columns 32w .. 32w+31 of every
-// stage (four k-steps of 8).  The eight warps' partial sums are added in
-// warp order through shared memory at the end.  Rows are padded so that the
-// fragment loads hit distinct banks.  Tokens past n are zero-filled and not
-// written.
-constexpr int kPxRow = kProjCols + 8;  // bf16 per staged token row of x
-constexpr int kPwRow = kProjCols + 4;  // floats per staged row of W
-struct ProjStage {
-    uint16_t x[kProjTok][kPxRow];
-    float w[kMix][kPwRow];
-};
-constexpr size_t kProjSmem = sizeof(ProjStage) * kProjStages;
-static_assert(sizeof(ProjStage) % 16 == 0 && (kPxRow * 2) % 16 == 0 && (kPwRow * 4) % 16 == 0,
-              "staged rows must keep 16-byte alignment");
-static_assert(kProjSmem >= sizeof(float) * kWarps * kProjTok * kMix, "the partial sums reuse the ring");
-static_assert(kProjTok == 32 && kProjCols == 32 * kWarps, "k_bwd_proj's fragment map");
-
-__global__ void __launch_bounds__(kThreads, 2)
-k_bwd_proj(const uint16_t *__restrict__ x, const float *__restrict__ hc_fn, int64_t n, int K,
-           float *__restrict__ ws) {
-    extern __shared__ uint4 smem_u4[];
-    ProjStage *stg = reinterpret_cast<ProjStage *>(smem_u4);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int g = lane >> 2, q = lane & 3;
-    const int64_t t0 = (int64_t)blockIdx.x * kProjTok;
-    const int nst = K / kProjCols;
-    auto issue = [&](int st) {
-        if (st < nst) {
-            ProjStage &S = stg[st % kProjStages];
-            for (int k = threadIdx.x; k < kProjTok * (kProjCols / 8); k += kThreads) {
-                const int tt = k / (kProjCols / 8), kc = k % (kProjCols / 8);
-                const bool ok = t0 + tt < n;
-                cp_async16(&S.x[tt][kc * 8], ok ? x + (t0 + tt) * K + (int64_t)st * kProjCols + kc * 8 : x,
-                           ok ? 16 : 0);
-            }
-            for (int k = threadIdx.x; k < kMix * (kProjCols / 4); k += kThreads) {
-                const int i = k / (kProjCols / 4), kc = k % (kProjCols / 4);
-                cp_async16(&S.w[i][4 * kc], hc_fn + (int64_t)i * K + (int64_t)st * kProjCols + 4 * kc, 16);
-            }
-        }
-        cp_async_commit();  // an empty group past the end keeps the count uniform
-    };
-    float acc[2][3][4];  // tokens 16mt + g (+8), rows 8nt + 2q (+1)
-#pragma unroll
-    for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-        for (int nt = 0; nt < 3; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) acc[mt][nt][e] = 0.0f;
-#pragma unroll
-    for (int st = 0; st < kProjStages - 1; ++st) issue(st);
-    for (int st = 0; st < nst; ++st) {
-        cp_async_wait<kProjStages - 2>();
-        __syncthreads();  // stage st landed for every thread; slot (st - 1) is free
-        issue(st + kProjStages - 1);
-        const ProjStage &S = stg[st % kProjStages];
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-            const int k0 = 32 * warp + 8 * ks;
-            uint32_t bh[3][2], bl[3][2];
-#pragma unroll
-            for (int nt = 0; nt < 3; ++nt) {
-                tf32_split(S.w[8 * nt + g][k0 + q], bh[nt][0], bl[nt][0]);
-                tf32_split(S.w[8 * nt + g][k0 + q + 4], bh[nt][1], bl[nt][1]);
-            }
-#pragma unroll
-            for (int mt = 0; mt < 2; ++mt) {
-                const uint32_t a[4] = {(uint32_t)S.x[16 * mt + g][k0 + q] << 16,
-                                       (uint32_t)S.x[16 * mt + g + 8][k0 + q] << 16,
-                                       (uint32_t)S.x[16 * mt + g][k0 + q + 4] << 16,
-                                       (uint32_t)S.x[16 * mt + g + 8][k0 + q + 4] << 16};
-#pragma unroll
-                for (int nt = 0; nt < 3; ++nt) {
-                    mma_tf32(acc[mt][nt], a, bl[nt][0], bl[nt][1]);
-                    mma_tf32(acc[mt][nt], a, bh[nt][0], bh[nt][1]);
-                }
-            }
-        }
-    }
-    cp_async_wait<0>();
-    __syncthreads();  // every warp is done with the ring: reuse it for the partial sums
-    float *red = reinterpret_cast<float *>(smem_u4);  // [warp][token][row]
-#pragma unroll
-    for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-        for (int nt = 0; nt < 3; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int tt = 16 * mt + g + 8 * (e >> 1), i = 8 * nt + 2 * q + (e & 1);
-                red[(warp * kProjTok + tt) * kMix + i] = acc[mt][nt][e];
-            }
-    __syncthreads();
-    for (int o = threadIdx.x; o < kProjTok * kMix; o += kThreads) {
-        const int tt = o / kMix, i = o % kMix;
-        float v = red[tt * kMix + i];
-#pragma unroll
-        for (int w = 1; w < kWarps; ++w) v += red[(w * kProjTok + tt) * kMix + i];
-        if (t0 + tt < n) ws[(t0 + tt) * kWs + kA + i] = v;
-    }
-}
-
 // One warp per token, kTokWarps tokens per CTA; no CTA-wide barrier, so
 // while one warp runs its Sinkhorn the others keep streaming.  The token is
 // read once, in chunks of four channels (small register footprint, many
 // warps in flight).  Shared memory per warp: the Sinkhorn iterates and the
 // reciprocals of their sums
-// (2 * iters matrices of 16 each).  Reads a from the record (k_bwd_proj),
+// (2 * iters matrices of 16 each).  Reads a from the record (the projection),
 // writes the rest of it.
 __global__ void __launch_bounds__(kTokWarps * 32, kTokMinCtas)
 k_bwd_token(const uint16_t *__restrict__ x, const float *__restrict__ pre_mix,
@@ -716,7 +609,8 @@ cudaError_t backward_static_scratch(void **ptr) { return cudaGetSymbolAddress(pt
 size_t backward_workspace_bytes(int64_t n, int d) {
     const int64_t blocks = (n + bw::kTokBlock - 1) / bw::kTokBlock;
     const int64_t K = (int64_t)kHC * d;
-    return (size_t)(n * bw::kWs + blocks * (kMix * K + d + bw::kSmall)) * sizeof(float);
+    return (size_t)(n * bw::kWs + blocks * (kMix * K + d + bw::kSmall)) * sizeof(float) +
+           proj_umma_wsplit_bytes(kHC, K);
 }
 
 cudaError_t launch_block_step_backward(const uint16_t *x, const float *pre_mix, const uint16_t *f,
@@ -733,15 +627,12 @@ cudaError_t launch_block_step_backward(const uint16_t *x, const float *pre_mix, 
     float *part_fn = ws + n * kWs;
     float *part_w = part_fn + (int64_t)blocks * kMix * K;
     float *part_s = part_w + (int64_t)blocks * d;
+    uint16_t *wsplit = reinterpret_cast<uint16_t *>(part_s + (int64_t)blocks * kSmall);
     const size_t smem = kTokWarps * (size_t)(4 * iters) * kHC * kHC * sizeof(float);
     cudaError_t e = cudaFuncSetAttribute(k_bwd_token, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
-    if ((e = cudaFuncSetAttribute(k_bwd_proj, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)kProjSmem)) != cudaSuccess)
-        return e;
-    k_bwd_proj<<<(unsigned)((n + kProjTok - 1) / kProjTok), kThreads, kProjSmem, s>>>(x, hc_fn, n, (int)K,
-                                                                                   ws);
+    if ((e = launch_proj_umma(x, hc_fn, n, kHC, d, wsplit, ws + kA, kWs, s)) != cudaSuccess) return e;
     k_bwd_token<<<(unsigned)((n + kTokWarps - 1) / kTokWarps), kTokWarps * 32, smem, s>>>(
         x, pre_mix, f, hc_scale, hc_base, norm_w, n, d, iters, eps, norm_eps, g_hn, g_y, g_pre, g_pm, ws);
     if ((e = cudaFuncSetAttribute(k_bwd_gx, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGxSmem)) !=

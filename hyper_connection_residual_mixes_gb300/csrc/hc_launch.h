@@ -29,6 +29,14 @@ cudaError_t launch_post(const uint16_t *f, const uint16_t *residual, const float
 cudaError_t launch_proj_tiled(const uint16_t *x, const float *hc_fn, int64_t n, int hc, int d, float *dots,
                               int dots_stride, cudaStream_t s);
 
+// The projection a = x hc_fn^T alone on the tcgen05 tensor cores
+// (hc_proj_umma.cu): a[t][i] at out[t * out_stride + i].  `wsplit` is device
+// scratch of proj_umma_wsplit_bytes(hc, hc * d) bytes (16-byte aligned) for the
+// split weights; it is dead once the launch has completed.
+size_t proj_umma_wsplit_bytes(int hc, int64_t K);
+cudaError_t launch_proj_umma(const uint16_t *x, const float *hc_fn, int64_t n, int hc, int d, uint16_t *wsplit,
+                             float *out, int out_stride, cudaStream_t s);
+
 // a1-a3 (write pre/post/comb, optional mixes) or, when `f` is non-null, the
 // whole side step a1-a6.  Simple path: a CTA owns a few whole tokens.
 cudaError_t launch_tokens_simple(const uint16_t *x, const float *pre_mix, const uint16_t *f,
@@ -95,6 +103,7 @@ cudaError_t launch_chain_norm(const uint16_t *h_pre, const float *state, const f
 cudaError_t consume_device_error(cudaStream_t s, unsigned int *flag);
 cudaError_t consume_slices_device_error(cudaStream_t s, unsigned int *flag);
 cudaError_t consume_backward_device_error(cudaStream_t s, unsigned int *flag);
+cudaError_t consume_proj_device_error(cudaStream_t s, unsigned int *flag);
 // one warp waits on a barrier nothing arrives on (the bounded-wait self-test)
 cudaError_t launch_selftest_wait(cudaStream_t s);
 
