@@ -39,9 +39,9 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kTokBlock = 1024;  // tokens per partial sum of a parameter gradient
 
-// The per-token record in the workspace (floats).  [0, kA) is what k_bwd_gx
-// stages for each token; [kA, kA + 24) comes from the projection.
-constexpr int kWs = 112;
+// The per-token record in the workspace (floats).  [0, kStaged) is what
+// k_bwd_gx stages for each token; [kA, kA + 24) comes from the projection.
+constexpr int kWs = 140;
 constexpr int kGa = 0;      // g_a[24]: the gradient of the projection a
 constexpr int kPost = 24;   // post[4]
 constexpr int kComb = 28;   // comb[16]
@@ -51,7 +51,9 @@ constexpr int kCr = 49;     // the statistic's coefficient of x in g_x
 constexpr int kK3 = 50;     // rs_h^3 / d * sum(h w g_hn)
 constexpr int kGz = 52;     // g_z[24]: the gradient of the pre-activations (= g_hc_base terms)
 constexpr int kGzm = 76;    // gzm[3]: the g_hc_scale terms
-constexpr int kA = 80;      // a[24] (the projection)
+constexpr int kGaP = 80;    // g_a as three bf16 parts hi, mid, lo: 72 bf16 (36 floats), part-major
+constexpr int kStaged = 116;
+constexpr int kA = 116;     // a[24] (the projection)
 constexpr int kSmall = 32;  // partial sums per block for hc_base (24) and hc_scale (3)
 
 constexpr int kTokWarps = 4;    // tokens (one warp each) per CTA of k_bwd_token
@@ -244,8 +246,18 @@ k_bwd_token(const uint16_t *__restrict__ x, const float *__restrict__ pre_mix,
     z2 = warp_sum(z2);
     gr = warp_sum(gr);
     if (live) {
-        wt[kGa + i] = gm * r;
+        const float ga = gm * r;
+        wt[kGa + i] = ga;
         wt[kGz + i] = gz;
+        // the three bf16 parts of g_a for the bf16 MMAs of k_bwd_gx: ga = hi + mid + lo to ~2^-24
+        const uint32_t hi = pack_bf16x2(ga, 0.0f) & 0xffffu;
+        const float r1 = ga - bf16lo(hi);
+        const uint32_t mid = pack_bf16x2(r1, 0.0f) & 0xffffu;
+        const uint32_t lo = pack_bf16x2(r1 - bf16lo(mid), 0.0f) & 0xffffu;
+        uint16_t *gp = reinterpret_cast<uint16_t *>(wt + kGaP);
+        gp[i] = (uint16_t)hi;
+        gp[kMix + i] = (uint16_t)mid;
+        gp[2 * kMix + i] = (uint16_t)lo;
     }
     if (lane == 0) {
         *reinterpret_cast<float4 *>(wt + kPm) = make_float4(pm[0], pm[1], pm[2], pm[3]);
@@ -284,7 +296,8 @@ k_bwd_token(const uint16_t *__restrict__ x, const float *__restrict__ pre_mix,
 constexpr int kXRow = kHC * kGxCols + 8;   // bf16 per token row of the x tile
 constexpr int kGyRow = kHC * kGxCols + 8;  // floats per token row of the g_y tile
 constexpr int kGhRow = kGxCols + 8;        // floats per token row of the g_hn tile
-constexpr int kRecRow = kA + 4;            // floats per staged token record
+constexpr int kRecRow = kStaged + 8;       // floats per staged token record (496 bytes: ldmatrix rows
+                                           // of 8 records fall in distinct 16-byte bank groups)
 struct GxStage {
     uint16_t x[kGxTile][kXRow];
     float gy[kGxTile][kGyRow];
@@ -318,7 +331,7 @@ k_bwd_gx(const uint16_t *__restrict__ x, const float *__restrict__ hc_fn,
     __shared__ __align__(8) uint64_t full_bar[kGxStages];
     __shared__ __align__(8) uint64_t empty_bar[kGxStages];  // one arrive per warp when done with a tile
     __shared__ volatile int s_abort;
-    constexpr uint32_t kRowBytes = kHC * kGxCols * 2 + kHC * kGxCols * 4 + kGxCols * 4 + kA * 4;  // per token
+    constexpr uint32_t kRowBytes = kHC * kGxCols * 2 + kHC * kGxCols * 4 + kGxCols * 4 + kStaged * 4;  // per token
     {
         // zero the ring once (finite values in rows that partial tiles do not copy)
         uint4 *z = smem_u4;
@@ -363,7 +376,7 @@ k_bwd_gx(const uint16_t *__restrict__ x, const float *__restrict__ hc_fn,
                 if (u < cnt) bulk_load(smem_u32(&S.ghn[u][0]), g_hn + (tb + u) * d + c0, kGxCols * 4, bar);
             } else {
                 const int u = k - 2 * kGxTile * kHC - kGxTile;
-                if (u < cnt) bulk_load(smem_u32(&S.rec[u][0]), ws + (tb + u) * kWs, kA * 4, bar);
+                if (u < cnt) bulk_load(smem_u32(&S.rec[u][0]), ws + (tb + u) * kWs, kStaged * 4, bar);
             }
         }
     };
@@ -379,13 +392,29 @@ k_bwd_gx(const uint16_t *__restrict__ x, const float *__restrict__ hc_fn,
             for (int h = 0; h < 2; ++h)
                 tf32_split(__ldg(hc_fn + (8 * ks + q + 4 * h) * K + (int64_t)nt * d + c0 + cw + g),
                            bh[nt][ks][h], bl[nt][ks][h]);
-    float accW[2][kHC][4];  // g_hc_fn: rows 16mt + g (+8), stream nt, columns 2q, 2q + 1
+    // g_hc_fn partials (the second contraction, bf16 m16n8k16): accumulator row
+    // g (+8) of m-tile mt = column c0 + cw + g of stream 2mt (2mt + 1), column
+    // 2q (+1) of n-tile nt = mix row 8nt + 2q (+1)
+    float accW[2][3][4];
 #pragma unroll
     for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-        for (int nt = 0; nt < kHC; ++nt)
+        for (int nt = 0; nt < 3; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) accW[mt][nt][e] = 0.0f;
+    // ldmatrix row addresses.  x^T as A (.trans): lane l gives token (l & 7) +
+    // 8 (l >> 4) of stream 2mt + ((l >> 3) & 1) at the warp's 8 columns.  g_a^T
+    // parts as B (.trans): matrix 2 (3p + nt) + h = tokens 8h .. 8h + 7, mixes
+    // 8nt .. 8nt + 7 of part p.
+    const int xl_tok = (lane & 7) + 8 * (lane >> 4), xl_str = (lane >> 3) & 1;
+    const uint32_t xl_off = (uint32_t)((xl_tok * kXRow + xl_str * kGxCols + cw) * 2);
+    uint32_t gl_off[5];
+#pragma unroll
+    for (int j = 0; j < 5; ++j) {
+        const int mi = 4 * j + (lane >> 3) < 18 ? 4 * j + (lane >> 3) : 17;
+        const int pn = mi >> 1, h = mi & 1;  // pn = 3p + nt
+        gl_off[j] = (uint32_t)(((lane & 7) + 8 * h) * kRecRow * 4 + kGaP * 4 + ((pn / 3) * kMix + 8 * (pn % 3)) * 2);
+    }
     const int cc0 = c0 + cw + 2 * q;         // the lane's two columns of d: cc0, cc0 + 1
     const float wn0 = __ldg(norm_w + cc0), wn1 = __ldg(norm_w + cc0 + 1);
     float gw0 = 0.0f, gw1 = 0.0f, sm = 0.0f;
@@ -424,34 +453,37 @@ k_bwd_gx(const uint16_t *__restrict__ x, const float *__restrict__ hc_fn,
             }
         }
 
-        // (2) g_hc_fn[i][s, c] += sum_t g_a[t][i] x[t][s][c]; x is exact in tf32
+        // (2) g_hc_fn[i][s, c] += sum_t g_a[t][i] x[t][s][c]: bf16 MMAs, x exact,
+        // g_a as hi + mid + lo; tokens past the tile masked out of g_a
+        {
+            const uint32_t xs = smem_u32(&S.x[0][0]) + xl_off;
+            uint32_t xa[2][4];
 #pragma unroll
-        for (int ks = 0; ks < 2; ++ks) {
-            const int ta = 8 * ks + q, tb4 = ta + 4;
-            uint32_t bx[kHC][2];
+            for (int mt = 0; mt < 2; ++mt)
+                ldmatrix_x4_trans(xs + (uint32_t)(mt * 2 * kGxCols * 2), xa[mt][0], xa[mt][1], xa[mt][2], xa[mt][3]);
+            const uint32_t rs0 = smem_u32(&S.rec[0][0]);
+            uint32_t gb[20];  // matrix m = 2 (3p + nt) + h
 #pragma unroll
-            for (int nt = 0; nt < kHC; ++nt) {
-                bx[nt][0] = (uint32_t)S.x[ta][nt * kGxCols + cw + g] << 16;
-                bx[nt][1] = (uint32_t)S.x[tb4][nt * kGxCols + cw + g] << 16;
-            }
-            const bool va = ta < cnt, vb = tb4 < cnt;  // rows past the tile take no part
+            for (int j = 0; j < 4; ++j)
+                ldmatrix_x4_trans(rs0 + gl_off[j], gb[4 * j], gb[4 * j + 1], gb[4 * j + 2], gb[4 * j + 3]);
+            ldmatrix_x2_trans(rs0 + gl_off[4], gb[16], gb[17]);
+            if (cnt < kGxTile) {
+                const uint32_t m0 = (2 * q < cnt ? 0xffffu : 0u) | (2 * q + 1 < cnt ? 0xffff0000u : 0u);
+                const uint32_t m1 = (2 * q + 8 < cnt ? 0xffffu : 0u) | (2 * q + 9 < cnt ? 0xffff0000u : 0u);
 #pragma unroll
-            for (int mt = 0; mt < 2; ++mt) {
-                uint32_t ah[4], al[4];
-                tf32_split(va ? S.rec[ta][kGa + 16 * mt + g] : 0.0f, ah[0], al[0]);
-                tf32_split(vb ? S.rec[tb4][kGa + 16 * mt + g] : 0.0f, ah[2], al[2]);
-                if (mt == 0) {
-                    tf32_split(va ? S.rec[ta][kGa + g + 8] : 0.0f, ah[1], al[1]);
-                    tf32_split(vb ? S.rec[tb4][kGa + g + 8] : 0.0f, ah[3], al[3]);
-                } else {  // rows 24 .. 31 are padding
-                    ah[1] = al[1] = ah[3] = al[3] = 0u;
-                }
-#pragma unroll
-                for (int nt = 0; nt < kHC; ++nt) {
-                    mma_tf32(accW[mt][nt], al, bx[nt][0], bx[nt][1]);
-                    mma_tf32(accW[mt][nt], ah, bx[nt][0], bx[nt][1]);
+                for (int m = 0; m < 18; m += 2) {
+                    gb[m] &= m0;
+                    gb[m + 1] &= m1;
                 }
             }
+#pragma unroll
+            for (int p = 2; p >= 0; --p)
+#pragma unroll
+                for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+                    for (int nt = 0; nt < 3; ++nt)
+                        mma_bf16_16816(accW[mt][nt], xa[mt][0], xa[mt][1], xa[mt][2], xa[mt][3],
+                                       gb[2 * (3 * p + nt)], gb[2 * (3 * p + nt) + 1]);
         }
 
         // (3) the rest, per (token, column)
@@ -515,17 +547,17 @@ k_bwd_gx(const uint16_t *__restrict__ x, const float *__restrict__ hc_fn,
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&empty_bar[it % kGxStages]));
     }
-    // g_hc_fn partials: accumulator (row 16mt + g (+8), stream nt, columns 2q, 2q + 1)
+    // g_hc_fn partials: accumulator (m-tile mt, n-tile nt, e) = mix row 8nt + 2q + (e & 1),
+    // stream 2mt + (e >> 1), column c0 + cw + g
 #pragma unroll
     for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-        for (int nt = 0; nt < kHC; ++nt) {
-            const int64_t colx = (int64_t)nt * d + cc0;
-            float *row = part_fn + ((int64_t)blockIdx.y * kMix + 16 * mt + g) * K + colx;
-            *reinterpret_cast<float2 *>(row) = make_float2(accW[mt][nt][0], accW[mt][nt][1]);
-            if (mt == 0)
-                *reinterpret_cast<float2 *>(row + 8 * K) = make_float2(accW[mt][nt][2], accW[mt][nt][3]);
-        }
+        for (int nt = 0; nt < 3; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int i = 8 * nt + 2 * q + (e & 1), sI = 2 * mt + (e >> 1);
+                part_fn[((int64_t)blockIdx.y * kMix + i) * K + (int64_t)sI * d + c0 + cw + g] = accW[mt][nt][e];
+            }
     // g_norm_w partials: sum over the eight token rows g (lanes q, q+4, ..., q+28)
 #pragma unroll
     for (int m = 4; m < 32; m <<= 1) {
