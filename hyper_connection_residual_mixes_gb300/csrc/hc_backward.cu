@@ -445,12 +445,14 @@ k_bwd_gx(const uint16_t *__restrict__ x, const float *__restrict__ hc_fn,
             tf32_split(S.rec[g + 8][kGa + 8 * ks + q], ah[1], al[1]);
             tf32_split(S.rec[g][kGa + 8 * ks + q + 4], ah[2], al[2]);
             tf32_split(S.rec[g + 8][kGa + 8 * ks + q + 4], ah[3], al[3]);
+            // term by term over the four streams, so that consecutive MMAs feed
+            // different accumulators (each accumulator sees the same order)
 #pragma unroll
-            for (int nt = 0; nt < kHC; ++nt) {
-                mma_tf32(dA[nt], al, bh[nt][ks][0], bh[nt][ks][1]);
-                mma_tf32(dA[nt], ah, bl[nt][ks][0], bl[nt][ks][1]);
-                mma_tf32(dA[nt], ah, bh[nt][ks][0], bh[nt][ks][1]);
-            }
+            for (int nt = 0; nt < kHC; ++nt) mma_tf32(dA[nt], al, bh[nt][ks][0], bh[nt][ks][1]);
+#pragma unroll
+            for (int nt = 0; nt < kHC; ++nt) mma_tf32(dA[nt], ah, bl[nt][ks][0], bl[nt][ks][1]);
+#pragma unroll
+            for (int nt = 0; nt < kHC; ++nt) mma_tf32(dA[nt], ah, bh[nt][ks][0], bh[nt][ks][1]);
         }
 
         // (2) g_hc_fn[i][s, c] += sum_t g_a[t][i] x[t][s][c]: bf16 MMAs, x exact,

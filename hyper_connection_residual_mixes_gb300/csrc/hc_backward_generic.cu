@@ -9,8 +9,9 @@
 // it, and Sinkhorn is differentiated step by step through its iterates.
 //
 // These kernels favour plainness over speed; the four-stream model runs the
-// tensor-core kernels of hc_backward.cu.  The projection a = x W^T runs on
-// token tiles (launch_proj_tiled, hc_kernels_simple.cu); then one CTA per token:
+// tensor-core kernels of hc_backward.cu.  The projection a = x W^T runs on the
+// fifth-generation tensor cores (launch_proj_umma, hc_proj_umma.cu); then one
+// CTA per token:
 //   kg_token  the token's sums in one pass, the split, Sinkhorn forward with
 //             its iterates and backward (one thread), g_pre_mix and the
 //             per-token record;
@@ -33,7 +34,7 @@ constexpr int kFnTile = 16;      // tokens per staged g_a tile in kg_fn_partial
 template <int HC>
 struct Lay {
     static constexpr int kMix = (2 + HC) * HC;
-    static constexpr int kA = 0;                // a[mix]: the projection (kg_proj)
+    static constexpr int kA = 0;                // a[mix]: the projection
     static constexpr int kGa = kMix;            // g_a[mix]: the gradient of a
     static constexpr int kGz = 2 * kMix;        // g_z[mix]: the g_hc_base terms
     static constexpr int kGzm = 3 * kMix;       // gzm[3]: the g_hc_scale terms
@@ -471,7 +472,8 @@ size_t ws_bytes(int64_t n, int d) {
     using L = Lay<HC>;
     const int64_t blocks = (n + kTokBlock - 1) / kTokBlock;
     const int64_t K = (int64_t)HC * d;
-    return (size_t)(n * L::kWs + blocks * (L::kMix * K + d + L::kSmall)) * sizeof(float);
+    return (size_t)(n * L::kWs + blocks * (L::kMix * K + d + L::kSmall)) * sizeof(float) +
+           proj_umma_wsplit_bytes(HC, K);
 }
 
 template <int HC>
@@ -488,10 +490,11 @@ cudaError_t launch(const uint16_t *x, const float *pre_mix, const uint16_t *f, c
     float *part_fn = ws + n * L::kWs;
     float *part_w = part_fn + (int64_t)blocks * M * K;
     float *part_s = part_w + (int64_t)blocks * d;
+    uint16_t *wsplit = reinterpret_cast<uint16_t *>(part_s + (int64_t)blocks * L::kSmall);
     const size_t smem = (size_t)(2 * iters + 1) * HC * HC * sizeof(float);
     cudaError_t e = cudaFuncSetAttribute(kg_token<HC>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    e = launch_proj_tiled(x, hc_fn, n, HC, d, ws + L::kA, L::kWs, s);  // hc_fn read once per 32 tokens
+    e = launch_proj_umma(x, hc_fn, n, HC, d, wsplit, ws + L::kA, L::kWs, s);  // tcgen05, hc_proj_umma.cu
     if (e != cudaSuccess) return e;
     kg_token<HC><<<(unsigned)n, kThreads, smem, s>>>(x, pre_mix, f, hc_scale, hc_base, norm_w, d, iters, eps,
                                                      norm_eps, g_hn, g_y, g_pre, g_pm, ws);

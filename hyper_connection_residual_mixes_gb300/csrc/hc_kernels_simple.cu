@@ -674,7 +674,7 @@ k_mixes_tiled(const uint16_t *__restrict__ x, const float *__restrict__ hc_fn,
               const float *__restrict__ hc_scale, const float *__restrict__ hc_base, int64_t n, int d,
               int iters, float eps, float norm_eps, float *__restrict__ pre_out,
               float *__restrict__ post_out, float *__restrict__ comb_out, float *__restrict__ mixes_out,
-              uint16_t *__restrict__ coef_rows, float *__restrict__ dots_out, int dots_stride) {
+              uint16_t *__restrict__ coef_rows) {
     using M = Mx<HC>;
     constexpr int MIX = M::MIX, NTW = M::NTW, COLS = M::COLS, CG = M::CG;
     extern __shared__ uint4 smem_u4[];
@@ -785,17 +785,6 @@ k_mixes_tiled(const uint16_t *__restrict__ x, const float *__restrict__ hc_fn,
         }
     }
     __syncthreads();
-    if (dots_out) {  // the raw projection x W^T (the backward's record), nothing else
-        for (int o = threadIdx.x; o < kMxTok * MIX; o += kMxThreads) {
-            const int tt = o / MIX, i = o % MIX;
-            if (t0 + tt >= n) continue;
-            float v = 0.0f;
-#pragma unroll
-            for (int w = 0; w < CG; ++w) v += red[(w * kMxTok + tt) * (MIX + 1) + i];
-            dots_out[(t0 + tt) * dots_stride + i] = v;
-        }
-        return;
-    }
     if (threadIdx.x < kMxTok && t0 + threadIdx.x < n) {
         const int tt = threadIdx.x;
         const int64_t t = t0 + tt;
@@ -848,30 +837,10 @@ cudaError_t launch_mixes_tiled_hc(const uint16_t *x, const float *hc_fn, const f
     const int64_t blocks = (n + kMxTok - 1) / kMxTok;
     k_mixes_tiled<HC><<<(unsigned)blocks, kMxThreads, smem, s>>>(x, hc_fn, hc_scale, hc_base, n, d, iters, eps,
                                                                  norm_eps, pre_out, post_out, comb_out, mixes_out,
-                                                                 coef_rows, nullptr, 0);
+                                                                 coef_rows);
     return cudaGetLastError();
 }
 
-cudaError_t launch_proj_tiled(const uint16_t *x, const float *hc_fn, int64_t n, int hc, int d, float *dots,
-                              int dots_stride, cudaStream_t s) {
-#define HC_PROJ(H)                                                                                        \
-    do {                                                                                                  \
-        const int smem = (int)Mx<H>::SMEM;                                                                \
-        cudaError_t e = cudaFuncSetAttribute(k_mixes_tiled<H>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem); \
-        if (e != cudaSuccess) return e;                                                                   \
-        k_mixes_tiled<H><<<(unsigned)((n + kMxTok - 1) / kMxTok), kMxThreads, smem, s>>>(                  \
-            x, hc_fn, nullptr, nullptr, n, d, 0, 0.0f, 0.0f, nullptr, nullptr, nullptr, nullptr, nullptr,   \
-            dots, dots_stride);                                                                           \
-        return cudaGetLastError();                                                                        \
-    } while (0)
-    switch (hc) {
-        case 2: HC_PROJ(2);
-        case 4: HC_PROJ(4);
-        case 8: HC_PROJ(8);
-        default: return cudaErrorInvalidValue;
-    }
-#undef HC_PROJ
-}
 
 template <int HC>
 cudaError_t launch_tokens_simple_hc(const uint16_t *x, const float *pre_mix, const uint16_t *f,

@@ -24,11 +24,6 @@ cudaError_t launch_pre_norm_mxfp8(const uint16_t *x, const float *pre_mix, const
 cudaError_t launch_post(const uint16_t *f, const uint16_t *residual, const float *post,
                         const float *comb, int64_t n, int hc, int d, uint16_t *y, cudaStream_t s);
 
-// The projection a = x hc_fn^T alone (no statistic, no split), on token tiles
-// (hc_kernels_simple.cu): a[t][i] at dots[t * dots_stride + i].
-cudaError_t launch_proj_tiled(const uint16_t *x, const float *hc_fn, int64_t n, int hc, int d, float *dots,
-                              int dots_stride, cudaStream_t s);
-
 // The projection a = x hc_fn^T alone on the tcgen05 tensor cores
 // (hc_proj_umma.cu): a[t][i] at out[t * out_stride + i].  `wsplit` is device
 // scratch of proj_umma_wsplit_bytes(hc, hc * d) bytes (16-byte aligned) for the
