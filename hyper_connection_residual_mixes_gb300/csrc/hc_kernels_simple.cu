@@ -853,10 +853,18 @@ cudaError_t launch_tokens_simple_hc(const uint16_t *x, const float *pre_mix, con
     const int64_t blocks = (n + kTok - 1) / kTok;
     cudaError_t e;
     if (n >= kTiledMinTokens) {
-        // a1-a3 on token tiles (hc_fn read once per 32 tokens), then a4-a6 per token from
-        // the coefficients parked in the y rows
-        e = launch_mixes_tiled_hc<HC>(x, hc_fn, hc_scale, hc_base, n, d, iters, eps, norm_eps, pre_out,
-                                      post_out, comb_out, mixes_out, f ? y : nullptr, s);
+        // a1-a3 on token tiles, then a4-a6 per token from the coefficients parked in
+        // the y rows.  For the side step at four and eight streams, the tcgen05
+        // kernel when its split weights fit the h_norm output (written only by the
+        // a4-a6 pass, after it); else the mma.sync kernel (hc_fn read once per 32
+        // tokens), which is also the faster one at two streams (measured at 8,192
+        // tokens x d = 5120: 154 against 193 us per side).
+        if (HC >= 4 && f && (size_t)n * (size_t)d * 2 >= proj_umma_wsplit_bytes(HC, (int64_t)HC * d))
+            e = launch_mixes_umma(x, hc_fn, hc_scale, hc_base, n, HC, d, iters, eps, norm_eps, h_norm, pre_out,
+                                  post_out, comb_out, mixes_out, y, s);
+        else
+            e = launch_mixes_tiled_hc<HC>(x, hc_fn, hc_scale, hc_base, n, d, iters, eps, norm_eps, pre_out,
+                                          post_out, comb_out, mixes_out, f ? y : nullptr, s);
         if (e != cudaSuccess || !f) return e;
         const size_t smem = (size_t)kTok * d * 2;
         e = cudaFuncSetAttribute(k_tokens_simple<true, HC, true>,

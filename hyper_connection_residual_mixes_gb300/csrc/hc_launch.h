@@ -31,6 +31,14 @@ cudaError_t launch_post(const uint16_t *f, const uint16_t *residual, const float
 size_t proj_umma_wsplit_bytes(int hc, int64_t K);
 cudaError_t launch_proj_umma(const uint16_t *x, const float *hc_fn, int64_t n, int hc, int d, uint16_t *wsplit,
                              float *out, int out_stride, cudaStream_t s);
+// a1-a3 on the same kernel: the projection, the sum of squares of x, the RMS
+// scale, split + Sinkhorn; pre / post / comb / mixes out (each may be null)
+// and post + comb at the start of each token's row of `coef_rows` (the y
+// output, row length hc * d bf16) for the a4-a6 pass.
+cudaError_t launch_mixes_umma(const uint16_t *x, const float *hc_fn, const float *hc_scale, const float *hc_base,
+                              int64_t n, int hc, int d, int iters, float eps, float norm_eps, uint16_t *wsplit,
+                              float *pre_out, float *post_out, float *comb_out, float *mixes_out,
+                              uint16_t *coef_rows, cudaStream_t s);
 
 // a1-a3 (write pre/post/comb, optional mixes) or, when `f` is non-null, the
 // whole side step a1-a6.  Simple path: a CTA owns a few whole tokens.

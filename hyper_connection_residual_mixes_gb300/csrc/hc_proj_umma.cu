@@ -27,6 +27,12 @@
 //                 adds; two accumulators alternate so that the MMAs go on
 //                 while one is drained.  Lane r of drain warp w holds token
 //                 32 w + r of the tile.
+//   The forward flavour (a1-a3 for hc_block_step) also has the drain warps
+//   read each stage's x rows for the token's sum of squares (one swizzled
+//   128-byte row per lane), and at the end of a tile each lane finishes its
+//   token: the RMS scale, split + Sinkhorn (Stream combination page,
+//   hc_split_sinkhorn), pre / post / comb (and the mixes) out, and post +
+//   comb parked at the start of the token's y row for the a4-a6 pass.
 // Every wait is bounded; on a timeout the CTA records the error, waits
 // (bounded) for its copies and MMAs in flight, frees its tensor memory and
 // returns.
@@ -139,11 +145,24 @@ __device__ __forceinline__ void mbar_wait_exit(uint32_t bar, uint32_t parity) {
     atomicOr(&g_device_error, kErrWaitTimeout);
 }
 
-template <int MIX>
+// What the forward flavour needs beyond the projection.
+struct FwdArgs {
+    const float *hc_scale, *hc_base;
+    int iters;
+    float eps, norm_eps;
+    float *pre_out, *post_out, *comb_out, *mixes_out;  // each may be null
+    float *coef_rows;                                 // post, comb at the start of row t (stride K / 2 floats)
+};
+
+constexpr int hc_of_mix(int mix) { return mix == 8 ? 2 : mix == 24 ? 4 : 8; }
+
+template <int MIX, bool kFwd>
 __global__ void __launch_bounds__(kThreads, 1)
 k_proj_umma(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w, int64_t n,
-            int K, int rows_per_cta, float *__restrict__ out, int out_stride) {
+            int K, int rows_per_cta, float *__restrict__ out, int out_stride, FwdArgs fa) {
     using C = Cfg<MIX>;
+    constexpr int HC = hc_of_mix(MIX);
+    static_assert((2 + HC) * HC == MIX, "mix rows of a stream count");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
     __shared__ __align__(8) uint64_t full_bar[kStages];
@@ -163,7 +182,7 @@ k_proj_umma(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(smem_u32(&full_bar[s]), 1);
-            mbar_init(smem_u32(&empty_bar[s]), 1);
+            mbar_init(smem_u32(&empty_bar[s]), kFwd ? 5 : 1);  // the MMAs (+ the four drain warps)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&acc_full[b]), 1);
@@ -248,12 +267,44 @@ k_proj_umma(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
         // drain warps: lane r of warp w holds token 32 w + r of the tile
         const uint32_t lane_base = tbase + ((uint32_t)(32 * warp) << 16);
         float run[MIX];
-        int c = 0;
+        int c = 0, it = 0;
         for (int tile = 0; tile < ntiles; ++tile) {
 #pragma unroll
             for (int i = 0; i < MIX; ++i) run[i] = 0.0f;
+            float ssx = 0.0f;
             bool ok = true;
             for (int ch = 0; ch < nch; ++ch, ++c) {
+                if constexpr (kFwd) {
+                    // this lane's x row of each stage of the chunk: 8 chunks of 16 bytes,
+                    // chunk j at position j ^ (row & 7) (the 128-byte swizzle)
+                    const int r = 32 * warp + lane;
+                    const int kb1 = (ch + 1) * kDrain < nkb ? (ch + 1) * kDrain : nkb;
+                    for (int kb = ch * kDrain; kb < kb1 && ok; ++kb, ++it) {
+                        const int slot = it % kStages;
+                        if (!(ok = mbar_wait_warp<false>(smem_u32(&full_bar[slot]), (uint32_t)(it / kStages) & 1u,
+                                                         &s_abort)))
+                            break;
+                        const uint8_t *row = smem_raw + (sbase - smem_u32(smem_raw)) + slot * C::kStageBytes + r * 128;
+                        f32x2 acc2 = f2_dup(0.0f);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const uint4 v = *reinterpret_cast<const uint4 *>(row + ((j ^ (r & 7)) << 4));
+                            const f32x2 a = f2_from_bf16x2(v.x), b2 = f2_from_bf16x2(v.y);
+                            const f32x2 c2 = f2_from_bf16x2(v.z), d2 = f2_from_bf16x2(v.w);
+                            acc2 = f2_fma(a, a, acc2);
+                            acc2 = f2_fma(b2, b2, acc2);
+                            acc2 = f2_fma(c2, c2, acc2);
+                            acc2 = f2_fma(d2, d2, acc2);
+                        }
+                        ssx += f2_hsum(acc2);
+                        // the loaded values are used before the slot is handed back
+                        asm volatile("" ::"f"(ssx));
+                        __threadfence_block();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(smem_u32(&empty_bar[slot]));
+                    }
+                    if (!ok) break;
+                }
                 const int b = c & 1;
                 if (!(ok = mbar_wait_warp<false>(smem_u32(&acc_full[b]), (uint32_t)(c >> 1) & 1u, &s_abort)))
                     break;
@@ -274,10 +325,39 @@ k_proj_umma(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             }
             if (!ok) break;
             const int64_t row = r0 + (int64_t)tile * kM + 32 * warp + lane;
-            if (row < r1) {
-                float *o = out + row * (int64_t)out_stride;
+            if constexpr (!kFwd) {
+                if (row < r1) {
+                    float *o = out + row * (int64_t)out_stride;
 #pragma unroll
-                for (int i = 0; i < MIX; ++i) o[i] = run[i];
+                    for (int i = 0; i < MIX; ++i) o[i] = run[i];
+                }
+            } else if (row < r1) {
+                const float rsx = rsqrtf(ssx / (float)K + fa.norm_eps);
+#pragma unroll
+                for (int i = 0; i < MIX; ++i) run[i] *= rsx;
+                float pr[HC], po[HC], cm[HC * HC];
+                split_sinkhorn_token_hc<HC>(run, __ldg(fa.hc_scale), __ldg(fa.hc_scale + 1), __ldg(fa.hc_scale + 2),
+                                            fa.hc_base, fa.iters, fa.eps, pr, po, cm);
+#pragma unroll
+                for (int k = 0; k < HC; ++k) {
+                    if (fa.pre_out) fa.pre_out[row * HC + k] = pr[k];
+                    if (fa.post_out) fa.post_out[row * HC + k] = po[k];
+                }
+                if (fa.comb_out) {
+#pragma unroll
+                    for (int i = 0; i < HC * HC; ++i) fa.comb_out[row * HC * HC + i] = cm[i];
+                }
+                if (fa.mixes_out) {
+#pragma unroll
+                    for (int i = 0; i < MIX; ++i) fa.mixes_out[row * MIX + i] = run[i];
+                }
+                if (fa.coef_rows) {
+                    float *dst = fa.coef_rows + row * (int64_t)(K / 2);
+#pragma unroll
+                    for (int k = 0; k < HC; ++k) dst[k] = po[k];
+#pragma unroll
+                    for (int i = 0; i < HC * HC; ++i) dst[HC + i] = cm[i];
+                }
             }
         }
     }
@@ -331,9 +411,9 @@ int sm_count() {
     return count[dev];
 }
 
-template <int MIX>
+template <int MIX, bool kFwd>
 cudaError_t proj_umma_impl(const uint16_t *x, const float *hc_fn, int64_t n, int64_t K, uint16_t *wsplit,
-                           float *out, int out_stride, cudaStream_t s) {
+                           float *out, int out_stride, const pu::FwdArgs &fa, cudaStream_t s) {
     using C = pu::Cfg<MIX>;
     {
         const int64_t blocks = ((int64_t)MIX * K + 255) / 256;
@@ -342,18 +422,16 @@ cudaError_t proj_umma_impl(const uint16_t *x, const float *hc_fn, int64_t n, int
     CUtensorMap tmx, tmw;
     if (!proj_tmap(&tmx, x, n, K, pu::kGroup) || !proj_tmap(&tmw, wsplit, C::kN, K, C::kN))
         return cudaErrorInvalidValue;
-    // contiguous token ranges, multiples of 32 rows, at least 64 tokens each,
-    // about one range per CTA slot
+    // contiguous token ranges of whole 32-row boxes, about one range per CTA slot
     const int64_t slots = (int64_t)sm_count() * C::kCtasPerSm;
     int64_t per = (n + slots - 1) / slots;
     per = (per + pu::kGroup - 1) / pu::kGroup * pu::kGroup;
-    if (per < 64) per = 64;
     const int64_t grid = (n + per - 1) / per;
-    cudaError_t e = cudaFuncSetAttribute(pu::k_proj_umma<MIX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(pu::k_proj_umma<MIX, kFwd>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::kSmem);
     if (e != cudaSuccess) return e;
-    pu::k_proj_umma<MIX><<<(unsigned)grid, pu::kThreads, C::kSmem, s>>>(tmx, tmw, n, (int)K, (int)per, out,
-                                                                        out_stride);
+    pu::k_proj_umma<MIX, kFwd><<<(unsigned)grid, pu::kThreads, C::kSmem, s>>>(tmx, tmw, n, (int)K, (int)per, out,
+                                                                              out_stride, fa);
     return cudaGetLastError();
 }
 
@@ -368,10 +446,26 @@ size_t proj_umma_wsplit_bytes(int hc, int64_t K) {
 cudaError_t launch_proj_umma(const uint16_t *x, const float *hc_fn, int64_t n, int hc, int d, uint16_t *wsplit,
                              float *out, int out_stride, cudaStream_t s) {
     const int64_t K = (int64_t)hc * d;
+    const pu::FwdArgs none{};
     switch (hc) {
-        case 2: return proj_umma_impl<8>(x, hc_fn, n, K, wsplit, out, out_stride, s);
-        case 4: return proj_umma_impl<24>(x, hc_fn, n, K, wsplit, out, out_stride, s);
-        case 8: return proj_umma_impl<80>(x, hc_fn, n, K, wsplit, out, out_stride, s);
+        case 2: return proj_umma_impl<8, false>(x, hc_fn, n, K, wsplit, out, out_stride, none, s);
+        case 4: return proj_umma_impl<24, false>(x, hc_fn, n, K, wsplit, out, out_stride, none, s);
+        case 8: return proj_umma_impl<80, false>(x, hc_fn, n, K, wsplit, out, out_stride, none, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_mixes_umma(const uint16_t *x, const float *hc_fn, const float *hc_scale, const float *hc_base,
+                              int64_t n, int hc, int d, int iters, float eps, float norm_eps, uint16_t *wsplit,
+                              float *pre_out, float *post_out, float *comb_out, float *mixes_out,
+                              uint16_t *coef_rows, cudaStream_t s) {
+    const int64_t K = (int64_t)hc * d;
+    const pu::FwdArgs fa{hc_scale, hc_base, iters, eps, norm_eps, pre_out, post_out, comb_out, mixes_out,
+                         reinterpret_cast<float *>(coef_rows)};
+    switch (hc) {
+        case 2: return proj_umma_impl<8, true>(x, hc_fn, n, K, wsplit, nullptr, 0, fa, s);
+        case 4: return proj_umma_impl<24, true>(x, hc_fn, n, K, wsplit, nullptr, 0, fa, s);
+        case 8: return proj_umma_impl<80, true>(x, hc_fn, n, K, wsplit, nullptr, 0, fa, s);
         default: return cudaErrorInvalidValue;
     }
 }
