@@ -26,6 +26,7 @@
 // The partial sums are then added over the blocks in a fixed order, so every
 // result is deterministic (no atomics).
 #include <cuda.h>
+#include <cuda_fp16.h>
 
 #include "hc_device.cuh"
 #include "hc_launch.h"
@@ -41,19 +42,23 @@ constexpr int kTokBlock = 1024;  // tokens per partial sum of a parameter gradie
 
 // The per-token record in the workspace (floats).  [0, kStaged) is what
 // k_bwd_gx stages for each token; [kA, kA + 24) comes from the projection.
-constexpr int kWs = 140;
-constexpr int kGa = 0;      // g_a[24]: the gradient of the projection a
-constexpr int kPost = 24;   // post[4]
-constexpr int kComb = 28;   // comb[16]
-constexpr int kPm = 44;     // pre_mix[4]
-constexpr int kRs = 48;     // rs_h = 1 / RMS(h)
-constexpr int kCr = 49;     // the statistic's coefficient of x in g_x
-constexpr int kK3 = 50;     // rs_h^3 / d * sum(h w g_hn)
-constexpr int kGz = 52;     // g_z[24]: the gradient of the pre-activations (= g_hc_base terms)
-constexpr int kGzm = 76;    // gzm[3]: the g_hc_scale terms
-constexpr int kGaP = 80;    // g_a as three bf16 parts hi, mid, lo: 72 bf16 (36 floats), part-major
-constexpr int kStaged = 116;
-constexpr int kA = 116;     // a[24] (the projection)
+// g_a, the gradient of the projection a, is kept only in the two split forms
+// the tensor cores of k_bwd_gx read.
+constexpr int kWs = 156;
+constexpr int kPost = 0;    // post[4]
+constexpr int kComb = 4;    // comb[16]
+constexpr int kPm = 20;     // pre_mix[4]
+constexpr int kRs = 24;     // rs_h = 1 / RMS(h)
+constexpr int kCr = 25;     // the statistic's coefficient of x in g_x
+constexpr int kK3 = 26;     // rs_h^3 / d * sum(h w g_hn)
+constexpr int kGs = 27;     // 2^e: g_a = 2^e * (h1 + h2) below
+constexpr int kGaP = 28;    // g_a as three bf16 parts hi, mid, lo: 72 bf16 (36 floats), part-major
+constexpr int kGaH = 64;    // g_a / 2^e as fp16 h1 + h2 laid out for the W contraction:
+                            // [h1 (24), h1 (24), h2 (24), 0 (8)], 80 fp16 (40 floats)
+constexpr int kStaged = 104;
+constexpr int kGz = 104;    // g_z[24]: the gradient of the pre-activations (= g_hc_base terms)
+constexpr int kGzm = 128;   // gzm[3]: the g_hc_scale terms (right after g_z)
+constexpr int kA = 132;     // a[24] (the projection)
 constexpr int kSmall = 32;  // partial sums per block for hc_base (24) and hc_scale (3)
 
 constexpr int kTokWarps = 4;    // tokens (one warp each) per CTA of k_bwd_token
@@ -63,6 +68,11 @@ constexpr int kGxTile = 16;     // tokens per staged tile of k_bwd_gx
 constexpr int kGxStages = 3;
 
 __device__ __forceinline__ float sigm(float z) { return 1.0f / (1.0f + expf(-z)); }
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
 
 __device__ __forceinline__ void unpack4(const uint2 &v, float (&o)[4]) {
     o[0] = bf16lo(v.x);
@@ -245,9 +255,28 @@ k_bwd_token(const uint16_t *__restrict__ x, const float *__restrict__ pre_mix,
     z1 = warp_sum(z1);
     z2 = warp_sum(z2);
     gr = warp_sum(gr);
+    // g_a = 2^e (h1 + h2) in fp16 for the W contraction of k_bwd_gx: 2^-e brings
+    // the token's largest |g_a| into [2^13, 2^14), well inside fp16's normal
+    // range, so h1 + h2 carries g_a to about 2^-22 of itself
+    const float ga = gm * r;
+    const float gmax = warp_max(live ? fabsf(ga) : 0.0f);
+    int se = 13 - (int)((__float_as_uint(gmax) >> 23) & 0xffu) + 127;  // 2^se scales g_a up
+    se = se < -126 ? -126 : (se > 126 ? 126 : se);
+    const float up = __uint_as_float((uint32_t)(se + 127) << 23);
+    {
+        const float as = live ? ga * up : 0.0f;
+        const __half h1 = __float2half_rn(as);
+        const __half h2 = __float2half_rn(as - __half2float(h1));
+        __half *gh = reinterpret_cast<__half *>(wt + kGaH);
+        if (live) {
+            gh[i] = h1;
+            gh[kMix + i] = h1;
+            gh[2 * kMix + i] = h2;
+        } else {
+            gh[3 * kMix + (lane - kMix)] = __float2half_rn(0.0f);  // lanes 24-31: the 8 zero columns
+        }
+    }
     if (live) {
-        const float ga = gm * r;
-        wt[kGa + i] = ga;
         wt[kGz + i] = gz;
         // the three bf16 parts of g_a for the bf16 MMAs of k_bwd_gx: ga = hi + mid + lo to ~2^-24
         const uint32_t hi = pack_bf16x2(ga, 0.0f) & 0xffffu;
@@ -267,6 +296,7 @@ k_bwd_token(const uint16_t *__restrict__ x, const float *__restrict__ pre_mix,
         wt[kRs] = rs;
         wt[kCr] = -gr * r * r * r / (float)K;  // the statistic's term: cr * x_k
         wt[kK3] = k3;
+        wt[kGs] = __uint_as_float((uint32_t)(127 - se) << 23);
     }
 }
 
@@ -277,27 +307,30 @@ k_bwd_token(const uint16_t *__restrict__ x, const float *__restrict__ pre_mix,
 //   g_x  = pm_s g_h + cr x_s + sum_k comb_sk g_y_k + sum_i g_a_i W[i][s, c]
 //   g_f  = sum_k post_k g_y_k
 // and summed over the block: g_hc_fn[i][s, c] += g_a_i x_s, g_norm_w[c] +=
-// h_c rs_h g_hn.  The CTAs of column block 0 also sum the block's g_z and gzm
-// (the hc_base and hc_scale terms).
+// h_c rs_h g_hn.  (The block sums of g_z and gzm, the hc_base and hc_scale
+// terms, are k_bwd_gz_partial's.)
 // Tiles of kGxTile = 16 tokens (x, g_y, g_hn for the CTA's columns and the
 // token records) are staged through a ring of bulk copies, one per staged
 // row (160 per tile), each stage completing on its mbarrier.  Warp w owns the
 // columns c0 + 8w .. +7 of all four streams.  The two contractions over the
-// 24 mix rows run on the tensor cores (mma m16n8k8, tf32 split in hi + lo):
-//   g_a (16 tokens x 24) . W (24 x the warp's 32 columns), n-tile = stream;
-//   g_a^T (24, padded to 32, x 16 tokens) . x (16 tokens x 32 columns),
-//   accumulated over the block in registers.
-// The rest is per (token, column) in the accumulator layout: lane (g, q) =
-// (lane / 4, lane % 4) holds tokens g and g + 8, columns c0 + 8w + 2q and +1,
-// for the four streams.  The staged rows are padded so that these loads hit
-// distinct shared-memory banks.  Rows past the block are not copied: they
-// keep finite values (the ring is zeroed once), their g_a is masked to zero in
-// the g_hc_fn sum, and their outputs are not written.
+// 24 mix rows run on the tensor cores (mma.sync m16n8k16):
+//   g_a (16 tokens x 24) . W (24 x the warp's 32 columns), n-tile = stream,
+//   in fp16: both operands scaled by powers of two and split in two fp16
+//   parts, the three cross terms laid along one K axis of 80;
+//   x^T (the warp's 32 columns x 16 tokens) . g_a (16 tokens x 24), in bf16:
+//   x exact, g_a in three bf16 parts, accumulated over the block in registers.
+// The rest is per (token, column) in the accumulator layout of the first:
+// lane (g, q) = (lane / 4, lane % 4) holds tokens g and g + 8, columns
+// c0 + 8w + 2q and +1, for the four streams.  The staged rows are padded so
+// that these loads hit distinct shared-memory banks.  Rows past the block are
+// not copied: they keep finite values (the ring is zeroed once), their g_a is
+// masked to zero in the g_hc_fn sum, and their outputs are not written.
 constexpr int kXRow = kHC * kGxCols + 8;   // bf16 per token row of the x tile
 constexpr int kGyRow = kHC * kGxCols + 8;  // floats per token row of the g_y tile
 constexpr int kGhRow = kGxCols + 8;        // floats per token row of the g_hn tile
-constexpr int kRecRow = kStaged + 8;       // floats per staged token record (496 bytes: ldmatrix rows
-                                           // of 8 records fall in distinct 16-byte bank groups)
+constexpr int kRecRow = kStaged + 4;       // floats per staged token record (432 bytes, an odd number
+                                           // of 16-byte units: ldmatrix rows of 8 records fall in
+                                           // distinct 16-byte bank groups)
 struct GxStage {
     uint16_t x[kGxTile][kXRow];
     float gy[kGxTile][kGyRow];
@@ -315,7 +348,7 @@ k_bwd_gx(const uint16_t *__restrict__ x, const float *__restrict__ hc_fn,
          const float *__restrict__ norm_w, const float *__restrict__ g_hn,
          const float *__restrict__ g_y, const float *__restrict__ ws, int64_t n, int d,
          float *__restrict__ g_x, float *__restrict__ g_f, float *__restrict__ part_fn,
-         float *__restrict__ part_w, float *__restrict__ part_s) {
+         float *__restrict__ part_w) {
     extern __shared__ uint4 smem_u4[];
     GxStage *stg = reinterpret_cast<GxStage *>(smem_u4);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -326,7 +359,6 @@ k_bwd_gx(const uint16_t *__restrict__ x, const float *__restrict__ hc_fn,
     const int64_t t0 = (int64_t)blockIdx.y * kTokBlock;
     const int64_t t1 = (t0 + kTokBlock < n) ? t0 + kTokBlock : n;
     const int ntiles = (int)((t1 - t0 + kGxTile - 1) / kGxTile);
-    const bool small = blockIdx.x == 0;
 
     __shared__ __align__(8) uint64_t full_bar[kGxStages];
     __shared__ __align__(8) uint64_t empty_bar[kGxStages];  // one arrive per warp when done with a tile
@@ -381,17 +413,49 @@ k_bwd_gx(const uint16_t *__restrict__ x, const float *__restrict__ hc_fn,
         }
     };
 
-    // W fragments (B of the first contraction): stream nt, mix rows 8ks + q (+4),
-    // column c0 + cw + g, as tf32 hi + lo
-    uint32_t bh[kHC][3][2], bl[kHC][3][2];
+    // W fragments (B of the first contraction, fp16 m16n8k16): W / 2^ew = w1 + w2
+    // in fp16, 2^-ew bringing the CTA's largest |W| into [2^13, 2^14); the K
+    // axis (80) runs over [w1 (24 mixes), w2 (24), w1 (24), 0 (8)] against the
+    // record's [h1, h1, h2, 0], so one pass takes h1 w1 + h1 w2 + h2 w1.
+    // Lane (g, q): column c0 + cw + g of stream nt, K rows 16 ks + 2q (+1, +8, +9).
+    __shared__ float s_wmax[kWarps];
+    float wmax = 0.0f;
+#pragma unroll 4
+    for (int k = threadIdx.x; k < kMix * kHC * kGxCols; k += kThreads) {  // each element once, coalesced
+        const int i = k / (kHC * kGxCols), col = k % (kHC * kGxCols);
+        wmax = fmaxf(wmax, fabsf(__ldg(hc_fn + (int64_t)i * K + (int64_t)(col / kGxCols) * d + c0 + col % kGxCols)));
+    }
+    wmax = warp_max(wmax);
+    if (lane == 0) s_wmax[warp] = wmax;
+    __syncthreads();
+    wmax = s_wmax[0];
 #pragma unroll
-    for (int nt = 0; nt < kHC; ++nt)
+    for (int w = 1; w < kWarps; ++w) wmax = fmaxf(wmax, s_wmax[w]);
+    int sw = 13 - (int)((__float_as_uint(wmax) >> 23) & 0xffu) + 127;
+    sw = sw < -126 ? -126 : (sw > 126 ? 126 : sw);
+    const float w_up = __uint_as_float((uint32_t)(sw + 127) << 23);
+    const float w_down = __uint_as_float((uint32_t)(127 - sw) << 23);
+    uint32_t bw[kHC][5][2];
 #pragma unroll
-        for (int ks = 0; ks < 3; ++ks)
+    for (int nt = 0; nt < kHC; ++nt) {
+        const float *wc = hc_fn + (int64_t)nt * d + c0 + cw + g;
+        auto part = [&](int k) -> __half {  // row k of the concatenated K axis
+            if (k >= 3 * kMix) return __float2half_rn(0.0f);
+            const float ws_ = __ldg(wc + (int64_t)(k % kMix) * K) * w_up;
+            const __half w1 = __float2half_rn(ws_);
+            return (k >= kMix && k < 2 * kMix) ? __float2half_rn(ws_ - __half2float(w1)) : w1;
+        };
 #pragma unroll
-            for (int h = 0; h < 2; ++h)
-                tf32_split(__ldg(hc_fn + (8 * ks + q + 4 * h) * K + (int64_t)nt * d + c0 + cw + g),
-                           bh[nt][ks][h], bl[nt][ks][h]);
+        for (int ks = 0; ks < 5; ++ks)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const __half2 v = __halves2half2(part(16 * ks + 2 * q + 8 * h), part(16 * ks + 2 * q + 8 * h + 1));
+                bw[nt][ks][h] = *reinterpret_cast<const uint32_t *>(&v);
+            }
+    }
+    // A fragments of the W contraction (ldmatrix, not transposed): lane l gives
+    // token (l & 7) + 8 ((l >> 3) & 1), K columns 8 (l >> 4) .. + 7 of the step
+    const uint32_t ah_off = (uint32_t)((((lane & 7) + 8 * ((lane >> 3) & 1)) * kRecRow + kGaH) * 4 + 16 * (lane >> 4));
     // g_hc_fn partials (the second contraction, bf16 m16n8k16): accumulator row
     // g (+8) of m-tile mt = column c0 + cw + g of stream 2mt (2mt + 1), column
     // 2q (+1) of n-tile nt = mix row 8nt + 2q (+1)
@@ -417,7 +481,7 @@ k_bwd_gx(const uint16_t *__restrict__ x, const float *__restrict__ hc_fn,
     }
     const int cc0 = c0 + cw + 2 * q;         // the lane's two columns of d: cc0, cc0 + 1
     const float wn0 = __ldg(norm_w + cc0), wn1 = __ldg(norm_w + cc0 + 1);
-    float gw0 = 0.0f, gw1 = 0.0f, sm = 0.0f;
+    float gw0 = 0.0f, gw1 = 0.0f;
 
     // One tile ahead: tile it + 1 goes into the slot of tile it + 1 - kGxStages,
     // which every warp released at least one tile ago, so warps drift apart by
@@ -429,30 +493,31 @@ k_bwd_gx(const uint16_t *__restrict__ x, const float *__restrict__ hc_fn,
         const GxStage &S = stg[it % kGxStages];
         const int64_t tb = t0 + (int64_t)it * kGxTile;
         const int cnt = (int)((t1 - tb < kGxTile) ? t1 - tb : kGxTile);
-        if (small && threadIdx.x < kMix + 3)
-            for (int u = 0; u < cnt; ++u) sm += S.rec[u][kGz + threadIdx.x];
-
-        // (1) D[t][s, c] = sum_i g_a[t][i] W[i][s, c]; tokens g, g + 8
+        // (1) D[t][s, c] = sum_i g_a[t][i] W[i][s, c]; tokens g, g + 8.  Scaled
+        // operands: D = 2^e_t 2^ew (A_s . B_s), both factors powers of two.
         float dA[kHC][4];
 #pragma unroll
         for (int nt = 0; nt < kHC; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) dA[nt][e] = 0.0f;
+        {
+            const uint32_t ra = smem_u32(&S.rec[0][0]) + ah_off;
 #pragma unroll
-        for (int ks = 0; ks < 3; ++ks) {
-            uint32_t ah[4], al[4];
-            tf32_split(S.rec[g][kGa + 8 * ks + q], ah[0], al[0]);
-            tf32_split(S.rec[g + 8][kGa + 8 * ks + q], ah[1], al[1]);
-            tf32_split(S.rec[g][kGa + 8 * ks + q + 4], ah[2], al[2]);
-            tf32_split(S.rec[g + 8][kGa + 8 * ks + q + 4], ah[3], al[3]);
-            // term by term over the four streams, so that consecutive MMAs feed
-            // different accumulators (each accumulator sees the same order)
+            for (int ks = 0; ks < 5; ++ks) {
+                uint32_t a0, a1, a2, a3;
+                ldmatrix_x4(ra + (uint32_t)(32 * ks), a0, a1, a2, a3);
 #pragma unroll
-            for (int nt = 0; nt < kHC; ++nt) mma_tf32(dA[nt], al, bh[nt][ks][0], bh[nt][ks][1]);
+                for (int nt = 0; nt < kHC; ++nt)
+                    mma_f16_16816(dA[nt], a0, a1, a2, a3, bw[nt][ks][0], bw[nt][ks][1]);
+            }
+            const float f0 = S.rec[g][kGs] * w_down, f1 = S.rec[g + 8][kGs] * w_down;
 #pragma unroll
-            for (int nt = 0; nt < kHC; ++nt) mma_tf32(dA[nt], ah, bl[nt][ks][0], bl[nt][ks][1]);
-#pragma unroll
-            for (int nt = 0; nt < kHC; ++nt) mma_tf32(dA[nt], ah, bh[nt][ks][0], bh[nt][ks][1]);
+            for (int nt = 0; nt < kHC; ++nt) {
+                dA[nt][0] *= f0;
+                dA[nt][1] *= f0;
+                dA[nt][2] *= f1;
+                dA[nt][3] *= f1;
+            }
         }
 
         // (2) g_hc_fn[i][s, c] += sum_t g_a[t][i] x[t][s][c]: bf16 MMAs, x exact,
@@ -567,7 +632,6 @@ k_bwd_gx(const uint16_t *__restrict__ x, const float *__restrict__ hc_fn,
         gw1 += __shfl_xor_sync(0xffffffffu, gw1, m);
     }
     if (g == 0) *reinterpret_cast<float2 *>(part_w + (int64_t)blockIdx.y * d + cc0) = make_float2(gw0, gw1);
-    if (small && threadIdx.x < kMix + 3) part_s[(int64_t)blockIdx.y * kSmall + threadIdx.x] = sm;
 }
 
 // out[j] = sum_b part[b][j], blocks in order.
@@ -578,6 +642,30 @@ __global__ void k_bwd_sum_blocks(const float *__restrict__ part, int blocks, int
     float s = 0.0f;
     for (int b = 0; b < blocks; ++b) s += part[(int64_t)b * len + j];
     out[j] = s;
+}
+
+// The block partials of the g_hc_base and g_hc_scale terms: thread (w, j)
+// sums field j of tokens 128 w .. 128 w + 127 of block b; the eight warp sums
+// are then added in warp order.
+__global__ void __launch_bounds__(kThreads)
+k_bwd_gz_partial(const float *__restrict__ ws, int64_t n, float *__restrict__ part_s) {
+    __shared__ float red[kWarps][32];
+    const int warp = threadIdx.x >> 5, j = threadIdx.x & 31;
+    const int64_t t0 = (int64_t)blockIdx.x * kTokBlock + (int64_t)warp * (kTokBlock / kWarps);
+    float s = 0.0f;
+    if (j < kMix + 3) {
+#pragma unroll 8
+        for (int u = 0; u < kTokBlock / kWarps; ++u)
+            if (t0 + u < n) s += ws[(t0 + u) * kWs + kGz + j];
+    }
+    red[warp][j] = s;
+    __syncthreads();
+    if (warp == 0 && j < kMix + 3) {
+        float v = red[0][j];
+#pragma unroll
+        for (int w = 1; w < kWarps; ++w) v += red[w][j];
+        part_s[(int64_t)blockIdx.x * kSmall + j] = v;
+    }
 }
 
 // g_hc_base[i] = sum_b part_s[b][i], g_hc_scale[j] = sum_b part_s[b][24 + j],
@@ -673,9 +761,10 @@ cudaError_t launch_block_step_backward(const uint16_t *x, const float *pre_mix, 
         cudaSuccess)
         return e;
     k_bwd_gx<<<dim3((unsigned)(d / kGxCols), (unsigned)blocks), kThreads, kGxSmem, s>>>(
-        x, hc_fn, norm_w, g_hn, g_y, ws, n, d, g_x, g_f, part_fn, part_w, part_s);
+        x, hc_fn, norm_w, g_hn, g_y, ws, n, d, g_x, g_f, part_fn, part_w);
     k_bwd_sum_blocks<<<(unsigned)((kMix * K + 255) / 256), 256, 0, s>>>(part_fn, blocks, kMix * K, g_fn);
     k_bwd_sum_blocks<<<(unsigned)((d + 255) / 256), 256, 0, s>>>(part_w, blocks, d, g_w);
+    k_bwd_gz_partial<<<(unsigned)blocks, kThreads, 0, s>>>(ws, n, part_s);
     k_bwd_small<<<1, 32, 0, s>>>(part_s, blocks, g_base, g_scale);
     return cudaGetLastError();
 }

@@ -185,8 +185,8 @@ hc_status hc_block_step(const uint16_t *x, const float *pre_mix, const uint16_t 
  *   workspace: device scratch of at least
  *   hc_block_step_backward_workspace_bytes(n, hc, d) bytes, 16-byte
  *   aligned, owned by the caller (the library allocates nothing); at hc = 4
- *   that is 4 * (140 n + B (24 * 4d + d + 32) + 160 d) bytes, B = ceil(n / 1024):
- *   a 140-float record per token, then per block of 1,024 tokens the partial
+ *   that is 4 * (156 n + B (24 * 4d + d + 32) + 160 d) bytes, B = ceil(n / 1024):
+ *   a 156-float record per token, then per block of 1,024 tokens the partial
  *   sums of g_hc_fn, g_norm_w and g_hc_base / g_hc_scale, then hc_fn split
  *   into three bf16 parts for the tensor cores (80 rows of 4d bf16)
  * Results are deterministic: the token sums run in a fixed order.
@@ -198,7 +198,7 @@ size_t hc_block_step_backward_workspace_bytes(int64_t n, int hc, int d);
  * hc_block_step_backward without a caller workspace: the scratch is a fixed
  * 64 MiB array in device memory that is part of the library's module, so the
  * call allocates nothing.  hc = 4 only.  Inputs whose workspace would not fit
- * (for d = 5120, more than 25,294 tokens) return HC_ERR_UNSUPPORTED.  There is one such
+ * (for d = 5120, more than 24,576 tokens) return HC_ERR_UNSUPPORTED.  There is one such
  * array per process and device: calls must not overlap in time (for
  * instance, issue them on one stream).  Results equal
  * hc_block_step_backward's bit for bit.
