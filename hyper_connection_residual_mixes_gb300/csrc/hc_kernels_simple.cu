@@ -439,8 +439,10 @@ constexpr int64_t kTiledMinTokens = 128;
 template <int HC>
 __host__ __device__ constexpr int tok_per_cta() { return HC <= 4 ? 4 : 1; }
 
+// The a4-a6 flavour (kCoefIn) keeps at most 128 registers, so that two CTAs
+// share an SM: at eight streams one CTA per SM left too few warps in flight.
 template <bool kFull, int HC, bool kCoefIn = false>
-__global__ void __launch_bounds__(kTokThreads)
+__global__ void __launch_bounds__(kTokThreads, kCoefIn ? 2 : 1)
 k_tokens_simple(const uint16_t *__restrict__ x, const float *__restrict__ pre_mix,
                 const uint16_t *__restrict__ f, const float *__restrict__ hc_fn,
                 const float *__restrict__ hc_scale, const float *__restrict__ hc_base,
@@ -566,43 +568,61 @@ k_tokens_simple(const uint16_t *__restrict__ x, const float *__restrict__ pre_mi
     for (int u = 0; u < kTok; ++u) {
         if (u >= ntok) break;
         const int64_t t = t0 + u;
-        float pm[HC];
+        // packed fp32 pairs (adjacent columns), each lane rounded as the scalar
+        // instruction would be
+        f32x2 pm2[HC];
 #pragma unroll
-        for (int s = 0; s < HC; ++s) pm[s] = __ldg(pre_mix + t * HC + s);
+        for (int s = 0; s < HC; ++s) pm2[s] = f2_dup(__ldg(pre_mix + t * HC + s));
         const uint4 *xs = reinterpret_cast<const uint4 *>(x + t * K);
         const uint4 *fs = reinterpret_cast<const uint4 *>(f + t * d);
         uint4 *ys = reinterpret_cast<uint4 *>(y + t * K);
+        f32x2 hs2 = f2_dup(0.0f);
         for (int c = threadIdx.x; c < d8; c += kTokThreads) {
-            float fv[8], xv[HC][8];
-            unpack8(__ldg(fs + c), fv);
+            f32x2 fv[4], xv[HC][4];
+            {
+                const uint4 fr = __ldg(fs + c);
+                fv[0] = f2_from_bf16x2(fr.x); fv[1] = f2_from_bf16x2(fr.y);
+                fv[2] = f2_from_bf16x2(fr.z); fv[3] = f2_from_bf16x2(fr.w);
+            }
 #pragma unroll
-            for (int j = 0; j < HC; ++j) unpack8(__ldg(xs + j * d8 + c), xv[j]);
+            for (int j = 0; j < HC; ++j) {
+                const uint4 xr = __ldg(xs + j * d8 + c);
+                xv[j][0] = f2_from_bf16x2(xr.x); xv[j][1] = f2_from_bf16x2(xr.y);
+                xv[j][2] = f2_from_bf16x2(xr.z); xv[j][3] = f2_from_bf16x2(xr.w);
+            }
 #pragma unroll
             for (int k = 0; k < HC; ++k) {
-                float o[8];
+                const f32x2 ck = f2_dup(coef[u][k]);
+                f32x2 o[4];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    float a = coef[u][k] * fv[i];
+                for (int p = 0; p < 4; ++p) o[p] = f2_mul(ck, fv[p]);
 #pragma unroll
-                    for (int j = 0; j < HC; ++j) a = fmaf(coef[u][HC + j * HC + k], xv[j][i], a);
-                    o[i] = a;
+                for (int j = 0; j < HC; ++j) {
+                    const f32x2 cjk = f2_dup(coef[u][HC + j * HC + k]);
+#pragma unroll
+                    for (int p = 0; p < 4; ++p) o[p] = f2_fma(cjk, xv[j][p], o[p]);
                 }
-                ys[k * d8 + c] = pack8(o);
+                ys[k * d8 + c] = make_uint4(f2_to_bf16x2(o[0]), f2_to_bf16x2(o[1]), f2_to_bf16x2(o[2]),
+                                            f2_to_bf16x2(o[3]));
             }
-            float h[8];
+            f32x2 h[4];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                h[i] = pm[0] * xv[0][i];
+            for (int p = 0; p < 4; ++p) {
+                h[p] = f2_mul(pm2[0], xv[0][p]);
 #pragma unroll
-                for (int s2 = 1; s2 < HC; ++s2) h[i] = fmaf(pm[s2], xv[s2][i], h[i]);
+                for (int s2 = 1; s2 < HC; ++s2) h[p] = f2_fma(pm2[s2], xv[s2][p], h[p]);
             }
-            const uint4 hb = pack8(h);
+            const uint4 hb = make_uint4(f2_to_bf16x2(h[0]), f2_to_bf16x2(h[1]), f2_to_bf16x2(h[2]),
+                                        f2_to_bf16x2(h[3]));
             hbuf[u * d8 + c] = hb;
-            float r8[8];
-            unpack8(hb, r8);
+            const uint32_t hw[4] = {hb.x, hb.y, hb.z, hb.w};
 #pragma unroll
-            for (int i = 0; i < 8; ++i) hs[u] = fmaf(r8[i], r8[i], hs[u]);
+            for (int p = 0; p < 4; ++p) {
+                const f32x2 r = f2_from_bf16x2(hw[p]);
+                hs2 = f2_fma(r, r, hs2);
+            }
         }
+        hs[u] = f2_hsum(hs2);
     }
 #pragma unroll
     for (int u = 0; u < kTok; ++u) {
