@@ -152,6 +152,7 @@ struct FwdArgs {
     float eps, norm_eps;
     float *pre_out, *post_out, *comb_out, *mixes_out;  // each may be null
     float *coef_rows;                                 // post, comb at the start of row t (stride K / 2 floats)
+    int part_off;                                     // K split: partial sums at this float of row t
 };
 
 constexpr int hc_of_mix(int mix) { return mix == 8 ? 2 : mix == 24 ? 4 : 8; }
@@ -176,7 +177,11 @@ k_proj_umma(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
     const int64_t r0 = (int64_t)blockIdx.x * rows_per_cta;
     const int64_t r1 = (r0 + rows_per_cta < n) ? r0 + rows_per_cta : n;
     const int ntiles = r1 > r0 ? (int)((r1 - r0 + kM - 1) / kM) : 0;
-    const int nkb = (K + kBK - 1) / kBK;
+    // this CTA's slice of K: stages [kb_lo, kb_lo + nkb) of the row (all of it
+    // unless the launch splits K over gridDim.y CTAs)
+    const int nkb_all = (K + kBK - 1) / kBK;
+    const int kb_lo = (int)((int64_t)blockIdx.y * nkb_all / gridDim.y);
+    const int nkb = (int)((int64_t)(blockIdx.y + 1) * nkb_all / gridDim.y) - kb_lo;
     const int nch = (nkb + kDrain - 1) / kDrain;  // accumulator chunks per tile
 
     if (threadIdx.x == 0) {
@@ -220,9 +225,9 @@ k_proj_umma(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
                     const uint32_t bar = smem_u32(&full_bar[slot]);
                     mbar_arrive_expect_tx(bar, (uint32_t)(groups * kGroup * kBK * 2 + C::kBBytes));
                     for (int g = 0; g < groups; ++g)
-                        tma_load_2d(st + (uint32_t)(g * kGroup * kBK * 2), &tm_x, bar, kb * kBK,
+                        tma_load_2d(st + (uint32_t)(g * kGroup * kBK * 2), &tm_x, bar, (kb_lo + kb) * kBK,
                                     (int)(tr + g * kGroup), pol_x);
-                    tma_load_2d(st + C::kABytes, &tm_w, bar, kb * kBK, 0, pol_w);
+                    tma_load_2d(st + C::kABytes, &tm_w, bar, (kb_lo + kb) * kBK, 0, pol_w);
                 }
             }
             // the last stages issued must land before the CTA leaves
@@ -325,7 +330,16 @@ k_proj_umma(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
             }
             if (!ok) break;
             const int64_t row = r0 + (int64_t)tile * kM + 32 * warp + lane;
-            if constexpr (!kFwd) {
+            if (kFwd && gridDim.y > 1) {
+                // K split over CTAs: this slice's dots and sum of squares, summed and
+                // finished by k_mix_finish; at float fa.part_off of the token's y row
+                if (row < r1) {
+                    float *o = fa.coef_rows + row * (int64_t)(K / 2) + fa.part_off + blockIdx.y * (MIX + 1);
+#pragma unroll
+                    for (int i = 0; i < MIX; ++i) o[i] = run[i];
+                    o[MIX] = ssx;
+                }
+            } else if constexpr (!kFwd) {
                 if (row < r1) {
                     float *o = out + row * (int64_t)out_stride;
 #pragma unroll
@@ -365,6 +379,51 @@ k_proj_umma(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
     __syncthreads();
     tmem_fence_after_sync();
     if (warp == 0) tmem_dealloc(tbase, C::kTmemCols);
+}
+
+// The K-split forward's last step, one thread per token: the slices' dots and
+// sums of squares added in slice order, the RMS scale, split + Sinkhorn, and
+// the outputs (as the unsplit kernel's drain warps write them).
+template <int HC>
+__global__ void __launch_bounds__(128)
+k_mix_finish(int64_t n, int K, int ksplit, FwdArgs fa) {
+    constexpr int MIX = (2 + HC) * HC;
+    const int64_t row = (int64_t)blockIdx.x * 128 + threadIdx.x;
+    if (row >= n) return;
+    float *rowp = fa.coef_rows + row * (int64_t)(K / 2);
+    float m[MIX];
+    float ssx = 0.0f;
+#pragma unroll
+    for (int i = 0; i < MIX; ++i) m[i] = 0.0f;
+    for (int ks = 0; ks < ksplit; ++ks) {
+        const float *p = rowp + fa.part_off + ks * (MIX + 1);
+#pragma unroll
+        for (int i = 0; i < MIX; ++i) m[i] += p[i];
+        ssx += p[MIX];
+    }
+    const float rsx = rsqrtf(ssx / (float)K + fa.norm_eps);
+#pragma unroll
+    for (int i = 0; i < MIX; ++i) m[i] *= rsx;
+    float pr[HC], po[HC], cm[HC * HC];
+    split_sinkhorn_token_hc<HC>(m, __ldg(fa.hc_scale), __ldg(fa.hc_scale + 1), __ldg(fa.hc_scale + 2),
+                                fa.hc_base, fa.iters, fa.eps, pr, po, cm);
+#pragma unroll
+    for (int k = 0; k < HC; ++k) {
+        if (fa.pre_out) fa.pre_out[row * HC + k] = pr[k];
+        if (fa.post_out) fa.post_out[row * HC + k] = po[k];
+    }
+    if (fa.comb_out) {
+#pragma unroll
+        for (int i = 0; i < HC * HC; ++i) fa.comb_out[row * HC * HC + i] = cm[i];
+    }
+    if (fa.mixes_out) {
+#pragma unroll
+        for (int i = 0; i < MIX; ++i) fa.mixes_out[row * MIX + i] = m[i];
+    }
+#pragma unroll
+    for (int k = 0; k < HC; ++k) rowp[k] = po[k];
+#pragma unroll
+    for (int i = 0; i < HC * HC; ++i) rowp[HC + i] = cm[i];
 }
 
 static_assert(Cfg<24>::kCtasPerSm == 2 && Cfg<8>::kCtasPerSm == 2 && Cfg<80>::kCtasPerSm == 1,
@@ -422,16 +481,37 @@ cudaError_t proj_umma_impl(const uint16_t *x, const float *hc_fn, int64_t n, int
     CUtensorMap tmx, tmw;
     if (!proj_tmap(&tmx, x, n, K, pu::kGroup) || !proj_tmap(&tmw, wsplit, C::kN, K, C::kN))
         return cudaErrorInvalidValue;
-    // contiguous token ranges of whole 32-row boxes, about one range per CTA slot
+    // Contiguous token ranges of whole 32-row boxes, about one range per CTA
+    // slot.  In the forward, when there are fewer 128-token tiles than slots,
+    // each tile's K is split over several CTAs instead (full tiles: no MMA rows
+    // wasted, the split weights streamed once per tile), with partial sums in
+    // the token's y row, as long as they fit there, and k_mix_finish after.
     const int64_t slots = (int64_t)sm_count() * C::kCtasPerSm;
-    int64_t per = (n + slots - 1) / slots;
-    per = (per + pu::kGroup - 1) / pu::kGroup * pu::kGroup;
+    const int64_t tiles = (n + pu::kM - 1) / pu::kM;
+    int ksplit = 1;
+    if (kFwd && tiles < slots) {
+        const int64_t nkb_all = (K + pu::kBK - 1) / pu::kBK;
+        int64_t cand = slots / tiles;
+        if (cand > nkb_all / 8) cand = nkb_all / 8;  // at least 8 stages per slice
+        if (cand > 8) cand = 8;
+        while (cand > 1 && fa.part_off + cand * (MIX + 1) > K / 2) --cand;
+        ksplit = cand > 1 ? (int)cand : 1;
+    }
+    int64_t per;
+    if (ksplit > 1) {
+        per = pu::kM;
+    } else {
+        per = (n + slots - 1) / slots;
+        per = (per + pu::kGroup - 1) / pu::kGroup * pu::kGroup;
+    }
     const int64_t grid = (n + per - 1) / per;
     cudaError_t e = cudaFuncSetAttribute(pu::k_proj_umma<MIX, kFwd>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::kSmem);
     if (e != cudaSuccess) return e;
-    pu::k_proj_umma<MIX, kFwd><<<(unsigned)grid, pu::kThreads, C::kSmem, s>>>(tmx, tmw, n, (int)K, (int)per, out,
-                                                                              out_stride, fa);
+    pu::k_proj_umma<MIX, kFwd><<<dim3((unsigned)grid, (unsigned)ksplit), pu::kThreads, C::kSmem, s>>>(
+        tmx, tmw, n, (int)K, (int)per, out, out_stride, fa);
+    if (ksplit > 1)
+        pu::k_mix_finish<pu::hc_of_mix(MIX)><<<(unsigned)((n + 127) / 128), 128, 0, s>>>(n, (int)K, ksplit, fa);
     return cudaGetLastError();
 }
 
@@ -461,7 +541,7 @@ cudaError_t launch_mixes_umma(const uint16_t *x, const float *hc_fn, const float
                               uint16_t *coef_rows, cudaStream_t s) {
     const int64_t K = (int64_t)hc * d;
     const pu::FwdArgs fa{hc_scale, hc_base, iters, eps, norm_eps, pre_out, post_out, comb_out, mixes_out,
-                         reinterpret_cast<float *>(coef_rows)};
+                         reinterpret_cast<float *>(coef_rows), 128};
     switch (hc) {
         case 2: return proj_umma_impl<8, true>(x, hc_fn, n, K, wsplit, nullptr, 0, fa, s);
         case 4: return proj_umma_impl<24, true>(x, hc_fn, n, K, wsplit, nullptr, 0, fa, s);
