@@ -439,10 +439,10 @@ constexpr int64_t kTiledMinTokens = 128;
 template <int HC>
 __host__ __device__ constexpr int tok_per_cta() { return HC <= 4 ? 4 : 1; }
 
-// The a4-a6 flavour (kCoefIn) keeps at most 128 registers, so that two CTAs
-// share an SM: at eight streams one CTA per SM left too few warps in flight.
+// The a4-a6 flavour (kCoefIn) keeps its registers low enough for two CTAs per
+// SM at eight streams (one left too few warps in flight), four at two.
 template <bool kFull, int HC, bool kCoefIn = false>
-__global__ void __launch_bounds__(kTokThreads, kCoefIn ? 2 : 1)
+__global__ void __launch_bounds__(kTokThreads, kCoefIn ? (HC <= 2 ? 4 : 2) : 1)
 k_tokens_simple(const uint16_t *__restrict__ x, const float *__restrict__ pre_mix,
                 const uint16_t *__restrict__ f, const float *__restrict__ hc_fn,
                 const float *__restrict__ hc_scale, const float *__restrict__ hc_base,
@@ -874,12 +874,10 @@ cudaError_t launch_tokens_simple_hc(const uint16_t *x, const float *pre_mix, con
     cudaError_t e;
     if (n >= kTiledMinTokens) {
         // a1-a3 on token tiles, then a4-a6 per token from the coefficients parked in
-        // the y rows.  For the side step at four and eight streams, the tcgen05
-        // kernel when its split weights fit the h_norm output (written only by the
-        // a4-a6 pass, after it); else the mma.sync kernel (hc_fn read once per 32
-        // tokens), which is also the faster one at two streams (measured at 8,192
-        // tokens x d = 5120: 154 against 193 us per side).
-        if (HC >= 4 && f && (size_t)n * (size_t)d * 2 >= proj_umma_wsplit_bytes(HC, (int64_t)HC * d))
+        // the y rows.  For the side step, the tcgen05 kernel when its split weights
+        // fit the h_norm output (written only by the a4-a6 pass, after it); else
+        // the mma.sync kernel (hc_fn read once per 32 tokens).
+        if (f && (size_t)n * (size_t)d * 2 >= proj_umma_wsplit_bytes(HC, (int64_t)HC * d))
             e = launch_mixes_umma(x, hc_fn, hc_scale, hc_base, n, HC, d, iters, eps, norm_eps, h_norm, pre_out,
                                   post_out, comb_out, mixes_out, y, s);
         else

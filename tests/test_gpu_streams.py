@@ -99,10 +99,11 @@ def test_pre_norm_and_post_hc(hc, n, d):
 @pytest.mark.parametrize("hc,n,d", [(2, 16, 5120), (8, 16, 5120), (2, 41, 1024), (8, 9, 2048),
                                     (2, 300, 5120), (8, 160, 5120), (8, 130, 64), (4, 200, 3072),
                                     (4, 131, 5184),
-                                    # the tcgen05 a1-a3 kernel at four and eight streams (its split
-                                    # weights fit h_norm): ragged 128-token tiles and 32-row boxes
+                                    # the tcgen05 a1-a3 kernel (its split weights fit h_norm): ragged
+                                    # 128-token tiles and 32-row boxes; K split over CTAs (all but
+                                    # the two at d = 64), partial slices of 8 or more stages
                                     (2, 100, 64), (2, 513, 1024), (4, 333, 3072), (4, 700, 5184),
-                                    (8, 1925, 256), (4, 321, 64)])
+                                    (8, 1925, 256), (4, 321, 64), (2, 4099, 5120)])
 def test_block_step_hc(hc, n, d):
     case = inputs.tiny(seed=70 + n + hc, n=n, d=d, hc=hc)
     p = case.params[0]
