@@ -18,9 +18,12 @@
 //   kg_gx     g_x and g_f;
 // then partial sums of the parameter gradients over blocks of 1,024 tokens,
 // added block by block in a fixed order (deterministic, no atomics).
+#include <cuda.h>
+
 #include "hc_backward_generic.h"
 #include "hc_launch.h"
 #include "hc_device.cuh"
+#include "hc_ptx.cuh"
 
 namespace hc {
 namespace bwg {
@@ -28,7 +31,7 @@ namespace bwg {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kTokBlock = 1024;  // tokens per partial sum of a parameter gradient
-constexpr int kFnTile = 16;      // tokens per staged g_a tile in kg_fn_partial
+constexpr int kFnTile = 16;      // tokens per staged tile in kg_fn_tc
 
 // The per-token record in the workspace (floats).
 template <int HC>
@@ -44,7 +47,10 @@ struct Lay {
     static constexpr int kRs = kPm + HC;        // 1 / RMS(h)
     static constexpr int kCr = kRs + 1;         // the statistic's coefficient of x in g_x
     static constexpr int kK3 = kRs + 2;         // rs^3 / d * sum(h w g_hn)
-    static constexpr int kWs = (kK3 + 1 + 3) / 4 * 4;
+    // g_a as three bf16 parts hi, mid, lo (part-major, 3 * mix bf16) for the
+    // tensor cores of kg_fn_tc; 16-byte aligned
+    static constexpr int kGaP = (kK3 + 1 + 3) / 4 * 4;
+    static constexpr int kWs = kGaP + (3 * kMix / 2 + 3) / 4 * 4;
     static constexpr int kSmall = (kMix + 3 + 3) / 4 * 4;  // per-block partials of g_hc_base, g_hc_scale
     // token sums of kg_token: sum h^2, T = sum h w g_hn, sum x^2, g_post[HC],
     // g_comb[HC*HC], A[HC] = sum x_s w g_hn, B[HC] = sum x_s h
@@ -229,9 +235,18 @@ kg_token(const uint16_t *__restrict__ x, const float *__restrict__ pre_mix,
     }
     float gr = 0.0f;
     for (int i = 0; i < M; ++i) gr = fmaf(gm[i], wt[L::kA + i], gr);
+    uint16_t *gp = reinterpret_cast<uint16_t *>(wt + L::kGaP);
     for (int i = 0; i < M; ++i) {
-        wt[L::kGa + i] = gm[i] * r;
+        const float ga = gm[i] * r;
+        wt[L::kGa + i] = ga;
         wt[L::kGz + i] = gz[i];
+        // ga = hi + mid + lo in bf16, to about 2^-24 of itself
+        const uint32_t hi = pack_bf16x2(ga, 0.0f) & 0xffffu;
+        const float r1 = ga - bf16lo(hi);
+        const uint32_t mid = pack_bf16x2(r1, 0.0f) & 0xffffu;
+        gp[i] = (uint16_t)hi;
+        gp[M + i] = (uint16_t)mid;
+        gp[2 * M + i] = (uint16_t)(pack_bf16x2(r1 - bf16lo(mid), 0.0f) & 0xffffu);
     }
     wt[L::kGzm] = gzm0;
     wt[L::kGzm + 1] = gzm1;
@@ -378,37 +393,106 @@ kg_gx_tiled(const uint16_t *__restrict__ x, const float *__restrict__ hc_fn, con
     }
 }
 
-// g_hc_fn partial sums over a block of tokens: part[b][i][k] = sum_t g_a[t][i] x[t][k];
-// one thread per column k of hc*d.
+// g_hc_fn partial sums on the tensor cores: part[b][i][k] = sum_t g_a[t][i]
+// x[t][k] over block b, as bf16 mma.sync m16n8k16 with x exact and g_a in
+// three bf16 parts (from the record).  A CTA takes 256 columns k of one
+// block; tiles of 16 tokens (x and the parts) are double-buffered through
+// cp.async (rows past the block are zero-filled).  Warp w owns columns
+// 32w .. 32w + 31 (two m-tiles of 16; A = x^T by ldmatrix.trans), all mix
+// rows (n-tiles of 8; B = the parts by ldmatrix.trans).
+constexpr int kFnCols = 256;
 template <int HC>
-__global__ void __launch_bounds__(kThreads)
-kg_fn_partial(const uint16_t *__restrict__ x, const float *__restrict__ ws, int64_t n, int K,
-              float *__restrict__ part) {
+struct FnTc {
+    static constexpr int M = (2 + HC) * HC;
+    static constexpr int NT = M / 8;                        // n-tiles
+    static constexpr int XROW = kFnCols + 8;                // bf16 per staged x row (528 B: odd 16-byte units)
+    static constexpr int PB = 3 * M;                        // bf16 of parts per token
+    static constexpr int PROW = (PB * 2 / 16) % 2 ? PB : PB + 8;  // padded to an odd number of 16-byte units
+    struct Stage {
+        uint16_t x[kFnTile][XROW];
+        uint16_t p[kFnTile][PROW];
+    };
+    static_assert(M % 8 == 0 && (PB * 2) % 16 == 0, "whole n-tiles, 16-byte part rows");
+    static_assert(sizeof(Stage) % 16 == 0, "16-byte stage size");
+};
+
+template <int HC>
+__global__ void __launch_bounds__(kThreads, 2)
+kg_fn_tc(const uint16_t *__restrict__ x, const float *__restrict__ ws, int64_t n, int K,
+         float *__restrict__ part) {
     using L = Lay<HC>;
-    constexpr int M = L::kMix;
-    __shared__ float sga[kFnTile][M];
-    const int k = blockIdx.x * kThreads + threadIdx.x;
+    using F = FnTc<HC>;
+    constexpr int M = F::M, NT = F::NT;
+    __shared__ __align__(16) typename F::Stage stg[2];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, q = lane & 3;
+    const int k0 = blockIdx.x * kFnCols;
     const int64_t t0 = (int64_t)blockIdx.y * kTokBlock;
     const int64_t t1 = (t0 + kTokBlock < n) ? t0 + kTokBlock : n;
-    float acc[M];
-#pragma unroll
-    for (int i = 0; i < M; ++i) acc[i] = 0.0f;
-    for (int64_t tb = t0; tb < t1; tb += kFnTile) {
-        const int cnt = (int)((t1 - tb < kFnTile) ? t1 - tb : kFnTile);
-        __syncthreads();
-        for (int q = threadIdx.x; q < cnt * M; q += kThreads)
-            sga[q / M][q % M] = ws[(tb + q / M) * L::kWs + L::kGa + q % M];
-        __syncthreads();
-        if (k < K)
-            for (int u = 0; u < cnt; ++u) {
-                const float xv = __uint_as_float((uint32_t)x[(tb + u) * K + k] << 16);
-#pragma unroll
-                for (int i = 0; i < M; ++i) acc[i] = fmaf(sga[u][i], xv, acc[i]);
+    const int ntiles = (int)((t1 - t0 + kFnTile - 1) / kFnTile);
+    auto issue = [&](int it) {
+        if (it < ntiles) {
+            typename F::Stage &S = stg[it & 1];
+            const int64_t tb = t0 + (int64_t)it * kFnTile;
+            for (int c = threadIdx.x; c < kFnTile * (kFnCols / 8); c += kThreads) {
+                const int u = c / (kFnCols / 8), j = c % (kFnCols / 8);
+                const bool ok = tb + u < t1 && k0 + 8 * j < K;
+                cp_async16(&S.x[u][8 * j], ok ? x + (tb + u) * K + k0 + 8 * j : x, ok ? 16 : 0);
             }
-    }
-    if (k < K)
+            for (int c = threadIdx.x; c < kFnTile * (F::PB / 8); c += kThreads) {
+                const int u = c / (F::PB / 8), j = c % (F::PB / 8);
+                const bool ok = tb + u < t1;
+                const uint16_t *src = reinterpret_cast<const uint16_t *>(ws + (tb + u) * L::kWs + L::kGaP) + 8 * j;
+                cp_async16(&S.p[u][8 * j], ok ? src : reinterpret_cast<const uint16_t *>(ws), ok ? 16 : 0);
+            }
+        }
+        cp_async_commit();
+    };
+    float acc[2][NT][4];
 #pragma unroll
-        for (int i = 0; i < M; ++i) part[((int64_t)blockIdx.y * M + i) * K + k] = acc[i];
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[mt][nt][e] = 0.0f;
+    // ldmatrix rows: x^T (A): token (l & 7) + 8 (l >> 4), columns 8 ((l >> 3) & 1) of the m-tile;
+    // parts (B): matrix 2 (3p + nt) + h = tokens 8h .. 8h + 7, mixes 8nt .. of part p
+    const uint32_t xa_off = (uint32_t)((((lane & 7) + 8 * (lane >> 4)) * F::XROW + 32 * warp + 8 * ((lane >> 3) & 1)) * 2);
+    issue(0);
+    for (int it = 0; it < ntiles; ++it) {
+        issue(it + 1);
+        cp_async_wait<1>();
+        __syncthreads();
+        const typename F::Stage &S = stg[it & 1];
+        const uint32_t xs = smem_u32(&S.x[0][0]) + xa_off, ps = smem_u32(&S.p[0][0]);
+        uint32_t xa[2][4];
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) ldmatrix_x4_trans(xs + 32 * mt, xa[mt][0], xa[mt][1], xa[mt][2], xa[mt][3]);
+#pragma unroll
+        for (int p = 2; p >= 0; --p)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                // b0: tokens 0-7, b1: tokens 8-15, mixes 8nt .. 8nt + 7 of part p (two 8x8 matrices)
+                const int lrow = (lane & 7) + 8 * ((lane >> 3) & 1);
+                uint32_t b0, b1;
+                ldmatrix_x2_trans(ps + (uint32_t)((lrow * F::PROW + p * M + 8 * nt) * 2), b0, b1);
+#pragma unroll
+                for (int mt = 0; mt < 2; ++mt)
+                    mma_bf16_16816(acc[mt][nt], xa[mt][0], xa[mt][1], xa[mt][2], xa[mt][3], b0, b1);
+            }
+        __syncthreads();  // every warp is done with this stage before it is refilled
+    }
+    cp_async_wait<0>();
+    // accumulator (mt, nt, e): column k0 + 32 w + 16 mt + g + 8 (e >> 1), mix 8 nt + 2q + (e & 1)
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int k = k0 + 32 * warp + 16 * mt + g + 8 * (e >> 1), i = 8 * nt + 2 * q + (e & 1);
+                if (k < K) part[((int64_t)blockIdx.y * M + i) * K + k] = acc[mt][nt][e];
+            }
 }
 
 // g_norm_w partial sums: part[b][c] = sum_t h[t][c] rs_h[t] g_hn[t][c], h as the forward rounds it.
@@ -503,7 +587,7 @@ cudaError_t launch(const uint16_t *x, const float *pre_mix, const uint16_t *f, c
                                                                              n, d, g_x, g_f);
     else
         kg_gx<HC><<<(unsigned)n, kThreads, 0, s>>>(x, hc_fn, norm_w, g_hn, g_y, ws, d, g_x, g_f);
-    kg_fn_partial<HC><<<dim3((unsigned)((K + kThreads - 1) / kThreads), (unsigned)blocks), kThreads, 0, s>>>(
+    kg_fn_tc<HC><<<dim3((unsigned)((K + kFnCols - 1) / kFnCols), (unsigned)blocks), kThreads, 0, s>>>(
         x, ws, n, (int)K, part_fn);
     kg_sum_blocks<<<(unsigned)((M * K + 255) / 256), 256, 0, s>>>(part_fn, blocks, M * K, g_fn);
     kg_w_partial<HC><<<dim3((unsigned)((d + kThreads - 1) / kThreads), (unsigned)blocks), kThreads, 0, s>>>(
