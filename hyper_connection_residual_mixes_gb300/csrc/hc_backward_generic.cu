@@ -73,34 +73,63 @@ __device__ __forceinline__ void ld4f(const float *p, float (&o)[4]) {
 }
 __device__ __forceinline__ float round_bf16(float v) { return bf16lo(pack_bf16x2(v, 0.0f)); }
 
-// One pass over the token for its sums, then (one thread) the split, the
-// Sinkhorn iterates and their backward, the gradients of the mix numbers,
-// g_pre_mix and the record.  Dynamic shared memory: 2 * iters iterates of
-// HC*HC, then the row softmax.
+// One warp per token (no CTA barrier): one pass over the token for its sums
+// (every lane ends with the totals), then the split and Sinkhorn forward and
+// backward with the comb matrix spread over the lanes (element e = lane +
+// 32 r, r < max(1, HC*HC / 32); at HC*HC < 32 the lanes repeat it), the
+// gradients of the mix numbers (mix row i = lane + 32 r), g_pre_mix and the
+// record.  Row sums reduce over lanes ^1 .. ^HC/2, column sums over lanes
+// ^HC .. ^16 and, at HC = 8, over the two elements a lane holds.  Dynamic
+// shared memory per warp: the row softmax S, the iterates P_0 ..
+// P_{2 iters - 1} (the backward recomputes each step's 1 / (sum + eps) from
+// them, with the same sums the forward took), then the token's sums.
 template <int HC>
-__global__ void __launch_bounds__(kThreads)
+__device__ __forceinline__ float row_sum(float v) {
+#pragma unroll
+    for (int m = 1; m < HC; m <<= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
+    return v;
+}
+template <int HC>
+__device__ __forceinline__ float row_max(float v) {
+#pragma unroll
+    for (int m = 1; m < HC; m <<= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, m));
+    return v;
+}
+template <int HC>
+__device__ __forceinline__ float col_sum_lanes(float v) {
+#pragma unroll
+    for (int m = HC; m < 32 && m < HC * HC; m <<= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
+    return v;
+}
+
+template <int HC>
+__global__ void __launch_bounds__(128)
 kg_token(const uint16_t *__restrict__ x, const float *__restrict__ pre_mix,
          const uint16_t *__restrict__ f, const float *__restrict__ hc_scale,
-         const float *__restrict__ hc_base, const float *__restrict__ norm_w, int d, int iters,
+         const float *__restrict__ hc_base, const float *__restrict__ norm_w, int64_t n, int d, int iters,
          float eps, float norm_eps, const float *__restrict__ g_hn, const float *__restrict__ g_y,
          const float *__restrict__ g_pre, float *__restrict__ g_pm, float *__restrict__ ws) {
     using L = Lay<HC>;
     constexpr int M = L::kMix, H2 = HC * HC;
+    constexpr int EPL = H2 > 32 ? H2 / 32 : 1;  // comb elements per lane
+    constexpr int MPL = (M + 31) / 32;          // mix rows per lane
     extern __shared__ float sdyn[];
-    __shared__ float red[kWarps][L::kSums];
-    __shared__ float tot[L::kSums];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t t = blockIdx.x;
+    const int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + warp;
+    if (t >= n) return;  // warp-uniform
     const int K = HC * d;
     const uint16_t *xt = x + t * K;
     float *wt = ws + t * L::kWs;
+    float *sS = sdyn + (size_t)warp * ((2 * iters + 1) * H2 + L::kSums);
+    float *sP = sS + H2;
+    float *sT = sP + 2 * iters * H2;
     float pm[HC];
 #pragma unroll
     for (int s = 0; s < HC; ++s) pm[s] = __ldg(pre_mix + t * HC + s);
     float v[L::kSums];
 #pragma unroll
     for (int i = 0; i < L::kSums; ++i) v[i] = 0.0f;
-    for (int c = threadIdx.x; c < d / 4; c += kThreads) {
+    for (int c = lane; c < d / 4; c += 32) {
         float xv[HC][4], fv[4], gh[4], w[4], h[4];
 #pragma unroll
         for (int s = 0; s < HC; ++s) ld4bf(xt + (int64_t)s * d + 4 * c, xv[s]);
@@ -136,126 +165,149 @@ kg_token(const uint16_t *__restrict__ x, const float *__restrict__ pre_mix,
             }
         }
     }
-    // the CTA's sums, added in a fixed order
 #pragma unroll
     for (int i = 0; i < L::kSums; ++i) {
-        const float sv = warp_sum(v[i]);
-        if (lane == 0) red[warp][i] = sv;
+        const float tv = warp_sum(v[i]);
+        if (lane == 0) sT[i] = tv;
     }
-    __syncthreads();
-    for (int i = threadIdx.x; i < L::kSums; i += kThreads) {
-        float sv = 0.0f;
-        for (int w2 = 0; w2 < kWarps; ++w2) sv += red[w2][i];
-        tot[i] = sv;
-    }
-    __syncthreads();
-    if (threadIdx.x != 0) return;
+    __syncwarp();
 
-    const float r = rsqrtf(tot[L::kSX2] / (float)K + norm_eps);
-    const float rs = rsqrtf(tot[L::kSH2] / (float)d + norm_eps);
-    const float k3 = rs * rs * rs / (float)d * tot[L::kST];
+    const float r = rsqrtf(sT[L::kSX2] / (float)K + norm_eps);
+    const float rs = rsqrtf(sT[L::kSH2] / (float)d + norm_eps);
+    const float k3 = rs * rs * rs / (float)d * sT[L::kST];
     const float s0 = __ldg(hc_scale), s1 = __ldg(hc_scale + 1), s2 = __ldg(hc_scale + 2);
-    float *sP = sdyn;
-    float *sS = sdyn + 2 * iters * H2;
-    float m[M];
-    for (int i = 0; i < M; ++i) m[i] = wt[L::kA + i] * r;
-    // the row softmax S and P[0] = S + eps
-    for (int j = 0; j < HC; ++j) {
-        float Lg[HC], mx = -INFINITY, sum = 0.0f;
-        for (int k = 0; k < HC; ++k) {
-            Lg[k] = fmaf(m[2 * HC + j * HC + k], s2, __ldg(hc_base + 2 * HC + j * HC + k));
-            mx = fmaxf(mx, Lg[k]);
-        }
-        for (int k = 0; k < HC; ++k) {
-            Lg[k] = expf(Lg[k] - mx);
-            sum += Lg[k];
-        }
-        for (int k = 0; k < HC; ++k) {
-            sS[j * HC + k] = Lg[k] / sum;
-            sP[j * HC + k] = sS[j * HC + k] + eps;
+
+    // the row softmax S of the comb logits and P_0 = S + eps
+    float S[EPL], P[EPL];
+    int el[EPL];
+#pragma unroll
+    for (int q = 0; q < EPL; ++q) {
+        el[q] = (lane + 32 * q) % H2;
+        const float lg = fmaf(wt[L::kA + 2 * HC + el[q]] * r, s2, __ldg(hc_base + 2 * HC + el[q]));
+        const float ex = expf(lg - row_max<HC>(lg));
+        S[q] = ex / row_sum<HC>(ex);
+        P[q] = S[q] + eps;
+        if (lane + 32 * q < H2) {
+            sS[el[q]] = S[q];
+            sP[el[q]] = P[q];
         }
     }
+    auto axis_sum = [&](const float (&a)[EPL], int st, float (&o)[EPL]) {
+        if (st & 1) {  // a column step: over the rows
+            float cs = 0.0f;
+#pragma unroll
+            for (int q = 0; q < EPL; ++q) cs += col_sum_lanes<HC>(a[q]);
+#pragma unroll
+            for (int q = 0; q < EPL; ++q) o[q] = cs;
+        } else {
+#pragma unroll
+            for (int q = 0; q < EPL; ++q) o[q] = row_sum<HC>(a[q]);
+        }
+    };
     // steps 1 .. 2*iters-1: a column step for odd, a row step for even steps
     for (int st = 1; st < 2 * iters; ++st) {
-        const float *pa = sP + (st - 1) * H2;
-        float *pb = sP + st * H2;
-        for (int i = 0; i < HC; ++i) {
-            float sum = 0.0f;
-            for (int o = 0; o < HC; ++o) sum += (st & 1) ? pa[o * HC + i] : pa[i * HC + o];
-            const float inv = 1.0f / (sum + eps);
-            for (int o = 0; o < HC; ++o) {
-                const int idx = (st & 1) ? o * HC + i : i * HC + o;
-                pb[idx] = pa[idx] * inv;
-            }
+        float sm[EPL];
+        axis_sum(P, st, sm);
+#pragma unroll
+        for (int q = 0; q < EPL; ++q) {
+            P[q] *= 1.0f / (sm[q] + eps);
+            if (lane + 32 * q < H2) sP[st * H2 + el[q]] = P[q];
         }
     }
-    const float *comb = sP + (2 * iters - 1) * H2;
-    for (int i = 0; i < H2; ++i) wt[L::kComb + i] = comb[i];
+#pragma unroll
+    for (int q = 0; q < EPL; ++q)
+        if (lane + 32 * q < H2) wt[L::kComb + el[q]] = P[q];
     // back through the steps: g, the gradient of the current iterate
-    float g[H2];
-    for (int i = 0; i < H2; ++i) g[i] = tot[L::kSComb + i];
+    float g[EPL];
+#pragma unroll
+    for (int q = 0; q < EPL; ++q) g[q] = sT[L::kSComb + el[q]];
+    __syncwarp();
     for (int st = 2 * iters - 1; st >= 1; --st) {
-        const float *pa = sP + (st - 1) * H2, *pb = sP + st * H2;
-        for (int i = 0; i < HC; ++i) {
-            float sum = 0.0f, dot = 0.0f;
-            for (int o = 0; o < HC; ++o) {
-                const int idx = (st & 1) ? o * HC + i : i * HC + o;
-                sum += pa[idx];
-                dot = fmaf(g[idx], pb[idx], dot);
-            }
-            const float inv = 1.0f / (sum + eps);
-            for (int o = 0; o < HC; ++o) {
-                const int idx = (st & 1) ? o * HC + i : i * HC + o;
-                g[idx] = (g[idx] - dot) * inv;
-            }
+        float pa[EPL], pb[EPL], gp[EPL], sm[EPL], dot[EPL];
+#pragma unroll
+        for (int q = 0; q < EPL; ++q) {
+            pa[q] = sP[(st - 1) * H2 + el[q]];
+            pb[q] = sP[st * H2 + el[q]];
+            gp[q] = g[q] * pb[q];
         }
+        axis_sum(pa, st, sm);
+        axis_sum(gp, st, dot);
+#pragma unroll
+        for (int q = 0; q < EPL; ++q) g[q] = (g[q] - dot[q]) * (1.0f / (sm[q] + eps));
     }
-    float gz[M], gm[M];
-    for (int j = 0; j < HC; ++j) {  // through the row softmax
-        float dot = 0.0f;
-        for (int k = 0; k < HC; ++k) dot = fmaf(g[j * HC + k], sS[j * HC + k], dot);
-        for (int k = 0; k < HC; ++k) gz[2 * HC + j * HC + k] = sS[j * HC + k] * (g[j * HC + k] - dot);
+    // through the row softmax
+    float gzc[EPL];
+#pragma unroll
+    for (int q = 0; q < EPL; ++q) {
+        const float dt = row_sum<HC>(g[q] * S[q]);
+        gzc[q] = S[q] * (g[q] - dt);
     }
-    float gzm0 = 0.0f, gzm1 = 0.0f, gzm2 = 0.0f;
-    for (int j = 0; j < HC; ++j) {  // pre and post: the sigmoids
-        const float sp = sigm(fmaf(m[j], s0, __ldg(hc_base + j)));
-        gz[j] = (g_pre ? __ldg(g_pre + t * HC + j) : 0.0f) * sp * (1.0f - sp);
-        const float sq = sigm(fmaf(m[HC + j], s1, __ldg(hc_base + HC + j)));
-        gz[HC + j] = tot[L::kSPost + j] * 2.0f * sq * (1.0f - sq);
-        wt[L::kPost + j] = 2.0f * sq;
-        wt[L::kPm + j] = pm[j];
-        gm[j] = gz[j] * s0;
-        gm[HC + j] = gz[HC + j] * s1;
-        gzm0 = fmaf(gz[j], m[j], gzm0);
-        gzm1 = fmaf(gz[HC + j], m[HC + j], gzm1);
-    }
-    for (int i = 2 * HC; i < M; ++i) {
-        gm[i] = gz[i] * s2;
-        gzm2 = fmaf(gz[i], m[i], gzm2);
-    }
-    float gr = 0.0f;
-    for (int i = 0; i < M; ++i) gr = fmaf(gm[i], wt[L::kA + i], gr);
-    uint16_t *gp = reinterpret_cast<uint16_t *>(wt + L::kGaP);
-    for (int i = 0; i < M; ++i) {
-        const float ga = gm[i] * r;
+
+    // pre and post (sigmoids), then the gradient of the projection; mix row
+    // i = lane + 32 u (pre 0 .. HC-1, post HC .. 2HC-1, comb the rest)
+    float z0 = 0.0f, z1 = 0.0f, z2 = 0.0f, gr = 0.0f;
+    uint16_t *gpart = reinterpret_cast<uint16_t *>(wt + L::kGaP);
+#pragma unroll
+    for (int u = 0; u < MPL; ++u) {
+        const int i = lane + 32 * u;
+        const int ic = i < M ? i : 0;
+        const float a = wt[L::kA + ic];
+        const float m = a * r;
+        // the comb gradient of element i - 2HC sits in lane (i - 2HC) % 32, slot (i - 2HC) / 32
+        const int ec = (ic >= 2 * HC ? ic - 2 * HC : 0);
+        float gzc_i = 0.0f;
+#pragma unroll
+        for (int q = 0; q < EPL; ++q) {
+            const float vq = __shfl_sync(0xffffffffu, gzc[q], ec & 31);
+            if (ec / 32 == q) gzc_i = vq;
+        }
+        if (i >= M) continue;
+        float gz, gm;
+        if (i < HC) {
+            const float sp = sigm(fmaf(m, s0, __ldg(hc_base + i)));
+            gz = (g_pre ? __ldg(g_pre + t * HC + i) : 0.0f) * sp * (1.0f - sp);
+            gm = gz * s0;
+            z0 = fmaf(gz, m, z0);
+        } else if (i < 2 * HC) {
+            const float sq = sigm(fmaf(m, s1, __ldg(hc_base + i)));
+            gz = sT[L::kSPost + i - HC] * 2.0f * sq * (1.0f - sq);
+            gm = gz * s1;
+            z1 = fmaf(gz, m, z1);
+            wt[L::kPost + i - HC] = 2.0f * sq;
+        } else {
+            gz = gzc_i;
+            gm = gz * s2;
+            z2 = fmaf(gz, m, z2);
+        }
+        gr = fmaf(gm, a, gr);
+        const float ga = gm * r;
         wt[L::kGa + i] = ga;
-        wt[L::kGz + i] = gz[i];
+        wt[L::kGz + i] = gz;
         // ga = hi + mid + lo in bf16, to about 2^-24 of itself
         const uint32_t hi = pack_bf16x2(ga, 0.0f) & 0xffffu;
         const float r1 = ga - bf16lo(hi);
         const uint32_t mid = pack_bf16x2(r1, 0.0f) & 0xffffu;
-        gp[i] = (uint16_t)hi;
-        gp[M + i] = (uint16_t)mid;
-        gp[2 * M + i] = (uint16_t)(pack_bf16x2(r1 - bf16lo(mid), 0.0f) & 0xffffu);
+        gpart[i] = (uint16_t)hi;
+        gpart[M + i] = (uint16_t)mid;
+        gpart[2 * M + i] = (uint16_t)(pack_bf16x2(r1 - bf16lo(mid), 0.0f) & 0xffffu);
     }
-    wt[L::kGzm] = gzm0;
-    wt[L::kGzm + 1] = gzm1;
-    wt[L::kGzm + 2] = gzm2;
-    wt[L::kRs] = rs;
-    wt[L::kCr] = -gr * r * r * r / (float)K;  // the statistic's term: cr * x_k
-    wt[L::kK3] = k3;
-    // g_pre_mix_s = sum_c x_s (rs w g_hn - k3 h) = rs A_s - k3 B_s
-    for (int s = 0; s < HC; ++s) g_pm[t * HC + s] = rs * tot[L::kSA + s] - k3 * tot[L::kSB + s];
+    z0 = warp_sum(z0);
+    z1 = warp_sum(z1);
+    z2 = warp_sum(z2);
+    gr = warp_sum(gr);
+    if (lane < HC) {
+        wt[L::kPm + lane] = pm[lane];
+        // g_pre_mix_s = sum_c x_s (rs w g_hn - k3 h) = rs A_s - k3 B_s
+        g_pm[t * HC + lane] = rs * sT[L::kSA + lane] - k3 * sT[L::kSB + lane];
+    }
+    if (lane == 0) {
+        wt[L::kGzm] = z0;
+        wt[L::kGzm + 1] = z1;
+        wt[L::kGzm + 2] = z2;
+        wt[L::kRs] = rs;
+        wt[L::kCr] = -gr * r * r * r / (float)K;  // the statistic's term: cr * x_k
+        wt[L::kK3] = k3;
+    }
 }
 
 // g_x[s][c] = pm_s g_h + cr x_s + sum_k comb_sk g_y_k + sum_i g_a_i W[i][s*d + c],
@@ -575,13 +627,17 @@ cudaError_t launch(const uint16_t *x, const float *pre_mix, const uint16_t *f, c
     float *part_w = part_fn + (int64_t)blocks * M * K;
     float *part_s = part_w + (int64_t)blocks * d;
     uint16_t *wsplit = reinterpret_cast<uint16_t *>(part_s + (int64_t)blocks * L::kSmall);
-    const size_t smem = (size_t)(2 * iters + 1) * HC * HC * sizeof(float);
+    // kg_token: one warp per token, up to four per CTA within 200 KB of iterates
+    const size_t per_warp = ((size_t)(2 * iters + 1) * HC * HC + L::kSums) * sizeof(float);
+    int tok_warps = (int)((200u << 10) / per_warp);
+    tok_warps = tok_warps < 1 ? 1 : (tok_warps > 4 ? 4 : tok_warps);
+    const size_t smem = per_warp * tok_warps;
     cudaError_t e = cudaFuncSetAttribute(kg_token<HC>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     e = launch_proj_umma(x, hc_fn, n, HC, d, wsplit, ws + L::kA, L::kWs, s);  // tcgen05, hc_proj_umma.cu
     if (e != cudaSuccess) return e;
-    kg_token<HC><<<(unsigned)n, kThreads, smem, s>>>(x, pre_mix, f, hc_scale, hc_base, norm_w, d, iters, eps,
-                                                     norm_eps, g_hn, g_y, g_pre, g_pm, ws);
+    kg_token<HC><<<(unsigned)((n + tok_warps - 1) / tok_warps), 32 * tok_warps, smem, s>>>(
+        x, pre_mix, f, hc_scale, hc_base, norm_w, n, d, iters, eps, norm_eps, g_hn, g_y, g_pre, g_pm, ws);
     if (HC >= 8)  // hc_fn of 13 MB: read once per 16 tokens; at two streams (330 KB) the per-token kernel wins
         kg_gx_tiled<HC><<<(unsigned)((n + kGxT - 1) / kGxT), kThreads, 0, s>>>(x, hc_fn, norm_w, g_hn, g_y, ws,
                                                                              n, d, g_x, g_f);
