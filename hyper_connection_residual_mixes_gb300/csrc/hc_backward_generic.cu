@@ -547,15 +547,18 @@ kg_fn_tc(const uint16_t *__restrict__ x, const float *__restrict__ ws, int64_t n
             }
 }
 
-// g_norm_w partial sums: part[b][c] = sum_t h[t][c] rs_h[t] g_hn[t][c], h as the forward rounds it.
+// g_norm_w partial sums over runs of kWRun tokens: part[b][c] = sum_t h[t][c]
+// rs_h[t] g_hn[t][c], h as the forward rounds it (short runs: enough CTAs to
+// keep the loads in flight).
+constexpr int kWRun = 64;
 template <int HC>
 __global__ void __launch_bounds__(kThreads)
 kg_w_partial(const uint16_t *__restrict__ x, const float *__restrict__ g_hn, const float *__restrict__ ws,
              int64_t n, int d, float *__restrict__ part) {
     using L = Lay<HC>;
     const int c = blockIdx.x * kThreads + threadIdx.x;
-    const int64_t t0 = (int64_t)blockIdx.y * kTokBlock;
-    const int64_t t1 = (t0 + kTokBlock < n) ? t0 + kTokBlock : n;
+    const int64_t t0 = (int64_t)blockIdx.y * kWRun;
+    const int64_t t1 = (t0 + kWRun < n) ? t0 + kWRun : n;
     if (c >= d) return;
     float acc = 0.0f;
     for (int64_t t = t0; t < t1; ++t) {
@@ -607,8 +610,9 @@ template <int HC>
 size_t ws_bytes(int64_t n, int d) {
     using L = Lay<HC>;
     const int64_t blocks = (n + kTokBlock - 1) / kTokBlock;
+    const int64_t wruns = (n + kWRun - 1) / kWRun;
     const int64_t K = (int64_t)HC * d;
-    return (size_t)(n * L::kWs + blocks * (L::kMix * K + d + L::kSmall)) * sizeof(float) +
+    return (size_t)(n * L::kWs + blocks * (L::kMix * K + L::kSmall) + wruns * d) * sizeof(float) +
            proj_umma_wsplit_bytes(HC, K);
 }
 
@@ -624,8 +628,9 @@ cudaError_t launch(const uint16_t *x, const float *pre_mix, const uint16_t *f, c
     const int blocks = (int)((n + kTokBlock - 1) / kTokBlock);
     float *ws = reinterpret_cast<float *>(workspace);
     float *part_fn = ws + n * L::kWs;
+    const int wruns = (int)((n + kWRun - 1) / kWRun);
     float *part_w = part_fn + (int64_t)blocks * M * K;
-    float *part_s = part_w + (int64_t)blocks * d;
+    float *part_s = part_w + (int64_t)wruns * d;
     uint16_t *wsplit = reinterpret_cast<uint16_t *>(part_s + (int64_t)blocks * L::kSmall);
     // kg_token: one warp per token, up to four per CTA within 200 KB of iterates
     const size_t per_warp = ((size_t)(2 * iters + 1) * HC * HC + L::kSums) * sizeof(float);
@@ -646,9 +651,9 @@ cudaError_t launch(const uint16_t *x, const float *pre_mix, const uint16_t *f, c
     kg_fn_tc<HC><<<dim3((unsigned)((K + kFnCols - 1) / kFnCols), (unsigned)blocks), kThreads, 0, s>>>(
         x, ws, n, (int)K, part_fn);
     kg_sum_blocks<<<(unsigned)((M * K + 255) / 256), 256, 0, s>>>(part_fn, blocks, M * K, g_fn);
-    kg_w_partial<HC><<<dim3((unsigned)((d + kThreads - 1) / kThreads), (unsigned)blocks), kThreads, 0, s>>>(
+    kg_w_partial<HC><<<dim3((unsigned)((d + kThreads - 1) / kThreads), (unsigned)wruns), kThreads, 0, s>>>(
         x, g_hn, ws, n, d, part_w);
-    kg_sum_blocks<<<(unsigned)((d + 255) / 256), 256, 0, s>>>(part_w, blocks, d, g_w);
+    kg_sum_blocks<<<(unsigned)((d + 255) / 256), 256, 0, s>>>(part_w, wruns, d, g_w);
     kg_small_partial<HC><<<(unsigned)blocks, 128, 0, s>>>(ws, n, part_s);
     kg_small_final<HC><<<1, 128, 0, s>>>(part_s, blocks, g_base, g_scale);
     return cudaGetLastError();
