@@ -381,49 +381,113 @@ k_proj_umma(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
     if (warp == 0) tmem_dealloc(tbase, C::kTmemCols);
 }
 
-// The K-split forward's last step, one thread per token: the slices' dots and
-// sums of squares added in slice order, the RMS scale, split + Sinkhorn, and
-// the outputs (as the unsplit kernel's drain warps write them).
+// The K-split forward's last step, one warp per token: the slices' dots and
+// sums of squares added in slice order, the RMS scale, then split + Sinkhorn
+// with the same formulas as split_sinkhorn_token_hc (accurate flavour), the
+// comb matrix spread over the lanes (element e = lane + 32 q; at HC*HC < 32
+// the lanes repeat it): row sums over lanes ^1 .. ^HC/2, column sums over
+// ^HC .. ^16 and the lane's elements.  Mix row i = lane + 32 u.
+template <int HC>
+__device__ __forceinline__ float wrow_sum(float v) {
+#pragma unroll
+    for (int m = 1; m < HC; m <<= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
+    return v;
+}
+template <int HC>
+__device__ __forceinline__ float wrow_max(float v) {
+#pragma unroll
+    for (int m = 1; m < HC; m <<= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, m));
+    return v;
+}
+template <int HC>
+__device__ __forceinline__ float wcol_sum(float v) {
+#pragma unroll
+    for (int m = HC; m < 32 && m < HC * HC; m <<= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
+    return v;
+}
+
 template <int HC>
 __global__ void __launch_bounds__(128)
 k_mix_finish(int64_t n, int K, int ksplit, FwdArgs fa) {
-    constexpr int MIX = (2 + HC) * HC;
-    const int64_t row = (int64_t)blockIdx.x * 128 + threadIdx.x;
-    if (row >= n) return;
+    constexpr int MIX = (2 + HC) * HC, H2 = HC * HC;
+    constexpr int EPL = H2 > 32 ? H2 / 32 : 1, MPL = (MIX + 31) / 32;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t row = (int64_t)blockIdx.x * 4 + warp;
+    if (row >= n) return;  // warp-uniform
     float *rowp = fa.coef_rows + row * (int64_t)(K / 2);
-    float m[MIX];
+    float mv[MPL];
+#pragma unroll
+    for (int u = 0; u < MPL; ++u) {
+        const int i = lane + 32 * u;
+        float acc = 0.0f;
+        if (i < MIX)
+            for (int ks = 0; ks < ksplit; ++ks) acc += rowp[fa.part_off + ks * (MIX + 1) + i];
+        mv[u] = acc;
+    }
     float ssx = 0.0f;
-#pragma unroll
-    for (int i = 0; i < MIX; ++i) m[i] = 0.0f;
-    for (int ks = 0; ks < ksplit; ++ks) {
-        const float *p = rowp + fa.part_off + ks * (MIX + 1);
-#pragma unroll
-        for (int i = 0; i < MIX; ++i) m[i] += p[i];
-        ssx += p[MIX];
-    }
+    for (int ks = 0; ks < ksplit; ++ks) ssx += rowp[fa.part_off + ks * (MIX + 1) + MIX];
     const float rsx = rsqrtf(ssx / (float)K + fa.norm_eps);
+    const float s0 = __ldg(fa.hc_scale), s1 = __ldg(fa.hc_scale + 1), s2 = __ldg(fa.hc_scale + 2);
 #pragma unroll
-    for (int i = 0; i < MIX; ++i) m[i] *= rsx;
-    float pr[HC], po[HC], cm[HC * HC];
-    split_sinkhorn_token_hc<HC>(m, __ldg(fa.hc_scale), __ldg(fa.hc_scale + 1), __ldg(fa.hc_scale + 2),
-                                fa.hc_base, fa.iters, fa.eps, pr, po, cm);
-#pragma unroll
-    for (int k = 0; k < HC; ++k) {
-        if (fa.pre_out) fa.pre_out[row * HC + k] = pr[k];
-        if (fa.post_out) fa.post_out[row * HC + k] = po[k];
+    for (int u = 0; u < MPL; ++u) {
+        const int i = lane + 32 * u;
+        mv[u] *= rsx;
+        if (i >= MIX) continue;
+        if (fa.mixes_out) fa.mixes_out[row * MIX + i] = mv[u];
+        if (i < HC) {
+            const float pr = sigmoid<false>(fmaf(mv[u], s0, __ldg(fa.hc_base + i))) + fa.eps;
+            if (fa.pre_out) fa.pre_out[row * HC + i] = pr;
+        } else if (i < 2 * HC) {
+            const float po = 2.0f * sigmoid<false>(fmaf(mv[u], s1, __ldg(fa.hc_base + i)));
+            if (fa.post_out) fa.post_out[row * HC + i - HC] = po;
+        }
     }
-    if (fa.comb_out) {
+    // comb logits: element e is mix 2HC + e, held by lane (2HC + e) % 32 in slot (2HC + e) / 32
+    float c[EPL];
+    int el[EPL];
 #pragma unroll
-        for (int i = 0; i < HC * HC; ++i) fa.comb_out[row * HC * HC + i] = cm[i];
+    for (int q = 0; q < EPL; ++q) {
+        el[q] = (lane + 32 * q) % H2;
+        const int src = 2 * HC + el[q];
+        float v = 0.0f;
+#pragma unroll
+        for (int u = 0; u < MPL; ++u) {
+            const float t = __shfl_sync(0xffffffffu, mv[u], src & 31);
+            if ((src >> 5) == u) v = t;
+        }
+        c[q] = fmaf(v, s2, __ldg(fa.hc_base + src));
     }
-    if (fa.mixes_out) {
+    // first round: row softmax + eps, then columns; then (iters - 1) rounds of rows, columns
 #pragma unroll
-        for (int i = 0; i < MIX; ++i) fa.mixes_out[row * MIX + i] = m[i];
+    for (int q = 0; q < EPL; ++q) {
+        const float ex = expo<false>(c[q] - wrow_max<HC>(c[q]));
+        c[q] = fmaf(ex, recip<false>(wrow_sum<HC>(ex)), fa.eps);
+    }
+    for (int it = 0; it < fa.iters; ++it) {
+        if (it > 0) {
+#pragma unroll
+            for (int q = 0; q < EPL; ++q) c[q] *= recip<false>(wrow_sum<HC>(c[q]) + fa.eps);
+        }
+        float cs = 0.0f;
+#pragma unroll
+        for (int q = 0; q < EPL; ++q) cs += wcol_sum<HC>(c[q]);
+        const float r = recip<false>(cs + fa.eps);
+#pragma unroll
+        for (int q = 0; q < EPL; ++q) c[q] *= r;
+    }
+    // post and comb at the start of the token's y row for the a4-a6 pass (the
+    // slices' partial sums sit further along the row)
+#pragma unroll
+    for (int u = 0; u < MPL; ++u) {
+        const int i = lane + 32 * u;
+        if (i >= HC && i < 2 * HC) rowp[i - HC] = 2.0f * sigmoid<false>(fmaf(mv[u], s1, __ldg(fa.hc_base + i)));
     }
 #pragma unroll
-    for (int k = 0; k < HC; ++k) rowp[k] = po[k];
-#pragma unroll
-    for (int i = 0; i < HC * HC; ++i) rowp[HC + i] = cm[i];
+    for (int q = 0; q < EPL; ++q)
+        if (lane + 32 * q < H2) {
+            if (fa.comb_out) fa.comb_out[row * H2 + el[q]] = c[q];
+            rowp[HC + el[q]] = c[q];
+        }
 }
 
 static_assert(Cfg<24>::kCtasPerSm == 2 && Cfg<8>::kCtasPerSm == 2 && Cfg<80>::kCtasPerSm == 1,
@@ -511,7 +575,7 @@ cudaError_t proj_umma_impl(const uint16_t *x, const float *hc_fn, int64_t n, int
     pu::k_proj_umma<MIX, kFwd><<<dim3((unsigned)grid, (unsigned)ksplit), pu::kThreads, C::kSmem, s>>>(
         tmx, tmw, n, (int)K, (int)per, out, out_stride, fa);
     if (ksplit > 1)
-        pu::k_mix_finish<pu::hc_of_mix(MIX)><<<(unsigned)((n + 127) / 128), 128, 0, s>>>(n, (int)K, ksplit, fa);
+        pu::k_mix_finish<pu::hc_of_mix(MIX)><<<(unsigned)((n + 3) / 4), 128, 0, s>>>(n, (int)K, ksplit, fa);
     return cudaGetLastError();
 }
 
