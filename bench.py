@@ -940,16 +940,42 @@ def run_reference(args, rank, world):
     }
 
 
+def run_side_step_op(args, dev):
+    """One hc_block_step at --hc streams (2, 4 or 8) over --tokens tokens
+    (default 8,192) x d = 5120, the inputs of the stream_counts sub-record:
+    for profiler captures of one stream count's side step."""
+    hc, n, d = args.hc, args.tokens or 8192, D
+    g = torch.Generator(device=dev).manual_seed(40 + hc)
+    x = inputs.streams(g, n, hc, d, device=dev)
+    pm = inputs.pre_mix(g, n, hc, device=dev)
+    f = inputs.sublayer_out(g, n, d, device=dev)
+    p = inputs.side_params(g, hc, d, device=dev)
+    mix = (2 + hc) * hc
+    alg = n * (hc * d * 2 + d * 2 + hc * 4 + hc * d * 2 + d * 2 + hc * 4) + mix * hc * d * 4 + 12 + mix * 4 + d * 4
+    fn = lambda: hcg.hc_block_step(x, pm, f, *p.astuple())
+    # launches per call: at four streams (d = 5120) the fused cluster kernel; else the
+    # weight split, the tcgen05 projection, (with K split over CTAs, when there are
+    # fewer 128-token tiles than CTA slots) the finish, and a4-a6
+    slots = torch.cuda.get_device_properties(dev).multi_processor_count * (1 if hc == 8 else 2)
+    launches = 1 if hc == 4 else (4 if (n + 127) // 128 < slots else 3)
+    return fn, alg, n, d, "one side step at %d streams (hc_block_step)" % hc, launches
+
+
 def run_op(args, local_rank):
     """One kernel of the widened rows, timed alone at the long-prefill size
     (65,536 tokens x d = 5120): the MXFP8 cast of the bf16 h_norm
     (hc_mxfp8_cast) or RMSNorm(hc_pre) with the cast in its epilogue
     (hc_pre_norm_mxfp8), or the side step's backward (hc_block_step_backward,
-    its launches over the batch).  One step is one call over the whole batch; the
-    inputs are larger than L2.  The oracle is timed beside it on a sample."""
+    its launches over the batch); or one side step at another stream count
+    (side_step, --hc, 8,192 tokens).  One step is one call over the whole
+    batch; the inputs are larger than L2.  The oracle is timed beside it on a
+    sample (not for side_step: the stream_counts sub-record's workload)."""
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     hcg._lib.load()
+    if args.op == "side_step":
+        fn, alg, n, d, what, launches = run_side_step_op(args, dev)
+        return _time_op(args, dev, local_rank, fn, alg, n, d, what, None, launches)
     case = inputs.long_prefill(device=dev, materialize_f=False, n=args.tokens or TOKENS)
     n, d = case.n, case.d
     p = case.params[0]
@@ -980,6 +1006,17 @@ def run_op(args, local_rank):
         fn = lambda: hcg.hc_pre_norm_mxfp8(case.x, case.pre_mix, p.norm_w, codes=codes, scales=scales)
         alg = n * HC * d * 2 + n * HC * 4 + d * 4 + n * d + n * d // 32
         what = "RMSNorm(hc_pre) cast to MXFP8 in one pass (hc_pre_norm_mxfp8)"
+    ctx = dict(case=case, p=p, h=h)
+    if args.op == "backward":
+        ctx.update(f0=f0, g_hn=g_hn, g_y=g_y, g_pre=g_pre)
+    # backward: the weight split, the projection, the per-token pass, the g_x pass,
+    # two block sums, the g_z block partials and their sum
+    return _time_op(args, dev, local_rank, fn, alg, n, d, what, ctx, 8 if args.op == "backward" else 1)
+
+
+def _time_op(args, dev, local_rank, fn, alg, n, d, what, ctx, launches):
+    """Warm-up, then args.steps calls timed with CUDA events, clocks sampled
+    meanwhile; the oracle on a sample where ctx carries the inputs."""
     for _ in range(args.warmup):
         fn()
     torch.cuda.synchronize(dev)
@@ -1001,16 +1038,19 @@ def run_op(args, local_rank):
            "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
            "dtype": ("bf16 + fp32 in, fp32 arithmetic, fp32 gradients out" if args.op == "backward"
+                     else "bf16 in, fp32 arithmetic, bf16 out" if args.op == "side_step"
                      else "bf16 in, fp32 arithmetic, e4m3 + ue8m0 out"), "data": "synthetic, seeded",
            "config": {"workload": ("long_prefill, one side step" if args.op == "backward"
-                                   else "long_prefill, one side's h_norm"), "op": args.op, "tokens": n, "d": d,
-                      "l2": "inputs larger than L2; no flush"},
+                                   else "stream_counts, one side step at hc = %d" % args.hc
+                                   if args.op == "side_step" else "long_prefill, one side's h_norm"),
+                      "op": args.op, "tokens": n, "d": d, "l2": "inputs larger than L2; no flush"},
            "roofline": {"bound": "hbm", "achieved": alg / (ms / 1e3) / 1e9, "peak": peak, "unit": "GB/s",
                         "frac": alg / (ms / 1e3) / 1e9 / peak, "traffic": None,
                         "peak_source": peak_kind, "algorithmic_bytes_per_launch": alg},
-           "clocks": clk, "gpu_launches": args.steps * (6 if args.op == "backward" else 1), "e2e": None}
-    if not args.no_cpu_baseline:
+           "clocks": clk, "gpu_launches": args.steps * launches, "e2e": None}
+    if not args.no_cpu_baseline and ctx is not None:
         import oracle
+        case, p, h = ctx["case"], ctx["p"], ctx["h"]
         rows = torch.arange(0, n, n // 64, device=dev)
         hs = oracle.bf16_bits(h.index_select(0, rows).cpu())
         xs = oracle.bf16_bits(case.x.index_select(0, rows).cpu())
@@ -1024,9 +1064,9 @@ def run_op(args, local_rank):
             rows = rows[:4]
             sel = lambda tt: tt.index_select(0, rows).cpu().numpy().astype(np.float64)
             oracle.side_backward(oracle.bf16_to_f64(xs[:4]), pms[:4], oracle.bf16_to_f64(
-                oracle.bf16_bits(f0.index_select(0, rows).cpu())),
-                *(t.cpu().numpy().astype(np.float64) for t in p.astuple()), sel(g_hn), sel(g_y),
-                sel(g_pre))
+                oracle.bf16_bits(ctx["f0"].index_select(0, rows).cpu())),
+                *(t.cpu().numpy().astype(np.float64) for t in p.astuple()), sel(ctx["g_hn"]), sel(ctx["g_y"]),
+                sel(ctx["g_pre"]))
         else:
             oracle.mxfp8(oracle.rmsnorm(oracle.pre(xs, pms), w))
         dt = time.perf_counter() - t0
@@ -1053,8 +1093,10 @@ def main():
                     help="with the chain, skip timing the one-launch-per-side path beside it")
     ap.add_argument("--path", choices=["chain", "step"], default="chain",
                     help="chain: the sides fused across sides (hc_chain_*); step: one hc_block_step per side")
-    ap.add_argument("--op", choices=["mxfp8_cast", "pre_norm_mxfp8", "backward"], default=None,
-                    help="time one kernel of the widened rows alone instead of the side steps")
+    ap.add_argument("--op", choices=["mxfp8_cast", "pre_norm_mxfp8", "backward", "side_step"], default=None,
+                    help="time one kernel of the widened rows alone instead of the side steps "
+                         "(side_step: one hc_block_step at --hc streams)")
+    ap.add_argument("--hc", type=int, choices=[2, 4, 8], default=4, help="with --op side_step: the stream count")
     ap.add_argument("--tokens", type=int, default=None,
                     help="with --op: tokens in the batch (default 65,536; smaller for profiler captures)")
     args = ap.parse_args()
