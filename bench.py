@@ -961,6 +961,28 @@ def run_side_step_op(args, dev):
     return fn, alg, n, d, "one side step at %d streams (hc_block_step)" % hc, launches
 
 
+def run_backward_hc_op(args, dev):
+    """hc_block_step_backward at --hc streams (2 or 8) over --tokens tokens
+    (default 8,192) x d = 5120, the inputs of the stream_counts sub-record."""
+    hc, n, d = args.hc, args.tokens or 8192, D
+    g = torch.Generator(device=dev).manual_seed(40 + hc)
+    x = inputs.streams(g, n, hc, d, device=dev)
+    pm = inputs.pre_mix(g, n, hc, device=dev)
+    f = inputs.sublayer_out(g, n, d, device=dev)
+    p = inputs.side_params(g, hc, d, device=dev)
+    ws = torch.empty(hcg._lib.load().hc_block_step_backward_workspace_bytes(n, hc, d), dtype=torch.uint8,
+                     device=dev)
+    g_hn = torch.randn((n, d), device=dev, generator=g)
+    g_y = torch.randn((n, hc, d), device=dev, generator=g)
+    mix = (2 + hc) * hc
+    w_bytes = mix * hc * d * 4 + 12 + mix * 4 + d * 4
+    alg = n * (hc * d * 2 + d * 2 + hc * 4 + d * 4 + hc * d * 4 + hc * d * 4 + hc * 4 + d * 4) + 2 * w_bytes
+    fn = lambda: hcg.hc_block_step_backward(x, pm, f, *p.astuple(), g_hn, g_y, workspace=ws)
+    # the weight split, the projection, kg_token, the g_x pass, the g_hc_fn and g_norm_w
+    # partials, their two sums, the g_hc_base / g_hc_scale partials and their sum
+    return fn, alg, n, d, "the side step's backward at %d streams (hc_block_step_backward)" % hc, 10
+
+
 def run_op(args, local_rank):
     """One kernel of the widened rows, timed alone at the long-prefill size
     (65,536 tokens x d = 5120): the MXFP8 cast of the bf16 h_norm
@@ -973,8 +995,8 @@ def run_op(args, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     hcg._lib.load()
-    if args.op == "side_step":
-        fn, alg, n, d, what, launches = run_side_step_op(args, dev)
+    if args.op == "side_step" or (args.op == "backward" and args.hc != HC):
+        fn, alg, n, d, what, launches = (run_side_step_op if args.op == "side_step" else run_backward_hc_op)(args, dev)
         return _time_op(args, dev, local_rank, fn, alg, n, d, what, None, launches)
     case = inputs.long_prefill(device=dev, materialize_f=False, n=args.tokens or TOKENS)
     n, d = case.n, case.d
@@ -1040,9 +1062,9 @@ def _time_op(args, dev, local_rank, fn, alg, n, d, what, ctx, launches):
            "dtype": ("bf16 + fp32 in, fp32 arithmetic, fp32 gradients out" if args.op == "backward"
                      else "bf16 in, fp32 arithmetic, bf16 out" if args.op == "side_step"
                      else "bf16 in, fp32 arithmetic, e4m3 + ue8m0 out"), "data": "synthetic, seeded",
-           "config": {"workload": ("long_prefill, one side step" if args.op == "backward"
-                                   else "stream_counts, one side step at hc = %d" % args.hc
-                                   if args.op == "side_step" else "long_prefill, one side's h_norm"),
+           "config": {"workload": ("stream_counts, one side step at hc = %d" % args.hc if args.hc != HC
+                                   else "long_prefill, one side step" if args.op == "backward"
+                                   else "long_prefill, one side's h_norm"),
                       "op": args.op, "tokens": n, "d": d, "l2": "inputs larger than L2; no flush"},
            "roofline": {"bound": "hbm", "achieved": alg / (ms / 1e3) / 1e9, "peak": peak, "unit": "GB/s",
                         "frac": alg / (ms / 1e3) / 1e9 / peak, "traffic": None,
@@ -1096,7 +1118,8 @@ def main():
     ap.add_argument("--op", choices=["mxfp8_cast", "pre_norm_mxfp8", "backward", "side_step"], default=None,
                     help="time one kernel of the widened rows alone instead of the side steps "
                          "(side_step: one hc_block_step at --hc streams)")
-    ap.add_argument("--hc", type=int, choices=[2, 4, 8], default=4, help="with --op side_step: the stream count")
+    ap.add_argument("--hc", type=int, choices=[2, 4, 8], default=4,
+                    help="with --op side_step or backward: the stream count (2 and 8 on the stream_counts inputs)")
     ap.add_argument("--tokens", type=int, default=None,
                     help="with --op: tokens in the batch (default 65,536; smaller for profiler captures)")
     args = ap.parse_args()

@@ -561,6 +561,7 @@ kg_w_partial(const uint16_t *__restrict__ x, const float *__restrict__ g_hn, con
     const int64_t t1 = (t0 + kWRun < n) ? t0 + kWRun : n;
     if (c >= d) return;
     float acc = 0.0f;
+#pragma unroll 8
     for (int64_t t = t0; t < t1; ++t) {
         const float *rec = ws + t * L::kWs;
         const uint16_t *xt = x + t * HC * d;
@@ -574,15 +575,33 @@ kg_w_partial(const uint16_t *__restrict__ x, const float *__restrict__ g_hn, con
 
 // per block: the sums over its tokens of g_z (g_hc_base terms) and gzm (g_hc_scale terms)
 template <int HC>
-__global__ void kg_small_partial(const float *__restrict__ ws, int64_t n, float *__restrict__ part) {
+__global__ void __launch_bounds__(kThreads)
+kg_small_partial(const float *__restrict__ ws, int64_t n, float *__restrict__ part) {
+    // field j (g_z, then gzm: kGz + kMix = kGzm) = 32 fc + lane; warp w sums
+    // tokens 128 w .. 128 w + 127 of the block, then the warp sums in warp order
     using L = Lay<HC>;
-    const int i = threadIdx.x;
-    if (i >= L::kMix + 3) return;
-    const int64_t t0 = (int64_t)blockIdx.x * kTokBlock;
-    const int64_t t1 = (t0 + kTokBlock < n) ? t0 + kTokBlock : n;
-    float acc = 0.0f;
-    for (int64_t t = t0; t < t1; ++t) acc += ws[t * L::kWs + L::kGz + i];  // kGz + kMix = kGzm
-    part[(int64_t)blockIdx.x * L::kSmall + i] = acc;
+    constexpr int F = L::kMix + 3;
+    __shared__ float red[kWarps][32];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t tw = (int64_t)blockIdx.x * kTokBlock + (int64_t)warp * (kTokBlock / kWarps);
+    for (int fc = 0; fc < (F + 31) / 32; ++fc) {
+        const int j = 32 * fc + lane;
+        float acc = 0.0f;
+        if (j < F) {
+#pragma unroll 8
+            for (int u = 0; u < kTokBlock / kWarps; ++u)
+                if (tw + u < n) acc += ws[(tw + u) * L::kWs + L::kGz + j];
+        }
+        red[warp][lane] = acc;
+        __syncthreads();
+        if (warp == 0 && j < F) {
+            float v = red[0][lane];
+#pragma unroll
+            for (int w = 1; w < kWarps; ++w) v += red[w][lane];
+            part[(int64_t)blockIdx.x * L::kSmall + j] = v;
+        }
+        __syncthreads();
+    }
 }
 
 // out[j] = sum_b part[b][j], blocks in order.
@@ -654,7 +673,7 @@ cudaError_t launch(const uint16_t *x, const float *pre_mix, const uint16_t *f, c
     kg_w_partial<HC><<<dim3((unsigned)((d + kThreads - 1) / kThreads), (unsigned)wruns), kThreads, 0, s>>>(
         x, g_hn, ws, n, d, part_w);
     kg_sum_blocks<<<(unsigned)((d + 255) / 256), 256, 0, s>>>(part_w, wruns, d, g_w);
-    kg_small_partial<HC><<<(unsigned)blocks, 128, 0, s>>>(ws, n, part_s);
+    kg_small_partial<HC><<<(unsigned)blocks, kThreads, 0, s>>>(ws, n, part_s);
     kg_small_final<HC><<<1, 128, 0, s>>>(part_s, blocks, g_base, g_scale);
     return cudaGetLastError();
 }
