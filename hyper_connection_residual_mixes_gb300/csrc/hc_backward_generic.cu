@@ -311,58 +311,71 @@ kg_token(const uint16_t *__restrict__ x, const float *__restrict__ pre_mix,
 }
 
 // g_x[s][c] = pm_s g_h + cr x_s + sum_k comb_sk g_y_k + sum_i g_a_i W[i][s*d + c],
-// g_h = rs w g_hn - k3 h; g_f[c] = sum_k post_k g_y_k.  Four channels per step.
-template <int HC>
+// g_h = rs w g_hn - k3 h; g_f[c] = sum_k post_k g_y_k.  Four channels per step,
+// TOK tokens per CTA (the W columns of a step loaded once for all of them).
+template <int HC, int TOK>
 __global__ void __launch_bounds__(kThreads)
 kg_gx(const uint16_t *__restrict__ x, const float *__restrict__ hc_fn, const float *__restrict__ norm_w,
-      const float *__restrict__ g_hn, const float *__restrict__ g_y, const float *__restrict__ ws, int d,
-      float *__restrict__ g_x, float *__restrict__ g_f) {
+      const float *__restrict__ g_hn, const float *__restrict__ g_y, const float *__restrict__ ws, int64_t n,
+      int d, float *__restrict__ g_x, float *__restrict__ g_f) {
     using L = Lay<HC>;
-    __shared__ float rec[L::kWs];
-    const int64_t t = blockIdx.x;
+    constexpr int M = L::kMix;
+    __shared__ float rec[TOK][L::kWs];
+    const int64_t t0 = (int64_t)blockIdx.x * TOK;
+    const int ntok = (n - t0 < TOK) ? (int)(n - t0) : TOK;
     const int64_t K = (int64_t)HC * d;
-    for (int i = threadIdx.x; i < L::kWs; i += kThreads) rec[i] = ws[t * L::kWs + i];
+    for (int i = threadIdx.x; i < ntok * L::kWs; i += kThreads) rec[i / L::kWs][i % L::kWs] = ws[t0 * L::kWs + i];
     __syncthreads();
-    const float rs = rec[L::kRs], cr = rec[L::kCr], k3 = rec[L::kK3];
     for (int c = threadIdx.x; c < d / 4; c += kThreads) {
-        float xv[HC][4], gy[HC][4], gh[4], w[4], ghh[4], gf[4];
+        // the W columns of these 4 channels, read once for the CTA's TOK tokens
+        float wv[M][HC][4];
 #pragma unroll
-        for (int s = 0; s < HC; ++s) {
-            ld4bf(x + t * K + (int64_t)s * d + 4 * c, xv[s]);
-            ld4f(g_y + (t * HC + s) * d + 4 * c, gy[s]);
-        }
-        ld4f(g_hn + t * d + 4 * c, gh);
+        for (int i = 0; i < M; ++i)
+#pragma unroll
+            for (int s = 0; s < HC; ++s) ld4f(hc_fn + i * K + (int64_t)s * d + 4 * c, wv[i][s]);
+        float w[4];
         ld4f(norm_w + 4 * c, w);
+        for (int u = 0; u < ntok; ++u) {
+            const int64_t t = t0 + u;
+            const float *r = rec[u];
+            const float rs = r[L::kRs], cr = r[L::kCr], k3 = r[L::kK3];
+            float xv[HC][4], gy[HC][4], gh[4], ghh[4], gf[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            float hv = rec[L::kPm] * xv[0][e];
-#pragma unroll
-            for (int s = 1; s < HC; ++s) hv = fmaf(rec[L::kPm + s], xv[s][e], hv);
-            ghh[e] = rs * (w[e] * gh[e]) - k3 * round_bf16(hv);
-            float fvv = rec[L::kPost] * gy[0][e];
-#pragma unroll
-            for (int k = 1; k < HC; ++k) fvv = fmaf(rec[L::kPost + k], gy[k][e], fvv);
-            gf[e] = fvv;
-        }
-        *reinterpret_cast<float4 *>(g_f + t * d + 4 * c) = make_float4(gf[0], gf[1], gf[2], gf[3]);
-#pragma unroll
-        for (int s = 0; s < HC; ++s) {
-            float gx[4];
+            for (int s = 0; s < HC; ++s) {
+                ld4bf(x + t * K + (int64_t)s * d + 4 * c, xv[s]);
+                ld4f(g_y + (t * HC + s) * d + 4 * c, gy[s]);
+            }
+            ld4f(g_hn + t * d + 4 * c, gh);
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                float a = fmaf(rec[L::kPm + s], ghh[e], cr * xv[s][e]);
+                float hv = r[L::kPm] * xv[0][e];
 #pragma unroll
-                for (int k = 0; k < HC; ++k) a = fmaf(rec[L::kComb + s * HC + k], gy[k][e], a);
-                gx[e] = a;
-            }
-            for (int i = 0; i < L::kMix; ++i) {
-                float wv[4];
-                ld4f(hc_fn + i * K + (int64_t)s * d + 4 * c, wv);
-                const float ga = rec[L::kGa + i];
+                for (int s = 1; s < HC; ++s) hv = fmaf(r[L::kPm + s], xv[s][e], hv);
+                ghh[e] = rs * (w[e] * gh[e]) - k3 * round_bf16(hv);
+                float fvv = r[L::kPost] * gy[0][e];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) gx[e] = fmaf(ga, wv[e], gx[e]);
+                for (int k = 1; k < HC; ++k) fvv = fmaf(r[L::kPost + k], gy[k][e], fvv);
+                gf[e] = fvv;
             }
-            *reinterpret_cast<float4 *>(g_x + (t * HC + s) * d + 4 * c) = make_float4(gx[0], gx[1], gx[2], gx[3]);
+            *reinterpret_cast<float4 *>(g_f + t * d + 4 * c) = make_float4(gf[0], gf[1], gf[2], gf[3]);
+#pragma unroll
+            for (int s = 0; s < HC; ++s) {
+                float gx[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    float a = fmaf(r[L::kPm + s], ghh[e], cr * xv[s][e]);
+#pragma unroll
+                    for (int k = 0; k < HC; ++k) a = fmaf(r[L::kComb + s * HC + k], gy[k][e], a);
+                    gx[e] = a;
+                }
+#pragma unroll
+                for (int i = 0; i < M; ++i) {
+                    const float ga = r[L::kGa + i];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) gx[e] = fmaf(ga, wv[i][s][e], gx[e]);
+                }
+                *reinterpret_cast<float4 *>(g_x + (t * HC + s) * d + 4 * c) = make_float4(gx[0], gx[1], gx[2], gx[3]);
+            }
         }
     }
 }
@@ -375,6 +388,7 @@ kg_gx(const uint16_t *__restrict__ x, const float *__restrict__ hc_fn, const flo
 // then the rest per (token, column) as kg_gx computes it, plus D.  Sums are
 // fp32 in index order (i, then the terms in kg_gx's order), as kg_gx.
 constexpr int kGxT = 16;     // tokens per CTA
+constexpr int kGxTokSmall = 4;  // tokens per CTA of kg_gx (hc = 2): hc_fn read once per 4 tokens
 template <int HC>
 __host__ __device__ constexpr int gx_cols() { return HC == 8 ? 32 : 64; }  // columns of d per chunk
 template <int HC>
@@ -662,11 +676,12 @@ cudaError_t launch(const uint16_t *x, const float *pre_mix, const uint16_t *f, c
     if (e != cudaSuccess) return e;
     kg_token<HC><<<(unsigned)((n + tok_warps - 1) / tok_warps), 32 * tok_warps, smem, s>>>(
         x, pre_mix, f, hc_scale, hc_base, norm_w, n, d, iters, eps, norm_eps, g_hn, g_y, g_pre, g_pm, ws);
-    if (HC >= 8)  // hc_fn of 13 MB: read once per 16 tokens; at two streams (330 KB) the per-token kernel wins
+    if constexpr (HC >= 8)  // hc_fn of 13 MB: read once per 16 tokens, the projection term in shared memory
         kg_gx_tiled<HC><<<(unsigned)((n + kGxT - 1) / kGxT), kThreads, 0, s>>>(x, hc_fn, norm_w, g_hn, g_y, ws,
                                                                              n, d, g_x, g_f);
-    else
-        kg_gx<HC><<<(unsigned)n, kThreads, 0, s>>>(x, hc_fn, norm_w, g_hn, g_y, ws, d, g_x, g_f);
+    else  // hc_fn of 330 KB: its columns in registers, read once per kGxTokSmall tokens
+        kg_gx<HC, kGxTokSmall><<<(unsigned)((n + kGxTokSmall - 1) / kGxTokSmall), kThreads, 0, s>>>(
+            x, hc_fn, norm_w, g_hn, g_y, ws, n, d, g_x, g_f);
     kg_fn_tc<HC><<<dim3((unsigned)((K + kFnCols - 1) / kFnCols), (unsigned)blocks), kThreads, 0, s>>>(
         x, ws, n, (int)K, part_fn);
     kg_sum_blocks<<<(unsigned)((M * K + 255) / 256), 256, 0, s>>>(part_fn, blocks, M * K, g_fn);
