@@ -754,7 +754,10 @@ cudaError_t launch_block_step_backward(const uint16_t *x, const float *pre_mix, 
     cudaError_t e = cudaFuncSetAttribute(k_bwd_token, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
-    if ((e = launch_proj_umma(x, hc_fn, n, kHC, d, wsplit, ws + kA, kWs, s)) != cudaSuccess) return e;
+    // (part_fn, written later by k_bwd_gx, holds the projection's K slices meanwhile)
+    if ((e = launch_proj_umma(x, hc_fn, n, kHC, d, wsplit, ws + kA, kWs, s, part_fn, (int64_t)blocks * kMix * K)) !=
+        cudaSuccess)
+        return e;
     k_bwd_token<<<(unsigned)((n + kTokWarps - 1) / kTokWarps), kTokWarps * 32, smem, s>>>(
         x, pre_mix, f, hc_scale, hc_base, norm_w, n, d, iters, eps, norm_eps, g_hn, g_y, g_pre, g_pm, ws);
     if ((e = cudaFuncSetAttribute(k_bwd_gx, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGxSmem)) !=

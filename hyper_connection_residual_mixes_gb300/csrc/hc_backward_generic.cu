@@ -672,7 +672,8 @@ cudaError_t launch(const uint16_t *x, const float *pre_mix, const uint16_t *f, c
     const size_t smem = per_warp * tok_warps;
     cudaError_t e = cudaFuncSetAttribute(kg_token<HC>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    e = launch_proj_umma(x, hc_fn, n, HC, d, wsplit, ws + L::kA, L::kWs, s);  // tcgen05, hc_proj_umma.cu
+    // tcgen05 (hc_proj_umma.cu); part_fn, written later by kg_fn_tc, holds its K slices meanwhile
+    e = launch_proj_umma(x, hc_fn, n, HC, d, wsplit, ws + L::kA, L::kWs, s, part_fn, (int64_t)blocks * M * K);
     if (e != cudaSuccess) return e;
     kg_token<HC><<<(unsigned)((n + tok_warps - 1) / tok_warps), 32 * tok_warps, smem, s>>>(
         x, pre_mix, f, hc_scale, hc_base, norm_w, n, d, iters, eps, norm_eps, g_hn, g_y, g_pre, g_pm, ws);

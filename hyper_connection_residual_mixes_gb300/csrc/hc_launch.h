@@ -27,10 +27,14 @@ cudaError_t launch_post(const uint16_t *f, const uint16_t *residual, const float
 // The projection a = x hc_fn^T alone on the tcgen05 tensor cores
 // (hc_proj_umma.cu): a[t][i] at out[t * out_stride + i].  `wsplit` is device
 // scratch of proj_umma_wsplit_bytes(hc, hc * d) bytes (16-byte aligned) for the
-// split weights; it is dead once the launch has completed.
+// split weights; it is dead once the launch has completed.  With `scratch`
+// (scratch_floats floats) K may be split over CTAs when the batch has fewer
+// 128-token tiles than CTA slots, the slices' partial sums held there and
+// added in slice order.
 size_t proj_umma_wsplit_bytes(int hc, int64_t K);
 cudaError_t launch_proj_umma(const uint16_t *x, const float *hc_fn, int64_t n, int hc, int d, uint16_t *wsplit,
-                             float *out, int out_stride, cudaStream_t s);
+                             float *out, int out_stride, cudaStream_t s, float *scratch = nullptr,
+                             int64_t scratch_floats = 0);
 // a1-a3 on the same kernel: the projection, the sum of squares of x, the RMS
 // scale, split + Sinkhorn; pre / post / comb / mixes out (each may be null)
 // and post + comb at the start of each token's row of `coef_rows` (the y

@@ -153,6 +153,7 @@ struct FwdArgs {
     float *pre_out, *post_out, *comb_out, *mixes_out;  // each may be null
     float *coef_rows;                                 // post, comb at the start of row t (stride K / 2 floats)
     int part_off;                                     // K split: partial sums at this float of row t
+    int64_t part_stride;                              // K split, raw output: floats between slices
 };
 
 constexpr int hc_of_mix(int mix) { return mix == 8 ? 2 : mix == 24 ? 4 : 8; }
@@ -341,7 +342,9 @@ k_proj_umma(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CU
                 }
             } else if constexpr (!kFwd) {
                 if (row < r1) {
-                    float *o = out + row * (int64_t)out_stride;
+                    // with K split over gridDim.y CTAs, slice blockIdx.y's partial sums go
+                    // to the slice's own array (fa.part_stride floats apart)
+                    float *o = out + (int64_t)blockIdx.y * fa.part_stride + row * (int64_t)out_stride;
 #pragma unroll
                     for (int i = 0; i < MIX; ++i) o[i] = run[i];
                 }
@@ -490,6 +493,18 @@ k_mix_finish(int64_t n, int K, int ksplit, FwdArgs fa) {
         }
 }
 
+// The raw projection with K split: out[t][i] = sum over the slices, in order.
+__global__ void k_proj_sum_slices(const float *__restrict__ part, int64_t n, int mix, int ksplit,
+                                  int64_t part_stride, float *__restrict__ out, int out_stride) {
+    const int64_t o = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (o >= n * mix) return;
+    const int64_t t = o / mix;
+    const int i = (int)(o % mix);
+    float v = 0.0f;
+    for (int ks = 0; ks < ksplit; ++ks) v += part[(int64_t)ks * part_stride + t * mix + i];
+    out[t * out_stride + i] = v;
+}
+
 static_assert(Cfg<24>::kCtasPerSm == 2 && Cfg<8>::kCtasPerSm == 2 && Cfg<80>::kCtasPerSm == 1,
               "occupancy the launcher assumes");
 
@@ -536,7 +551,8 @@ int sm_count() {
 
 template <int MIX, bool kFwd>
 cudaError_t proj_umma_impl(const uint16_t *x, const float *hc_fn, int64_t n, int64_t K, uint16_t *wsplit,
-                           float *out, int out_stride, const pu::FwdArgs &fa, cudaStream_t s) {
+                           float *out, int out_stride, pu::FwdArgs fa, cudaStream_t s, float *scratch = nullptr,
+                           int64_t scratch_floats = 0) {
     using C = pu::Cfg<MIX>;
     {
         const int64_t blocks = ((int64_t)MIX * K + 255) / 256;
@@ -552,14 +568,26 @@ cudaError_t proj_umma_impl(const uint16_t *x, const float *hc_fn, int64_t n, int
     // the token's y row, as long as they fit there, and k_mix_finish after.
     const int64_t slots = (int64_t)sm_count() * C::kCtasPerSm;
     const int64_t tiles = (n + pu::kM - 1) / pu::kM;
+    // (the raw projection of the backward: slices into the caller's scratch,
+    // added by k_proj_sum_slices)
     int ksplit = 1;
-    if (kFwd && tiles < slots) {
+    if (tiles < slots && (kFwd || scratch)) {
         const int64_t nkb_all = (K + pu::kBK - 1) / pu::kBK;
         int64_t cand = slots / tiles;
         if (cand > nkb_all / 8) cand = nkb_all / 8;  // at least 8 stages per slice
         if (cand > 8) cand = 8;
-        while (cand > 1 && fa.part_off + cand * (MIX + 1) > K / 2) --cand;
+        if (kFwd)
+            while (cand > 1 && fa.part_off + cand * (MIX + 1) > K / 2) --cand;
+        else
+            while (cand > 1 && cand * n * MIX > scratch_floats) --cand;
         ksplit = cand > 1 ? (int)cand : 1;
+    }
+    float *const final_out = out;
+    const int final_stride = out_stride;
+    if (!kFwd && ksplit > 1) {
+        out = scratch;
+        out_stride = MIX;
+        fa.part_stride = n * MIX;
     }
     int64_t per;
     if (ksplit > 1) {
@@ -574,8 +602,13 @@ cudaError_t proj_umma_impl(const uint16_t *x, const float *hc_fn, int64_t n, int
     if (e != cudaSuccess) return e;
     pu::k_proj_umma<MIX, kFwd><<<dim3((unsigned)grid, (unsigned)ksplit), pu::kThreads, C::kSmem, s>>>(
         tmx, tmw, n, (int)K, (int)per, out, out_stride, fa);
-    if (ksplit > 1)
-        pu::k_mix_finish<pu::hc_of_mix(MIX)><<<(unsigned)((n + 3) / 4), 128, 0, s>>>(n, (int)K, ksplit, fa);
+    if (ksplit > 1) {
+        if (kFwd)
+            pu::k_mix_finish<pu::hc_of_mix(MIX)><<<(unsigned)((n + 3) / 4), 128, 0, s>>>(n, (int)K, ksplit, fa);
+        else
+            pu::k_proj_sum_slices<<<(unsigned)((n * MIX + 255) / 256), 256, 0, s>>>(
+                scratch, n, MIX, ksplit, fa.part_stride, final_out, final_stride);
+    }
     return cudaGetLastError();
 }
 
@@ -588,13 +621,13 @@ size_t proj_umma_wsplit_bytes(int hc, int64_t K) {
 }
 
 cudaError_t launch_proj_umma(const uint16_t *x, const float *hc_fn, int64_t n, int hc, int d, uint16_t *wsplit,
-                             float *out, int out_stride, cudaStream_t s) {
+                             float *out, int out_stride, cudaStream_t s, float *scratch, int64_t scratch_floats) {
     const int64_t K = (int64_t)hc * d;
     const pu::FwdArgs none{};
     switch (hc) {
-        case 2: return proj_umma_impl<8, false>(x, hc_fn, n, K, wsplit, out, out_stride, none, s);
-        case 4: return proj_umma_impl<24, false>(x, hc_fn, n, K, wsplit, out, out_stride, none, s);
-        case 8: return proj_umma_impl<80, false>(x, hc_fn, n, K, wsplit, out, out_stride, none, s);
+        case 2: return proj_umma_impl<8, false>(x, hc_fn, n, K, wsplit, out, out_stride, none, s, scratch, scratch_floats);
+        case 4: return proj_umma_impl<24, false>(x, hc_fn, n, K, wsplit, out, out_stride, none, s, scratch, scratch_floats);
+        case 8: return proj_umma_impl<80, false>(x, hc_fn, n, K, wsplit, out, out_stride, none, s, scratch, scratch_floats);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -605,7 +638,7 @@ cudaError_t launch_mixes_umma(const uint16_t *x, const float *hc_fn, const float
                               uint16_t *coef_rows, cudaStream_t s) {
     const int64_t K = (int64_t)hc * d;
     const pu::FwdArgs fa{hc_scale, hc_base, iters, eps, norm_eps, pre_out, post_out, comb_out, mixes_out,
-                         reinterpret_cast<float *>(coef_rows), 128};
+                         reinterpret_cast<float *>(coef_rows), 128, 0};
     switch (hc) {
         case 2: return proj_umma_impl<8, true>(x, hc_fn, n, K, wsplit, nullptr, 0, fa, s);
         case 4: return proj_umma_impl<24, true>(x, hc_fn, n, K, wsplit, nullptr, 0, fa, s);
