@@ -431,6 +431,11 @@ cudaError_t launch_post(const uint16_t *f, const uint16_t *residual, const float
 // Phase 2 (side step only): y and h for every token (x re-read through L1/L2),
 // sum of squares of the rounded h, then h_norm.
 constexpr int kTokThreads = 256;
+// threads per CTA of k_tokens_simple: the a4-a6 flavour at eight streams takes
+// 128 (one token per CTA; d = 5120 is 640 chunks of 8 channels, 5 per thread
+// rather than 2 or 3), the rest 256
+template <int HC, bool kCoefIn>
+__host__ __device__ constexpr int tok_threads() { return (kCoefIn && HC == 8) ? 128 : kTokThreads; }
 // from this many tokens on, a1-a3 run on token tiles (k_mixes_tiled): below it the
 // 32-token tiles would leave most SMs idle
 constexpr int64_t kTiledMinTokens = 128;
@@ -439,10 +444,11 @@ constexpr int64_t kTiledMinTokens = 128;
 template <int HC>
 __host__ __device__ constexpr int tok_per_cta() { return HC <= 4 ? 4 : 1; }
 
-// The a4-a6 flavour (kCoefIn) keeps its registers low enough for two CTAs per
-// SM at eight streams (one left too few warps in flight), four at two.
+// The a4-a6 flavour (kCoefIn) keeps its registers low enough for four CTAs of
+// 128 threads per SM at eight streams (one CTA of 256 per SM left too few warps
+// in flight), four of 256 at two streams.
 template <bool kFull, int HC, bool kCoefIn = false>
-__global__ void __launch_bounds__(kTokThreads, kCoefIn ? (HC <= 2 ? 4 : 2) : 1)
+__global__ void __launch_bounds__(tok_threads<HC, kCoefIn>(), kCoefIn ? (HC == 8 ? 4 : HC <= 2 ? 4 : 2) : 1)
 k_tokens_simple(const uint16_t *__restrict__ x, const float *__restrict__ pre_mix,
                 const uint16_t *__restrict__ f, const float *__restrict__ hc_fn,
                 const float *__restrict__ hc_scale, const float *__restrict__ hc_base,
@@ -451,13 +457,14 @@ k_tokens_simple(const uint16_t *__restrict__ x, const float *__restrict__ pre_mi
                 float *__restrict__ pre_out, float *__restrict__ post_out,
                 float *__restrict__ comb_out, float *__restrict__ mixes_out) {
     constexpr int kTok = tok_per_cta<HC>();
+    constexpr int NT = tok_threads<HC, kCoefIn>();
     constexpr int MIX = (2 + HC) * HC;
     constexpr int kVals = MIX * kTok + kTok;  // MIX dots per token + sum of squares per token
     extern __shared__ uint4 hbuf[];            // kTok * d/8 chunks (side step only)
-    __shared__ float red[kTokThreads / 32][kVals];
+    __shared__ float red[NT / 32][kVals];
     __shared__ float tot[kVals];
     __shared__ float coef[kTok][HC + HC * HC];
-    __shared__ float ssh[kTokThreads / 32][kTok];
+    __shared__ float ssh[NT / 32][kTok];
 
     const int64_t t0 = (int64_t)blockIdx.x * kTok;
     const int ntok = (n - t0 < kTok) ? (int)(n - t0) : kTok;
@@ -466,11 +473,9 @@ k_tokens_simple(const uint16_t *__restrict__ x, const float *__restrict__ pre_mi
     if constexpr (kCoefIn) {
         // post and comb of each token, parked by k_mixes_tiled at the start of the
         // token's own y row (read here before this CTA writes that row)
-        if (threadIdx.x < ntok) {
-            const float *src = reinterpret_cast<const float *>(y + (t0 + threadIdx.x) * K);
-#pragma unroll
-            for (int i = 0; i < HC + HC * HC; ++i) coef[threadIdx.x][i] = src[i];
-        }
+        constexpr int C = HC + HC * HC;
+        for (int q = threadIdx.x; q < ntok * C; q += NT)  // one load per thread
+            coef[q / C][q % C] = reinterpret_cast<const float *>(y + (t0 + q / C) * K)[q % C];
     } else {
 
     float acc[MIX][kTok];
@@ -482,7 +487,7 @@ k_tokens_simple(const uint16_t *__restrict__ x, const float *__restrict__ pre_mi
 #pragma unroll
     for (int u = 0; u < kTok; ++u) ss[u] = 0.0f;
 
-    for (int ch = threadIdx.x; ch < K8; ch += kTokThreads) {
+    for (int ch = threadIdx.x; ch < K8; ch += NT) {
         float xv[kTok][8];
 #pragma unroll
         for (int u = 0; u < kTok; ++u) {
@@ -520,10 +525,10 @@ k_tokens_simple(const uint16_t *__restrict__ x, const float *__restrict__ pre_mi
         if (lane == 0) red[warp][MIX * kTok + u] = v;
     }
     __syncthreads();
-    for (int v = threadIdx.x; v < kVals; v += kTokThreads) {
+    for (int v = threadIdx.x; v < kVals; v += NT) {
         float s = 0.0f;
 #pragma unroll
-        for (int w = 0; w < kTokThreads / 32; ++w) s += red[w][v];
+        for (int w = 0; w < NT / 32; ++w) s += red[w][v];
         tot[v] = s;
     }
     __syncthreads();
@@ -577,7 +582,7 @@ k_tokens_simple(const uint16_t *__restrict__ x, const float *__restrict__ pre_mi
         const uint4 *fs = reinterpret_cast<const uint4 *>(f + t * d);
         uint4 *ys = reinterpret_cast<uint4 *>(y + t * K);
         f32x2 hs2 = f2_dup(0.0f);
-        for (int c = threadIdx.x; c < d8; c += kTokThreads) {
+        for (int c = threadIdx.x; c < d8; c += NT) {
             f32x2 fv[4], xv[HC][4];
             {
                 const uint4 fr = __ldg(fs + c);
@@ -634,10 +639,10 @@ k_tokens_simple(const uint16_t *__restrict__ x, const float *__restrict__ pre_mi
     for (int u = 0; u < ntok; ++u) {
         float s = 0.0f;
 #pragma unroll
-        for (int w = 0; w < kTokThreads / 32; ++w) s += ssh[w][u];
+        for (int w = 0; w < NT / 32; ++w) s += ssh[w][u];
         const float rs = rsqrtf(s / (float)d + norm_eps);
         uint4 *o = reinterpret_cast<uint4 *>(h_norm + (t0 + u) * d);
-        for (int c = threadIdx.x; c < d8; c += kTokThreads) {
+        for (int c = threadIdx.x; c < d8; c += NT) {
             float h[8];
             unpack8(hbuf[u * d8 + c], h);
             const float4 wa = __ldg(w4 + 2 * c), wb = __ldg(w4 + 2 * c + 1);
@@ -888,7 +893,7 @@ cudaError_t launch_tokens_simple_hc(const uint16_t *x, const float *pre_mix, con
         e = cudaFuncSetAttribute(k_tokens_simple<true, HC, true>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        k_tokens_simple<true, HC, true><<<(unsigned)blocks, kTokThreads, smem, s>>>(
+        k_tokens_simple<true, HC, true><<<(unsigned)blocks, tok_threads<HC, true>(), smem, s>>>(
             x, pre_mix, f, hc_fn, hc_scale, hc_base, norm_w, n, d, iters, eps, norm_eps, h_norm, y,
             nullptr, nullptr, nullptr, nullptr);
         return cudaGetLastError();
