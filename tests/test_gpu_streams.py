@@ -103,7 +103,10 @@ def test_pre_norm_and_post_hc(hc, n, d):
                                     # 128-token tiles and 32-row boxes; K split over CTAs (all but
                                     # the two at d = 64), partial slices of 8 or more stages
                                     (2, 100, 64), (2, 513, 1024), (4, 333, 3072), (4, 700, 5184),
-                                    (8, 1925, 256), (4, 321, 64), (2, 4099, 5120)])
+                                    (8, 1925, 256), (4, 321, 64), (2, 4099, 5120),
+                                    # at least one 128-token tile per CTA slot: K not split, CTAs
+                                    # owning two tiles (the second ragged) and finishing in place
+                                    (8, 20011, 64), (4, 40003, 64), (2, 40000, 64)])
 def test_block_step_hc(hc, n, d):
     case = inputs.tiny(seed=70 + n + hc, n=n, d=d, hc=hc)
     p = case.params[0]
