@@ -401,6 +401,22 @@ def _event_ms(fn, k, stream, flush=None):
     return [a.elapsed_time(b) for a, b in out]
 
 
+def _graph_ms(make_fn, k, stream, flush):
+    """CUDA-event durations (ms) of k replays of a CUDA graph holding one call.
+    make_fn(st) returns the call with its launches on stream st; it is
+    captured once on a side stream (after the eager calls that precede it)
+    and replayed on `stream`, with L2 flushed before every replay."""
+    cs = torch.cuda.Stream(device=stream.device)
+    cs.wait_stream(stream)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=cs):
+        make_fn(cs)()
+    stream.wait_stream(cs)
+    for _ in range(3):
+        graph.replay()
+    return _event_ms(graph.replay, k, stream, flush)
+
+
 def _oracle_rate(fn, units, what):
     """The oracle on a sample, timed on one host core: units per second."""
     t0 = time.perf_counter()
@@ -430,12 +446,14 @@ def run_configs(dev, peak, stream):
     h = torch.empty((case.n, case.d), dtype=torch.bfloat16, device=dev)
     y = torch.empty_like(case.x)
     pre = torch.empty_like(case.pre_mix)
-    fn = lambda: hcg.hc_block_step(case.x, case.pre_mix, case.fs[0], *p.astuple(), h_norm=h, y=y,
-                                   pre_out=pre, stream=stream)
+    make = lambda st: (lambda: hcg.hc_block_step(case.x, case.pre_mix, case.fs[0], *p.astuple(), h_norm=h,
+                                                 y=y, pre_out=pre, stream=st))
+    fn = make(stream)
     for _ in range(5):
         fn()
     cold = _event_ms(fn, 50, stream, flush)
     warm = _event_ms(fn, 50, stream)
+    graph = _graph_ms(make, 50, stream, flush)
     alg = side_bytes(case.n)
     xb, fb = inputs.bf16_bits_np(case.x), inputs.bf16_bits_np(case.fs[0])
     pmn = case.pre_mix.cpu().numpy().astype(np.float64)
@@ -446,10 +464,12 @@ def run_configs(dev, peak, stream):
         "workload": "tiny: B=1, T=16, one hc_block_step side (seed 0)", "tokens": case.n, "sides": 1,
         "us_per_side": 1e3 * statistics.mean(cold), "us_per_side_median": 1e3 * statistics.median(cold),
         "us_per_side_l2_warm": 1e3 * statistics.mean(warm),
+        "us_per_side_graph": 1e3 * statistics.mean(graph),
         "tokens_per_s": case.n / (statistics.mean(cold) / 1e3),
         "algorithmic_bytes": alg, "hbm_gbs": alg / (statistics.mean(cold) / 1e3) / 1e9,
         "roofline_frac": alg / (statistics.mean(cold) / 1e3) / 1e9 / peak,
         "l2": "flushed before every call (256 MB written); l2_warm: back to back", "calls": len(cold),
+        "graph": "the call captured once into a CUDA graph and replayed, L2 flushed before each replay",
         "cpu_baseline": cpu}
 
     # decode: 128 tokens, attention side then FFN side (the FFN side reads with the attention side's pre)
@@ -459,13 +479,17 @@ def run_configs(dev, peak, stream):
     ha = torch.empty((case.n, case.d), dtype=torch.bfloat16, device=dev)
     prea, pref = torch.empty_like(case.pre_mix), torch.empty_like(case.pre_mix)
 
-    def two_sides():
-        hcg.hc_block_step(case.x, case.pre_mix, case.fs[0], *pa.astuple(), h_norm=ha, y=ya, pre_out=prea,
-                          stream=stream)
-        hcg.hc_block_step(ya, prea, case.fs[1], *pf.astuple(), h_norm=ha, y=yf, pre_out=pref, stream=stream)
+    def make_two(st):
+        def two_sides():
+            hcg.hc_block_step(case.x, case.pre_mix, case.fs[0], *pa.astuple(), h_norm=ha, y=ya, pre_out=prea,
+                              stream=st)
+            hcg.hc_block_step(ya, prea, case.fs[1], *pf.astuple(), h_norm=ha, y=yf, pre_out=pref, stream=st)
+        return two_sides
+    two_sides = make_two(stream)
     for _ in range(5):
         two_sides()
     cold = _event_ms(two_sides, 50, stream, flush)
+    graph = _graph_ms(make_two, 50, stream, flush)
     alg = 2 * side_bytes(case.n)
     xb = inputs.bf16_bits_np(case.x)
     fbs = [inputs.bf16_bits_np(f) for f in case.fs]
@@ -480,6 +504,8 @@ def run_configs(dev, peak, stream):
         "workload": "decode: B=128, T=1, attention + FFN side, two hc_block_step launches (seed 1)",
         "tokens": case.n, "sides": 2, "us_per_side": 1e3 * statistics.mean(cold) / 2,
         "us_two_sides_median": 1e3 * statistics.median(cold),
+        "us_per_side_graph": 1e3 * statistics.mean(graph) / 2,
+        "graph": "both sides captured once into one CUDA graph and replayed, L2 flushed before each replay",
         "tokens_per_s": case.n / (statistics.mean(cold) / 1e3),
         "algorithmic_bytes": alg, "hbm_gbs": alg / (statistics.mean(cold) / 1e3) / 1e9,
         "roofline_frac": alg / (statistics.mean(cold) / 1e3) / 1e9 / peak,

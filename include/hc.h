@@ -313,6 +313,13 @@ hc_status hc_pre_norm_mxfp8(const uint16_t *x, const float *pre_mix, const float
  * Launch notes.  The chain kernels run one CTA on each of 16 * floor(SMs / 16)
  * SMs as a cooperative launch: they need that many SMs free to start, and a
  * CTA waits (bounded) on flags other CTAs write into the state buffer.
+ * hc_chain_begin and hc_chain_side cannot be captured into a CUDA graph: the
+ * flags carry an epoch that each launch draws on the host, and a replayed
+ * launch would take the previous replay's flags for its own.  On a stream
+ * that is capturing they return HC_ERR_UNSUPPORTED and enqueue nothing.
+ * hc_chain_norm and the other entry points have no such flags and can be
+ * captured (after one call outside the capture, which sets the kernels'
+ * attributes and caches the device's cluster occupancy).
  */
 #define HC_STATE_FLOATS 32
 

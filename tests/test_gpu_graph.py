@@ -1,0 +1,148 @@
+"""GPU: the side step recorded into a CUDA graph and replayed.
+
+A serving loop issues its small-batch side steps as graph replays; the
+kernels must then compute exactly what an eager call computes.  hc_block_step
+(the cluster kernel at four streams, the tcgen05 path at eight) and the
+backward are captured once and replayed on fresh inputs copied into the
+captured buffers; every output must equal the eager call's bit for bit.  The
+chain's launches carry a per-launch epoch for their cross-CTA flags, so they
+refuse a capturing stream (HC_ERR_UNSUPPORTED) and record nothing."""
+import pytest
+import torch
+
+import hyper_connection_residual_mixes_gb300 as hcg
+from hyper_connection_residual_mixes_gb300 import _lib, inputs
+from hyper_connection_residual_mixes_gb300 import build as hc_build
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    hc_build.build()
+    _lib.load()
+
+
+def _same(a, b):
+    assert a.dtype == b.dtype and a.shape == b.shape
+    if a.dtype == torch.bfloat16:
+        a, b = a.view(torch.int16), b.view(torch.int16)
+    elif a.dtype == torch.float32:
+        a, b = a.view(torch.int32), b.view(torch.int32)
+    assert torch.equal(a, b)
+
+
+def _inputs(seed, n, hc, d):
+    g = torch.Generator(device=DEV).manual_seed(seed)
+    x = inputs.streams(g, n, hc, d, device=DEV)
+    pm = inputs.pre_mix(g, n, hc, device=DEV)
+    fs = [inputs.sublayer_out(g, n, d, device=DEV) for _ in range(2)]
+    ps = [inputs.side_params(g, hc, d, device=DEV) for _ in range(2)]
+    return x, pm, fs, ps
+
+
+@pytest.mark.parametrize("n,hc,d", [(16, 4, 5120), (128, 4, 5120), (1000, 4, 1024), (2000, 8, 256)])
+def test_block_step_graph_replay(n, hc, d):
+    """Two side steps (the decode wiring: the second side reads the first
+    side's y with its pre) captured once; each replay on new streams equals
+    the eager calls."""
+    x, pm, fs, ps = _inputs(70 + n, n, hc, d)
+    h = [torch.empty((n, d), dtype=torch.bfloat16, device=DEV) for _ in range(2)]
+    y = [torch.empty_like(x) for _ in range(2)]
+    pre = [torch.empty_like(pm) for _ in range(2)]
+
+    def two_sides():
+        hcg.hc_block_step(x, pm, fs[0], *ps[0].astuple(), h_norm=h[0], y=y[0], pre_out=pre[0])
+        hcg.hc_block_step(y[0], pre[0], fs[1], *ps[1].astuple(), h_norm=h[1], y=y[1], pre_out=pre[1])
+
+    two_sides()  # one eager call first: kernel attributes, cached occupancy
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            two_sides()
+    torch.cuda.synchronize()
+    for rep in range(3):
+        x2, pm2, fs2, _ = _inputs(900 + 7 * rep + n, n, hc, d)
+        x.copy_(x2), pm.copy_(pm2), fs[0].copy_(fs2[0]), fs[1].copy_(fs2[1])
+        graph.replay()
+        torch.cuda.synchronize()
+        got = [t.clone() for t in (*h, *y, *pre)]
+        two_sides()
+        torch.cuda.synchronize()
+        for a, b in zip(got, (*h, *y, *pre)):
+            _same(a, b)
+    assert _lib.raw("hc_consume_device_error", None) == 0
+
+
+def test_backward_graph_replay():
+    """hc_block_step_backward (four streams, its eight launches) captured with
+    its workspace and replayed."""
+    n, hc, d = 257, 4, 1024
+    x, pm, fs, ps = _inputs(81, n, hc, d)
+    g = torch.Generator(device=DEV).manual_seed(82)
+    g_hn = torch.randn((n, d), device=DEV, generator=g)
+    g_y = torch.randn((n, hc, d), device=DEV, generator=g)
+    ws = torch.empty(_lib.load().hc_block_step_backward_workspace_bytes(n, hc, d), dtype=torch.uint8,
+                     device=DEV)
+    eager = hcg.hc_block_step_backward(x, pm, fs[0], *ps[0].astuple(), g_hn, g_y, workspace=ws)
+    torch.cuda.synchronize()
+    out = {k: torch.empty_like(v) for k, v in eager.items()}
+
+    def bwd():
+        r = hcg.hc_block_step_backward(x, pm, fs[0], *ps[0].astuple(), g_hn, g_y, workspace=ws)
+        for k in out:
+            out[k].copy_(r[k])
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            bwd()
+    torch.cuda.synchronize()
+    g_y.mul_(-0.5)
+    graph.replay()
+    torch.cuda.synchronize()
+    ref = hcg.hc_block_step_backward(x, pm, fs[0], *ps[0].astuple(), g_hn, g_y, workspace=ws)
+    torch.cuda.synchronize()
+    for k in ref:
+        _same(out[k], ref[k])
+    assert _lib.raw("hc_consume_device_error", None) == 0
+
+
+@pytest.mark.filterwarnings("ignore:The CUDA Graph is empty")  # nothing was recorded, as intended
+def test_chain_refuses_capture():
+    """hc_chain_begin and hc_chain_side return HC_ERR_UNSUPPORTED on a
+    capturing stream and record nothing; outside the capture they run."""
+    n, hc, d = 64, 4, 1024
+    x, pm, fs, ps = _inputs(83, n, hc, d)
+    p0, p1 = ps
+    state = hcg.hc_chain_begin(x, pm, p0.hc_fn, p0.hc_scale, p0.hc_base)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    errs = []
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            for call in (lambda: hcg.hc_chain_begin(x, pm, p0.hc_fn, p0.hc_scale, p0.hc_base),
+                         lambda: hcg.hc_chain_side(x, fs[0], state, p0.norm_w, p1.hc_fn, p1.hc_scale,
+                                                   p1.hc_base)):
+                with pytest.raises(_lib.HcError) as ei:
+                    call()
+                errs.append(str(ei.value))
+    torch.cuda.synchronize()
+    assert len(errs) == 2 and all("HC_ERR_UNSUPPORTED" in e for e in errs)
+    h, y, _ = hcg.hc_chain_side(x, fs[0], state, p0.norm_w)
+    hs, ys, _ = hcg.hc_block_step(x, pm, fs[0], *p0.astuple())
+    torch.cuda.synchronize()
+    _same(h, hs)
+    _same(y, ys)
+    assert _lib.raw("hc_consume_device_error", None) == 0
