@@ -1015,12 +1015,26 @@ def run_op(args, local_rank):
     (hc_mxfp8_cast) or RMSNorm(hc_pre) with the cast in its epilogue
     (hc_pre_norm_mxfp8), or the side step's backward (hc_block_step_backward,
     its launches over the batch); or one side step at another stream count
-    (side_step, --hc, 8,192 tokens).  One step is one call over the whole
-    batch; the inputs are larger than L2.  The oracle is timed beside it on a
-    sample (not for side_step: the stream_counts sub-record's workload)."""
+    (side_step, --hc, 8,192 tokens); or hc_split_sinkhorn on the Sinkhorn-only
+    stress rows (sinkhorn; 100 MB of inputs, below L2: for profiler captures,
+    the configs sub-record times it with L2 flushed).  One step is one call
+    over the whole batch.  The oracle is timed beside it on a sample (not for
+    side_step and sinkhorn: the stream_counts and configs sub-records'
+    workloads)."""
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     hcg._lib.load()
+    if args.op == "sinkhorn":
+        # the Sinkhorn-only stress rows (2^20, or --tokens rows), one hc_split_sinkhorn per step
+        m, sc, base = (t.to(dev) for t in inputs.sinkhorn_stress(device="cpu"))
+        if args.tokens:
+            m = m[:args.tokens].contiguous()
+        rows = m.shape[0]
+        pre_s, post_s = torch.empty((rows, HC), device=dev), torch.empty((rows, HC), device=dev)
+        comb_s = torch.empty((rows, HC, HC), device=dev)
+        fn = lambda: hcg.hc_split_sinkhorn(m, sc, base, pre=pre_s, post=post_s, comb=comb_s)
+        return _time_op(args, dev, local_rank, fn, rows * 192 + 12 + MIX * 4, rows, 0,
+                        "the split and Sinkhorn (hc_split_sinkhorn)", None, 1)
     if args.op == "side_step" or (args.op == "backward" and args.hc != HC):
         fn, alg, n, d, what, launches = (run_side_step_op if args.op == "side_step" else run_backward_hc_op)(args, dev)
         return _time_op(args, dev, local_rank, fn, alg, n, d, what, None, launches)
@@ -1082,16 +1096,23 @@ def _time_op(args, dev, local_rank, fn, alg, n, d, what, ctx, launches):
     clk = clocks.stop()
     ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
     peak, peak_kind = measured_peaks()
-    out = {"metric": "tokens/s through %s, %s tokens x d = %d" % (what, format(n, ","), d), "value": n / (ms / 1e3),
-           "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+    rows_op = d == 0  # the Sinkhorn op: rows of mixes, no d
+    out = {"metric": ("rows/s through %s, %s rows" % (what, format(n, ",")) if rows_op else
+                      "tokens/s through %s, %s tokens x d = %d" % (what, format(n, ","), d)),
+           "value": n / (ms / 1e3), "unit": "rows/s" if rows_op else "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
            "dtype": ("bf16 + fp32 in, fp32 arithmetic, fp32 gradients out" if args.op == "backward"
                      else "bf16 in, fp32 arithmetic, bf16 out" if args.op == "side_step"
+                     else "fp32" if rows_op
                      else "bf16 in, fp32 arithmetic, e4m3 + ue8m0 out"), "data": "synthetic, seeded",
-           "config": {"workload": ("stream_counts, one side step at hc = %d" % args.hc if args.hc != HC
+           "config": {"workload": ("sinkhorn_stress, 96 B of mixes in and 96 B out per row" if rows_op
+                                   else "stream_counts, one side step at hc = %d" % args.hc if args.hc != HC
                                    else "long_prefill, one side step" if args.op == "backward"
                                    else "long_prefill, one side's h_norm"),
-                      "op": args.op, "tokens": n, "d": d, "l2": "inputs larger than L2; no flush"},
+                      "op": args.op, "tokens": n, "d": d,
+                      "l2": ("inputs of %.1f MB, below L2, back to back (for profiler captures; the configs "
+                             "sub-record flushes L2)" % (n * 96 / 1e6) if rows_op
+                             else "inputs larger than L2; no flush")},
            "roofline": {"bound": "hbm", "achieved": alg / (ms / 1e3) / 1e9, "peak": peak, "unit": "GB/s",
                         "frac": alg / (ms / 1e3) / 1e9 / peak, "traffic": None,
                         "peak_source": peak_kind, "algorithmic_bytes_per_launch": alg},
@@ -1141,13 +1162,16 @@ def main():
                     help="with the chain, skip timing the one-launch-per-side path beside it")
     ap.add_argument("--path", choices=["chain", "step"], default="chain",
                     help="chain: the sides fused across sides (hc_chain_*); step: one hc_block_step per side")
-    ap.add_argument("--op", choices=["mxfp8_cast", "pre_norm_mxfp8", "backward", "side_step"], default=None,
+    ap.add_argument("--op", choices=["mxfp8_cast", "pre_norm_mxfp8", "backward", "side_step", "sinkhorn"],
+                    default=None,
                     help="time one kernel of the widened rows alone instead of the side steps "
-                         "(side_step: one hc_block_step at --hc streams)")
+                         "(side_step: one hc_block_step at --hc streams; sinkhorn: hc_split_sinkhorn on "
+                         "the Sinkhorn-only stress rows)")
     ap.add_argument("--hc", type=int, choices=[2, 4, 8], default=4,
                     help="with --op side_step or backward: the stream count (2 and 8 on the stream_counts inputs)")
     ap.add_argument("--tokens", type=int, default=None,
-                    help="with --op: tokens in the batch (default 65,536; smaller for profiler captures)")
+                    help="with --op: tokens (sinkhorn: rows) in the batch (default 65,536; 2^20 rows; "
+                         "smaller for profiler captures)")
     args = ap.parse_args()
     rank, local_rank, world = dist_env()
     if args.op is not None and args.impl == "ours":
