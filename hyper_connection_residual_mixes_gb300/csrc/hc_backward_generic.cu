@@ -562,29 +562,49 @@ kg_fn_tc(const uint16_t *__restrict__ x, const float *__restrict__ ws, int64_t n
 }
 
 // g_norm_w partial sums over runs of kWRun tokens: part[b][c] = sum_t h[t][c]
-// rs_h[t] g_hn[t][c], h as the forward rounds it (short runs: enough CTAs to
-// keep the loads in flight).
+// rs_h[t] g_hn[t][c], h as the forward rounds it.  A thread takes eight
+// columns (16-byte loads of each stream's x, two of g_hn) and walks the run's
+// tokens in order; 64-thread CTAs, enough of them to keep the loads in flight.
 constexpr int kWRun = 64;
+constexpr int kWThreads = 64;
 template <int HC>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kWThreads)
 kg_w_partial(const uint16_t *__restrict__ x, const float *__restrict__ g_hn, const float *__restrict__ ws,
              int64_t n, int d, float *__restrict__ part) {
     using L = Lay<HC>;
-    const int c = blockIdx.x * kThreads + threadIdx.x;
+    const int c = 8 * (blockIdx.x * kWThreads + threadIdx.x);  // columns c .. c + 7
     const int64_t t0 = (int64_t)blockIdx.y * kWRun;
     const int64_t t1 = (t0 + kWRun < n) ? t0 + kWRun : n;
     if (c >= d) return;
-    float acc = 0.0f;
-#pragma unroll 8
+    float acc[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
+#pragma unroll 4
     for (int64_t t = t0; t < t1; ++t) {
         const float *rec = ws + t * L::kWs;
-        const uint16_t *xt = x + t * HC * d;
-        float hv = __ldg(rec + L::kPm) * __uint_as_float((uint32_t)xt[c] << 16);
+        const uint16_t *xt = x + t * HC * d + c;
+        float hv[8], xv[8];
+        unpack8(__ldg(reinterpret_cast<const uint4 *>(xt)), xv);
+        const float pm0 = __ldg(rec + L::kPm);
 #pragma unroll
-        for (int s = 1; s < HC; ++s) hv = fmaf(__ldg(rec + L::kPm + s), __uint_as_float((uint32_t)xt[s * d + c] << 16), hv);
-        acc = fmaf(round_bf16(hv) * __ldg(rec + L::kRs), __ldg(g_hn + t * d + c), acc);
+        for (int e = 0; e < 8; ++e) hv[e] = pm0 * xv[e];
+#pragma unroll
+        for (int s = 1; s < HC; ++s) {
+            unpack8(__ldg(reinterpret_cast<const uint4 *>(xt + (int64_t)s * d)), xv);
+            const float pm = __ldg(rec + L::kPm + s);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) hv[e] = fmaf(pm, xv[e], hv[e]);
+        }
+        const float rs = __ldg(rec + L::kRs);
+        const float4 g0 = __ldg(reinterpret_cast<const float4 *>(g_hn + t * d + c));
+        const float4 g1 = __ldg(reinterpret_cast<const float4 *>(g_hn + t * d + c + 4));
+        const float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] = fmaf(round_bf16(hv[e]) * rs, g[e], acc[e]);
     }
-    part[(int64_t)blockIdx.y * d + c] = acc;
+    float4 *o = reinterpret_cast<float4 *>(part + (int64_t)blockIdx.y * d + c);
+    o[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    o[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
 }
 
 // per block: the sums over its tokens of g_z (g_hc_base terms) and gzm (g_hc_scale terms)
@@ -686,7 +706,7 @@ cudaError_t launch(const uint16_t *x, const float *pre_mix, const uint16_t *f, c
     kg_fn_tc<HC><<<dim3((unsigned)((K + kFnCols - 1) / kFnCols), (unsigned)blocks), kThreads, 0, s>>>(
         x, ws, n, (int)K, part_fn);
     kg_sum_blocks<<<(unsigned)((M * K + 255) / 256), 256, 0, s>>>(part_fn, blocks, M * K, g_fn);
-    kg_w_partial<HC><<<dim3((unsigned)((d + kThreads - 1) / kThreads), (unsigned)wruns), kThreads, 0, s>>>(
+    kg_w_partial<HC><<<dim3((unsigned)((d / 8 + kWThreads - 1) / kWThreads), (unsigned)wruns), kWThreads, 0, s>>>(
         x, g_hn, ws, n, d, part_w);
     kg_sum_blocks<<<(unsigned)((d + 255) / 256), 256, 0, s>>>(part_w, wruns, d, g_w);
     kg_small_partial<HC><<<(unsigned)blocks, kThreads, 0, s>>>(ws, n, part_s);
