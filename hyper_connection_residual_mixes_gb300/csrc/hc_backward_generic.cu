@@ -51,7 +51,7 @@ struct Lay {
     // tensor cores of kg_fn_tc; 16-byte aligned
     static constexpr int kGaP = (kK3 + 1 + 3) / 4 * 4;
     static constexpr int kWs = kGaP + (3 * kMix / 2 + 3) / 4 * 4;
-    static constexpr int kSmall = (kMix + 3 + 3) / 4 * 4;  // per-block partials of g_hc_base, g_hc_scale
+    static constexpr int kSmall = (kMix + 3 + 3) / 4 * 4;  // per-run partials of g_hc_base, g_hc_scale
     // token sums of kg_token: sum h^2, T = sum h w g_hn, sum x^2, g_post[HC],
     // g_comb[HC*HC], A[HC] = sum x_s w g_hn, B[HC] = sum x_s h
     static constexpr int kSH2 = 0, kST = 1, kSX2 = 2, kSPost = 3, kSComb = 3 + HC,
@@ -607,23 +607,26 @@ kg_w_partial(const uint16_t *__restrict__ x, const float *__restrict__ g_hn, con
     o[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
 }
 
-// per block: the sums over its tokens of g_z (g_hc_base terms) and gzm (g_hc_scale terms)
+// per run of kSRun tokens: the sums over its tokens of g_z (g_hc_base terms)
+// and gzm (g_hc_scale terms).  Short runs, so that the launch has enough CTAs
+// to keep the record loads in flight.
+constexpr int kSRun = 128;
 template <int HC>
 __global__ void __launch_bounds__(kThreads)
 kg_small_partial(const float *__restrict__ ws, int64_t n, float *__restrict__ part) {
     // field j (g_z, then gzm: kGz + kMix = kGzm) = 32 fc + lane; warp w sums
-    // tokens 128 w .. 128 w + 127 of the block, then the warp sums in warp order
+    // tokens 16 w .. 16 w + 15 of the run, then the warp sums in warp order
     using L = Lay<HC>;
     constexpr int F = L::kMix + 3;
     __shared__ float red[kWarps][32];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t tw = (int64_t)blockIdx.x * kTokBlock + (int64_t)warp * (kTokBlock / kWarps);
+    const int64_t tw = (int64_t)blockIdx.x * kSRun + (int64_t)warp * (kSRun / kWarps);
     for (int fc = 0; fc < (F + 31) / 32; ++fc) {
         const int j = 32 * fc + lane;
         float acc = 0.0f;
         if (j < F) {
 #pragma unroll 8
-            for (int u = 0; u < kTokBlock / kWarps; ++u)
+            for (int u = 0; u < kSRun / kWarps; ++u)
                 if (tw + u < n) acc += ws[(tw + u) * L::kWs + L::kGz + j];
         }
         red[warp][lane] = acc;
@@ -638,7 +641,7 @@ kg_small_partial(const float *__restrict__ ws, int64_t n, float *__restrict__ pa
     }
 }
 
-// out[j] = sum_b part[b][j], blocks in order.
+// out[j] = sum_b part[b][j], blocks (or runs) in order.
 __global__ void kg_sum_blocks(const float *__restrict__ part, int blocks, int64_t len, float *__restrict__ out) {
     const int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (j >= len) return;
@@ -648,13 +651,13 @@ __global__ void kg_sum_blocks(const float *__restrict__ part, int blocks, int64_
 }
 
 template <int HC>
-__global__ void kg_small_final(const float *__restrict__ part, int blocks, float *__restrict__ g_base,
+__global__ void kg_small_final(const float *__restrict__ part, int runs, float *__restrict__ g_base,
                                float *__restrict__ g_scale) {
     using L = Lay<HC>;
     const int j = threadIdx.x;
     if (j >= L::kMix + 3) return;
     float s = 0.0f;
-    for (int b = 0; b < blocks; ++b) s += part[(int64_t)b * L::kSmall + j];
+    for (int b = 0; b < runs; ++b) s += part[(int64_t)b * L::kSmall + j];
     if (j < L::kMix) g_base[j] = s;
     else g_scale[j - L::kMix] = s;
 }
@@ -664,8 +667,9 @@ size_t ws_bytes(int64_t n, int d) {
     using L = Lay<HC>;
     const int64_t blocks = (n + kTokBlock - 1) / kTokBlock;
     const int64_t wruns = (n + kWRun - 1) / kWRun;
+    const int64_t sruns = (n + kSRun - 1) / kSRun;
     const int64_t K = (int64_t)HC * d;
-    return (size_t)(n * L::kWs + blocks * (L::kMix * K + L::kSmall) + wruns * d) * sizeof(float) +
+    return (size_t)(n * L::kWs + blocks * L::kMix * K + sruns * L::kSmall + wruns * d) * sizeof(float) +
            proj_umma_wsplit_bytes(HC, K);
 }
 
@@ -684,7 +688,8 @@ cudaError_t launch(const uint16_t *x, const float *pre_mix, const uint16_t *f, c
     const int wruns = (int)((n + kWRun - 1) / kWRun);
     float *part_w = part_fn + (int64_t)blocks * M * K;
     float *part_s = part_w + (int64_t)wruns * d;
-    uint16_t *wsplit = reinterpret_cast<uint16_t *>(part_s + (int64_t)blocks * L::kSmall);
+    const int sruns = (int)((n + kSRun - 1) / kSRun);
+    uint16_t *wsplit = reinterpret_cast<uint16_t *>(part_s + (int64_t)sruns * L::kSmall);
     // kg_token: one warp per token, up to four per CTA within 200 KB of iterates
     const size_t per_warp = ((size_t)(2 * iters + 1) * HC * HC + L::kSums) * sizeof(float);
     int tok_warps = (int)((200u << 10) / per_warp);
@@ -709,8 +714,8 @@ cudaError_t launch(const uint16_t *x, const float *pre_mix, const uint16_t *f, c
     kg_w_partial<HC><<<dim3((unsigned)((d / 8 + kWThreads - 1) / kWThreads), (unsigned)wruns), kWThreads, 0, s>>>(
         x, g_hn, ws, n, d, part_w);
     kg_sum_blocks<<<(unsigned)((d + 255) / 256), 256, 0, s>>>(part_w, wruns, d, g_w);
-    kg_small_partial<HC><<<(unsigned)blocks, kThreads, 0, s>>>(ws, n, part_s);
-    kg_small_final<HC><<<1, 128, 0, s>>>(part_s, blocks, g_base, g_scale);
+    kg_small_partial<HC><<<(unsigned)sruns, kThreads, 0, s>>>(ws, n, part_s);
+    kg_small_final<HC><<<1, 128, 0, s>>>(part_s, sruns, g_base, g_scale);
     return cudaGetLastError();
 }
 
