@@ -650,6 +650,30 @@ __global__ void kg_sum_blocks(const float *__restrict__ part, int blocks, int64_
     out[j] = s;
 }
 
+// out[c] = sum_r part[r][c] over many runs: a CTA takes 32 columns, its eight
+// warps each add an eighth of the runs in order, then the warp sums are added
+// in warp order (enough CTAs for the loads to be in flight together).
+__global__ void __launch_bounds__(kThreads)
+kg_sum_runs(const float *__restrict__ part, int runs, int d, float *__restrict__ out) {
+    __shared__ float red[kWarps][32];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int c = blockIdx.x * 32 + lane;
+    const int per = (runs + kWarps - 1) / kWarps;
+    const int r0 = warp * per, r1 = (r0 + per < runs) ? r0 + per : runs;
+    float acc = 0.0f;
+    if (c < d)
+#pragma unroll 4
+        for (int r = r0; r < r1; ++r) acc += part[(int64_t)r * d + c];
+    red[warp][lane] = acc;
+    __syncthreads();
+    if (warp == 0 && c < d) {
+        float v = red[0][lane];
+#pragma unroll
+        for (int w = 1; w < kWarps; ++w) v += red[w][lane];
+        out[c] = v;
+    }
+}
+
 template <int HC>
 __global__ void kg_small_final(const float *__restrict__ part, int runs, float *__restrict__ g_base,
                                float *__restrict__ g_scale) {
@@ -713,7 +737,7 @@ cudaError_t launch(const uint16_t *x, const float *pre_mix, const uint16_t *f, c
     kg_sum_blocks<<<(unsigned)((M * K + 255) / 256), 256, 0, s>>>(part_fn, blocks, M * K, g_fn);
     kg_w_partial<HC><<<dim3((unsigned)((d / 8 + kWThreads - 1) / kWThreads), (unsigned)wruns), kWThreads, 0, s>>>(
         x, g_hn, ws, n, d, part_w);
-    kg_sum_blocks<<<(unsigned)((d + 255) / 256), 256, 0, s>>>(part_w, wruns, d, g_w);
+    kg_sum_runs<<<(unsigned)((d + 31) / 32), kThreads, 0, s>>>(part_w, wruns, d, g_w);
     kg_small_partial<HC><<<(unsigned)sruns, kThreads, 0, s>>>(ws, n, part_s);
     kg_small_final<HC><<<1, 128, 0, s>>>(part_s, sruns, g_base, g_scale);
     return cudaGetLastError();
