@@ -55,23 +55,6 @@ hc_status check_shape(int64_t n, int hc, int d, bool uses_d) {
     return HC_OK;
 }
 
-// HC_ERR_UNSUPPORTED when work enqueued on s would be recorded into a CUDA
-// graph (or the query is refused because a capture is under way, as it is
-// for the legacy stream while another stream captures); HC_ERR_CUDA for any
-// other failure of the query.  The chain's cross-CTA flags carry a
-// per-launch epoch passed as a kernel argument, so a replayed capture would
-// see the flags of its previous replay as current: the chain refuses capture.
-hc_status refuse_capture(cudaStream_t s) {
-    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-    const cudaError_t e = cudaStreamIsCapturing(s, &cs);
-    if (e == cudaErrorStreamCaptureImplicit || e == cudaErrorStreamCaptureUnsupported) {
-        (void)cudaGetLastError();  // the refused query is not the caller's error
-        return HC_ERR_UNSUPPORTED;
-    }
-    if (e != cudaSuccess) return cuda_status(e);
-    return cs == cudaStreamCaptureStatusNone ? HC_OK : HC_ERR_UNSUPPORTED;
-}
-
 // Every output span must be disjoint from every input span and from the other outputs.
 hc_status check_alias(const Span *outs, int n_out, const Span *ins, int n_in) {
     for (int i = 0; i < n_out; ++i) {
@@ -369,7 +352,6 @@ hc_status hc_chain_begin(const uint16_t *x, const float *pre_mix, const float *h
     const Span outs[] = {span(state_out, (int64_t)state_bytes), span(pre_out, pre_out ? n * hc * 4 : 0),
                          span(h_pre_out, h_pre_out ? n * d * 2 : 0)};
     if ((st = check_alias(outs, 3, ins, 5)) != HC_OK) return st;
-    if ((st = refuse_capture(stream)) != HC_OK) return st;
     return cuda_status(hc::launch_slices_begin(x, pre_mix, hc_fn, hc_scale, hc_base, n, d,
                                                sinkhorn_iters, eps, norm_eps, state_out, pre_out,
                                                h_pre_out, stream));
@@ -417,7 +399,6 @@ hc_status hc_chain_side(const uint16_t *x, const uint16_t *f, const float *state
                          span(pre_out, (next && pre_out) ? n * hc * 4 : 0),
                          span(h_pre_out, h_pre_out ? n * d * 2 : 0)};
     if ((st = check_alias(outs, 5, ins, 7)) != HC_OK) return st;
-    if ((st = refuse_capture(stream)) != HC_OK) return st;
     return cuda_status(hc::launch_slices_side(x, f, state_in, norm_w, hc_fn_next, hc_scale_next,
                                               hc_base_next, n, d, sinkhorn_iters, eps, norm_eps,
                                               h_norm, y, next ? state_out : nullptr,

@@ -24,7 +24,10 @@
 //    the sublayer input h_norm) reads them, so no CTA waits for another within
 //    a launch except an owner for the 16 partial sums of its tokens.
 //  * Flags hold the launch's epoch (a 64-bit value that differs from launch to
-//    launch), so scratch never needs clearing.  Launches are cooperative: every
+//    launch), so scratch never needs clearing.  A one-thread kernel enqueued
+//    just before each launch writes the epoch into the state buffer's header
+//    from a device counter, so a launch recorded into a CUDA graph draws a new
+//    epoch at every replay.  Launches are cooperative: every
 //    CTA is resident, so a wait on another CTA's flag always ends; every wait
 //    is bounded anyway and reports a timeout through the device error flag.
 //
@@ -44,7 +47,6 @@
 // quadrant w); warp 4 TMA producer; warp 5 owner reduction + Sinkhorn; warps
 // 6-13 CUDA-core streaming math; warp 14 sends each tile's partial sums; warp
 // 15 TMA stores of y and h_norm.
-#include <atomic>
 #include <chrono>
 
 #include <cuda.h>
@@ -115,7 +117,7 @@ struct Params {
     int64_t part_tok, part_slice;
     unsigned long long *arrive;  // arrival flag of (tile j, slice c): arrive + j*arr_tile + c*arr_slice
     int64_t arr_tile, arr_slice;
-    unsigned long long epoch;
+    const unsigned long long *epoch;  // this launch's epoch (header of state_out)
     int64_t n;
     int d;
     int iters;
@@ -123,6 +125,15 @@ struct Params {
     float norm_eps;
     int num_tiles;
 };
+
+// The next epoch into a state buffer's header, just before the launch that
+// writes the buffer (same stream): each launch, and each replay of a captured
+// one, takes a value no earlier launch of the process has taken.
+__device__ unsigned long long g_chain_launches = 0;
+__global__ void k_chain_epoch(unsigned long long *hdr, unsigned long long base) {
+    *hdr = base + atomicAdd(&g_chain_launches, 1ull) + 1ull;
+}
+constexpr bool kAnyP1Of(int mode) { return mode != kLast; }
 
 // Shared-memory layout (byte offsets from a 1024-aligned base).
 struct Layout {
@@ -194,6 +205,8 @@ k_slices(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUten
          const __grid_constant__ CUtensorMap tm_s, const Params p) {
     constexpr bool kAnyP1 = kMode != kLast;
     constexpr bool kAnyP3 = kMode != kBegin;
+    // written by k_chain_epoch, which ran to completion before this launch began
+    const unsigned long long epoch = kAnyP1 ? *reinterpret_cast<const volatile unsigned long long *>(p.epoch) : 0ull;
     constexpr bool kPmRows = kMode == kBegin;  // phase 1 reads pre_mix rows
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -486,7 +499,7 @@ k_slices(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUten
                 const int tile = g + k * m;
                 const int64_t tok = (int64_t)tile * kT + tk;
                 bool ok = true;
-                if (lane < kS) ok = flag_wait(p.arrive + (int64_t)tile * p.arr_tile + (int64_t)lane * p.arr_slice, p.epoch, &s_abort);
+                if (lane < kS) ok = flag_wait(p.arrive + (int64_t)tile * p.arr_tile + (int64_t)lane * p.arr_slice, epoch, &s_abort);
                 if (!__all_sync(0xffffffffu, ok)) break;
                 __threadfence();
                 float mv[kMix + 2];
@@ -590,7 +603,7 @@ k_slices(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUten
                 }
                 __threadfence();
                 __syncwarp();
-                if (lane == 0) st_release_u64(p.arrive + (int64_t)tile * p.arr_tile + (int64_t)c * p.arr_slice, p.epoch);
+                if (lane == 0) st_release_u64(p.arrive + (int64_t)tile * p.arr_tile + (int64_t)c * p.arr_slice, epoch);
                 ++tiles_done;
             }
         }
@@ -890,13 +903,14 @@ bool slices_state_tmap(CUtensorMap *map, const float *base, int64_t rows) {
                CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// A value no earlier launch of this process used: flags written by an earlier
-// launch (or left in a reused buffer) never match the current launch's.
-unsigned long long next_epoch() {
-    static std::atomic<unsigned long long> counter{0};
+// The epochs: a per-process base (below 2^63, drawn from the clock) plus the
+// count of chain launches so far on the device, so that flags written by an
+// earlier launch (or left in a reused buffer) never match the current one's.
+unsigned long long epoch_base() {
     static const unsigned long long base =
-        (unsigned long long)std::chrono::steady_clock::now().time_since_epoch().count() * 0x9E3779B97F4A7C15ull;
-    return base + 2 * counter.fetch_add(1) + 1;
+        ((unsigned long long)std::chrono::steady_clock::now().time_since_epoch().count() * 0x9E3779B97F4A7C15ull) >>
+        1;
+    return base;
 }
 
 int g_slices_ctas[64] = {};  // co-resident CTAs per device (one per SM)
@@ -948,17 +962,21 @@ cudaError_t launch_slices_impl(sl::Params p, const uint16_t *x, const uint16_t *
     }
     if (kH != sl::kHNone && !slices_tmap(&tmh, h, p.n, d)) return cudaErrorInvalidValue;
     p.num_tiles = (int)tiles;
-    p.epoch = next_epoch();
+    if (sl::kAnyP1Of(kMode)) {
+        sl::k_chain_epoch<<<1, 1, 0, s>>>(const_cast<unsigned long long *>(p.epoch), epoch_base());
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
     e = cudaLaunchKernelEx(&cfg, kern, tmx, tmf, tmy, tmh, tms, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
 // Scratch of the chain inside a state buffer: after the n coefficient rows
-// (rounded up to 256 bytes), the partial sums [n][16][28] fp32, then the
-// arrival flags [tiles][16] u64.
+// (rounded up to 256 bytes), the partial sums [n][16][28] fp32, the arrival
+// flags [tiles][16] u64, then a 16-byte header holding the epoch of the launch
+// that writes this buffer.
 struct ChainScratch {
-    size_t part_off, flag_off, total;
+    size_t part_off, flag_off, hdr_off, total;
 };
 ChainScratch chain_scratch(int64_t n) {
     ChainScratch cs;
@@ -966,7 +984,8 @@ ChainScratch chain_scratch(int64_t n) {
     cs.part_off = rows;
     cs.flag_off = cs.part_off + (size_t)n * sl::kS * sl::kPartF * 4;
     const size_t tiles = (size_t)((n + sl::kT - 1) / sl::kT);
-    cs.total = cs.flag_off + tiles * sl::kS * 8;
+    cs.hdr_off = cs.flag_off + tiles * sl::kS * 8;
+    cs.total = cs.hdr_off + 16;
     return cs;
 }
 
@@ -979,6 +998,7 @@ void set_chain_scratch(sl::Params &p, float *state_out) {
     p.arrive = reinterpret_cast<unsigned long long *>(base + cs.flag_off);
     p.arr_tile = sl::kS;
     p.arr_slice = 1;
+    p.epoch = reinterpret_cast<const unsigned long long *>(base + cs.hdr_off);
 }
 
 }  // namespace

@@ -266,8 +266,8 @@ hc_status hc_pre_norm_mxfp8(const uint16_t *x, const float *pre_mix, const float
  *   rsqrt(mean(h^2) + norm_eps), [21:24] zero, [24:28] pre (the side's pre:
  *   the next side's pre_mix), [28:32] pre_mix (the one the side reads with);
  * the rest is the kernels' scratch for one launch (partial sums of the
- * cross-slice reductions and their arrival flags; nothing in it needs
- * clearing).  The caller keeps two buffers in rotation: side i reads the rows
+ * cross-slice reductions, their arrival flags and the launch's epoch;
+ * nothing in it needs clearing).  The caller keeps two buffers in rotation: side i reads the rows
  * of side i and writes the buffer of side i + 1 (the two may not overlap:
  * HC_ERR_ALIAS).  No cited passage has a counterpart for the state: it
  * carries one side's coefficients to the next launch.
@@ -313,13 +313,12 @@ hc_status hc_pre_norm_mxfp8(const uint16_t *x, const float *pre_mix, const float
  * Launch notes.  The chain kernels run one CTA on each of 16 * floor(SMs / 16)
  * SMs as a cooperative launch: they need that many SMs free to start, and a
  * CTA waits (bounded) on flags other CTAs write into the state buffer.
- * hc_chain_begin and hc_chain_side cannot be captured into a CUDA graph: the
- * flags carry an epoch that each launch draws on the host, and a replayed
- * launch would take the previous replay's flags for its own.  On a stream
- * that is capturing they return HC_ERR_UNSUPPORTED and enqueue nothing.
- * hc_chain_norm and the other entry points have no such flags and can be
- * captured (after one call outside the capture, which sets the kernels'
- * attributes and caches the device's cluster occupancy).
+ * The flags carry an epoch that a one-thread kernel, enqueued just before
+ * each hc_chain_begin / hc_chain_side launch, writes into the state buffer
+ * from a device counter; so the chain, like every other entry point, can be
+ * recorded into a CUDA graph and replayed (after one call outside the
+ * capture, which sets the kernels' attributes and caches the device's SM and
+ * cluster occupancy).
  */
 #define HC_STATE_FLOATS 32
 

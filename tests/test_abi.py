@@ -188,10 +188,11 @@ def test_chain_side_last_needs_no_state_and_empty_is_ok(lib):
 
 def test_chain_state_bytes(lib):
     """Coefficient rows (128 bytes per token, rounded up to 256), then 16 x 28
-    fp32 partial sums per token, then 16 eight-byte flags per 64-token tile."""
+    fp32 partial sums per token, then 16 eight-byte flags per 64-token tile,
+    then a 16-byte header (the epoch of the launch that writes the buffer)."""
     for n in (1, 64, 65, 1000, 65536):
         tiles = -(-n // 64)
-        assert lib.hc_chain_state_bytes(n, 4, 5120) == ((128 * n + 255) // 256) * 256 + 1792 * n + 128 * tiles
+        assert lib.hc_chain_state_bytes(n, 4, 5120) == ((128 * n + 255) // 256) * 256 + 1792 * n + 128 * tiles + 16
     assert lib.hc_chain_state_bytes(16, 4, 320) == 0      # not served by the chain
     assert lib.hc_chain_state_bytes(16, 2, 5120) == 0
     assert lib.hc_chain_state_bytes(-1, 4, 5120) == 0

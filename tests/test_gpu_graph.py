@@ -4,9 +4,9 @@ A serving loop issues its small-batch side steps as graph replays; the
 kernels must then compute exactly what an eager call computes.  hc_block_step
 (the cluster kernel at four streams, the tcgen05 path at eight) and the
 backward are captured once and replayed on fresh inputs copied into the
-captured buffers; every output must equal the eager call's bit for bit.  The
-chain's launches carry a per-launch epoch for their cross-CTA flags, so they
-refuse a capturing stream (HC_ERR_UNSUPPORTED) and record nothing."""
+captured buffers; every output must equal the eager call's bit for bit.  So
+is the chain, whose cross-CTA flags take a new epoch at every replay (written
+on the device into its state buffer just before each launch)."""
 import pytest
 import torch
 
@@ -117,32 +117,43 @@ def test_backward_graph_replay():
     assert _lib.raw("hc_consume_device_error", None) == 0
 
 
-@pytest.mark.filterwarnings("ignore:The CUDA Graph is empty")  # nothing was recorded, as intended
-def test_chain_refuses_capture():
-    """hc_chain_begin and hc_chain_side return HC_ERR_UNSUPPORTED on a
-    capturing stream and record nothing; outside the capture they run."""
-    n, hc, d = 64, 4, 1024
+def test_chain_graph_replay():
+    """The chain (its first launch, a side with the next side's weights, the
+    last side) captured once; each replay on new streams and sublayer outputs
+    equals hc_block_step side after side, bit for bit.  Each replay draws new
+    epochs for the cross-CTA flags, while the state buffers still hold the
+    flags of the replay before it."""
+    n, hc, d = 200, 4, 1024
     x, pm, fs, ps = _inputs(83, n, hc, d)
     p0, p1 = ps
-    state = hcg.hc_chain_begin(x, pm, p0.hc_fn, p0.hc_scale, p0.hc_base)
+    st = [hcg.chain_state(n, d, DEV) for _ in range(2)]
+    h = [torch.empty((n, d), dtype=torch.bfloat16, device=DEV) for _ in range(2)]
+    y = [torch.empty_like(x) for _ in range(2)]
+    pre = [torch.empty_like(pm) for _ in range(2)]
+
+    def chain():
+        hcg.hc_chain_begin(x, pm, p0.hc_fn, p0.hc_scale, p0.hc_base, state_out=st[0], pre_out=pre[0])
+        hcg.hc_chain_side(x, fs[0], st[0], p0.norm_w, p1.hc_fn, p1.hc_scale, p1.hc_base, h_norm=h[0], y=y[0],
+                          state_out=st[1], pre_out=pre[1])
+        hcg.hc_chain_side(y[0], fs[1], st[1], p1.norm_w, h_norm=h[1], y=y[1])
+
+    chain()  # one eager call first
     torch.cuda.synchronize()
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
     graph = torch.cuda.CUDAGraph()
-    errs = []
     with torch.cuda.stream(s):
         with torch.cuda.graph(graph, stream=s):
-            for call in (lambda: hcg.hc_chain_begin(x, pm, p0.hc_fn, p0.hc_scale, p0.hc_base),
-                         lambda: hcg.hc_chain_side(x, fs[0], state, p0.norm_w, p1.hc_fn, p1.hc_scale,
-                                                   p1.hc_base)):
-                with pytest.raises(_lib.HcError) as ei:
-                    call()
-                errs.append(str(ei.value))
+            chain()
     torch.cuda.synchronize()
-    assert len(errs) == 2 and all("HC_ERR_UNSUPPORTED" in e for e in errs)
-    h, y, _ = hcg.hc_chain_side(x, fs[0], state, p0.norm_w)
-    hs, ys, _ = hcg.hc_block_step(x, pm, fs[0], *p0.astuple())
-    torch.cuda.synchronize()
-    _same(h, hs)
-    _same(y, ys)
+    for rep in range(4):
+        x2, pm2, fs2, _ = _inputs(950 + 3 * rep, n, hc, d)
+        x.copy_(x2), pm.copy_(pm2), fs[0].copy_(fs2[0]), fs[1].copy_(fs2[1])
+        graph.replay()
+        torch.cuda.synchronize()
+        h0, y0, q0 = hcg.hc_block_step(x, pm, fs[0], *p0.astuple())
+        h1, y1, q1 = hcg.hc_block_step(y0, q0, fs[1], *p1.astuple())
+        torch.cuda.synchronize()
+        for a, b in ((h[0], h0), (y[0], y0), (pre[0], q0), (h[1], h1), (y[1], y1), (pre[1], q1)):
+            _same(a, b)
     assert _lib.raw("hc_consume_device_error", None) == 0
