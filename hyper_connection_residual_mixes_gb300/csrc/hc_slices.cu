@@ -27,9 +27,10 @@
 //    launch), so scratch never needs clearing.  A one-thread kernel enqueued
 //    just before each launch writes the epoch into the state buffer's header
 //    from a device counter, so a launch recorded into a CUDA graph draws a new
-//    epoch at every replay.  Launches are cooperative: every
-//    CTA is resident, so a wait on another CTA's flag always ends; every wait
-//    is bounded anyway and reports a timeout through the device error flag.
+//    epoch at every replay.  Launches with flags are cooperative: every CTA
+//    is resident, so a wait on another CTA's flag always ends; every wait is
+//    bounded anyway and reports a timeout through the device error flag.  The
+//    last side's launch (phase 3 alone) has no flags and is an ordinary one.
 //
 // Modes: kBegin (phase 1 of a chain's first side, on its x), kSide (phase 3 of
 // side i, then phase 1 of side i + 1 on the y it has just produced), kLast
@@ -946,7 +947,9 @@ cudaError_t launch_slices_impl(sl::Params p, const uint16_t *x, const uint16_t *
     attr[0].id = cudaLaunchAttributeCooperative;
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    // only launches with a cross-slice reduction wait on other CTAs' flags and need
+    // every CTA resident; the last side's (phase 3 alone) is an ordinary launch
+    cfg.numAttrs = sl::kAnyP1Of(kMode) ? 1 : 0;
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(sl::kThreads);
     cfg.dynamicSmemBytes = L.total;

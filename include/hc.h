@@ -311,8 +311,9 @@ hc_status hc_pre_norm_mxfp8(const uint16_t *x, const float *pre_mix, const float
  *   At least one of h_norm and codes; d a multiple of 64.
  *
  * Launch notes.  The chain kernels run one CTA on each of 16 * floor(SMs / 16)
- * SMs as a cooperative launch: they need that many SMs free to start, and a
- * CTA waits (bounded) on flags other CTAs write into the state buffer.
+ * SMs; hc_chain_begin and hc_chain_side with the next side's weights launch
+ * cooperatively: they need that many SMs free to start, and a CTA waits
+ * (bounded) on flags other CTAs write into the state buffer.
  * The flags carry an epoch that a one-thread kernel, enqueued just before
  * each hc_chain_begin / hc_chain_side launch, writes into the state buffer
  * from a device counter; so the chain, like every other entry point, can be
