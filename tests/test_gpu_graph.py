@@ -157,3 +157,59 @@ def test_chain_graph_replay():
         for a, b in ((h[0], h0), (y[0], y0), (pre[0], q0), (h[1], h1), (y[1], y1), (pre[1], q1)):
             _same(a, b)
     assert _lib.raw("hc_consume_device_error", None) == 0
+
+
+def test_chain_model_order_graph_replay():
+    """The model's inner loop as one CUDA graph: per side, hc_chain_norm (the
+    side's h_norm), a stand-in sublayer on it (torch on the GPU), and the
+    side's chain launch (y_i and side i + 1's bf16 h), over three sides.
+    Replays on new streams equal the same sequence run eagerly, bit for bit."""
+    n, hc, d, S = 256, 4, 2048, 3
+    g = torch.Generator(device=DEV).manual_seed(85)
+    x = inputs.streams(g, n, hc, d, device=DEV)
+    pm = inputs.pre_mix(g, n, hc, device=DEV)
+    ps = [inputs.side_params(g, hc, d, device=DEV) for _ in range(S)]
+    st = [hcg.chain_state(n, d, DEV) for _ in range(2)]
+    hp = [torch.empty((n, d), dtype=torch.bfloat16, device=DEV) for _ in range(2)]
+    hn = [torch.empty((n, d), dtype=torch.bfloat16, device=DEV) for _ in range(S)]
+    fo = [torch.empty((n, d), dtype=torch.bfloat16, device=DEV) for _ in range(S)]
+    ys = [torch.empty_like(x) for _ in range(S)]
+    pre = [torch.empty_like(pm) for _ in range(S)]
+
+    def model():
+        p0 = ps[0]
+        hcg.hc_chain_begin(x, pm, p0.hc_fn, p0.hc_scale, p0.hc_base, state_out=st[0], pre_out=pre[0],
+                           h_pre_out=hp[0])
+        xi = x
+        for i in range(S):
+            hcg.hc_chain_norm(hp[i % 2], st[i % 2], ps[i].norm_w, h_norm=hn[i])
+            fo[i].copy_((2.0 * torch.tanh(hn[i].float())).to(torch.bfloat16))  # the sublayer stand-in
+            if i + 1 < S:
+                q = ps[i + 1]
+                hcg.hc_chain_side(xi, fo[i], st[i % 2], ps[i].norm_w, q.hc_fn, q.hc_scale, q.hc_base, y=ys[i],
+                                  state_out=st[(i + 1) % 2], pre_out=pre[i + 1], h_pre_out=hp[(i + 1) % 2])
+            else:
+                hcg.hc_chain_side(xi, fo[i], st[i % 2], ps[i].norm_w, y=ys[i], write_h_norm=False)
+            xi = ys[i]
+
+    model()  # one eager call first
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            model()
+    torch.cuda.synchronize()
+    for rep in range(3):
+        g2 = torch.Generator(device=DEV).manual_seed(990 + rep)
+        x.copy_(inputs.streams(g2, n, hc, d, device=DEV))
+        pm.copy_(inputs.pre_mix(g2, n, hc, device=DEV))
+        graph.replay()
+        torch.cuda.synchronize()
+        got = [t.clone() for t in (*hn, *fo, *ys, *pre)]
+        model()
+        torch.cuda.synchronize()
+        for a, b in zip(got, (*hn, *fo, *ys, *pre)):
+            _same(a, b)
+    assert _lib.raw("hc_consume_device_error", None) == 0
