@@ -380,80 +380,127 @@ kg_gx(const uint16_t *__restrict__ x, const float *__restrict__ hc_fn, const flo
     }
 }
 
-// The same g_x and g_f for 16 tokens per CTA, so that hc_fn is read once per 16
-// tokens (kg_gx reads all of it per token: 13 MB at eight streams).  The CTA
-// walks d in chunks of 64 columns (32 at eight streams): first the projection term
-// D[t][s][c] = sum_i g_a[t][i] W[i][s*d + c] for its tokens into shared memory
-// (each thread two (stream, column) pairs, W read from L2 once per chunk),
-// then the rest per (token, column) as kg_gx computes it, plus D.  Sums are
-// fp32 in index order (i, then the terms in kg_gx's order), as kg_gx.
+// The same g_x and g_f for 16 tokens per CTA (hc >= 8), so that hc_fn is read
+// once per 16 tokens (kg_gx reads all of it per token: 13 MB at eight
+// streams).  The CTA walks d in chunks of 64 columns: first the projection
+// term D[t][s][c] = sum_i g_a[t][i] W[i][s*d + c] for its tokens into shared
+// memory (each thread HC * 64 / 256 (stream, column) pairs, W read from L2
+// once per chunk, g_a kept mix-major so that one i gives the 16 tokens' values
+// in four 16-byte loads); then the rest per (token, column) as kg_gx computes
+// it, plus D, with two adjacent columns per thread (8-byte loads and stores of
+// the fp32 streams) in two passes of eight tokens.  Only the record fields
+// that part reads are staged.  Sums are fp32 in index order (i, then the
+// terms in kg_gx's order), as kg_gx.  At most 64 registers: four CTAs per SM,
+// so that 8,192 tokens (512 CTAs) fit in one wave.
 constexpr int kGxT = 16;     // tokens per CTA
 constexpr int kGxTokSmall = 4;  // tokens per CTA of kg_gx (hc = 2): hc_fn read once per 4 tokens
+constexpr int kGxC = 64;     // columns of d per chunk
 template <int HC>
-__host__ __device__ constexpr int gx_cols() { return HC == 8 ? 32 : 64; }  // columns of d per chunk
-template <int HC>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 4)
 kg_gx_tiled(const uint16_t *__restrict__ x, const float *__restrict__ hc_fn, const float *__restrict__ norm_w,
             const float *__restrict__ g_hn, const float *__restrict__ g_y, const float *__restrict__ ws,
             int64_t n, int d, float *__restrict__ g_x, float *__restrict__ g_f) {
     using L = Lay<HC>;
     constexpr int M = L::kMix;
-    constexpr int kGxC = gx_cols<HC>();
-    __shared__ float rec[kGxT][L::kWs];
-    __shared__ float dsum[kGxT][HC][kGxC];  // at most 48 KB with rec
+    constexpr int kPairs = HC * kGxC / kThreads;
+    constexpr int kF = L::kK3 + 1 - L::kPost;
+    static_assert(HC * kGxC % kThreads == 0 && kGxT == 16 && kGxT * kGxC / 2 == 2 * kThreads, "thread maps");
+    __shared__ __align__(16) float gaT[M][kGxT];
+    __shared__ float fld[kGxT][kF];
+    __shared__ __align__(16) float dsum[kGxT][HC][kGxC];
     const int64_t t0 = (int64_t)blockIdx.x * kGxT;
     const int cnt = (int)((n - t0 < kGxT) ? n - t0 : kGxT);
     const int64_t K = (int64_t)HC * d;
-    for (int q = threadIdx.x; q < kGxT * L::kWs; q += kThreads) {
-        const int u = q / L::kWs, j = q % L::kWs;
-        rec[u][j] = u < cnt ? ws[(t0 + u) * L::kWs + j] : 0.0f;
+    for (int q = threadIdx.x; q < kGxT * M; q += kThreads) {
+        const int u = q / M, i = q % M;
+        gaT[i][u] = u < cnt ? ws[(t0 + u) * L::kWs + L::kGa + i] : 0.0f;
+    }
+    for (int q = threadIdx.x; q < kGxT * kF; q += kThreads) {
+        const int u = q / kF, j = q % kF;
+        fld[u][j] = u < cnt ? ws[(t0 + u) * L::kWs + L::kPost + j] : 0.0f;
     }
     for (int c0 = 0; c0 < d; c0 += kGxC) {
-        __syncthreads();  // the records are in; the previous chunk's D has been used
-        // (1) D for (stream, column) pairs p = threadIdx.x + kThreads * j
-        for (int pr = threadIdx.x; pr < HC * kGxC; pr += kThreads) {
-            const int sI = pr / kGxC, cc = pr % kGxC;
-            if (c0 + cc >= d) continue;
-            float acc[kGxT];
+        __syncthreads();
+        {
+            // (1) D for (stream, column) pairs p = threadIdx.x + kThreads * j
+            float acc[kPairs][kGxT];
+            const float *wcol[kPairs];
 #pragma unroll
-            for (int u = 0; u < kGxT; ++u) acc[u] = 0.0f;
-            const float *wcol = hc_fn + (int64_t)sI * d + c0 + cc;
+            for (int j = 0; j < kPairs; ++j) {
+                const int pr = threadIdx.x + kThreads * j;
+                wcol[j] = hc_fn + (int64_t)(pr / kGxC) * d + c0 + pr % kGxC;
+#pragma unroll
+                for (int u = 0; u < kGxT; ++u) acc[j][u] = 0.0f;
+            }
             for (int i = 0; i < M; ++i) {
-                const float w = __ldg(wcol + (int64_t)i * K);
+                float w[kPairs];
 #pragma unroll
-                for (int u = 0; u < kGxT; ++u) acc[u] = fmaf(rec[u][L::kGa + i], w, acc[u]);
+                for (int j = 0; j < kPairs; ++j) w[j] = __ldg(wcol[j] + (int64_t)i * K);
+                const float4 *g4 = reinterpret_cast<const float4 *>(gaT[i]);
+#pragma unroll
+                for (int v = 0; v < kGxT / 4; ++v) {
+                    const float4 a = g4[v];
+#pragma unroll
+                    for (int j = 0; j < kPairs; ++j) {
+                        acc[j][4 * v + 0] = fmaf(a.x, w[j], acc[j][4 * v + 0]);
+                        acc[j][4 * v + 1] = fmaf(a.y, w[j], acc[j][4 * v + 1]);
+                        acc[j][4 * v + 2] = fmaf(a.z, w[j], acc[j][4 * v + 2]);
+                        acc[j][4 * v + 3] = fmaf(a.w, w[j], acc[j][4 * v + 3]);
+                    }
+                }
             }
 #pragma unroll
-            for (int u = 0; u < kGxT; ++u) dsum[u][sI][cc] = acc[u];
+            for (int j = 0; j < kPairs; ++j) {
+                const int pr = threadIdx.x + kThreads * j;
+#pragma unroll
+                for (int u = 0; u < kGxT; ++u) dsum[u][pr / kGxC][pr % kGxC] = acc[j][u];
+            }
         }
         __syncthreads();
-        // (2) per (token, column)
-        for (int q = threadIdx.x; q < cnt * kGxC; q += kThreads) {
-            const int u = q / kGxC, cc = q % kGxC;
-            const int c = c0 + cc;
-            if (c >= d) continue;
-            const int64_t t = t0 + u;
-            const float *r = rec[u];
-            float xv[HC], gy[HC];
+        // (2) thread: tokens u = tid / 32 and u + 8, columns c0 + 2 (tid % 32), + 1
+#pragma unroll 1
+        for (int half = 0; half < 2; ++half) {
+            const int u = threadIdx.x / (kGxC / 2) + half * (kThreads / (kGxC / 2)), cc = 2 * (threadIdx.x % (kGxC / 2));
+            if (u < cnt) {
+                const int c = c0 + cc;
+                const int64_t t = t0 + u;
+                const float *r = fld[u];
+                float xv[HC][2], gy[HC][2];
 #pragma unroll
-            for (int sI = 0; sI < HC; ++sI) {
-                xv[sI] = __uint_as_float((uint32_t)x[t * K + (int64_t)sI * d + c] << 16);
-                gy[sI] = __ldg(g_y + (t * HC + sI) * d + c);
-            }
-            float hv = r[L::kPm] * xv[0];
+                for (int sI = 0; sI < HC; ++sI) {
+                    const uint32_t xb = __ldg(reinterpret_cast<const uint32_t *>(x + t * K + (int64_t)sI * d + c));
+                    xv[sI][0] = bf16lo(xb);
+                    xv[sI][1] = __uint_as_float(xb & 0xffff0000u);
+                    const float2 g2 = __ldg(reinterpret_cast<const float2 *>(g_y + (t * HC + sI) * d + c));
+                    gy[sI][0] = g2.x;
+                    gy[sI][1] = g2.y;
+                }
+                const float2 gh2 = __ldg(reinterpret_cast<const float2 *>(g_hn + t * d + c));
+                const float2 wn2 = __ldg(reinterpret_cast<const float2 *>(norm_w + c));
+                const float gh[2] = {gh2.x, gh2.y}, wn[2] = {wn2.x, wn2.y};
+                float gf[2], gx[HC][2];
 #pragma unroll
-            for (int sI = 1; sI < HC; ++sI) hv = fmaf(r[L::kPm + sI], xv[sI], hv);
-            const float ghh = r[L::kRs] * (__ldg(norm_w + c) * __ldg(g_hn + t * d + c)) - r[L::kK3] * round_bf16(hv);
-            float fvv = r[L::kPost] * gy[0];
+                for (int e = 0; e < 2; ++e) {
+                    float hv = r[L::kPm - L::kPost] * xv[0][e];
 #pragma unroll
-            for (int k = 1; k < HC; ++k) fvv = fmaf(r[L::kPost + k], gy[k], fvv);
-            g_f[t * d + c] = fvv;
+                    for (int sI = 1; sI < HC; ++sI) hv = fmaf(r[L::kPm - L::kPost + sI], xv[sI][e], hv);
+                    const float ghh = r[L::kRs - L::kPost] * (wn[e] * gh[e]) - r[L::kK3 - L::kPost] * round_bf16(hv);
+                    float fvv = r[L::kPost - L::kPost] * gy[0][e];
 #pragma unroll
-            for (int sI = 0; sI < HC; ++sI) {
-                float a = fmaf(r[L::kPm + sI], ghh, r[L::kCr] * xv[sI]);
+                    for (int k = 1; k < HC; ++k) fvv = fmaf(r[L::kPost - L::kPost + k], gy[k][e], fvv);
+                    gf[e] = fvv;
 #pragma unroll
-                for (int k = 0; k < HC; ++k) a = fmaf(r[L::kComb + sI * HC + k], gy[k], a);
-                g_x[(t * HC + sI) * d + c] = a + dsum[u][sI][cc];
+                    for (int sI = 0; sI < HC; ++sI) {
+                        float a = fmaf(r[L::kPm - L::kPost + sI], ghh, r[L::kCr - L::kPost] * xv[sI][e]);
+#pragma unroll
+                        for (int k = 0; k < HC; ++k) a = fmaf(r[L::kComb - L::kPost + sI * HC + k], gy[k][e], a);
+                        gx[sI][e] = a + dsum[u][sI][cc + e];
+                    }
+                }
+                *reinterpret_cast<float2 *>(g_f + t * d + c) = make_float2(gf[0], gf[1]);
+#pragma unroll
+                for (int sI = 0; sI < HC; ++sI)
+                    *reinterpret_cast<float2 *>(g_x + (t * HC + sI) * d + c) = make_float2(gx[sI][0], gx[sI][1]);
             }
         }
     }
