@@ -103,7 +103,7 @@ __device__ __forceinline__ float col_sum_lanes(float v) {
 }
 
 template <int HC>
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(128, HC >= 8 ? 3 : 1)
 kg_token(const uint16_t *__restrict__ x, const float *__restrict__ pre_mix,
          const uint16_t *__restrict__ f, const float *__restrict__ hc_scale,
          const float *__restrict__ hc_base, const float *__restrict__ norm_w, int64_t n, int d, int iters,
@@ -129,39 +129,94 @@ kg_token(const uint16_t *__restrict__ x, const float *__restrict__ pre_mix,
     float v[L::kSums];
 #pragma unroll
     for (int i = 0; i < L::kSums; ++i) v[i] = 0.0f;
-    for (int c = lane; c < d / 4; c += 32) {
-        float xv[HC][4], fv[4], gh[4], w[4], h[4];
+    if constexpr (HC >= 8) {
+        // lane l: columns 4c .. 4c + 3 for c = l, l + 32, ..., taken as two halves of
+        // two columns in column order (fewer loaded values live at a time: the
+        // same sums in the same order)
+        for (int c = lane; c < d / 4; c += 32) {
 #pragma unroll
-        for (int s = 0; s < HC; ++s) ld4bf(xt + (int64_t)s * d + 4 * c, xv[s]);
-        ld4bf(f + t * d + 4 * c, fv);
-        ld4f(g_hn + t * d + 4 * c, gh);
-        ld4f(norm_w + 4 * c, w);
+            for (int hf = 0; hf < 2; ++hf) {
+                const int c2 = 4 * c + 2 * hf;
+                float xv[HC][2], fv[2], gh[2], w[2], h[2];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            float hv = pm[0] * xv[0][e];
+                for (int s = 0; s < HC; ++s) {
+                    const uint32_t xb = __ldg(reinterpret_cast<const uint32_t *>(xt + (int64_t)s * d + c2));
+                    xv[s][0] = bf16lo(xb);
+                    xv[s][1] = __uint_as_float(xb & 0xffff0000u);
+                }
+                {
+                    const uint32_t fb = __ldg(reinterpret_cast<const uint32_t *>(f + t * d + c2));
+                    fv[0] = bf16lo(fb);
+                    fv[1] = __uint_as_float(fb & 0xffff0000u);
+                    const float2 g2 = __ldg(reinterpret_cast<const float2 *>(g_hn + t * d + c2));
+                    const float2 w2 = __ldg(reinterpret_cast<const float2 *>(norm_w + c2));
+                    gh[0] = g2.x; gh[1] = g2.y; w[0] = w2.x; w[1] = w2.y;
+                }
 #pragma unroll
-            for (int s = 1; s < HC; ++s) hv = fmaf(pm[s], xv[s][e], hv);
-            h[e] = round_bf16(hv);  // the forward's bf16 h
-            const float wg = w[e] * gh[e];
-            v[L::kSH2] = fmaf(h[e], h[e], v[L::kSH2]);
-            v[L::kST] = fmaf(h[e], wg, v[L::kST]);
+                for (int e = 0; e < 2; ++e) {
+                    float hv = pm[0] * xv[0][e];
 #pragma unroll
-            for (int j = 0; j < HC; ++j) {
-                v[L::kSX2] = fmaf(xv[j][e], xv[j][e], v[L::kSX2]);
-                v[L::kSA + j] = fmaf(xv[j][e], wg, v[L::kSA + j]);
-                v[L::kSB + j] = fmaf(xv[j][e], h[e], v[L::kSB + j]);
+                    for (int s = 1; s < HC; ++s) hv = fmaf(pm[s], xv[s][e], hv);
+                    h[e] = round_bf16(hv);  // the forward's bf16 h
+                    const float wg = w[e] * gh[e];
+                    v[L::kSH2] = fmaf(h[e], h[e], v[L::kSH2]);
+                    v[L::kST] = fmaf(h[e], wg, v[L::kST]);
+#pragma unroll
+                    for (int j = 0; j < HC; ++j) {
+                        v[L::kSX2] = fmaf(xv[j][e], xv[j][e], v[L::kSX2]);
+                        v[L::kSA + j] = fmaf(xv[j][e], wg, v[L::kSA + j]);
+                        v[L::kSB + j] = fmaf(xv[j][e], h[e], v[L::kSB + j]);
+                    }
+                }
+#pragma unroll
+                for (int k = 0; k < HC; ++k) {
+                    const float2 g2 = __ldg(reinterpret_cast<const float2 *>(g_y + (t * HC + k) * d + c2));
+                    const float gy[2] = {g2.x, g2.y};
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        v[L::kSPost + k] = fmaf(fv[e], gy[e], v[L::kSPost + k]);
+#pragma unroll
+                        for (int j = 0; j < HC; ++j)
+                            v[L::kSComb + j * HC + k] = fmaf(xv[j][e], gy[e], v[L::kSComb + j * HC + k]);
+                    }
+                }
             }
         }
-#pragma unroll
-        for (int k = 0; k < HC; ++k) {
-            float gy[4];
-            ld4f(g_y + (t * HC + k) * d + 4 * c, gy);
-#pragma unroll
+    } else {
+        for (int c = lane; c < d / 4; c += 32) {
+            float xv[HC][4], fv[4], gh[4], w[4], h[4];
+    #pragma unroll
+            for (int s = 0; s < HC; ++s) ld4bf(xt + (int64_t)s * d + 4 * c, xv[s]);
+            ld4bf(f + t * d + 4 * c, fv);
+            ld4f(g_hn + t * d + 4 * c, gh);
+            ld4f(norm_w + 4 * c, w);
+    #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                v[L::kSPost + k] = fmaf(fv[e], gy[e], v[L::kSPost + k]);
-#pragma unroll
-                for (int j = 0; j < HC; ++j)
-                    v[L::kSComb + j * HC + k] = fmaf(xv[j][e], gy[e], v[L::kSComb + j * HC + k]);
+                float hv = pm[0] * xv[0][e];
+    #pragma unroll
+                for (int s = 1; s < HC; ++s) hv = fmaf(pm[s], xv[s][e], hv);
+                h[e] = round_bf16(hv);  // the forward's bf16 h
+                const float wg = w[e] * gh[e];
+                v[L::kSH2] = fmaf(h[e], h[e], v[L::kSH2]);
+                v[L::kST] = fmaf(h[e], wg, v[L::kST]);
+    #pragma unroll
+                for (int j = 0; j < HC; ++j) {
+                    v[L::kSX2] = fmaf(xv[j][e], xv[j][e], v[L::kSX2]);
+                    v[L::kSA + j] = fmaf(xv[j][e], wg, v[L::kSA + j]);
+                    v[L::kSB + j] = fmaf(xv[j][e], h[e], v[L::kSB + j]);
+                }
+            }
+    #pragma unroll
+            for (int k = 0; k < HC; ++k) {
+                float gy[4];
+                ld4f(g_y + (t * HC + k) * d + 4 * c, gy);
+    #pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    v[L::kSPost + k] = fmaf(fv[e], gy[e], v[L::kSPost + k]);
+    #pragma unroll
+                    for (int j = 0; j < HC; ++j)
+                        v[L::kSComb + j * HC + k] = fmaf(xv[j][e], gy[e], v[L::kSComb + j * HC + k]);
+                }
             }
         }
     }
